@@ -1,0 +1,402 @@
+"""Benchmark of one verification round per layer on GB300.
+
+Workload: the DSpark-style verification configuration (K = 4 draft queries
+per request at positions S..S+3, batch 8, S = 32768, int8 indexer d_idx = 64,
+top-k 2048, GQA 8/1 with d = 128 in bf16, hot cache 4096 rows per request
+with ~70% overlap to the previous selection, draft ring window 2048,
+accepted_len uniform in 0..4), synthetic and seeded.  A step is one whole
+round: select (indexer + top-k), resolve (union, probe, compaction, shared
+host gather), attend (ring write, split-KV attention, merge, hot-cache
+install) and commit.  Metric: verified query-tokens per second per layer =
+N * K / step time.
+
+Each timed step starts from the same state (the snapshot taken after the
+previous-step round), restored outside the timed region, and the L2 cache is
+flushed (a 512 MiB write) before every step, also outside it.
+
+Multi-GPU: requests are independent, so every rank runs its own batch of
+requests on its own GPU (weak scaling, no collective on the data path); the
+step time is the maximum over ranks.
+
+--impl reference times the oracle (the plain CPU restatement in ``oracle/``)
+on the host cores: each step is one request's round, a bounded sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "cfg2"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu)
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- CPU baseline
+def oracle_requests(rec, slots):
+    """Run round 0 (previous step) on the oracle for ``slots``; return the oracle."""
+    import oracle
+    cfg = oracle.Config(n_slots=rec.N, k_max=rec.kmax, topk=rec.topk, s_max=rec.s_max,
+                        idx_heads=rec.H_idx, idx_dim=rec.d_idx, q_heads=rec.Hq, Hkv=rec.Hkv,
+                        qk_dim=rec.qk_dim, v_dim=rec.v_dim, kv_layout=rec.kv_layout,
+                        budget=rec.B, ring_window=rec.W, page_rows=rec.p,
+                        opt_rows_max=rec.opt_rows_max)
+    o = oracle.Oracle(cfg)
+    for r in slots:
+        o.bind(r, rec.host_rows(r, r + 1)[0], rec.index_keys(r, r + 1)[0], rec.S)
+    return o
+
+
+def oracle_round_inputs(rec, rnd, slots):
+    N, Km = rec.N, rec.kmax
+    qi = np.zeros((N, Km, rec.idx_row), np.int8)
+    qa = np.zeros((N, Km, rec.Hq, rec.qk_dim), np.uint16)
+    bl = np.zeros((N, Km, rec.row_elems), np.uint16)
+    for r in slots:
+        qi[r] = rec.index_queries(rnd, r, r + 1)[0]
+        qa[r] = rec.attn_queries(rnd, r, r + 1)[0]
+        bl[r] = rec.block_rows(rnd, r, r + 1)[0]
+    return qi, qa, bl
+
+
+def oracle_step(o, rec, rnd, slots):
+    kr = np.zeros(rec.N, np.int32)
+    kr[slots] = rec.K
+    qi, qa, bl = oracle_round_inputs(rec, rnd, slots)
+    sel = o.select(qi, kr)
+    o.resolve(sel)
+    o.attend(qa, bl)
+    acc = rec.accepted(rnd)
+    acc_s = np.zeros(rec.N, np.int32)
+    acc_s[slots] = acc[slots]
+    o.commit(acc_s)
+
+
+def cpu_baseline(rec, budget_s=12.0):
+    """Time the oracle on the host: round 1 of as many requests as fit in
+    about ``budget_s`` seconds (round 0 of each request is set-up, untimed)."""
+    done, t_total = 0, 0.0
+    for r in range(rec.N):
+        o = oracle_requests(rec, [r])
+        oracle_step(o, rec, 0, [r])          # previous step: warms the hot cache
+        t0 = time.perf_counter()
+        oracle_step(o, rec, 1, [r])
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total > budget_s:
+            break
+    value = done * rec.K / t_total
+    return {"value": value, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of %d requests, one verification round each (K=%d, S=%d), "
+                      "single-threaded numpy (int64 scores, float64 attention)"
+                      % (done, rec.N, rec.K, rec.S),
+            "seconds": t_total}
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+def algorithmic_bytes(rec, counts, k_per_req):
+    """Bytes each step must move (not the work it avoids), per kernel family.
+
+    select: index keys of the domain (read once for all K queries), the int8
+    queries and the int32 top-k lists.  attend: each distinct selected row
+    once, the block rows, bf16 queries and outputs and the int32 locations.
+    gather: the distinct missing rows over the host link.
+    """
+    K = int(k_per_req.max())
+    n_act = int((k_per_req > 0).sum())
+    rb = rec.row_bytes
+    keys = n_act * rec.S * rec.idx_row
+    select = keys + n_act * K * rec.idx_row + 4 * n_act * K * rec.topk
+    U = int(counts[:, 0].sum())
+    M = int(counts[:, 1].sum())
+    attend = U * rb + n_act * K * rb + 2 * n_act * K * rec.Hq * (rec.qk_dim + rec.v_dim) \
+        + 4 * n_act * K * rec.topk
+    return {"index_score": keys + n_act * K * rec.idx_row, "select": select,
+            "attn": attend, "gather": M * rb, "union": U, "misses": M}
+
+
+# ---------------------------------------------------------------- native arm
+def run_native(args):
+    import torch
+    import workload as wl
+    import hierarchical_sparse_kv_int8_gb300 as dhs
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dhs.build()
+    rec = wl.CONFIGS[WORKLOAD]
+    if world > 1:
+        rec = rec.scaled(seed=rec.seed + rank)   # each rank serves its own requests
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        run = Runner(rec, stream=stream)
+        kr = rec.k_per_req()
+        # previous decode step: leaves the hot cache holding its selection
+        run.load_round(0)
+        run.round(kr, rec.accepted(0))
+        run.load_round(1)
+        snap = run.ctx.snapshot(stream)
+        acc1 = rec.accepted(1)
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        stream.synchronize()
+
+        def step():
+            run.select(kr)
+            run.resolve(True)
+            run.attend()
+            run.commit(acc1)
+
+        for _ in range(args.warmup):
+            run.ctx.restore(snap, stream)
+            step()
+        stream.synchronize()
+        counts = run.export("counts", torch.int32, (rec.N, 4)).cpu().numpy()
+        st_before = run.ctx.stats(stream)
+
+        run.ctx.set_timing(True)
+        sampler = ClockSampler(local) if rank == 0 or True else None
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        barrier(world)
+        stream.synchronize()
+        sampler.start()
+        for i in range(args.steps):
+            run.ctx.restore(snap, stream)
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        stream.synchronize()
+        clocks = sampler.stop()
+        barrier(world)
+        kt = run.ctx.kernel_times()
+        run.ctx.set_timing(False)
+        ms_steps = [a.elapsed_time(b) for a, b in ev]
+        ms_local = float(np.mean(ms_steps))
+        st_after = run.ctx.stats(stream)
+
+        # end to end through the host-buffer entry point
+        hq = torch.from_numpy(rec.index_queries(1, 0, rec.N)).pin_memory()
+        hqa = torch.from_numpy(rec.attn_queries(1, 0, rec.N).view(np.int16)).pin_memory()
+        hbl = torch.from_numpy(rec.block_rows(1, 0, rec.N).view(np.int16)).pin_memory()
+        hout = torch.empty((rec.N, rec.kmax, rec.Hq, rec.v_dim), dtype=torch.int16).pin_memory()
+        hlse = torch.empty((rec.N, rec.kmax, rec.Hq), dtype=torch.float32).pin_memory()
+        e2e_times = []
+        for i in range(args.warmup + args.steps):
+            run.ctx.restore(snap, stream)
+            flush.fill_(i & 0xFF)
+            stream.synchronize()
+            t0 = time.perf_counter()
+            run.ctx.round_host(hq, kr, hqa, hbl, acc1, hout, hlse, stream)
+            t1 = time.perf_counter()
+            if i >= args.warmup:
+                e2e_times.append(t1 - t0)
+        e2e_ms_local = 1e3 * float(np.mean(e2e_times))
+        h2d = hq.numel() + hqa.numel() * 2 + hbl.numel() * 2
+        d2h = hout.numel() * 2 + hlse.numel() * 4
+
+    ms = max_over_ranks(ms_local, world)
+    e2e_ms = max_over_ranks(e2e_ms_local, world)
+    tokens = int(kr.sum())
+    value = world * tokens / (ms * 1e-3)
+    e2e_value = world * tokens / (e2e_ms * 1e-3)
+
+    # roofline of the dominant kernel (largest share of the timed region)
+    ab = algorithmic_bytes(rec, counts, kr)
+    per = {name: (n, t) for name, (n, t) in kt.items() if n > 0}
+    dom = max(per, key=lambda k: per[k][1])
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
+    hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
+    algo = {"index_score": ab["index_score"], "attn": ab["attn"], "gather": ab["gather"]}
+    n_l, t_l = per[dom]
+    avg_ms = t_l / n_l
+    bytes_per_launch = algo.get(dom)
+    roof = None
+    if bytes_per_launch is not None:
+        ach = bytes_per_launch / (avg_ms * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": None,
+                "algorithmic_bytes": bytes_per_launch, "avg_launch_ms": round(avg_ms, 5),
+                "peak_source": "MEASURED_PEAKS.json hbm_gbs (burst copy)" if peaks else
+                "fallback 6.8 TB/s"}
+    breakdown = {k: {"launches": n, "avg_us": round(1e3 * t / n, 2),
+                     "share": round(t / sum(v[1] for v in per.values()), 4)}
+                 for k, (n, t) in per.items()}
+    launches_per_step = sum(n for n, _ in per.values()) / args.steps
+    # upload launches are counted as ours too (control words for each call)
+    line = {
+        "metric": "verified query-tokens/s per layer (select+resolve+attend)",
+        "value": round(value, 1), "unit": "query-tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+int8",
+        "data": "synthetic (seeded; shapes of the DSpark-style verification configuration)",
+        "config": {"workload": rec.name, "batch": rec.N, "K": rec.K, "S": rec.S,
+                   "topk": rec.topk, "d_idx": rec.d_idx, "q_heads": rec.Hq,
+                   "kv_heads": rec.Hkv, "head_dim": rec.qk_dim, "hot_cache_rows": rec.B,
+                   "ring_window": rec.W, "l2": "flushed (512 MiB write) before every step",
+                   "state": "restored from snapshot before every step (untimed)"},
+        "e2e": {"value": round(e2e_value, 1), "unit": "query-tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_ms, 5),
+                "api": "dhs_round_host (pinned host inputs and outputs)"},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "roofline": roof,
+        "kernels": breakdown,
+        "workload_stats": {"union_rows": ab["union"], "misses": ab["misses"],
+                           "hot_hits": int(counts[:, 3].sum()),
+                           "host_bytes_per_step": ab["gather"]},
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(rec)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import workload as wl
+    rec = wl.CONFIGS[WORKLOAD]
+    times = []
+    for i in range(args.warmup + args.steps):
+        r = i % rec.N
+        o = oracle_requests(rec, [r])
+        oracle_step(o, rec, 0, [r])
+        t0 = time.perf_counter()
+        oracle_step(o, rec, 1, [r])
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1e3 * float(np.mean(times))
+    value = rec.K / (ms * 1e-3)
+    line = {
+        "impl": "reference",
+        "metric": "verified query-tokens/s per layer (select+resolve+attend)",
+        "value": round(value, 2), "unit": "query-tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64",
+        "data": "synthetic (seeded; shapes of the DSpark-style verification configuration)",
+        "config": {"workload": rec.name, "batch": rec.N, "K": rec.K, "S": rec.S,
+                   "topk": rec.topk, "sample": "one request's round per step"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "query-tokens/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": "one request's verification round per step, "
+                                   "single-threaded numpy"},
+        "e2e": {"value": round(value, 2), "unit": "query-tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_native(a)

@@ -1,0 +1,259 @@
+"""Python binding of libdhs (speculative-verification sparse attention over a
+two-tier KV cache on one GB300 GPU).
+
+This module only marshals arguments to the C ABI declared in
+``include/dhs.h``; every step of the hot path runs in the library's CUDA
+kernels.  Device buffers are passed as CUDA tensors (or raw device
+addresses), small per-request control arrays as host numpy arrays, and the
+stream defaults to torch's current stream.  There is no CPU fallback: if the
+library is not built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import numpy as np
+
+from . import _build
+
+__all__ = ["Config", "Context", "DhsError", "build", "load", "LOC_RING", "LOC_OPT", "LOC_HOT",
+           "LOC_STAGE", "BUF"]
+
+LOC_RING, LOC_OPT, LOC_HOT, LOC_STAGE = 0, 1, 2, 3
+LOC_TIER_SHIFT = 28
+KV_SPLIT, KV_LATENT = 0, 1
+BUF = dict(hot_row=0, hot_stamp=1, hot_data=2, ring=3, stage=4, opt=5, union=6, miss=7,
+           counts=8, lru=9, frontier=10, hot_map=11, opt_map=12)
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_slots", ctypes.c_int32), ("k_max", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("s_max", ctypes.c_int64), ("idx_heads", ctypes.c_int32),
+                ("idx_dim", ctypes.c_int32), ("q_heads", ctypes.c_int32),
+                ("kv_heads", ctypes.c_int32), ("qk_dim", ctypes.c_int32),
+                ("v_dim", ctypes.c_int32), ("kv_layout", ctypes.c_int32),
+                ("budget", ctypes.c_int32), ("ring_window", ctypes.c_int32),
+                ("page_rows", ctypes.c_int32), ("opt_rows_max", ctypes.c_int64),
+                ("softmax_scale", ctypes.c_float)]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "resolve_calls", "selections", "union_rows", "ring_hits", "opt_hits", "hot_hits",
+        "misses", "miss_selections", "host_rows_fetched", "host_bytes", "installs", "evictions",
+        "direct_only")] + [("device_error", ctypes.c_int32), ("device_error_site", ctypes.c_int32)]
+
+
+class DhsError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s: %s (code %d)" % (what, load().dhs_strerror(code).decode(), code))
+
+
+_lib = None
+_SIGS = {
+    "dhs_create": ([ctypes.POINTER(Config), ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
+    "dhs_destroy": ([ctypes.c_void_p], None),
+    "dhs_ring_rows": ([ctypes.c_void_p], ctypes.c_int64),
+    "dhs_device_bytes": ([ctypes.c_void_p], ctypes.c_int64),
+    "dhs_bind_request": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                          ctypes.c_int64, ctypes.c_void_p], ctypes.c_int),
+    "dhs_select": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                    ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "dhs_resolve": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                     ctypes.c_void_p], ctypes.c_int),
+    "dhs_attend": ([ctypes.c_void_p] * 6 + [ctypes.c_void_p], ctypes.c_int),
+    "dhs_commit": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "dhs_set_residency": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                           ctypes.c_void_p], ctypes.c_int),
+    "dhs_get_stats": ([ctypes.c_void_p, ctypes.POINTER(Stats), ctypes.c_void_p], ctypes.c_int),
+    "dhs_reset_stats": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "dhs_buffer_bytes": ([ctypes.c_void_p, ctypes.c_int32], ctypes.c_int64),
+    "dhs_export": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                    ctypes.c_void_p], ctypes.c_int),
+    "dhs_set_timing": ([ctypes.c_void_p, ctypes.c_int32], ctypes.c_int),
+    "dhs_kernel_times": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p],
+                         ctypes.c_int),
+    "dhs_kernel_name": ([ctypes.c_int32], ctypes.c_char_p),
+    "dhs_kernel_count": ([], ctypes.c_int32),
+    "dhs_snapshot": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p],
+                     ctypes.c_int),
+    "dhs_restore": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
+    "dhs_round_host": ([ctypes.c_void_p] * 9, ctypes.c_int),
+    "dhs_strerror": ([ctypes.c_int], ctypes.c_char_p),
+    "dhs_last_error": ([ctypes.c_void_p], ctypes.c_char_p),
+}
+
+
+def build(force: bool = False) -> str:
+    """Compile libdhs.so for sm_103a (nvcc; works without a GPU)."""
+    return _build.build(force=force)
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libdhs.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError("libdhs.so is not built (%s); call "
+                               "hierarchical_sparse_kv_int8_gb300.build() first" % _build.LIB)
+        lib = ctypes.CDLL(_build.LIB)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+    return _lib
+
+
+def _dptr(x) -> Optional[int]:
+    """Device (or pinned host) address of a tensor, or an int address, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    return x.data_ptr()
+
+
+def _host_i32(x, n) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+    if a.size < n:
+        raise ValueError("expected %d int32 values, got %d" % (n, a.size))
+    return a
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_config(**kw) -> Config:
+    c = Config()
+    for name, _ in Config._fields_:
+        setattr(c, name, kw.get(name, 0))
+    return c
+
+
+class Context:
+    """One KV source (layer) with ``n_slots`` request slots; see include/dhs.h."""
+
+    def __init__(self, cfg: Config):
+        self.cfg = cfg
+        self._lib = load()
+        h = ctypes.c_void_p()
+        rc = self._lib.dhs_create(ctypes.byref(cfg), ctypes.byref(h))
+        if rc:
+            raise DhsError(rc, "dhs_create")
+        self.h = h
+
+    def close(self):
+        if getattr(self, "h", None):
+            self._lib.dhs_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _check(self, rc, what):
+        if rc:
+            detail = self._lib.dhs_last_error(self.h).decode() if rc == 4 else ""
+            raise DhsError(rc, what + (" [%s]" % detail if detail else ""))
+
+    @property
+    def ring_rows(self) -> int:
+        return self._lib.dhs_ring_rows(self.h)
+
+    def device_bytes(self) -> int:
+        return self._lib.dhs_device_bytes(self.h)
+
+    def bind(self, slot, host_kv, idx_keys, n_committed, stream=None):
+        self._check(self._lib.dhs_bind_request(self.h, slot, _dptr(host_kv), _dptr(idx_keys),
+                                               n_committed, _stream(stream)), "dhs_bind_request")
+
+    def select(self, q_idx, k_per_req, topk_out, pos=None, stream=None):
+        kr = _host_i32(k_per_req, self.cfg.n_slots)
+        p = None
+        if pos is not None:
+            p = np.ascontiguousarray(np.asarray(pos, dtype=np.int64))
+        self._check(self._lib.dhs_select(self.h, _dptr(q_idx), kr.ctypes.data,
+                                         None if p is None else p.ctypes.data, _dptr(topk_out),
+                                         _stream(stream)), "dhs_select")
+
+    def resolve(self, topk, loc_out, shared=True, stream=None):
+        self._check(self._lib.dhs_resolve(self.h, _dptr(topk), _dptr(loc_out), 1 if shared else 0,
+                                          _stream(stream)), "dhs_resolve")
+
+    def attend(self, q, block_kv, loc, out, lse=None, stream=None):
+        self._check(self._lib.dhs_attend(self.h, _dptr(q), _dptr(block_kv), _dptr(loc), _dptr(out),
+                                         _dptr(lse), _stream(stream)), "dhs_attend")
+
+    def commit(self, accepted_len, stream=None):
+        a = _host_i32(accepted_len, self.cfg.n_slots)
+        self._check(self._lib.dhs_commit(self.h, a.ctypes.data, _stream(stream)), "dhs_commit")
+
+    def set_residency(self, slot, rows, stream=None):
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        self._check(self._lib.dhs_set_residency(self.h, slot, rows.ctypes.data if rows.size else None,
+                                                rows.size, _stream(stream)), "dhs_set_residency")
+
+    def stats(self, stream=None, check=True) -> Dict[str, int]:
+        st = Stats()
+        rc = self._lib.dhs_get_stats(self.h, ctypes.byref(st), _stream(stream))
+        if rc and (check or rc != 5):
+            raise DhsError(rc, "dhs_get_stats")
+        return {n: getattr(st, n) for n, _ in Stats._fields_}
+
+    def reset_stats(self, stream=None):
+        self._check(self._lib.dhs_reset_stats(self.h, _stream(stream)), "dhs_reset_stats")
+
+    def buffer_bytes(self, which: str) -> int:
+        return self._lib.dhs_buffer_bytes(self.h, BUF[which])
+
+    def export(self, which: str, dst, stream=None):
+        """Copy internal buffer ``which`` into the CUDA tensor ``dst`` (its nbytes)."""
+        nbytes = dst.numel() * dst.element_size()
+        self._check(self._lib.dhs_export(self.h, BUF[which], _dptr(dst), nbytes, _stream(stream)),
+                    "dhs_export")
+
+    def set_timing(self, enable: bool):
+        self._check(self._lib.dhs_set_timing(self.h, 1 if enable else 0), "dhs_set_timing")
+
+    def kernel_times(self) -> Dict[str, tuple]:
+        n = self._lib.dhs_kernel_count()
+        launches = np.zeros(n, np.int64)
+        ms = np.zeros(n, np.float64)
+        self._check(self._lib.dhs_kernel_times(self.h, n, launches.ctypes.data, ms.ctypes.data),
+                    "dhs_kernel_times")
+        return {self._lib.dhs_kernel_name(i).decode(): (int(launches[i]), float(ms[i]))
+                for i in range(n)}
+
+    def snapshot(self, stream=None) -> int:
+        sid = ctypes.c_int32()
+        self._check(self._lib.dhs_snapshot(self.h, ctypes.byref(sid), _stream(stream)),
+                    "dhs_snapshot")
+        return sid.value
+
+    def restore(self, sid: int, stream=None):
+        self._check(self._lib.dhs_restore(self.h, sid, _stream(stream)), "dhs_restore")
+
+    def round_host(self, q_idx, k_per_req, q, block_kv, accepted_len, out, lse=None, stream=None):
+        kr = _host_i32(k_per_req, self.cfg.n_slots)
+        a = _host_i32(accepted_len, self.cfg.n_slots)
+        self._check(self._lib.dhs_round_host(self.h, _dptr(q_idx), kr.ctypes.data, _dptr(q),
+                                             _dptr(block_kv), a.ctypes.data, _dptr(out),
+                                             _dptr(lse), _stream(stream)), "dhs_round_host")

@@ -1,0 +1,698 @@
+// Host side of libdhs: context lifetime, argument checks, host mirrors of the
+// per-request round state, and the launch sequence of each C-ABI call.
+#include "dhs_internal.cuh"
+
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+#include <vector>
+
+namespace dhs {
+
+const char *const kKernelNames[K_COUNT] = {
+    "upload",         "index_score",     "topk",          "union_probe",
+    "gather",         "attn",            "merge",         "post_attend",
+    "commit",         "residency_clear", "residency_fill", "residency_publish",
+    "bind_reset"};
+
+// ---------------------------------------------------------------- Timer
+cudaEvent_t Timer::take() {
+  if (!pool_.empty()) {
+    cudaEvent_t e = pool_.back();
+    pool_.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+void Timer::begin(int id, cudaStream_t s) {
+  if (!enabled) return;
+  open_id_ = id;
+  open_a_ = take();
+  cudaEventRecord(open_a_, s);
+}
+void Timer::end(int id, cudaStream_t s) {
+  if (!enabled || open_id_ != id || !open_a_) return;
+  cudaEvent_t b = take();
+  cudaEventRecord(b, s);
+  pending_.push_back({id, open_a_, b});
+  open_a_ = nullptr;
+  open_id_ = -1;
+  if (pending_.size() > 8192) drain(1024);
+}
+void Timer::drain(size_t keep) {
+  size_t n = pending_.size() > keep ? pending_.size() - keep : 0;
+  for (size_t i = 0; i < n; ++i) {
+    Pending &p = pending_[i];
+    cudaEventSynchronize(p.b);
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+      launches_[p.id] += 1;
+      ms_[p.id] += ms;
+    }
+    pool_.push_back(p.a);
+    pool_.push_back(p.b);
+  }
+  pending_.erase(pending_.begin(), pending_.begin() + n);
+}
+void Timer::collect(int64_t *launches, double *ms) {
+  drain(0);
+  for (int i = 0; i < K_COUNT; ++i) {
+    launches[i] = launches_[i];
+    ms[i] = ms_[i];
+  }
+}
+void Timer::reset() {
+  drain(0);
+  for (int i = 0; i < K_COUNT; ++i) {
+    launches_[i] = 0;
+    ms_[i] = 0.0;
+  }
+}
+Timer::~Timer() {
+  for (auto &p : pending_) {
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  for (auto e : pool_) cudaEventDestroy(e);
+}
+
+}  // namespace dhs
+
+using namespace dhs;
+
+enum Phase { PH_IDLE = 0, PH_SELECTED, PH_RESOLVED, PH_ATTENDED };
+
+struct Snapshot {
+  std::vector<void *> bufs;
+  std::vector<int64_t> n, ring_first, opt_count;
+  std::vector<int32_t> K;
+  int64_t tick;
+  int phase;
+};
+
+struct dhs_ctx {
+  dhs_config cfg;
+  DevCtx d;
+  int n_split = 1;
+  int device = 0;
+  std::vector<void *> allocs;
+  // host mirrors
+  std::vector<int64_t> n, ring_first, opt_count;
+  std::vector<int32_t> K;
+  std::vector<char> bound;
+  std::vector<const void *> host_ptr;
+  std::vector<const int8_t *> key_ptr;
+  int64_t tick = 0;
+  int phase = PH_IDLE;
+  Timer timer;
+  std::vector<Snapshot> snaps;
+  // device staging for dhs_round_host
+  int8_t *rh_qidx = nullptr;
+  uint16_t *rh_q = nullptr, *rh_block = nullptr, *rh_out = nullptr;
+  float *rh_lse = nullptr;
+  int32_t *rh_topk = nullptr, *rh_loc = nullptr;
+  // device arrays of per-slot pointers
+  const int8_t **d_keys = nullptr;
+  const uint16_t **d_host = nullptr;
+  const char *last_error = "";
+};
+
+namespace {
+
+template <typename T>
+cudaError_t dalloc(dhs_ctx *c, T **p, size_t count) {
+  void *q = nullptr;
+  size_t bytes = count * sizeof(T);
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e;
+  }
+  c->allocs.push_back(q);
+  *p = static_cast<T *>(q);
+  return cudaSuccess;
+}
+
+void free_all(dhs_ctx *c) {
+  for (void *p : c->allocs) cudaFree(p);
+  c->allocs.clear();
+  for (auto &s : c->snaps)
+    for (void *p : s.bufs) cudaFree(p);
+  c->snaps.clear();
+}
+
+struct BufDesc {
+  void *ptr;
+  size_t bytes;
+};
+
+BufDesc buffer_desc(const dhs_ctx *c, int which) {
+  const DevCtx &d = c->d;
+  const size_t N = d.N, B = d.B, KK = (size_t)d.Kmax * d.k, row2 = (size_t)d.row * 2;
+  switch (which) {
+    case DHS_BUF_HOT_ROW: return {d.hot_row, N * B * 4};
+    case DHS_BUF_HOT_STAMP: return {d.hot_stamp, N * B * 4};
+    case DHS_BUF_HOT_DATA: return {d.hot_data, N * B * row2};
+    case DHS_BUF_RING: return {d.ring, N * d.Rd * row2};
+    case DHS_BUF_STAGE: return {d.stage, N * KK * row2};
+    case DHS_BUF_OPT: return {d.opt, N * d.opt_max * row2};
+    case DHS_BUF_UNION: return {d.uni, N * KK * 4};
+    case DHS_BUF_MISS: return {d.miss, N * KK * 4};
+    case DHS_BUF_COUNTS: return {d.counts, N * 16};
+    case DHS_BUF_LRU: return {d.lru, N * B * 4};
+    case DHS_BUF_FRONTIER: return {d.n, N * 8};
+    case DHS_BUF_HOT_MAP: return {d.hot_map, N * d.Sm * 4};
+    case DHS_BUF_OPT_MAP: return {d.opt_map, N * d.Sm * 4};
+    default: return {nullptr, 0};
+  }
+}
+
+// Buffers that make up the mutable state (snapshot / restore).
+const int kStateBufs[] = {DHS_BUF_HOT_ROW, DHS_BUF_HOT_STAMP, DHS_BUF_HOT_DATA, DHS_BUF_RING,
+                          DHS_BUF_OPT,     DHS_BUF_LRU,       DHS_BUF_FRONTIER, DHS_BUF_HOT_MAP,
+                          DHS_BUF_OPT_MAP};
+
+// Record the CUDA error behind a DHS_ERR_CUDA return.
+int cuda_fail(dhs_ctx *c, cudaError_t e) {
+  c->last_error = cudaGetErrorString(e);
+  cudaGetLastError();
+  return DHS_ERR_CUDA;
+}
+
+int upload_words(dhs_ctx *c, int32_t *dst, const std::vector<int32_t> &w, cudaStream_t s) {
+  for (size_t off = 0; off < w.size(); off += kUploadWords) {
+    int n = (int)std::min<size_t>(kUploadWords, w.size() - off);
+    cudaError_t e_ = launch_upload(dst + off, w.data() + off, n, s);
+    if (e_ != cudaSuccess) return cuda_fail(c, e_);
+  }
+  return DHS_OK;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+
+}  // namespace
+
+extern "C" {
+
+const char *dhs_last_error(const dhs_ctx *c) { return c ? c->last_error : ""; }
+
+const char *dhs_strerror(int code) {
+  switch (code) {
+    case DHS_OK: return "ok";
+    case DHS_ERR_INVALID: return "invalid argument or call order";
+    case DHS_ERR_OOM: return "out of device or pinned memory";
+    case DHS_ERR_CAPACITY: return "request exceeds a configured capacity";
+    case DHS_ERR_CUDA: return "CUDA runtime error";
+    case DHS_ERR_DEVICE_CHECK: return "a kernel found an out-of-range index";
+    case DHS_ERR_TIMEOUT: return "timed out";
+    default: return "unknown error";
+  }
+}
+
+int32_t dhs_kernel_count(void) { return K_COUNT; }
+const char *dhs_kernel_name(int32_t id) {
+  return (id >= 0 && id < K_COUNT) ? kKernelNames[id] : "?";
+}
+
+int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
+  if (!cfg || !out) return DHS_ERR_INVALID;
+  *out = nullptr;
+  const dhs_config &g = *cfg;
+  if (g.n_slots < 1 || g.n_slots > kMaxSlots || g.k_max < 1 || g.k_max > kMaxKmax ||
+      g.topk < 32 || g.topk > kMaxTopk || g.topk % 32 || g.s_max < 1 || g.s_max > (1 << 27) ||
+      g.idx_heads < 1 || g.idx_dim < 1 || (g.idx_heads * g.idx_dim) % 16 ||
+      g.idx_heads * g.idx_dim > 1024 || g.q_heads < 1 || g.kv_heads < 1 ||
+      g.q_heads % g.kv_heads || g.q_heads / g.kv_heads > 16 || g.q_heads > 128 || g.budget < 1 ||
+      g.budget > 65535 || g.ring_window < 1 || g.page_rows < 1 || g.opt_rows_max < 0 ||
+      g.opt_rows_max > g.s_max)
+    return DHS_ERR_INVALID;
+  if (g.kv_layout != DHS_KV_SPLIT && g.kv_layout != DHS_KV_LATENT) return DHS_ERR_INVALID;
+  if (g.kv_layout == DHS_KV_LATENT && (g.kv_heads != 1 || g.v_dim > g.qk_dim))
+    return DHS_ERR_INVALID;
+  if (!attn_shape_supported(g.qk_dim, g.v_dim, g.kv_layout)) return DHS_ERR_INVALID;
+  const int row = g.kv_layout == DHS_KV_LATENT ? g.qk_dim : g.kv_heads * (g.qk_dim + g.v_dim);
+  if (row * 2 > 2048) return DHS_ERR_INVALID;
+  const int64_t Rd = (int64_t)g.page_rows *
+                     ((g.ring_window + g.page_rows - 1 + g.k_max + g.page_rows - 1) / g.page_rows);
+  if (Rd > DHS_LOC_INDEX_MASK) return DHS_ERR_INVALID;
+
+  dhs_ctx *c = new (std::nothrow) dhs_ctx();
+  if (!c) return DHS_ERR_OOM;
+  c->cfg = g;
+  cudaGetDevice(&c->device);
+  DevCtx &d = c->d;
+  memset(&d, 0, sizeof(d));
+  d.N = g.n_slots;
+  d.Kmax = g.k_max;
+  d.k = g.topk;
+  d.Sm = g.s_max;
+  d.idx_row = g.idx_heads * g.idx_dim;
+  d.Hq = g.q_heads;
+  d.Hkv = g.kv_heads;
+  d.dqk = g.qk_dim;
+  d.dv = g.v_dim;
+  d.row = row;
+  d.layout = g.kv_layout;
+  d.B = g.budget;
+  d.W = g.ring_window;
+  d.p = g.page_rows;
+  d.Rd = (int)Rd;
+  d.opt_max = g.opt_rows_max;
+  const float scale = g.softmax_scale > 0.f ? g.softmax_scale : 1.0f / sqrtf((float)g.qk_dim);
+  d.scale_log2 = scale * 1.4426950408889634f;
+  if (union_smem_bytes(d) > kMaxDynSmem) {
+    delete c;
+    return DHS_ERR_CAPACITY;
+  }
+  c->n_split = attn_splits(d, d.N * d.Kmax);
+
+  const size_t N = d.N, KK = (size_t)d.Kmax * d.k, B = d.B, R = row;
+  cudaError_t e = cudaSuccess;
+#define ALLOC(ptr, count) \
+  if (e == cudaSuccess) e = dalloc(c, &(ptr), (count))
+  uint16_t *pool = nullptr;
+  const size_t pool_rows = N * (B + KK + (size_t)d.Rd + (size_t)d.opt_max);
+  ALLOC(pool, pool_rows * R);
+  if (e == cudaSuccess) {
+    d.hot_data = pool;
+    d.stage = d.hot_data + N * B * R;
+    d.ring = d.stage + N * KK * R;
+    d.opt = d.ring + N * d.Rd * R;
+  }
+  ALLOC(c->d_keys, N);
+  ALLOC(c->d_host, N);
+  ALLOC(d.n, N);
+  ALLOC(d.ring_first, N);
+  ALLOC(d.Kr, N);
+  ALLOC(d.dom, N * d.Kmax);
+  ALLOC(d.hot_row, N * B);
+  ALLOC(d.hot_stamp, N * B);
+  ALLOC(d.lru, N * B);
+  ALLOC(d.hot_map, N * (size_t)d.Sm);
+  ALLOC(d.opt_map, N * (size_t)d.Sm);
+  ALLOC(d.opt_list, N * (size_t)std::max<int64_t>(1, d.opt_max));
+  ALLOC(d.opt_count, N);
+  ALLOC(d.scores, N * d.Kmax * (size_t)d.Sm);
+  ALLOC(d.minmax, N * d.Kmax * 2);
+  ALLOC(d.uni, N * KK);
+  ALLOC(d.uloc, N * KK);
+  ALLOC(d.miss, N * KK);
+  ALLOC(d.first_occ, N * KK);
+  ALLOC(d.counts, N * 4);
+  ALLOC(d.promo_src, N * B);
+  ALLOC(d.promo_dst, N * B);
+  ALLOC(d.aux, N * 4);
+  const size_t pf = attn_partial_floats(d, c->n_split);
+  ALLOC(d.part_o, c->n_split > 1 ? pf : 1);
+  d.part_ml = nullptr;
+  ALLOC(d.part_ml, c->n_split > 1 ? N * d.Kmax * d.Hq * c->n_split * 2 : 1);
+  ALLOC(d.stats, ST_COUNT);
+  ALLOC(d.err, 2);
+  ALLOC(c->rh_qidx, N * d.Kmax * d.idx_row);
+  ALLOC(c->rh_q, N * d.Kmax * d.Hq * d.dqk);
+  ALLOC(c->rh_block, N * d.Kmax * R);
+  ALLOC(c->rh_out, N * d.Kmax * d.Hq * d.dv);
+  ALLOC(c->rh_lse, N * d.Kmax * d.Hq);
+  ALLOC(c->rh_topk, N * KK);
+  ALLOC(c->rh_loc, N * KK);
+#undef ALLOC
+  if (e != cudaSuccess) {
+    free_all(c);
+    delete c;
+    return DHS_ERR_OOM;
+  }
+  d.keys = c->d_keys;
+  d.host = c->d_host;
+  e = cudaMemset(c->d_keys, 0, N * sizeof(void *));
+  if (e == cudaSuccess) e = cudaMemset(c->d_host, 0, N * sizeof(void *));
+  if (e == cudaSuccess) e = cudaMemset(d.Kr, 0, N * 4);
+  if (e == cudaSuccess) e = cudaMemset(d.n, 0, N * 8);
+  if (e == cudaSuccess) e = cudaMemset(d.stats, 0, ST_COUNT * 8);
+  if (e == cudaSuccess) e = cudaMemset(d.err, 0, 8);
+  if (e == cudaSuccess) e = cudaMemset(d.counts, 0, N * 16);
+  if (e == cudaSuccess) e = cudaMemset(d.opt_count, 0, N * 8);
+  if (e == cudaSuccess) e = cudaMemset(pool, 0, pool_rows * R * 2);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    free_all(c);
+    delete c;
+    return DHS_ERR_CUDA;
+  }
+  c->n.assign(N, 0);
+  c->ring_first.assign(N, 0);
+  c->opt_count.assign(N, 0);
+  c->K.assign(N, 0);
+  c->bound.assign(N, 0);
+  c->host_ptr.assign(N, nullptr);
+  c->key_ptr.assign(N, nullptr);
+  *out = c;
+  return DHS_OK;
+}
+
+void dhs_destroy(dhs_ctx *c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  free_all(c);
+  delete c;
+}
+
+int64_t dhs_ring_rows(const dhs_ctx *c) { return c ? c->d.Rd : 0; }
+
+int64_t dhs_device_bytes(const dhs_ctx *c) {
+  if (!c) return 0;
+  int64_t total = 0;
+  for (int i = 0; i < DHS_BUF_COUNT_; ++i) total += (int64_t)buffer_desc(c, i).bytes;
+  return total;
+}
+
+int dhs_bind_request(dhs_ctx *c, int32_t slot, const void *host_kv, const int8_t *idx_keys,
+                     int64_t n_committed, dhs_stream stream) {
+  if (!c || slot < 0 || slot >= c->d.N || !host_kv || !idx_keys || n_committed < 0 ||
+      n_committed > c->d.Sm || !aligned16(host_kv) || !aligned16(idx_keys))
+    return DHS_ERR_INVALID;
+  if (c->phase != PH_IDLE) return DHS_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void *dev_host = nullptr;
+  if (cudaHostGetDevicePointer(&dev_host, const_cast<void *>(host_kv), 0) != cudaSuccess) {
+    cudaGetLastError();
+    return DHS_ERR_INVALID;  // not page-locked host memory
+  }
+  c->host_ptr[slot] = dev_host;
+  c->key_ptr[slot] = idx_keys;
+  if (cudaMemcpyAsync(c->d_host, c->host_ptr.data(), c->d.N * sizeof(void *),
+                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(c->d_keys, c->key_ptr.data(), c->d.N * sizeof(void *),
+                      cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return DHS_ERR_CUDA;
+  // the host arrays above are pageable: the copies are staged before returning
+  {
+    cudaError_t e_ = launch_bind_reset(c->d, slot, n_committed, s, &c->timer);
+    if (e_ != cudaSuccess) return cuda_fail(c, e_);
+  }
+  c->n[slot] = n_committed;
+  c->ring_first[slot] = n_committed;
+  c->opt_count[slot] = 0;
+  c->K[slot] = 0;
+  c->bound[slot] = 1;
+  return DHS_OK;
+}
+
+int dhs_select(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const int64_t *pos,
+               int32_t *topk_out, dhs_stream stream) {
+  if (!c || !q_idx || !k_per_req || !topk_out || !aligned16(q_idx)) return DHS_ERR_INVALID;
+  if (c->phase != PH_IDLE) return DHS_ERR_INVALID;
+  const DevCtx &d = c->d;
+  std::vector<int32_t> w(d.N + d.N * d.Kmax, 0);
+  int max_dom = 0, active = 0;
+  for (int r = 0; r < d.N; ++r) {
+    const int kr = k_per_req[r];
+    if (kr < 0 || kr > d.Kmax || (kr > 0 && !c->bound[r])) return DHS_ERR_INVALID;
+  }
+  for (int r = 0; r < d.N; ++r) {
+    const int kr = k_per_req[r];
+    w[r] = kr;
+    active += kr;
+    for (int j = 0; j < kr; ++j) {
+      int64_t p = pos ? pos[(size_t)r * d.Kmax + j] : c->n[r] + j;
+      int64_t dom = std::max<int64_t>(0, std::min<int64_t>(c->n[r], p + 1));
+      w[d.N + r * d.Kmax + j] = (int32_t)dom;
+      max_dom = std::max<int>(max_dom, (int)dom);
+    }
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // Kr and dom are consecutive in one upload when they are adjacent in memory;
+  // they are separate allocations, so upload twice.
+  std::vector<int32_t> wk(w.begin(), w.begin() + d.N), wd(w.begin() + d.N, w.end());
+  if (upload_words(c, d.Kr, wk, s) || upload_words(c, d.dom, wd, s)) return DHS_ERR_CUDA;
+  {
+    cudaError_t e_ = launch_select(d, q_idx, topk_out, max_dom, active, s, &c->timer);
+    if (e_ != cudaSuccess) return cuda_fail(c, e_);
+  }
+  for (int r = 0; r < d.N; ++r) c->K[r] = k_per_req[r];
+  c->phase = PH_SELECTED;
+  return DHS_OK;
+}
+
+int dhs_resolve(dhs_ctx *c, const int32_t *topk, int32_t *loc_out, int32_t shared,
+                dhs_stream stream) {
+  if (!c || !topk || !loc_out || (shared != 0 && shared != 1)) return DHS_ERR_INVALID;
+  if (c->phase != PH_SELECTED) return DHS_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  c->tick += 1;
+  if (c->tick > 0x7FFFFFF0) return DHS_ERR_CAPACITY;
+  {
+    cudaError_t e_ = launch_resolve(c->d, topk, loc_out, shared, (int)c->tick, s, &c->timer);
+    if (e_ != cudaSuccess) return cuda_fail(c, e_);
+  }
+  c->phase = PH_RESOLVED;
+  return DHS_OK;
+}
+
+int dhs_attend(dhs_ctx *c, const void *q, const void *block_kv, const int32_t *loc, void *out,
+               float *lse, dhs_stream stream) {
+  if (!c || !q || !block_kv || !loc || !out) return DHS_ERR_INVALID;
+  if (!aligned16(block_kv) || ((uintptr_t)q & 3u) || ((uintptr_t)out & 3u))
+    return DHS_ERR_INVALID;
+  if (c->phase != PH_RESOLVED) return DHS_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  {
+    cudaError_t e_ = launch_attend(c->d, static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(block_kv),
+                    loc, static_cast<uint16_t *>(out), lse, c->n_split, s,
+                    &c->timer);
+    if (e_ != cudaSuccess) return cuda_fail(c, e_);
+  }
+  c->phase = PH_ATTENDED;
+  return DHS_OK;
+}
+
+int dhs_commit(dhs_ctx *c, const int32_t *accepted_len, dhs_stream stream) {
+  if (!c || !accepted_len) return DHS_ERR_INVALID;
+  if (c->phase != PH_ATTENDED) return DHS_ERR_INVALID;
+  const DevCtx &d = c->d;
+  for (int r = 0; r < d.N; ++r) {
+    if (c->K[r] == 0) continue;
+    const int a = accepted_len[r];
+    if (a < 0 || a > c->K[r]) return DHS_ERR_INVALID;
+    if (c->n[r] + a > d.Sm) return DHS_ERR_CAPACITY;
+  }
+  std::vector<int32_t> w(d.N * 4, 0);
+  for (int r = 0; r < d.N; ++r) {
+    const int a = c->K[r] ? accepted_len[r] : 0;
+    w[r * 4 + 0] = a;
+    w[r * 4 + 1] = (int32_t)(uint32_t)(c->n[r] & 0xFFFFFFFF);
+    w[r * 4 + 2] = (int32_t)(c->n[r] >> 32);
+    w[r * 4 + 3] = c->K[r] ? 1 : 0;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (upload_words(c, d.aux, w, s)) return DHS_ERR_CUDA;
+  {
+    cudaError_t e_ = launch_commit(d, s, &c->timer);
+    if (e_ != cudaSuccess) return cuda_fail(c, e_);
+  }
+  for (int r = 0; r < d.N; ++r) {
+    if (c->K[r] == 0) continue;
+    c->n[r] += accepted_len[r];
+    c->K[r] = 0;
+  }
+  c->phase = PH_IDLE;
+  return DHS_OK;
+}
+
+int dhs_set_residency(dhs_ctx *c, int32_t slot, const int32_t *rows, int64_t n_rows,
+                      dhs_stream stream) {
+  if (!c || slot < 0 || slot >= c->d.N || n_rows < 0 || (n_rows > 0 && !rows))
+    return DHS_ERR_INVALID;
+  if (!c->bound[slot]) return DHS_ERR_INVALID;
+  if (c->phase == PH_RESOLVED) return DHS_ERR_INVALID;
+  if (n_rows > c->d.opt_max) return DHS_ERR_CAPACITY;
+  {
+    std::vector<char> seen((size_t)c->n[slot], 0);
+    for (int64_t i = 0; i < n_rows; ++i) {
+      const int32_t v = rows[i];
+      if (v < 0 || v >= c->n[slot] || seen[v]) return DHS_ERR_INVALID;
+      seen[v] = 1;
+    }
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  {
+    cudaError_t e_ = launch_residency(c->d, slot, c->opt_count[slot], -1, s, &c->timer);
+    if (e_ != cudaSuccess) return cuda_fail(c, e_);
+  }
+  if (n_rows > 0 &&
+      cudaMemcpyAsync(c->d.opt_list + (size_t)slot * c->d.opt_max, rows, n_rows * 4,
+                      cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return DHS_ERR_CUDA;
+  {
+    cudaError_t e_ = launch_residency(c->d, slot, -1, n_rows, s, &c->timer);
+    if (e_ != cudaSuccess) return cuda_fail(c, e_);
+  }
+  c->opt_count[slot] = n_rows;
+  return DHS_OK;
+}
+
+int dhs_get_stats(dhs_ctx *c, dhs_stats *out, dhs_stream stream) {
+  if (!c || !out) return DHS_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned long long st[ST_COUNT];
+  int32_t err[2];
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DHS_ERR_CUDA;
+  if (cudaMemcpy(st, c->d.stats, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(err, c->d.err, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DHS_ERR_CUDA;
+  memset(out, 0, sizeof(*out));
+  out->resolve_calls = c->tick;
+  out->selections = st[ST_SEL];
+  out->union_rows = st[ST_UNION];
+  out->ring_hits = st[ST_RING];
+  out->opt_hits = st[ST_OPT];
+  out->hot_hits = st[ST_HOT];
+  out->misses = st[ST_MISS];
+  out->miss_selections = st[ST_MISS_SEL];
+  out->host_rows_fetched = st[ST_FETCHED];
+  out->host_bytes = (int64_t)st[ST_FETCHED] * c->d.row * 2;
+  out->installs = st[ST_INSTALL];
+  out->evictions = st[ST_EVICT];
+  out->direct_only = st[ST_DIRECT];
+  out->device_error = err[0];
+  out->device_error_site = err[1];
+  return err[0] ? DHS_ERR_DEVICE_CHECK : DHS_OK;
+}
+
+int dhs_reset_stats(dhs_ctx *c, dhs_stream stream) {
+  if (!c) return DHS_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(c->d.stats, 0, ST_COUNT * 8, s) != cudaSuccess ||
+      cudaMemsetAsync(c->d.err, 0, 8, s) != cudaSuccess)
+    return DHS_ERR_CUDA;
+  return DHS_OK;
+}
+
+int64_t dhs_buffer_bytes(const dhs_ctx *c, int32_t which) {
+  if (!c || which < 0 || which >= DHS_BUF_COUNT_) return -1;
+  return (int64_t)buffer_desc(c, which).bytes;
+}
+
+int dhs_export(dhs_ctx *c, int32_t which, void *dst, int64_t bytes, dhs_stream stream) {
+  if (!c || !dst || which < 0 || which >= DHS_BUF_COUNT_) return DHS_ERR_INVALID;
+  BufDesc b = buffer_desc(c, which);
+  if (bytes < 0 || (size_t)bytes > b.bytes) return DHS_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dst, b.ptr, bytes, cudaMemcpyDefault, s) != cudaSuccess) return DHS_ERR_CUDA;
+  return DHS_OK;
+}
+
+int dhs_set_timing(dhs_ctx *c, int32_t enable) {
+  if (!c) return DHS_ERR_INVALID;
+  c->timer.enabled = enable != 0;
+  c->timer.reset();
+  return DHS_OK;
+}
+
+int dhs_kernel_times(dhs_ctx *c, int32_t max_ids, int64_t *launches, double *total_ms) {
+  if (!c || !launches || !total_ms || max_ids < 1) return DHS_ERR_INVALID;
+  int64_t l[K_COUNT];
+  double ms[K_COUNT];
+  c->timer.collect(l, ms);
+  for (int i = 0; i < max_ids && i < K_COUNT; ++i) {
+    launches[i] = l[i];
+    total_ms[i] = ms[i];
+  }
+  return DHS_OK;
+}
+
+int dhs_snapshot(dhs_ctx *c, int32_t *snapshot_id, dhs_stream stream) {
+  if (!c || !snapshot_id) return DHS_ERR_INVALID;
+  if (c->phase != PH_IDLE) return DHS_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Snapshot sn;
+  for (int which : kStateBufs) {
+    BufDesc b = buffer_desc(c, which);
+    void *p = nullptr;
+    if (cudaMalloc(&p, b.bytes ? b.bytes : 16) != cudaSuccess) {
+      cudaGetLastError();
+      for (void *q : sn.bufs) cudaFree(q);
+      return DHS_ERR_OOM;
+    }
+    sn.bufs.push_back(p);
+    if (b.bytes && cudaMemcpyAsync(p, b.ptr, b.bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return DHS_ERR_CUDA;
+  }
+  sn.n = c->n;
+  sn.ring_first = c->ring_first;
+  sn.opt_count = c->opt_count;
+  sn.K = c->K;
+  sn.tick = c->tick;
+  sn.phase = c->phase;
+  c->snaps.push_back(std::move(sn));
+  *snapshot_id = (int32_t)c->snaps.size() - 1;
+  return DHS_OK;
+}
+
+int dhs_restore(dhs_ctx *c, int32_t id, dhs_stream stream) {
+  if (!c || id < 0 || id >= (int32_t)c->snaps.size()) return DHS_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Snapshot &sn = c->snaps[id];
+  int i = 0;
+  for (int which : kStateBufs) {
+    BufDesc b = buffer_desc(c, which);
+    if (b.bytes &&
+        cudaMemcpyAsync(b.ptr, sn.bufs[i], b.bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return DHS_ERR_CUDA;
+    ++i;
+  }
+  // ring_first, Kr and the optional counts are small: upload from the mirrors
+  std::vector<int32_t> w(c->d.N * 2);
+  for (int r = 0; r < c->d.N; ++r) {
+    w[2 * r] = (int32_t)(uint32_t)(sn.ring_first[r] & 0xFFFFFFFF);
+    w[2 * r + 1] = (int32_t)(sn.ring_first[r] >> 32);
+  }
+  if (upload_words(c, reinterpret_cast<int32_t *>(c->d.ring_first), w, s)) return DHS_ERR_CUDA;
+  for (int r = 0; r < c->d.N; ++r) {
+    w[2 * r] = (int32_t)(uint32_t)(sn.opt_count[r] & 0xFFFFFFFF);
+    w[2 * r + 1] = (int32_t)(sn.opt_count[r] >> 32);
+  }
+  if (upload_words(c, reinterpret_cast<int32_t *>(c->d.opt_count), w, s)) return DHS_ERR_CUDA;
+  std::vector<int32_t> wk(sn.K.begin(), sn.K.end());
+  if (upload_words(c, c->d.Kr, wk, s)) return DHS_ERR_CUDA;
+  c->n = sn.n;
+  c->ring_first = sn.ring_first;
+  c->opt_count = sn.opt_count;
+  c->K = sn.K;
+  c->tick = sn.tick;
+  c->phase = sn.phase;
+  return DHS_OK;
+}
+
+int dhs_round_host(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const void *q,
+                   const void *block_kv, const int32_t *accepted_len, void *out, float *lse,
+                   dhs_stream stream) {
+  if (!c || !q_idx || !k_per_req || !q || !block_kv || !accepted_len || !out)
+    return DHS_ERR_INVALID;
+  const DevCtx &d = c->d;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t nq = (size_t)d.N * d.Kmax;
+  if (cudaMemcpyAsync(c->rh_qidx, q_idx, nq * d.idx_row, cudaMemcpyHostToDevice, s) ||
+      cudaMemcpyAsync(c->rh_q, q, nq * d.Hq * d.dqk * 2, cudaMemcpyHostToDevice, s) ||
+      cudaMemcpyAsync(c->rh_block, block_kv, nq * d.row * 2, cudaMemcpyHostToDevice, s))
+    return DHS_ERR_CUDA;
+  int rc = dhs_select(c, c->rh_qidx, k_per_req, nullptr, c->rh_topk, stream);
+  if (!rc) rc = dhs_resolve(c, c->rh_topk, c->rh_loc, 1, stream);
+  if (!rc) rc = dhs_attend(c, c->rh_q, c->rh_block, c->rh_loc, c->rh_out, lse ? c->rh_lse : nullptr,
+                           stream);
+  if (!rc) rc = dhs_commit(c, accepted_len, stream);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(out, c->rh_out, nq * d.Hq * d.dv * 2, cudaMemcpyDeviceToHost, s) ||
+      (lse && cudaMemcpyAsync(lse, c->rh_lse, nq * d.Hq * 4, cudaMemcpyDeviceToHost, s)))
+    return DHS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DHS_ERR_CUDA;
+  return DHS_OK;
+}
+
+}  // extern "C"

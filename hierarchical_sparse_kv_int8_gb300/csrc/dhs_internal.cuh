@@ -1,0 +1,186 @@
+// Internal declarations shared by the translation units of libdhs.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/dhs.h"
+
+namespace dhs {
+
+constexpr int kMaxSlots = 256;
+constexpr int kMaxKmax = 8;
+constexpr int kMaxTopk = 4096;
+constexpr int kUploadWords = 4096;  // int32 words carried by one k_upload launch
+
+// Kernel ids (per-kernel timing and device error sites).
+enum KernelId {
+  K_UPLOAD = 0,
+  K_SCORE,
+  K_TOPK,
+  K_UNION_PROBE,
+  K_GATHER,
+  K_ATTN,
+  K_MERGE,
+  K_POST_ATTEND,
+  K_COMMIT,
+  K_RESIDENCY_CLEAR,
+  K_RESIDENCY_FILL,
+  K_RESIDENCY_PUBLISH,
+  K_BIND_RESET,
+  K_COUNT
+};
+extern const char *const kKernelNames[K_COUNT];
+
+// Device error codes recorded by kernels (first one wins).
+enum DeviceCheck {
+  DC_OK = 0,
+  DC_ROW_RANGE = 1,   // a selected row outside [0, n_r)
+  DC_LOC_RANGE = 2,   // a location tag or index outside its tier
+  DC_CAPACITY = 3,    // a staging or pool index beyond capacity
+};
+
+// Everything a kernel needs to know about the context, passed by value.
+struct DevCtx {
+  int N, Kmax, k;
+  int64_t Sm;
+  int idx_row;           // H_idx * d_idx bytes per index-key row
+  int Hq, Hkv, dqk, dv, row;  // row = bf16 elements per stored row
+  int layout;
+  int B;
+  int W, p, Rd;
+  int64_t opt_max;
+  float scale_log2;      // softmax scale * log2(e)
+
+  // per-slot binding
+  const int8_t *const *keys;     // [N] device index keys
+  const uint16_t *const *host;   // [N] device-visible host backing
+  int64_t *n;                    // [N] committed frontier
+  int64_t *ring_first;           // [N]
+  int32_t *Kr;                   // [N] queries this round
+  int32_t *dom;                  // [N][Kmax] selectable rows per query
+
+  // payload tiers (one pool, four regions)
+  uint16_t *hot_data;            // [N][B][row]
+  uint16_t *stage;               // [N][Kmax*k][row]
+  uint16_t *ring;                // [N][Rd][row]
+  uint16_t *opt;                 // [N][opt_max][row]
+
+  // metadata
+  int32_t *hot_row, *hot_stamp, *lru;  // [N][B]
+  int32_t *hot_map, *opt_map;          // [N][Sm]
+  int32_t *opt_list;                   // [N][opt_max]
+  int64_t *opt_count;                  // [N]
+
+  // scratch of one round
+  int32_t *scores;      // [N][Kmax][Sm]
+  int32_t *minmax;      // [N][Kmax][2]
+  int32_t *uni;         // [N][Kmax*k]
+  int32_t *uloc;        // [N][Kmax*k]
+  int32_t *miss;        // [N][Kmax*k]
+  int32_t *first_occ;   // [N][Kmax*k]
+  int32_t *counts;      // [N][4]
+  int32_t *promo_src;   // [N][B]
+  int32_t *promo_dst;   // [N][B]
+  int32_t *topk_last;   // [N][Kmax][k] selection seen by the last resolve
+  int32_t *aux;         // [N][4]: a_r and n_old for commit
+  float *part_o;        // attention partials
+  float *part_ml;
+  unsigned long long *stats;  // counters, see StatIdx
+  int32_t *err;               // [2]: code, site
+};
+
+enum StatIdx {
+  ST_RESOLVE = 0, ST_SEL, ST_UNION, ST_RING, ST_OPT, ST_HOT, ST_MISS, ST_MISS_SEL,
+  ST_FETCHED, ST_INSTALL, ST_EVICT, ST_DIRECT, ST_COUNT
+};
+
+__device__ __forceinline__ void record_error(int32_t *err, int code, int site) {
+  if (atomicCAS(err, 0, code) == 0) err[1] = site;
+}
+
+__device__ __forceinline__ int loc_tier(int32_t l) { return (l >> DHS_LOC_TIER_SHIFT) & 3; }
+__device__ __forceinline__ int loc_index(int32_t l) { return l & DHS_LOC_INDEX_MASK; }
+__device__ __forceinline__ int32_t make_loc(int tier, int idx) {
+  return (int32_t)((tier << DHS_LOC_TIER_SHIFT) | idx);
+}
+
+// Device address of the payload row a location names, or nullptr when the
+// tag or index is out of range (the caller records DC_LOC_RANGE).
+__device__ __forceinline__ const uint16_t *loc_row(const DevCtx &c, int r, int32_t l) {
+  int tier = loc_tier(l), idx = loc_index(l);
+  size_t row = (size_t)c.row;
+  switch (tier) {
+    case DHS_LOC_RING:
+      return idx < c.Rd ? c.ring + ((size_t)r * c.Rd + idx) * row : nullptr;
+    case DHS_LOC_OPT:
+      return idx < c.opt_max ? c.opt + ((size_t)r * c.opt_max + idx) * row : nullptr;
+    case DHS_LOC_HOT:
+      return idx < c.B ? c.hot_data + ((size_t)r * c.B + idx) * row : nullptr;
+    default:
+      return idx < c.Kmax * c.k ? c.stage + ((size_t)r * c.Kmax * c.k + idx) * row : nullptr;
+  }
+}
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` (cached).
+template <typename F>
+cudaError_t ensure_smem(F *func, size_t bytes, size_t &granted) {
+  if (bytes <= granted) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) granted = bytes;
+  return e;
+}
+constexpr size_t kMaxDynSmem = 226 * 1024;  // leaves room for static shared memory
+
+// Words uploaded by k_upload (kernel parameter, <= 16 KB).
+struct UploadWords {
+  int32_t w[kUploadWords];
+};
+
+// ---- launchers (each returns the cudaGetLastError of its launch) -------
+cudaError_t launch_upload(int32_t *dst, const int32_t *words, int n, cudaStream_t s);
+cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_out,
+                          int max_dom, int active, cudaStream_t s, class Timer *tm);
+cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_out,
+                           int shared, int tick, cudaStream_t s, class Timer *tm);
+cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *block,
+                          const int32_t *loc, uint16_t *out, float *lse, int n_split,
+                          cudaStream_t s, class Timer *tm);
+cudaError_t launch_commit(const DevCtx &c, cudaStream_t s, class Timer *tm);
+cudaError_t launch_residency(const DevCtx &c, int slot, int64_t old_count, int64_t new_count,
+                             cudaStream_t s, class Timer *tm);
+cudaError_t launch_bind_reset(const DevCtx &c, int slot, int64_t n_committed, cudaStream_t s,
+                              class Timer *tm);
+
+// Attention split heuristic and scratch size (floats) for a context.
+int attn_splits(const DevCtx &c, int active_queries);
+size_t attn_partial_floats(const DevCtx &c, int max_splits);
+size_t union_smem_bytes(const DevCtx &c);
+bool attn_shape_supported(int dqk, int dv, int layout);
+
+// Per-kernel CUDA-event timing (host side).
+class Timer {
+ public:
+  bool enabled = false;
+  void begin(int id, cudaStream_t s);
+  void end(int id, cudaStream_t s);
+  void collect(int64_t *launches, double *ms);  // synchronises pending events
+  void reset();
+  ~Timer();
+
+ private:
+  struct Pending { int id; cudaEvent_t a, b; };
+  std::vector<Pending> pending_;
+  std::vector<cudaEvent_t> pool_;
+  int64_t launches_[K_COUNT] = {};
+  double ms_[K_COUNT] = {};
+  cudaEvent_t take();
+  void drain(size_t keep);
+  int open_id_ = -1;
+  cudaEvent_t open_a_ = nullptr;
+};
+
+}  // namespace dhs

@@ -1,0 +1,272 @@
+/*
+ * dhs.h -- C ABI of libdhs: speculative-verification sparse attention over a
+ * two-tier KV cache, for one GB300 GPU (sm_103a).
+ *
+ * Source of every operation: "Adaptive DHiSparse: Speculative Decoding over a
+ * Load-Adaptive KV Hierarchy" (arXiv 2610.13708), cited as [ADHS] with the
+ * section, equation or figure that defines it.
+ *
+ * One dhs_ctx is one KV source (one payload layer, [ADHS] 2.2 "physical-source
+ * sharing") serving n_slots request slots.  A verification round of request r
+ * runs, all on one caller stream:
+ *
+ *   dhs_select   indexer scores + per-query top-k over the causal history
+ *   dhs_resolve  union of the K_r selections, probe ring / optional map / hot
+ *                cache, compact the misses, fetch each missing row once from
+ *                pinned host memory into staging, emit one location per
+ *                selected entry
+ *   dhs_attend   write the block rows into the draft ring, attend every query
+ *                over its own selection plus the block rows up to itself, then
+ *                copy promoted rows from staging into the hot cache
+ *   dhs_commit   keep the accepted prefix of the block, roll back the rest
+ *
+ * Conventions
+ *   - Pointers marked "device" are CUDA device pointers; "host" pointers are
+ *     read by the calling thread before the function returns; "pinned" host
+ *     memory must stay allocated and page-locked (cudaHostAlloc or
+ *     cudaHostRegister) while bound.
+ *   - All calls that take a stream only enqueue work on it and return; argument
+ *     errors are detected on the host before anything is launched.
+ *   - Kernels check the indices they read (selected rows, locations) and, on
+ *     a bad one, skip the access and record DHS_ERR_DEVICE_CHECK in a device
+ *     error word, which dhs_get_stats reports after synchronising the stream.
+ *     No kernel ever traps or waits on a flag.
+ *   - Buffers passed by the caller stay owned by the caller.  Everything the
+ *     context allocates (hot cache, staging, ring, optional pool, maps,
+ *     scratch) is owned by it and freed by dhs_destroy.
+ *   - bf16 values are passed as raw 16-bit storage (uint16_t).
+ */
+#ifndef DHS_H_
+#define DHS_H_
+
+#include <stdint.h>
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dhs_ctx dhs_ctx;
+typedef struct CUstream_st *dhs_stream; /* a cudaStream_t; NULL = legacy default stream */
+
+/* Error codes. */
+enum {
+  DHS_OK = 0,
+  DHS_ERR_INVALID = 1,      /* bad argument, shape or call order             */
+  DHS_ERR_OOM = 2,          /* device or pinned allocation failed            */
+  DHS_ERR_CAPACITY = 3,     /* request exceeds a configured capacity         */
+  DHS_ERR_CUDA = 4,         /* a CUDA runtime call failed                    */
+  DHS_ERR_DEVICE_CHECK = 5, /* a kernel found an out-of-range index          */
+  DHS_ERR_TIMEOUT = 6       /* reserved: a bounded host wait ran out         */
+};
+
+/* Location tags, [ADHS] 3.5 eq. (12): each selected entry l_{r,j,i} names the
+ * GPU tier that holds row s_{r,j,i} and its index within request r's part of
+ * that tier: loc = (tier << 28) | index, or -1 for an empty entry.
+ *   RING : draft-ring row (t mod R_d) of committed position t, eq. (10)
+ *   OPT  : slot of the optional-history pool, [ADHS] 3.1
+ *   HOT  : slot of the B-row hot cache, [ADHS] 2.2 / 3.2
+ *   STAGE: row of the verification staging arena, [ADHS] 3.3-3.4 */
+enum { DHS_LOC_RING = 0, DHS_LOC_OPT = 1, DHS_LOC_HOT = 2, DHS_LOC_STAGE = 3 };
+#define DHS_LOC_TIER_SHIFT 28
+#define DHS_LOC_INDEX_MASK ((1 << DHS_LOC_TIER_SHIFT) - 1)
+
+/* Row layouts of the stored KV payload. */
+enum {
+  DHS_KV_SPLIT = 0, /* GQA: row = K of kv heads 0..Hkv-1 (qk_dim each), then V heads (v_dim each) */
+  DHS_KV_LATENT = 1 /* MLA-like shared latent: row = qk_dim elements; K = row, V = row[0:v_dim]     */
+};
+
+/* Fixed at dhs_create.  Limits: n_slots <= 256, k_max <= 8, topk <= 4096 (a
+ * multiple of 32), q_heads / kv_heads <= 16, qk_dim and v_dim multiples of 16,
+ * idx_heads * idx_dim a multiple of 16 and <= 1024, budget <= 65535. */
+typedef struct {
+  int32_t n_slots;      /* N request slots                                      */
+  int32_t k_max;        /* K_max: widest verification block, [ADHS] 3.3         */
+  int32_t topk;         /* k: rows selected per query, [ADHS] eq. (1)           */
+  int64_t s_max;        /* rows of history (plus room for commits) per request  */
+  int32_t idx_heads;    /* H_idx: indexer heads, summed                         */
+  int32_t idx_dim;      /* d_idx: int8 elements per indexer head                */
+  int32_t q_heads;      /* Hq attention query heads                             */
+  int32_t kv_heads;     /* Hkv kv heads (1 for DHS_KV_LATENT)                   */
+  int32_t qk_dim;       /* key/query head dim (latent width for DHS_KV_LATENT)  */
+  int32_t v_dim;        /* value head dim                                       */
+  int32_t kv_layout;    /* DHS_KV_SPLIT or DHS_KV_LATENT                        */
+  int32_t budget;       /* B: hot-cache rows per request, [ADHS] 2.2            */
+  int32_t ring_window;  /* W: drafter window, [ADHS] eq. (9)                    */
+  int32_t page_rows;    /* p: rows per page, [ADHS] eq. (9)                     */
+  int64_t opt_rows_max; /* optional-pool rows per request (0 = no optional map) */
+  float softmax_scale;  /* 0 = 1/sqrt(qk_dim)                                   */
+} dhs_config;
+
+/* Cumulative counters since dhs_create (or dhs_reset_stats). */
+typedef struct {
+  int64_t resolve_calls;
+  int64_t selections;        /* valid selected entries resolved               */
+  int64_t union_rows;        /* sum over requests of |U_r|, eq. (6)           */
+  int64_t ring_hits;         /* union rows served by the draft ring (tail)    */
+  int64_t opt_hits;          /* union rows served by the optional map         */
+  int64_t hot_hits;          /* union rows served by the hot cache            */
+  int64_t misses;            /* distinct missing rows |D_r|, eq. (6)          */
+  int64_t miss_selections;   /* selected entries whose row was missing        */
+  int64_t host_rows_fetched; /* rows copied from host (shared: |D_r|)         */
+  int64_t host_bytes;        /* bytes copied from host                        */
+  int64_t installs;          /* rows promoted into the hot cache              */
+  int64_t evictions;         /* promotions that replaced a cached row         */
+  int64_t direct_only;       /* requests whose union resolved in step 1 only  */
+  int32_t device_error;      /* first device check code (0 = none)           */
+  int32_t device_error_site; /* kernel id that recorded it                    */
+} dhs_stats;
+
+/* Create a context.  Allocates (cudaMalloc, on the current device) the hot
+ * cache, staging arena (k_max * topk rows per slot, [ADHS] 3.4 with chi = 1),
+ * draft ring (R_d = p * ceil((W + p - 1 + k_max) / p) rows per slot, [ADHS]
+ * eq. (9)), optional pool, the row->slot maps and all scratch.  All slots start
+ * unbound.  Returns DHS_ERR_INVALID on a bad config, DHS_ERR_OOM if an
+ * allocation fails (nothing is leaked). */
+int dhs_create(const dhs_config *cfg, dhs_ctx **out);
+
+/* Free everything the context owns.  Synchronises the device first.  NULL is a no-op. */
+void dhs_destroy(dhs_ctx *ctx);
+
+/* Ring rows per slot, eq. (9), and staging bytes, M_stage of [ADHS] 3.4 with chi = 1. */
+int64_t dhs_ring_rows(const dhs_ctx *ctx);
+int64_t dhs_device_bytes(const dhs_ctx *ctx); /* total device memory the context holds */
+
+/* Bind request slot `slot` to its history.
+ *   host_kv  pinned host, bf16 [s_max][row_elems]: the full host backing H_r
+ *            ([ADHS] 2.2 fixed-cache offloading).  Read by dhs_resolve and
+ *            dhs_set_residency, written by dhs_commit.
+ *   idx_keys device, int8 [s_max][idx_heads * idx_dim]: GPU index state
+ *            ([ADHS] 2.2 "compact indexer state remains on the GPU").  Rows at
+ *            or beyond n_committed may be filled later by the caller.
+ *   n_committed  n_r, committed history rows (0 <= n_committed <= s_max).
+ * Resets the slot's hot cache (empty), optional set (empty) and ring (no live
+ * rows: positions before n_committed are served by the hierarchy). */
+int dhs_bind_request(dhs_ctx *ctx, int32_t slot, const void *host_kv, const int8_t *idx_keys,
+                     int64_t n_committed, dhs_stream stream);
+
+/* Step 1, [ADHS] 2.1 eq. (1) with the causal domain of eq. (5).
+ *   q_idx      device int8 [n_slots][k_max][idx_heads][idx_dim]
+ *   k_per_req  host int32 [n_slots]: K_r queries of request r this round
+ *              (0 = slot idle this round; bound slots only; <= k_max)
+ *   pos        host int64 [n_slots][k_max] or NULL: position of query j; NULL
+ *              means n_r + j.  Query j selects among rows [0, min(n_r, pos+1)).
+ *   topk_out   device int32 [n_slots][k_max][topk]: rows ordered by score
+ *              descending, ties to the lower row, padded with -1.  Entries of
+ *              idle queries are left untouched.
+ * Score I[s] = sum_h sum_d q[h][d] * K[s][h][d] in exact int32 arithmetic. */
+int dhs_select(dhs_ctx *ctx, const int8_t *q_idx, const int32_t *k_per_req,
+               const int64_t *pos, int32_t *topk_out, dhs_stream stream);
+
+/* Steps 2-4, [ADHS] 3.2-3.3, eq. (6), Fig. 2, Fig. 3 callouts 2-3.
+ *   topk     device int32 [n_slots][k_max][topk] (from dhs_select or the caller;
+ *            entries must be -1 or rows < n_r)
+ *   loc_out  device int32 [n_slots][k_max][topk]: one location per entry
+ *   shared   1: each distinct missing row of a request is fetched once and its
+ *            staging location returned to every query that selected it;
+ *            0: per-query baseline, every missing selection fetched on its own
+ *            into staging row j*topk+i.  The cache state is the same in both.
+ * Probe order per union row (ascending): live draft-ring rows
+ * [max(first, n_r - W), n_r), then the ready optional map, then the hot cache
+ * (a hit refreshes the slot's stamp to this call's tick).  Hot rows of the
+ * union are protected; victims are the other slots ordered by (stamp, slot),
+ * empty first; the first min(|D_r|, #victims) missing rows, ascending, take
+ * them.  Their bytes reach the hot cache in dhs_attend, after attention.
+ * One tick of the LRU clock per call.  Must be followed by dhs_attend before
+ * the next dhs_resolve or dhs_set_residency on this context. */
+int dhs_resolve(dhs_ctx *ctx, const int32_t *topk, int32_t *loc_out, int32_t shared,
+                dhs_stream stream);
+
+/* Step 5, [ADHS] eq. (1), (5), (11): for every active (r, j < K_r) and query
+ * head h (kv head h / (q_heads / kv_heads)):
+ *   out = softmax(scale * K q) V over the rows at loc[r][j][*] (entries -1
+ *   skipped) followed by block rows 0..j.
+ *   q         device bf16 [n_slots][k_max][q_heads][qk_dim]
+ *   block_kv  device bf16 [n_slots][k_max][row_elems]: rows the target computed
+ *             for positions n_r .. n_r + K_r - 1; written to the draft ring
+ *             at phi(r, n_r + u), eq. (10)
+ *   loc       device int32 [n_slots][k_max][topk] from dhs_resolve
+ *   out       device bf16 [n_slots][k_max][q_heads][v_dim]
+ *   lse       device fp32 [n_slots][k_max][q_heads] natural-log sum-exp, or NULL
+ * Then copies promoted rows from staging to their hot-cache slots ([ADHS] 3.4). */
+int dhs_attend(dhs_ctx *ctx, const void *q, const void *block_kv, const int32_t *loc,
+               void *out, float *lse, dhs_stream stream);
+
+/* Commit / rollback, [ADHS] eq. (7).
+ *   accepted_len  host int32 [n_slots]: a_r rows kept, 0 <= a_r <= K_r (the
+ *                 anchor plus accepted drafts, 1 + A_r; 0 rolls back all).
+ * Kept rows become history: n_r += a_r, and the rows are written back to the
+ * host backing (so every row not ready on the GPU has a host copy, eq. (6)).
+ * Rejected rows are never published.  DHS_ERR_INVALID if a_r is out of range,
+ * DHS_ERR_CAPACITY if n_r + a_r > s_max; nothing changes on error. */
+int dhs_commit(dhs_ctx *ctx, const int32_t *accepted_len, dhs_stream stream);
+
+/* Optional residency, [ADHS] 3.1: make `rows` (host int32 [n_rows], distinct,
+ * each < n_r) the ready optional history of `slot`; rows[i] occupies pool slot
+ * i.  Bytes are copied from the host backing first and the map entries
+ * published after the copy, in stream order.  The previous optional set of the
+ * slot stops being ready.  n_rows = 0 clears it.  DHS_ERR_CAPACITY if n_rows >
+ * opt_rows_max. */
+int dhs_set_residency(dhs_ctx *ctx, int32_t slot, const int32_t *rows, int64_t n_rows,
+                      dhs_stream stream);
+
+/* Synchronise `stream` and copy out the counters; returns DHS_ERR_DEVICE_CHECK
+ * if a kernel recorded a bad index (the counters are still filled). */
+int dhs_get_stats(dhs_ctx *ctx, dhs_stats *out, dhs_stream stream);
+int dhs_reset_stats(dhs_ctx *ctx, dhs_stream stream);
+
+/* Internal buffers, readable for tests and tools (dhs_export copies `bytes`
+ * bytes of buffer `which` into the caller's device buffer `dst`). */
+enum {
+  DHS_BUF_HOT_ROW = 0,   /* int32 [n_slots][budget], -1 = empty                */
+  DHS_BUF_HOT_STAMP = 1, /* int32 [n_slots][budget], -1 = never used           */
+  DHS_BUF_HOT_DATA = 2,  /* bf16 [n_slots][budget][row_elems]                  */
+  DHS_BUF_RING = 3,      /* bf16 [n_slots][R_d][row_elems]                     */
+  DHS_BUF_STAGE = 4,     /* bf16 [n_slots][k_max*topk][row_elems]              */
+  DHS_BUF_OPT = 5,       /* bf16 [n_slots][opt_rows_max][row_elems]            */
+  DHS_BUF_UNION = 6,     /* int32 [n_slots][k_max*topk], ascending             */
+  DHS_BUF_MISS = 7,      /* int32 [n_slots][k_max*topk], ascending             */
+  DHS_BUF_COUNTS = 8,    /* int32 [n_slots][4]: |U_r|, |D_r|, promoted, hits   */
+  DHS_BUF_LRU = 9,       /* int32 [n_slots][budget]: slots by (stamp, slot)    */
+  DHS_BUF_FRONTIER = 10, /* int64 [n_slots]: n_r                               */
+  DHS_BUF_HOT_MAP = 11,  /* int32 [n_slots][s_max]: row -> hot slot or -1      */
+  DHS_BUF_OPT_MAP = 12,  /* int32 [n_slots][s_max]: row -> pool slot or -1     */
+  DHS_BUF_COUNT_ = 13
+};
+int64_t dhs_buffer_bytes(const dhs_ctx *ctx, int32_t which);
+int dhs_export(dhs_ctx *ctx, int32_t which, void *dst, int64_t bytes, dhs_stream stream);
+
+/* Per-kernel timing: when enabled, every kernel launch of the context is
+ * bracketed by CUDA events on its stream; dhs_kernel_times synchronises and
+ * returns, per kernel id, the number of launches and total milliseconds since
+ * the last reset.  Kernel ids and names: dhs_kernel_name(id). */
+int dhs_set_timing(dhs_ctx *ctx, int32_t enable);
+int dhs_kernel_times(dhs_ctx *ctx, int32_t max_ids, int64_t *launches, double *total_ms);
+const char *dhs_kernel_name(int32_t id);
+int32_t dhs_kernel_count(void);
+
+/* Snapshot of all mutable state (device buffers and host-side frontiers), for
+ * benchmarks that repeat one round from the same state.  dhs_restore enqueues
+ * device copies on `stream`. */
+int dhs_snapshot(dhs_ctx *ctx, int32_t *snapshot_id, dhs_stream stream);
+int dhs_restore(dhs_ctx *ctx, int32_t snapshot_id, dhs_stream stream);
+
+/* One whole round through host buffers: copies q_idx, q and block_kv from host
+ * (pinned for asynchrony) to the context's device staging buffers, runs
+ * select, resolve (shared), attend and commit, and copies out and lse (lse may
+ * be NULL) back to host.  Synchronises `stream` before returning.  Shapes as in
+ * the calls above. */
+int dhs_round_host(dhs_ctx *ctx, const int8_t *q_idx, const int32_t *k_per_req, const void *q,
+                   const void *block_kv, const int32_t *accepted_len, void *out, float *lse,
+                   dhs_stream stream);
+
+const char *dhs_strerror(int code);
+
+/* Text of the CUDA runtime error behind the context's last DHS_ERR_CUDA ("" if none). */
+const char *dhs_last_error(const dhs_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DHS_H_ */

@@ -1,0 +1,152 @@
+"""GPU path against the oracle, element by element, through the C ABI.
+
+Small recipes run the oracle on every request and cover the edges: domains
+shorter than k (padding), queries placed inside the history, idle slots,
+union overflow of the hot cache, optional residency, ring hits after commits
+over several rounds, both kv layouts, shared and per-query retrieval.  The
+full-size configurations run with the bench's launch shapes and check sampled
+requests (every step is request-local, so a request is checked completely).
+"""
+import numpy as np
+import pytest
+
+import workload as wl
+from harness import build_oracle, compare_round, compare_state, oracle_round
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import hierarchical_sparse_kv_int8_gb300 as dhs
+    dhs.build()
+    dhs.load()
+
+
+def _runner(rec, **kw):
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+    return Runner(rec, **kw)
+
+
+TINY_GQA = wl.Recipe("tiny_gqa", N=3, K=4, S=700, H_idx=2, d_idx=32, topk=64, Hq=8, Hkv=1,
+                     qk_dim=128, v_dim=128, kv_layout=0, B=48, rho_within=0.6, rho_cross=0.7,
+                     W=40, p=8, opt_frac=0.1, seed=11)
+TINY_GQA2 = wl.Recipe("tiny_gqa_hkv2", N=2, K=3, S=333, H_idx=1, d_idx=48, topk=32, Hq=8, Hkv=2,
+                      qk_dim=128, v_dim=128, kv_layout=0, B=20, rho_within=0.5, rho_cross=0.5,
+                      W=16, p=4, seed=12)
+TINY_MLA = wl.Recipe("tiny_mla", N=2, K=3, S=517, H_idx=1, d_idx=128, topk=32, Hq=16, Hkv=1,
+                     qk_dim=576, v_dim=512, kv_layout=1, B=40, rho_within=0.5, rho_cross=0.6,
+                     W=24, p=8, opt_frac=0.25, seed=13)
+TINY_SHORT = wl.Recipe("tiny_short_history", N=2, K=2, S=45, H_idx=1, d_idx=64, topk=64, Hq=8,
+                       Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=32, rho_within=0.3,
+                       rho_cross=0.5, W=8, p=4, seed=14)
+
+
+def _rounds(rec, n_rounds, shared=True, k_sched=None, residency=True, label=""):
+    run = _runner(rec)
+    slots = list(range(rec.N))
+    o = build_oracle(rec, slots)
+    if residency and rec.opt_frac > 0:
+        run.set_residency()
+        for r in slots:
+            o.set_residency(r, rec.residency_rows(r))
+    for rnd in range(n_rounds):
+        kr = rec.k_per_req() if k_sched is None else k_sched(rnd)
+        acc = rec.accepted(rnd, kr)
+        run.load_round(rnd)
+        run.select(kr)
+        run.resolve(shared)
+        run.attend()
+        ores = oracle_round(o, rec, rnd, slots, kr, None, shared)
+        compare_round(run, o, ores, slots, kr, "%s round %d" % (label, rnd))
+        run.commit(acc)
+        o.commit(acc)
+        compare_state(run, o, slots, "%s round %d" % (label, rnd))
+    st = run.ctx.stats()
+    assert st["device_error"] == 0
+    return run, o, st
+
+
+@pytest.mark.parametrize("shared", [True, False])
+def test_tiny_gqa_rounds(shared):
+    _, o, st = _rounds(TINY_GQA, 4, shared=shared, label="tiny_gqa")
+    assert st["misses"] == o.stats.misses and st["hot_hits"] == o.stats.hot_hits
+    assert st["ring_hits"] == o.stats.ring_hits and st["opt_hits"] == o.stats.opt_hits
+    assert st["host_rows_fetched"] == o.stats.host_rows_fetched
+    assert st["installs"] == o.stats.installs and st["evictions"] == o.stats.evictions
+    assert o.stats.ring_hits > 0 and o.stats.opt_hits > 0 and o.stats.evictions > 0
+
+
+def test_tiny_two_kv_heads():
+    _rounds(TINY_GQA2, 3, label="tiny_hkv2")
+
+
+def test_tiny_mla_latent():
+    _rounds(TINY_MLA, 3, label="tiny_mla")
+
+
+def test_history_shorter_than_k_and_idle_slots():
+    sched = lambda rnd: np.array([2, 0] if rnd % 2 == 0 else [1, 2], np.int32)
+    _rounds(TINY_SHORT, 4, k_sched=sched, label="short")
+
+
+def test_queries_inside_history():
+    rec = TINY_GQA
+    run = _runner(rec)
+    slots = list(range(rec.N))
+    o = build_oracle(rec, slots)
+    kr = rec.k_per_req()
+    pos = np.array([[5, 63, 64, 400], [0, 1, 699, 10_000], [-1, 30, 2, 100]], np.int64)
+    run.load_round(0)
+    run.select(kr, pos)
+    run.resolve(True)
+    run.attend()
+    ores = oracle_round(o, rec, 0, slots, kr, None, True, pos)
+    compare_round(run, o, ores, slots, kr, "pos")
+
+
+def test_cfg1_full():
+    rec = wl.CONFIGS["cfg1"]
+    _rounds(rec, 2, label="cfg1")
+
+
+def test_cfg2_full():
+    """The benchmark workload: round 0 is the previous step, round 1 is timed."""
+    rec = wl.CONFIGS["cfg2"]
+    _, o, st = _rounds(rec, 2, label="cfg2")
+    assert o.stats.hot_hits > 0 and o.stats.misses > 0
+
+
+def _sampled(rec, slots, rounds=2, shared=True, k_max=None, opt_rows_max=None, kr=None,
+             residency=None):
+    run = _runner(rec, k_max=k_max, opt_rows_max=opt_rows_max)
+    o = build_oracle(rec, slots, k_max=k_max, opt_rows_max=opt_rows_max)
+    if residency is not None or rec.opt_frac > 0:
+        rows_of = residency or rec.residency_rows
+        run.set_residency(rows_of)
+        for r in slots:
+            o.set_residency(r, rows_of(r))
+    kr = rec.k_per_req() if kr is None else kr
+    for rnd in range(rounds):
+        acc = rec.accepted(rnd, kr)
+        run.load_round(rnd)
+        run.select(kr)
+        run.resolve(shared)
+        run.attend()
+        ores = oracle_round(o, rec, rnd, slots, kr, None, shared)
+        compare_round(run, o, ores, slots, kr, "%s round %d" % (rec.name, rnd))
+        run.commit(acc)
+        o.commit(acc)
+        compare_state(run, o, slots, "%s round %d" % (rec.name, rnd), full_host=False)
+    assert run.ctx.stats()["device_error"] == 0
+    return run, o
+
+
+def test_cfg3_full_sampled():
+    rec = wl.CONFIGS["cfg3"]
+    _sampled(rec, [0, 77, 127])
+
+
+def test_cfg4_full_sampled():
+    rec = wl.CONFIGS["cfg4"]
+    _sampled(rec, [5, 63])
