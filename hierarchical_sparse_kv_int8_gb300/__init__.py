@@ -84,6 +84,9 @@ _SIGS = {
     "dhs_round_host": ([ctypes.c_void_p] * 9, ctypes.c_int),
     "dhs_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "dhs_last_error": ([ctypes.c_void_p], ctypes.c_char_p),
+    "dhs_select_noalloc": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                            ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p],
+                           ctypes.c_int),
 }
 
 
@@ -137,6 +140,19 @@ def _stream(stream) -> Optional[int]:
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def select_noalloc(q_idx, keys, n_queries, n_rows, idx_row_bytes, topk, topk_out, stream=None):
+    """Indexer + top-k through dhs_select_noalloc, which allocates nothing.
+
+    For callers that cannot allocate device memory at the call (graph capture,
+    engines that own all device memory, decode loops that must not
+    synchronise); see include/dhs.h for the limits and the shared scratch.
+    """
+    rc = load().dhs_select_noalloc(_dptr(q_idx), _dptr(keys), n_queries, n_rows, idx_row_bytes,
+                                   topk, _dptr(topk_out), _stream(stream))
+    if rc:
+        raise DhsError(rc, "dhs_select_noalloc")
 
 
 def make_config(**kw) -> Config:

@@ -263,6 +263,33 @@ int dhs_round_host(dhs_ctx *ctx, const int8_t *q_idx, const int32_t *k_per_req, 
 
 const char *dhs_strerror(int code);
 
+/* Indexer scores and ordered top-k without allocating anything.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory at the moment they need a selection:
+ * code recording a CUDA graph (cudaMalloc is not allowed during stream
+ * capture), plug-ins inside an inference engine that owns every byte of
+ * device memory, and decode loops where cudaMalloc or cudaFree would
+ * synchronise the device.  It computes what dhs_select computes for one
+ * request whose queries all see the whole key array, with no context:
+ *   q_idx     device int8 [n_queries][idx_row_bytes], 16-byte aligned
+ *   keys      device int8 [n_rows][idx_row_bytes], 16-byte aligned
+ *   topk_out  device int32 [n_queries][topk]: rows by score descending,
+ *             ties to the lower row, padded with -1 when n_rows < topk
+ * Limits: 1 <= n_queries <= 8, 16 <= idx_row_bytes <= 1024 (a multiple of
+ * 16), topk a multiple of 32 up to 4096, and n_queries * n_rows <= 2^21
+ * (DHS_ERR_CAPACITY beyond it).  The intermediate scores live in one
+ * fixed 8 MiB array inside the library image, which every GPU that loads
+ * the library keeps until the process exits; no call allocates or frees
+ * memory.  The first call on a device looks up that array's device address
+ * (once per device, with the device current), so make the first call before
+ * any stream capture.  All calls share the array and it keeps the last
+ * call's contents: calls that overlap on the GPU race, so order them (for
+ * example on one stream). */
+int dhs_select_noalloc(const int8_t *q_idx, const int8_t *keys, int32_t n_queries,
+                       int64_t n_rows, int32_t idx_row_bytes, int32_t topk, int32_t *topk_out,
+                       dhs_stream stream);
+
 /* Text of the CUDA runtime error behind the context's last DHS_ERR_CUDA ("" if none). */
 const char *dhs_last_error(const dhs_ctx *ctx);
 
