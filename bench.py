@@ -252,8 +252,33 @@ def run_native(args):
         counts = run.export("counts", torch.int32, (rec.N, 4)).cpu().numpy()
         st_before = run.ctx.stats(stream)
 
+        # Eager (one C-ABI call at a time) step time, for reference.
+        ev0 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            run.ctx.restore(snap, stream)
+            flush.fill_(i & 0xFF)
+            ev0[i][0].record(stream)
+            step()
+            ev0[i][1].record(stream)
+        stream.synchronize()
+        eager_ms = float(np.mean([a.elapsed_time(b) for a, b in ev0]))
+
+        # The timed step is the same round captured once as a CUDA graph (the
+        # state is restored before every launch, so the round is identical).
         run.ctx.set_timing(True)
-        sampler = ClockSampler(local) if rank == 0 or True else None
+        run.ctx.restore(snap, stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+            step()
+        stream.synchronize()
+        run.ctx.set_timing(True)            # drop anything recorded during capture
+        for _ in range(args.warmup):
+            run.ctx.restore(snap, stream)
+            graph.replay()
+        stream.synchronize()
+        run.ctx.set_timing(True)
+        sampler = ClockSampler(local)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         barrier(world)
@@ -263,9 +288,10 @@ def run_native(args):
             run.ctx.restore(snap, stream)
             flush.fill_(i & 0xFF)
             ev[i][0].record(stream)
-            step()
+            graph.replay()
             ev[i][1].record(stream)
-        stream.synchronize()
+            stream.synchronize()
+            run.ctx.timing_accumulate_graph()
         clocks = sampler.stop()
         barrier(world)
         kt = run.ctx.kernel_times()
@@ -322,7 +348,9 @@ def run_native(args):
     breakdown = {k: {"launches": n, "avg_us": round(1e3 * t / n, 2),
                      "share": round(t / sum(v[1] for v in per.values()), 4)}
                  for k, (n, t) in per.items()}
-    launches_per_step = sum(n for n, _ in per.values()) / args.steps
+    # timed kernels plus the untimed ones: three control-word uploads and the
+    # min/max reset of the indexer
+    launches_per_step = sum(n for n, _ in per.values()) / args.steps + 4
     # upload launches are counted as ours too (control words for each call)
     line = {
         "metric": "verified query-tokens/s per layer (select+resolve+attend)",
@@ -340,6 +368,8 @@ def run_native(args):
                 "ms_per_step": round(e2e_ms, 5),
                 "api": "dhs_round_host (pinned host inputs and outputs)"},
         "gpu_launches": int(round(launches_per_step * args.steps)),
+        "eager_ms_per_step": round(eager_ms, 5),
+        "launch": "CUDA graph of one round (select, resolve, attend, commit), replayed per step",
         "roofline": roof,
         "kernels": breakdown,
         "workload_stats": {"union_rows": ab["union"], "misses": ab["misses"],

@@ -78,6 +78,7 @@ _SIGS = {
                          ctypes.c_int),
     "dhs_kernel_name": ([ctypes.c_int32], ctypes.c_char_p),
     "dhs_kernel_count": ([], ctypes.c_int32),
+    "dhs_timing_accumulate_graph": ([ctypes.c_void_p], ctypes.c_int),
     "dhs_snapshot": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p],
                      ctypes.c_int),
     "dhs_restore": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
@@ -257,6 +258,9 @@ class Context:
                     "dhs_kernel_times")
         return {self._lib.dhs_kernel_name(i).decode(): (int(launches[i]), float(ms[i]))
                 for i in range(n)}
+
+    def timing_accumulate_graph(self):
+        self._check(self._lib.dhs_timing_accumulate_graph(self.h), "dhs_timing_accumulate_graph")
 
     def snapshot(self, stream=None) -> int:
         sid = ctypes.c_int32()

@@ -29,20 +29,53 @@ cudaEvent_t Timer::take() {
   cudaEventCreate(&e);
   return e;
 }
+static bool stream_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return st == cudaStreamCaptureStatusActive;
+}
 void Timer::begin(int id, cudaStream_t s) {
   if (!enabled) return;
   open_id_ = id;
-  open_a_ = take();
-  cudaEventRecord(open_a_, s);
+  open_captured_ = stream_capturing(s);
+  if (open_captured_) {
+    cudaEventCreate(&open_a_);
+    cudaEventRecordWithFlags(open_a_, s, cudaEventRecordExternal);
+  } else {
+    open_a_ = take();
+    cudaEventRecord(open_a_, s);
+  }
 }
 void Timer::end(int id, cudaStream_t s) {
   if (!enabled || open_id_ != id || !open_a_) return;
-  cudaEvent_t b = take();
-  cudaEventRecord(b, s);
-  pending_.push_back({id, open_a_, b});
+  cudaEvent_t b = nullptr;
+  if (open_captured_) {
+    cudaEventCreate(&b);
+    cudaEventRecordWithFlags(b, s, cudaEventRecordExternal);
+    graph_pairs_.push_back({id, open_a_, b});
+  } else {
+    b = take();
+    cudaEventRecord(b, s);
+    pending_.push_back({id, open_a_, b});
+  }
   open_a_ = nullptr;
   open_id_ = -1;
   if (pending_.size() > 8192) drain(1024);
+}
+void Timer::accumulate_graph() {
+  for (auto &p : graph_pairs_) {
+    cudaEventSynchronize(p.b);
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+      launches_[p.id] += 1;
+      ms_[p.id] += ms;
+    } else {
+      cudaGetLastError();
+    }
+  }
 }
 void Timer::drain(size_t keep) {
   size_t n = pending_.size() > keep ? pending_.size() - keep : 0;
@@ -74,6 +107,10 @@ void Timer::reset() {
   }
 }
 Timer::~Timer() {
+  for (auto &p : graph_pairs_) {
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
   for (auto &p : pending_) {
     cudaEventDestroy(p.a);
     cudaEventDestroy(p.b);
@@ -300,9 +337,7 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   ALLOC(d.opt_list, N * (size_t)std::max<int64_t>(1, d.opt_max));
   ALLOC(d.opt_count, N);
   ALLOC(d.scores, N * d.Kmax * (size_t)d.Sm);
-  ALLOC(d.minmax, N * d.Kmax * 2);
   ALLOC(d.uni, N * KK);
-  ALLOC(d.uloc, N * KK);
   ALLOC(d.miss, N * KK);
   ALLOC(d.first_occ, N * KK);
   ALLOC(d.counts, N * 4);
@@ -311,8 +346,8 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   ALLOC(d.aux, N * 4);
   const size_t pf = attn_partial_floats(d, c->n_split);
   ALLOC(d.part_o, c->n_split > 1 ? pf : 1);
-  d.part_ml = nullptr;
   ALLOC(d.part_ml, c->n_split > 1 ? N * d.Kmax * d.Hq * c->n_split * 2 : 1);
+  ALLOC(d.ticket, N * d.Kmax * d.Hkv);
   ALLOC(d.stats, ST_COUNT);
   ALLOC(d.err, 2);
   ALLOC(c->rh_qidx, N * d.Kmax * d.idx_row);
@@ -337,6 +372,7 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   if (e == cudaSuccess) e = cudaMemset(d.stats, 0, ST_COUNT * 8);
   if (e == cudaSuccess) e = cudaMemset(d.err, 0, 8);
   if (e == cudaSuccess) e = cudaMemset(d.counts, 0, N * 16);
+  if (e == cudaSuccess) e = cudaMemset(d.ticket, 0, N * d.Kmax * d.Hkv * 4);
   if (e == cudaSuccess) e = cudaMemset(d.opt_count, 0, N * 8);
   if (e == cudaSuccess) e = cudaMemset(pool, 0, pool_rows * R * 2);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -604,6 +640,12 @@ int dhs_kernel_times(dhs_ctx *c, int32_t max_ids, int64_t *launches, double *tot
     launches[i] = l[i];
     total_ms[i] = ms[i];
   }
+  return DHS_OK;
+}
+
+int dhs_timing_accumulate_graph(dhs_ctx *c) {
+  if (!c) return DHS_ERR_INVALID;
+  c->timer.accumulate_graph();
   return DHS_OK;
 }
 

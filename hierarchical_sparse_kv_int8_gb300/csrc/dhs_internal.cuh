@@ -77,9 +77,7 @@ struct DevCtx {
 
   // scratch of one round
   int32_t *scores;      // [N][Kmax][Sm]
-  int32_t *minmax;      // [N][Kmax][2]
   int32_t *uni;         // [N][Kmax*k]
-  int32_t *uloc;        // [N][Kmax*k]
   int32_t *miss;        // [N][Kmax*k]
   int32_t *first_occ;   // [N][Kmax*k]
   int32_t *counts;      // [N][4]
@@ -87,8 +85,9 @@ struct DevCtx {
   int32_t *promo_dst;   // [N][B]
   int32_t *topk_last;   // [N][Kmax][k] selection seen by the last resolve
   int32_t *aux;         // [N][4]: a_r and n_old for commit
-  float *part_o;        // attention partials
-  float *part_ml;
+  float *part_o;        // attention partials [N][Kmax][Hq][n_split][dv]
+  float *part_ml;       // [N][Kmax][Hq][n_split][2]: max (log2 units), sum
+  int32_t *ticket;      // [N][Kmax][Hkv]: finished splits of each attention item
   unsigned long long *stats;  // counters, see StatIdx
   int32_t *err;               // [2]: code, site
 };
@@ -149,6 +148,8 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
 cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *block,
                           const int32_t *loc, uint16_t *out, float *lse, int n_split,
                           cudaStream_t s, class Timer *tm);
+cudaError_t launch_post_attend(const DevCtx &c, const uint16_t *block, cudaStream_t s,
+                               class Timer *tm);
 cudaError_t launch_commit(const DevCtx &c, cudaStream_t s, class Timer *tm);
 cudaError_t launch_residency(const DevCtx &c, int slot, int64_t old_count, int64_t new_count,
                              cudaStream_t s, class Timer *tm);
@@ -169,11 +170,17 @@ class Timer {
   void end(int id, cudaStream_t s);
   void collect(int64_t *launches, double *ms);  // synchronises pending events
   void reset();
+  // Event pairs recorded while the stream was being captured into a CUDA
+  // graph are external event-record nodes; after each launch of that graph,
+  // accumulate_graph() adds their durations to the totals.
+  void accumulate_graph();
   ~Timer();
 
  private:
   struct Pending { int id; cudaEvent_t a, b; };
   std::vector<Pending> pending_;
+  std::vector<Pending> graph_pairs_;
+  bool open_captured_ = false;
   std::vector<cudaEvent_t> pool_;
   int64_t launches_[K_COUNT] = {};
   double ms_[K_COUNT] = {};

@@ -1,0 +1,399 @@
+// Step 5 of the verification round: sparse attention over located rows.
+//
+// "Adaptive DHiSparse", eq. (1) and (5): query j of request r attends over its
+// own ordered selection S_{r,j}, read through the locations l_{r,j,i} of
+// eq. (11)-(12), and over the block rows n_r .. n_r + j of the tail.
+//
+// Split-KV flash decoding.  One CTA of four warps handles one split (a range
+// of the row list) of one (request, query, kv head) item.  Rows are gathered
+// by location into shared memory with 16-byte cp.async, three stages in
+// flight.  The query heads that share the kv head (padded to 16) form the M
+// side of bf16 mma.sync m16n8k16 tensor-core products with fp32 accumulation:
+// S = Q K^T over 16 rows at a time, online softmax in log2 units, O += P V.
+//   - GQA rows (128-dim heads): the four warps are independent, each takes
+//     every fourth 16-row tile of the split; their (m, l, O) are combined in
+//     shared memory at the end.
+//   - MLA latent rows (576-dim keys, 512-dim values): the four warps share
+//     each tile, each owning a quarter of the key dims (partial S summed in
+//     shared memory) and a quarter of the value dims.
+// Splits of one item are merged by the CTA that finishes last (a per-item
+// ticket taken with one atomic after the partial is written and fenced), so
+// no separate merge launch and no device-side waiting are needed.
+#include "dhs_internal.cuh"
+#include "ptx_util.cuh"
+
+#include <math_constants.h>
+
+namespace dhs {
+
+constexpr int kAttnStages = 3;
+constexpr int kTileRows = 16;
+constexpr int kAttnThreads = 128;
+
+bool attn_shape_supported(int dqk, int dv, int layout) {
+  if (layout == DHS_KV_SPLIT) return dqk == 128 && dv == 128;
+  return dqk == 576 && dv == 512;
+}
+
+template <int DQK, int DV>
+struct AttnShape {
+  static constexpr int NW = (DQK > 256) ? 4 : 1;  // warps sharing one row tile
+  static constexpr int SUB = 4 / NW;              // independent warp groups per CTA
+  static constexpr int KW = DQK / NW;             // key dims per warp
+  static constexpr int VW = DV / NW;              // value dims per warp
+  static constexpr int KS = KW / 16;              // k-steps per warp
+  static constexpr int VT = VW / 8;               // output n-tiles per warp
+  static_assert(KW % 16 == 0 && VW % 16 == 0, "dims per warp must be multiples of 16");
+};
+
+static int attn_rows_per_tile_group(const DevCtx &c) { return c.dqk > 256 ? 16 : 64; }
+
+// Splits per item, fixed at context creation: about two CTAs per SM over all
+// items, at least one 16-row tile per warp group.
+int attn_splits(const DevCtx &c, int active_queries) {
+  (void)active_queries;
+  const int rows = c.k + c.Kmax;
+  const int gran = attn_rows_per_tile_group(c);
+  const int target = 152 * 2;
+  const int items = c.N * c.Kmax * c.Hkv;
+  int ns = (target + items - 1) / items;
+  const int max_ns = (rows + gran - 1) / gran;
+  if (ns > max_ns) ns = max_ns;
+  if (ns < 1) ns = 1;
+  int chunk = (rows + ns - 1) / ns;
+  chunk = (chunk + gran - 1) / gran * gran;
+  return (rows + chunk - 1) / chunk;
+}
+
+static int attn_chunk(const DevCtx &c, int n_split) {
+  const int rows = c.k + c.Kmax;
+  const int gran = attn_rows_per_tile_group(c);
+  int chunk = (rows + n_split - 1) / n_split;
+  return (chunk + gran - 1) / gran * gran;
+}
+
+size_t attn_partial_floats(const DevCtx &c, int n_split) {
+  return (size_t)c.N * c.Kmax * c.Hq * n_split * c.dv;
+}
+
+template <int DQK, int DV>
+static size_t attn_smem_bytes(int row_elems, int n_split) {
+  using SH = AttnShape<DQK, DV>;
+  const size_t stride = (size_t)row_elems * 2 + 16;
+  const size_t stages = (size_t)SH::SUB * kAttnStages * kTileRows * stride;
+  const size_t epilogue = ((size_t)SH::SUB * 16 * DV + 2 * SH::SUB * 16 + 16 * n_split) * 4;
+  const size_t body = stages > epilogue ? stages : epilogue;
+  return body + (size_t)SH::SUB * kAttnStages * kTileRows * 4 + 2 * SH::NW * 32 * 8 * 4 + 64;
+}
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(kAttnThreads)
+k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restrict__ block,
+       const int32_t *__restrict__ loc, uint16_t *__restrict__ out, float *__restrict__ lse,
+       int n_split, int chunk, size_t body_bytes) {
+  using SH = AttnShape<DQK, DV>;
+  constexpr int NW = SH::NW, SUB = SH::SUB, KS = SH::KS, VT = SH::VT;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int sh_last;
+  const int split = blockIdx.x, j = blockIdx.y;
+  const int r = blockIdx.z / c.Hkv, kvh = blockIdx.z % c.Hkv;
+  if (j >= c.Kr[r]) return;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int grp = w / NW, wi = w % NW;  // warp group and warp within it
+  const int g = lane >> 2, t4 = lane & 3;
+  const int G = c.Hq / c.Hkv;
+  const int k = c.k;
+  const int total = k + j + 1;
+  const int e0 = split * chunk;
+  const int e1 = min(e0 + chunk, total);
+  const int rowb = c.row * 2;
+  const int stride = rowb + 16;  // 16 bytes of padding: ldmatrix rows fall in distinct banks
+  const int nv = rowb >> 4;
+  unsigned char *stage_base = smem + (size_t)grp * kAttnStages * kTileRows * stride;
+  int *vflag_all = reinterpret_cast<int *>(smem + body_bytes);
+  int *vflag = vflag_all + grp * kAttnStages * kTileRows;
+  float *red = reinterpret_cast<float *>(vflag_all + SUB * kAttnStages * kTileRows);
+  const int koff = (c.layout == DHS_KV_LATENT) ? 0 : kvh * DQK;
+  const int voff = (c.layout == DHS_KV_LATENT) ? 0 : c.Hkv * DQK + kvh * DV;
+  const int32_t *lrow = loc + ((size_t)r * c.Kmax + j) * k;
+  const uint16_t *brow = block + (size_t)r * c.Kmax * c.row;
+
+  // query fragments: rows of the A operand are the query heads of this kv head
+  uint32_t qa[KS][4];
+  {
+    const uint16_t *qb = q + (((size_t)r * c.Kmax + j) * c.Hq + (size_t)kvh * G) * DQK;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int col = wi * SH::KW + ks * 16 + 2 * t4;
+      const uint32_t *r0 = reinterpret_cast<const uint32_t *>(qb + (size_t)g * DQK + col);
+      const uint32_t *r1 = reinterpret_cast<const uint32_t *>(qb + (size_t)(g + 8) * DQK + col);
+      qa[ks][0] = g < G ? r0[0] : 0u;
+      qa[ks][1] = g + 8 < G ? r1[0] : 0u;
+      qa[ks][2] = g < G ? r0[4] : 0u;
+      qa[ks][3] = g + 8 < G ? r1[4] : 0u;
+    }
+  }
+
+  // this warp group's tiles: grp, grp + SUB, ...
+  const int ntiles_all = e1 > e0 ? (e1 - e0 + kTileRows - 1) / kTileRows : 0;
+  const int ntiles = ntiles_all > grp ? (ntiles_all - grp + SUB - 1) / SUB : 0;
+  const int gtid = wi * 32 + lane;  // thread index within the group
+  auto issue = [&](int it) {
+    if (it < ntiles) {
+      const int tile = grp + it * SUB;
+      unsigned char *st = stage_base + (size_t)(it % kAttnStages) * kTileRows * stride;
+      int *vf = vflag + (it % kAttnStages) * kTileRows;
+      for (int cid = gtid; cid < kTileRows * nv; cid += NW * 32) {
+        const int rr = cid / nv, v = cid - rr * nv;
+        const int e = e0 + tile * kTileRows + rr;
+        const uint16_t *src = nullptr;
+        if (e < e1) {
+          if (e < k) {
+            const int32_t l = lrow[e];
+            if (l >= 0) {
+              src = loc_row(c, r, l);
+              if (src == nullptr && v == 0) record_error(c.err, DC_LOC_RANGE, K_ATTN);
+            }
+          } else {
+            src = brow + (size_t)(e - k) * c.row;
+          }
+        }
+        cp_async_16_zfill(st + (size_t)rr * stride + v * 16,
+                          src ? (const void *)(src + v * 8) : (const void *)brow, src ? 16 : 0);
+        if (v == 0) vf[rr] = src != nullptr;
+      }
+    }
+    cp_async_commit();
+  };
+  auto group_sync = [&]() {
+    if (NW == 1) __syncwarp(); else __syncthreads();
+  };
+
+  float o[VT][4];
+#pragma unroll
+  for (int i = 0; i < VT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+
+#pragma unroll
+  for (int s = 0; s < kAttnStages - 1; ++s) issue(s);
+  for (int it = 0; it < ntiles; ++it) {
+    issue(it + kAttnStages - 1);
+    cp_async_wait_group<kAttnStages - 1>();
+    group_sync();
+    const unsigned char *st = stage_base + (size_t)(it % kAttnStages) * kTileRows * stride;
+    const int *vf = vflag + (it % kAttnStages) * kTileRows;
+
+    // S = Q K^T over this warp's key dims: two n-tiles of 8 rows
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int mi = lane >> 3, ri = lane & 7;
+      const unsigned char *rowp = st + (size_t)((mi >> 1) * 8 + ri) * stride;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int col = koff + wi * SH::KW + ks * 16 + (mi & 1) * 8;
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(b0, b1, b2, b3, rowp + col * 2);
+        mma_bf16_16816(s[0], qa[ks], b0, b1);
+        mma_bf16_16816(s[1], qa[ks], b2, b3);
+      }
+    }
+    if (NW > 1) {  // sum the key-dim partials of the group's warps, same order everywhere
+      float *my = red + ((size_t)((it & 1) * NW + wi) * 32 + lane) * 8;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) my[i] = s[i >> 2][i & 3];
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s[i >> 2][i & 3] = 0.f;
+      for (int ww = 0; ww < NW; ++ww) {
+        const float *src = red + ((size_t)((it & 1) * NW + ww) * 32 + lane) * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s[i >> 2][i & 3] += src[i];
+      }
+    }
+    // log2-domain logits, invalid rows masked
+    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int col = nt * 8 + 2 * t4 + (i & 1);
+        const float x = vf[col] ? s[nt][i] * c.scale_log2 : -CUDART_INF_F;
+        s[nt][i] = x;
+        if (i < 2) mx0 = fmaxf(mx0, x); else mx1 = fmaxf(mx1, x);
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float ref0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+    const float ref1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+    const float al0 = exp2f(m0 - ref0), al1 = exp2f(m1 - ref1);
+    m0 = mn0;
+    m1 = mn1;
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = exp2f(s[nt][0] - ref0);
+      s[nt][1] = exp2f(s[nt][1] - ref0);
+      s[nt][2] = exp2f(s[nt][2] - ref1);
+      s[nt][3] = exp2f(s[nt][3] - ref1);
+      ps0 += s[nt][0] + s[nt][1];
+      ps1 += s[nt][2] + s[nt][3];
+    }
+    l0 = l0 * al0 + ps0;
+    l1 = l1 * al1 + ps1;
+#pragma unroll
+    for (int i = 0; i < VT; ++i) {
+      o[i][0] *= al0;
+      o[i][1] *= al0;
+      o[i][2] *= al1;
+      o[i][3] *= al1;
+    }
+    uint32_t pa[4];
+    pa[0] = pack_bf16(s[0][0], s[0][1]);
+    pa[1] = pack_bf16(s[0][2], s[0][3]);
+    pa[2] = pack_bf16(s[1][0], s[1][1]);
+    pa[3] = pack_bf16(s[1][2], s[1][3]);
+    {
+      const int mi = lane >> 3, ri = lane & 7;
+      const unsigned char *rowp = st + (size_t)((mi & 1) * 8 + ri) * stride;
+#pragma unroll
+      for (int vt = 0; vt < VT / 2; ++vt) {
+        const int dim = voff + wi * SH::VW + vt * 16 + (mi >> 1) * 8;
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4_trans(b0, b1, b2, b3, rowp + dim * 2);
+        mma_bf16_16816(o[2 * vt], pa, b0, b1);
+        mma_bf16_16816(o[2 * vt + 1], pa, b2, b3);
+      }
+    }
+    group_sync();  // the stage is refilled by a later issue
+  }
+  cp_async_wait_all();
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+  // ---- combine the warp groups of this CTA (the stage area is reused)
+  __syncthreads();
+  float *Ob = reinterpret_cast<float *>(smem);  // [SUB][16][DV]
+  float *Mb = Ob + SUB * 16 * DV;               // [SUB][16]
+  float *Lb = Mb + SUB * 16;                    // [SUB][16]
+  float *Wt = Lb + SUB * 16;                    // [16][n_split]
+#pragma unroll
+  for (int i = 0; i < VT; ++i) {
+    const int dim = wi * SH::VW + i * 8 + 2 * t4;
+    Ob[(grp * 16 + g) * DV + dim] = o[i][0];
+    Ob[(grp * 16 + g) * DV + dim + 1] = o[i][1];
+    Ob[(grp * 16 + g + 8) * DV + dim] = o[i][2];
+    Ob[(grp * 16 + g + 8) * DV + dim + 1] = o[i][3];
+  }
+  if (wi == 0 && t4 == 0) {
+    Mb[grp * 16 + g] = m0;
+    Mb[grp * 16 + g + 8] = m1;
+    Lb[grp * 16 + g] = l0;
+    Lb[grp * 16 + g + 8] = l1;
+  }
+  __syncthreads();
+  const size_t qbase = ((size_t)r * c.Kmax + j) * c.Hq + (size_t)kvh * G;
+  const float ln2 = 0.69314718055994531f;
+  for (int idx = tid; idx < G * DV / 2; idx += kAttnThreads) {
+    const int h = (2 * idx) / DV, d = (2 * idx) % DV;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int sg = 0; sg < SUB; ++sg) M = fmaxf(M, Mb[sg * 16 + h]);
+    const float ref = M == -CUDART_INF_F ? 0.f : M;
+    float L = 0.f, a = 0.f, b = 0.f;
+#pragma unroll
+    for (int sg = 0; sg < SUB; ++sg) {
+      const float wgt = exp2f(Mb[sg * 16 + h] - ref);
+      L += wgt * Lb[sg * 16 + h];
+      a += wgt * Ob[(sg * 16 + h) * DV + d];
+      b += wgt * Ob[(sg * 16 + h) * DV + d + 1];
+    }
+    if (n_split == 1) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      *reinterpret_cast<uint32_t *>(out + (qbase + h) * DV + d) = pack_bf16(a * inv, b * inv);
+      if (lse && d == 0) lse[qbase + h] = L > 0.f ? (M + log2f(L)) * ln2 : -CUDART_INF_F;
+    } else {
+      float *po = c.part_o + ((qbase + h) * n_split + split) * DV + d;
+      po[0] = a;
+      po[1] = b;
+      if (d == 0) {
+        c.part_ml[((qbase + h) * n_split + split) * 2 + 0] = M;
+        c.part_ml[((qbase + h) * n_split + split) * 2 + 1] = L;
+      }
+    }
+  }
+  if (n_split == 1) return;
+
+  // ---- the CTA that finishes an item last merges its splits
+  const int item = ((r * c.Kmax + j) * c.Hkv) + kvh;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh_last = atomicAdd(&c.ticket[item], 1) == n_split - 1;
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  for (int h = tid; h < G; h += kAttnThreads) {
+    const float *ml = c.part_ml + (qbase + h) * n_split * 2;
+    float M = -CUDART_INF_F;
+    for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, __ldcg(ml + 2 * sp));
+    const float ref = M == -CUDART_INF_F ? 0.f : M;
+    float L = 0.f;
+    for (int sp = 0; sp < n_split; ++sp) L += __ldcg(ml + 2 * sp + 1) * exp2f(__ldcg(ml + 2 * sp) - ref);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int sp = 0; sp < n_split; ++sp) Wt[h * n_split + sp] = exp2f(__ldcg(ml + 2 * sp) - ref) * inv;
+    if (lse) lse[qbase + h] = L > 0.f ? (M + log2f(L)) * ln2 : -CUDART_INF_F;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * DV / 2; idx += kAttnThreads) {
+    const int h = (2 * idx) / DV, d = (2 * idx) % DV;
+    const float *po = c.part_o + (qbase + h) * n_split * DV + d;
+    float a = 0.f, b = 0.f;
+#pragma unroll 4
+    for (int sp = 0; sp < n_split; ++sp) {
+      const float2 v = __ldcg(reinterpret_cast<const float2 *>(po + (size_t)sp * DV));
+      const float wgt = Wt[h * n_split + sp];
+      a += wgt * v.x;
+      b += wgt * v.y;
+    }
+    *reinterpret_cast<uint32_t *>(out + (qbase + h) * DV + d) = pack_bf16(a, b);
+  }
+  if (tid == 0) c.ticket[item] = 0;  // ready for the next launch
+}
+
+template <int DQK, int DV>
+static cudaError_t launch_attn_t(const DevCtx &c, const uint16_t *q, const uint16_t *block,
+                                 const int32_t *loc, uint16_t *out, float *lse, int n_split,
+                                 cudaStream_t s, Timer *tm) {
+  using SH = AttnShape<DQK, DV>;
+  const size_t stride = (size_t)c.row * 2 + 16;
+  const size_t stages = (size_t)SH::SUB * kAttnStages * kTileRows * stride;
+  const size_t epi = ((size_t)SH::SUB * 16 * DV + 2 * SH::SUB * 16 + 16 * (size_t)n_split) * 4;
+  const size_t body = ((stages > epi ? stages : epi) + 127) / 128 * 128;
+  const size_t smem = attn_smem_bytes<DQK, DV>(c.row, n_split) + 128;
+  static size_t granted = 0;
+  cudaError_t e = ensure_smem(k_attn<DQK, DV>, smem, granted);
+  if (e != cudaSuccess) return e;
+  dim3 grid(n_split, c.Kmax, c.N * c.Hkv);
+  if (tm) tm->begin(K_ATTN, s);
+  k_attn<DQK, DV><<<grid, kAttnThreads, smem, s>>>(c, q, block, loc, out, lse, n_split,
+                                                     attn_chunk(c, n_split), body);
+  if (tm) tm->end(K_ATTN, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *block,
+                          const int32_t *loc, uint16_t *out, float *lse, int n_split,
+                          cudaStream_t s, Timer *tm) {
+  cudaError_t e = (c.dqk == 128 && c.dv == 128)
+                      ? launch_attn_t<128, 128>(c, q, block, loc, out, lse, n_split, s, tm)
+                      : launch_attn_t<576, 512>(c, q, block, loc, out, lse, n_split, s, tm);
+  if (e != cudaSuccess) return e;
+  return launch_post_attend(c, block, s, tm);
+}
+
+}  // namespace dhs

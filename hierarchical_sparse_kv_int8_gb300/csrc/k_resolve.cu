@@ -49,19 +49,22 @@ __device__ __forceinline__ int ublock_excl_scan(int v, int *warp_sums, int &tota
 size_t union_smem_bytes(const DevCtx &c) {
   const size_t nw = (size_t)((c.Sm + 31) / 32);
   const size_t pw = (size_t)((c.B + 31) / 32);
-  return nw * 8 + pw * 4 + (size_t)c.B * 8;
+  return nw * 8 + pw * 4 + (size_t)c.B * 8 + (size_t)c.Kmax * c.k * 4;
 }
 
 constexpr int32_t kMissMark = -2;
+constexpr int kBatch = 8;  // independent global loads in flight per thread
 
-// One CTA per request.
+// One CTA per request.  Shared memory holds the union bitmap over the
+// history, the per-word prefix counts, the protected-slot bitmap, two B-entry
+// slot lists and the location of every union row.
 __global__ void __launch_bounds__(kUnionThreads)
 k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restrict__ loc_out,
               int shared, int tick) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
   __shared__ int sh_cnt[4];  // ring, opt, hot hits; selections
-  __shared__ int sh_missel;
+  __shared__ int sh_missel, sh_evict;
   const int r = blockIdx.x;
   const int Kr = c.Kr[r];
   if (Kr == 0) return;
@@ -76,10 +79,10 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   uint32_t *prot = wp + nw_cap;
   int32_t *candB = reinterpret_cast<int32_t *>(prot + pw);
   int32_t *tmpB = candB + B;
+  int32_t *ul = tmpB + B;  // location of union row q
 
   const int32_t *tk = topk + (size_t)r * KK;
   int32_t *uni = c.uni + (size_t)r * KK;
-  int32_t *uloc = c.uloc + (size_t)r * KK;
   int32_t *miss = c.miss + (size_t)r * KK;
   int32_t *hot_row = c.hot_row + (size_t)r * B;
   int32_t *hot_stamp = c.hot_stamp + (size_t)r * B;
@@ -87,19 +90,29 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   int32_t *hot_map = c.hot_map + (size_t)r * c.Sm;
   const int32_t *opt_map = c.opt_map + (size_t)r * c.Sm;
   const int64_t ring_lo = max(c.ring_first[r], n - (int64_t)c.W);
+  const int nsel = Kr * k;
 
   // 1. union bitmap over the history rows
   for (int i = tid; i < nw; i += bs) bm[i] = 0;
   for (int i = tid; i < pw; i += bs) prot[i] = 0;
   if (tid < 4) sh_cnt[tid] = 0;
-  if (tid == 0) sh_missel = 0;
+  if (tid == 0) {
+    sh_missel = 0;
+    sh_evict = 0;
+  }
   __syncthreads();
-  for (int e = tid; e < Kr * k; e += bs) {
-    const int32_t s = tk[e];
-    if (s >= 0 && s < n) {
-      atomicOr(&bm[s >> 5], 1u << (s & 31));
-    } else if (s != -1) {
-      record_error(c.err, DC_ROW_RANGE, K_UNION_PROBE);
+  for (int e0 = tid; e0 < nsel; e0 += kBatch * bs) {
+    int32_t sv[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int e = e0 + i * bs;
+      sv[i] = e < nsel ? tk[e] : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int32_t s = sv[i];
+      if (s >= 0 && s < n) atomicOr(&bm[s >> 5], 1u << (s & 31));
+      else if (s != -1) record_error(c.err, DC_ROW_RANGE, K_UNION_PROBE);
     }
   }
   __syncthreads();
@@ -112,38 +125,67 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   int U;
   const int u_base = ublock_excl_scan(cnt, warp_sums, U);
 
-  // 3. probe each union row: live ring tail, optional map, hot cache, miss
+  // 3. probe each union row: live ring tail, optional map, hot cache, else miss
   int misses_here = 0, ring_h = 0, opt_h = 0, hot_h = 0;
   {
     int q = u_base;
-    for (int w = w0; w < w1; ++w) {
+    int w = w0;
+    uint32_t bits = 0;
+    if (w < w1) {
       wp[w] = q;
-      uint32_t bits = bm[w];
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1;
-        const int32_t u = (w << 5) | b;
-        uni[q] = u;
-        const int32_t hs = hot_map[u];
+      bits = bm[w];
+    }
+    for (;;) {
+      int32_t ub[kBatch];
+      int nb = 0;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        while (bits == 0 && w < w1) {
+          if (++w < w1) {
+            wp[w] = q + i;
+            bits = bm[w];
+          }
+        }
+        if (bits) {
+          ub[i] = (w << 5) | (__ffs(bits) - 1);
+          bits &= bits - 1;
+          nb = i + 1;
+        } else {
+          ub[i] = -1;
+        }
+      }
+      int32_t hm[kBatch], om[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        hm[i] = ub[i] >= 0 ? hot_map[ub[i]] : -1;
+        om[i] = ub[i] >= 0 ? opt_map[ub[i]] : -1;
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int32_t u = ub[i];
+        if (u < 0) continue;
+        const int32_t hs = hm[i];
         if (hs >= 0) atomicOr(&prot[hs >> 5], 1u << (hs & 31));  // selected rows are protected
         int32_t l;
         if (u >= ring_lo && u < n) {
           l = make_loc(DHS_LOC_RING, (int)(u % c.Rd));
           ++ring_h;
-        } else if (opt_map[u] >= 0) {
-          l = make_loc(DHS_LOC_OPT, opt_map[u]);
+        } else if (om[i] >= 0) {
+          l = make_loc(DHS_LOC_OPT, om[i]);
           ++opt_h;
         } else if (hs >= 0) {
           l = make_loc(DHS_LOC_HOT, hs);
           hot_stamp[hs] = tick;
           ++hot_h;
         } else {
-          l = kMissMark;
+          l = kMissMark - u;  // a miss, row kept until its rank is known
           ++misses_here;
         }
-        uloc[q] = l;
+        uni[q] = u;
+        ul[q] = l;
         ++q;
       }
+      if (nb < kBatch) break;
     }
   }
   atomicAdd(&sh_cnt[0], ring_h);
@@ -154,9 +196,10 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   if (misses_here) {
     int m = m_base;
     for (int q = u_base; q < u_base + cnt; ++q) {
-      if (uloc[q] == kMissMark) {
-        uloc[q] = make_loc(DHS_LOC_STAGE, m);
-        miss[m] = uni[q];
+      const int32_t l = ul[q];
+      if (l <= kMissMark) {
+        miss[m] = kMissMark - l;
+        ul[q] = make_loc(DHS_LOC_STAGE, m);
         ++m;
       }
     }
@@ -165,12 +208,13 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   __syncthreads();
   const int hits = sh_cnt[2];
 
-  // 4. victims: unprotected slots in LRU order (stamp, slot), empty first
+  // 4. victims: unprotected slots in LRU order (stamp, slot), empty slots first
   int P = 0;
   const int perB = (B + bs - 1) / bs;
   const int b0 = min(B, tid * perB), b1 = min(B, b0 + perB);
   if (M > 0) {
     int nc = 0;
+#pragma unroll 4
     for (int i = b0; i < b1; ++i) {
       const int v = lru[i];
       nc += !((prot[v >> 5] >> (v & 31)) & 1u);
@@ -184,64 +228,88 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
     __syncthreads();
     P = min(M, ncand);
     int ev = 0;
-    for (int p = tid; p < P; p += bs) {
-      const int v = candB[p];
-      const int32_t old = hot_row[v];
-      if (old >= 0) {
-        hot_map[old] = -1;
-        ++ev;
+    for (int p0 = tid; p0 < P; p0 += kBatch * bs) {
+      int vv[kBatch], old[kBatch], uu[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int p = p0 + i * bs;
+        vv[i] = p < P ? candB[p] : -1;
+        old[i] = vv[i] >= 0 ? hot_row[vv[i]] : -1;
+        uu[i] = p < P ? miss[p] : -1;
       }
-      const int32_t u = miss[p];
-      hot_row[v] = u;
-      hot_stamp[v] = tick;
-      hot_map[u] = v;
-      c.promo_dst[(size_t)r * B + p] = v;
-      c.promo_src[(size_t)r * B + p] = p;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int p = p0 + i * bs;
+        if (vv[i] < 0) continue;
+        if (old[i] >= 0) {
+          hot_map[old[i]] = -1;
+          ++ev;
+        }
+        hot_row[vv[i]] = uu[i];
+        hot_stamp[vv[i]] = tick;
+        hot_map[uu[i]] = vv[i];
+        c.promo_dst[(size_t)r * B + p] = vv[i];
+        c.promo_src[(size_t)r * B + p] = p;
+      }
     }
-    if (ev) atomicAdd(&c.stats[ST_EVICT], (unsigned long long)ev);
+    if (ev) atomicAdd(&sh_evict, ev);
     __syncthreads();
   }
 
   // 5. LRU order after this tick: untouched slots keep their order, slots
   //    stamped now follow in ascending slot order
   if (hits + P > 0) {
-    int na = 0;
-    for (int i = b0; i < b1; ++i) na += hot_stamp[lru[i]] != tick;
-    int A;
-    int ab = ublock_excl_scan(na, warp_sums, A);
-    int nb = 0;
-    for (int v = b0; v < b1; ++v) nb += hot_stamp[v] == tick;
-    int Bt;
-    int bb = ublock_excl_scan(nb, warp_sums, Bt);
+    int na = 0, nb = 0;
+#pragma unroll 4
     for (int i = b0; i < b1; ++i) {
       const int v = lru[i];
-      if (hot_stamp[v] != tick) tmpB[ab++] = v;
+      const bool now = hot_stamp[v] == tick;
+      na += !now;
+      tmpB[i] = now ? -1 : v;  // scratch: this thread's positions only
     }
+#pragma unroll 4
+    for (int v = b0; v < b1; ++v) nb += hot_stamp[v] == tick;
+    int A, Bt;
+    int ab = ublock_excl_scan(na, warp_sums, A);
+    int bb = ublock_excl_scan(nb, warp_sums, Bt);
+    for (int i = b0; i < b1; ++i)
+      if (tmpB[i] >= 0) candB[ab++] = tmpB[i];
     for (int v = b0; v < b1; ++v)
-      if (hot_stamp[v] == tick) tmpB[A + bb++] = v;
+      if (hot_stamp[v] == tick) candB[A + bb++] = v;
     __syncthreads();
-    for (int i = tid; i < B; i += bs) lru[i] = tmpB[i];
+    for (int i = tid; i < B; i += bs) lru[i] = candB[i];
   }
 
   // 6. one location per selected entry, in each query's selection order
   int sel_here = 0, missel = 0;
-  for (int e = tid; e < Kr * k; e += bs) {
-    const int32_t s = tk[e];
-    int32_t l = -1;
-    if (s >= 0 && s < n) {
-      const uint32_t word = bm[s >> 5];
-      const int q = wp[s >> 5] + __popc(word & ((1u << (s & 31)) - 1u));
-      l = uloc[q];
-      ++sel_here;
-      if (loc_tier(l) == DHS_LOC_STAGE) {
-        ++missel;
-        if (!shared) {
-          atomicMin(&c.first_occ[(size_t)r * KK + loc_index(l)], e);
-          l = make_loc(DHS_LOC_STAGE, e);
+  for (int e0 = tid; e0 < nsel; e0 += kBatch * bs) {
+    int32_t sv[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int e = e0 + i * bs;
+      sv[i] = e < nsel ? tk[e] : -2;
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int e = e0 + i * bs;
+      const int32_t s = sv[i];
+      if (s == -2) continue;
+      int32_t l = -1;
+      if (s >= 0 && s < n) {
+        const uint32_t word = bm[s >> 5];
+        const int q = wp[s >> 5] + __popc(word & ((1u << (s & 31)) - 1u));
+        l = ul[q];
+        ++sel_here;
+        if (loc_tier(l) == DHS_LOC_STAGE) {
+          ++missel;
+          if (!shared) {
+            atomicMin(&c.first_occ[(size_t)r * KK + loc_index(l)], e);
+            l = make_loc(DHS_LOC_STAGE, e);
+          }
         }
       }
+      loc_out[(size_t)r * KK + e] = l;
     }
-    loc_out[(size_t)r * KK + e] = l;
   }
   atomicAdd(&sh_cnt[3], sel_here);
   atomicAdd(&sh_missel, missel);
@@ -264,6 +332,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
     atomicAdd(&c.stats[ST_MISS_SEL], (unsigned long long)sh_missel);
     atomicAdd(&c.stats[ST_FETCHED], (unsigned long long)(shared ? M : sh_missel));
     atomicAdd(&c.stats[ST_INSTALL], (unsigned long long)P);
+    if (sh_evict) atomicAdd(&c.stats[ST_EVICT], (unsigned long long)sh_evict);
     if (M == 0 && hits == 0) atomicAdd(&c.stats[ST_DIRECT], 1ull);
   }
 }

@@ -243,6 +243,12 @@ int dhs_export(dhs_ctx *ctx, int32_t which, void *dst, int64_t bytes, dhs_stream
  * the last reset.  Kernel ids and names: dhs_kernel_name(id). */
 int dhs_set_timing(dhs_ctx *ctx, int32_t enable);
 int dhs_kernel_times(dhs_ctx *ctx, int32_t max_ids, int64_t *launches, double *total_ms);
+
+/* Calls made while `stream` is being captured into a CUDA graph (with timing
+ * enabled) record their kernel events as event-record nodes of the graph.
+ * After each launch of such a graph, this call waits for those events and
+ * adds the kernel durations to the totals dhs_kernel_times reports. */
+int dhs_timing_accumulate_graph(dhs_ctx *ctx);
 const char *dhs_kernel_name(int32_t id);
 int32_t dhs_kernel_count(void);
 
