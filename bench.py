@@ -266,18 +266,20 @@ def run_native(args):
 
         # The timed step is the same round captured once as a CUDA graph (the
         # state is restored before every launch, so the round is identical).
-        run.ctx.set_timing(True)
-        run.ctx.restore(snap, stream)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
-            step()
-        stream.synchronize()
-        run.ctx.set_timing(True)            # drop anything recorded during capture
+        def capture(timing):
+            run.ctx.set_timing(timing)
+            run.ctx.restore(snap, stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                step()
+            stream.synchronize()
+            return g
+        graph = capture(False)
+        graph_timed = capture(True)
         for _ in range(args.warmup):
             run.ctx.restore(snap, stream)
             graph.replay()
         stream.synchronize()
-        run.ctx.set_timing(True)
         sampler = ClockSampler(local)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
@@ -290,10 +292,18 @@ def run_native(args):
             ev[i][0].record(stream)
             graph.replay()
             ev[i][1].record(stream)
-            stream.synchronize()
-            run.ctx.timing_accumulate_graph()
+        stream.synchronize()
         clocks = sampler.stop()
         barrier(world)
+        # per-kernel durations: the same steps, replayed from the graph that
+        # carries an event pair around every kernel
+        run.ctx.set_timing(True)
+        for i in range(args.steps):
+            run.ctx.restore(snap, stream)
+            flush.fill_(i & 0xFF)
+            graph_timed.replay()
+            stream.synchronize()
+            run.ctx.timing_accumulate_graph()
         kt = run.ctx.kernel_times()
         run.ctx.set_timing(False)
         ms_steps = [a.elapsed_time(b) for a, b in ev]
@@ -348,9 +358,8 @@ def run_native(args):
     breakdown = {k: {"launches": n, "avg_us": round(1e3 * t / n, 2),
                      "share": round(t / sum(v[1] for v in per.values()), 4)}
                  for k, (n, t) in per.items()}
-    # timed kernels plus the untimed ones: three control-word uploads and the
-    # min/max reset of the indexer
-    launches_per_step = sum(n for n, _ in per.values()) / args.steps + 4
+    # timed kernels plus the untimed one that writes select's control words
+    launches_per_step = sum(n for n, _ in per.values()) / args.steps + 1
     # upload launches are counted as ours too (control words for each call)
     line = {
         "metric": "verified query-tokens/s per layer (select+resolve+attend)",
@@ -369,7 +378,8 @@ def run_native(args):
                 "api": "dhs_round_host (pinned host inputs and outputs)"},
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "eager_ms_per_step": round(eager_ms, 5),
-        "launch": "CUDA graph of one round (select, resolve, attend, commit), replayed per step",
+        "launch": "CUDA graph of one round (select, resolve, attend, commit), replayed per step; "
+                  "kernel times from a second replay of the same steps with per-kernel events",
         "roofline": roof,
         "kernels": breakdown,
         "workload_stats": {"union_rows": ab["union"], "misses": ab["misses"],

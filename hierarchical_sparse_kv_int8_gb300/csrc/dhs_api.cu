@@ -337,13 +337,13 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   ALLOC(d.opt_list, N * (size_t)std::max<int64_t>(1, d.opt_max));
   ALLOC(d.opt_count, N);
   ALLOC(d.scores, N * d.Kmax * (size_t)d.Sm);
+  ALLOC(d.minmax, N * d.Kmax * 2);
   ALLOC(d.uni, N * KK);
   ALLOC(d.miss, N * KK);
   ALLOC(d.first_occ, N * KK);
   ALLOC(d.counts, N * 4);
   ALLOC(d.promo_src, N * B);
   ALLOC(d.promo_dst, N * B);
-  ALLOC(d.aux, N * 4);
   const size_t pf = attn_partial_floats(d, c->n_split);
   ALLOC(d.part_o, c->n_split > 1 ? pf : 1);
   ALLOC(d.part_ml, c->n_split > 1 ? N * d.Kmax * d.Hq * c->n_split * 2 : 1);
@@ -446,7 +446,7 @@ int dhs_select(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const 
   if (c->phase != PH_IDLE) return DHS_ERR_INVALID;
   const DevCtx &d = c->d;
   std::vector<int32_t> w(d.N + d.N * d.Kmax, 0);
-  int max_dom = 0, active = 0;
+  int max_dom = 0;
   for (int r = 0; r < d.N; ++r) {
     const int kr = k_per_req[r];
     if (kr < 0 || kr > d.Kmax || (kr > 0 && !c->bound[r])) return DHS_ERR_INVALID;
@@ -454,7 +454,6 @@ int dhs_select(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const 
   for (int r = 0; r < d.N; ++r) {
     const int kr = k_per_req[r];
     w[r] = kr;
-    active += kr;
     for (int j = 0; j < kr; ++j) {
       int64_t p = pos ? pos[(size_t)r * d.Kmax + j] : c->n[r] + j;
       int64_t dom = std::max<int64_t>(0, std::min<int64_t>(c->n[r], p + 1));
@@ -463,12 +462,8 @@ int dhs_select(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const 
     }
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // Kr and dom are consecutive in one upload when they are adjacent in memory;
-  // they are separate allocations, so upload twice.
-  std::vector<int32_t> wk(w.begin(), w.begin() + d.N), wd(w.begin() + d.N, w.end());
-  if (upload_words(c, d.Kr, wk, s) || upload_words(c, d.dom, wd, s)) return DHS_ERR_CUDA;
   {
-    cudaError_t e_ = launch_select(d, q_idx, topk_out, max_dom, active, s, &c->timer);
+    cudaError_t e_ = launch_select(d, q_idx, topk_out, max_dom, w.data(), s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
   }
   for (int r = 0; r < d.N; ++r) c->K[r] = k_per_req[r];
@@ -527,9 +522,8 @@ int dhs_commit(dhs_ctx *c, const int32_t *accepted_len, dhs_stream stream) {
     w[r * 4 + 3] = c->K[r] ? 1 : 0;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (upload_words(c, d.aux, w, s)) return DHS_ERR_CUDA;
   {
-    cudaError_t e_ = launch_commit(d, s, &c->timer);
+    cudaError_t e_ = launch_commit(d, w.data(), s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
   }
   for (int r = 0; r < d.N; ++r) {

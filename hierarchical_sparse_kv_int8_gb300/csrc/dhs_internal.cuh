@@ -13,7 +13,7 @@ namespace dhs {
 
 constexpr int kMaxSlots = 256;
 constexpr int kMaxKmax = 8;
-constexpr int kMaxTopk = 4096;
+constexpr int kMaxTopk = 2048;
 constexpr int kUploadWords = 4096;  // int32 words carried by one k_upload launch
 
 // Kernel ids (per-kernel timing and device error sites).
@@ -77,6 +77,7 @@ struct DevCtx {
 
   // scratch of one round
   int32_t *scores;      // [N][Kmax][Sm]
+  int32_t *minmax;      // [N][Kmax][2]: range of each query's scores
   int32_t *uni;         // [N][Kmax*k]
   int32_t *miss;        // [N][Kmax*k]
   int32_t *first_occ;   // [N][Kmax*k]
@@ -84,7 +85,6 @@ struct DevCtx {
   int32_t *promo_src;   // [N][B]
   int32_t *promo_dst;   // [N][B]
   int32_t *topk_last;   // [N][Kmax][k] selection seen by the last resolve
-  int32_t *aux;         // [N][4]: a_r and n_old for commit
   float *part_o;        // attention partials [N][Kmax][Hq][n_split][dv]
   float *part_ml;       // [N][Kmax][Hq][n_split][2]: max (log2 units), sum
   int32_t *ticket;      // [N][Kmax][Hkv]: finished splits of each attention item
@@ -142,7 +142,7 @@ struct UploadWords {
 // ---- launchers (each returns the cudaGetLastError of its launch) -------
 cudaError_t launch_upload(int32_t *dst, const int32_t *words, int n, cudaStream_t s);
 cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_out,
-                          int max_dom, int active, cudaStream_t s, class Timer *tm);
+                          int max_dom, const int32_t *ctl_words, cudaStream_t s, class Timer *tm);
 cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_out,
                            int shared, int tick, cudaStream_t s, class Timer *tm);
 cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *block,
@@ -150,7 +150,8 @@ cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *bl
                           cudaStream_t s, class Timer *tm);
 cudaError_t launch_post_attend(const DevCtx &c, const uint16_t *block, cudaStream_t s,
                                class Timer *tm);
-cudaError_t launch_commit(const DevCtx &c, cudaStream_t s, class Timer *tm);
+cudaError_t launch_commit(const DevCtx &c, const int32_t *aux_words, cudaStream_t s,
+                          class Timer *tm);
 cudaError_t launch_residency(const DevCtx &c, int slot, int64_t old_count, int64_t new_count,
                              cudaStream_t s, class Timer *tm);
 cudaError_t launch_bind_reset(const DevCtx &c, int slot, int64_t n_committed, cudaStream_t s,

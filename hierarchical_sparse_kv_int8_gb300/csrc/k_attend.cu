@@ -60,10 +60,10 @@ cudaError_t launch_post_attend(const DevCtx &c, const uint16_t *block, cudaStrea
 
 // ---------------------------------------------------------------- commit
 // aux[r*4 + 0] = a_r, aux[r*4 + 1..2] = n_r before the commit (lo, hi words).
-__global__ void __launch_bounds__(256) k_commit(const DevCtx c) {
+__global__ void __launch_bounds__(256) k_commit(const DevCtx c, const __grid_constant__ UploadWords aux) {
   const int r = blockIdx.y;
-  const int a = c.aux[r * 4 + 0];
-  const int64_t n_old = (int64_t)(uint32_t)c.aux[r * 4 + 1] | ((int64_t)c.aux[r * 4 + 2] << 32);
+  const int a = aux.w[r * 4 + 0];
+  const int64_t n_old = (int64_t)(uint32_t)aux.w[r * 4 + 1] | ((int64_t)aux.w[r * 4 + 2] << 32);
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), nwt = gridDim.x * 8;
   const int nv = (c.row * 2) >> 4;
@@ -74,15 +74,17 @@ __global__ void __launch_bounds__(256) k_commit(const DevCtx c) {
     uint4 *dst = reinterpret_cast<uint4 *>(host + (size_t)(n_old + u) * c.row);
     for (int v = lane; v < nv; v += 32) dst[v] = src[v];
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0 && c.aux[r * 4 + 3]) {
+  if (blockIdx.x == 0 && threadIdx.x == 0 && aux.w[r * 4 + 3]) {
     c.n[r] = n_old + a;
     c.Kr[r] = 0;
   }
 }
 
-cudaError_t launch_commit(const DevCtx &c, cudaStream_t s, Timer *tm) {
+cudaError_t launch_commit(const DevCtx &c, const int32_t *aux_words, cudaStream_t s, Timer *tm) {
+  UploadWords aux;
+  for (int i = 0; i < c.N * 4; ++i) aux.w[i] = aux_words[i];
   if (tm) tm->begin(K_COMMIT, s);
-  k_commit<<<dim3(1, c.N), 256, 0, s>>>(c);
+  k_commit<<<dim3(1, c.N), 256, 0, s>>>(c, aux);
   if (tm) tm->end(K_COMMIT, s);
   return cudaGetLastError();
 }

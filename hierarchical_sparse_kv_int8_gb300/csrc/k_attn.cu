@@ -86,11 +86,14 @@ static size_t attn_smem_bytes(int row_elems, int n_split) {
   return body + (size_t)SH::SUB * kAttnStages * kTileRows * 4 + 2 * SH::NW * 32 * 8 * 4 + 64;
 }
 
+// Locations of one split, prefetched once into shared memory.
+static size_t attn_loc_bytes(int chunk) { return ((size_t)chunk * 4 + 127) / 128 * 128; }
+
 template <int DQK, int DV>
 __global__ void __launch_bounds__(kAttnThreads)
 k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restrict__ block,
        const int32_t *__restrict__ loc, uint16_t *__restrict__ out, float *__restrict__ lse,
-       int n_split, int chunk, size_t body_bytes) {
+       int n_split, int chunk, size_t body_bytes, size_t loc_off) {
   using SH = AttnShape<DQK, DV>;
   constexpr int NW = SH::NW, SUB = SH::SUB, KS = SH::KS, VT = SH::VT;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -113,6 +116,7 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   int *vflag_all = reinterpret_cast<int *>(smem + body_bytes);
   int *vflag = vflag_all + grp * kAttnStages * kTileRows;
   float *red = reinterpret_cast<float *>(vflag_all + SUB * kAttnStages * kTileRows);
+  int32_t *lsm = reinterpret_cast<int32_t *>(smem + body_bytes + loc_off);
   const int koff = (c.layout == DHS_KV_LATENT) ? 0 : kvh * DQK;
   const int voff = (c.layout == DHS_KV_LATENT) ? 0 : c.Hkv * DQK + kvh * DV;
   const int32_t *lrow = loc + ((size_t)r * c.Kmax + j) * k;
@@ -134,33 +138,46 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
     }
   }
 
+  // locations of this split's selected rows, read once (coalesced)
+  for (int e = e0 + tid; e < min(e1, k); e += kAttnThreads) lsm[e - e0] = lrow[e];
+  __syncthreads();
+
   // this warp group's tiles: grp, grp + SUB, ...
   const int ntiles_all = e1 > e0 ? (e1 - e0 + kTileRows - 1) / kTileRows : 0;
   const int ntiles = ntiles_all > grp ? (ntiles_all - grp + SUB - 1) / SUB : 0;
   const int gtid = wi * 32 + lane;  // thread index within the group
+  // Copy one 16-row tile into its stage.  Lanes 0..15 of every warp decode
+  // one row's source address (location tag, bounds check) and the group's
+  // threads then copy the rows chunk by chunk, the address broadcast by shuffle.
   auto issue = [&](int it) {
     if (it < ntiles) {
       const int tile = grp + it * SUB;
       unsigned char *st = stage_base + (size_t)(it % kAttnStages) * kTileRows * stride;
       int *vf = vflag + (it % kAttnStages) * kTileRows;
-      for (int cid = gtid; cid < kTileRows * nv; cid += NW * 32) {
-        const int rr = cid / nv, v = cid - rr * nv;
-        const int e = e0 + tile * kTileRows + rr;
-        const uint16_t *src = nullptr;
+      const uint16_t *mysrc = nullptr;
+      if (lane < kTileRows) {
+        const int e = e0 + tile * kTileRows + lane;
         if (e < e1) {
           if (e < k) {
-            const int32_t l = lrow[e];
+            const int32_t l = lsm[e - e0];
             if (l >= 0) {
-              src = loc_row(c, r, l);
-              if (src == nullptr && v == 0) record_error(c.err, DC_LOC_RANGE, K_ATTN);
+              mysrc = loc_row(c, r, l);
+              if (mysrc == nullptr && wi == 0) record_error(c.err, DC_LOC_RANGE, K_ATTN);
             }
           } else {
-            src = brow + (size_t)(e - k) * c.row;
+            mysrc = brow + (size_t)(e - k) * c.row;
           }
         }
-        cp_async_16_zfill(st + (size_t)rr * stride + v * 16,
-                          src ? (const void *)(src + v * 8) : (const void *)brow, src ? 16 : 0);
-        if (v == 0) vf[rr] = src != nullptr;
+        if (wi == 0) vf[lane] = mysrc != nullptr;
+      }
+#pragma unroll 4
+      for (int rr = 0; rr < kTileRows; ++rr) {
+        const uint16_t *src = reinterpret_cast<const uint16_t *>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mysrc), rr));
+        unsigned char *dst = st + (size_t)rr * stride;
+        for (int v = gtid; v < nv; v += NW * 32)
+          cp_async_16_zfill(dst + v * 16, src ? (const void *)(src + v * 8) : (const void *)brow,
+                            src ? 16 : 0);
       }
     }
     cp_async_commit();
@@ -374,14 +391,18 @@ static cudaError_t launch_attn_t(const DevCtx &c, const uint16_t *q, const uint1
   const size_t stages = (size_t)SH::SUB * kAttnStages * kTileRows * stride;
   const size_t epi = ((size_t)SH::SUB * 16 * DV + 2 * SH::SUB * 16 + 16 * (size_t)n_split) * 4;
   const size_t body = ((stages > epi ? stages : epi) + 127) / 128 * 128;
-  const size_t smem = attn_smem_bytes<DQK, DV>(c.row, n_split) + 128;
+  const size_t loc_off = ((size_t)SH::SUB * kAttnStages * kTileRows * 4 + 2 * SH::NW * 32 * 8 * 4 +
+                          127) / 128 * 128;
+  const int chunk = attn_chunk(c, n_split);
+  const size_t smem = attn_smem_bytes<DQK, DV>(c.row, n_split) + 128 + loc_off +
+                      attn_loc_bytes(chunk);
   static size_t granted = 0;
   cudaError_t e = ensure_smem(k_attn<DQK, DV>, smem, granted);
   if (e != cudaSuccess) return e;
   dim3 grid(n_split, c.Kmax, c.N * c.Hkv);
   if (tm) tm->begin(K_ATTN, s);
-  k_attn<DQK, DV><<<grid, kAttnThreads, smem, s>>>(c, q, block, loc, out, lse, n_split,
-                                                     attn_chunk(c, n_split), body);
+  k_attn<DQK, DV><<<grid, kAttnThreads, smem, s>>>(c, q, block, loc, out, lse, n_split, chunk,
+                                                     body, loc_off);
   if (tm) tm->end(K_ATTN, s);
   return cudaGetLastError();
 }

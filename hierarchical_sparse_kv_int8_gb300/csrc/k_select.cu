@@ -7,6 +7,8 @@
 #include "dhs_internal.cuh"
 #include "ptx_util.cuh"
 
+#include <cooperative_groups.h>
+
 #include <climits>
 
 namespace dhs {
@@ -22,6 +24,21 @@ cudaError_t launch_upload(int32_t *dst, const int32_t *words, int n, cudaStream_
   for (int i = 0; i < n; ++i) w.w[i] = words[i];
   k_upload<<<(n + 255) / 256, 256, 0, s>>>(dst, n, w);
   return cudaGetLastError();
+}
+
+// Per-round control words of select (K_r, then the domain of every query),
+// written from the kernel parameter, and the score ranges reset.
+__global__ void k_select_prep(const DevCtx c, const __grid_constant__ UploadWords w) {
+  const int n = c.N + c.N * c.Kmax;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    if (i < c.N) c.Kr[i] = w.w[i];
+    else c.dom[i - c.N] = w.w[i];
+  }
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < c.N * c.Kmax;
+       i += gridDim.x * blockDim.x) {
+    c.minmax[2 * i] = INT_MAX;
+    c.minmax[2 * i + 1] = INT_MIN;
+  }
 }
 
 // ---------------------------------------------------------------- scores
@@ -122,19 +139,57 @@ k_index_score(const DevCtx c, const int8_t *__restrict__ q_idx) {
     for (int j = 0; j < kMaxKmax; ++j)
       if (j < Kr) c.scores[((size_t)r * c.Kmax + j) * c.Sm + s] = acc[j];
   }
+  // range of each query's scores over its domain: one atomic per CTA and query
+  __shared__ int smn[kScoreThreads / 32][kMaxKmax], smx[kScoreThreads / 32][kMaxKmax];
+  const int lane = t & 31, wid = t >> 5;
+#pragma unroll
+  for (int j = 0; j < kMaxKmax; ++j) {
+    if (j >= Kr) break;
+    const bool valid = t < rows && row0 + t < c.dom[r * c.Kmax + j];
+    int mn = valid ? acc[j] : INT_MAX, mx = valid ? acc[j] : INT_MIN;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) {
+      smn[wid][j] = mn;
+      smx[wid][j] = mx;
+    }
+  }
+  __syncthreads();
+  if (t < Kr) {
+    int mn = INT_MAX, mx = INT_MIN;
+#pragma unroll
+    for (int w = 0; w < kScoreThreads / 32; ++w) {
+      mn = min(mn, smn[w][t]);
+      mx = max(mx, smx[w][t]);
+    }
+    if (mn <= mx) {
+      atomicMin(&c.minmax[(r * c.Kmax + t) * 2 + 0], mn);
+      atomicMax(&c.minmax[(r * c.Kmax + t) * 2 + 1], mx);
+    }
+  }
 }
 
 // ---------------------------------------------------------------- top-k
-// One CTA of 1024 threads per (request, query).  (1) min and max of the
-// query's scores; (2) exact radix select on the score minus the minimum, at
-// most 13 bits per pass (one pass when the scores span fewer than 8192
-// values); (3) ordered collection: each warp owns a contiguous run of rows,
-// counts the rows above the threshold and those equal to it, and after one
-// exchange of the 32 per-warp counts writes its rows in row order, keeping
-// the lowest-index rows among those equal to the threshold; (4) bitonic sort
-// of the k winners by (score descending, row ascending), with warp-local
-// synchronisation for the strides that stay inside one warp's 64 elements.
+// One thread-block cluster of kTopkCluster CTAs per (request, query); CTA c
+// of the cluster owns the c-th contiguous quarter of the query's domain.
+//  (1) the score range comes from the scoring kernel;
+//  (2) exact radix select on the score minus the minimum, at most 13 bits
+//      per pass (one pass when the scores span fewer than 8192 values): each
+//      CTA histograms its rows, then every CTA sums the cluster's histograms
+//      through distributed shared memory and finds the same threshold;
+//  (3) ordered collection: each warp owns a contiguous run of rows, counts
+//      those above the threshold and those equal to it; after the counts of
+//      all warps and CTAs are known every warp writes its rows, in row order,
+//      into the leader CTA's candidate array (the lowest-index rows win the
+//      ties at the threshold);
+//  (4) the leader sorts the k winners by (score descending, row ascending)
+//      with a bitonic network held in registers, two elements per thread,
+//      exchanging through shared memory only for strides that cross warps.
 constexpr int kTopkThreads = 1024;
+constexpr int kTopkCluster = 4;
 constexpr int kRadixBits = 13;
 
 __device__ __forceinline__ int block_excl_scan(int v, int *warp_sums, int &total) {
@@ -167,11 +222,71 @@ __device__ __forceinline__ unsigned long long topk_key(uint32_t v, int s) {
   return ((unsigned long long)(0xFFFFFFFFu - v) << 32) | (uint32_t)s;
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
+// Compare-exchange of a bitonic stage between two registers of one thread.
+__device__ __forceinline__ void cmpx(unsigned long long &lo, unsigned long long &hi, bool asc) {
+  if ((lo > hi) == asc) {
+    const unsigned long long t = lo;
+    lo = hi;
+    hi = t;
+  }
+}
+
+// Ascending bitonic sort of kp (a power of two, <= 2 * blockDim.x) keys,
+// element e = 2 * thread + h held in x[h]; buf is kp keys of shared memory.
+__device__ void bitonic_sort_regs(unsigned long long (&x)[2], unsigned long long *buf, int kp) {
+  const int t = threadIdx.x, lane = t & 31;
+  const bool active = 2 * t < kp;
+  const bool warp_active = (t >> 5) * 64 < kp;  // warps past the data skip register stages
+  for (int size = 2; size <= kp; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int e0 = 2 * t;
+      const bool asc = (e0 & size) == 0;
+      if (stride == 1) {
+        if (active) cmpx(x[0], x[1], asc);
+      } else if (stride <= 32) {
+        if (!warp_active) continue;
+        // partner thread t ^ (stride / 2) holds e ^ stride; both lanes keep
+        // the value their position should hold
+        const int pm = stride >> 1;
+        const bool lower = (t & pm) == 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const unsigned long long o = __shfl_xor_sync(0xffffffffu, x[h], pm);
+          const bool keep_min = lower == asc;
+          x[h] = keep_min ? (x[h] < o ? x[h] : o) : (x[h] > o ? x[h] : o);
+        }
+      } else {
+        __syncthreads();
+        if (active) {
+          buf[e0] = x[0];
+          buf[e0 + 1] = x[1];
+        }
+        __syncthreads();
+        if (active) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int e = e0 + h;
+            const unsigned long long o = buf[e ^ stride];
+            const bool lower = (e & stride) == 0;
+            const bool keep_min = lower == asc;
+            x[h] = keep_min ? (x[h] < o ? x[h] : o) : (x[h] > o ? x[h] : o);
+          }
+        }
+      }
+    }
+  }
+  (void)lane;
+}
+
+__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
 k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char smem[];
-  const int r = blockIdx.x / c.Kmax, j = blockIdx.x % c.Kmax;
-  if (j >= c.Kr[r]) return;
+  const int crank = (int)cl.block_rank();
+  const int prob = blockIdx.x / kTopkCluster;
+  const int r = prob / c.Kmax, j = prob % c.Kmax;
+  if (j >= c.Kr[r]) return;  // the whole cluster leaves together
   const int dom = c.dom[r * c.Kmax + j];
   const int k = c.k;
   const int32_t *__restrict__ sc = c.scores + ((size_t)r * c.Kmax + j) * c.Sm;
@@ -181,77 +296,68 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
   unsigned long long *cand = reinterpret_cast<unsigned long long *>(smem);
   uint32_t *hist = reinterpret_cast<uint32_t *>(cand + kp);
   __shared__ int warp_sums[32];
-  __shared__ int wmin[32], wmax[32], wgt[32], weq[32];
-  __shared__ int sh_bin, sh_above;
+  __shared__ int wgt[32], weq[32];
+  __shared__ int sh_bin, sh_above, sh_cta_gt, sh_cta_eq;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int ksel = min(k, dom);
+  const int part = (((dom + kTopkCluster - 1) / kTopkCluster) + 31) & ~31;
+  const int p0 = min(dom, crank * part), p1 = min(dom, p0 + part);
+  const int lo = c.minmax[(r * c.Kmax + j) * 2 + 0];
+  const int hi = c.minmax[(r * c.Kmax + j) * 2 + 1];
 
-  // (1) range of the scores
-  int mn = INT_MAX, mx = INT_MIN;
-#pragma unroll 4
-  for (int s = tid; s < dom; s += kTopkThreads) {
-    const int v = sc[s];
-    mn = min(mn, v);
-    mx = max(mx, v);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-  if (lane == 0) {
-    wmin[wid] = mn;
-    wmax[wid] = mx;
-  }
-  __syncthreads();
-  mn = wmin[lane];
-  mx = wmax[lane];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-  const int lo = mn, hi = mx;
-
+  int nloc = 0;  // candidates this CTA holds
   if (dom <= k) {
-    for (int s = tid; s < dom; s += kTopkThreads) cand[s] = topk_key((uint32_t)(sc[s] - lo), s);
+    for (int s = p0 + tid; s < p1; s += kTopkThreads)
+      cand[s - p0] = topk_key((uint32_t)(sc[s] - lo), s);
+    nloc = p1 - p0;
   } else {
-    // (2) radix select of the k-th largest offset score T
     const uint32_t range = (uint32_t)(hi - lo);
     int shift = range ? 32 - __clz((int)range) : 0;
     uint32_t prefix = 0;
     int k_rem = k;
+    const uint32_t *hr[kTopkCluster];
+#pragma unroll
+    for (int q = 0; q < kTopkCluster; ++q) hr[q] = cl.map_shared_rank(hist, q);
+    int passes = 0, nb_last = 1;
     while (shift > 0) {
       const int width = min(kRadixBits, shift);
       shift -= width;
       const int nbins = 1 << width;
+      ++passes;
+      nb_last = nbins;
+      cl.sync();  // every CTA has finished reading the previous histograms
       for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
       __syncthreads();
 #pragma unroll 4
-      for (int s = tid; s < dom; s += kTopkThreads) {
+      for (int s = p0 + tid; s < p1; s += kTopkThreads) {
         const uint32_t v = (uint32_t)(sc[s] - lo);
         if ((uint32_t)((unsigned long long)v >> (shift + width)) == prefix)
           atomicAdd(&hist[(v >> shift) & (nbins - 1)], 1u);
       }
-      __syncthreads();
+      cl.sync();  // all histograms of the cluster are complete
       // thread t owns a run of bins counted from the top; an exclusive scan in
-      // thread order then counts the rows above each run
+      // thread order counts the rows above each run
       const int per = (nbins + kTopkThreads - 1) / kTopkThreads;
       const int b_hi = nbins - tid * per;
       const int b_lo = max(0, b_hi - per);
       int local = 0;
-      for (int b = b_lo; b < b_hi; ++b) local += hist[b];
+      for (int b = b_lo; b < b_hi; ++b)
+#pragma unroll
+        for (int q = 0; q < kTopkCluster; ++q) local += hr[q][b];
       int total;
       const int above = block_excl_scan(b_hi > 0 ? local : 0, warp_sums, total);
       if (b_hi > 0 && above < k_rem && k_rem <= above + local) {
         int acc = above;
         for (int b = b_hi - 1; b >= b_lo; --b) {
-          if (acc + (int)hist[b] >= k_rem) {
+          int hb = 0;
+#pragma unroll
+          for (int q = 0; q < kTopkCluster; ++q) hb += hr[q][b];
+          if (acc + hb >= k_rem) {
             sh_bin = b;
             sh_above = acc;
             break;
           }
-          acc += hist[b];
+          acc += hb;
         }
       }
       __syncthreads();
@@ -259,13 +365,13 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
       prefix = (prefix << width) | (uint32_t)sh_bin;
       __syncthreads();
     }
-    const uint32_t T = prefix;       // the k-th largest offset score
-    const int need = k_rem;          // rows equal to T that are kept
-    const int c_gt = k - need;       // rows strictly above T
+    const uint32_t T = prefix;  // the k-th largest offset score
+    const int need = k_rem;     // rows equal to T that are kept
+    const int c_gt = k - need;  // rows strictly above T
 
-    // (3) ordered collection, one contiguous run of rows per warp
-    const int run = (((dom + 31) / 32) + 31) & ~31;
-    const int r0 = min(dom, wid * run), r1 = min(dom, r0 + run);
+    // counts of this CTA's warps, then of the cluster's CTAs
+    const int run = ((((p1 - p0) + 31) / 32) + 31) & ~31;
+    const int r0 = min(p1, p0 + wid * run), r1 = min(p1, r0 + run);
     int ngt = 0, neq = 0;
 #pragma unroll 8
     for (int base = r0; base < r1; base += 32) {
@@ -289,59 +395,169 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
         ex += ea;
       }
     }
-    int gt_off = __shfl_sync(0xffffffffu, gx - wgt[lane], wid);
+    if (tid == 31) {
+      sh_cta_gt = gx;
+      sh_cta_eq = ex;
+    }
+    int gt_off = __shfl_sync(0xffffffffu, gx - wgt[lane], wid);   // within this CTA
     int eq_off = __shfl_sync(0xffffffffu, ex - weq[lane], wid);
+    cl.sync();  // every CTA's totals are published
+    int eq_base = 0;                       // rows equal to T in earlier CTAs
+    for (int q = 0; q < crank; ++q) eq_base += *cl.map_shared_rank(&sh_cta_eq, q);
+    const int my_gt = sh_cta_gt, my_eq = sh_cta_eq;
+    const int kept_eq = max(0, min(my_eq, need - eq_base));
+    nloc = my_gt + kept_eq;
+    // Exact bins (one radix pass, or none): every winner's place follows from
+    // the histograms.  base[b] = rows of the domain above offset value b plus
+    // rows equal to b in earlier CTAs; the rows equal to b in this CTA follow
+    // in row order.
+    const bool exact = passes <= 1;
+    int *base = reinterpret_cast<int *>(hist + (1 << kRadixBits));
+    if (exact) {
+      const int per = (nb_last + kTopkThreads - 1) / kTopkThreads;
+      const int b_hi = nb_last - tid * per;
+      const int b_lo = max(0, b_hi - per);
+      int run_sum = 0;
+      for (int b = b_lo; b < b_hi; ++b) {
+        int pc = 0, g = 0;
+        if (b > (int)T) {
+#pragma unroll
+          for (int q = 0; q < kTopkCluster; ++q) {
+            const int hv = (int)hr[q][b];
+            g += hv;
+            if (q < crank) pc += hv;
+          }
+        }
+        base[b] = pc;
+        run_sum += g;
+      }
+      int tot;
+      int acc = block_excl_scan(b_hi > 0 ? run_sum : 0, warp_sums, tot);
+      for (int b = b_hi - 1; b >= b_lo; --b) {
+        base[b] += acc;
+        if (b > (int)T) {
+#pragma unroll
+          for (int q = 0; q < kTopkCluster; ++q) acc += (int)hr[q][b];
+        }
+      }
+    }
+    cl.sync();  // no CTA reads another's histogram after this point
     const unsigned lt = (1u << lane) - 1u;
-    const int gt_end = gt_off + ngt, eq_end = eq_off + neq;  // this warp's share
+    const int gt_end = gt_off + ngt, eq_end = eq_off + neq;
 #pragma unroll 4
-    for (int base = r0; base < r1 && (gt_off < gt_end || (eq_off < eq_end && eq_off < need));
-         base += 32) {
-      const int s = base + lane;
+    for (int bs = r0; bs < r1 && (gt_off < gt_end || (eq_off < eq_end && eq_off < kept_eq));
+         bs += 32) {
+      const int s = bs + lane;
       const bool ok = s < r1;
       const uint32_t v = ok ? (uint32_t)(sc[s] - lo) : 0u;
       const unsigned bgt = __ballot_sync(0xffffffffu, ok && v > T);
       const unsigned beq = __ballot_sync(0xffffffffu, ok && v == T);
       if (ok && v > T) cand[gt_off + __popc(bgt & lt)] = topk_key(v, s);
       if (ok && v == T) {
-        const int rr = eq_off + __popc(beq & lt);
-        if (rr < need) cand[c_gt + rr] = topk_key(v, s);
+        const int rr = eq_off + __popc(beq & lt);  // rank among this CTA's ties
+        if (rr < kept_eq) {
+          if (exact) out[c_gt + eq_base + rr] = s;
+          else cand[my_gt + rr] = topk_key(v, s);
+        }
       }
       gt_off += __popc(bgt);
       eq_off += __popc(beq);
     }
-  }
-
-  // (4) bitonic sort ascending on (~score, row); pairs whose elements stay in
-  // one warp's block of 64 only need a warp barrier
-  for (int i = ksel + tid; i < kp; i += kTopkThreads) cand[i] = ~0ull;
-  __syncthreads();
-  int prev_stride = 0;
-  for (int size = 2; size <= kp; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      // a stage whose pairs cross warp blocks, or that follows one, needs the
-      // whole block; two warp-local stages in a row only need the warp
-      if (stride > 32 || prev_stride > 32) __syncthreads(); else __syncwarp();
-      prev_stride = stride;
-      for (int i = tid; i < (kp >> 1); i += kTopkThreads) {
-        const int a = 2 * stride * (i / stride) + (i % stride);
-        const int b = a + stride;
-        const bool asc = (a & size) == 0;
-        const unsigned long long x = cand[a], y = cand[b];
-        if ((x > y) == asc) {
-          cand[a] = y;
-          cand[b] = x;
+    if (exact) {
+      // one warp walks this CTA's winners above T in row order; equal values
+      // are ranked with a per-value running count
+      int *lcnt = reinterpret_cast<int *>(hist);
+      for (int i = tid; i < nb_last; i += kTopkThreads) lcnt[i] = 0;
+      __syncthreads();
+      if (wid == 0) {
+        for (int i0 = 0; i0 < my_gt; i0 += 32) {
+          const int i = i0 + lane;
+          const bool ok = i < my_gt;
+          const unsigned long long key = ok ? cand[i] : 0ull;
+          const uint32_t v = ok ? 0xFFFFFFFFu - (uint32_t)(key >> 32) : (0x80000000u | lane);
+          const unsigned peers = __match_any_sync(0xffffffffu, v);
+          if (ok) {
+            const int pos = base[v] + lcnt[v] + __popc(peers & lt);
+            out[pos] = (int32_t)(uint32_t)(key & 0xFFFFFFFFull);
+          }
+          __syncwarp();
+          if (ok && lane == 31 - __clz((int)peers)) lcnt[v] += __popc(peers);
+          __syncwarp();
         }
       }
+      if (crank == 0)
+        for (int i = ksel + tid; i < k; i += kTopkThreads) out[i] = -1;
+      return;
     }
   }
+  // each CTA sorts its own candidates ...
+  __shared__ int sh_nloc;
+  if (tid == 0) sh_nloc = nloc;
+  int kpl = 1;
+  while (kpl < nloc) kpl <<= 1;
   __syncthreads();
-  for (int i = tid; i < k; i += kTopkThreads)
-    out[i] = i < ksel ? (int32_t)(uint32_t)(cand[i] & 0xFFFFFFFFull) : -1;
+  unsigned long long x[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int e = 2 * tid + h;
+    x[h] = e < nloc ? cand[e] : ~0ull;
+  }
+  if (nloc > 1) bitonic_sort_regs(x, cand, kpl);
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    if (2 * tid + h < nloc) cand[2 * tid + h] = x[h];
+  cl.sync();  // every CTA's sorted list is in place
+  // ... copies the other CTAs' lists next to it (one pass of distributed
+  // shared-memory reads into the histogram area, free by now) ...
+  int lens[kTopkCluster], offs[kTopkCluster];
+  int tot = 0;
+#pragma unroll
+  for (int q = 0; q < kTopkCluster; ++q) {
+    lens[q] = *cl.map_shared_rank(&sh_nloc, q);
+    offs[q] = tot;
+    tot += lens[q];
+  }
+  unsigned long long *all = reinterpret_cast<unsigned long long *>(hist);
+#pragma unroll
+  for (int q = 0; q < kTopkCluster; ++q) {
+    if (q == crank) continue;
+    const unsigned long long *src = cl.map_shared_rank(cand, q);
+    for (int i = tid; i < lens[q]; i += kTopkThreads) all[offs[q] + i] = src[i];
+  }
+  cl.sync();  // copies done: no CTA reads another's memory after this
+  // ... and places each key by counting the smaller keys of the other lists
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int e = 2 * tid + h;
+    if (e >= nloc) continue;
+    const unsigned long long key = x[h];
+    int pos = e;
+#pragma unroll
+    for (int q = 0; q < kTopkCluster; ++q) {
+      if (q == crank) continue;
+      const unsigned long long *lst = all + offs[q];
+      int a = 0, b = lens[q];  // lower bound of key in list q
+      while (a < b) {
+        const int m = (a + b) >> 1;
+        if (lst[m] < key) a = m + 1; else b = m;
+      }
+      pos += a;
+    }
+    if (pos < k) out[pos] = (int32_t)(uint32_t)(key & 0xFFFFFFFFull);
+  }
+  if (crank == 0)
+    for (int i = ksel + tid; i < k; i += kTopkThreads) out[i] = -1;
 }
 
 cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_out, int max_dom,
-                          int active, cudaStream_t s, Timer *tm) {
-  (void)active;
+                          const int32_t *ctl_words, cudaStream_t s, Timer *tm) {
+  {
+    UploadWords w;
+    const int n = c.N + c.N * c.Kmax;
+    for (int i = 0; i < n; ++i) w.w[i] = ctl_words[i];
+    k_select_prep<<<(c.N * c.Kmax + 255) / 256, 256, 0, s>>>(c, w);
+  }
   if (max_dom > 0) {
     const int nc = c.idx_row >> 4;
     const size_t smem = (size_t)c.Kmax * c.idx_row +
@@ -366,12 +582,12 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_ou
   }
   int kp = 1;
   while (kp < c.k) kp <<= 1;
-  const size_t smem_topk = (size_t)kp * 8 + ((size_t)1 << kRadixBits) * 4;
+  const size_t smem_topk = (size_t)kp * 8 + ((size_t)1 << kRadixBits) * 8;
   static size_t granted_topk = 0;
   cudaError_t e2 = ensure_smem(k_topk, smem_topk, granted_topk);
   if (e2 != cudaSuccess) return e2;
   if (tm) tm->begin(K_TOPK, s);
-  k_topk<<<c.N * c.Kmax, kTopkThreads, smem_topk, s>>>(c, topk_out);
+  k_topk<<<c.N * c.Kmax * kTopkCluster, kTopkThreads, smem_topk, s>>>(c, topk_out);
   if (tm) tm->end(K_TOPK, s);
   return cudaGetLastError();
 }

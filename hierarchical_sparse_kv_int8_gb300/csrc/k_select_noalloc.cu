@@ -272,7 +272,7 @@ extern "C" int dhs_select_noalloc(const int8_t *q_idx, const int8_t *keys, int32
   using namespace dhs;
   if (!q_idx || !keys || !topk_out || n_queries < 1 || n_queries > kMaxKmax || n_rows < 1 ||
       idx_row_bytes < 16 || idx_row_bytes > 1024 || idx_row_bytes % 16 || topk < 32 ||
-      topk > kMaxTopk || topk % 32 || ((uintptr_t)q_idx & 15u) || ((uintptr_t)keys & 15u))
+      topk > 4096 || topk % 32 || ((uintptr_t)q_idx & 15u) || ((uintptr_t)keys & 15u))
     return DHS_ERR_INVALID;
   if ((int64_t)n_queries * n_rows > kNoallocScoreWords) return DHS_ERR_CAPACITY;
   int32_t *scratch = nullptr;

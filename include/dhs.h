@@ -77,7 +77,7 @@ enum {
   DHS_KV_LATENT = 1 /* MLA-like shared latent: row = qk_dim elements; K = row, V = row[0:v_dim]     */
 };
 
-/* Fixed at dhs_create.  Limits: n_slots <= 256, k_max <= 8, topk <= 4096 (a
+/* Fixed at dhs_create.  Limits: n_slots <= 256, k_max <= 8, topk <= 2048 (a
  * multiple of 32), q_heads / kv_heads <= 16, qk_dim and v_dim multiples of 16,
  * idx_heads * idx_dim a multiple of 16 and <= 1024, budget <= 65535. */
 typedef struct {
