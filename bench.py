@@ -42,7 +42,7 @@ WORKLOAD = "cfg2"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -91,7 +91,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -165,47 +165,85 @@ def oracle_step(o, rec, rnd, slots):
     o.commit(acc_s)
 
 
-def cpu_baseline(rec, budget_s=12.0):
-    """Time the oracle on the host: round 1 of as many requests as fit in
-    about ``budget_s`` seconds (round 0 of each request is set-up, untimed)."""
-    done, t_total = 0, 0.0
+def cpu_baseline(rec, budget_s=10.0):
+    """Time the oracle on the host: round 1 (select, resolve, attend, commit)
+    of the workload's requests, repeated from the state round 0 leaves, until
+    about ``budget_s`` seconds of oracle work have been timed.  Set-up (input
+    generation, round 0, copying the state) is not timed."""
+    import copy
+    prepared = []
     for r in range(rec.N):
         o = oracle_requests(rec, [r])
         oracle_step(o, rec, 0, [r])          # previous step: warms the hot cache
-        t0 = time.perf_counter()
-        oracle_step(o, rec, 1, [r])
-        t_total += time.perf_counter() - t0
-        done += 1
-        if t_total > budget_s:
-            break
+        prepared.append(o)
+    done, t_total = 0, 0.0
+    while t_total < budget_s:
+        for r in range(rec.N):
+            o = copy.deepcopy(prepared[r])
+            t0 = time.perf_counter()
+            oracle_step(o, rec, 1, [r])
+            t_total += time.perf_counter() - t0
+            done += 1
     value = done * rec.K / t_total
     return {"value": value, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of %d requests, one verification round each (K=%d, S=%d), "
-                      "single-threaded numpy (int64 scores, float64 attention)"
-                      % (done, rec.N, rec.K, rec.S),
-            "seconds": t_total}
+            "sample": "%d request-rounds (K=%d, S=%d; the %d requests of the workload, "
+                      "repeated), single-threaded numpy (int64 scores, float64 attention)"
+                      % (done, rec.K, rec.S, rec.N),
+            "seconds": round(t_total, 2)}
 
 
 # ---------------------------------------------------------------- algorithmic bytes
 def algorithmic_bytes(rec, counts, k_per_req):
-    """Bytes each step must move (not the work it avoids), per kernel family.
+    """Bytes each step must move (not the work it avoids), per kernel and family.
 
-    select: index keys of the domain (read once for all K queries), the int8
-    queries and the int32 top-k lists.  attend: each distinct selected row
-    once, the block rows, bf16 queries and outputs and the int32 locations.
-    gather: the distinct missing rows over the host link.
+    select family: index keys of the domain (read once for all K queries), the
+    int8 queries and the int32 top-k lists.  attend family: each distinct
+    selected row once, the block rows, bf16 queries and outputs, int32
+    locations.  Per kernel: index_score reads keys and queries; topk reads the
+    int32 scores and writes the lists; union_probe reads the lists and two
+    row maps per union row and writes locations and the union and miss lists;
+    gather moves the distinct missing rows over the host link; attn is the
+    attend family; post_attend copies block rows into the ring and promoted
+    rows into the hot cache (read + write); commit copies accepted rows.
     """
     K = int(k_per_req.max())
     n_act = int((k_per_req > 0).sum())
     rb = rec.row_bytes
     keys = n_act * rec.S * rec.idx_row
-    select = keys + n_act * K * rec.idx_row + 4 * n_act * K * rec.topk
+    qbytes = n_act * K * rec.idx_row
+    lists = 4 * n_act * K * rec.topk
+    select = keys + qbytes + lists
     U = int(counts[:, 0].sum())
     M = int(counts[:, 1].sum())
+    P = int(counts[:, 2].sum())
     attend = U * rb + n_act * K * rb + 2 * n_act * K * rec.Hq * (rec.qk_dim + rec.v_dim) \
-        + 4 * n_act * K * rec.topk
-    return {"index_score": keys + n_act * K * rec.idx_row, "select": select,
-            "attn": attend, "gather": M * rb, "union": U, "misses": M}
+        + lists
+    kernel = {
+        "index_score": keys + qbytes,
+        "topk": 4 * n_act * K * rec.S + lists,
+        "union_probe": 2 * lists + 8 * U + 4 * (U + M),
+        "gather": M * rb,
+        "attn": attend,
+        "post_attend": 2 * (n_act * K + P) * rb,
+    }
+    return {"select": select, "attn": attend, "gather": M * rb, "union": U, "misses": M,
+            "kernel_bytes": kernel}
+
+
+def measure_h2d(torch, stream, nbytes=256 << 20):
+    """Host-to-device link bandwidth: best of 5 pinned 256 MiB copies."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = 0.0
+    for _ in range(6):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        d.copy_(h, non_blocking=True)
+        b.record(stream)
+        stream.synchronize()
+        best = max(best, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del h, d
+    return best
 
 
 # ---------------------------------------------------------------- native arm
@@ -238,6 +276,7 @@ def run_native(args):
         acc1 = rec.accepted(1)
         flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
         stream.synchronize()
+        h2d_peak = measure_h2d(torch, stream)
 
         def step():
             run.select(kr)
@@ -276,16 +315,19 @@ def run_native(args):
             return g
         graph = capture(False)
         graph_timed = capture(True)
+        # clocks are sampled from just before the warm-up to the end of the
+        # timed steps (nvidia-smi needs a moment to start)
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.3)
         for _ in range(args.warmup):
             run.ctx.restore(snap, stream)
             graph.replay()
         stream.synchronize()
-        sampler = ClockSampler(local)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         barrier(world)
         stream.synchronize()
-        sampler.start()
         for i in range(args.steps):
             run.ctx.restore(snap, stream)
             flush.fill_(i & 0xFF)
@@ -336,25 +378,42 @@ def run_native(args):
     value = world * tokens / (ms * 1e-3)
     e2e_value = world * tokens / (e2e_ms * 1e-3)
 
-    # roofline of the dominant kernel (largest share of the timed region)
+    # roofline of every kernel and of the dominant one (largest share of the
+    # timed region): algorithmic bytes per launch / average launch duration
     ab = algorithmic_bytes(rec, counts, kr)
     per = {name: (n, t) for name, (n, t) in kt.items() if n > 0}
     dom = max(per, key=lambda k: per[k][1])
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
     hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
-    algo = {"index_score": ab["index_score"], "attn": ab["attn"], "gather": ab["gather"]}
-    n_l, t_l = per[dom]
-    avg_ms = t_l / n_l
-    bytes_per_launch = algo.get(dom)
-    roof = None
-    if bytes_per_launch is not None:
-        ach = bytes_per_launch / (avg_ms * 1e-3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
-                "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": None,
-                "algorithmic_bytes": bytes_per_launch, "avg_launch_ms": round(avg_ms, 5),
-                "peak_source": "MEASURED_PEAKS.json hbm_gbs (burst copy)" if peaks else
-                "fallback 6.8 TB/s"}
+    hbm_src = "MEASURED_PEAKS.json hbm_gbs (copy, burst)" if peaks else "fallback 6.8 TB/s"
+    roofs = {}
+    for name, (n_l, t_l) in per.items():
+        byts = ab["kernel_bytes"].get(name)
+        if byts is None:
+            continue
+        avg_ms = t_l / n_l
+        ach = byts / (avg_ms * 1e-3) / 1e9
+        link = name == "gather"
+        peak = h2d_peak if link else hbm_peak
+        roofs[name] = {"kernel": name, "bound": "h2d" if link else "hbm",
+                       "achieved": round(ach, 1), "peak": round(peak, 1), "unit": "GB/s",
+                       "frac": round(ach / peak, 4), "traffic": None, "algorithmic_bytes": byts,
+                       "avg_launch_ms": round(avg_ms, 5),
+                       "peak_source": ("host link: pinned host-to-device copy measured in this run"
+                                       if link else hbm_src)}
+    roof = roofs.get(dom)
+    fam_t = sum(per[k][1] / per[k][0] for k in ("index_score", "topk", "attn") if k in per)
+    fam_b = ab["select"] + ab["attn"]
+    families = {
+        "select+attend": {"achieved": round(fam_b / (fam_t * 1e-3) / 1e9, 1), "unit": "GB/s",
+                          "frac_of_hbm": round(fam_b / (fam_t * 1e-3) / 1e9 / hbm_peak, 4),
+                          "algorithmic_bytes": fam_b, "ms": round(fam_t, 5)},
+    }
+    if "gather" in roofs:
+        families["shared gather"] = {"achieved": roofs["gather"]["achieved"], "unit": "GB/s",
+                                     "frac_of_h2d": roofs["gather"]["frac"],
+                                     "h2d_peak": round(h2d_peak, 1)}
     breakdown = {k: {"launches": n, "avg_us": round(1e3 * t / n, 2),
                      "share": round(t / sum(v[1] for v in per.values()), 4)}
                  for k, (n, t) in per.items()}
@@ -381,6 +440,8 @@ def run_native(args):
         "launch": "CUDA graph of one round (select, resolve, attend, commit), replayed per step; "
                   "kernel times from a second replay of the same steps with per-kernel events",
         "roofline": roof,
+        "roofline_all": roofs,
+        "families": families,
         "kernels": breakdown,
         "workload_stats": {"union_rows": ab["union"], "misses": ab["misses"],
                            "hot_hits": int(counts[:, 3].sum()),

@@ -124,9 +124,23 @@ __device__ __forceinline__ const uint16_t *loc_row(const DevCtx &c, int r, int32
   }
 }
 
-// Raise a kernel's dynamic shared-memory limit to at least `bytes` (cached).
+// Every kernel of the library asks for the same L1/shared-memory split (all
+// shared), so consecutive kernels never make the SMs change their carveout.
+template <typename F>
+cudaError_t same_carveout(F *func) {
+  return cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` (cached);
+// the first call also sets the common carveout.
 template <typename F>
 cudaError_t ensure_smem(F *func, size_t bytes, size_t &granted) {
+  if (granted == 0) {
+    cudaError_t e0 = same_carveout(func);
+    if (e0 != cudaSuccess) return e0;
+    if (bytes == 0) granted = 1;
+  }
   if (bytes <= granted) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess) granted = bytes;

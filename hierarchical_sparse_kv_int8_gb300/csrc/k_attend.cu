@@ -53,6 +53,11 @@ cudaError_t launch_post_attend(const DevCtx &c, const uint16_t *block, cudaStrea
   int bpr = (152 * 4 + c.N - 1) / c.N;
   if (bpr > 64) bpr = 64;
   if (tm) tm->begin(K_POST_ATTEND, s);
+  static bool carve_k_post_attend = false;
+  if (!carve_k_post_attend) {
+    same_carveout(k_post_attend);
+    carve_k_post_attend = true;
+  }
   k_post_attend<<<dim3(bpr, c.N), 256, 0, s>>>(c, block);
   if (tm) tm->end(K_POST_ATTEND, s);
   return cudaGetLastError();
@@ -84,6 +89,11 @@ cudaError_t launch_commit(const DevCtx &c, const int32_t *aux_words, cudaStream_
   UploadWords aux;
   for (int i = 0; i < c.N * 4; ++i) aux.w[i] = aux_words[i];
   if (tm) tm->begin(K_COMMIT, s);
+  static bool carve_k_commit = false;
+  if (!carve_k_commit) {
+    same_carveout(k_commit);
+    carve_k_commit = true;
+  }
   k_commit<<<dim3(1, c.N), 256, 0, s>>>(c, aux);
   if (tm) tm->end(K_COMMIT, s);
   return cudaGetLastError();

@@ -81,7 +81,7 @@ static size_t attn_smem_bytes(int row_elems, int n_split) {
   using SH = AttnShape<DQK, DV>;
   const size_t stride = (size_t)row_elems * 2 + 16;
   const size_t stages = (size_t)SH::SUB * kAttnStages * kTileRows * stride;
-  const size_t epilogue = ((size_t)SH::SUB * 16 * DV + 2 * SH::SUB * 16 + 16 * n_split) * 4;
+  const size_t epilogue = ((size_t)SH::SUB * 16 * DV + 2 * SH::SUB * 16 + 48 * n_split) * 4;
   const size_t body = stages > epilogue ? stages : epilogue;
   return body + (size_t)SH::SUB * kAttnStages * kTileRows * 4 + 2 * SH::NW * 32 * 8 * 4 + 64;
 }
@@ -354,28 +354,46 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   __syncthreads();
   if (!sh_last) return;
   __threadfence();
+  // every (head, split) pair's max and sum in one parallel load ...
+  float *Ms = Wt + 16 * n_split;  // [16][n_split] maxima, then sums
+  float *Ls = Ms + 16 * n_split;
+  for (int i = tid; i < G * n_split; i += kAttnThreads) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(c.part_ml + (qbase * n_split + i) * 2));
+    Ms[i] = ml.x;
+    Ls[i] = ml.y;
+  }
+  __syncthreads();
+  // ... then the weights of each split, from shared memory
   for (int h = tid; h < G; h += kAttnThreads) {
-    const float *ml = c.part_ml + (qbase + h) * n_split * 2;
     float M = -CUDART_INF_F;
-    for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, __ldcg(ml + 2 * sp));
+    for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, Ms[h * n_split + sp]);
     const float ref = M == -CUDART_INF_F ? 0.f : M;
     float L = 0.f;
-    for (int sp = 0; sp < n_split; ++sp) L += __ldcg(ml + 2 * sp + 1) * exp2f(__ldcg(ml + 2 * sp) - ref);
+    for (int sp = 0; sp < n_split; ++sp) L += Ls[h * n_split + sp] * exp2f(Ms[h * n_split + sp] - ref);
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int sp = 0; sp < n_split; ++sp) Wt[h * n_split + sp] = exp2f(__ldcg(ml + 2 * sp) - ref) * inv;
+    for (int sp = 0; sp < n_split; ++sp) Wt[h * n_split + sp] = exp2f(Ms[h * n_split + sp] - ref) * inv;
     if (lse) lse[qbase + h] = L > 0.f ? (M + log2f(L)) * ln2 : -CUDART_INF_F;
   }
   __syncthreads();
+  constexpr int kMaxUnrolledSplits = 16;  // all partial loads of a thread in flight at once
   for (int idx = tid; idx < G * DV / 2; idx += kAttnThreads) {
     const int h = (2 * idx) / DV, d = (2 * idx) % DV;
     const float *po = c.part_o + (qbase + h) * n_split * DV + d;
     float a = 0.f, b = 0.f;
-#pragma unroll 4
-    for (int sp = 0; sp < n_split; ++sp) {
-      const float2 v = __ldcg(reinterpret_cast<const float2 *>(po + (size_t)sp * DV));
-      const float wgt = Wt[h * n_split + sp];
-      a += wgt * v.x;
-      b += wgt * v.y;
+    for (int sp0 = 0; sp0 < n_split; sp0 += kMaxUnrolledSplits) {
+      float2 v[kMaxUnrolledSplits];
+#pragma unroll
+      for (int u = 0; u < kMaxUnrolledSplits; ++u)
+        if (sp0 + u < n_split)
+          v[u] = __ldcg(reinterpret_cast<const float2 *>(po + (size_t)(sp0 + u) * DV));
+#pragma unroll
+      for (int u = 0; u < kMaxUnrolledSplits; ++u) {
+        if (sp0 + u < n_split) {
+          const float wgt = Wt[h * n_split + sp0 + u];
+          a += wgt * v[u].x;
+          b += wgt * v[u].y;
+        }
+      }
     }
     *reinterpret_cast<uint32_t *>(out + (qbase + h) * DV + d) = pack_bf16(a, b);
   }
@@ -389,7 +407,7 @@ static cudaError_t launch_attn_t(const DevCtx &c, const uint16_t *q, const uint1
   using SH = AttnShape<DQK, DV>;
   const size_t stride = (size_t)c.row * 2 + 16;
   const size_t stages = (size_t)SH::SUB * kAttnStages * kTileRows * stride;
-  const size_t epi = ((size_t)SH::SUB * 16 * DV + 2 * SH::SUB * 16 + 16 * (size_t)n_split) * 4;
+  const size_t epi = ((size_t)SH::SUB * 16 * DV + 2 * SH::SUB * 16 + 48 * (size_t)n_split) * 4;
   const size_t body = ((stages > epi ? stages : epi) + 127) / 128 * 128;
   const size_t loc_off = ((size_t)SH::SUB * kAttnStages * kTileRows * 4 + 2 * SH::NW * 32 * 8 * 4 +
                           127) / 128 * 128;

@@ -14,6 +14,8 @@
 #include "dhs_internal.cuh"
 #include "ptx_util.cuh"
 
+#include <cooperative_groups.h>
+
 #include <climits>
 
 namespace dhs {
@@ -46,40 +48,68 @@ __device__ __forceinline__ int ublock_excl_scan(int v, int *warp_sums, int &tota
   return excl;
 }
 
-size_t union_smem_bytes(const DevCtx &c) {
-  const size_t nw = (size_t)((c.Sm + 31) / 32);
-  const size_t pw = (size_t)((c.B + 31) / 32);
-  return nw * 8 + pw * 4 + (size_t)c.B * 8 + (size_t)c.Kmax * c.k * 4;
-}
-
+// The union/probe of one request runs on a cluster of kUnionCluster CTAs.
+// CTA c owns the c-th slice of the history rows: its shared memory holds the
+// union bitmap of that slice, the prefix count of every word and the
+// location of every union row in the slice.  The leader CTA (rank 0) also
+// holds the protected-slot and stamped-now bitmaps of the hot cache, filled
+// by every CTA through distributed shared memory, and chooses the victims.
+constexpr int kUnionCluster = 8;
 constexpr int32_t kMissMark = -2;
 constexpr int kBatch = 8;  // independent global loads in flight per thread
 
-// One CTA per request.  Shared memory holds the union bitmap over the
-// history, the per-word prefix counts, the protected-slot bitmap, two B-entry
-// slot lists and the location of every union row.
-__global__ void __launch_bounds__(kUnionThreads)
+__host__ __device__ static inline int union_slice(int64_t s_max) {
+  return (int)((((s_max + kUnionCluster - 1) / kUnionCluster) + 31) & ~31);
+}
+
+// Slices of up to this many rows also keep their hot and optional map entries
+// in shared memory, fetched while the bitmap is built.
+constexpr int kMapPrefetchRows = 8192;
+
+size_t union_smem_bytes(const DevCtx &c) {
+  const int slice = union_slice(c.Sm);
+  const size_t sw = (size_t)slice / 32;  // words of one slice
+  const size_t pw = (size_t)((c.B + 31) / 32);
+  const size_t maps = slice <= kMapPrefetchRows ? (size_t)slice * 8 : 0;
+  return sw * 8 + pw * 8 + (size_t)c.B * 16 + (size_t)c.Kmax * c.k * 4 + maps;
+}
+
+__global__ void __cluster_dims__(kUnionCluster, 1, 1) __launch_bounds__(kUnionThreads)
 k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restrict__ loc_out,
               int shared, int tick) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
-  __shared__ int sh_cnt[4];  // ring, opt, hot hits; selections
-  __shared__ int sh_missel, sh_evict;
-  const int r = blockIdx.x;
+  __shared__ int sh_cnt[6];  // ring, opt, hot hits, selections, miss selections, evictions
+  __shared__ int sh_u, sh_m, sh_p;  // this CTA's union rows and misses; the leader's P
+  const int crank = (int)cl.block_rank();
+  const int r = blockIdx.x / kUnionCluster;
   const int Kr = c.Kr[r];
-  if (Kr == 0) return;
+  if (Kr == 0) return;  // the whole cluster leaves together
   const int tid = threadIdx.x, bs = blockDim.x;
   const int64_t n = c.n[r];
   const int k = c.k, KK = c.Kmax * k, B = c.B;
-  const int nw_cap = (int)((c.Sm + 31) / 32);
-  const int nw = (int)((n + 31) >> 5);
+  const int slice = union_slice(c.Sm);
+  const int sw = slice / 32;
   const int pw = (B + 31) >> 5;
+  const int64_t row_lo = (int64_t)crank * slice;
+  const int64_t row_hi = min(n, row_lo + slice);
+  const int nw = row_hi > row_lo ? (int)((row_hi - row_lo + 31) >> 5) : 0;
   uint32_t *bm = reinterpret_cast<uint32_t *>(smem);
-  uint32_t *wp = bm + nw_cap;
-  uint32_t *prot = wp + nw_cap;
-  int32_t *candB = reinterpret_cast<int32_t *>(prot + pw);
+  uint32_t *wp = bm + sw;
+  uint32_t *prot = wp + sw;  // leader: protected slots
+  uint32_t *now = prot + pw;  // leader: slots stamped by this tick
+  int32_t *candB = reinterpret_cast<int32_t *>(now + pw);
   int32_t *tmpB = candB + B;
-  int32_t *ul = tmpB + B;  // location of union row q
+  int32_t *lru_s = tmpB + B;   // leader: LRU order at the start of the call
+  int32_t *hrow_s = lru_s + B;  // leader: row held by each slot at the start
+  int32_t *ul = hrow_s + B;     // location of each union row of this slice
+  const bool pf = slice <= kMapPrefetchRows;
+  int32_t *hmap_s = ul + KK;     // this slice's hot-map entries (when pf)
+  int32_t *omap_s = hmap_s + slice;
+  uint32_t *prot0 = cl.map_shared_rank(prot, 0);
+  uint32_t *now0 = cl.map_shared_rank(now, 0);
 
   const int32_t *tk = topk + (size_t)r * KK;
   int32_t *uni = c.uni + (size_t)r * KK;
@@ -92,14 +122,28 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   const int64_t ring_lo = max(c.ring_first[r], n - (int64_t)c.W);
   const int nsel = Kr * k;
 
-  // 1. union bitmap over the history rows
-  for (int i = tid; i < nw; i += bs) bm[i] = 0;
-  for (int i = tid; i < pw; i += bs) prot[i] = 0;
-  if (tid < 4) sh_cnt[tid] = 0;
-  if (tid == 0) {
-    sh_missel = 0;
-    sh_evict = 0;
+  // 0. start fetching what the later phases read: this slice's map entries,
+  //    and for the leader the LRU order and the rows of the slots
+  const bool any_opt = c.opt_count[r] > 0;
+  if (pf) {
+    for (int i = tid; i < row_hi - row_lo; i += bs) {
+      cp_async_4(&hmap_s[i], &hot_map[row_lo + i]);
+      if (any_opt) cp_async_4(&omap_s[i], &opt_map[row_lo + i]);
+    }
   }
+  if (crank == 0) {
+    for (int i = tid; i < B; i += bs) {
+      cp_async_4(&lru_s[i], &lru[i]);
+      cp_async_4(&hrow_s[i], &hot_row[i]);
+    }
+  }
+  cp_async_commit();
+
+  // 1. union bitmap of this CTA's slice
+  for (int i = tid; i < sw; i += bs) bm[i] = 0;
+  if (crank == 0)
+    for (int i = tid; i < 2 * pw; i += bs) prot[i] = 0;  // prot and now
+  if (tid < 6) sh_cnt[tid] = 0;
   __syncthreads();
   for (int e0 = tid; e0 < nsel; e0 += kBatch * bs) {
     int32_t sv[kBatch];
@@ -111,24 +155,32 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int32_t s = sv[i];
-      if (s >= 0 && s < n) atomicOr(&bm[s >> 5], 1u << (s & 31));
-      else if (s != -1) record_error(c.err, DC_ROW_RANGE, K_UNION_PROBE);
+      if (s >= row_lo && s < row_hi) {
+        const int rel = (int)(s - row_lo);
+        atomicOr(&bm[rel >> 5], 1u << (rel & 31));
+      } else if (crank == 0 && s != -1 && (s < 0 || s >= n)) {
+        record_error(c.err, DC_ROW_RANGE, K_UNION_PROBE);
+      }
     }
   }
-  __syncthreads();
+  cl.sync();  // the leader's bitmaps are cleared before anyone marks them
 
-  // 2. ascending compaction; each thread owns a contiguous run of words
+  // 2. ascending compaction of the slice; each thread owns a run of words
   const int per = (nw + bs - 1) / bs;
   const int w0 = min(nw, tid * per), w1 = min(nw, w0 + per);
   int cnt = 0;
   for (int w = w0; w < w1; ++w) cnt += __popc(bm[w]);
-  int U;
-  const int u_base = ublock_excl_scan(cnt, warp_sums, U);
+  int Uc;
+  const int u_local = ublock_excl_scan(cnt, warp_sums, Uc);
 
-  // 3. probe each union row: live ring tail, optional map, hot cache, else miss
+  cp_async_wait_all();
+  __syncthreads();
+
+  // 3. probe each union row of the slice: live ring tail, optional map, hot
+  //    cache, else miss; hot rows of the union are protected in the leader
   int misses_here = 0, ring_h = 0, opt_h = 0, hot_h = 0;
   {
-    int q = u_base;
+    int q = u_local;
     int w = w0;
     uint32_t bits = 0;
     if (w < w1) {
@@ -147,7 +199,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
           }
         }
         if (bits) {
-          ub[i] = (w << 5) | (__ffs(bits) - 1);
+          ub[i] = (int32_t)(row_lo + ((w << 5) | (__ffs(bits) - 1)));
           bits &= bits - 1;
           nb = i + 1;
         } else {
@@ -157,15 +209,22 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       int32_t hm[kBatch], om[kBatch];
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
-        hm[i] = ub[i] >= 0 ? hot_map[ub[i]] : -1;
-        om[i] = ub[i] >= 0 ? opt_map[ub[i]] : -1;
+        if (ub[i] < 0) {
+          hm[i] = om[i] = -1;
+        } else if (pf) {
+          hm[i] = hmap_s[ub[i] - row_lo];
+          om[i] = any_opt ? omap_s[ub[i] - row_lo] : -1;
+        } else {
+          hm[i] = hot_map[ub[i]];
+          om[i] = any_opt ? opt_map[ub[i]] : -1;
+        }
       }
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
         const int32_t u = ub[i];
         if (u < 0) continue;
         const int32_t hs = hm[i];
-        if (hs >= 0) atomicOr(&prot[hs >> 5], 1u << (hs & 31));  // selected rows are protected
+        if (hs >= 0) atomicOr(&prot0[hs >> 5], 1u << (hs & 31));
         int32_t l;
         if (u >= ring_lo && u < n) {
           l = make_loc(DHS_LOC_RING, (int)(u % c.Rd));
@@ -176,12 +235,12 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
         } else if (hs >= 0) {
           l = make_loc(DHS_LOC_HOT, hs);
           hot_stamp[hs] = tick;
+          atomicOr(&now0[hs >> 5], 1u << (hs & 31));
           ++hot_h;
         } else {
-          l = kMissMark - u;  // a miss, row kept until its rank is known
+          l = kMissMark;
           ++misses_here;
         }
-        uni[q] = u;
         ul[q] = l;
         ++q;
       }
@@ -191,149 +250,177 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   atomicAdd(&sh_cnt[0], ring_h);
   atomicAdd(&sh_cnt[1], opt_h);
   atomicAdd(&sh_cnt[2], hot_h);
-  int M;
-  const int m_base = ublock_excl_scan(misses_here, warp_sums, M);
-  if (misses_here) {
-    int m = m_base;
-    for (int q = u_base; q < u_base + cnt; ++q) {
-      const int32_t l = ul[q];
-      if (l <= kMissMark) {
-        miss[m] = kMissMark - l;
-        ul[q] = make_loc(DHS_LOC_STAGE, m);
-        ++m;
+  int Mc;
+  const int m_local = ublock_excl_scan(misses_here, warp_sums, Mc);
+  if (tid == 0) {
+    sh_u = Uc;
+    sh_m = Mc;
+  }
+  cl.sync();  // S1: counts published, protected and stamped slots complete
+
+  int u_base = 0, m_base = 0, U = 0, M = 0, hits = 0;
+#pragma unroll
+  for (int qr = 0; qr < kUnionCluster; ++qr) {
+    const int uq = *cl.map_shared_rank(&sh_u, qr), mq = *cl.map_shared_rank(&sh_m, qr);
+    if (qr < crank) {
+      u_base += uq;
+      m_base += mq;
+    }
+    U += uq;
+    M += mq;
+    if (crank == 0) hits += *cl.map_shared_rank(&sh_cnt[2], qr);
+  }
+  // union rows and misses of the slice get their request-wide ranks
+  {
+    int q = u_local, m = m_local;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t bits = bm[w];
+      while (bits) {
+        const int32_t u = (int32_t)(row_lo + ((w << 5) | (__ffs(bits) - 1)));
+        bits &= bits - 1;
+        uni[u_base + q] = u;
+        if (ul[q] == kMissMark) {
+          miss[m_base + m] = u;
+          c.first_occ[(size_t)r * KK + m_base + m] = INT_MAX;
+          ul[q] = make_loc(DHS_LOC_STAGE, m_base + m);
+          ++m;
+        }
+        ++q;
       }
     }
   }
-  for (int i = tid; i < M; i += bs) c.first_occ[(size_t)r * KK + i] = INT_MAX;
-  __syncthreads();
-  const int hits = sh_cnt[2];
 
-  // 4. victims: unprotected slots in LRU order (stamp, slot), empty slots first
-  int P = 0;
+  // 4. victims (leader): unprotected slots in LRU order (stamp, slot), empty first
   const int perB = (B + bs - 1) / bs;
   const int b0 = min(B, tid * perB), b1 = min(B, b0 + perB);
-  if (M > 0) {
-    int nc = 0;
+  if (crank == 0) {
+    int P = 0;
+    if (M > 0) {
+      int nc = 0;
 #pragma unroll 4
-    for (int i = b0; i < b1; ++i) {
-      const int v = lru[i];
-      nc += !((prot[v >> 5] >> (v & 31)) & 1u);
-    }
-    int ncand;
-    int cb = ublock_excl_scan(nc, warp_sums, ncand);
-    for (int i = b0; i < b1; ++i) {
-      const int v = lru[i];
-      if (!((prot[v >> 5] >> (v & 31)) & 1u)) candB[cb++] = v;
-    }
-    __syncthreads();
-    P = min(M, ncand);
-    int ev = 0;
-    for (int p0 = tid; p0 < P; p0 += kBatch * bs) {
-      int vv[kBatch], old[kBatch], uu[kBatch];
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int p = p0 + i * bs;
-        vv[i] = p < P ? candB[p] : -1;
-        old[i] = vv[i] >= 0 ? hot_row[vv[i]] : -1;
-        uu[i] = p < P ? miss[p] : -1;
+      for (int i = b0; i < b1; ++i) {
+        const int v = lru_s[i];
+        nc += !((prot[v >> 5] >> (v & 31)) & 1u);
       }
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int p = p0 + i * bs;
-        if (vv[i] < 0) continue;
-        if (old[i] >= 0) {
-          hot_map[old[i]] = -1;
-          ++ev;
+      int ncand;
+      int cb = ublock_excl_scan(nc, warp_sums, ncand);
+      P = min(M, ncand);
+      for (int i = b0; i < b1; ++i) {
+        const int v = lru_s[i];
+        if (!((prot[v >> 5] >> (v & 31)) & 1u)) {
+          candB[cb] = v;
+          if (cb < P) atomicOr(&now[v >> 5], 1u << (v & 31));  // stamped by this tick
+          ++cb;
         }
-        hot_row[vv[i]] = uu[i];
-        hot_stamp[vv[i]] = tick;
-        hot_map[uu[i]] = vv[i];
-        c.promo_dst[(size_t)r * B + p] = vv[i];
-        c.promo_src[(size_t)r * B + p] = p;
       }
     }
-    if (ev) atomicAdd(&sh_evict, ev);
-    __syncthreads();
+    if (tid == 0) sh_p = P;
   }
-
-  // 5. LRU order after this tick: untouched slots keep their order, slots
-  //    stamped now follow in ascending slot order
-  if (hits + P > 0) {
-    int na = 0, nb = 0;
-#pragma unroll 4
-    for (int i = b0; i < b1; ++i) {
-      const int v = lru[i];
-      const bool now = hot_stamp[v] == tick;
-      na += !now;
-      tmpB[i] = now ? -1 : v;  // scratch: this thread's positions only
+  cl.sync();  // S2: every slice's misses are in the miss list; no CTA reads the
+              // leader's memory after this point
+  int P = 0;
+  if (crank == 0) {
+    P = sh_p;
+    // promotions: the first P misses take the victims, in order
+    int ev = 0;
+    for (int p = tid; p < P; p += bs) {
+      const int v = candB[p];
+      const int32_t old = hrow_s[v];
+      const int32_t u = miss[p];
+      if (old >= 0) {
+        hot_map[old] = -1;
+        ++ev;
+      }
+      hot_row[v] = u;
+      hot_stamp[v] = tick;
+      hot_map[u] = v;
+      c.promo_dst[(size_t)r * B + p] = v;
+      c.promo_src[(size_t)r * B + p] = p;
     }
-#pragma unroll 4
-    for (int v = b0; v < b1; ++v) nb += hot_stamp[v] == tick;
-    int A, Bt;
-    int ab = ublock_excl_scan(na, warp_sums, A);
-    int bb = ublock_excl_scan(nb, warp_sums, Bt);
-    for (int i = b0; i < b1; ++i)
-      if (tmpB[i] >= 0) candB[ab++] = tmpB[i];
-    for (int v = b0; v < b1; ++v)
-      if (hot_stamp[v] == tick) candB[A + bb++] = v;
-    __syncthreads();
-    for (int i = tid; i < B; i += bs) lru[i] = candB[i];
+    if (ev) atomicAdd(&sh_cnt[5], ev);
+    // 5. LRU order after this tick: untouched slots keep their order, slots
+    //    stamped now follow in ascending slot order
+    if (hits + P > 0) {
+      int na = 0, nb = 0;
+      for (int i = b0; i < b1; ++i) {
+        const int v = lru_s[i];
+        const bool nw_ = (now[v >> 5] >> (v & 31)) & 1u;
+        na += !nw_;
+        tmpB[i] = nw_ ? -1 : v;
+      }
+      for (int v = b0; v < b1; ++v) nb += (now[v >> 5] >> (v & 31)) & 1u;
+      int A, Bt;
+      int ab = ublock_excl_scan(na, warp_sums, A);
+      int bb = ublock_excl_scan(nb, warp_sums, Bt);
+      for (int i = b0; i < b1; ++i)
+        if (tmpB[i] >= 0) lru[ab++] = tmpB[i];
+      for (int v = b0; v < b1; ++v)
+        if ((now[v >> 5] >> (v & 31)) & 1u) lru[A + bb++] = v;
+    }
   }
 
-  // 6. one location per selected entry, in each query's selection order
+  // 6. one location per selected entry whose row lies in this slice
   int sel_here = 0, missel = 0;
   for (int e0 = tid; e0 < nsel; e0 += kBatch * bs) {
     int32_t sv[kBatch];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int e = e0 + i * bs;
-      sv[i] = e < nsel ? tk[e] : -2;
+      sv[i] = e < nsel ? tk[e] : -1;
     }
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int e = e0 + i * bs;
+      if (e >= nsel) continue;
       const int32_t s = sv[i];
-      if (s == -2) continue;
-      int32_t l = -1;
-      if (s >= 0 && s < n) {
-        const uint32_t word = bm[s >> 5];
-        const int q = wp[s >> 5] + __popc(word & ((1u << (s & 31)) - 1u));
-        l = ul[q];
-        ++sel_here;
-        if (loc_tier(l) == DHS_LOC_STAGE) {
-          ++missel;
-          if (!shared) {
-            atomicMin(&c.first_occ[(size_t)r * KK + loc_index(l)], e);
-            l = make_loc(DHS_LOC_STAGE, e);
-          }
+      const bool mine = s >= row_lo && s < row_hi;
+      if (!mine) {
+        if (crank == 0 && (s < 0 || s >= n)) loc_out[(size_t)r * KK + e] = -1;
+        continue;
+      }
+      const int rel = (int)(s - row_lo);
+      const uint32_t word = bm[rel >> 5];
+      const int q = wp[rel >> 5] + __popc(word & ((1u << (rel & 31)) - 1u));
+      int32_t l = ul[q];
+      ++sel_here;
+      if (loc_tier(l) == DHS_LOC_STAGE) {
+        ++missel;
+        if (!shared) {
+          atomicMin(&c.first_occ[(size_t)r * KK + loc_index(l)], e);
+          l = make_loc(DHS_LOC_STAGE, e);
         }
       }
       loc_out[(size_t)r * KK + e] = l;
     }
   }
   atomicAdd(&sh_cnt[3], sel_here);
-  atomicAdd(&sh_missel, missel);
-  __syncthreads();
+  atomicAdd(&sh_cnt[4], missel);
   if (!shared) {
-    for (int p = tid; p < P; p += bs)
-      c.promo_src[(size_t)r * B + p] = c.first_occ[(size_t)r * KK + p];
+    cl.sync();  // every first selection of a miss is known
+    if (crank == 0)
+      for (int p = tid; p < P; p += bs)
+        c.promo_src[(size_t)r * B + p] = c.first_occ[(size_t)r * KK + p];
   }
+  __syncthreads();
   if (tid == 0) {
-    c.counts[r * 4 + 0] = U;
-    c.counts[r * 4 + 1] = M;
-    c.counts[r * 4 + 2] = P;
-    c.counts[r * 4 + 3] = hits;
     atomicAdd(&c.stats[ST_SEL], (unsigned long long)sh_cnt[3]);
-    atomicAdd(&c.stats[ST_UNION], (unsigned long long)U);
     atomicAdd(&c.stats[ST_RING], (unsigned long long)sh_cnt[0]);
     atomicAdd(&c.stats[ST_OPT], (unsigned long long)sh_cnt[1]);
-    atomicAdd(&c.stats[ST_HOT], (unsigned long long)hits);
-    atomicAdd(&c.stats[ST_MISS], (unsigned long long)M);
-    atomicAdd(&c.stats[ST_MISS_SEL], (unsigned long long)sh_missel);
-    atomicAdd(&c.stats[ST_FETCHED], (unsigned long long)(shared ? M : sh_missel));
-    atomicAdd(&c.stats[ST_INSTALL], (unsigned long long)P);
-    if (sh_evict) atomicAdd(&c.stats[ST_EVICT], (unsigned long long)sh_evict);
-    if (M == 0 && hits == 0) atomicAdd(&c.stats[ST_DIRECT], 1ull);
+    atomicAdd(&c.stats[ST_HOT], (unsigned long long)sh_cnt[2]);
+    atomicAdd(&c.stats[ST_MISS_SEL], (unsigned long long)sh_cnt[4]);
+    if (sh_cnt[5]) atomicAdd(&c.stats[ST_EVICT], (unsigned long long)sh_cnt[5]);
+    if (!shared) atomicAdd(&c.stats[ST_FETCHED], (unsigned long long)sh_cnt[4]);
+    if (crank == 0) {
+      c.counts[r * 4 + 0] = U;
+      c.counts[r * 4 + 1] = M;
+      c.counts[r * 4 + 2] = P;
+      c.counts[r * 4 + 3] = hits;
+      atomicAdd(&c.stats[ST_UNION], (unsigned long long)U);
+      atomicAdd(&c.stats[ST_MISS], (unsigned long long)M);
+      if (shared) atomicAdd(&c.stats[ST_FETCHED], (unsigned long long)M);
+      atomicAdd(&c.stats[ST_INSTALL], (unsigned long long)P);
+      if (M == 0 && hits == 0) atomicAdd(&c.stats[ST_DIRECT], 1ull);
+    }
   }
 }
 
@@ -408,13 +495,19 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
   cudaError_t e = ensure_smem(k_union_probe, union_smem_bytes(c), granted);
   if (e != cudaSuccess) return e;
   if (tm) tm->begin(K_UNION_PROBE, s);
-  k_union_probe<<<c.N, kUnionThreads, union_smem_bytes(c), s>>>(c, topk, loc_out, shared, tick);
+  k_union_probe<<<c.N * kUnionCluster, kUnionThreads, union_smem_bytes(c), s>>>(c, topk, loc_out,
+                                                                               shared, tick);
   if (tm) tm->end(K_UNION_PROBE, s);
   // enough warps in flight to cover the host link's bandwidth-delay product
   int blocks_per_req = (152 * 8 + c.N - 1) / c.N;
   if (blocks_per_req < 1) blocks_per_req = 1;
   dim3 grid(blocks_per_req, c.N);
   if (tm) tm->begin(K_GATHER, s);
+  static bool carve_k_gather = false;
+  if (!carve_k_gather) {
+    same_carveout(k_gather);
+    carve_k_gather = true;
+  }
   k_gather<<<grid, kGatherWarps * 32, 0, s>>>(c, topk, loc_out, shared);
   if (tm) tm->end(K_GATHER, s);
   return cudaGetLastError();

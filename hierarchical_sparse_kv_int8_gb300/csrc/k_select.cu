@@ -22,6 +22,11 @@ __global__ void k_upload(int32_t *dst, int n, const __grid_constant__ UploadWord
 cudaError_t launch_upload(int32_t *dst, const int32_t *words, int n, cudaStream_t s) {
   UploadWords w;
   for (int i = 0; i < n; ++i) w.w[i] = words[i];
+  static bool carve_k_upload = false;
+  if (!carve_k_upload) {
+    same_carveout(k_upload);
+    carve_k_upload = true;
+  }
   k_upload<<<(n + 255) / 256, 256, 0, s>>>(dst, n, w);
   return cudaGetLastError();
 }
@@ -556,6 +561,11 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_ou
     UploadWords w;
     const int n = c.N + c.N * c.Kmax;
     for (int i = 0; i < n; ++i) w.w[i] = ctl_words[i];
+    static bool carve_k_select_prep = false;
+    if (!carve_k_select_prep) {
+      same_carveout(k_select_prep);
+      carve_k_select_prep = true;
+    }
     k_select_prep<<<(c.N * c.Kmax + 255) / 256, 256, 0, s>>>(c, w);
   }
   if (max_dom > 0) {

@@ -23,6 +23,12 @@ __device__ __forceinline__ void cp_async_16_zfill(void *smem_dst, const void *gm
                "l"(gmem_src), "r"(src_bytes));
 }
 
+// 4-byte global->shared copy (for arrays without 16-byte alignment).
+__device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(smem_dst)),
+               "l"(gmem_src));
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::); }
 template <int N>
