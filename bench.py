@@ -393,6 +393,9 @@ def run_native(args):
         if byts is None:
             continue
         avg_ms = t_l / n_l
+        if name == "attn" and "attn_staged" in per:
+            # attention runs as two launches (resident rows, then staged rows)
+            avg_ms += per["attn_staged"][1] / per["attn_staged"][0]
         ach = byts / (avg_ms * 1e-3) / 1e9
         link = name == "gather"
         peak = h2d_peak if link else hbm_peak
@@ -403,7 +406,8 @@ def run_native(args):
                        "peak_source": ("host link: pinned host-to-device copy measured in this run"
                                        if link else hbm_src)}
     roof = roofs.get(dom)
-    fam_t = sum(per[k][1] / per[k][0] for k in ("index_score", "topk", "attn") if k in per)
+    fam_t = sum(per[k][1] / per[k][0] for k in ("index_score", "topk", "attn", "attn_staged")
+                if k in per)
     fam_b = ab["select"] + ab["attn"]
     families = {
         "select+attend": {"achieved": round(fam_b / (fam_t * 1e-3) / 1e9, 1), "unit": "GB/s",
