@@ -202,9 +202,10 @@ def algorithmic_bytes(rec, counts, k_per_req):
     locations.  Per kernel: index_score reads keys and queries; topk reads the
     int32 scores and writes the lists; union_probe reads the lists and two
     row maps per union row and writes locations and the union and miss lists;
-    gather moves the distinct missing rows over the host link; attn is the
-    attend family; post_attend copies block rows into the ring and promoted
-    rows into the hot cache (read + write); commit copies accepted rows.
+    gather moves the distinct missing rows over the host link (their writes
+    to staging and to promoted hot slots are HBM-side); attn is the attend
+    family plus the block rows it writes into the draft ring; commit copies
+    accepted rows.
     """
     K = int(k_per_req.max())
     n_act = int((k_per_req > 0).sum())
@@ -215,7 +216,6 @@ def algorithmic_bytes(rec, counts, k_per_req):
     select = keys + qbytes + lists
     U = int(counts[:, 0].sum())
     M = int(counts[:, 1].sum())
-    P = int(counts[:, 2].sum())
     attend = U * rb + n_act * K * rb + 2 * n_act * K * rec.Hq * (rec.qk_dim + rec.v_dim) \
         + lists
     kernel = {
@@ -223,8 +223,7 @@ def algorithmic_bytes(rec, counts, k_per_req):
         "topk": 4 * n_act * K * rec.S + lists,
         "union_probe": 2 * lists + 8 * U + 4 * (U + M),
         "gather": M * rb,
-        "attn": attend,
-        "post_attend": 2 * (n_act * K + P) * rb,
+        "attn": attend + n_act * K * rb,
     }
     return {"select": select, "attn": attend, "gather": M * rb, "union": U, "misses": M,
             "kernel_bytes": kernel}
@@ -393,9 +392,6 @@ def run_native(args):
         if byts is None:
             continue
         avg_ms = t_l / n_l
-        if name == "attn" and "attn_staged" in per:
-            # attention runs as two launches (resident rows, then staged rows)
-            avg_ms += per["attn_staged"][1] / per["attn_staged"][0]
         ach = byts / (avg_ms * 1e-3) / 1e9
         link = name == "gather"
         peak = h2d_peak if link else hbm_peak
@@ -406,7 +402,7 @@ def run_native(args):
                        "peak_source": ("host link: pinned host-to-device copy measured in this run"
                                        if link else hbm_src)}
     roof = roofs.get(dom)
-    fam_t = sum(per[k][1] / per[k][0] for k in ("index_score", "topk", "attn", "attn_staged")
+    fam_t = sum(per[k][1] / per[k][0] for k in ("index_score", "topk", "attn")
                 if k in per)
     fam_b = ab["select"] + ab["attn"]
     families = {

@@ -14,8 +14,7 @@ namespace dhs {
 
 const char *const kKernelNames[K_COUNT] = {
     "upload",         "index_score",     "topk",          "union_probe",
-    "gather",         "attn",            "merge",         "post_attend",
-    "commit",         "residency_clear", "residency_fill", "residency_publish",
+    "gather",         "attn",            "commit",         "residency_clear", "residency_fill", "residency_publish",
     "bind_reset"};
 
 // ---------------------------------------------------------------- Timer
@@ -304,6 +303,11 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   d.opt_max = g.opt_rows_max;
   const float scale = g.softmax_scale > 0.f ? g.softmax_scale : 1.0f / sqrtf((float)g.qk_dim);
   d.scale_log2 = scale * 1.4426950408889634f;
+  if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess ||
+      d.sms < 1) {
+    cudaGetLastError();
+    d.sms = 1;
+  }
   if (union_smem_bytes(d) > kMaxDynSmem) {
     delete c;
     return DHS_ERR_CAPACITY;
@@ -342,8 +346,8 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   ALLOC(d.miss, N * KK);
   ALLOC(d.first_occ, N * KK);
   ALLOC(d.counts, N * 4);
-  ALLOC(d.promo_src, N * B);
   ALLOC(d.promo_dst, N * B);
+  ALLOC(d.inst, N * KK);
   const size_t pf = attn_partial_floats(d, c->n_split);
   ALLOC(d.part_o, c->n_split > 1 ? pf : 1);
   ALLOC(d.part_ml, c->n_split > 1 ? N * d.Kmax * d.Hq * c->n_split * 2 : 1);
@@ -373,6 +377,15 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   if (e == cudaSuccess) e = cudaMemset(d.err, 0, 8);
   if (e == cudaSuccess) e = cudaMemset(d.counts, 0, N * 16);
   if (e == cudaSuccess) e = cudaMemset(d.ticket, 0, N * d.Kmax * d.Hkv * 4);
+  if (e == cudaSuccess) {
+    // score ranges start empty; top-k empties each range again after reading it
+    std::vector<int32_t> mm((size_t)N * d.Kmax * 2);
+    for (size_t i = 0; i < mm.size(); i += 2) {
+      mm[i] = INT32_MAX;
+      mm[i + 1] = INT32_MIN;
+    }
+    e = cudaMemcpy(d.minmax, mm.data(), mm.size() * 4, cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) e = cudaMemset(d.opt_count, 0, N * 8);
   if (e == cudaSuccess) e = cudaMemset(pool, 0, pool_rows * R * 2);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();

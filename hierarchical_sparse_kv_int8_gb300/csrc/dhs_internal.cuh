@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
 #include <vector>
 
 #include "../../include/dhs.h"
@@ -24,8 +25,6 @@ enum KernelId {
   K_UNION_PROBE,
   K_GATHER,
   K_ATTN,
-  K_MERGE,
-  K_POST_ATTEND,
   K_COMMIT,
   K_RESIDENCY_CLEAR,
   K_RESIDENCY_FILL,
@@ -54,6 +53,7 @@ struct DevCtx {
   int W, p, Rd;
   int64_t opt_max;
   float scale_log2;      // softmax scale * log2(e)
+  int sms;               // streaming multiprocessors of the device
 
   // per-slot binding
   const int8_t *const *keys;     // [N] device index keys
@@ -82,8 +82,9 @@ struct DevCtx {
   int32_t *miss;        // [N][Kmax*k]
   int32_t *first_occ;   // [N][Kmax*k]
   int32_t *counts;      // [N][4]
-  int32_t *promo_src;   // [N][B]
-  int32_t *promo_dst;   // [N][B]
+  int32_t *promo_dst;   // [N][B]: hot slot taken by miss p (p < P)
+  int32_t *inst;        // [N][Kmax*k] per-query mode: hot slot a staged entry
+                        // also fills, else -1 (written for staged entries only)
   int32_t *topk_last;   // [N][Kmax][k] selection seen by the last resolve
   float *part_o;        // attention partials [N][Kmax][Hq][n_split][dv]
   float *part_ml;       // [N][Kmax][Hq][n_split][2]: max (log2 units), sum
@@ -148,6 +149,27 @@ cudaError_t ensure_smem(F *func, size_t bytes, size_t &granted) {
 }
 constexpr size_t kMaxDynSmem = 226 * 1024;  // leaves room for static shared memory
 
+// Launch with programmatic stream serialization: the kernel's CTAs may be
+// placed while the preceding launch on the stream finishes; the kernel orders
+// itself after it with pdl_wait().  Kernels launched this way call
+// pdl_trigger() only after pdl_wait(), so when one starts, every launch before
+// its immediate predecessor has completed.
+template <typename... P, typename... A>
+cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       A &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
+}
+
 // Words uploaded by k_upload (kernel parameter, <= 16 KB).
 struct UploadWords {
   int32_t w[kUploadWords];
@@ -162,8 +184,6 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
 cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *block,
                           const int32_t *loc, uint16_t *out, float *lse, int n_split,
                           cudaStream_t s, class Timer *tm);
-cudaError_t launch_post_attend(const DevCtx &c, const uint16_t *block, cudaStream_t s,
-                               class Timer *tm);
 cudaError_t launch_commit(const DevCtx &c, const int32_t *aux_words, cudaStream_t s,
                           class Timer *tm);
 cudaError_t launch_residency(const DevCtx &c, int slot, int64_t old_count, int64_t new_count,

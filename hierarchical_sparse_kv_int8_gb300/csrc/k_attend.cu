@@ -1,71 +1,19 @@
-// Step 5 of the verification round and the state updates around it.
+// State updates around the verification round: commit, residency, binding.
 //
-// "Adaptive DHiSparse", eq. (1) and (5): query j of request r attends over its
-// own ordered selection S_{r,j} (through the locations of eq. (11)-(12)) and
-// the block rows n_r .. n_r + j read from the tail.  Section 3.4: promoted rows
-// are copied from staging to their stable hot-cache addresses after the
-// attention readers.  Eq. (7), (9), (10): block rows live in a draft ring at
-// phi(r, t) = r R_d + (t mod R_d); commit keeps the accepted prefix.
-//
-// The attention kernel itself is in k_attn.cu; this file holds the state
-// updates around it.
+// "Adaptive DHiSparse", eq. (7), (9), (10): block rows live in a draft ring at
+// phi(r, t) = r R_d + (t mod R_d) (written by the attention launch, k_attn.cu);
+// commit keeps the accepted prefix.  This file holds commit and the residency
+// and binding updates between rounds.
 #include "dhs_internal.cuh"
 #include "ptx_util.cuh"
 
 namespace dhs {
 
-// After attention: block rows into the draft ring at phi(r, n_r + u), and
-// promoted rows from staging into their hot-cache slots.  One warp per row.
-__global__ void __launch_bounds__(256)
-k_post_attend(const DevCtx c, const uint16_t *__restrict__ block) {
-  const int r = blockIdx.y;
-  const int Kr = c.Kr[r];
-  if (Kr == 0) return;
-  const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), nwt = gridDim.x * 8;
-  const int P = c.counts[r * 4 + 2];
-  const int64_t n = c.n[r];
-  const int nv = (c.row * 2) >> 4;
-  const int KK = c.Kmax * c.k;
-  for (int job = gw; job < Kr + P; job += nwt) {
-    const uint4 *src;
-    uint4 *dst;
-    if (job < Kr) {
-      src = reinterpret_cast<const uint4 *>(block + ((size_t)r * c.Kmax + job) * c.row);
-      dst = reinterpret_cast<uint4 *>(c.ring + ((size_t)r * c.Rd + (n + job) % c.Rd) * c.row);
-    } else {
-      const int p = job - Kr;
-      const int sidx = c.promo_src[(size_t)r * c.B + p];
-      const int slot = c.promo_dst[(size_t)r * c.B + p];
-      if (sidx < 0 || sidx >= KK || slot < 0 || slot >= c.B) {
-        if (lane == 0) record_error(c.err, DC_CAPACITY, K_POST_ATTEND);
-        continue;
-      }
-      src = reinterpret_cast<const uint4 *>(c.stage + ((size_t)r * KK + sidx) * c.row);
-      dst = reinterpret_cast<uint4 *>(c.hot_data + ((size_t)r * c.B + slot) * c.row);
-    }
-    for (int v = lane; v < nv; v += 32) dst[v] = src[v];
-  }
-}
-
-
-cudaError_t launch_post_attend(const DevCtx &c, const uint16_t *block, cudaStream_t s, Timer *tm) {
-  int bpr = (152 * 4 + c.N - 1) / c.N;
-  if (bpr > 64) bpr = 64;
-  if (tm) tm->begin(K_POST_ATTEND, s);
-  static bool carve_k_post_attend = false;
-  if (!carve_k_post_attend) {
-    same_carveout(k_post_attend);
-    carve_k_post_attend = true;
-  }
-  k_post_attend<<<dim3(bpr, c.N), 256, 0, s>>>(c, block);
-  if (tm) tm->end(K_POST_ATTEND, s);
-  return cudaGetLastError();
-}
-
 // ---------------------------------------------------------------- commit
 // aux[r*4 + 0] = a_r, aux[r*4 + 1..2] = n_r before the commit (lo, hi words).
 __global__ void __launch_bounds__(256) k_commit(const DevCtx c, const __grid_constant__ UploadWords aux) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.y;
   const int a = aux.w[r * 4 + 0];
   const int64_t n_old = (int64_t)(uint32_t)aux.w[r * 4 + 1] | ((int64_t)aux.w[r * 4 + 2] << 32);
@@ -88,15 +36,15 @@ __global__ void __launch_bounds__(256) k_commit(const DevCtx c, const __grid_con
 cudaError_t launch_commit(const DevCtx &c, const int32_t *aux_words, cudaStream_t s, Timer *tm) {
   UploadWords aux;
   for (int i = 0; i < c.N * 4; ++i) aux.w[i] = aux_words[i];
-  if (tm) tm->begin(K_COMMIT, s);
   static bool carve_k_commit = false;
   if (!carve_k_commit) {
     same_carveout(k_commit);
     carve_k_commit = true;
   }
-  k_commit<<<dim3(1, c.N), 256, 0, s>>>(c, aux);
+  if (tm) tm->begin(K_COMMIT, s);
+  cudaError_t e = launch_pdl(k_commit, dim3(1, c.N), dim3(256), 0, s, c, aux);
   if (tm) tm->end(K_COMMIT, s);
-  return cudaGetLastError();
+  return e;
 }
 
 // ---------------------------------------------------------------- residency

@@ -18,7 +18,9 @@
 //     shared memory) and a quarter of the value dims.
 // Splits of one item are merged by the CTA that finishes last (a per-item
 // ticket taken with one atomic after the partial is written and fenced), so
-// no separate merge launch and no device-side waiting are needed.
+// no separate merge launch and no device-side waiting are needed.  The first
+// split of each (request, query) also writes that query's block row into the
+// draft ring (eq. (9)-(10)), so no launch follows attention before commit.
 #include "dhs_internal.cuh"
 #include "ptx_util.cuh"
 
@@ -54,7 +56,7 @@ int attn_splits(const DevCtx &c, int active_queries) {
   (void)active_queries;
   const int rows = c.k + c.Kmax;
   const int gran = attn_rows_per_tile_group(c);
-  const int target = 152 * 2;
+  const int target = c.sms * 2;
   const int items = c.N * c.Kmax * c.Hkv;
   int ns = (target + items - 1) / items;
   const int max_ns = (rows + gran - 1) / gran;
@@ -100,7 +102,10 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   __shared__ int sh_last;
   const int split = blockIdx.x, j = blockIdx.y;
   const int r = blockIdx.z / c.Hkv, kvh = blockIdx.z % c.Hkv;
-  if (j >= c.Kr[r]) return;
+  if (j >= c.Kr[r]) {
+    pdl_wait();
+    return;
+  }
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int grp = w / NW, wi = w % NW;  // warp group and warp within it
   const int g = lane >> 2, t4 = lane & 3;
@@ -122,6 +127,21 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   const int32_t *lrow = loc + ((size_t)r * c.Kmax + j) * k;
   const uint16_t *brow = block + (size_t)r * c.Kmax * c.row;
 
+  // locations of this split's selected rows (written two launches back, by
+  // the union/probe), read once, coalesced, before the preceding launch ends
+  for (int e = e0 + tid; e < min(e1, k); e += kAttnThreads) lsm[e - e0] = lrow[e];
+  pdl_wait();
+  pdl_trigger();
+  // eq. (9)-(10): block row j enters the draft ring at phi(r, n_r + j); the
+  // live ring rows this round reads lie in [n_r - W, n_r) and R_d >= W + K,
+  // so the write never lands on a row being read
+  if (split == 0 && kvh == 0) {
+    const int64_t n = c.n[r];
+    const uint4 *src = reinterpret_cast<const uint4 *>(brow + (size_t)j * c.row);
+    uint4 *dst = reinterpret_cast<uint4 *>(c.ring + ((size_t)r * c.Rd + (n + j) % c.Rd) * c.row);
+    for (int v = tid; v < nv; v += kAttnThreads) dst[v] = src[v];
+  }
+
   // query fragments: rows of the A operand are the query heads of this kv head
   uint32_t qa[KS][4];
   {
@@ -138,9 +158,7 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
     }
   }
 
-  // locations of this split's selected rows, read once (coalesced)
-  for (int e = e0 + tid; e < min(e1, k); e += kAttnThreads) lsm[e - e0] = lrow[e];
-  __syncthreads();
+  __syncthreads();  // the locations are in shared memory
 
   // this warp group's tiles: grp, grp + SUB, ...
   const int ntiles_all = e1 > e0 ? (e1 - e0 + kTileRows - 1) / kTileRows : 0;
@@ -419,20 +437,18 @@ static cudaError_t launch_attn_t(const DevCtx &c, const uint16_t *q, const uint1
   if (e != cudaSuccess) return e;
   dim3 grid(n_split, c.Kmax, c.N * c.Hkv);
   if (tm) tm->begin(K_ATTN, s);
-  k_attn<DQK, DV><<<grid, kAttnThreads, smem, s>>>(c, q, block, loc, out, lse, n_split, chunk,
-                                                     body, loc_off);
+  e = launch_pdl(k_attn<DQK, DV>, grid, dim3(kAttnThreads), smem, s, c, q, block, loc, out, lse,
+                 n_split, chunk, body, loc_off);
   if (tm) tm->end(K_ATTN, s);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *block,
                           const int32_t *loc, uint16_t *out, float *lse, int n_split,
                           cudaStream_t s, Timer *tm) {
-  cudaError_t e = (c.dqk == 128 && c.dv == 128)
-                      ? launch_attn_t<128, 128>(c, q, block, loc, out, lse, n_split, s, tm)
-                      : launch_attn_t<576, 512>(c, q, block, loc, out, lse, n_split, s, tm);
-  if (e != cudaSuccess) return e;
-  return launch_post_attend(c, block, s, tm);
+  return (c.dqk == 128 && c.dv == 128)
+             ? launch_attn_t<128, 128>(c, q, block, loc, out, lse, n_split, s, tm)
+             : launch_attn_t<576, 512>(c, q, block, loc, out, lse, n_split, s, tm);
 }
 
 }  // namespace dhs

@@ -85,8 +85,11 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   __shared__ int sh_u, sh_m, sh_p;  // this CTA's union rows and misses; the leader's P
   const int crank = (int)cl.block_rank();
   const int r = blockIdx.x / kUnionCluster;
-  const int Kr = c.Kr[r];
-  if (Kr == 0) return;  // the whole cluster leaves together
+  const int Kr = c.Kr[r];  // written two launches back (scoring)
+  if (Kr == 0) {
+    pdl_wait();
+    return;  // the whole cluster leaves together
+  }
   const int tid = threadIdx.x, bs = blockDim.x;
   const int64_t n = c.n[r];
   const int k = c.k, KK = c.Kmax * k, B = c.B;
@@ -123,7 +126,9 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   const int nsel = Kr * k;
 
   // 0. start fetching what the later phases read: this slice's map entries,
-  //    and for the leader the LRU order and the rows of the slots
+  //    and for the leader the LRU order and the rows of the slots.  These
+  //    are state of earlier rounds, complete before the preceding launch
+  //    (top-k) began, so the copies start before that launch has finished.
   const bool any_opt = c.opt_count[r] > 0;
   if (pf) {
     for (int i = tid; i < row_hi - row_lo; i += bs) {
@@ -138,6 +143,8 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
     }
   }
   cp_async_commit();
+  pdl_wait();  // the selections of the preceding launch are complete
+  pdl_trigger();
 
   // 1. union bitmap of this CTA's slice
   for (int i = tid; i < sw; i += bs) bm[i] = 0;
@@ -335,7 +342,6 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       hot_stamp[v] = tick;
       hot_map[u] = v;
       c.promo_dst[(size_t)r * B + p] = v;
-      c.promo_src[(size_t)r * B + p] = p;
     }
     if (ev) atomicAdd(&sh_cnt[5], ev);
     // 5. LRU order after this tick: untouched slots keep their order, slots
@@ -388,6 +394,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
         if (!shared) {
           atomicMin(&c.first_occ[(size_t)r * KK + loc_index(l)], e);
           l = make_loc(DHS_LOC_STAGE, e);
+          c.inst[(size_t)r * KK + e] = -1;
         }
       }
       loc_out[(size_t)r * KK + e] = l;
@@ -397,9 +404,10 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   atomicAdd(&sh_cnt[4], missel);
   if (!shared) {
     cl.sync();  // every first selection of a miss is known
+    // the first selection of each promoted miss also fills its hot slot
     if (crank == 0)
       for (int p = tid; p < P; p += bs)
-        c.promo_src[(size_t)r * B + p] = c.first_occ[(size_t)r * KK + p];
+        c.inst[(size_t)r * KK + c.first_occ[(size_t)r * KK + p]] = candB[p];
   }
   __syncthreads();
   if (tid == 0) {
@@ -427,14 +435,29 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
 // Shared host gather: staging[r][m] <- host[r][D_r[m]], one warp per row,
 // 16-byte zero-copy loads from pinned host memory, four rows in flight per
 // warp.  In per-query mode every missing selection (j, i) is fetched into
-// staging row j*k + i.
+// staging row j*k + i.  A promoted row is written to its hot-cache slot from
+// the same registers ("Adaptive DHiSparse", section 3.4, installs promoted
+// rows after the attention readers; the victim slots are unprotected, so no
+// location of this round names them and the install may come first).
+// VEC 16-byte vectors per lane cover a row (VEC x 512 B); BATCH rows are in
+// flight per warp, so each warp keeps about 4 KB of loads outstanding.
 constexpr int kGatherWarps = 8;
-constexpr int kGatherBatch = 4;
-constexpr int kGatherVec = 4;  // up to 4 x 32 x 16 B = 2 KB rows
+constexpr int kGatherMaxVec = 4;  // rows up to 2 KB
 
+template <int VEC>
+struct GatherShape {
+  static constexpr int kGatherVec = VEC;
+  static constexpr int kGatherBatch = VEC == 1 ? 8 : VEC == 2 ? 4 : 2;
+};
+
+template <int VEC>
 __global__ void __launch_bounds__(kGatherWarps * 32)
 k_gather(const DevCtx c, const int32_t *__restrict__ topk, const int32_t *__restrict__ loc,
          int shared) {
+  constexpr int kGatherVec = GatherShape<VEC>::kGatherVec;
+  constexpr int kGatherBatch = GatherShape<VEC>::kGatherBatch;
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.y;
   const int Kr = c.Kr[r];
   if (Kr == 0) return;
@@ -446,21 +469,31 @@ k_gather(const DevCtx c, const int32_t *__restrict__ topk, const int32_t *__rest
   const uint16_t *host = c.host[r];
   const int64_t n = c.n[r];
   const int count = shared ? c.counts[r * 4 + 1] : Kr * c.k;
+  const int P = c.counts[r * 4 + 2];
   for (int base = gw; base < count; base += kGatherBatch * nwt) {
     uint4 buf[kGatherBatch][kGatherVec];
     int64_t srow[kGatherBatch];
-    int dst[kGatherBatch];
+    int dst[kGatherBatch], slot[kGatherBatch];
 #pragma unroll
     for (int b = 0; b < kGatherBatch; ++b) {
       const int e = base + b * nwt;
       srow[b] = -1;
       dst[b] = e;
+      slot[b] = -1;
       if (e < count) {
         if (shared) {
           srow[b] = c.miss[(size_t)r * KK + e];
+          if (e < P) slot[b] = c.promo_dst[(size_t)r * c.B + e];
         } else {
           const int32_t l = loc[(size_t)r * KK + e];
-          if (l >= 0 && loc_tier(l) == DHS_LOC_STAGE) srow[b] = topk[(size_t)r * KK + e];
+          if (l >= 0 && loc_tier(l) == DHS_LOC_STAGE) {
+            srow[b] = topk[(size_t)r * KK + e];
+            slot[b] = c.inst[(size_t)r * KK + e];
+          }
+        }
+        if (slot[b] >= c.B) {
+          record_error(c.err, DC_CAPACITY, K_GATHER);
+          slot[b] = -1;
         }
         if (srow[b] >= n) {
           record_error(c.err, DC_ROW_RANGE, K_GATHER);
@@ -485,6 +518,14 @@ k_gather(const DevCtx c, const int32_t *__restrict__ topk, const int32_t *__rest
         const int v = lane + 32 * i;
         if (v < nv) d[v] = buf[b][i];
       }
+      if (slot[b] >= 0) {
+        uint4 *h = reinterpret_cast<uint4 *>(c.hot_data + ((size_t)r * c.B + slot[b]) * c.row);
+#pragma unroll
+        for (int i = 0; i < kGatherVec; ++i) {
+          const int v = lane + 32 * i;
+          if (v < nv) h[v] = buf[b][i];
+        }
+      }
     }
   }
 }
@@ -495,22 +536,34 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
   cudaError_t e = ensure_smem(k_union_probe, union_smem_bytes(c), granted);
   if (e != cudaSuccess) return e;
   if (tm) tm->begin(K_UNION_PROBE, s);
-  k_union_probe<<<c.N * kUnionCluster, kUnionThreads, union_smem_bytes(c), s>>>(c, topk, loc_out,
-                                                                               shared, tick);
+  e = launch_pdl(k_union_probe, dim3(c.N * kUnionCluster), dim3(kUnionThreads),
+                 union_smem_bytes(c), s, c, topk, loc_out, shared, tick);
   if (tm) tm->end(K_UNION_PROBE, s);
-  // enough warps in flight to cover the host link's bandwidth-delay product
-  int blocks_per_req = (152 * 8 + c.N - 1) / c.N;
+  if (e != cudaSuccess) return e;
+  const int vec = (c.row * 2 + 511) / 512;
+  if (vec > kGatherMaxVec) return cudaErrorInvalidValue;
+  void (*kern)(const DevCtx, const int32_t *, const int32_t *, int) =
+      vec == 1 ? k_gather<1> : vec == 2 ? k_gather<2> : vec == 3 ? k_gather<3> : k_gather<4>;
+  static int resident[kGatherMaxVec + 1] = {};  // CTAs per SM
+  if (!resident[vec]) {
+    same_carveout(kern);
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kGatherWarps * 32, 0) !=
+            cudaSuccess || occ < 1) {
+      cudaGetLastError();
+      occ = 1;
+    }
+    resident[vec] = occ;
+  }
+  // one resident wave over the whole device: every warp keeps BATCH rows of
+  // loads in flight, far more than the host link's bandwidth-delay product
+  int blocks_per_req = (c.sms * resident[vec] + c.N - 1) / c.N;
   if (blocks_per_req < 1) blocks_per_req = 1;
   dim3 grid(blocks_per_req, c.N);
   if (tm) tm->begin(K_GATHER, s);
-  static bool carve_k_gather = false;
-  if (!carve_k_gather) {
-    same_carveout(k_gather);
-    carve_k_gather = true;
-  }
-  k_gather<<<grid, kGatherWarps * 32, 0, s>>>(c, topk, loc_out, shared);
+  e = launch_pdl(kern, grid, dim3(kGatherWarps * 32), 0, s, c, topk, loc_out, shared);
   if (tm) tm->end(K_GATHER, s);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace dhs

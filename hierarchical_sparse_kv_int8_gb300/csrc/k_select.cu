@@ -31,21 +31,6 @@ cudaError_t launch_upload(int32_t *dst, const int32_t *words, int n, cudaStream_
   return cudaGetLastError();
 }
 
-// Per-round control words of select (K_r, then the domain of every query),
-// written from the kernel parameter, and the score ranges reset.
-__global__ void k_select_prep(const DevCtx c, const __grid_constant__ UploadWords w) {
-  const int n = c.N + c.N * c.Kmax;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    if (i < c.N) c.Kr[i] = w.w[i];
-    else c.dom[i - c.N] = w.w[i];
-  }
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < c.N * c.Kmax;
-       i += gridDim.x * blockDim.x) {
-    c.minmax[2 * i] = INT_MAX;
-    c.minmax[2 * i + 1] = INT_MIN;
-  }
-}
-
 // ---------------------------------------------------------------- scores
 // One thread per key row.  Rows of up to 128 bytes are read straight from
 // global memory with 16-byte loads (each thread consumes whole 32-byte
@@ -81,15 +66,26 @@ __device__ __forceinline__ void score_direct(const int8_t *__restrict__ krow, co
   }
 }
 
+// ctl.w holds the round's control words: K_r of every request, then the
+// domain of every (request, query); the first CTA of each request publishes
+// them for the later launches of the round.
 template <int NC>
 __global__ void __launch_bounds__(kScoreThreads)
-k_index_score(const DevCtx c, const int8_t *__restrict__ q_idx) {
+k_index_score(const DevCtx c, const int8_t *__restrict__ q_idx,
+              const __grid_constant__ UploadWords ctl) {
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.y;
-  const int Kr = c.Kr[r];
+  const int Kr = ctl.w[r];
+  const int *qdom = ctl.w + c.N + r * c.Kmax;
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0) c.Kr[r] = Kr;
+    for (int j = threadIdx.x; j < c.Kmax; j += blockDim.x) c.dom[r * c.Kmax + j] = qdom[j];
+  }
   if (Kr == 0) return;
   int dom_r = 0;
-  for (int j = 0; j < Kr; ++j) dom_r = max(dom_r, c.dom[r * c.Kmax + j]);
+  for (int j = 0; j < Kr; ++j) dom_r = max(dom_r, qdom[j]);
   const int64_t row0 = (int64_t)blockIdx.x * kScoreThreads;
   if (row0 >= dom_r) return;
   const int RB = c.idx_row, nc = RB >> 4;
@@ -150,7 +146,7 @@ k_index_score(const DevCtx c, const int8_t *__restrict__ q_idx) {
 #pragma unroll
   for (int j = 0; j < kMaxKmax; ++j) {
     if (j >= Kr) break;
-    const bool valid = t < rows && row0 + t < c.dom[r * c.Kmax + j];
+    const bool valid = t < rows && row0 + t < qdom[j];
     int mn = valid ? acc[j] : INT_MAX, mx = valid ? acc[j] : INT_MIN;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -288,6 +284,8 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_wait();
+  pdl_trigger();
   const int crank = (int)cl.block_rank();
   const int prob = blockIdx.x / kTopkCluster;
   const int r = prob / c.Kmax, j = prob % c.Kmax;
@@ -309,6 +307,14 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
   const int p0 = min(dom, crank * part), p1 = min(dom, p0 + part);
   const int lo = c.minmax[(r * c.Kmax + j) * 2 + 0];
   const int hi = c.minmax[(r * c.Kmax + j) * 2 + 1];
+  // Once every CTA of the cluster has read the range (after its first
+  // cluster barrier), the leader empties it for the next round's scores.
+  auto empty_range = [&]() {
+    if (crank == 0 && tid == 0) {
+      c.minmax[(r * c.Kmax + j) * 2 + 0] = INT_MAX;
+      c.minmax[(r * c.Kmax + j) * 2 + 1] = INT_MIN;
+    }
+  };
 
   int nloc = 0;  // candidates this CTA holds
   if (dom <= k) {
@@ -407,6 +413,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
     int gt_off = __shfl_sync(0xffffffffu, gx - wgt[lane], wid);   // within this CTA
     int eq_off = __shfl_sync(0xffffffffu, ex - weq[lane], wid);
     cl.sync();  // every CTA's totals are published
+    empty_range();
     int eq_base = 0;                       // rows equal to T in earlier CTAs
     for (int q = 0; q < crank; ++q) eq_base += *cl.map_shared_rank(&sh_cta_eq, q);
     const int my_gt = sh_cta_gt, my_eq = sh_cta_eq;
@@ -513,6 +520,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
   for (int h = 0; h < 2; ++h)
     if (2 * tid + h < nloc) cand[2 * tid + h] = x[h];
   cl.sync();  // every CTA's sorted list is in place
+  empty_range();
   // ... copies the other CTAs' lists next to it (one pass of distributed
   // shared-memory reads into the histogram area, free by now) ...
   int lens[kTopkCluster], offs[kTopkCluster];
@@ -557,38 +565,25 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
 
 cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_out, int max_dom,
                           const int32_t *ctl_words, cudaStream_t s, Timer *tm) {
+  UploadWords ctl;
+  const int nw = c.N + c.N * c.Kmax;
+  for (int i = 0; i < nw; ++i) ctl.w[i] = ctl_words[i];
   {
-    UploadWords w;
-    const int n = c.N + c.N * c.Kmax;
-    for (int i = 0; i < n; ++i) w.w[i] = ctl_words[i];
-    static bool carve_k_select_prep = false;
-    if (!carve_k_select_prep) {
-      same_carveout(k_select_prep);
-      carve_k_select_prep = true;
-    }
-    k_select_prep<<<(c.N * c.Kmax + 255) / 256, 256, 0, s>>>(c, w);
-  }
-  if (max_dom > 0) {
+    // one CTA per request at least, so that the control words are published
     const int nc = c.idx_row >> 4;
     const size_t smem = (size_t)c.Kmax * c.idx_row +
                         (nc > kDirectChunks ? (size_t)kScoreThreads * c.idx_row : 0);
-    dim3 grid((max_dom + kScoreThreads - 1) / kScoreThreads, c.N);
+    dim3 grid(max_dom > 0 ? (max_dom + kScoreThreads - 1) / kScoreThreads : 1, c.N);
     cudaError_t e;
+    void (*kern)(const DevCtx, const int8_t *, const UploadWords) =
+        nc == 4 ? k_index_score<4> : nc == 8 ? k_index_score<8> : k_index_score<0>;
+    static size_t g4 = 0, g8 = 0, g0 = 0;
+    size_t &granted = nc == 4 ? g4 : nc == 8 ? g8 : g0;
+    if ((e = ensure_smem(kern, smem, granted)) != cudaSuccess) return e;
     if (tm) tm->begin(K_SCORE, s);
-    if (nc == 4) {
-      static size_t g4 = 0;
-      if ((e = ensure_smem(k_index_score<4>, smem, g4)) != cudaSuccess) return e;
-      k_index_score<4><<<grid, kScoreThreads, smem, s>>>(c, q_idx);
-    } else if (nc == 8) {
-      static size_t g8 = 0;
-      if ((e = ensure_smem(k_index_score<8>, smem, g8)) != cudaSuccess) return e;
-      k_index_score<8><<<grid, kScoreThreads, smem, s>>>(c, q_idx);
-    } else {
-      static size_t g0 = 0;
-      if ((e = ensure_smem(k_index_score<0>, smem, g0)) != cudaSuccess) return e;
-      k_index_score<0><<<grid, kScoreThreads, smem, s>>>(c, q_idx);
-    }
+    e = launch_pdl(kern, grid, dim3(kScoreThreads), smem, s, c, q_idx, ctl);
     if (tm) tm->end(K_SCORE, s);
+    if (e != cudaSuccess) return e;
   }
   int kp = 1;
   while (kp < c.k) kp <<= 1;
@@ -597,9 +592,10 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_ou
   cudaError_t e2 = ensure_smem(k_topk, smem_topk, granted_topk);
   if (e2 != cudaSuccess) return e2;
   if (tm) tm->begin(K_TOPK, s);
-  k_topk<<<c.N * c.Kmax * kTopkCluster, kTopkThreads, smem_topk, s>>>(c, topk_out);
+  e2 = launch_pdl(k_topk, dim3(c.N * c.Kmax * kTopkCluster), dim3(kTopkThreads), smem_topk, s, c,
+                  topk_out);
   if (tm) tm->end(K_TOPK, s);
-  return cudaGetLastError();
+  return e2;
 }
 
 }  // namespace dhs

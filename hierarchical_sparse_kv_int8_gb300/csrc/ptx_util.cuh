@@ -1,9 +1,21 @@
-// Small inline-PTX helpers (sm_80+ instructions that sm_103a keeps):
-// cp.async 16-byte copies, ldmatrix and the bf16 m16n8k16 tensor-core MMA.
+// Small inline-PTX helpers: cp.async 16-byte copies, ldmatrix and the bf16
+// m16n8k16 tensor-core MMA (sm_80 instructions that sm_103a keeps), and the
+// grid-dependency controls of programmatic dependent launch (sm_90+).
 #pragma once
 #include <stdint.h>
 
 namespace dhs {
+
+// Programmatic dependent launch.  pdl_wait() returns once the grid this launch
+// depends on has completed and its memory operations are visible; every CTA
+// of a library kernel calls it before it reads or writes anything a preceding
+// launch may still touch, and before it exits.  pdl_trigger() lets the next
+// launch on the stream begin placing its CTAs.  Both are no-ops for a launch
+// without a programmatic dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);

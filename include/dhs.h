@@ -13,11 +13,10 @@
  *   dhs_select   indexer scores + per-query top-k over the causal history
  *   dhs_resolve  union of the K_r selections, probe ring / optional map / hot
  *                cache, compact the misses, fetch each missing row once from
- *                pinned host memory into staging, emit one location per
- *                selected entry
+ *                pinned host memory into staging (a promoted row also into
+ *                its hot-cache slot), emit one location per selected entry
  *   dhs_attend   write the block rows into the draft ring, attend every query
- *                over its own selection plus the block rows up to itself, then
- *                copy promoted rows from staging into the hot cache
+ *                over its own selection plus the block rows up to itself
  *   dhs_commit   keep the accepted prefix of the block, roll back the rest
  *
  * Conventions
@@ -27,6 +26,12 @@
  *     cudaHostRegister) while bound.
  *   - All calls that take a stream only enqueue work on it and return; argument
  *     errors are detected on the host before anything is launched.
+ *   - The round's kernels are launched with programmatic stream serialization
+ *     (each may be placed while the previous launch on the stream drains, and
+ *     waits for it before touching its results).  Stream order is kept for
+ *     ordinary caller work in between; a caller kernel placed between two
+ *     calls that itself uses programmatic dependent launch must wait on its
+ *     own grid dependency before it exits.
  *   - Kernels check the indices they read (selected rows, locations) and, on
  *     a bad one, skip the access and record DHS_ERR_DEVICE_CHECK in a device
  *     error word, which dhs_get_stats reports after synchronising the stream.
@@ -172,7 +177,8 @@ int dhs_select(dhs_ctx *ctx, const int8_t *q_idx, const int32_t *k_per_req,
  * (a hit refreshes the slot's stamp to this call's tick).  Hot rows of the
  * union are protected; victims are the other slots ordered by (stamp, slot),
  * empty first; the first min(|D_r|, #victims) missing rows, ascending, take
- * them.  Their bytes reach the hot cache in dhs_attend, after attention.
+ * them.  Their bytes are written to the slot as they arrive from host; no
+ * location of this round names a victim slot, so attention is unaffected.
  * One tick of the LRU clock per call.  Must be followed by dhs_attend before
  * the next dhs_resolve or dhs_set_residency on this context. */
 int dhs_resolve(dhs_ctx *ctx, const int32_t *topk, int32_t *loc_out, int32_t shared,
@@ -188,8 +194,7 @@ int dhs_resolve(dhs_ctx *ctx, const int32_t *topk, int32_t *loc_out, int32_t sha
  *             at phi(r, n_r + u), eq. (10)
  *   loc       device int32 [n_slots][k_max][topk] from dhs_resolve
  *   out       device bf16 [n_slots][k_max][q_heads][v_dim]
- *   lse       device fp32 [n_slots][k_max][q_heads] natural-log sum-exp, or NULL
- * Then copies promoted rows from staging to their hot-cache slots ([ADHS] 3.4). */
+ *   lse       device fp32 [n_slots][k_max][q_heads] natural-log sum-exp, or NULL */
 int dhs_attend(dhs_ctx *ctx, const void *q, const void *block_kv, const int32_t *loc,
                void *out, float *lse, dhs_stream stream);
 
