@@ -36,7 +36,9 @@ class Config(ctypes.Structure):
                 ("v_dim", ctypes.c_int32), ("kv_layout", ctypes.c_int32),
                 ("budget", ctypes.c_int32), ("ring_window", ctypes.c_int32),
                 ("page_rows", ctypes.c_int32), ("opt_rows_max", ctypes.c_int64),
-                ("softmax_scale", ctypes.c_float)]
+                ("softmax_scale", ctypes.c_float), ("attn_pass", ctypes.c_int32)]
+
+ATTN_AUTO, ATTN_PER_QUERY, ATTN_UNION = 0, 1, 2
 
 
 class Stats(ctypes.Structure):

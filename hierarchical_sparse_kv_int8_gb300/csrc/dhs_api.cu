@@ -13,9 +13,9 @@
 namespace dhs {
 
 const char *const kKernelNames[K_COUNT] = {
-    "upload",         "index_score",     "topk",          "union_probe",
-    "gather",         "attn",            "commit",         "residency_clear", "residency_fill", "residency_publish",
-    "bind_reset"};
+    "upload",          "index_score",    "topk",           "union_probe",
+    "gather",          "attn",           "attn_union",     "commit",
+    "residency_clear", "residency_fill", "residency_publish", "bind_reset"};
 
 // ---------------------------------------------------------------- Timer
 cudaEvent_t Timer::take() {
@@ -136,6 +136,8 @@ struct dhs_ctx {
   DevCtx d;
   int n_split = 1;
   int device = 0;
+  bool fused = false;      // shared retrieval attends with the union pass
+  int last_shared = 0;     // mode of the last dhs_resolve
   std::vector<void *> allocs;
   // host mirrors
   std::vector<int64_t> n, ring_first, opt_count;
@@ -246,7 +248,7 @@ const char *dhs_strerror(int code) {
     case DHS_ERR_OOM: return "out of device or pinned memory";
     case DHS_ERR_CAPACITY: return "request exceeds a configured capacity";
     case DHS_ERR_CUDA: return "CUDA runtime error";
-    case DHS_ERR_DEVICE_CHECK: return "a kernel found an out-of-range index";
+    case DHS_ERR_DEVICE_CHECK: return "a kernel found an out-of-range index or a wait ran out";
     case DHS_ERR_TIMEOUT: return "timed out";
     default: return "unknown error";
   }
@@ -267,7 +269,7 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
       g.idx_heads * g.idx_dim > 1024 || g.q_heads < 1 || g.kv_heads < 1 ||
       g.q_heads % g.kv_heads || g.q_heads / g.kv_heads > 16 || g.q_heads > 128 || g.budget < 1 ||
       g.budget > 65535 || g.ring_window < 1 || g.page_rows < 1 || g.opt_rows_max < 0 ||
-      g.opt_rows_max > g.s_max)
+      g.opt_rows_max > g.s_max || g.attn_pass < DHS_ATTN_AUTO || g.attn_pass > DHS_ATTN_UNION)
     return DHS_ERR_INVALID;
   if (g.kv_layout != DHS_KV_SPLIT && g.kv_layout != DHS_KV_LATENT) return DHS_ERR_INVALID;
   if (g.kv_layout == DHS_KV_LATENT && (g.kv_heads != 1 || g.v_dim > g.qk_dim))
@@ -313,6 +315,16 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
     return DHS_ERR_CAPACITY;
   }
   c->n_split = attn_splits(d, d.N * d.Kmax);
+  {
+    const bool can = uattn_supported(d);
+    const double pq_bytes = (double)d.N * d.Kmax * (d.k + d.Kmax) * row * 2;
+    if (g.attn_pass == DHS_ATTN_UNION && !can) {
+      delete c;
+      return DHS_ERR_INVALID;
+    }
+    c->fused = g.attn_pass == DHS_ATTN_UNION ||
+               (g.attn_pass == DHS_ATTN_AUTO && can && pq_bytes > 128.0 * 1024 * 1024);
+  }
 
   const size_t N = d.N, KK = (size_t)d.Kmax * d.k, B = d.B, R = row;
   cudaError_t e = cudaSuccess;
@@ -343,6 +355,7 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   ALLOC(d.scores, N * d.Kmax * (size_t)d.Sm);
   ALLOC(d.minmax, N * d.Kmax * 2);
   ALLOC(d.uni, N * KK);
+  ALLOC(d.uent, N * KK);
   ALLOC(d.miss, N * KK);
   ALLOC(d.first_occ, N * KK);
   ALLOC(d.counts, N * 4);
@@ -352,6 +365,8 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   ALLOC(d.part_o, c->n_split > 1 ? pf : 1);
   ALLOC(d.part_ml, c->n_split > 1 ? N * d.Kmax * d.Hq * c->n_split * 2 : 1);
   ALLOC(d.ticket, N * d.Kmax * d.Hkv);
+  ALLOC(d.u_part, c->fused ? uattn_partial_floats(d) : 1);
+  ALLOC(d.u_ticket, N * d.Hkv);
   ALLOC(d.stats, ST_COUNT);
   ALLOC(d.err, 2);
   ALLOC(c->rh_qidx, N * d.Kmax * d.idx_row);
@@ -377,6 +392,7 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   if (e == cudaSuccess) e = cudaMemset(d.err, 0, 8);
   if (e == cudaSuccess) e = cudaMemset(d.counts, 0, N * 16);
   if (e == cudaSuccess) e = cudaMemset(d.ticket, 0, N * d.Kmax * d.Hkv * 4);
+  if (e == cudaSuccess) e = cudaMemset(d.u_ticket, 0, N * d.Hkv * 4);
   if (e == cudaSuccess) {
     // score ranges start empty; top-k empties each range again after reading it
     std::vector<int32_t> mm((size_t)N * d.Kmax * 2);
@@ -492,9 +508,10 @@ int dhs_resolve(dhs_ctx *c, const int32_t *topk, int32_t *loc_out, int32_t share
   c->tick += 1;
   if (c->tick > 0x7FFFFFF0) return DHS_ERR_CAPACITY;
   {
-    cudaError_t e_ = launch_resolve(c->d, topk, loc_out, shared, (int)c->tick, s, &c->timer);
+    cudaError_t e_ = launch_resolve(c->d, topk, loc_out, shared, 1, (int)c->tick, s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
   }
+  c->last_shared = shared;
   c->phase = PH_RESOLVED;
   return DHS_OK;
 }
@@ -507,9 +524,12 @@ int dhs_attend(dhs_ctx *c, const void *q, const void *block_kv, const int32_t *l
   if (c->phase != PH_RESOLVED) return DHS_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   {
-    cudaError_t e_ = launch_attend(c->d, static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(block_kv),
-                    loc, static_cast<uint16_t *>(out), lse, c->n_split, s,
-                    &c->timer);
+    const uint16_t *q16 = static_cast<const uint16_t *>(q);
+    const uint16_t *b16 = static_cast<const uint16_t *>(block_kv);
+    uint16_t *o16 = static_cast<uint16_t *>(out);
+    cudaError_t e_ = (c->last_shared && c->fused)
+                         ? launch_uattn(c->d, q16, b16, o16, lse, s, &c->timer)
+                         : launch_attend(c->d, q16, b16, loc, o16, lse, c->n_split, s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
   }
   c->phase = PH_ATTENDED;

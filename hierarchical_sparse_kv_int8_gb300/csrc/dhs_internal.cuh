@@ -25,6 +25,7 @@ enum KernelId {
   K_UNION_PROBE,
   K_GATHER,
   K_ATTN,
+  K_ATTN_UNION,
   K_COMMIT,
   K_RESIDENCY_CLEAR,
   K_RESIDENCY_FILL,
@@ -40,6 +41,7 @@ enum DeviceCheck {
   DC_ROW_RANGE = 1,   // a selected row outside [0, n_r)
   DC_LOC_RANGE = 2,   // a location tag or index outside its tier
   DC_CAPACITY = 3,    // a staging or pool index beyond capacity
+  DC_TIMEOUT = 4,     // a bounded wait on copies in flight ran out
 };
 
 // Everything a kernel needs to know about the context, passed by value.
@@ -79,6 +81,8 @@ struct DevCtx {
   int32_t *scores;      // [N][Kmax][Sm]
   int32_t *minmax;      // [N][Kmax][2]: range of each query's scores
   int32_t *uni;         // [N][Kmax*k]
+  int4 *uent;           // [N][Kmax*k] per union row u: row, location, mask of the
+                        // queries that selected it, 0
   int32_t *miss;        // [N][Kmax*k]
   int32_t *first_occ;   // [N][Kmax*k]
   int32_t *counts;      // [N][4]
@@ -89,6 +93,9 @@ struct DevCtx {
   float *part_o;        // attention partials [N][Kmax][Hq][n_split][dv]
   float *part_ml;       // [N][Kmax][Hq][n_split][2]: max (log2 units), sum
   int32_t *ticket;      // [N][Kmax][Hkv]: finished splits of each attention item
+  float *u_part;        // union attention, per (request, kv head) and cluster:
+                        // O [C][M][dv], then (m, l) [C][M][2]
+  int32_t *u_ticket;    // [N][Hkv]: clusters of an item that have finished
   unsigned long long *stats;  // counters, see StatIdx
   int32_t *err;               // [2]: code, site
 };
@@ -180,7 +187,11 @@ cudaError_t launch_upload(int32_t *dst, const int32_t *words, int n, cudaStream_
 cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_out,
                           int max_dom, const int32_t *ctl_words, cudaStream_t s, class Timer *tm);
 cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_out,
-                           int shared, int tick, cudaStream_t s, class Timer *tm);
+                           int shared, int gather, int tick, cudaStream_t s, class Timer *tm);
+cudaError_t launch_uattn(const DevCtx &c, const uint16_t *q, const uint16_t *block,
+                         uint16_t *out, float *lse, cudaStream_t s, class Timer *tm);
+bool uattn_supported(const DevCtx &c);
+size_t uattn_partial_floats(const DevCtx &c);
 cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *block,
                           const int32_t *loc, uint16_t *out, float *lse, int n_split,
                           cudaStream_t s, class Timer *tm);

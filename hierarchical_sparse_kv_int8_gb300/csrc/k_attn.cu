@@ -130,6 +130,64 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   // locations of this split's selected rows (written two launches back, by
   // the union/probe), read once, coalesced, before the preceding launch ends
   for (int e = e0 + tid; e < min(e1, k); e += kAttnThreads) lsm[e - e0] = lrow[e];
+  __syncthreads();  // the locations are in shared memory
+
+  // this warp group's tiles: grp, grp + SUB, ...
+  const int ntiles_all = e1 > e0 ? (e1 - e0 + kTileRows - 1) / kTileRows : 0;
+  const int ntiles = ntiles_all > grp ? (ntiles_all - grp + SUB - 1) / SUB : 0;
+  const int gtid = wi * 32 + lane;  // thread index within the group
+  // Copy one 16-row tile into its stage.  Lanes 0..15 of every warp decode
+  // one row's source address (location tag, bounds check) and the group's
+  // threads then copy the rows chunk by chunk, the address broadcast by
+  // shuffle.  Rows of the hot cache, optional pool and draft ring are state of
+  // earlier rounds (the gather before this launch writes only staging rows and
+  // victim hot slots, which no location names): the early pass copies them,
+  // possibly before the preceding launch has finished.  The late pass copies
+  // the staging rows and the caller's block rows, after the wait.
+  auto issue_pass = [&](int it, bool late_pass) {
+    if (it >= ntiles) return;
+    const int tile = grp + it * SUB;
+    unsigned char *st = stage_base + (size_t)(it % kAttnStages) * kTileRows * stride;
+    int *vf = vflag + (it % kAttnStages) * kTileRows;
+    const uint16_t *mysrc = nullptr;
+    bool late = false;
+    if (lane < kTileRows) {
+      const int e = e0 + tile * kTileRows + lane;
+      if (e < e1) {
+        if (e < k) {
+          const int32_t l = lsm[e - e0];
+          if (l >= 0) {
+            mysrc = loc_row(c, r, l);
+            late = loc_tier(l) == DHS_LOC_STAGE;
+            if (mysrc == nullptr && wi == 0 && !late_pass) record_error(c.err, DC_LOC_RANGE, K_ATTN);
+          }
+        } else {
+          mysrc = brow + (size_t)(e - k) * c.row;
+          late = true;
+        }
+      }
+      if (wi == 0 && !late_pass) vf[lane] = mysrc != nullptr;
+    }
+    const unsigned late_rows = __ballot_sync(0xffffffffu, late);
+#pragma unroll 4
+    for (int rr = 0; rr < kTileRows; ++rr) {
+      const uint16_t *src = reinterpret_cast<const uint16_t *>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mysrc), rr));
+      if ((((late_rows >> rr) & 1u) != 0) != late_pass) continue;
+      unsigned char *dst = st + (size_t)rr * stride;
+      for (int v = gtid; v < nv; v += NW * 32)
+        cp_async_16_zfill(dst + v * 16, src ? (const void *)(src + v * 8) : (const void *)c.ring,
+                          src ? 16 : 0);
+    }
+  };
+  auto issue = [&](int it) {
+    issue_pass(it, false);
+    issue_pass(it, true);
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int s = 0; s < kAttnStages - 1; ++s) issue_pass(s, false);
+
   pdl_wait();
   pdl_trigger();
   // eq. (9)-(10): block row j enters the draft ring at phi(r, n_r + j); the
@@ -140,6 +198,11 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
     const uint4 *src = reinterpret_cast<const uint4 *>(brow + (size_t)j * c.row);
     uint4 *dst = reinterpret_cast<uint4 *>(c.ring + ((size_t)r * c.Rd + (n + j) % c.Rd) * c.row);
     for (int v = tid; v < nv; v += kAttnThreads) dst[v] = src[v];
+  }
+#pragma unroll
+  for (int s = 0; s < kAttnStages - 1; ++s) {
+    issue_pass(s, true);
+    cp_async_commit();
   }
 
   // query fragments: rows of the A operand are the query heads of this kv head
@@ -158,48 +221,6 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
     }
   }
 
-  __syncthreads();  // the locations are in shared memory
-
-  // this warp group's tiles: grp, grp + SUB, ...
-  const int ntiles_all = e1 > e0 ? (e1 - e0 + kTileRows - 1) / kTileRows : 0;
-  const int ntiles = ntiles_all > grp ? (ntiles_all - grp + SUB - 1) / SUB : 0;
-  const int gtid = wi * 32 + lane;  // thread index within the group
-  // Copy one 16-row tile into its stage.  Lanes 0..15 of every warp decode
-  // one row's source address (location tag, bounds check) and the group's
-  // threads then copy the rows chunk by chunk, the address broadcast by shuffle.
-  auto issue = [&](int it) {
-    if (it < ntiles) {
-      const int tile = grp + it * SUB;
-      unsigned char *st = stage_base + (size_t)(it % kAttnStages) * kTileRows * stride;
-      int *vf = vflag + (it % kAttnStages) * kTileRows;
-      const uint16_t *mysrc = nullptr;
-      if (lane < kTileRows) {
-        const int e = e0 + tile * kTileRows + lane;
-        if (e < e1) {
-          if (e < k) {
-            const int32_t l = lsm[e - e0];
-            if (l >= 0) {
-              mysrc = loc_row(c, r, l);
-              if (mysrc == nullptr && wi == 0) record_error(c.err, DC_LOC_RANGE, K_ATTN);
-            }
-          } else {
-            mysrc = brow + (size_t)(e - k) * c.row;
-          }
-        }
-        if (wi == 0) vf[lane] = mysrc != nullptr;
-      }
-#pragma unroll 4
-      for (int rr = 0; rr < kTileRows; ++rr) {
-        const uint16_t *src = reinterpret_cast<const uint16_t *>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mysrc), rr));
-        unsigned char *dst = st + (size_t)rr * stride;
-        for (int v = gtid; v < nv; v += NW * 32)
-          cp_async_16_zfill(dst + v * 16, src ? (const void *)(src + v * 8) : (const void *)brow,
-                            src ? 16 : 0);
-      }
-    }
-    cp_async_commit();
-  };
   auto group_sync = [&]() {
     if (NW == 1) __syncwarp(); else __syncthreads();
   };
@@ -209,8 +230,6 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   for (int i = 0; i < VT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
 
-#pragma unroll
-  for (int s = 0; s < kAttnStages - 1; ++s) issue(s);
   for (int it = 0; it < ntiles; ++it) {
     issue(it + kAttnStages - 1);
     cp_async_wait_group<kAttnStages - 1>();

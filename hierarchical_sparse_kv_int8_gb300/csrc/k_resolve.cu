@@ -71,7 +71,8 @@ size_t union_smem_bytes(const DevCtx &c) {
   const size_t sw = (size_t)slice / 32;  // words of one slice
   const size_t pw = (size_t)((c.B + 31) / 32);
   const size_t maps = slice <= kMapPrefetchRows ? (size_t)slice * 8 : 0;
-  return sw * 8 + pw * 8 + (size_t)c.B * 16 + (size_t)c.Kmax * c.k * 4 + maps;
+  const size_t KK = (size_t)c.Kmax * c.k;
+  return sw * 8 + pw * 8 + (size_t)c.B * 16 + KK * 4 + (KK + 3) / 4 * 4 + maps;
 }
 
 __global__ void __cluster_dims__(kUnionCluster, 1, 1) __launch_bounds__(kUnionThreads)
@@ -108,14 +109,17 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   int32_t *lru_s = tmpB + B;   // leader: LRU order at the start of the call
   int32_t *hrow_s = lru_s + B;  // leader: row held by each slot at the start
   int32_t *ul = hrow_s + B;     // location of each union row of this slice
+  uint32_t *umw = reinterpret_cast<uint32_t *>(ul + KK);  // query masks, one byte per union row
+  const int umw_words = (KK + 3) / 4;
   const bool pf = slice <= kMapPrefetchRows;
-  int32_t *hmap_s = ul + KK;     // this slice's hot-map entries (when pf)
+  int32_t *hmap_s = reinterpret_cast<int32_t *>(umw + umw_words);  // slice's hot-map entries (when pf)
   int32_t *omap_s = hmap_s + slice;
   uint32_t *prot0 = cl.map_shared_rank(prot, 0);
   uint32_t *now0 = cl.map_shared_rank(now, 0);
 
   const int32_t *tk = topk + (size_t)r * KK;
   int32_t *uni = c.uni + (size_t)r * KK;
+  int4 *uent = c.uent + (size_t)r * KK;
   int32_t *miss = c.miss + (size_t)r * KK;
   int32_t *hot_row = c.hot_row + (size_t)r * B;
   int32_t *hot_stamp = c.hot_stamp + (size_t)r * B;
@@ -148,6 +152,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
 
   // 1. union bitmap of this CTA's slice
   for (int i = tid; i < sw; i += bs) bm[i] = 0;
+  for (int i = tid; i < umw_words; i += bs) umw[i] = 0;
   if (crank == 0)
     for (int i = tid; i < 2 * pw; i += bs) prot[i] = 0;  // prot and now
   if (tid < 6) sh_cnt[tid] = 0;
@@ -292,6 +297,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
           ul[q] = make_loc(DHS_LOC_STAGE, m_base + m);
           ++m;
         }
+        *reinterpret_cast<int2 *>(&uent[u_base + q]) = make_int2(u, ul[q]);
         ++q;
       }
     }
@@ -388,6 +394,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       const uint32_t word = bm[rel >> 5];
       const int q = wp[rel >> 5] + __popc(word & ((1u << (rel & 31)) - 1u));
       int32_t l = ul[q];
+      atomicOr(&umw[q >> 2], 1u << ((q & 3) * 8 + e / k));
       ++sel_here;
       if (loc_tier(l) == DHS_LOC_STAGE) {
         ++missel;
@@ -402,13 +409,16 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   }
   atomicAdd(&sh_cnt[3], sel_here);
   atomicAdd(&sh_cnt[4], missel);
-  if (!shared) {
-    cl.sync();  // every first selection of a miss is known
-    // the first selection of each promoted miss also fills its hot slot
-    if (crank == 0)
-      for (int p = tid; p < P; p += bs)
-        c.inst[(size_t)r * KK + c.first_occ[(size_t)r * KK + p]] = candB[p];
-  }
+  __syncthreads();  // the query masks of the slice are complete
+  // 7. second half of each union entry: the queries that selected the row
+  for (int q = tid; q < Uc; q += bs)
+    *reinterpret_cast<int2 *>(&uent[u_base + q].z) =
+        make_int2((int)((umw[q >> 2] >> ((q & 3) * 8)) & 0xFFu), 0);
+  if (!shared) cl.sync();  // every first selection of a miss is known
+  // the first selection of each promoted miss also fills its hot slot
+  if (!shared && crank == 0)
+    for (int p = tid; p < P; p += bs)
+      c.inst[(size_t)r * KK + c.first_occ[(size_t)r * KK + p]] = candB[p];
   __syncthreads();
   if (tid == 0) {
     atomicAdd(&c.stats[ST_SEL], (unsigned long long)sh_cnt[3]);
@@ -531,7 +541,7 @@ k_gather(const DevCtx c, const int32_t *__restrict__ topk, const int32_t *__rest
 }
 
 cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_out, int shared,
-                           int tick, cudaStream_t s, Timer *tm) {
+                           int gather, int tick, cudaStream_t s, Timer *tm) {
   static size_t granted = 0;
   cudaError_t e = ensure_smem(k_union_probe, union_smem_bytes(c), granted);
   if (e != cudaSuccess) return e;
@@ -539,7 +549,7 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
   e = launch_pdl(k_union_probe, dim3(c.N * kUnionCluster), dim3(kUnionThreads),
                  union_smem_bytes(c), s, c, topk, loc_out, shared, tick);
   if (tm) tm->end(K_UNION_PROBE, s);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || !gather) return e;
   const int vec = (c.row * 2 + 511) / 512;
   if (vec > kGatherMaxVec) return cudaErrorInvalidValue;
   void (*kern)(const DevCtx, const int32_t *, const int32_t *, int) =
@@ -553,7 +563,9 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
       cudaGetLastError();
       occ = 1;
     }
-    resident[vec] = occ;
+    // two CTAs per SM (16 warps, 8-16 rows in flight each) saturate the host
+    // link and leave room on every SM for the attention launch that follows
+    resident[vec] = occ < 2 ? occ : 2;
   }
   // one resident wave over the whole device: every warp keeps BATCH rows of
   // loads in flight, far more than the host link's bandwidth-delay product

@@ -13,23 +13,24 @@ import numpy as np
 from . import Context, make_config
 
 
-def config_for(rec, k_max: Optional[int] = None, opt_rows_max: Optional[int] = None):
+def config_for(rec, k_max: Optional[int] = None, opt_rows_max: Optional[int] = None,
+               attn_pass: int = 0):
     return make_config(
         n_slots=rec.N, k_max=k_max or rec.kmax, topk=rec.topk, s_max=rec.s_max,
         idx_heads=rec.H_idx, idx_dim=rec.d_idx, q_heads=rec.Hq, kv_heads=rec.Hkv,
         qk_dim=rec.qk_dim, v_dim=rec.v_dim, kv_layout=rec.kv_layout, budget=rec.B,
         ring_window=rec.W, page_rows=rec.p,
         opt_rows_max=rec.opt_rows_max if opt_rows_max is None else opt_rows_max,
-        softmax_scale=0.0)
+        softmax_scale=0.0, attn_pass=attn_pass)
 
 
 class Runner:
     def __init__(self, rec, k_max: Optional[int] = None, opt_rows_max: Optional[int] = None,
-                 stream=None):
+                 stream=None, attn_pass: int = 0):
         import torch
         self.torch = torch
         self.rec = rec
-        self.cfg = config_for(rec, k_max, opt_rows_max)
+        self.cfg = config_for(rec, k_max, opt_rows_max, attn_pass)
         self.Km = self.cfg.k_max
         self.ctx = Context(self.cfg)
         self.stream = stream

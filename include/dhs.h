@@ -35,7 +35,9 @@
  *   - Kernels check the indices they read (selected rows, locations) and, on
  *     a bad one, skip the access and record DHS_ERR_DEVICE_CHECK in a device
  *     error word, which dhs_get_stats reports after synchronising the stream.
- *     No kernel ever traps or waits on a flag.
+ *     No kernel ever traps or waits on a flag set by another launch; the one
+ *     wait inside a kernel (on its own copies in flight) is bounded, and if
+ *     it runs out the same error word is set and the kernel carries on.
  *   - Buffers passed by the caller stay owned by the caller.  Everything the
  *     context allocates (hot cache, staging, ring, optional pool, maps,
  *     scratch) is owned by it and freed by dhs_destroy.
@@ -102,7 +104,21 @@ typedef struct {
   int32_t page_rows;    /* p: rows per page, [ADHS] eq. (9)                     */
   int64_t opt_rows_max; /* optional-pool rows per request (0 = no optional map) */
   float softmax_scale;  /* 0 = 1/sqrt(qk_dim)                                   */
+  int32_t attn_pass;    /* attention kernel for shared retrieval, DHS_ATTN_*    */
 } dhs_config;
+
+/* Attention kernel used after a shared dhs_resolve (per-query resolution
+ * always uses the per-query pass).  Both compute eq. (5) for every query; they
+ * differ in how rows reach the SMs:
+ *   PER_QUERY: each (request, query) streams its own k + j + 1 rows; few
+ *              dependent steps, best when the round is latency-bound.
+ *   UNION    : each (request, kv head) streams the union U_r once and masks
+ *              every score by the queries that selected the row; up to K_r
+ *              times fewer row reads, best when the round is bound by HBM.
+ *   AUTO     : UNION when the per-query pass would stream more than 128 MiB
+ *              of rows per round (n_slots * k_max * (topk + k_max) rows), else
+ *              PER_QUERY. */
+enum { DHS_ATTN_AUTO = 0, DHS_ATTN_PER_QUERY = 1, DHS_ATTN_UNION = 2 };
 
 /* Cumulative counters since dhs_create (or dhs_reset_stats). */
 typedef struct {

@@ -13,7 +13,7 @@ from __future__ import annotations
 import numpy as np
 
 import oracle
-from oracle import HOT, OPT, RING, STAGE
+from oracle import HOT, INDEX_MASK, OPT, RING, STAGE, TIER_SHIFT
 
 ABS_TOL = 2e-2
 REL_TOL = 1e-2
@@ -57,7 +57,8 @@ def oracle_round(o, rec, rnd, slots, k_per_req, accepted=None, shared=True, pos=
     out, lse = o.attend(qa, bl)
     res = dict(topk=sel.copy(), loc=o.loc.copy(), out=out, lse=lse,
                union={r: o.union[r].copy() for r in slots if r in o.union},
-               misses={r: o.misses[r].copy() for r in slots if r in o.misses})
+               misses={r: o.misses[r].copy() for r in slots if r in o.misses},
+               staging={r: o.staging[r].copy() for r in slots if r in o.staging})
     if accepted is not None:
         o.commit(accepted)
     return res
@@ -105,6 +106,19 @@ def compare_round(run, o, ores, slots, k_per_req, label=""):
             U, M = int(cnt[r, 0]), int(cnt[r, 1])
             assert np.array_equal(uni[r, :U], ores["union"][r]), "%s union r=%d" % (label, r)
             assert np.array_equal(mis[r, :M], ores["misses"][r]), "%s misses r=%d" % (label, r)
+    # every staging row a location names holds the host row it stands for
+    stage = run.export("stage", run.torch.int16, (rec.N, KK, rec.row_elems))  # stays on device
+    for r in slots:
+        K = int(k_per_req[r])
+        if not K or r not in ores["staging"]:
+            continue
+        lr = ores["loc"][r, :K].reshape(-1)
+        lr = lr[lr >= 0]
+        idx = np.unique(lr[(lr >> TIER_SHIFT) == STAGE] & INDEX_MASK)
+        if idx.size:
+            got = stage[r][run.torch.from_numpy(idx).to(stage.device)].cpu().numpy()
+            assert np.array_equal(got.view(np.uint16), ores["staging"][r][idx]), \
+                "%s staging rows r=%d" % (label, r)
     out = bf16_bits_to_f64(run.out)
     lse = run.lse.cpu().numpy().astype(np.float64)
     return compare_outputs(out, lse, ores, slots, k_per_req, label)

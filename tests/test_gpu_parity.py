@@ -3,9 +3,11 @@
 Small recipes run the oracle on every request and cover the edges: domains
 shorter than k (padding), queries placed inside the history, idle slots,
 union overflow of the hot cache, optional residency, ring hits after commits
-over several rounds, both kv layouts, shared and per-query retrieval.  The
-full-size configurations run with the bench's launch shapes and check sampled
-requests (every step is request-local, so a request is checked completely).
+over several rounds, both kv layouts, shared and per-query retrieval, and
+both attention passes after a shared resolve (per query, and over the union
+with query masks).  The full-size configurations run with the bench's launch
+shapes and check sampled requests (every step is request-local, so a request
+is checked completely).
 """
 import numpy as np
 import pytest
@@ -42,8 +44,8 @@ TINY_SHORT = wl.Recipe("tiny_short_history", N=2, K=2, S=45, H_idx=1, d_idx=64, 
                        rho_cross=0.5, W=8, p=4, seed=14)
 
 
-def _rounds(rec, n_rounds, shared=True, k_sched=None, residency=True, label=""):
-    run = _runner(rec)
+def _rounds(rec, n_rounds, shared=True, k_sched=None, residency=True, attn_pass=0, label=""):
+    run = _runner(rec, attn_pass=attn_pass)
     slots = list(range(rec.N))
     o = build_oracle(rec, slots)
     if residency and rec.opt_frac > 0:
@@ -67,9 +69,12 @@ def _rounds(rec, n_rounds, shared=True, k_sched=None, residency=True, label=""):
     return run, o, st
 
 
-@pytest.mark.parametrize("shared", [True, False])
-def test_tiny_gqa_rounds(shared):
-    _, o, st = _rounds(TINY_GQA, 4, shared=shared, label="tiny_gqa")
+PER_QUERY, UNION = 1, 2
+
+
+@pytest.mark.parametrize("shared,attn_pass", [(True, PER_QUERY), (True, UNION), (False, 0)])
+def test_tiny_gqa_rounds(shared, attn_pass):
+    _, o, st = _rounds(TINY_GQA, 4, shared=shared, attn_pass=attn_pass, label="tiny_gqa")
     assert st["misses"] == o.stats.misses and st["hot_hits"] == o.stats.hot_hits
     assert st["ring_hits"] == o.stats.ring_hits and st["opt_hits"] == o.stats.opt_hits
     assert st["host_rows_fetched"] == o.stats.host_rows_fetched
@@ -77,22 +82,26 @@ def test_tiny_gqa_rounds(shared):
     assert o.stats.ring_hits > 0 and o.stats.opt_hits > 0 and o.stats.evictions > 0
 
 
-def test_tiny_two_kv_heads():
-    _rounds(TINY_GQA2, 3, label="tiny_hkv2")
+@pytest.mark.parametrize("attn_pass", [PER_QUERY, UNION])
+def test_tiny_two_kv_heads(attn_pass):
+    _rounds(TINY_GQA2, 3, attn_pass=attn_pass, label="tiny_hkv2")
 
 
-def test_tiny_mla_latent():
-    _rounds(TINY_MLA, 3, label="tiny_mla")
+@pytest.mark.parametrize("attn_pass", [PER_QUERY, UNION])
+def test_tiny_mla_latent(attn_pass):
+    _rounds(TINY_MLA, 3, attn_pass=attn_pass, label="tiny_mla")
 
 
-def test_history_shorter_than_k_and_idle_slots():
+@pytest.mark.parametrize("attn_pass", [PER_QUERY, UNION])
+def test_history_shorter_than_k_and_idle_slots(attn_pass):
     sched = lambda rnd: np.array([2, 0] if rnd % 2 == 0 else [1, 2], np.int32)
-    _rounds(TINY_SHORT, 4, k_sched=sched, label="short")
+    _rounds(TINY_SHORT, 4, k_sched=sched, attn_pass=attn_pass, label="short")
 
 
-def test_queries_inside_history():
+@pytest.mark.parametrize("attn_pass", [PER_QUERY, UNION])
+def test_queries_inside_history(attn_pass):
     rec = TINY_GQA
-    run = _runner(rec)
+    run = _runner(rec, attn_pass=attn_pass)
     slots = list(range(rec.N))
     o = build_oracle(rec, slots)
     kr = rec.k_per_req()
@@ -110,10 +119,11 @@ def test_cfg1_full():
     _rounds(rec, 2, label="cfg1")
 
 
-def test_cfg2_full():
+@pytest.mark.parametrize("attn_pass", [0, UNION])
+def test_cfg2_full(attn_pass):
     """The benchmark workload: round 0 is the previous step, round 1 is timed."""
     rec = wl.CONFIGS["cfg2"]
-    _, o, st = _rounds(rec, 2, label="cfg2")
+    _, o, st = _rounds(rec, 2, attn_pass=attn_pass, label="cfg2")
     assert o.stats.hot_hits > 0 and o.stats.misses > 0
 
 
