@@ -32,12 +32,10 @@ cudaError_t launch_upload(int32_t *dst, const int32_t *words, int n, cudaStream_
 }
 
 // ---------------------------------------------------------------- scores
-// One thread per key row.  Rows of up to 128 bytes are read straight from
-// global memory with 16-byte loads (each thread consumes whole 32-byte
-// sectors); wider rows are first staged in shared memory by coalesced
-// cp.async copies, stored rotated by a per-row offset so that the eight rows
-// of one LDS.128 phase fall in distinct bank groups.  The K_r query chunks
-// are shared-memory broadcasts; dp4a accumulates exact int32 dot products.
+// Rows of up to 128 bytes: one thread per key row, read straight from global
+// memory with 16-byte loads (each thread consumes whole 32-byte sectors); the
+// K_r query chunks are shared-memory broadcasts; dp4a accumulates exact int32
+// dot products.  Wider rows use k_index_score_wide below.
 constexpr int kScoreThreads = 256;
 constexpr int kDirectChunks = 8;  // rows up to 128 bytes use direct loads
 
@@ -92,21 +90,8 @@ k_index_score(const DevCtx c, const int8_t *__restrict__ q_idx,
   const int rows = (int)(dom_r - row0 < kScoreThreads ? dom_r - row0 : kScoreThreads);
   const int8_t *keys = c.keys[r] + row0 * RB;
   uint4 *qs = reinterpret_cast<uint4 *>(smem);
-  uint4 *tile = qs + c.Kmax * nc;
-  const bool direct = nc <= kDirectChunks;
-  if (!direct) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(keys);
-    for (int u = threadIdx.x; u < rows * nc; u += blockDim.x) {
-      const int t = u / nc, ch = u - t * nc;
-      int pos = ch + (t & 7);
-      if (pos >= nc) pos -= nc;
-      cp_async_16(&tile[t * nc + pos], &src[u]);
-    }
-    cp_async_commit();
-  }
   const uint4 *qsrc = reinterpret_cast<const uint4 *>(q_idx + (size_t)r * c.Kmax * RB);
   for (int u = threadIdx.x; u < Kr * nc; u += blockDim.x) qs[u] = qsrc[u];
-  if (!direct) cp_async_wait_all();
   __syncthreads();
 
   const int t = threadIdx.x;
@@ -114,27 +99,7 @@ k_index_score(const DevCtx c, const int8_t *__restrict__ q_idx,
 #pragma unroll
   for (int j = 0; j < kMaxKmax; ++j) acc[j] = 0;
   if (t < rows) {
-    if (direct) {
-      score_direct<NC>(keys + (size_t)t * RB, qs, Kr, nc, acc);
-    } else {
-      const uint4 *myrow = tile + t * nc;
-      int pos = t & 7;
-      if (pos >= nc) pos %= nc;
-      for (int ch = 0; ch < nc; ++ch) {
-        const uint4 kv = myrow[pos];
-        if (++pos == nc) pos = 0;
-#pragma unroll
-        for (int j = 0; j < kMaxKmax; ++j) {
-          if (j < Kr) {
-            const uint4 qv = qs[j * nc + ch];
-            acc[j] = __dp4a((int)kv.x, (int)qv.x, acc[j]);
-            acc[j] = __dp4a((int)kv.y, (int)qv.y, acc[j]);
-            acc[j] = __dp4a((int)kv.z, (int)qv.z, acc[j]);
-            acc[j] = __dp4a((int)kv.w, (int)qv.w, acc[j]);
-          }
-        }
-      }
-    }
+    score_direct<NC>(keys + (size_t)t * RB, qs, Kr, nc, acc);
     const int64_t s = row0 + t;
 #pragma unroll
     for (int j = 0; j < kMaxKmax; ++j)
@@ -170,6 +135,147 @@ k_index_score(const DevCtx c, const int8_t *__restrict__ q_idx,
       atomicMin(&c.minmax[(r * c.Kmax + t) * 2 + 0], mn);
       atomicMax(&c.minmax[(r * c.Kmax + t) * 2 + 1], mx);
     }
+  }
+}
+
+// Rows wider than 128 bytes: LPR lanes share a row, each holding CPL of its
+// 16-byte chunks and the same chunks of every query in registers, so a warp
+// reads 32 / LPR whole rows per load instruction, coalesced.  Each lane forms
+// dp4a partial sums for the eight (padded) queries; a butterfly
+// reduce-scatter over the row's lanes (three halving exchanges, then plain
+// sums) leaves query q's score in lane q * LPR / 8 of the row's lanes.
+template <int LPR, int CPL>
+struct WideScore {
+  static constexpr int RPW = 32 / LPR;            // rows per warp load
+  static constexpr int BR = CPL == 1 ? 4 : 2;     // loads of rows in flight per lane
+  static constexpr int ITERS = 4;
+  static constexpr int RPB = (kScoreThreads / 32) * RPW * BR * ITERS;  // rows per CTA
+};
+
+template <int LPR, int CPL>
+__global__ void __launch_bounds__(kScoreThreads)
+k_index_score_wide(const DevCtx c, const int8_t *__restrict__ q_idx,
+                   const __grid_constant__ UploadWords ctl) {
+  using WS = WideScore<LPR, CPL>;
+  constexpr int RPW = WS::RPW, BR = WS::BR;
+  static_assert(kMaxKmax == 8, "the reduce-scatter is written for eight queries");
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.y;
+  const int Kr = ctl.w[r];
+  const int *qdom = ctl.w + c.N + r * c.Kmax;
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0) c.Kr[r] = Kr;
+    for (int j = threadIdx.x; j < c.Kmax; j += blockDim.x) c.dom[r * c.Kmax + j] = qdom[j];
+  }
+  if (Kr == 0) return;
+  int dom_r = 0;
+  for (int j = 0; j < Kr; ++j) dom_r = max(dom_r, qdom[j]);
+  const int64_t b0 = (int64_t)blockIdx.x * WS::RPB;
+  if (b0 >= dom_r) return;
+  const int64_t b1 = min((int64_t)dom_r, b0 + WS::RPB);
+  __shared__ int smn[kMaxKmax], smx[kMaxKmax];
+  if (threadIdx.x < kMaxKmax) {
+    smn[threadIdx.x] = INT_MAX;
+    smx[threadIdx.x] = INT_MIN;
+  }
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int RB = c.idx_row, NC = RB >> 4;
+  const int sub = lane % LPR, rsub = lane / LPR;
+  // this lane's chunks of every query (zero past K_r and past the row)
+  uint4 qv[kMaxKmax][CPL];
+#pragma unroll
+  for (int j = 0; j < kMaxKmax; ++j)
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int ch = sub + i * LPR;
+      qv[j][i] = (j < Kr && ch < NC)
+                     ? *reinterpret_cast<const uint4 *>(q_idx + ((size_t)r * c.Kmax + j) * RB + ch * 16)
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+  // after the reduce-scatter this lane holds query qm's score; one lane per
+  // (row, query) writes it
+  const int qm = ((lane & (LPR / 2)) ? 4 : 0) + ((lane & (LPR / 4)) ? 2 : 0) +
+                 ((lane & (LPR / 8)) ? 1 : 0);
+  const bool writer = (lane & (LPR / 8 - 1)) == 0 && qm < Kr;
+  const int dq = qm < Kr ? qdom[qm] : 0;
+  int mn = INT_MAX, mx = INT_MIN;
+  const int8_t *keys = c.keys[r];
+  int32_t *out = c.scores + ((size_t)r * c.Kmax + min(qm, c.Kmax - 1)) * c.Sm;
+  constexpr int kWarps = kScoreThreads / 32;
+  for (int64_t g0 = b0 + wid * RPW; g0 < b1; g0 += (int64_t)kWarps * RPW * BR) {
+    uint4 kv[BR][CPL];
+#pragma unroll
+    for (int b = 0; b < BR; ++b) {
+      const int64_t s = g0 + (int64_t)b * kWarps * RPW + rsub;
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int ch = sub + i * LPR;
+        kv[b][i] = (s < b1 && ch < NC)
+                       ? __ldg(reinterpret_cast<const uint4 *>(keys + s * RB + ch * 16))
+                       : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < BR; ++b) {
+      int v[kMaxKmax];
+#pragma unroll
+      for (int j = 0; j < kMaxKmax; ++j) {
+        int a = 0;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          a = __dp4a((int)kv[b][i].x, (int)qv[j][i].x, a);
+          a = __dp4a((int)kv[b][i].y, (int)qv[j][i].y, a);
+          a = __dp4a((int)kv[b][i].z, (int)qv[j][i].z, a);
+          a = __dp4a((int)kv[b][i].w, (int)qv[j][i].w, a);
+        }
+        v[j] = a;
+      }
+      {  // 8 values -> 4 (partner at distance LPR / 2)
+        const bool up = lane & (LPR / 2);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int send = up ? v[i] : v[i + 4];
+          v[i] = (up ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, LPR / 2);
+        }
+      }
+      {  // 4 -> 2
+        const bool up = lane & (LPR / 4);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int send = up ? v[i] : v[i + 2];
+          v[i] = (up ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, send, LPR / 4);
+        }
+      }
+      {  // 2 -> 1
+        const bool up = lane & (LPR / 8);
+        const int send = up ? v[0] : v[1];
+        v[0] = (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, LPR / 8);
+      }
+#pragma unroll
+      for (int d = LPR / 16; d >= 1; d >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], d);
+      const int64_t s = g0 + (int64_t)b * kWarps * RPW + rsub;
+      if (writer && s < b1) {
+        out[s] = v[0];
+        if (s < dq) {
+          mn = min(mn, v[0]);
+          mx = max(mx, v[0]);
+        }
+      }
+    }
+  }
+  // range of each query's scores: shared-memory atomics, then one global
+  // atomic per CTA and query
+  if (writer && mn <= mx) {
+    atomicMin(&smn[qm], mn);
+    atomicMax(&smx[qm], mx);
+  }
+  __syncthreads();
+  if (threadIdx.x < Kr && smn[threadIdx.x] <= smx[threadIdx.x]) {
+    atomicMin(&c.minmax[(r * c.Kmax + threadIdx.x) * 2 + 0], smn[threadIdx.x]);
+    atomicMax(&c.minmax[(r * c.Kmax + threadIdx.x) * 2 + 1], smx[threadIdx.x]);
   }
 }
 
@@ -571,15 +677,28 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_ou
   {
     // one CTA per request at least, so that the control words are published
     const int nc = c.idx_row >> 4;
-    const size_t smem = (size_t)c.Kmax * c.idx_row +
-                        (nc > kDirectChunks ? (size_t)kScoreThreads * c.idx_row : 0);
-    dim3 grid(max_dom > 0 ? (max_dom + kScoreThreads - 1) / kScoreThreads : 1, c.N);
     cudaError_t e;
-    void (*kern)(const DevCtx, const int8_t *, const UploadWords) =
-        nc == 4 ? k_index_score<4> : nc == 8 ? k_index_score<8> : k_index_score<0>;
-    static size_t g4 = 0, g8 = 0, g0 = 0;
-    size_t &granted = nc == 4 ? g4 : nc == 8 ? g8 : g0;
-    if ((e = ensure_smem(kern, smem, granted)) != cudaSuccess) return e;
+    void (*kern)(const DevCtx, const int8_t *, const UploadWords);
+    size_t smem = 0;
+    int rpb;
+    if (nc <= kDirectChunks) {
+      kern = nc == 4 ? k_index_score<4> : nc == 8 ? k_index_score<8> : k_index_score<0>;
+      smem = (size_t)c.Kmax * c.idx_row;
+      rpb = kScoreThreads;
+    } else if (nc <= 16) {
+      kern = k_index_score_wide<16, 1>;
+      rpb = WideScore<16, 1>::RPB;
+    } else if (nc <= 32) {
+      kern = k_index_score_wide<32, 1>;
+      rpb = WideScore<32, 1>::RPB;
+    } else {
+      kern = k_index_score_wide<32, 2>;
+      rpb = WideScore<32, 2>::RPB;
+    }
+    static size_t granted[5] = {};
+    const int gi = nc == 4 ? 0 : nc == 8 ? 1 : nc <= kDirectChunks ? 2 : nc <= 16 ? 3 : 4;
+    if ((e = ensure_smem(kern, smem, granted[gi])) != cudaSuccess) return e;
+    dim3 grid(max_dom > 0 ? (max_dom + rpb - 1) / rpb : 1, c.N);
     if (tm) tm->begin(K_SCORE, s);
     e = launch_pdl(kern, grid, dim3(kScoreThreads), smem, s, c, q_idx, ctl);
     if (tm) tm->end(K_SCORE, s);

@@ -44,6 +44,20 @@ TINY_SHORT = wl.Recipe("tiny_short_history", N=2, K=2, S=45, H_idx=1, d_idx=64, 
                        rho_cross=0.5, W=8, p=4, seed=14)
 
 
+# Index rows wider than 128 bytes: 192 B (16 lanes share a row, four of them
+# idle) and 768 B (32 lanes, two chunks each), five queries (padded to eight
+# in the reduce-scatter).  The second recipe draws full-range int8 keys and
+# queries, so every query's scores span far more than 2^13 values: top-k takes
+# several radix passes and the per-CTA sort and merge path.
+TINY_WIDE = wl.Recipe("tiny_wide_rows", N=2, K=5, S=900, H_idx=2, d_idx=96, topk=96, Hq=8,
+                      Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=64, rho_within=0.5,
+                      rho_cross=0.6, W=16, p=8, seed=21)
+TINY_WIDE_FULL = wl.Recipe("tiny_wide_full_range", N=2, K=3, S=1500, H_idx=4, d_idx=192,
+                           topk=128, Hq=8, Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=64,
+                           rho_within=0.5, rho_cross=0.6, W=16, p=8, seed=22,
+                           i8_lo=-128, i8_hi=127)
+
+
 def _rounds(rec, n_rounds, shared=True, k_sched=None, residency=True, attn_pass=0, label=""):
     run = _runner(rec, attn_pass=attn_pass)
     slots = list(range(rec.N))
@@ -90,6 +104,15 @@ def test_tiny_two_kv_heads(attn_pass):
 @pytest.mark.parametrize("attn_pass", [PER_QUERY, UNION])
 def test_tiny_mla_latent(attn_pass):
     _rounds(TINY_MLA, 3, attn_pass=attn_pass, label="tiny_mla")
+
+
+@pytest.mark.parametrize("rec", [TINY_WIDE, TINY_WIDE_FULL], ids=["192B", "768B_full_range"])
+def test_wide_index_rows(rec):
+    if rec.i8_hi > 8:  # the full-range recipe must leave the single-pass top-k
+        keys = rec.index_keys(0, 1)[0, :rec.S].astype(np.int64)
+        sc = keys @ rec.index_queries(0, 0, 1)[0, 0].astype(np.int64)
+        assert sc.max() - sc.min() >= 1 << 13
+    _rounds(rec, 3, attn_pass=UNION, label=rec.name)
 
 
 @pytest.mark.parametrize("attn_pass", [PER_QUERY, UNION])

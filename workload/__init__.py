@@ -152,6 +152,8 @@ class Recipe:
     opt_frac: float = 0.0
     seed: int = 0
     s_slack: int = 64
+    i8_lo: int = -8      # indexer keys and queries are uniform over i8_lo..i8_hi
+    i8_hi: int = 8
 
     @property
     def kmax(self) -> int:
@@ -188,10 +190,10 @@ class Recipe:
 
     # ---- inputs -------------------------------------------------------
     def index_keys(self, r0: int, r1: int) -> np.ndarray:
-        """int8 [r1-r0][s_max][H_idx*d_idx], uniform over -8..8."""
+        """int8 [r1-r0][s_max][H_idx*d_idx], uniform over i8_lo..i8_hi."""
         per = self.s_max * self.idx_row
         out = np.empty((r1 - r0, self.s_max, self.idx_row), np.int8)
-        fill_i8(out, self.seed, S_KEYS, r0 * per)
+        fill_i8(out, self.seed, S_KEYS, r0 * per, self.i8_lo, self.i8_hi)
         return out
 
     def host_rows_into(self, dst, r0: int, r1: int):
@@ -210,7 +212,7 @@ class Recipe:
         x = x0
         for y in range(1, rnd + 1):
             sel = u32(x.size, self.seed, s_sel + ROUND_STRIDE * y, off)
-            fresh = i8(x.size, self.seed, s_fresh + ROUND_STRIDE * y, off)
+            fresh = i8(x.size, self.seed, s_fresh + ROUND_STRIDE * y, off, self.i8_lo, self.i8_hi)
             keep = sel.astype(np.uint64).reshape(x.shape) < thr
             x = np.where(keep, x, fresh.reshape(x.shape))
         return x
@@ -225,10 +227,11 @@ class Recipe:
         elements from the previous step.
         """
         E, Km, n = self.idx_row, self.kmax, r1 - r0
-        base = i8(n * E, self.seed, S_QI_BASE, r0 * E).reshape(n, 1, E)
+        lo, hi = self.i8_lo, self.i8_hi
+        base = i8(n * E, self.seed, S_QI_BASE, r0 * E, lo, hi).reshape(n, 1, E)
         base = self._drift(base, rnd, S_QI_XSEL, S_QI_XFRESH, r0 * E)
         off = r0 * Km * E
-        own = i8(n * Km * E, self.seed, S_QI_FRESH, off).reshape(n, Km, E)
+        own = i8(n * Km * E, self.seed, S_QI_FRESH, off, lo, hi).reshape(n, Km, E)
         own = self._drift(own, rnd, S_QI_FSEL, S_QI_FFRESH, off)
         sel = u32(n * Km * E, self.seed, S_QI_SEL, off).reshape(n, Km, E)
         thr = np.uint64(int(self.rho_within * 4294967296.0))
