@@ -44,11 +44,19 @@ TINY_SHORT = wl.Recipe("tiny_short_history", N=2, K=2, S=45, H_idx=1, d_idx=64, 
                        rho_cross=0.5, W=8, p=4, seed=14)
 
 
-# Index rows wider than 128 bytes: 192 B (16 lanes share a row, four of them
-# idle) and 768 B (32 lanes, two chunks each), five queries (padded to eight
-# in the reduce-scatter).  The second recipe draws full-range int8 keys and
-# queries, so every query's scores span far more than 2^13 values: top-k takes
-# several radix passes and the per-CTA sort and merge path.
+# Index rows of other widths than the configurations': 16 B and 32 B (one
+# thread per row, one or two chunks), 192 B (16 lanes share a row, four of
+# them idle) and 768 B (32 lanes, two chunks each), with three or five queries
+# (the wide rows' reduce-scatter pads them to eight).  The last recipe draws
+# full-range int8 keys and queries, so every query's scores span far more
+# than 2^13 values: top-k takes several radix passes and the per-CTA sort and
+# merge path.
+TINY_IDX16 = wl.Recipe("tiny_idx16", N=2, K=3, S=400, H_idx=1, d_idx=16, topk=64, Hq=8, Hkv=1,
+                       qk_dim=128, v_dim=128, kv_layout=0, B=48, rho_within=0.5,
+                       rho_cross=0.6, W=16, p=8, seed=23)
+TINY_IDX32 = wl.Recipe("tiny_idx32", N=2, K=5, S=400, H_idx=2, d_idx=16, topk=64, Hq=8, Hkv=1,
+                       qk_dim=128, v_dim=128, kv_layout=0, B=48, rho_within=0.5,
+                       rho_cross=0.6, W=16, p=8, seed=24)
 TINY_WIDE = wl.Recipe("tiny_wide_rows", N=2, K=5, S=900, H_idx=2, d_idx=96, topk=96, Hq=8,
                       Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=64, rho_within=0.5,
                       rho_cross=0.6, W=16, p=8, seed=21)
@@ -106,8 +114,9 @@ def test_tiny_mla_latent(attn_pass):
     _rounds(TINY_MLA, 3, attn_pass=attn_pass, label="tiny_mla")
 
 
-@pytest.mark.parametrize("rec", [TINY_WIDE, TINY_WIDE_FULL], ids=["192B", "768B_full_range"])
-def test_wide_index_rows(rec):
+@pytest.mark.parametrize("rec", [TINY_IDX16, TINY_IDX32, TINY_WIDE, TINY_WIDE_FULL],
+                         ids=["16B", "32B", "192B", "768B_full_range"])
+def test_index_row_widths(rec):
     if rec.i8_hi > 8:  # the full-range recipe must leave the single-pass top-k
         keys = rec.index_keys(0, 1)[0, :rec.S].astype(np.int64)
         sc = keys @ rec.index_queries(0, 0, 1)[0, 0].astype(np.int64)
