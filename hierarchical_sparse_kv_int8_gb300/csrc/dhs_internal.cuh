@@ -42,6 +42,7 @@ enum DeviceCheck {
   DC_LOC_RANGE = 2,   // a location tag or index outside its tier
   DC_CAPACITY = 3,    // a staging or pool index beyond capacity
   DC_TIMEOUT = 4,     // a bounded wait on copies in flight ran out
+  DC_DUPLICATE = 5,   // a row listed twice in one query's selection
 };
 
 // Everything a kernel needs to know about the context, passed by value.

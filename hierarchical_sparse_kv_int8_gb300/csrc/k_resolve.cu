@@ -394,7 +394,8 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       const uint32_t word = bm[rel >> 5];
       const int q = wp[rel >> 5] + __popc(word & ((1u << (rel & 31)) - 1u));
       int32_t l = ul[q];
-      atomicOr(&umw[q >> 2], 1u << ((q & 3) * 8 + e / k));
+      const uint32_t qbit = 1u << ((q & 3) * 8 + e / k);
+      if (atomicOr(&umw[q >> 2], qbit) & qbit) record_error(c.err, DC_DUPLICATE, K_UNION_PROBE);
       ++sel_here;
       if (loc_tier(l) == DHS_LOC_STAGE) {
         ++missel;

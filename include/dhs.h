@@ -182,7 +182,9 @@ int dhs_select(dhs_ctx *ctx, const int8_t *q_idx, const int32_t *k_per_req,
 
 /* Steps 2-4, [ADHS] 3.2-3.3, eq. (6), Fig. 2, Fig. 3 callouts 2-3.
  *   topk     device int32 [n_slots][k_max][topk] (from dhs_select or the caller;
- *            entries must be -1 or rows < n_r)
+ *            entries must be -1 or rows < n_r, no row twice in one query's
+ *            list -- a selection is a set; a repeat is reported as
+ *            DHS_ERR_DEVICE_CHECK)
  *   loc_out  device int32 [n_slots][k_max][topk]: one location per entry
  *   shared   1: each distinct missing row of a request is fetched once and its
  *            staging location returned to every query that selected it;

@@ -192,3 +192,20 @@ def test_cfg3_full_sampled():
 def test_cfg4_full_sampled():
     rec = wl.CONFIGS["cfg4"]
     _sampled(rec, [5, 63])
+
+
+def test_repeated_row_in_a_selection_is_flagged():
+    """A selection is a set: a caller list that names a row twice is reported
+    through the device check word (code 5), and nothing faults."""
+    rec = TINY_GQA
+    run = _runner(rec, attn_pass=UNION)
+    kr = rec.k_per_req()
+    run.load_round(0)
+    run.select(kr)
+    assert run.ctx.stats()["device_error"] == 0
+    run.topk[1, 2, 7] = run.topk[1, 2, 3]
+    run.resolve(True)
+    run.attend()
+    run.commit(rec.accepted(0))
+    st = run.ctx.stats(check=False)
+    assert st["device_error"] == 5
