@@ -57,7 +57,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             if verbose:
                 print(log)
     tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-Xlinker", "--no-undefined"]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (p.stdout, p.stderr))

@@ -391,9 +391,22 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   __syncthreads();
   if (!sh_last) return;
   __threadfence();
-  // every (head, split) pair's max and sum in one parallel load ...
   float *Ms = Wt + 16 * n_split;  // [16][n_split] maxima, then sums
   float *Ls = Ms + 16 * n_split;
+  // The item's partial outputs are one contiguous block ([G][n_split][DV]
+  // floats): when it fits in the free stage area, it is copied into shared
+  // memory by one batch of cp.async while the weights are formed ...
+  float *Ps = reinterpret_cast<float *>(
+      (reinterpret_cast<uintptr_t>(Ls + 16 * n_split) + 15) & ~static_cast<uintptr_t>(15));
+  const size_t pbytes = (size_t)G * n_split * DV * 4;
+  const bool staged =
+      (size_t)(reinterpret_cast<unsigned char *>(Ps) - smem) + pbytes <= body_bytes;
+  if (staged) {
+    const float4 *src = reinterpret_cast<const float4 *>(c.part_o + qbase * n_split * DV);
+    for (int i = tid; i < (int)(pbytes / 16); i += kAttnThreads) cp_async_16(Ps + 4 * i, src + i);
+    cp_async_commit();
+  }
+  // ... every (head, split) pair's max and sum in one parallel load ...
   for (int i = tid; i < G * n_split; i += kAttnThreads) {
     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(c.part_ml + (qbase * n_split + i) * 2));
     Ms[i] = ml.x;
@@ -410,6 +423,23 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
     const float inv = L > 0.f ? 1.f / L : 0.f;
     for (int sp = 0; sp < n_split; ++sp) Wt[h * n_split + sp] = exp2f(Ms[h * n_split + sp] - ref) * inv;
     if (lse) lse[qbase + h] = L > 0.f ? (M + log2f(L)) * ln2 : -CUDART_INF_F;
+  }
+  if (staged) {
+    cp_async_wait_all();
+    __syncthreads();
+    for (int idx = tid; idx < G * DV / 2; idx += kAttnThreads) {
+      const int h = (2 * idx) / DV, d = (2 * idx) % DV;
+      float a = 0.f, b = 0.f;
+      for (int sp = 0; sp < n_split; ++sp) {
+        const float wgt = Wt[h * n_split + sp];
+        const float2 v = *reinterpret_cast<const float2 *>(Ps + ((size_t)h * n_split + sp) * DV + d);
+        a += wgt * v.x;
+        b += wgt * v.y;
+      }
+      *reinterpret_cast<uint32_t *>(out + (qbase + h) * DV + d) = pack_bf16(a, b);
+    }
+    if (tid == 0) c.ticket[item] = 0;  // ready for the next launch
+    return;
   }
   __syncthreads();
   constexpr int kMaxUnrolledSplits = 16;  // all partial loads of a thread in flight at once
