@@ -298,6 +298,8 @@ k_index_score_wide(const DevCtx c, const int8_t *__restrict__ q_idx,
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkCluster = 4;
 constexpr int kRadixBits = 13;
+constexpr int kBinsPerThread = (1 << kRadixBits) / kTopkThreads;
+static_assert(kMaxTopk <= 2 * kTopkThreads, "the exact placement holds two winners per thread");
 
 __device__ __forceinline__ int block_excl_scan(int v, int *warp_sums, int &total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -457,24 +459,51 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
       const int per = (nbins + kTopkThreads - 1) / kTopkThreads;
       const int b_hi = nbins - tid * per;
       const int b_lo = max(0, b_hi - per);
+      int gsum[kBinsPerThread], psum[kBinsPerThread];  // cluster count; count in earlier CTAs
       int local = 0;
-      for (int b = b_lo; b < b_hi; ++b)
 #pragma unroll
-        for (int q = 0; q < kTopkCluster; ++q) local += hr[q][b];
+      for (int t = 0; t < kBinsPerThread; ++t) {
+        const int b = b_lo + t;
+        int g = 0, pc = 0;
+        if (b < b_hi) {
+#pragma unroll
+          for (int q = 0; q < kTopkCluster; ++q) {
+            const int hv = (int)hr[q][b];
+            g += hv;
+            if (q < crank) pc += hv;
+          }
+        }
+        gsum[t] = g;
+        psum[t] = pc;
+        local += g;
+      }
       int total;
       const int above = block_excl_scan(b_hi > 0 ? local : 0, warp_sums, total);
       if (b_hi > 0 && above < k_rem && k_rem <= above + local) {
         int acc = above;
-        for (int b = b_hi - 1; b >= b_lo; --b) {
-          int hb = 0;
 #pragma unroll
-          for (int q = 0; q < kTopkCluster; ++q) hb += hr[q][b];
-          if (acc + hb >= k_rem) {
+        for (int t = kBinsPerThread - 1; t >= 0; --t) {
+          const int b = b_lo + t;
+          if (b >= b_hi) continue;
+          if (acc + gsum[t] >= k_rem) {
             sh_bin = b;
             sh_above = acc;
             break;
           }
-          acc += hb;
+          acc += gsum[t];
+        }
+      }
+      if (passes == 1 && shift == 0) {
+        // a single pass decides: base[b] = rows of the domain above offset
+        // value b plus rows equal to b in earlier CTAs, for the exact placement
+        int *base = reinterpret_cast<int *>(hist + (1 << kRadixBits));
+        int acc = above;
+#pragma unroll
+        for (int t = kBinsPerThread - 1; t >= 0; --t) {
+          const int b = b_lo + t;
+          if (b >= b_hi) continue;
+          base[b] = acc + psum[t];
+          acc += gsum[t];
         }
       }
       __syncthreads();
@@ -522,44 +551,16 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
     empty_range();
     int eq_base = 0;                       // rows equal to T in earlier CTAs
     for (int q = 0; q < crank; ++q) eq_base += *cl.map_shared_rank(&sh_cta_eq, q);
+    cluster_arrive();  // this CTA's distributed reads are done; waited for before it leaves
     const int my_gt = sh_cta_gt, my_eq = sh_cta_eq;
     const int kept_eq = max(0, min(my_eq, need - eq_base));
     nloc = my_gt + kept_eq;
     // Exact bins (one radix pass, or none): every winner's place follows from
-    // the histograms.  base[b] = rows of the domain above offset value b plus
-    // rows equal to b in earlier CTAs; the rows equal to b in this CTA follow
-    // in row order.
+    // the histograms (base[], formed in the pass); the rows equal to a value
+    // in this CTA follow in row order.  No CTA reads another's histogram after
+    // the cluster barrier above, so the histogram area is free for reuse.
     const bool exact = passes <= 1;
-    int *base = reinterpret_cast<int *>(hist + (1 << kRadixBits));
-    if (exact) {
-      const int per = (nb_last + kTopkThreads - 1) / kTopkThreads;
-      const int b_hi = nb_last - tid * per;
-      const int b_lo = max(0, b_hi - per);
-      int run_sum = 0;
-      for (int b = b_lo; b < b_hi; ++b) {
-        int pc = 0, g = 0;
-        if (b > (int)T) {
-#pragma unroll
-          for (int q = 0; q < kTopkCluster; ++q) {
-            const int hv = (int)hr[q][b];
-            g += hv;
-            if (q < crank) pc += hv;
-          }
-        }
-        base[b] = pc;
-        run_sum += g;
-      }
-      int tot;
-      int acc = block_excl_scan(b_hi > 0 ? run_sum : 0, warp_sums, tot);
-      for (int b = b_hi - 1; b >= b_lo; --b) {
-        base[b] += acc;
-        if (b > (int)T) {
-#pragma unroll
-          for (int q = 0; q < kTopkCluster; ++q) acc += (int)hr[q][b];
-        }
-      }
-    }
-    cl.sync();  // no CTA reads another's histogram after this point
+    const int *base = reinterpret_cast<const int *>(hist + (1 << kRadixBits));
     const unsigned lt = (1u << lane) - 1u;
     const int gt_end = gt_off + ngt, eq_end = eq_off + neq;
 #pragma unroll 4
@@ -582,31 +583,57 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
       eq_off += __popc(beq);
     }
     if (exact) {
-      // one warp walks this CTA's winners above T in row order; equal values
-      // are ranked with a per-value running count
+      // This CTA's winners above T, one thread each: a winner of value v takes
+      // a slot of v's group [base[v], base[v] + count) with a shared-memory
+      // atomic, then its place in the group is the number of the group's rows
+      // below its own (row order among equal values).  The candidate area
+      // holds the claimed rows meanwhile.
+      constexpr int kPer = 2;  // winners per thread: my_gt <= k <= 2 * kTopkThreads
       int *lcnt = reinterpret_cast<int *>(hist);
       for (int i = tid; i < nb_last; i += kTopkThreads) lcnt[i] = 0;
-      __syncthreads();
-      if (wid == 0) {
-        for (int i0 = 0; i0 < my_gt; i0 += 32) {
-          const int i = i0 + lane;
-          const bool ok = i < my_gt;
-          const unsigned long long key = ok ? cand[i] : 0ull;
-          const uint32_t v = ok ? 0xFFFFFFFFu - (uint32_t)(key >> 32) : (0x80000000u | lane);
-          const unsigned peers = __match_any_sync(0xffffffffu, v);
-          if (ok) {
-            const int pos = base[v] + lcnt[v] + __popc(peers & lt);
-            out[pos] = (int32_t)(uint32_t)(key & 0xFFFFFFFFull);
-          }
-          __syncwarp();
-          if (ok && lane == 31 - __clz((int)peers)) lcnt[v] += __popc(peers);
-          __syncwarp();
+      __syncthreads();  // every warp's winners are in the candidate area
+      uint32_t wv[kPer];
+      int wrow[kPer];
+#pragma unroll
+      for (int h = 0; h < kPer; ++h) {
+        const int i = tid + h * kTopkThreads;
+        const unsigned long long key = i < my_gt ? cand[i] : 0ull;
+        wv[h] = 0xFFFFFFFFu - (uint32_t)(key >> 32);
+        wrow[h] = i < my_gt ? (int32_t)(uint32_t)(key & 0xFFFFFFFFull) : -1;
+      }
+      __syncthreads();  // candidates read: the area now holds the claimed rows
+      int *claimed = reinterpret_cast<int *>(cand);
+#pragma unroll
+      for (int h = 0; h < kPer; ++h) {
+        if (wrow[h] < 0) continue;
+        if (wv[h] >= (uint32_t)nb_last) {
+          record_error(c.err, DC_CAPACITY, K_TOPK);
+          wrow[h] = -1;
+          continue;
         }
+        const int pos = base[wv[h]] + atomicAdd(&lcnt[wv[h]], 1);
+        if (pos < 0 || pos >= c_gt) {
+          record_error(c.err, DC_CAPACITY, K_TOPK);
+          wrow[h] = -1;
+          continue;
+        }
+        claimed[pos] = wrow[h];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int h = 0; h < kPer; ++h) {
+        if (wrow[h] < 0) continue;
+        const int b = base[wv[h]], cnt = min(lcnt[wv[h]], c_gt - b);
+        int rank = 0;
+        for (int t = 0; t < cnt; ++t) rank += claimed[b + t] < wrow[h];
+        out[b + rank] = wrow[h];
       }
       if (crank == 0)
         for (int i = ksel + tid; i < k; i += kTopkThreads) out[i] = -1;
+      cluster_wait();  // no CTA leaves while another may read its counts
       return;
     }
+    cluster_wait();
   }
   // each CTA sorts its own candidates ...
   __shared__ int sh_nloc;

@@ -98,9 +98,24 @@ __device__ __forceinline__ bool mbar_try_wait(void *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Split cluster barrier: arrive (release) now, wait (acquire) later; every
+// thread of the cluster's CTAs executes both, in this order.  The forms without
+// .aligned are used, so the instructions are valid wherever the warp stands;
+// the warp is also reconverged first.
+__device__ __forceinline__ void cluster_arrive() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  __syncwarp();
+  asm volatile("barrier.cluster.wait.acquire;\n" ::: "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
+// The non-.aligned form, after reconverging the warp.
 __device__ __forceinline__ void named_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+  __syncwarp();
+  asm volatile("barrier.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
 // 16-byte load that does not allocate in L1 (read-once streams, host memory).
