@@ -302,76 +302,11 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       }
     }
   }
+  __syncthreads();  // the slice's locations and first-selection slots are set
 
-  // 4. victims (leader): unprotected slots in LRU order (stamp, slot), empty first
-  const int perB = (B + bs - 1) / bs;
-  const int b0 = min(B, tid * perB), b1 = min(B, b0 + perB);
-  if (crank == 0) {
-    int P = 0;
-    if (M > 0) {
-      int nc = 0;
-#pragma unroll 4
-      for (int i = b0; i < b1; ++i) {
-        const int v = lru_s[i];
-        nc += !((prot[v >> 5] >> (v & 31)) & 1u);
-      }
-      int ncand;
-      int cb = ublock_excl_scan(nc, warp_sums, ncand);
-      P = min(M, ncand);
-      for (int i = b0; i < b1; ++i) {
-        const int v = lru_s[i];
-        if (!((prot[v >> 5] >> (v & 31)) & 1u)) {
-          candB[cb] = v;
-          if (cb < P) atomicOr(&now[v >> 5], 1u << (v & 31));  // stamped by this tick
-          ++cb;
-        }
-      }
-    }
-    if (tid == 0) sh_p = P;
-  }
-  cl.sync();  // S2: every slice's misses are in the miss list; no CTA reads the
-              // leader's memory after this point
-  int P = 0;
-  if (crank == 0) {
-    P = sh_p;
-    // promotions: the first P misses take the victims, in order
-    int ev = 0;
-    for (int p = tid; p < P; p += bs) {
-      const int v = candB[p];
-      const int32_t old = hrow_s[v];
-      const int32_t u = miss[p];
-      if (old >= 0) {
-        hot_map[old] = -1;
-        ++ev;
-      }
-      hot_row[v] = u;
-      hot_stamp[v] = tick;
-      hot_map[u] = v;
-      c.promo_dst[(size_t)r * B + p] = v;
-    }
-    if (ev) atomicAdd(&sh_cnt[5], ev);
-    // 5. LRU order after this tick: untouched slots keep their order, slots
-    //    stamped now follow in ascending slot order
-    if (hits + P > 0) {
-      int na = 0, nb = 0;
-      for (int i = b0; i < b1; ++i) {
-        const int v = lru_s[i];
-        const bool nw_ = (now[v >> 5] >> (v & 31)) & 1u;
-        na += !nw_;
-        tmpB[i] = nw_ ? -1 : v;
-      }
-      for (int v = b0; v < b1; ++v) nb += (now[v >> 5] >> (v & 31)) & 1u;
-      int A, Bt;
-      int ab = ublock_excl_scan(na, warp_sums, A);
-      int bb = ublock_excl_scan(nb, warp_sums, Bt);
-      for (int i = b0; i < b1; ++i)
-        if (tmpB[i] >= 0) lru[ab++] = tmpB[i];
-      for (int v = b0; v < b1; ++v)
-        if ((now[v >> 5] >> (v & 31)) & 1u) lru[A + bb++] = v;
-    }
-  }
-
-  // 6. one location per selected entry whose row lies in this slice
+  // 4. one location per selected entry whose row lies in this slice (they
+  //    depend on the ranks only, so every CTA forms them before the leader's
+  //    victim choice)
   int sel_here = 0, missel = 0;
   for (int e0 = tid; e0 < nsel; e0 += kBatch * bs) {
     int32_t sv[kBatch];
@@ -411,11 +346,79 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   atomicAdd(&sh_cnt[3], sel_here);
   atomicAdd(&sh_cnt[4], missel);
   __syncthreads();  // the query masks of the slice are complete
-  // 7. second half of each union entry: the queries that selected the row
+  // 5. second half of each union entry: the queries that selected the row
   for (int q = tid; q < Uc; q += bs)
     *reinterpret_cast<int2 *>(&uent[u_base + q].z) =
         make_int2((int)((umw[q >> 2] >> ((q & 3) * 8)) & 0xFFu), 0);
-  if (!shared) cl.sync();  // every first selection of a miss is known
+  // 6. victims (leader): unprotected slots in LRU order (stamp, slot), empty first
+  const int perB = (B + bs - 1) / bs;
+  const int b0 = min(B, tid * perB), b1 = min(B, b0 + perB);
+  if (crank == 0) {
+    int P = 0;
+    if (M > 0) {
+      int nc = 0;
+#pragma unroll 4
+      for (int i = b0; i < b1; ++i) {
+        const int v = lru_s[i];
+        nc += !((prot[v >> 5] >> (v & 31)) & 1u);
+      }
+      int ncand;
+      int cb = ublock_excl_scan(nc, warp_sums, ncand);
+      P = min(M, ncand);
+      for (int i = b0; i < b1; ++i) {
+        const int v = lru_s[i];
+        if (!((prot[v >> 5] >> (v & 31)) & 1u)) {
+          candB[cb] = v;
+          if (cb < P) atomicOr(&now[v >> 5], 1u << (v & 31));  // stamped by this tick
+          ++cb;
+        }
+      }
+    }
+    if (tid == 0) sh_p = P;
+  }
+  cl.sync();  // S2: every slice's misses are in the miss list and every first
+              // selection of a miss is known; no CTA reads the leader's memory
+              // after this point
+  int P = 0;
+  if (crank == 0) {
+    P = sh_p;
+    // promotions: the first P misses take the victims, in order
+    int ev = 0;
+    for (int p = tid; p < P; p += bs) {
+      const int v = candB[p];
+      const int32_t old = hrow_s[v];
+      const int32_t u = miss[p];
+      if (old >= 0) {
+        hot_map[old] = -1;
+        ++ev;
+      }
+      hot_row[v] = u;
+      hot_stamp[v] = tick;
+      hot_map[u] = v;
+      c.promo_dst[(size_t)r * B + p] = v;
+    }
+    if (ev) atomicAdd(&sh_cnt[5], ev);
+    // 7. LRU order after this tick: untouched slots keep their order, slots
+    //    stamped now follow in ascending slot order
+    if (hits + P > 0) {
+      int na = 0, nb = 0;
+      for (int i = b0; i < b1; ++i) {
+        const int v = lru_s[i];
+        const bool nw_ = (now[v >> 5] >> (v & 31)) & 1u;
+        na += !nw_;
+        tmpB[i] = nw_ ? -1 : v;
+      }
+      for (int v = b0; v < b1; ++v) nb += (now[v >> 5] >> (v & 31)) & 1u;
+      int A, Bt;
+      int ab = ublock_excl_scan(na, warp_sums, A);
+      int bb = ublock_excl_scan(nb, warp_sums, Bt);
+      for (int i = b0; i < b1; ++i)
+        if (tmpB[i] >= 0) lru[ab++] = tmpB[i];
+      for (int v = b0; v < b1; ++v)
+        if ((now[v >> 5] >> (v & 31)) & 1u) lru[A + bb++] = v;
+    }
+  }
+
   // the first selection of each promoted miss also fills its hot slot
   if (!shared && crank == 0)
     for (int p = tid; p < P; p += bs)
