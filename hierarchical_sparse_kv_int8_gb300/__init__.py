@@ -25,7 +25,7 @@ LOC_RING, LOC_OPT, LOC_HOT, LOC_STAGE = 0, 1, 2, 3
 LOC_TIER_SHIFT = 28
 KV_SPLIT, KV_LATENT = 0, 1
 BUF = dict(hot_row=0, hot_stamp=1, hot_data=2, ring=3, stage=4, opt=5, union=6, miss=7,
-           counts=8, lru=9, frontier=10, hot_map=11, opt_map=12)
+           counts=8, lru=9, frontier=10, hot_map=11, opt_map=12, scores=13)
 
 
 class Config(ctypes.Structure):

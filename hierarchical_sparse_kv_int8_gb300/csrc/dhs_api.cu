@@ -207,6 +207,7 @@ BufDesc buffer_desc(const dhs_ctx *c, int which) {
     case DHS_BUF_FRONTIER: return {d.n, N * 8};
     case DHS_BUF_HOT_MAP: return {d.hot_map, N * d.Sm * 4};
     case DHS_BUF_OPT_MAP: return {d.opt_map, N * d.Sm * 4};
+    case DHS_BUF_SCORES: return {d.scores, N * d.Kmax * d.Sm * 4};
     default: return {nullptr, 0};
   }
 }

@@ -9,6 +9,7 @@
 
 #include <cooperative_groups.h>
 
+#include <algorithm>
 #include <climits>
 
 namespace dhs {
@@ -35,7 +36,8 @@ cudaError_t launch_upload(int32_t *dst, const int32_t *words, int n, cudaStream_
 // Rows of up to 128 bytes: one thread per key row, read straight from global
 // memory with 16-byte loads (each thread consumes whole 32-byte sectors); the
 // K_r query chunks are shared-memory broadcasts; dp4a accumulates exact int32
-// dot products.  Wider rows use k_index_score_wide below.
+// dot products.  Rows of 192 to 512 bytes in 64-byte multiples take the
+// tensor cores (k_index_score_tc), other wider rows k_index_score_wide.
 constexpr int kScoreThreads = 256;
 constexpr int kDirectChunks = 8;  // rows up to 128 bytes use direct loads
 
@@ -696,12 +698,285 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
     for (int i = ksel + tid; i < k; i += kTopkThreads) out[i] = -1;
 }
 
+// ---------------------------------------------------------------- scores on tensor cores
+// Rows of 64 * NG bytes (NG = 3..8).  The score of eq. (1) is an exact
+// integer dot product, and so is this kernel's: every int8 value becomes the
+// f16 holding it exactly, the m16n8k16 MMA multiplies 16 key rows by the
+// eight (padded) queries with fp32 accumulation, and every partial sum is an
+// integer of magnitude at most 512 * 128 * 128 = 2^23 < 2^24, so no rounding
+// ever happens and the float result converts back to the exact int32.
+//
+// Work: tiles of 16 consecutive rows of one request; the tiles of all
+// requests form one list, and each warp of the persistent grid owns a
+// contiguous run of it.  Every warp streams its tiles through its own ring of
+// shared-memory stages, one bulk asynchronous copy per tile (the rows are
+// contiguous in global memory and stay dense in the stage), each stage
+// tracked by an mbarrier counting the bytes that landed.  For rows of a
+// multiple of 128 bytes the fragment loads of rows g and g + 1 meet in the
+// same banks (two wavefronts per quarter warp), which the shared-memory
+// pipe absorbs at the rate HBM delivers rows.
+//
+// Fragment layout: the MMA's k index is a permutation of the row's bytes.
+// At 64-byte group i, lane (g = lane / 4, t = lane % 4) loads the 16-byte
+// chunk 4i + t of rows g and g + 8 of the tile; word w of that chunk holds
+// the lane's four k positions (2t, 2t+1, 2t+8, 2t+9) of MMA step 4i + w.  The
+// query fragments are built from the same bytes of the query rows, so both
+// operands see the same permutation and the dot products are unchanged.
+constexpr int kTcWarps = 4;
+constexpr int kTcMaxStages = 8;
+constexpr int kTcSpinLimit = 1 << 22;
+constexpr int kTcMinGroups = 3;
+constexpr int kTcMaxGroups = 8;
+
+
+// int8 x 4 -> two f16 x 2 with the same values: byte b goes to the f16 whose
+// bits are 0x64 | (b ^ 0x80), i.e. 1024 + (b + 128); subtracting 1152 leaves b.
+__device__ __forceinline__ void i8x4_to_f16(uint32_t x, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = x ^ 0x80808080u;
+  uint32_t l = __byte_perm(u, 0x64646464u, 0x5140);
+  uint32_t h = __byte_perm(u, 0x64646464u, 0x7362);
+  const uint32_t bias = 0x64806480u;
+  asm("sub.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"(l), "r"(bias));
+  asm("sub.f16x2 %0, %1, %2;\n" : "=r"(hi) : "r"(h), "r"(bias));
+}
+
+template <int NG>
+__global__ void __launch_bounds__(kTcWarps * 32)
+k_index_score_tc(const DevCtx c, const int8_t *__restrict__ q_idx,
+                 const __grid_constant__ UploadWords ctl, int stages) {
+  constexpr int RB = 64 * NG;
+  constexpr int STRIDE = RB;
+  constexpr int TILE = 16 * STRIDE;
+  constexpr int STEPS = 4 * NG;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t mbar[kTcWarps][kTcMaxStages];
+  __shared__ int warp_sums[32];
+  pdl_wait();
+  pdl_trigger();
+  const int N = c.N, Kmax = c.Kmax;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < N; i += blockDim.x) c.Kr[i] = ctl.w[i];
+    for (int i = tid; i < N * Kmax; i += blockDim.x) c.dom[i] = ctl.w[N + i];
+  }
+  // tile list: request r owns tiles [tstart[r], tstart[r + 1])
+  int *tstart = reinterpret_cast<int *>(smem + (size_t)kTcWarps * stages * TILE);
+  {
+    int carry = 0;
+    for (int base = 0; base < N; base += blockDim.x) {
+      const int r = base + tid;
+      int cnt = 0;
+      if (r < N) {
+        const int Kr = ctl.w[r];
+        int dm = 0;
+        for (int j = 0; j < Kr; ++j) dm = max(dm, ctl.w[N + r * Kmax + j]);
+        cnt = (dm + 15) >> 4;
+      }
+      int tot;
+      const int ex = block_excl_scan(cnt, warp_sums, tot);
+      if (r < N) tstart[r] = carry + ex;
+      carry += tot;
+    }
+    if (tid == 0) tstart[N] = carry;
+    __syncthreads();
+  }
+  const int T = tstart[N];
+  const int64_t W = (int64_t)gridDim.x * kTcWarps, wg = (int64_t)blockIdx.x * kTcWarps + warp;
+  const int tb = (int)(wg * T / W), te = (int)((wg + 1) * T / W);
+  if (tb >= te) return;  // no block-wide barrier follows
+  unsigned char *ring = smem + (size_t)warp * stages * TILE;
+  uint64_t *bar = mbar[warp];
+  if (lane == 0) {
+    for (int s = 0; s < stages; ++s) mbar_init(&bar[s], 1);
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+
+  auto locate = [&](int tile) {  // the request whose tiles contain `tile`
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tstart[mid] <= tile) lo = mid;
+      else hi = mid - 1;
+    }
+    return lo;
+  };
+  auto dom_of = [&](int r) {
+    int dm = 0;
+    for (int j = 0; j < ctl.w[r]; ++j) dm = max(dm, ctl.w[N + r * Kmax + j]);
+    return dm;
+  };
+
+  // producer cursor
+  int pr = locate(tb), ptile = tb, pdom = dom_of(pr);
+  auto issue = [&](int slot) {
+    while (ptile >= tstart[pr + 1]) pdom = dom_of(++pr);
+    const int64_t row0 = (int64_t)(ptile - tstart[pr]) * 16;
+    const int nrows = (int)min((int64_t)16, (int64_t)pdom - row0);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar[slot], (uint32_t)(nrows * RB));
+      bulk_g2s(ring + (size_t)slot * TILE, c.keys[pr] + row0 * RB, (uint32_t)(nrows * RB),
+               &bar[slot]);
+    }
+    ++ptile;
+  };
+  const int pre = min(stages, te - tb);
+  for (int s = 0; s < pre; ++s) issue(s);
+
+  const int g = lane >> 2, t = lane & 3;
+  const int q0 = 2 * t, q1 = 2 * t + 1;
+  uint32_t bq[STEPS][2];
+  int cr = -1, Kr = 0, cdom = 0, dq0 = 0, dq1 = 0;
+  int mn0 = INT_MAX, mx0 = INT_MIN, mn1 = INT_MAX, mx1 = INT_MIN;
+  auto flush = [&]() {  // the request's score range, one atomic per query and warp
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mn0 = min(mn0, __shfl_xor_sync(0xffffffffu, mn0, o));
+      mx0 = max(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mn1 = min(mn1, __shfl_xor_sync(0xffffffffu, mn1, o));
+      mx1 = max(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    if (g == 0 && cr >= 0) {
+      if (q0 < Kr && mn0 <= mx0) {
+        atomicMin(&c.minmax[(cr * Kmax + q0) * 2 + 0], mn0);
+        atomicMax(&c.minmax[(cr * Kmax + q0) * 2 + 1], mx0);
+      }
+      if (q1 < Kr && mn1 <= mx1) {
+        atomicMin(&c.minmax[(cr * Kmax + q1) * 2 + 0], mn1);
+        atomicMax(&c.minmax[(cr * Kmax + q1) * 2 + 1], mx1);
+      }
+    }
+    mn0 = mn1 = INT_MAX;
+    mx0 = mx1 = INT_MIN;
+  };
+
+  int it = 0;
+  bool bad = false;
+  for (int tile = tb; tile < te; ++tile, ++it) {
+    if (cr < 0 || tile >= tstart[cr + 1]) {  // next request: its query fragments
+      flush();
+      cr = cr < 0 ? locate(tile) : cr + 1;
+      while (tile >= tstart[cr + 1]) ++cr;
+      Kr = ctl.w[cr];
+      cdom = dom_of(cr);
+      dq0 = q0 < Kr ? ctl.w[N + cr * Kmax + q0] : 0;
+      dq1 = q1 < Kr ? ctl.w[N + cr * Kmax + q1] : 0;
+      const int8_t *qrow = q_idx + ((size_t)cr * Kmax + g) * RB;
+#pragma unroll
+      for (int i = 0; i < NG; ++i) {
+        const uint4 v = g < Kr ? *reinterpret_cast<const uint4 *>(qrow + (4 * i + t) * 16)
+                               : make_uint4(0u, 0u, 0u, 0u);
+        i8x4_to_f16(v.x, bq[4 * i + 0][0], bq[4 * i + 0][1]);
+        i8x4_to_f16(v.y, bq[4 * i + 1][0], bq[4 * i + 1][1]);
+        i8x4_to_f16(v.z, bq[4 * i + 2][0], bq[4 * i + 2][1]);
+        i8x4_to_f16(v.w, bq[4 * i + 3][0], bq[4 * i + 3][1]);
+      }
+    }
+    const int slot = it % stages;
+    {
+      const uint32_t parity = (uint32_t)((it / stages) & 1);
+      int spins = 0;
+      bool late = false;
+      while (!mbar_try_wait(&bar[slot], parity))
+        if (++spins > kTcSpinLimit) {
+          late = true;
+          break;
+        }
+      if (__any_sync(0xffffffffu, late)) {
+        if (lane == 0) record_error(c.err, DC_TIMEOUT, K_SCORE);
+        bad = true;
+        break;
+      }
+    }
+    const unsigned char *st = ring + (size_t)slot * TILE;
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+#pragma unroll
+    for (int i = 0; i < NG; ++i) {
+      const uint4 lo = *reinterpret_cast<const uint4 *>(st + g * STRIDE + (4 * i + t) * 16);
+      const uint4 hi = *reinterpret_cast<const uint4 *>(st + (g + 8) * STRIDE + (4 * i + t) * 16);
+      const uint32_t wl[4] = {lo.x, lo.y, lo.z, lo.w}, wh[4] = {hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t a0, a1, a2, a3;
+        i8x4_to_f16(wl[w], a0, a2);
+        i8x4_to_f16(wh[w], a1, a3);
+        mma_f16_16816(acc[w], a0, a1, a2, a3, bq[4 * i + w][0], bq[4 * i + w][1]);
+      }
+    }
+    __syncwarp();  // every lane has read the stage: it may be refilled
+    if (ptile < te) issue(slot);
+
+    const int64_t row0 = (int64_t)(tile - tstart[cr]) * 16;
+    const int64_t ra = row0 + g, rb = row0 + g + 8;
+    int v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      v[e] = __float2int_rn((acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]));
+    if (q0 < Kr) {
+      int32_t *o = c.scores + ((size_t)cr * Kmax + q0) * c.Sm;
+      if (ra < cdom) o[ra] = v[0];
+      if (rb < cdom) o[rb] = v[2];
+      if (ra < dq0) { mn0 = min(mn0, v[0]); mx0 = max(mx0, v[0]); }
+      if (rb < dq0) { mn0 = min(mn0, v[2]); mx0 = max(mx0, v[2]); }
+    }
+    if (q1 < Kr) {
+      int32_t *o = c.scores + ((size_t)cr * Kmax + q1) * c.Sm;
+      if (ra < cdom) o[ra] = v[1];
+      if (rb < cdom) o[rb] = v[3];
+      if (ra < dq1) { mn1 = min(mn1, v[1]); mx1 = max(mx1, v[1]); }
+      if (rb < dq1) { mn1 = min(mn1, v[3]); mx1 = max(mx1, v[3]); }
+    }
+  }
+  if (bad) {
+    // copies still in flight land before the warp leaves (each wait bounded)
+    for (int k = it; k < ptile - tb; ++k) {
+      int spins = 0;
+      while (!mbar_try_wait(&bar[k % stages], (uint32_t)((k / stages) & 1)) &&
+             ++spins <= kTcSpinLimit) {
+      }
+    }
+    return;
+  }
+  flush();
+}
+
 cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_out, int max_dom,
                           const int32_t *ctl_words, cudaStream_t s, Timer *tm) {
   UploadWords ctl;
   const int nw = c.N + c.N * c.Kmax;
   for (int i = 0; i < nw; ++i) ctl.w[i] = ctl_words[i];
-  {
+  if (c.idx_row % 64 == 0 && c.idx_row >= 64 * kTcMinGroups && c.idx_row <= 64 * kTcMaxGroups) {
+    // tensor-core scoring on a persistent grid (rows of 192 to 512 bytes;
+    // narrower rows cost the one-thread-per-row kernel fewer dp4a than the
+    // persistent grid's set-up costs at small sizes)
+    using TcKern = void (*)(const DevCtx, const int8_t *, const UploadWords, int);
+    static const TcKern kerns[kTcMaxGroups] = {
+        nullptr, nullptr, k_index_score_tc<3>, k_index_score_tc<4>,
+        k_index_score_tc<5>, k_index_score_tc<6>, k_index_score_tc<7>, k_index_score_tc<8>};
+    static size_t granted[kTcMaxGroups] = {};
+    static int grid_of[kTcMaxGroups] = {};
+    static size_t grid_smem[kTcMaxGroups] = {};
+    const int ng = c.idx_row / 64;
+    const size_t stage_set = (size_t)kTcWarps * 16 * c.idx_row;
+    const int stages = (int)std::min<size_t>(kTcMaxStages, std::max<size_t>(2, (110u << 10) / stage_set));
+    const size_t smem = stage_set * stages + (size_t)(c.N + 1) * 4;
+    TcKern kern = kerns[ng - 1];
+    cudaError_t e;
+    if ((e = ensure_smem(kern, smem, granted[ng - 1])) != cudaSuccess) return e;
+    if (grid_smem[ng - 1] != smem) {
+      int per_sm = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTcWarps * 32, smem);
+      if (e != cudaSuccess) return e;
+      grid_of[ng - 1] = c.sms * std::max(1, per_sm);
+      grid_smem[ng - 1] = smem;
+    }
+    if (tm) tm->begin(K_SCORE, s);
+    e = launch_pdl(kern, dim3(grid_of[ng - 1]), dim3(kTcWarps * 32), smem, s, c, q_idx, ctl, stages);
+    if (tm) tm->end(K_SCORE, s);
+    if (e != cudaSuccess) return e;
+  } else {
     // one CTA per request at least, so that the control words are published
     const int nc = c.idx_row >> 4;
     cudaError_t e;

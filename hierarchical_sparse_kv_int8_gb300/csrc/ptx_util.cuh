@@ -98,6 +98,38 @@ __device__ __forceinline__ bool mbar_try_wait(void *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Bulk asynchronous copy (the tensor memory accelerator, untiled form):
+// `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to
+// this CTA's shared memory; completion is counted in bytes on `bar`, whose
+// current phase must expect them (mbar_arrive_expect_tx).
+__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                         void *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(void *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Makes initialised mbarriers visible to the asynchronous (bulk copy) proxy.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// D = A * B + D, A 16x16 f16 (row), B 16x8 f16 (col), D 16x8 fp32.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Split cluster barrier: arrive (release) now, wait (acquire) later; every
 // thread of the cluster's CTAs executes both, in this order.  The forms without
 // .aligned are used, so the instructions are valid wherever the warp stands;

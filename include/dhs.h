@@ -255,7 +255,10 @@ enum {
   DHS_BUF_FRONTIER = 10, /* int64 [n_slots]: n_r                               */
   DHS_BUF_HOT_MAP = 11,  /* int32 [n_slots][s_max]: row -> hot slot or -1      */
   DHS_BUF_OPT_MAP = 12,  /* int32 [n_slots][s_max]: row -> pool slot or -1     */
-  DHS_BUF_COUNT_ = 13
+  DHS_BUF_SCORES = 13,   /* int32 [n_slots][k_max][s_max]: indexer scores of
+                            the last dhs_select, valid for the rows below the
+                            request's widest query domain                     */
+  DHS_BUF_COUNT_ = 14
 };
 int64_t dhs_buffer_bytes(const dhs_ctx *ctx, int32_t which);
 int dhs_export(dhs_ctx *ctx, int32_t which, void *dst, int64_t bytes, dhs_stream stream);

@@ -65,6 +65,30 @@ TINY_WIDE_FULL = wl.Recipe("tiny_wide_full_range", N=2, K=3, S=1500, H_idx=4, d_
                            rho_within=0.5, rho_cross=0.6, W=16, p=8, seed=22,
                            i8_lo=-128, i8_hi=127)
 
+# Index rows for the remaining scoring paths: 512 B (eight 64-byte groups on
+# the tensor-core path) with full-range int8 and eight queries, so a score
+# reaches 2^23 in magnitude; 320 B, 256 B and 448 B (five, four and seven
+# groups), 144 B and 272 B (the dp4a paths with 16 and 32 lanes per row).
+TINY_TC512_FULL = wl.Recipe("tiny_tc512_full_range", N=3, K=8, S=2100, H_idx=4, d_idx=128,
+                            topk=128, Hq=8, Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=64,
+                            rho_within=0.5, rho_cross=0.6, W=16, p=8, seed=31,
+                            i8_lo=-128, i8_hi=127)
+TINY_TC320 = wl.Recipe("tiny_tc320", N=2, K=5, S=800, H_idx=1, d_idx=320, topk=64, Hq=8,
+                       Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=48, rho_within=0.5,
+                       rho_cross=0.6, W=16, p=8, seed=32, i8_lo=-128, i8_hi=127)
+TINY_TC256 = wl.Recipe("tiny_tc256", N=2, K=8, S=700, H_idx=2, d_idx=128, topk=64, Hq=8,
+                       Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=48, rho_within=0.5,
+                       rho_cross=0.6, W=16, p=8, seed=35, i8_lo=-128, i8_hi=127)
+TINY_TC448 = wl.Recipe("tiny_tc448", N=2, K=2, S=500, H_idx=1, d_idx=448, topk=64, Hq=8,
+                       Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=48, rho_within=0.5,
+                       rho_cross=0.6, W=16, p=8, seed=36)
+TINY_IDX144 = wl.Recipe("tiny_idx144", N=2, K=3, S=600, H_idx=1, d_idx=144, topk=64, Hq=8,
+                        Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=48, rho_within=0.5,
+                        rho_cross=0.6, W=16, p=8, seed=33)
+TINY_IDX272 = wl.Recipe("tiny_idx272", N=2, K=4, S=600, H_idx=1, d_idx=272, topk=64, Hq=8,
+                        Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=48, rho_within=0.5,
+                        rho_cross=0.6, W=16, p=8, seed=34)
+
 
 def _rounds(rec, n_rounds, shared=True, k_sched=None, residency=True, attn_pass=0, label=""):
     run = _runner(rec, attn_pass=attn_pass)
@@ -114,14 +138,65 @@ def test_tiny_mla_latent(attn_pass):
     _rounds(TINY_MLA, 3, attn_pass=attn_pass, label="tiny_mla")
 
 
-@pytest.mark.parametrize("rec", [TINY_IDX16, TINY_IDX32, TINY_WIDE, TINY_WIDE_FULL],
-                         ids=["16B", "32B", "192B", "768B_full_range"])
+@pytest.mark.parametrize("rec", [TINY_IDX16, TINY_IDX32, TINY_WIDE, TINY_WIDE_FULL,
+                                 TINY_TC512_FULL, TINY_TC320, TINY_IDX144, TINY_IDX272],
+                         ids=["16B", "32B", "192B", "768B_full_range", "512B_full_range",
+                              "320B_full_range", "144B", "272B"])
 def test_index_row_widths(rec):
     if rec.i8_hi > 8:  # the full-range recipe must leave the single-pass top-k
         keys = rec.index_keys(0, 1)[0, :rec.S].astype(np.int64)
         sc = keys @ rec.index_queries(0, 0, 1)[0, 0].astype(np.int64)
         assert sc.max() - sc.min() >= 1 << 13
     _rounds(rec, 3, attn_pass=UNION, label=rec.name)
+
+
+@pytest.mark.parametrize("rec", [TINY_GQA, TINY_GQA2, TINY_MLA, TINY_IDX16, TINY_WIDE,
+                                 TINY_WIDE_FULL, TINY_TC512_FULL, TINY_TC320, TINY_IDX144,
+                                 TINY_IDX272, TINY_TC256, TINY_TC448],
+                         ids=["64B", "48B", "128B", "16B", "192B", "768B_full_range",
+                              "512B_full_range", "320B_full_range", "144B", "272B",
+                              "256B_full_range", "448B"])
+def test_index_scores_exact(rec):
+    """Every indexer score over every query's domain equals the exact integer
+    dot product of eq. (1), on each scoring path."""
+    from oracle.dhs_oracle import index_scores
+    import torch
+    run = _runner(rec)
+    run.load_round(0)
+    kr = rec.k_per_req()
+    run.select(kr)
+    sc = run.export("scores", torch.int32, (rec.N, run.Km, rec.s_max)).cpu().numpy()
+    keys = rec.index_keys(0, rec.N)
+    qi = rec.index_queries(0, 0, rec.N)
+    for r in range(rec.N):
+        for j in range(int(kr[r])):
+            want = index_scores(qi[r, j], keys[r], rec.S)
+            assert np.array_equal(sc[r, j, :rec.S].astype(np.int64), want), \
+                "%s scores differ at r=%d j=%d" % (rec.name, r, j)
+    assert run.ctx.stats()["device_error"] == 0
+
+
+def test_index_scores_extreme_values():
+    """The largest magnitudes a 512-byte row can produce: every product is
+    (-128)(-128) or (-128)(127), so the scores are +2^23 and -2^23 + 65536
+    exactly, every row ties, and each top-k is the lowest rows in order."""
+    import torch
+    rec = TINY_TC512_FULL
+    run = _runner(rec)
+    run.load_round(0)
+    run.keys.fill_(-128)
+    run.q_idx.fill_(-128)
+    run.q_idx[:, 1::2].fill_(127)
+    kr = rec.k_per_req()
+    run.select(kr)
+    sc = run.export("scores", torch.int32, (rec.N, run.Km, rec.s_max)).cpu().numpy()
+    topk = run.topk.cpu().numpy()
+    for r in range(rec.N):
+        for j in range(int(kr[r])):
+            want = (1 << 23) if j % 2 == 0 else -(128 * 127 * 512)
+            assert (sc[r, j, :rec.S] == want).all(), "r=%d j=%d" % (r, j)
+            assert np.array_equal(topk[r, j], np.arange(rec.topk)), "r=%d j=%d" % (r, j)
+    assert run.ctx.stats()["device_error"] == 0
 
 
 @pytest.mark.parametrize("attn_pass", [PER_QUERY, UNION])
