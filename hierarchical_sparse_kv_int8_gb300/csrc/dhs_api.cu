@@ -207,7 +207,7 @@ BufDesc buffer_desc(const dhs_ctx *c, int which) {
     case DHS_BUF_FRONTIER: return {d.n, N * 8};
     case DHS_BUF_HOT_MAP: return {d.hot_map, N * d.Sm * 4};
     case DHS_BUF_OPT_MAP: return {d.opt_map, N * d.Sm * 4};
-    case DHS_BUF_SCORES: return {d.scores, N * d.Kmax * d.Sm * 4};
+    case DHS_BUF_SCORES: return {d.scores, N * d.Kmax * d.Ss * 4};
     default: return {nullptr, 0};
   }
 }
@@ -292,6 +292,7 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   d.Kmax = g.k_max;
   d.k = g.topk;
   d.Sm = g.s_max;
+  d.Ss = (g.s_max + 31) / 32 * 32;
   d.idx_row = g.idx_heads * g.idx_dim;
   d.Hq = g.q_heads;
   d.Hkv = g.kv_heads;
@@ -353,7 +354,7 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   ALLOC(d.opt_map, N * (size_t)d.Sm);
   ALLOC(d.opt_list, N * (size_t)std::max<int64_t>(1, d.opt_max));
   ALLOC(d.opt_count, N);
-  ALLOC(d.scores, N * d.Kmax * (size_t)d.Sm);
+  ALLOC(d.scores, N * d.Kmax * (size_t)d.Ss);
   ALLOC(d.minmax, N * d.Kmax * 2);
   ALLOC(d.uni, N * KK);
   ALLOC(d.uent, N * KK);

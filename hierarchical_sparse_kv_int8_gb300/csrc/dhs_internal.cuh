@@ -49,6 +49,7 @@ enum DeviceCheck {
 struct DevCtx {
   int N, Kmax, k;
   int64_t Sm;
+  int64_t Ss;  // row stride of the score buffer: Sm rounded up to 32
   int idx_row;           // H_idx * d_idx bytes per index-key row
   int Hq, Hkv, dqk, dv, row;  // row = bf16 elements per stored row
   int layout;

@@ -105,7 +105,7 @@ k_index_score(const DevCtx c, const int8_t *__restrict__ q_idx,
     const int64_t s = row0 + t;
 #pragma unroll
     for (int j = 0; j < kMaxKmax; ++j)
-      if (j < Kr) c.scores[((size_t)r * c.Kmax + j) * c.Sm + s] = acc[j];
+      if (j < Kr) c.scores[((size_t)r * c.Kmax + j) * c.Ss + s] = acc[j];
   }
   // range of each query's scores over its domain: one atomic per CTA and query
   __shared__ int smn[kScoreThreads / 32][kMaxKmax], smx[kScoreThreads / 32][kMaxKmax];
@@ -205,7 +205,7 @@ k_index_score_wide(const DevCtx c, const int8_t *__restrict__ q_idx,
   const int dq = qm < Kr ? qdom[qm] : 0;
   int mn = INT_MAX, mx = INT_MIN;
   const int8_t *keys = c.keys[r];
-  int32_t *out = c.scores + ((size_t)r * c.Kmax + min(qm, c.Kmax - 1)) * c.Sm;
+  int32_t *out = c.scores + ((size_t)r * c.Kmax + min(qm, c.Kmax - 1)) * c.Ss;
   constexpr int kWarps = kScoreThreads / 32;
   for (int64_t g0 = b0 + wid * RPW; g0 < b1; g0 += (int64_t)kWarps * RPW * BR) {
     uint4 kv[BR][CPL];
@@ -301,6 +301,7 @@ constexpr int kTopkThreads = 1024;
 constexpr int kTopkCluster = 4;
 constexpr int kRadixBits = 13;
 constexpr int kBinsPerThread = (1 << kRadixBits) / kTopkThreads;
+constexpr int kTopkSpinLimit = 1 << 22;  // bounded wait for the staged scores
 static_assert(kMaxTopk <= 2 * kTopkThreads, "the exact placement holds two winners per thread");
 
 __device__ __forceinline__ int block_excl_scan(int v, int *warp_sums, int &total) {
@@ -390,7 +391,7 @@ __device__ void bitonic_sort_regs(unsigned long long (&x)[2], unsigned long long
 }
 
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
-k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
+k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char smem[];
@@ -402,7 +403,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
   if (j >= c.Kr[r]) return;  // the whole cluster leaves together
   const int dom = c.dom[r * c.Kmax + j];
   const int k = c.k;
-  const int32_t *__restrict__ sc = c.scores + ((size_t)r * c.Kmax + j) * c.Sm;
+  const int32_t *__restrict__ sc = c.scores + ((size_t)r * c.Kmax + j) * c.Ss;
   int32_t *out = topk_out + ((size_t)r * c.Kmax + j) * k;
   int kp = 1;
   while (kp < k) kp <<= 1;
@@ -411,12 +412,40 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
   __shared__ int warp_sums[32];
   __shared__ int wgt[32], weq[32];
   __shared__ int sh_bin, sh_above, sh_cta_gt, sh_cta_eq;
+  __shared__ int ccnt[kTopkThreads];  // per-thread run counts of a radix pass
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int ksel = min(k, dom);
   const int part = (((dom + kTopkCluster - 1) / kTopkCluster) + 31) & ~31;
   const int p0 = min(dom, crank * part), p1 = min(dom, p0 + part);
   const int lo = c.minmax[(r * c.Kmax + j) * 2 + 0];
   const int hi = c.minmax[(r * c.Kmax + j) * 2 + 1];
+  // This CTA's part of the scores, read by every pass below: when it fits
+  // (stage_cap scores), one bulk asynchronous copy brings it into shared
+  // memory first; otherwise the passes read global memory.
+  const bool staged = p1 - p0 <= stage_cap && dom > k;
+  int32_t *stg = reinterpret_cast<int32_t *>(smem + (((size_t)kp * 8 + 15) & ~(size_t)15) +
+                                             ((size_t)2 << kRadixBits) * 4);
+  if (staged && p1 > p0) {
+    __shared__ __align__(8) uint64_t sbar;
+    if (tid == 0) {
+      mbar_init(&sbar, 1);
+      fence_proxy_async_smem();
+      const uint32_t bytes = (uint32_t)(((p1 - p0) * 4 + 15) & ~15);
+      mbar_arrive_expect_tx(&sbar, bytes);
+      bulk_g2s(stg, sc + p0, bytes, &sbar);
+    }
+    __syncthreads();
+    int spins = 0;
+    while (!mbar_try_wait(&sbar, 0u))
+      if (++spins > kTopkSpinLimit) {
+        record_error(c.err, DC_TIMEOUT, K_TOPK);
+        spins = 0;
+        while (!mbar_try_wait(&sbar, 0u) && ++spins <= kTopkSpinLimit) {
+        }
+        break;
+      }
+  }
+  auto val = [&](int s) -> int32_t { return staged ? stg[s - p0] : sc[s]; };
   // Once every CTA of the cluster has read the range (after its first
   // cluster barrier), the leader empties it for the next round's scores.
   auto empty_range = [&]() {
@@ -429,7 +458,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
   int nloc = 0;  // candidates this CTA holds
   if (dom <= k) {
     for (int s = p0 + tid; s < p1; s += kTopkThreads)
-      cand[s - p0] = topk_key((uint32_t)(sc[s] - lo), s);
+      cand[s - p0] = topk_key((uint32_t)(val(s) - lo), s);
     nloc = p1 - p0;
   } else {
     const uint32_t range = (uint32_t)(hi - lo);
@@ -451,61 +480,74 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
       __syncthreads();
 #pragma unroll 4
       for (int s = p0 + tid; s < p1; s += kTopkThreads) {
-        const uint32_t v = (uint32_t)(sc[s] - lo);
+        const uint32_t v = (uint32_t)(val(s) - lo);
         if ((uint32_t)((unsigned long long)v >> (shift + width)) == prefix)
           atomicAdd(&hist[(v >> shift) & (nbins - 1)], 1u);
       }
-      cl.sync();  // all histograms of the cluster are complete
-      // thread t owns a run of bins counted from the top; an exclusive scan in
-      // thread order counts the rows above each run
+      // thread t owns a run of bins counted from the top; the runs' counts
+      // in this CTA first, so that only runs at or above the threshold need
+      // the cluster's bins one by one
       const int per = (nbins + kTopkThreads - 1) / kTopkThreads;
       const int b_hi = nbins - tid * per;
       const int b_lo = max(0, b_hi - per);
-      int gsum[kBinsPerThread], psum[kBinsPerThread];  // cluster count; count in earlier CTAs
-      int local = 0;
-#pragma unroll
-      for (int t = 0; t < kBinsPerThread; ++t) {
-        const int b = b_lo + t;
-        int g = 0, pc = 0;
-        if (b < b_hi) {
-#pragma unroll
-          for (int q = 0; q < kTopkCluster; ++q) {
-            const int hv = (int)hr[q][b];
-            g += hv;
-            if (q < crank) pc += hv;
-          }
-        }
-        gsum[t] = g;
-        psum[t] = pc;
-        local += g;
+      __syncthreads();  // this CTA's histogram is complete
+      {
+        int lc = 0;
+        for (int b = b_lo; b < b_hi; ++b) lc += (int)hist[b];
+        ccnt[tid] = lc;
       }
+      cl.sync();  // all histograms of the cluster are complete
+      int local = 0;  // the run's count in the cluster
+#pragma unroll
+      for (int q = 0; q < kTopkCluster; ++q) local += *cl.map_shared_rank(&ccnt[tid], q);
+      // an exclusive scan in thread order counts the rows above each run
       int total;
-      const int above = block_excl_scan(b_hi > 0 ? local : 0, warp_sums, total);
-      if (b_hi > 0 && above < k_rem && k_rem <= above + local) {
-        int acc = above;
+      const int above = block_excl_scan(local, warp_sums, total);
+      const bool exact_pass = passes == 1 && shift == 0;
+      if (local > 0 && above < k_rem && (exact_pass || k_rem <= above + local)) {
+        int gsum[kBinsPerThread], psum[kBinsPerThread];  // cluster count; count in earlier CTAs
 #pragma unroll
-        for (int t = kBinsPerThread - 1; t >= 0; --t) {
+        for (int t = 0; t < kBinsPerThread; ++t) {
           const int b = b_lo + t;
-          if (b >= b_hi) continue;
-          if (acc + gsum[t] >= k_rem) {
-            sh_bin = b;
-            sh_above = acc;
-            break;
+          int g = 0, pc = 0;
+          if (b < b_hi) {
+#pragma unroll
+            for (int q = 0; q < kTopkCluster; ++q) {
+              const int hv = (int)hr[q][b];
+              g += hv;
+              if (q < crank) pc += hv;
+            }
           }
-          acc += gsum[t];
+          gsum[t] = g;
+          psum[t] = pc;
         }
-      }
-      if (passes == 1 && shift == 0) {
-        // a single pass decides: base[b] = rows of the domain above offset
-        // value b plus rows equal to b in earlier CTAs, for the exact placement
-        int *base = reinterpret_cast<int *>(hist + (1 << kRadixBits));
-        int acc = above;
+        if (k_rem <= above + local) {
+          int acc = above;
 #pragma unroll
-        for (int t = kBinsPerThread - 1; t >= 0; --t) {
-          const int b = b_lo + t;
-          if (b >= b_hi) continue;
-          base[b] = acc + psum[t];
-          acc += gsum[t];
+          for (int t = kBinsPerThread - 1; t >= 0; --t) {
+            const int b = b_lo + t;
+            if (b >= b_hi) continue;
+            if (acc + gsum[t] >= k_rem) {
+              sh_bin = b;
+              sh_above = acc;
+              break;
+            }
+            acc += gsum[t];
+          }
+        }
+        if (exact_pass) {
+          // a single pass decides: base[b] = rows of the domain above offset
+          // value b plus rows equal to b in earlier CTAs, for the exact
+          // placement (needed for the bins above the threshold only)
+          int *base = reinterpret_cast<int *>(hist + (1 << kRadixBits));
+          int acc = above;
+#pragma unroll
+          for (int t = kBinsPerThread - 1; t >= 0; --t) {
+            const int b = b_lo + t;
+            if (b >= b_hi) continue;
+            base[b] = acc + psum[t];
+            acc += gsum[t];
+          }
         }
       }
       __syncthreads();
@@ -525,7 +567,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
     for (int base = r0; base < r1; base += 32) {
       const int s = base + lane;
       const bool ok = s < r1;
-      const uint32_t v = ok ? (uint32_t)(sc[s] - lo) : 0u;
+      const uint32_t v = ok ? (uint32_t)(val(s) - lo) : 0u;
       ngt += __popc(__ballot_sync(0xffffffffu, ok && v > T));
       neq += __popc(__ballot_sync(0xffffffffu, ok && v == T));
     }
@@ -570,7 +612,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out) {
          bs += 32) {
       const int s = bs + lane;
       const bool ok = s < r1;
-      const uint32_t v = ok ? (uint32_t)(sc[s] - lo) : 0u;
+      const uint32_t v = ok ? (uint32_t)(val(s) - lo) : 0u;
       const unsigned bgt = __ballot_sync(0xffffffffu, ok && v > T);
       const unsigned beq = __ballot_sync(0xffffffffu, ok && v == T);
       if (ok && v > T) cand[gt_off + __popc(bgt & lt)] = topk_key(v, s);
@@ -915,14 +957,14 @@ k_index_score_tc(const DevCtx c, const int8_t *__restrict__ q_idx,
     for (int e = 0; e < 4; ++e)
       v[e] = __float2int_rn((acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]));
     if (q0 < Kr) {
-      int32_t *o = c.scores + ((size_t)cr * Kmax + q0) * c.Sm;
+      int32_t *o = c.scores + ((size_t)cr * Kmax + q0) * c.Ss;
       if (ra < cdom) o[ra] = v[0];
       if (rb < cdom) o[rb] = v[2];
       if (ra < dq0) { mn0 = min(mn0, v[0]); mx0 = max(mx0, v[0]); }
       if (rb < dq0) { mn0 = min(mn0, v[2]); mx0 = max(mx0, v[2]); }
     }
     if (q1 < Kr) {
-      int32_t *o = c.scores + ((size_t)cr * Kmax + q1) * c.Sm;
+      int32_t *o = c.scores + ((size_t)cr * Kmax + q1) * c.Ss;
       if (ra < cdom) o[ra] = v[1];
       if (rb < cdom) o[rb] = v[3];
       if (ra < dq1) { mn1 = min(mn1, v[1]); mx1 = max(mx1, v[1]); }
@@ -1008,13 +1050,21 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_ou
   }
   int kp = 1;
   while (kp < c.k) kp <<= 1;
-  const size_t smem_topk = (size_t)kp * 8 + ((size_t)1 << kRadixBits) * 8;
+  size_t smem_topk = (size_t)kp * 8 + ((size_t)1 << kRadixBits) * 8;
+  // a CTA's part of the widest domain, staged in shared memory when it fits
+  const int part = ((max(max_dom, 1) + kTopkCluster - 1) / kTopkCluster + 31) & ~31;
+  int stage_cap = 0;
+  if (smem_topk + 8 + (size_t)part * 4 <= kMaxDynSmem) {
+    stage_cap = part;
+    smem_topk = (((size_t)kp * 8 + 15) & ~(size_t)15) + ((size_t)2 << kRadixBits) * 4 +
+                (size_t)part * 4;
+  }
   static size_t granted_topk = 0;
   cudaError_t e2 = ensure_smem(k_topk, smem_topk, granted_topk);
   if (e2 != cudaSuccess) return e2;
   if (tm) tm->begin(K_TOPK, s);
   e2 = launch_pdl(k_topk, dim3(c.N * c.Kmax * kTopkCluster), dim3(kTopkThreads), smem_topk, s, c,
-                  topk_out);
+                  topk_out, stage_cap);
   if (tm) tm->end(K_TOPK, s);
   return e2;
 }

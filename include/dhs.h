@@ -255,8 +255,9 @@ enum {
   DHS_BUF_FRONTIER = 10, /* int64 [n_slots]: n_r                               */
   DHS_BUF_HOT_MAP = 11,  /* int32 [n_slots][s_max]: row -> hot slot or -1      */
   DHS_BUF_OPT_MAP = 12,  /* int32 [n_slots][s_max]: row -> pool slot or -1     */
-  DHS_BUF_SCORES = 13,   /* int32 [n_slots][k_max][s_max]: indexer scores of
-                            the last dhs_select, valid for the rows below the
+  DHS_BUF_SCORES = 13,   /* int32 [n_slots][k_max][S]: indexer scores of the
+                            last dhs_select, S = s_max rounded up to a
+                            multiple of 32; valid for the rows below the
                             request's widest query domain                     */
   DHS_BUF_COUNT_ = 14
 };

@@ -165,7 +165,8 @@ def test_index_scores_exact(rec):
     run.load_round(0)
     kr = rec.k_per_req()
     run.select(kr)
-    sc = run.export("scores", torch.int32, (rec.N, run.Km, rec.s_max)).cpu().numpy()
+    ss = (rec.s_max + 31) // 32 * 32  # score rows are padded to 32
+    sc = run.export("scores", torch.int32, (rec.N, run.Km, ss)).cpu().numpy()
     keys = rec.index_keys(0, rec.N)
     qi = rec.index_queries(0, 0, rec.N)
     for r in range(rec.N):
@@ -189,7 +190,8 @@ def test_index_scores_extreme_values():
     run.q_idx[:, 1::2].fill_(127)
     kr = rec.k_per_req()
     run.select(kr)
-    sc = run.export("scores", torch.int32, (rec.N, run.Km, rec.s_max)).cpu().numpy()
+    ss = (rec.s_max + 31) // 32 * 32  # score rows are padded to 32
+    sc = run.export("scores", torch.int32, (rec.N, run.Km, ss)).cpu().numpy()
     topk = run.topk.cpu().numpy()
     for r in range(rec.N):
         for j in range(int(kr[r])):
