@@ -21,11 +21,13 @@
 // pair of the kv head's group, K_max x G rows padded to 16; S = Q K^T over 16
 // rows at a time, a score is kept only if its query selected the row (a bit of
 // the row's query mask; block row i is seen by queries j >= i), online softmax
-// in log2 units, O += P V.
+// in log2 units, O += P V.  The query tile sits in shared memory and is read
+// with ldmatrix at every k-step, which keeps the registers of a 128-dim warp
+// within the budget of two CTAs per SM.
 //   - 128-dim heads: a warp owns one 16-row M-tile.
 //   - MLA latent rows (576-dim keys, 512-dim values): four warps share each
 //     M-tile, one quarter of the key and value dims each (partial scores
-//     summed in shared memory); the query tile is read from shared memory.
+//     summed in shared memory).
 // The warps that cover all M-tiles form a group; the CTA's groups walk
 // alternate 16-row tiles, each group with its own ring of stages whose copies
 // are tracked by mbarriers (every thread of the group ties its cp.async
@@ -50,6 +52,10 @@ constexpr int kUMaxGroups = 8;
 constexpr int kUMaxStages = 32;
 constexpr int kUMaxClusters = 8;  // clusters per (request, kv head)
 constexpr int kUSpinLimit = 1 << 20;  // bounded wait for a stage's copies
+constexpr int kUMinStages = 4;
+constexpr size_t kSmemPerSm = 228 * 1024;        // shared memory of one SM
+constexpr size_t kSmemReservedPerCta = 1024;     // taken by the system per resident CTA
+constexpr size_t kStaticSmemMargin = 512;        // the kernel's static shared memory
 
 template <int DQK, int DV>
 struct UShape {
@@ -65,8 +71,9 @@ struct UShape {
   static constexpr int KCH = DQK * 2 / 16;           // chunks of the key part
   static constexpr int kWarpsTarget = kMla ? 16 : 4;
   static constexpr int kMaxThreads = kMla ? 512 : 256;  // up to 8 M-tiles of 128-dim heads
-  // shared memory aimed at per CTA: three CTAs per SM for 128-dim heads
-  static constexpr size_t kSmemTarget = kMla ? kMaxDynSmem : 72 * 1024;
+  // CTAs per SM aimed at: three for 128-dim heads, one for MLA rows
+  static constexpr int kMaxCtasPerSm = kMla ? 1 : 3;
+  static constexpr int kMinCtas = kMla ? 1 : 2;  // registers sized for this many per SM
   static_assert(KW % 16 == 0 && VW % 16 == 0, "dims per warp must be multiples of 16");
 };
 
@@ -101,31 +108,42 @@ static UPlan make_uplan(const DevCtx &c) {
   const int tiles_per_group = (p.chunk_max / 16 + p.NG - 1) / p.NG;
   auto al = [](size_t x) { return (x + 127) / 128 * 128; };
   const size_t stride = (size_t)SH::RE * 2 + 16;
-  const size_t qbytes = SH::kMla ? (size_t)p.MT * 16 * (DQK * 2 + 16) : 0;
+  const size_t qbytes = (size_t)p.MT * 16 * (DQK * 2 + 16);
   const size_t red = SH::kMla ? (size_t)p.NG * 2 * p.MT * SH::NW * 32 * 8 * 4 : 0;
   // receive buffer of the cluster merge: every warp group of every CTA pushes
   // its (O, m, l) for the RO rows each CTA finishes
   p.RO = (p.M + kUCluster - 1) / kUCluster;
   const size_t part = (size_t)kUCluster * p.NG * p.RO * (DV + 2) * 4;
   const size_t wt = ((size_t)kUMaxRowsOwn * kUCluster * kUMaxGroups + 2 * kUMaxRowsOwn) * 4;
-  // enough stages for all of a group's tiles, as far as shared memory allows
+  // enough stages for all of a group's tiles, as far as shared memory allows:
+  // the most CTAs per SM that still leave each group kUMinStages stages (or
+  // all its tiles), then the most stages at that residency
   int stg0 = tiles_per_group + 1;
   if (stg0 > kUMaxStages) stg0 = kUMaxStages;
   if (stg0 < 2) stg0 = 2;
-  const size_t budget = SH::kSmemTarget;
-  for (int pass = 0; pass < 2; ++pass) {
-    for (p.STG = stg0; p.STG >= 2; --p.STG) {
-      const size_t stages = (size_t)p.NG * p.STG * 16 * stride;
-      p.off_q = (int)al(stages);
-      p.off_red = (int)al(p.off_q + qbytes);
-      const size_t main_end = al(p.off_red + red);
-      p.off_mbar = (int)al(main_end > part ? main_end : part);  // the merge reuses the stages
-      p.off_meta = (int)al(p.off_mbar + (size_t)p.NG * p.STG * 8);
-      p.off_wt = (int)al(p.off_meta + (size_t)p.chunk_max * 16);
-      p.smem = (int)(p.off_wt + wt);
-      if ((size_t)p.smem <= (pass == 0 ? budget : kMaxDynSmem)) return p;
-    }
+  const int stg_min = stg0 < kUMinStages ? stg0 : kUMinStages;
+  auto layout = [&](int stg) {
+    p.STG = stg;
+    const size_t stages = (size_t)p.NG * p.STG * 16 * stride;
+    p.off_q = (int)al(stages);
+    p.off_red = (int)al(p.off_q + qbytes);
+    const size_t main_end = al(p.off_red + red);
+    p.off_mbar = (int)al(main_end > part ? main_end : part);  // the merge reuses the stages
+    p.off_meta = (int)al(p.off_mbar + (size_t)p.NG * p.STG * 8);
+    p.off_wt = (int)al(p.off_meta + (size_t)p.chunk_max * 16);
+    p.smem = (int)(p.off_wt + wt);
+    return (size_t)p.smem;
+  };
+  for (int per_sm = SH::kMaxCtasPerSm; per_sm >= 1; --per_sm) {
+    const size_t budget =
+        per_sm == 1 ? kMaxDynSmem : kSmemPerSm / per_sm - kSmemReservedPerCta - kStaticSmemMargin;
+    if (layout(stg_min) > budget) continue;
+    for (int stg = stg0; stg > stg_min; --stg)
+      if (layout(stg) <= budget) return p;
+    layout(stg_min);
+    return p;
   }
+  layout(2);
   return p;
 }
 
@@ -142,7 +160,8 @@ __device__ __forceinline__ int useg(int ch, int kvh, int Hkv) {
 }
 
 template <int DQK, int DV>
-__global__ void __cluster_dims__(kUCluster, 1, 1) __launch_bounds__(UShape<DQK, DV>::kMaxThreads)
+__global__ void __cluster_dims__(kUCluster, 1, 1)
+    __launch_bounds__(UShape<DQK, DV>::kMaxThreads, UShape<DQK, DV>::kMinCtas)
 k_uattn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restrict__ block,
         uint16_t *__restrict__ out, float *__restrict__ lse, const UPlan pl) {
   using SH = UShape<DQK, DV>;
@@ -221,40 +240,23 @@ k_uattn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restri
     return (uint32_t)meta[e - cb].z;
   };
 
-  // query fragments (A operand): row m of the M side is query m / G, head m % G
+  // query tile in shared memory (A operand, read by ldmatrix): row m of the M
+  // side is query m / G, head m % G
   const int mrow0 = mt * 16 + g, mrow1 = mrow0 + 8;
   const int j0 = mrow0 / G, j1 = mrow1 / G;
-  uint32_t qa[SH::kMla ? 1 : KS][4];
   uint16_t *qs = reinterpret_cast<uint16_t *>(smem + pl.off_q);
   constexpr int QSTR = DQK + 8;  // elements per query row in shared memory
   auto load_q = [&]() {
-    if constexpr (!SH::kMla) {
-      const bool v0 = mrow0 < M && j0 < Kr, v1 = mrow1 < M && j1 < Kr;
-      const uint16_t *q0 =
-          q + (((size_t)r * c.Kmax + j0) * c.Hq + (size_t)kvh * G + (mrow0 - j0 * G)) * DQK;
-      const uint16_t *q1 =
-          q + (((size_t)r * c.Kmax + j1) * c.Hq + (size_t)kvh * G + (mrow1 - j1 * G)) * DQK;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const int col = ks * 16 + 2 * t4;
-        qa[ks][0] = v0 ? *reinterpret_cast<const uint32_t *>(q0 + col) : 0u;
-        qa[ks][1] = v1 ? *reinterpret_cast<const uint32_t *>(q1 + col) : 0u;
-        qa[ks][2] = v0 ? *reinterpret_cast<const uint32_t *>(q0 + col + 8) : 0u;
-        qa[ks][3] = v1 ? *reinterpret_cast<const uint32_t *>(q1 + col + 8) : 0u;
-      }
-    } else {
-      for (int idx = tid; idx < MT16 * (DQK / 8); idx += nthr) {
-        const int m = idx / (DQK / 8), ch = idx - m * (DQK / 8);
-        const int j = m / G;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (m < M && j < Kr)
-          v = *reinterpret_cast<const uint4 *>(
-              q + (((size_t)r * c.Kmax + j) * c.Hq + (size_t)kvh * G + (m - j * G)) * DQK +
-              ch * 8);
-        *reinterpret_cast<uint4 *>(qs + (size_t)m * QSTR + ch * 8) = v;
-      }
-      __syncthreads();
+    for (int idx = tid; idx < MT16 * (DQK / 8); idx += nthr) {
+      const int m = idx / (DQK / 8), ch = idx - m * (DQK / 8);
+      const int j = m / G;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (m < M && j < Kr)
+        v = *reinterpret_cast<const uint4 *>(
+            q + (((size_t)r * c.Kmax + j) * c.Hq + (size_t)kvh * G + (m - j * G)) * DQK + ch * 8);
+      *reinterpret_cast<uint4 *>(qs + (size_t)m * QSTR + ch * 8) = v;
     }
+    __syncthreads();
   };
 
   // this group's tiles of the CTA's part: grp, grp + NG, ...
@@ -351,16 +353,9 @@ k_uattn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restri
       for (int ks = 0; ks < KS; ++ks) {
         const int col = wi * SH::KW + ks * 16 + (mi & 1) * 8;
         uint32_t a[4];
-        if constexpr (SH::kMla) {
-          ldmatrix_x4(a[0], a[1], a[2], a[3],
-                      qs + (size_t)(mt * 16 + (lane & 15)) * QSTR + wi * SH::KW + ks * 16 +
-                          (lane >> 4) * 8);
-        } else {
-          a[0] = qa[ks][0];
-          a[1] = qa[ks][1];
-          a[2] = qa[ks][2];
-          a[3] = qa[ks][3];
-        }
+        ldmatrix_x4(a[0], a[1], a[2], a[3],
+                    qs + (size_t)(mt * 16 + (lane & 15)) * QSTR + wi * SH::KW + ks * 16 +
+                        (lane >> 4) * 8);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(b0, b1, b2, b3, rowp + col * 2);
         mma_bf16_16816(s[0], a, b0, b1);
