@@ -288,9 +288,24 @@ k_uattn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restri
     }
     if (late_pass) cp_async_arrive_noinc(&mbar[it % STG]);
   };
+  // both passes at once (inside the walk, after the wait): the tile's row
+  // addresses are decoded once
   auto issue = [&](int it) {
-    issue_pass(it, false);
-    issue_pass(it, true);
+    if (it >= ntg) return;
+    const int tile = grp + it * pl.NG;
+    unsigned char *sb = gbuf + (size_t)(it % STG) * 16 * stride;
+    bool late;
+    const uint16_t *mysrc = row_src(cb + tile * 16 + (lane & 15), late);
+    for (int rr = wig; rr < 16; rr += GW) {
+      const uint16_t *src = reinterpret_cast<const uint16_t *>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mysrc), rr));
+      for (int ch = lane; ch < NCH; ch += 32)
+        cp_async_16_zfill(sb + (size_t)rr * stride + ch * 16,
+                          src ? (const void *)(src + useg<DQK, DV>(ch, kvh, c.Hkv))
+                              : (const void *)c.ring,
+                          src ? 16 : 0);
+    }
+    cp_async_arrive_noinc(&mbar[it % STG]);
   };
   auto wait_stage = [&](int it) {
     const int slot = it % STG;
@@ -410,12 +425,14 @@ k_uattn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restri
     }
     l0 = l0 * al0 + ps0;
     l1 = l1 * al1 + ps1;
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {  // a running max moved
 #pragma unroll
-    for (int i = 0; i < VT; ++i) {
-      o[i][0] *= al0;
-      o[i][1] *= al0;
-      o[i][2] *= al1;
-      o[i][3] *= al1;
+      for (int i = 0; i < VT; ++i) {
+        o[i][0] *= al0;
+        o[i][1] *= al0;
+        o[i][2] *= al1;
+        o[i][3] *= al1;
+      }
     }
     uint32_t pa[4];
     pa[0] = pack_bf16(s[0][0], s[0][1]);
