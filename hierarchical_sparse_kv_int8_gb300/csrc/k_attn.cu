@@ -7,7 +7,10 @@
 // Split-KV flash decoding.  One CTA of four warps handles one split (a range
 // of the row list) of one (request, query, kv head) item.  Rows are gathered
 // by location into shared memory with 16-byte cp.async, three stages in
-// flight.  The query heads that share the kv head (padded to 16) form the M
+// flight, each tracked by an mbarrier.  The split's rows of the hot cache,
+// optional pool and draft ring, and its block rows, are attended first, while
+// the preceding gather may still be running; its staging rows follow once the
+// gather has finished.  The query heads that share the kv head (padded to 16) form the M
 // side of bf16 mma.sync m16n8k16 tensor-core products with fp32 accumulation:
 // S = Q K^T over 16 rows at a time, online softmax in log2 units, O += P V.
 //   - GQA rows (128-dim heads): the four warps are independent, each takes
@@ -31,6 +34,7 @@ namespace dhs {
 constexpr int kAttnStages = 3;
 constexpr int kTileRows = 16;
 constexpr int kAttnThreads = 128;
+constexpr int kAttnSpinLimit = 1 << 20;  // bounded wait for a stage's copies
 
 bool attn_shape_supported(int dqk, int dv, int layout) {
   if (layout == DHS_KV_SPLIT) return dqk == 128 && dv == 128;
@@ -88,8 +92,10 @@ static size_t attn_smem_bytes(int row_elems, int n_split) {
   return body + (size_t)SH::SUB * kAttnStages * kTileRows * 4 + 2 * SH::NW * 32 * 8 * 4 + 64;
 }
 
-// Locations of one split, prefetched once into shared memory.
+// Locations of one split, prefetched once into shared memory, followed by the
+// two row lists of the processing order (int16 positions within the split).
 static size_t attn_loc_bytes(int chunk) { return ((size_t)chunk * 4 + 127) / 128 * 128; }
+static size_t attn_ord_bytes(int chunk) { return ((size_t)chunk * 4 + 127) / 128 * 128; }
 
 template <int DQK, int DV>
 __global__ void __launch_bounds__(kAttnThreads)
@@ -132,78 +138,125 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   for (int e = e0 + tid; e < min(e1, k); e += kAttnThreads) lsm[e - e0] = lrow[e];
   __syncthreads();  // the locations are in shared memory
 
-  // this warp group's tiles: grp, grp + SUB, ...
-  const int ntiles_all = e1 > e0 ? (e1 - e0 + kTileRows - 1) / kTileRows : 0;
-  const int ntiles = ntiles_all > grp ? (ntiles_all - grp + SUB - 1) / SUB : 0;
-  const int gtid = wi * 32 + lane;  // thread index within the group
-  // Copy one 16-row tile into its stage.  Lanes 0..15 of every warp decode
-  // one row's source address (location tag, bounds check) and the group's
-  // threads then copy the rows chunk by chunk, the address broadcast by
-  // shuffle.  Rows of the hot cache, optional pool and draft ring are state of
-  // earlier rounds (the gather before this launch writes only staging rows and
-  // victim hot slots, which no location names): the early pass copies them,
-  // possibly before the preceding launch has finished.  The late pass copies
-  // the staging rows and the caller's block rows, after the wait.
-  auto issue_pass = [&](int it, bool late_pass) {
-    if (it >= ntiles) return;
-    const int tile = grp + it * SUB;
-    unsigned char *st = stage_base + (size_t)(it % kAttnStages) * kTileRows * stride;
-    int *vf = vflag + (it % kAttnStages) * kTileRows;
-    const uint16_t *mysrc = nullptr;
-    bool late = false;
-    if (lane < kTileRows) {
-      const int e = e0 + tile * kTileRows + lane;
-      if (e < e1) {
-        if (e < k) {
-          const int32_t l = lsm[e - e0];
-          if (l >= 0) {
-            mysrc = loc_row(c, r, l);
-            late = loc_tier(l) == DHS_LOC_STAGE;
-            if (mysrc == nullptr && wi == 0 && !late_pass) record_error(c.err, DC_LOC_RANGE, K_ATTN);
-          }
-        } else {
-          mysrc = brow + (size_t)(e - k) * c.row;
-          late = true;
-        }
-      }
-      if (wi == 0 && !late_pass) vf[lane] = mysrc != nullptr;
-    }
-    const unsigned late_rows = __ballot_sync(0xffffffffu, late);
-#pragma unroll 4
-    for (int rr = 0; rr < kTileRows; ++rr) {
-      const uint16_t *src = reinterpret_cast<const uint16_t *>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mysrc), rr));
-      if ((((late_rows >> rr) & 1u) != 0) != late_pass) continue;
-      unsigned char *dst = st + (size_t)rr * stride;
-      for (int v = gtid; v < nv; v += NW * 32)
-        cp_async_16_zfill(dst + v * 16, src ? (const void *)(src + v * 8) : (const void *)c.ring,
-                          src ? 16 : 0);
-    }
-  };
-  auto issue = [&](int it) {
-    issue_pass(it, false);
-    issue_pass(it, true);
-    cp_async_commit();
-  };
-#pragma unroll
-  for (int s = 0; s < kAttnStages - 1; ++s) issue_pass(s, false);
-
-  pdl_wait();
-  pdl_trigger();
   // eq. (9)-(10): block row j enters the draft ring at phi(r, n_r + j); the
   // live ring rows this round reads lie in [n_r - W, n_r) and R_d >= W + K,
-  // so the write never lands on a row being read
+  // so the write never lands on a row being read, and the preceding launch
+  // (the gather) touches no ring row
   if (split == 0 && kvh == 0) {
     const int64_t n = c.n[r];
     const uint4 *src = reinterpret_cast<const uint4 *>(brow + (size_t)j * c.row);
     uint4 *dst = reinterpret_cast<uint4 *>(c.ring + ((size_t)r * c.Rd + (n + j) % c.Rd) * c.row);
     for (int v = tid; v < nv; v += kAttnThreads) dst[v] = src[v];
   }
+
+  // Processing order of the split's rows.  Rows of the hot cache, optional
+  // pool and draft ring are state of earlier rounds, and the caller's queries
+  // and block rows are complete before the round's first kernel; all of them
+  // are attended before the wait on the preceding launch (the gather, which
+  // writes only staging rows and victim hot slots, none of them named by a
+  // location of this round).  Staging rows follow after the wait.  An empty
+  // location adds nothing and is dropped.  Only the order of the softmax sum
+  // changes.
+  int16_t *ord_e = reinterpret_cast<int16_t *>(reinterpret_cast<unsigned char *>(lsm) +
+                                               (((size_t)chunk * 4 + 127) & ~(size_t)127));
+  int16_t *ord_l = ord_e + chunk;
+  __shared__ int wcnt[2][kAttnThreads / 32];
+  int n_early = 0, n_late = 0;
+  for (int base = e0; base < e1; base += kAttnThreads) {
+    const int e = base + tid;
+    bool early = false, late = false;
+    if (e < e1) {
+      if (e >= k) {
+        early = true;  // a block row
+      } else {
+        const int32_t l = lsm[e - e0];
+        if (l >= 0) {
+          late = loc_tier(l) == DHS_LOC_STAGE;
+          early = !late;
+        }
+      }
+    }
+    const unsigned be = __ballot_sync(0xffffffffu, early), bl = __ballot_sync(0xffffffffu, late);
+    if (lane == 0) {
+      wcnt[0][w] = __popc(be);
+      wcnt[1][w] = __popc(bl);
+    }
+    __syncthreads();
+    int pe = n_early, pl = n_late;
 #pragma unroll
-  for (int s = 0; s < kAttnStages - 1; ++s) {
-    issue_pass(s, true);
-    cp_async_commit();
+    for (int ww = 0; ww < kAttnThreads / 32; ++ww) {
+      if (ww < w) {
+        pe += wcnt[0][ww];
+        pl += wcnt[1][ww];
+      }
+      n_early += wcnt[0][ww];
+      n_late += wcnt[1][ww];
+    }
+    const unsigned lt = (1u << lane) - 1u;
+    if (early) ord_e[pe + __popc(be & lt)] = (int16_t)(e - e0);
+    if (late) ord_l[pl + __popc(bl & lt)] = (int16_t)(e - e0);
+    __syncthreads();
   }
+
+  // tiles of 16 listed rows, early tiles first; this group takes tiles grp,
+  // grp + SUB, ...; the first n_pre of them are attended before the wait
+  const int nE = (n_early + kTileRows - 1) / kTileRows;
+  const int ntiles_all = nE + (n_late + kTileRows - 1) / kTileRows;
+  const int ntiles = ntiles_all > grp ? (ntiles_all - grp + SUB - 1) / SUB : 0;
+  const int n_pre = nE > grp ? (nE - grp + SUB - 1) / SUB : 0;
+  const int gtid = wi * 32 + lane;  // thread index within the group
+  __shared__ __align__(8) uint64_t mbar[SUB][kAttnStages];
+  if (gtid == 0)
+    for (int s = 0; s < kAttnStages; ++s) mbar_init(&mbar[grp][s], NW * 32);
+  __syncthreads();
+  // Copy one tile into its stage: lanes 0..15 of every warp decode one row's
+  // source address (location tag, bounds check), the group's threads copy the
+  // rows chunk by chunk with the address broadcast by shuffle, and then tie
+  // their copies to the stage's barrier.
+  auto issue = [&](int it) {
+    const int tile = grp + it * SUB;
+    const bool late_tile = tile >= nE;
+    const int16_t *lst = late_tile ? ord_l : ord_e;
+    const int i0 = (late_tile ? tile - nE : tile) * kTileRows;
+    const int n_in = late_tile ? n_late : n_early;
+    unsigned char *st = stage_base + (size_t)(it % kAttnStages) * kTileRows * stride;
+    int *vf = vflag + (it % kAttnStages) * kTileRows;
+    const uint16_t *mysrc = nullptr;
+    if (lane < kTileRows) {
+      const int i = i0 + lane;
+      if (i < n_in) {
+        const int e = e0 + lst[i];
+        if (e < k) {
+          mysrc = loc_row(c, r, lsm[e - e0]);
+          if (mysrc == nullptr && wi == 0) record_error(c.err, DC_LOC_RANGE, K_ATTN);
+        } else {
+          mysrc = brow + (size_t)(e - k) * c.row;
+        }
+      }
+      if (wi == 0) vf[lane] = mysrc != nullptr;
+    }
+#pragma unroll 4
+    for (int rr = 0; rr < kTileRows; ++rr) {
+      const uint16_t *src = reinterpret_cast<const uint16_t *>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mysrc), rr));
+      unsigned char *dst = st + (size_t)rr * stride;
+      for (int v = gtid; v < nv; v += NW * 32)
+        cp_async_16_zfill(dst + v * 16, src ? (const void *)(src + v * 8) : (const void *)c.ring,
+                          src ? 16 : 0);
+    }
+    cp_async_arrive_noinc(&mbar[grp][it % kAttnStages]);
+  };
+  auto wait_stage = [&](int it) {
+    const uint32_t parity = (uint32_t)((it / kAttnStages) & 1);
+    int spins = 0;
+    while (!mbar_try_wait(&mbar[grp][it % kAttnStages], parity))
+      if (++spins > kAttnSpinLimit) {
+        record_error(c.err, DC_TIMEOUT, K_ATTN);
+        break;
+      }
+  };
+  int issued = 0;
+  for (; issued < min(n_pre, kAttnStages - 1); ++issued) issue(issued);
 
   // query fragments: rows of the A operand are the query heads of this kv head
   uint32_t qa[KS][4];
@@ -230,10 +283,18 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   for (int i = 0; i < VT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
 
+  bool waited = false;
   for (int it = 0; it < ntiles; ++it) {
-    issue(it + kAttnStages - 1);
-    cp_async_wait_group<kAttnStages - 1>();
-    group_sync();
+    if (it == n_pre) {  // the staging rows: after the gather
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
+    // keep kAttnStages - 1 tiles ahead: early tiles at any time, staging
+    // tiles once the wait is over
+    for (; issued < min(waited ? ntiles : n_pre, it + kAttnStages); ++issued) issue(issued);
+    wait_stage(it);
+    group_sync();  // the tile's row flags are visible to the group
     const unsigned char *st = stage_base + (size_t)(it % kAttnStages) * kTileRows * stride;
     const int *vf = vflag + (it % kAttnStages) * kTileRows;
 
@@ -325,6 +386,10 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
     group_sync();  // the stage is refilled by a later issue
   }
   cp_async_wait_all();
+  if (!waited) {  // a split without staging rows still orders itself after the gather
+    pdl_wait();
+    pdl_trigger();
+  }
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -480,7 +545,7 @@ static cudaError_t launch_attn_t(const DevCtx &c, const uint16_t *q, const uint1
                           127) / 128 * 128;
   const int chunk = attn_chunk(c, n_split);
   const size_t smem = attn_smem_bytes<DQK, DV>(c.row, n_split) + 128 + loc_off +
-                      attn_loc_bytes(chunk);
+                      attn_loc_bytes(chunk) + attn_ord_bytes(chunk);
   static size_t granted = 0;
   cudaError_t e = ensure_smem(k_attn<DQK, DV>, smem, granted);
   if (e != cudaSuccess) return e;

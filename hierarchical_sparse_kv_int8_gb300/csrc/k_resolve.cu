@@ -558,22 +558,17 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
   if (vec > kGatherMaxVec) return cudaErrorInvalidValue;
   void (*kern)(const DevCtx, const int32_t *, const int32_t *, int) =
       vec == 1 ? k_gather<1> : vec == 2 ? k_gather<2> : vec == 3 ? k_gather<3> : k_gather<4>;
-  static int resident[kGatherMaxVec + 1] = {};  // CTAs per SM
-  if (!resident[vec]) {
+  static bool carved[kGatherMaxVec + 1] = {};
+  if (!carved[vec]) {
     same_carveout(kern);
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kGatherWarps * 32, 0) !=
-            cudaSuccess || occ < 1) {
-      cudaGetLastError();
-      occ = 1;
-    }
-    // two CTAs per SM (16 warps, 8-16 rows in flight each) saturate the host
-    // link and leave room on every SM for the attention launch that follows
-    resident[vec] = occ < 2 ? occ : 2;
+    carved[vec] = true;
   }
-  // one resident wave over the whole device: every warp keeps BATCH rows of
-  // loads in flight, far more than the host link's bandwidth-delay product
-  int blocks_per_req = (c.sms * resident[vec] + c.N - 1) / c.N;
+  // One CTA per SM, one resident wave over the whole device: 8 warps with
+  // 4-8 rows in flight each saturate the host link (far more than its
+  // bandwidth-delay product), and the registers of two attention CTAs stay
+  // free on every SM, so the attention launch that follows works on its
+  // resident rows while the gather runs.
+  int blocks_per_req = (c.sms + c.N - 1) / c.N;
   if (blocks_per_req < 1) blocks_per_req = 1;
   dim3 grid(blocks_per_req, c.N);
   if (tm) tm->begin(K_GATHER, s);

@@ -212,7 +212,13 @@ int dhs_resolve(dhs_ctx *ctx, const int32_t *topk, int32_t *loc_out, int32_t sha
  *             at phi(r, n_r + u), eq. (10)
  *   loc       device int32 [n_slots][k_max][topk] from dhs_resolve
  *   out       device bf16 [n_slots][k_max][q_heads][v_dim]
- *   lse       device fp32 [n_slots][k_max][q_heads] natural-log sum-exp, or NULL */
+ *   lse       device fp32 [n_slots][k_max][q_heads] natural-log sum-exp, or NULL
+ * Follows the dhs_resolve of the same round on the stream.  The kernel
+ * attends the rows held on the GPU (hot cache, optional pool, draft ring) and
+ * the block rows while the resolve's host gather is still running, and the
+ * staging rows after it; q, block_kv and loc must therefore be complete when
+ * the call's first kernel starts (in stream order, with no caller kernel in
+ * between that releases its dependents before writing them). */
 int dhs_attend(dhs_ctx *ctx, const void *q, const void *block_kv, const int32_t *loc,
                void *out, float *lse, dhs_stream stream);
 
