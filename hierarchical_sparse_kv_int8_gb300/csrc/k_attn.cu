@@ -118,8 +118,9 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   const int G = c.Hq / c.Hkv;
   const int k = c.k;
   const int total = k + j + 1;
-  const int e0 = split * chunk;
-  const int e1 = min(e0 + chunk, total);
+  // the split's rows are positions i of the row list e = split + i * n_split
+  // (interleaved, so every split gets its share of each tier)
+  const int nrows = total > split ? (total - split + n_split - 1) / n_split : 0;
   const int rowb = c.row * 2;
   const int stride = rowb + 16;  // 16 bytes of padding: ldmatrix rows fall in distinct banks
   const int nv = rowb >> 4;
@@ -135,7 +136,10 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
 
   // locations of this split's selected rows (written two launches back, by
   // the union/probe), read once, coalesced, before the preceding launch ends
-  for (int e = e0 + tid; e < min(e1, k); e += kAttnThreads) lsm[e - e0] = lrow[e];
+  for (int i = tid; i < nrows; i += kAttnThreads) {
+    const int e = split + i * n_split;
+    if (e < k) lsm[i] = lrow[e];
+  }
   __syncthreads();  // the locations are in shared memory
 
   // eq. (9)-(10): block row j enters the draft ring at phi(r, n_r + j); the
@@ -162,14 +166,14 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   int16_t *ord_l = ord_e + chunk;
   __shared__ int wcnt[2][kAttnThreads / 32];
   int n_early = 0, n_late = 0;
-  for (int base = e0; base < e1; base += kAttnThreads) {
-    const int e = base + tid;
+  for (int base = 0; base < nrows; base += kAttnThreads) {
+    const int i = base + tid;
     bool early = false, late = false;
-    if (e < e1) {
-      if (e >= k) {
+    if (i < nrows) {
+      if (split + i * n_split >= k) {
         early = true;  // a block row
       } else {
-        const int32_t l = lsm[e - e0];
+        const int32_t l = lsm[i];
         if (l >= 0) {
           late = loc_tier(l) == DHS_LOC_STAGE;
           early = !late;
@@ -193,8 +197,8 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
       n_late += wcnt[1][ww];
     }
     const unsigned lt = (1u << lane) - 1u;
-    if (early) ord_e[pe + __popc(be & lt)] = (int16_t)(e - e0);
-    if (late) ord_l[pl + __popc(bl & lt)] = (int16_t)(e - e0);
+    if (early) ord_e[pe + __popc(be & lt)] = (int16_t)i;
+    if (late) ord_l[pl + __popc(bl & lt)] = (int16_t)i;
     __syncthreads();
   }
 
@@ -225,9 +229,9 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
     if (lane < kTileRows) {
       const int i = i0 + lane;
       if (i < n_in) {
-        const int e = e0 + lst[i];
+        const int pos = lst[i], e = split + pos * n_split;
         if (e < k) {
-          mysrc = loc_row(c, r, lsm[e - e0]);
+          mysrc = loc_row(c, r, lsm[pos]);
           if (mysrc == nullptr && wi == 0) record_error(c.err, DC_LOC_RANGE, K_ATTN);
         } else {
           mysrc = brow + (size_t)(e - k) * c.row;

@@ -572,7 +572,11 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
   if (blocks_per_req < 1) blocks_per_req = 1;
   dim3 grid(blocks_per_req, c.N);
   if (tm) tm->begin(K_GATHER, s);
-  e = launch_pdl(kern, grid, dim3(kGatherWarps * 32), 0, s, c, topk, loc_out, shared);
+  // An ordinary launch: its CTAs are placed once the union/probe has left the
+  // SMs, one per SM; placed early they would crowd onto the SMs the
+  // union/probe leaves free and keep attention CTAs off them.
+  kern<<<grid, kGatherWarps * 32, 0, s>>>(c, topk, loc_out, shared);
+  e = cudaGetLastError();
   if (tm) tm->end(K_GATHER, s);
   return e;
 }
