@@ -185,6 +185,17 @@ void free_all(dhs_ctx *c) {
   c->snaps.clear();
 }
 
+// Device address of page-locked, mapped host memory, or nullptr for any other
+// pointer (pageable host memory, device memory).
+void *mapped_ptr(const void *h) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 struct BufDesc {
   void *ptr;
   size_t bytes;
@@ -749,18 +760,35 @@ int dhs_round_host(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, co
   const DevCtx &d = c->d;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t nq = (size_t)d.N * d.Kmax;
-  if (cudaMemcpyAsync(c->rh_qidx, q_idx, nq * d.idx_row, cudaMemcpyHostToDevice, s) ||
-      cudaMemcpyAsync(c->rh_q, q, nq * d.Hq * d.dqk * 2, cudaMemcpyHostToDevice, s) ||
-      cudaMemcpyAsync(c->rh_block, block_kv, nq * d.row * 2, cudaMemcpyHostToDevice, s))
+  // Queries, block rows and outputs in page-locked host memory are used in
+  // place: the attention kernel reads them and writes its results across the
+  // host link (zero copy).  Other host memory goes through device buffers.
+  const void *q_dev = mapped_ptr(q), *b_dev = mapped_ptr(block_kv);
+  void *o_dev = mapped_ptr(out);
+  float *l_dev = lse ? static_cast<float *>(mapped_ptr(lse)) : nullptr;
+  if (!q_dev) {
+    if (cudaMemcpyAsync(c->rh_q, q, nq * d.Hq * d.dqk * 2, cudaMemcpyHostToDevice, s))
+      return DHS_ERR_CUDA;
+    q_dev = c->rh_q;
+  }
+  if (!b_dev) {
+    if (cudaMemcpyAsync(c->rh_block, block_kv, nq * d.row * 2, cudaMemcpyHostToDevice, s))
+      return DHS_ERR_CUDA;
+    b_dev = c->rh_block;
+  }
+  if (cudaMemcpyAsync(c->rh_qidx, q_idx, nq * d.idx_row, cudaMemcpyHostToDevice, s))
     return DHS_ERR_CUDA;
   int rc = dhs_select(c, c->rh_qidx, k_per_req, nullptr, c->rh_topk, stream);
   if (!rc) rc = dhs_resolve(c, c->rh_topk, c->rh_loc, 1, stream);
-  if (!rc) rc = dhs_attend(c, c->rh_q, c->rh_block, c->rh_loc, c->rh_out, lse ? c->rh_lse : nullptr,
-                           stream);
+  if (!rc)
+    rc = dhs_attend(c, q_dev, b_dev, c->rh_loc, o_dev ? o_dev : c->rh_out,
+                    lse ? (l_dev ? l_dev : c->rh_lse) : nullptr, stream);
   if (!rc) rc = dhs_commit(c, accepted_len, stream);
   if (rc) return rc;
-  if (cudaMemcpyAsync(out, c->rh_out, nq * d.Hq * d.dv * 2, cudaMemcpyDeviceToHost, s) ||
-      (lse && cudaMemcpyAsync(lse, c->rh_lse, nq * d.Hq * 4, cudaMemcpyDeviceToHost, s)))
+  if ((!o_dev &&
+       cudaMemcpyAsync(out, c->rh_out, nq * d.Hq * d.dv * 2, cudaMemcpyDeviceToHost, s)) ||
+      (lse && !l_dev &&
+       cudaMemcpyAsync(lse, c->rh_lse, nq * d.Hq * 4, cudaMemcpyDeviceToHost, s)))
     return DHS_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return DHS_ERR_CUDA;
   return DHS_OK;

@@ -291,11 +291,14 @@ int32_t dhs_kernel_count(void);
 int dhs_snapshot(dhs_ctx *ctx, int32_t *snapshot_id, dhs_stream stream);
 int dhs_restore(dhs_ctx *ctx, int32_t snapshot_id, dhs_stream stream);
 
-/* One whole round through host buffers: copies q_idx, q and block_kv from host
- * (pinned for asynchrony) to the context's device staging buffers, runs
- * select, resolve (shared), attend and commit, and copies out and lse (lse may
- * be NULL) back to host.  Synchronises `stream` before returning.  Shapes as in
- * the calls above. */
+/* One whole round through host buffers: runs select, resolve (shared),
+ * attend and commit on q_idx, q and block_kv in host memory and returns out
+ * and lse (lse may be NULL) in host memory.  q_idx is copied to a device
+ * buffer.  q, block_kv, out and lse are used in place when they are
+ * page-locked (cudaHostAlloc / cudaHostRegister): the attention kernel reads
+ * and writes them across the host link.  Pageable buffers are copied through
+ * device buffers instead.  Synchronises `stream` before returning.  Shapes as
+ * in the calls above. */
 int dhs_round_host(dhs_ctx *ctx, const int8_t *q_idx, const int32_t *k_per_req, const void *q,
                    const void *block_kv, const int32_t *accepted_len, void *out, float *lse,
                    dhs_stream stream);

@@ -286,3 +286,43 @@ def test_repeated_row_in_a_selection_is_flagged():
     run.commit(rec.accepted(0))
     st = run.ctx.stats(check=False)
     assert st["device_error"] == 5
+
+
+@pytest.mark.parametrize("attn_pass,pinned", [(PER_QUERY, True), (UNION, True), (PER_QUERY, False)],
+                         ids=["per_query_pinned", "union_pinned", "per_query_pageable"])
+def test_round_through_host_buffers(attn_pass, pinned):
+    """dhs_round_host gives the same outputs and cache state as the device
+    calls, whether its host buffers are page-locked (used in place) or not
+    (copied through device buffers)."""
+    import torch
+    rec = TINY_GQA
+    run = _runner(rec, attn_pass=attn_pass)
+    run.set_residency()
+    kr = rec.k_per_req()
+    run.load_round(0)
+    run.round(kr, rec.accepted(0))
+    run.load_round(1)
+    sid = run.ctx.snapshot()
+    acc1 = rec.accepted(1)
+    run.round(kr, acc1)
+    want_out = run.out.cpu()
+    want_lse = run.lse.cpu()
+    B, N = rec.B, rec.N
+    want_state = [run.export(w, torch.int32, (N, B)).cpu() for w in ("hot_row", "hot_stamp", "lru")]
+    run.ctx.restore(sid)
+
+    def host(t):
+        h = t.cpu()
+        return h.pin_memory() if pinned else h
+    qi, q, bl = host(run.q_idx), host(run.q), host(run.block)
+    out = torch.zeros(run.out.shape, dtype=run.out.dtype, pin_memory=pinned)
+    lse = torch.zeros(run.lse.shape, dtype=run.lse.dtype, pin_memory=pinned)
+    run.ctx.round_host(qi, kr, q, bl, acc1, out, lse)
+    for r in range(N):
+        for j in range(int(kr[r])):
+            assert torch.equal(out[r, j], want_out[r, j]), "out r=%d j=%d" % (r, j)
+            assert torch.equal(lse[r, j], want_lse[r, j]), "lse r=%d j=%d" % (r, j)
+    got_state = [run.export(w, torch.int32, (N, B)).cpu() for w in ("hot_row", "hot_stamp", "lru")]
+    for g, w in zip(got_state, want_state):
+        assert torch.equal(g, w)
+    assert run.ctx.stats()["device_error"] == 0
