@@ -373,6 +373,8 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   ALLOC(d.first_occ, N * KK);
   ALLOC(d.counts, N * 4);
   ALLOC(d.promo_dst, N * B);
+  ALLOC(d.now_bits, N * (size_t)((B + 31) / 32));
+  ALLOC(d.lru_next, N * B);
   ALLOC(d.inst, N * KK);
   const size_t pf = attn_partial_floats(d, c->n_split);
   ALLOC(d.part_o, c->n_split > 1 ? pf : 1);

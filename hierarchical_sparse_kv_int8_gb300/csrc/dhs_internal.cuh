@@ -89,6 +89,8 @@ struct DevCtx {
   int32_t *first_occ;   // [N][Kmax*k]
   int32_t *counts;      // [N][4]
   int32_t *promo_dst;   // [N][B]: hot slot taken by miss p (p < P)
+  uint32_t *now_bits;   // [N][ceil(B/32)]: hot slots stamped by this tick
+  int32_t *lru_next;    // [N][B]: the LRU order being rebuilt
   int32_t *inst;        // [N][Kmax*k] per-query mode: hot slot a staged entry
                         // also fills, else -1 (written for staged entries only)
   int32_t *topk_last;   // [N][Kmax][k] selection seen by the last resolve

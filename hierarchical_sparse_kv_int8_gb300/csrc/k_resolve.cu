@@ -72,7 +72,7 @@ size_t union_smem_bytes(const DevCtx &c) {
   const size_t pw = (size_t)((c.B + 31) / 32);
   const size_t maps = slice <= kMapPrefetchRows ? (size_t)slice * 8 : 0;
   const size_t KK = (size_t)c.Kmax * c.k;
-  return sw * 8 + pw * 8 + (size_t)c.B * 16 + KK * 4 + (KK + 3) / 4 * 4 + maps;
+  return sw * 8 + pw * 8 + (size_t)c.B * 8 + KK * 4 + (KK + 3) / 4 * 4 + maps;
 }
 
 __global__ void __cluster_dims__(kUnionCluster, 1, 1) __launch_bounds__(kUnionThreads)
@@ -82,7 +82,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
-  __shared__ int sh_cnt[6];  // ring, opt, hot hits, selections, miss selections, evictions
+  __shared__ int sh_cnt[5];  // ring, opt, hot hits, selections, miss selections
   __shared__ int sh_u, sh_m, sh_p;  // this CTA's union rows and misses; the leader's P
   const int crank = (int)cl.block_rank();
   const int r = blockIdx.x / kUnionCluster;
@@ -105,10 +105,8 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   uint32_t *prot = wp + sw;  // leader: protected slots
   uint32_t *now = prot + pw;  // leader: slots stamped by this tick
   int32_t *candB = reinterpret_cast<int32_t *>(now + pw);
-  int32_t *tmpB = candB + B;
-  int32_t *lru_s = tmpB + B;   // leader: LRU order at the start of the call
-  int32_t *hrow_s = lru_s + B;  // leader: row held by each slot at the start
-  int32_t *ul = hrow_s + B;     // location of each union row of this slice
+  int32_t *lru_s = candB + B;  // leader: LRU order at the start of the call
+  int32_t *ul = lru_s + B;     // location of each union row of this slice
   uint32_t *umw = reinterpret_cast<uint32_t *>(ul + KK);  // query masks, one byte per union row
   const int umw_words = (KK + 3) / 4;
   const bool pf = slice <= kMapPrefetchRows;
@@ -121,7 +119,6 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   int32_t *uni = c.uni + (size_t)r * KK;
   int4 *uent = c.uent + (size_t)r * KK;
   int32_t *miss = c.miss + (size_t)r * KK;
-  int32_t *hot_row = c.hot_row + (size_t)r * B;
   int32_t *hot_stamp = c.hot_stamp + (size_t)r * B;
   int32_t *lru = c.lru + (size_t)r * B;
   int32_t *hot_map = c.hot_map + (size_t)r * c.Sm;
@@ -130,7 +127,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   const int nsel = Kr * k;
 
   // 0. start fetching what the later phases read: this slice's map entries,
-  //    and for the leader the LRU order and the rows of the slots.  These
+  //    and for the leader the LRU order.  These
   //    are state of earlier rounds, complete before the preceding launch
   //    (top-k) began, so the copies start before that launch has finished.
   const bool any_opt = c.opt_count[r] > 0;
@@ -143,7 +140,6 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   if (crank == 0) {
     for (int i = tid; i < B; i += bs) {
       cp_async_4(&lru_s[i], &lru[i]);
-      cp_async_4(&hrow_s[i], &hot_row[i]);
     }
   }
   cp_async_commit();
@@ -155,7 +151,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   for (int i = tid; i < umw_words; i += bs) umw[i] = 0;
   if (crank == 0)
     for (int i = tid; i < 2 * pw; i += bs) prot[i] = 0;  // prot and now
-  if (tid < 6) sh_cnt[tid] = 0;
+  if (tid < 5) sh_cnt[tid] = 0;
   __syncthreads();
   for (int e0 = tid; e0 < nsel; e0 += kBatch * bs) {
     int32_t sv[kBatch];
@@ -369,55 +365,26 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
         const int v = lru_s[i];
         if (!((prot[v >> 5] >> (v & 31)) & 1u)) {
           candB[cb] = v;
-          if (cb < P) atomicOr(&now[v >> 5], 1u << (v & 31));  // stamped by this tick
+          if (cb < P) {
+            atomicOr(&now[v >> 5], 1u << (v & 31));  // stamped by this tick
+            c.promo_dst[(size_t)r * B + cb] = v;      // the cb-th miss takes slot v
+          }
           ++cb;
         }
       }
     }
     if (tid == 0) sh_p = P;
+    __syncthreads();  // every stamped-now bit is set
+    for (int i = tid; i < pw; i += bs) c.now_bits[(size_t)r * pw + i] = now[i];
   }
   cl.sync();  // S2: every slice's misses are in the miss list and every first
               // selection of a miss is known; no CTA reads the leader's memory
               // after this point
-  int P = 0;
-  if (crank == 0) {
-    P = sh_p;
-    // promotions: the first P misses take the victims, in order
-    int ev = 0;
-    for (int p = tid; p < P; p += bs) {
-      const int v = candB[p];
-      const int32_t old = hrow_s[v];
-      const int32_t u = miss[p];
-      if (old >= 0) {
-        hot_map[old] = -1;
-        ++ev;
-      }
-      hot_row[v] = u;
-      hot_stamp[v] = tick;
-      hot_map[u] = v;
-      c.promo_dst[(size_t)r * B + p] = v;
-    }
-    if (ev) atomicAdd(&sh_cnt[5], ev);
-    // 7. LRU order after this tick: untouched slots keep their order, slots
-    //    stamped now follow in ascending slot order
-    if (hits + P > 0) {
-      int na = 0, nb = 0;
-      for (int i = b0; i < b1; ++i) {
-        const int v = lru_s[i];
-        const bool nw_ = (now[v >> 5] >> (v & 31)) & 1u;
-        na += !nw_;
-        tmpB[i] = nw_ ? -1 : v;
-      }
-      for (int v = b0; v < b1; ++v) nb += (now[v >> 5] >> (v & 31)) & 1u;
-      int A, Bt;
-      int ab = ublock_excl_scan(na, warp_sums, A);
-      int bb = ublock_excl_scan(nb, warp_sums, Bt);
-      for (int i = b0; i < b1; ++i)
-        if (tmpB[i] >= 0) lru[ab++] = tmpB[i];
-      for (int v = b0; v < b1; ++v)
-        if ((now[v >> 5] >> (v & 31)) & 1u) lru[A + bb++] = v;
-    }
-  }
+  // The promotions' cache state (slot rows, stamps, maps) and the LRU order
+  // after this tick are written by the gather (hot_update below): only the
+  // next round and the exported state read them, so they leave this
+  // kernel's critical path.
+  const int P = crank == 0 ? sh_p : 0;
 
   // the first selection of each promoted miss also fills its hot slot
   if (!shared && crank == 0)
@@ -430,7 +397,6 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
     atomicAdd(&c.stats[ST_OPT], (unsigned long long)sh_cnt[1]);
     atomicAdd(&c.stats[ST_HOT], (unsigned long long)sh_cnt[2]);
     atomicAdd(&c.stats[ST_MISS_SEL], (unsigned long long)sh_cnt[4]);
-    if (sh_cnt[5]) atomicAdd(&c.stats[ST_EVICT], (unsigned long long)sh_cnt[5]);
     if (!shared) atomicAdd(&c.stats[ST_FETCHED], (unsigned long long)sh_cnt[4]);
     if (crank == 0) {
       c.counts[r * 4 + 0] = U;
@@ -464,20 +430,82 @@ struct GatherShape {
   static constexpr int kGatherBatch = VEC == 1 ? 8 : VEC == 2 ? 4 : 2;
 };
 
+// Cache state after this tick for request r, written by one CTA of the
+// gather while the others fetch (section 3.2, Fig. 2): each promoted miss p
+// takes slot promo_dst[p] (the slot's previous row leaves the hot map), and
+// the LRU order becomes the slots not stamped by this tick in their previous
+// order, followed by the stamped ones (hits and promotions) in ascending slot
+// order.  Only the next round's union/probe and the exported state read
+// these; the order is rebuilt in a scratch array and copied back.
+__device__ void hot_update(const DevCtx &c, int r, int tick, int *warp_sums) {
+  const int B = c.B, pw = (B + 31) >> 5, KK = c.Kmax * c.k;
+  const int tid = threadIdx.x, bs = blockDim.x;
+  const int P = c.counts[r * 4 + 2], hits = c.counts[r * 4 + 3];
+  int32_t *hot_row = c.hot_row + (size_t)r * B;
+  int32_t *hot_stamp = c.hot_stamp + (size_t)r * B;
+  int32_t *hot_map = c.hot_map + (size_t)r * c.Sm;
+  int32_t *lru = c.lru + (size_t)r * B;
+  int32_t *nxt = c.lru_next + (size_t)r * B;
+  const uint32_t *now = c.now_bits + (size_t)r * pw;
+  const int32_t *dst = c.promo_dst + (size_t)r * B;
+  const int32_t *miss = c.miss + (size_t)r * KK;
+  int ev = 0;
+  for (int p = tid; p < P; p += bs) {
+    const int v = dst[p];
+    const int32_t old = hot_row[v], u = miss[p];
+    if (old >= 0) {
+      hot_map[old] = -1;
+      ++ev;
+    }
+    hot_row[v] = u;
+    hot_stamp[v] = tick;
+    hot_map[u] = v;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ev += __shfl_xor_sync(0xffffffffu, ev, o);
+  if ((tid & 31) == 0 && ev) atomicAdd(&c.stats[ST_EVICT], (unsigned long long)ev);
+  if (hits + P == 0) return;  // nothing stamped: the order stands
+  const int per = (B + bs - 1) / bs;
+  const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+  auto stamped = [&](int v) { return (now[v >> 5] >> (v & 31)) & 1u; };
+  int na = 0, nb = 0;
+  for (int i = b0; i < b1; ++i) na += !stamped(lru[i]);
+  for (int v = b0; v < b1; ++v) nb += stamped(v);
+  int A, Bt;
+  int ab = ublock_excl_scan(na, warp_sums, A);
+  int bb = ublock_excl_scan(nb, warp_sums, Bt);
+  for (int i = b0; i < b1; ++i) {
+    const int v = lru[i];
+    if (!stamped(v)) nxt[ab++] = v;
+  }
+  for (int v = b0; v < b1; ++v)
+    if (stamped(v)) nxt[A + bb++] = v;
+  __syncthreads();  // the new order is complete
+  for (int i = tid; i < B; i += bs) lru[i] = nxt[i];
+}
+
 template <int VEC>
 __global__ void __launch_bounds__(kGatherWarps * 32)
 k_gather(const DevCtx c, const int32_t *__restrict__ topk, const int32_t *__restrict__ loc,
-         int shared) {
+         int shared, int tick) {
   constexpr int kGatherVec = GatherShape<VEC>::kGatherVec;
   constexpr int kGatherBatch = GatherShape<VEC>::kGatherBatch;
+  __shared__ int warp_sums[32];
   pdl_wait();
   pdl_trigger();
   const int r = blockIdx.y;
   const int Kr = c.Kr[r];
   if (Kr == 0) return;
+  // CTA 0 of the request writes the cache state; with more than one CTA per
+  // request it leaves the fetching to the others, so no fetch waits for it
+  if (blockIdx.x == 0) {
+    hot_update(c, r, tick, warp_sums);
+    if (gridDim.x > 1) return;
+  }
+  const int fetchers = gridDim.x > 1 ? gridDim.x - 1 : 1;
   const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
-  const int nwt = gridDim.x * kGatherWarps;
+  const int gw = (gridDim.x > 1 ? blockIdx.x - 1 : 0) * kGatherWarps + (threadIdx.x >> 5);
+  const int nwt = fetchers * kGatherWarps;
   const int KK = c.Kmax * c.k;
   const int nv = (c.row * 2) >> 4;
   const uint16_t *host = c.host[r];
@@ -556,7 +584,7 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
   if (e != cudaSuccess || !gather) return e;
   const int vec = (c.row * 2 + 511) / 512;
   if (vec > kGatherMaxVec) return cudaErrorInvalidValue;
-  void (*kern)(const DevCtx, const int32_t *, const int32_t *, int) =
+  void (*kern)(const DevCtx, const int32_t *, const int32_t *, int, int) =
       vec == 1 ? k_gather<1> : vec == 2 ? k_gather<2> : vec == 3 ? k_gather<3> : k_gather<4>;
   static bool carved[kGatherMaxVec + 1] = {};
   if (!carved[vec]) {
@@ -575,7 +603,7 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
   // An ordinary launch: its CTAs are placed once the union/probe has left the
   // SMs, one per SM; placed early they would crowd onto the SMs the
   // union/probe leaves free and keep attention CTAs off them.
-  kern<<<grid, kGatherWarps * 32, 0, s>>>(c, topk, loc_out, shared);
+  kern<<<grid, kGatherWarps * 32, 0, s>>>(c, topk, loc_out, shared, tick);
   e = cudaGetLastError();
   if (tm) tm->end(K_GATHER, s);
   return e;
