@@ -48,12 +48,21 @@ __device__ __forceinline__ int ublock_excl_scan(int v, int *warp_sums, int &tota
   return excl;
 }
 
+// Adds the warp's values to a shared counter with one atomic per warp (all
+// lanes call it).
+__device__ __forceinline__ void warp_add(int *dst, int v) {
+  v = __reduce_add_sync(0xffffffffu, v);
+  if ((threadIdx.x & 31) == 0 && v) atomicAdd(dst, v);
+}
+
 // The union/probe of one request runs on a cluster of kUnionCluster CTAs.
 // CTA c owns the c-th slice of the history rows: its shared memory holds the
 // union bitmap of that slice, the prefix count of every word and the
-// location of every union row in the slice.  The leader CTA (rank 0) also
-// holds the protected-slot and stamped-now bitmaps of the hot cache, filled
-// by every CTA through distributed shared memory, and chooses the victims.
+// location of every union row in the slice, and the protected-slot and
+// stamped-now bitmaps of the hot cache marked by its own probes (shared-memory
+// atomics).  After the first cluster barrier the leader CTA (rank 0) merges
+// the slices' bitmaps through distributed shared memory and chooses the
+// victims.
 constexpr int kUnionCluster = 8;
 constexpr int32_t kMissMark = -2;
 constexpr int kBatch = 8;  // independent global loads in flight per thread
@@ -102,8 +111,8 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   const int nw = row_hi > row_lo ? (int)((row_hi - row_lo + 31) >> 5) : 0;
   uint32_t *bm = reinterpret_cast<uint32_t *>(smem);
   uint32_t *wp = bm + sw;
-  uint32_t *prot = wp + sw;  // leader: protected slots
-  uint32_t *now = prot + pw;  // leader: slots stamped by this tick
+  uint32_t *prot = wp + sw;  // protected slots (the leader: of the request)
+  uint32_t *now = prot + pw;  // slots stamped by this tick (likewise)
   int32_t *candB = reinterpret_cast<int32_t *>(now + pw);
   int32_t *lru_s = candB + B;  // leader: LRU order at the start of the call
   int32_t *ul = lru_s + B;     // location of each union row of this slice
@@ -112,8 +121,6 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   const bool pf = slice <= kMapPrefetchRows;
   int32_t *hmap_s = reinterpret_cast<int32_t *>(umw + umw_words);  // slice's hot-map entries (when pf)
   int32_t *omap_s = hmap_s + slice;
-  uint32_t *prot0 = cl.map_shared_rank(prot, 0);
-  uint32_t *now0 = cl.map_shared_rank(now, 0);
 
   const int32_t *tk = topk + (size_t)r * KK;
   int32_t *uni = c.uni + (size_t)r * KK;
@@ -149,8 +156,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   // 1. union bitmap of this CTA's slice
   for (int i = tid; i < sw; i += bs) bm[i] = 0;
   for (int i = tid; i < umw_words; i += bs) umw[i] = 0;
-  if (crank == 0)
-    for (int i = tid; i < 2 * pw; i += bs) prot[i] = 0;  // prot and now
+  for (int i = tid; i < 2 * pw; i += bs) prot[i] = 0;  // prot and now
   if (tid < 5) sh_cnt[tid] = 0;
   __syncthreads();
   for (int e0 = tid; e0 < nsel; e0 += kBatch * bs) {
@@ -171,7 +177,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       }
     }
   }
-  cl.sync();  // the leader's bitmaps are cleared before anyone marks them
+  __syncthreads();  // the slice's bitmap is complete
 
   // 2. ascending compaction of the slice; each thread owns a run of words
   const int per = (nw + bs - 1) / bs;
@@ -232,7 +238,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
         const int32_t u = ub[i];
         if (u < 0) continue;
         const int32_t hs = hm[i];
-        if (hs >= 0) atomicOr(&prot0[hs >> 5], 1u << (hs & 31));
+        if (hs >= 0) atomicOr(&prot[hs >> 5], 1u << (hs & 31));
         int32_t l;
         if (u >= ring_lo && u < n) {
           l = make_loc(DHS_LOC_RING, (int)(u % c.Rd));
@@ -243,7 +249,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
         } else if (hs >= 0) {
           l = make_loc(DHS_LOC_HOT, hs);
           hot_stamp[hs] = tick;
-          atomicOr(&now0[hs >> 5], 1u << (hs & 31));
+          atomicOr(&now[hs >> 5], 1u << (hs & 31));
           ++hot_h;
         } else {
           l = kMissMark;
@@ -255,9 +261,9 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       if (nb < kBatch) break;
     }
   }
-  atomicAdd(&sh_cnt[0], ring_h);
-  atomicAdd(&sh_cnt[1], opt_h);
-  atomicAdd(&sh_cnt[2], hot_h);
+  warp_add(&sh_cnt[0], ring_h);
+  warp_add(&sh_cnt[1], opt_h);
+  warp_add(&sh_cnt[2], hot_h);
   int Mc;
   const int m_local = ublock_excl_scan(misses_here, warp_sums, Mc);
   if (tid == 0) {
@@ -278,6 +284,18 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
     M += mq;
     if (crank == 0) hits += *cl.map_shared_rank(&sh_cnt[2], qr);
   }
+  // the leader merges the protected and stamped slots of every slice
+  if (crank == 0)
+    for (int i = tid; i < pw; i += bs) {
+      uint32_t pv = 0, nv = 0;
+#pragma unroll
+      for (int qr = 0; qr < kUnionCluster; ++qr) {
+        pv |= cl.map_shared_rank(prot, qr)[i];
+        nv |= cl.map_shared_rank(now, qr)[i];
+      }
+      prot[i] = pv;
+      now[i] = nv;
+    }
   // union rows and misses of the slice get their request-wide ranks
   {
     int q = u_local, m = m_local;
@@ -339,8 +357,8 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       loc_out[(size_t)r * KK + e] = l;
     }
   }
-  atomicAdd(&sh_cnt[3], sel_here);
-  atomicAdd(&sh_cnt[4], missel);
+  warp_add(&sh_cnt[3], sel_here);
+  warp_add(&sh_cnt[4], missel);
   __syncthreads();  // the query masks of the slice are complete
   // 5. second half of each union entry: the queries that selected the row
   for (int q = tid; q < Uc; q += bs)
