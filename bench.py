@@ -55,6 +55,9 @@ def parse():
                     help="configuration to time (the headline is %s)" % WORKLOAD)
     ap.add_argument("--attn-pass", type=int, default=0, choices=[0, 1, 2],
                     help="attention pass after a shared resolve: 0 auto, 1 per query, 2 union")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="requests per GPU (default: the configuration's); a smaller batch is a "
+                         "cut of the workload for profiling, not a bench line")
     return ap.parse_args()
 
 
@@ -310,6 +313,8 @@ def run_native(args):
         torch.cuda.set_device(0)
     dhs.build()
     rec = wl.CONFIGS[args.workload]
+    if args.batch:
+        rec = rec.scaled(N=args.batch)
     if world > 1:
         rec = rec.scaled(seed=rec.seed + rank)   # each rank serves its own requests
     stream = torch.cuda.Stream()
@@ -517,6 +522,8 @@ def run_reference(args):
         return
     import workload as wl
     rec = wl.CONFIGS[args.workload]
+    if args.batch:
+        rec = rec.scaled(N=args.batch)
     times = []
     for i in range(args.warmup + args.steps):
         r = i % rec.N
