@@ -130,7 +130,10 @@ def _dptr(x) -> Optional[int]:
 
 
 def _host_i32(x, n) -> np.ndarray:
-    a = np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+    if isinstance(x, np.ndarray) and x.dtype == np.int32 and x.flags.c_contiguous:
+        a = x
+    else:
+        a = np.ascontiguousarray(np.asarray(x, dtype=np.int32))
     if a.size < n:
         raise ValueError("expected %d int32 values, got %d" % (n, a.size))
     return a

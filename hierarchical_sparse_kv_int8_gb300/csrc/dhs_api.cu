@@ -484,9 +484,14 @@ int dhs_bind_request(dhs_ctx *c, int32_t slot, const void *host_kv, const int8_t
   return DHS_OK;
 }
 
-int dhs_select(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const int64_t *pos,
-               int32_t *topk_out, dhs_stream stream) {
-  if (!c || !q_idx || !k_per_req || !topk_out || !aligned16(q_idx)) return DHS_ERR_INVALID;
+}  // extern "C"
+
+namespace {
+// dhs_select, with the index rows either in device memory (q_idx) or, when
+// q_idx is null, on the host (q_inline), carried in the launch parameters.
+int select_impl(dhs_ctx *c, const int8_t *q_idx, const int8_t *q_inline,
+                const int32_t *k_per_req, const int64_t *pos, int32_t *topk_out,
+                dhs_stream stream) {
   if (c->phase != PH_IDLE) return DHS_ERR_INVALID;
   const DevCtx &d = c->d;
   std::vector<int32_t> w(d.N + d.N * d.Kmax, 0);
@@ -507,12 +512,21 @@ int dhs_select(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const 
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   {
-    cudaError_t e_ = launch_select(d, q_idx, topk_out, max_dom, w.data(), s, &c->timer);
+    cudaError_t e_ = launch_select(d, q_idx, q_inline, topk_out, max_dom, w.data(), s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
   }
   for (int r = 0; r < d.N; ++r) c->K[r] = k_per_req[r];
   c->phase = PH_SELECTED;
   return DHS_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int dhs_select(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const int64_t *pos,
+               int32_t *topk_out, dhs_stream stream) {
+  if (!c || !q_idx || !k_per_req || !topk_out || !aligned16(q_idx)) return DHS_ERR_INVALID;
+  return select_impl(c, q_idx, nullptr, k_per_req, pos, topk_out, stream);
 }
 
 int dhs_resolve(dhs_ctx *c, const int32_t *topk, int32_t *loc_out, int32_t shared,
@@ -778,9 +792,15 @@ int dhs_round_host(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, co
       return DHS_ERR_CUDA;
     b_dev = c->rh_block;
   }
-  if (cudaMemcpyAsync(c->rh_qidx, q_idx, nq * d.idx_row, cudaMemcpyHostToDevice, s))
+  // small index rows travel in the indexer's launch parameters, else through
+  // a device buffer
+  const bool inline_q =
+      (size_t)ctl_qidx_word(d.N, d.Kmax) * 4 + nq * d.idx_row <= (size_t)kUploadWords * 4;
+  if (!inline_q &&
+      cudaMemcpyAsync(c->rh_qidx, q_idx, nq * d.idx_row, cudaMemcpyHostToDevice, s))
     return DHS_ERR_CUDA;
-  int rc = dhs_select(c, c->rh_qidx, k_per_req, nullptr, c->rh_topk, stream);
+  int rc = inline_q ? select_impl(c, nullptr, q_idx, k_per_req, nullptr, c->rh_topk, stream)
+                    : dhs_select(c, c->rh_qidx, k_per_req, nullptr, c->rh_topk, stream);
   if (!rc) rc = dhs_resolve(c, c->rh_topk, c->rh_loc, 1, stream);
   if (!rc)
     rc = dhs_attend(c, q_dev, b_dev, c->rh_loc, o_dev ? o_dev : c->rh_out,

@@ -181,15 +181,21 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
   return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
 }
 
-// Words uploaded by k_upload (kernel parameter, <= 16 KB).
-struct UploadWords {
+// Words uploaded by k_upload (kernel parameter, <= 16 KB).  The indexer
+// launch carries its control words here and, when they fit, the queries'
+// index rows after them (at a 16-byte aligned word offset).
+struct __align__(16) UploadWords {
   int32_t w[kUploadWords];
 };
+__host__ __device__ inline int ctl_qidx_word(int N, int Kmax) { return (N + N * Kmax + 3) & ~3; }
 
 // ---- launchers (each returns the cudaGetLastError of its launch) -------
 cudaError_t launch_upload(int32_t *dst, const int32_t *words, int n, cudaStream_t s);
-cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_out,
-                          int max_dom, const int32_t *ctl_words, cudaStream_t s, class Timer *tm);
+// q_idx: device index rows, or nullptr with q_inline holding them on the host
+// (carried in the launch parameters; ctl_qidx_word + bytes/4 <= kUploadWords).
+cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, const int8_t *q_inline,
+                          int32_t *topk_out, int max_dom, const int32_t *ctl_words,
+                          cudaStream_t s, class Timer *tm);
 cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_out,
                            int shared, int gather, int tick, cudaStream_t s, class Timer *tm);
 cudaError_t launch_uattn(const DevCtx &c, const uint16_t *q, const uint16_t *block,

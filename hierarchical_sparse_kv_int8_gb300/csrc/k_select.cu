@@ -11,6 +11,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <cstring>
 
 namespace dhs {
 
@@ -92,7 +93,8 @@ k_index_score(const DevCtx c, const int8_t *__restrict__ q_idx,
   const int rows = (int)(dom_r - row0 < kScoreThreads ? dom_r - row0 : kScoreThreads);
   const int8_t *keys = c.keys[r] + row0 * RB;
   uint4 *qs = reinterpret_cast<uint4 *>(smem);
-  const uint4 *qsrc = reinterpret_cast<const uint4 *>(q_idx + (size_t)r * c.Kmax * RB);
+  const int8_t *qb = q_idx ? q_idx : reinterpret_cast<const int8_t *>(ctl.w + ctl_qidx_word(c.N, c.Kmax));
+  const uint4 *qsrc = reinterpret_cast<const uint4 *>(qb + (size_t)r * c.Kmax * RB);
   for (int u = threadIdx.x; u < Kr * nc; u += blockDim.x) qs[u] = qsrc[u];
   __syncthreads();
 
@@ -187,6 +189,7 @@ k_index_score_wide(const DevCtx c, const int8_t *__restrict__ q_idx,
   const int RB = c.idx_row, NC = RB >> 4;
   const int sub = lane % LPR, rsub = lane / LPR;
   // this lane's chunks of every query (zero past K_r and past the row)
+  const int8_t *qb = q_idx ? q_idx : reinterpret_cast<const int8_t *>(ctl.w + ctl_qidx_word(c.N, c.Kmax));
   uint4 qv[kMaxKmax][CPL];
 #pragma unroll
   for (int j = 0; j < kMaxKmax; ++j)
@@ -194,7 +197,7 @@ k_index_score_wide(const DevCtx c, const int8_t *__restrict__ q_idx,
     for (int i = 0; i < CPL; ++i) {
       const int ch = sub + i * LPR;
       qv[j][i] = (j < Kr && ch < NC)
-                     ? *reinterpret_cast<const uint4 *>(q_idx + ((size_t)r * c.Kmax + j) * RB + ch * 16)
+                     ? *reinterpret_cast<const uint4 *>(qb + ((size_t)r * c.Kmax + j) * RB + ch * 16)
                      : make_uint4(0u, 0u, 0u, 0u);
     }
   // after the reduce-scatter this lane holds query qm's score; one lane per
@@ -903,7 +906,9 @@ k_index_score_tc(const DevCtx c, const int8_t *__restrict__ q_idx,
       cdom = dom_of(cr);
       dq0 = q0 < Kr ? ctl.w[N + cr * Kmax + q0] : 0;
       dq1 = q1 < Kr ? ctl.w[N + cr * Kmax + q1] : 0;
-      const int8_t *qrow = q_idx + ((size_t)cr * Kmax + g) * RB;
+      const int8_t *qrow = (q_idx ? q_idx : reinterpret_cast<const int8_t *>(
+                                                ctl.w + ctl_qidx_word(N, Kmax))) +
+                           ((size_t)cr * Kmax + g) * RB;
 #pragma unroll
       for (int i = 0; i < NG; ++i) {
         const uint4 v = g < Kr ? *reinterpret_cast<const uint4 *>(qrow + (4 * i + t) * 16)
@@ -984,11 +989,15 @@ k_index_score_tc(const DevCtx c, const int8_t *__restrict__ q_idx,
   flush();
 }
 
-cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, int32_t *topk_out, int max_dom,
-                          const int32_t *ctl_words, cudaStream_t s, Timer *tm) {
+cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, const int8_t *q_inline,
+                          int32_t *topk_out, int max_dom, const int32_t *ctl_words,
+                          cudaStream_t s, Timer *tm) {
   UploadWords ctl;
   const int nw = c.N + c.N * c.Kmax;
   for (int i = 0; i < nw; ++i) ctl.w[i] = ctl_words[i];
+  if (!q_idx)
+    std::memcpy(ctl.w + ctl_qidx_word(c.N, c.Kmax), q_inline,
+                (size_t)c.N * c.Kmax * c.idx_row);
   if (c.idx_row % 64 == 0 && c.idx_row >= 64 * kTcMinGroups && c.idx_row <= 64 * kTcMaxGroups) {
     // tensor-core scoring on a persistent grid (rows of 192 to 512 bytes;
     // narrower rows cost the one-thread-per-row kernel fewer dp4a than the

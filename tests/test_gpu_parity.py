@@ -288,14 +288,17 @@ def test_repeated_row_in_a_selection_is_flagged():
     assert st["device_error"] == 5
 
 
-@pytest.mark.parametrize("attn_pass,pinned", [(PER_QUERY, True), (UNION, True), (PER_QUERY, False)],
-                         ids=["per_query_pinned", "union_pinned", "per_query_pageable"])
-def test_round_through_host_buffers(attn_pass, pinned):
+@pytest.mark.parametrize("attn_pass,pinned,big", [(PER_QUERY, True, False), (UNION, True, False),
+                                                  (PER_QUERY, False, False), (UNION, True, True)],
+                         ids=["per_query_pinned", "union_pinned", "per_query_pageable",
+                              "union_pinned_20KB_index_rows"])
+def test_round_through_host_buffers(attn_pass, pinned, big):
     """dhs_round_host gives the same outputs and cache state as the device
     calls, whether its host buffers are page-locked (used in place) or not
-    (copied through device buffers)."""
+    (copied through device buffers), and whether the index rows fit in the
+    indexer's launch parameters (16 KB) or go through a device buffer."""
     import torch
-    rec = TINY_GQA
+    rec = TINY_TC512_FULL.scaled(N=5) if big else TINY_GQA
     run = _runner(rec, attn_pass=attn_pass)
     run.set_residency()
     kr = rec.k_per_req()
