@@ -431,14 +431,15 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
 }
 
 // Shared host gather: staging[r][m] <- host[r][D_r[m]], one warp per row,
-// 16-byte zero-copy loads from pinned host memory, four rows in flight per
+// 16-byte zero-copy loads from pinned host memory, several rows in flight per
 // warp.  In per-query mode every missing selection (j, i) is fetched into
 // staging row j*k + i.  A promoted row is written to its hot-cache slot from
 // the same registers ("Adaptive DHiSparse", section 3.4, installs promoted
 // rows after the attention readers; the victim slots are unprotected, so no
 // location of this round names them and the install may come first).
 // VEC 16-byte vectors per lane cover a row (VEC x 512 B); BATCH rows are in
-// flight per warp, so each warp keeps about 4 KB of loads outstanding.
+// flight per warp, so each warp keeps about 4 KB of loads outstanding (deeper
+// batches measured no faster: the host link is already saturated).
 constexpr int kGatherWarps = 8;
 constexpr int kGatherMaxVec = 4;  // rows up to 2 KB
 
@@ -532,13 +533,11 @@ k_gather(const DevCtx c, const int32_t *__restrict__ topk, const int32_t *__rest
   const int P = c.counts[r * 4 + 2];
   for (int base = gw; base < count; base += kGatherBatch * nwt) {
     uint4 buf[kGatherBatch][kGatherVec];
-    int64_t srow[kGatherBatch];
-    int dst[kGatherBatch], slot[kGatherBatch];
+    int32_t srow[kGatherBatch], slot[kGatherBatch];
 #pragma unroll
     for (int b = 0; b < kGatherBatch; ++b) {
       const int e = base + b * nwt;
       srow[b] = -1;
-      dst[b] = e;
       slot[b] = -1;
       if (e < count) {
         if (shared) {
@@ -561,7 +560,7 @@ k_gather(const DevCtx c, const int32_t *__restrict__ topk, const int32_t *__rest
         }
       }
       if (srow[b] >= 0) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(host + srow[b] * c.row);
+        const uint4 *src = reinterpret_cast<const uint4 *>(host + (int64_t)srow[b] * c.row);
 #pragma unroll
         for (int i = 0; i < kGatherVec; ++i) {
           const int v = lane + 32 * i;
@@ -572,7 +571,7 @@ k_gather(const DevCtx c, const int32_t *__restrict__ topk, const int32_t *__rest
 #pragma unroll
     for (int b = 0; b < kGatherBatch; ++b) {
       if (srow[b] < 0) continue;
-      uint4 *d = reinterpret_cast<uint4 *>(c.stage + ((size_t)r * KK + dst[b]) * c.row);
+      uint4 *d = reinterpret_cast<uint4 *>(c.stage + ((size_t)r * KK + base + b * nwt) * c.row);
 #pragma unroll
       for (int i = 0; i < kGatherVec; ++i) {
         const int v = lane + 32 * i;
