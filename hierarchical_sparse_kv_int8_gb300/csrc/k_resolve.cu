@@ -81,7 +81,7 @@ size_t union_smem_bytes(const DevCtx &c) {
   const size_t pw = (size_t)((c.B + 31) / 32);
   const size_t maps = slice <= kMapPrefetchRows ? (size_t)slice * 8 : 0;
   const size_t KK = (size_t)c.Kmax * c.k;
-  return sw * 8 + pw * 8 + (size_t)c.B * 8 + KK * 4 + (KK + 3) / 4 * 4 + maps;
+  return sw * 12 + pw * 8 + (size_t)c.B * 8 + KK * 4 + (KK + 3) / 4 * 4 + maps;
 }
 
 __global__ void __cluster_dims__(kUnionCluster, 1, 1) __launch_bounds__(kUnionThreads)
@@ -111,7 +111,8 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   const int nw = row_hi > row_lo ? (int)((row_hi - row_lo + 31) >> 5) : 0;
   uint32_t *bm = reinterpret_cast<uint32_t *>(smem);
   uint32_t *wp = bm + sw;
-  uint32_t *prot = wp + sw;  // protected slots (the leader: of the request)
+  int *mcw = reinterpret_cast<int *>(wp + sw);  // misses per word, then their prefix
+  uint32_t *prot = reinterpret_cast<uint32_t *>(mcw + sw);  // protected slots (the leader: of the request)
   uint32_t *now = prot + pw;  // slots stamped by this tick (likewise)
   int32_t *candB = reinterpret_cast<int32_t *>(now + pw);
   int32_t *lru_s = candB + B;  // leader: LRU order at the start of the call
@@ -179,93 +180,80 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   }
   __syncthreads();  // the slice's bitmap is complete
 
-  // 2. ascending compaction of the slice; each thread owns a run of words
+  // 2. ascending compaction of the slice: each thread owns a run of words and
+  //    records, for every word, the union index of its first row
   const int per = (nw + bs - 1) / bs;
   const int w0 = min(nw, tid * per), w1 = min(nw, w0 + per);
   int cnt = 0;
   for (int w = w0; w < w1; ++w) cnt += __popc(bm[w]);
   int Uc;
-  const int u_local = ublock_excl_scan(cnt, warp_sums, Uc);
+  {
+    int q = ublock_excl_scan(cnt, warp_sums, Uc);
+    for (int w = w0; w < w1; ++w) {
+      wp[w] = q;
+      q += __popc(bm[w]);
+    }
+  }
 
   cp_async_wait_all();
-  __syncthreads();
+  __syncthreads();  // word prefixes and prefetched map entries are in place
 
   // 3. probe each union row of the slice: live ring tail, optional map, hot
-  //    cache, else miss; hot rows of the union are protected in the leader
-  int misses_here = 0, ring_h = 0, opt_h = 0, hot_h = 0;
-  {
-    int q = u_local;
-    int w = w0;
-    uint32_t bits = 0;
-    if (w < w1) {
-      wp[w] = q;
-      bits = bm[w];
+  //    cache, else miss; the protected and stamped hot slots are marked.  A
+  //    warp takes one word at a time, a lane one bit, so the rows of a word
+  //    are probed side by side; each word's miss count is kept for the ranks.
+  const int lane = tid & 31, nwarps = bs >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  int ring_h = 0, opt_h = 0, hot_h = 0;
+  for (int w = tid >> 5; w < nw; w += nwarps) {
+    const uint32_t bits = bm[w];
+    if (bits == 0) {
+      if (lane == 0) mcw[w] = 0;
+      continue;
     }
-    for (;;) {
-      int32_t ub[kBatch];
-      int nb = 0;
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        while (bits == 0 && w < w1) {
-          if (++w < w1) {
-            wp[w] = q + i;
-            bits = bm[w];
-          }
-        }
-        if (bits) {
-          ub[i] = (int32_t)(row_lo + ((w << 5) | (__ffs(bits) - 1)));
-          bits &= bits - 1;
-          nb = i + 1;
-        } else {
-          ub[i] = -1;
-        }
+    bool missing = false;
+    if ((bits >> lane) & 1u) {
+      const int rel = (w << 5) | lane;
+      const int32_t u = (int32_t)(row_lo + rel);
+      const int32_t hs = pf ? hmap_s[rel] : hot_map[u];
+      const int32_t om = !any_opt ? -1 : pf ? omap_s[rel] : opt_map[u];
+      if (hs >= 0) atomicOr(&prot[hs >> 5], 1u << (hs & 31));
+      int32_t l;
+      if (u >= ring_lo && u < n) {
+        l = make_loc(DHS_LOC_RING, (int)(u % c.Rd));
+        ++ring_h;
+      } else if (om >= 0) {
+        l = make_loc(DHS_LOC_OPT, om);
+        ++opt_h;
+      } else if (hs >= 0) {
+        l = make_loc(DHS_LOC_HOT, hs);
+        hot_stamp[hs] = tick;
+        atomicOr(&now[hs >> 5], 1u << (hs & 31));
+        ++hot_h;
+      } else {
+        l = kMissMark;
+        missing = true;
       }
-      int32_t hm[kBatch], om[kBatch];
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        if (ub[i] < 0) {
-          hm[i] = om[i] = -1;
-        } else if (pf) {
-          hm[i] = hmap_s[ub[i] - row_lo];
-          om[i] = any_opt ? omap_s[ub[i] - row_lo] : -1;
-        } else {
-          hm[i] = hot_map[ub[i]];
-          om[i] = any_opt ? opt_map[ub[i]] : -1;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int32_t u = ub[i];
-        if (u < 0) continue;
-        const int32_t hs = hm[i];
-        if (hs >= 0) atomicOr(&prot[hs >> 5], 1u << (hs & 31));
-        int32_t l;
-        if (u >= ring_lo && u < n) {
-          l = make_loc(DHS_LOC_RING, (int)(u % c.Rd));
-          ++ring_h;
-        } else if (om[i] >= 0) {
-          l = make_loc(DHS_LOC_OPT, om[i]);
-          ++opt_h;
-        } else if (hs >= 0) {
-          l = make_loc(DHS_LOC_HOT, hs);
-          hot_stamp[hs] = tick;
-          atomicOr(&now[hs >> 5], 1u << (hs & 31));
-          ++hot_h;
-        } else {
-          l = kMissMark;
-          ++misses_here;
-        }
-        ul[q] = l;
-        ++q;
-      }
-      if (nb < kBatch) break;
+      ul[wp[w] + __popc(bits & lt)] = l;
     }
+    const uint32_t mm = __ballot_sync(0xffffffffu, missing);
+    if (lane == 0) mcw[w] = __popc(mm);
   }
   warp_add(&sh_cnt[0], ring_h);
   warp_add(&sh_cnt[1], opt_h);
   warp_add(&sh_cnt[2], hot_h);
+  __syncthreads();  // every word's miss count is known
   int Mc;
-  const int m_local = ublock_excl_scan(misses_here, warp_sums, Mc);
+  {
+    int mc = 0;
+    for (int w = w0; w < w1; ++w) mc += mcw[w];
+    int m = ublock_excl_scan(mc, warp_sums, Mc);
+    for (int w = w0; w < w1; ++w) {  // miss count -> index of the word's first miss
+      const int x = mcw[w];
+      mcw[w] = m;
+      m += x;
+    }
+  }
   if (tid == 0) {
     sh_u = Uc;
     sh_m = Mc;
@@ -296,25 +284,25 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       prot[i] = pv;
       now[i] = nv;
     }
-  // union rows and misses of the slice get their request-wide ranks
-  {
-    int q = u_local, m = m_local;
-    for (int w = w0; w < w1; ++w) {
-      uint32_t bits = bm[w];
-      while (bits) {
-        const int32_t u = (int32_t)(row_lo + ((w << 5) | (__ffs(bits) - 1)));
-        bits &= bits - 1;
-        uni[u_base + q] = u;
-        if (ul[q] == kMissMark) {
-          miss[m_base + m] = u;
-          c.first_occ[(size_t)r * KK + m_base + m] = INT_MAX;
-          ul[q] = make_loc(DHS_LOC_STAGE, m_base + m);
-          ++m;
-        }
-        *reinterpret_cast<int2 *>(&uent[u_base + q]) = make_int2(u, ul[q]);
-        ++q;
-      }
+  // union rows and misses of the slice get their request-wide ranks, a word
+  // per warp as in the probe
+  for (int w = tid >> 5; w < nw; w += nwarps) {
+    const uint32_t bits = bm[w];
+    if (bits == 0) continue;
+    const bool mine = (bits >> lane) & 1u;
+    const int q = wp[w] + __popc(bits & lt);
+    const bool missing = mine && ul[q] == kMissMark;
+    const uint32_t mm = __ballot_sync(0xffffffffu, missing);
+    if (!mine) continue;
+    const int32_t u = (int32_t)(row_lo + ((w << 5) | lane));
+    uni[u_base + q] = u;
+    if (missing) {
+      const int m = m_base + mcw[w] + __popc(mm & lt);
+      miss[m] = u;
+      c.first_occ[(size_t)r * KK + m] = INT_MAX;
+      ul[q] = make_loc(DHS_LOC_STAGE, m);
     }
+    *reinterpret_cast<int2 *>(&uent[u_base + q]) = make_int2(u, ul[q]);
   }
   __syncthreads();  // the slice's locations and first-selection slots are set
 
