@@ -71,17 +71,21 @@ __host__ __device__ static inline int union_slice(int64_t s_max) {
   return (int)((((s_max + kUnionCluster - 1) / kUnionCluster) + 31) & ~31);
 }
 
-// Slices of up to this many rows also keep their hot and optional map entries
-// in shared memory, fetched while the bitmap is built.
-constexpr int kMapPrefetchRows = 8192;
-
-size_t union_smem_bytes(const DevCtx &c) {
+// Shared memory of one CTA without, and with, the slice's hot and optional
+// map entries; the entries are kept (fetched while the bitmap is built) when
+// they fit.
+__host__ __device__ inline size_t union_base_bytes(const DevCtx &c) {
   const int slice = union_slice(c.Sm);
   const size_t sw = (size_t)slice / 32;  // words of one slice
   const size_t pw = (size_t)((c.B + 31) / 32);
-  const size_t maps = slice <= kMapPrefetchRows ? (size_t)slice * 8 : 0;
   const size_t KK = (size_t)c.Kmax * c.k;
-  return sw * 12 + pw * 8 + (size_t)c.B * 8 + KK * 4 + (KK + 3) / 4 * 4 + maps;
+  return sw * 12 + pw * 8 + (size_t)c.B * 8 + KK * 4 + (KK + 3) / 4 * 4;
+}
+__host__ __device__ inline bool union_map_prefetch(const DevCtx &c) {
+  return union_base_bytes(c) + (size_t)union_slice(c.Sm) * 8 <= kMaxDynSmem;
+}
+size_t union_smem_bytes(const DevCtx &c) {
+  return union_base_bytes(c) + (union_map_prefetch(c) ? (size_t)union_slice(c.Sm) * 8 : 0);
 }
 
 __global__ void __cluster_dims__(kUnionCluster, 1, 1) __launch_bounds__(kUnionThreads)
@@ -119,7 +123,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   int32_t *ul = lru_s + B;     // location of each union row of this slice
   uint32_t *umw = reinterpret_cast<uint32_t *>(ul + KK);  // query masks, one byte per union row
   const int umw_words = (KK + 3) / 4;
-  const bool pf = slice <= kMapPrefetchRows;
+  const bool pf = union_map_prefetch(c);
   int32_t *hmap_s = reinterpret_cast<int32_t *>(umw + umw_words);  // slice's hot-map entries (when pf)
   int32_t *omap_s = hmap_s + slice;
 
@@ -205,39 +209,57 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   const int lane = tid & 31, nwarps = bs >> 5;
   const uint32_t lt = (1u << lane) - 1u;
   int ring_h = 0, opt_h = 0, hot_h = 0;
-  for (int w = tid >> 5; w < nw; w += nwarps) {
-    const uint32_t bits = bm[w];
-    if (bits == 0) {
-      if (lane == 0) mcw[w] = 0;
-      continue;
-    }
-    bool missing = false;
-    if ((bits >> lane) & 1u) {
-      const int rel = (w << 5) | lane;
-      const int32_t u = (int32_t)(row_lo + rel);
-      const int32_t hs = pf ? hmap_s[rel] : hot_map[u];
-      const int32_t om = !any_opt ? -1 : pf ? omap_s[rel] : opt_map[u];
-      if (hs >= 0) atomicOr(&prot[hs >> 5], 1u << (hs & 31));
-      int32_t l;
-      if (u >= ring_lo && u < n) {
-        l = make_loc(DHS_LOC_RING, (int)(u % c.Rd));
-        ++ring_h;
-      } else if (om >= 0) {
-        l = make_loc(DHS_LOC_OPT, om);
-        ++opt_h;
-      } else if (hs >= 0) {
-        l = make_loc(DHS_LOC_HOT, hs);
-        hot_stamp[hs] = tick;
-        atomicOr(&now[hs >> 5], 1u << (hs & 31));
-        ++hot_h;
-      } else {
-        l = kMissMark;
-        missing = true;
+  constexpr int kWordsInFlight = 4;  // map loads of several words in flight (global maps)
+  for (int w0p = tid >> 5; w0p < nw; w0p += kWordsInFlight * nwarps) {
+    uint32_t wb[kWordsInFlight];
+    int32_t hsv[kWordsInFlight], omv[kWordsInFlight];
+#pragma unroll
+    for (int k = 0; k < kWordsInFlight; ++k) {
+      const int w = w0p + k * nwarps;
+      wb[k] = w < nw ? bm[w] : 0u;
+      hsv[k] = omv[k] = -1;
+      if ((wb[k] >> lane) & 1u) {
+        const int rel = (w << 5) | lane;
+        const int32_t u = (int32_t)(row_lo + rel);
+        hsv[k] = pf ? hmap_s[rel] : hot_map[u];
+        if (any_opt) omv[k] = pf ? omap_s[rel] : opt_map[u];
       }
-      ul[wp[w] + __popc(bits & lt)] = l;
     }
-    const uint32_t mm = __ballot_sync(0xffffffffu, missing);
-    if (lane == 0) mcw[w] = __popc(mm);
+#pragma unroll
+    for (int k = 0; k < kWordsInFlight; ++k) {
+      const int w = w0p + k * nwarps;
+      if (w >= nw) break;
+      const uint32_t bits = wb[k];
+      if (bits == 0) {
+        if (lane == 0) mcw[w] = 0;
+        continue;
+      }
+      bool missing = false;
+      if ((bits >> lane) & 1u) {
+        const int32_t u = (int32_t)(row_lo + ((w << 5) | lane));
+        const int32_t hs = hsv[k], om = omv[k];
+        if (hs >= 0) atomicOr(&prot[hs >> 5], 1u << (hs & 31));
+        int32_t l;
+        if (u >= ring_lo && u < n) {
+          l = make_loc(DHS_LOC_RING, (int)(u % c.Rd));
+          ++ring_h;
+        } else if (om >= 0) {
+          l = make_loc(DHS_LOC_OPT, om);
+          ++opt_h;
+        } else if (hs >= 0) {
+          l = make_loc(DHS_LOC_HOT, hs);
+          hot_stamp[hs] = tick;
+          atomicOr(&now[hs >> 5], 1u << (hs & 31));
+          ++hot_h;
+        } else {
+          l = kMissMark;
+          missing = true;
+        }
+        ul[wp[w] + __popc(bits & lt)] = l;
+      }
+      const uint32_t mm = __ballot_sync(0xffffffffu, missing);
+      if (lane == 0) mcw[w] = __popc(mm);
+    }
   }
   warp_add(&sh_cnt[0], ring_h);
   warp_add(&sh_cnt[1], opt_h);

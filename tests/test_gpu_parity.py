@@ -177,6 +177,35 @@ def test_index_scores_exact(rec):
     assert run.ctx.stats()["device_error"] == 0
 
 
+@pytest.mark.parametrize("d_idx", [64, 128], ids=["64B", "128B"])
+def test_index_scores_exact_large_launch(d_idx):
+    """64- and 128-byte index rows go to the tensor-core scorer once a launch
+    streams 256 MB of keys or more: sampled requests' scores and top-k lists
+    equal the oracle's."""
+    from oracle.dhs_oracle import index_scores, topk_ordered
+    import torch
+    S = 65536 if d_idx == 64 else 32768
+    rec = wl.Recipe("large_launch_%dB" % d_idx, N=64, K=4, S=S, H_idx=1, d_idx=d_idx, topk=256,
+                    Hq=8, Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=64, rho_within=0.5,
+                    rho_cross=0.6, W=16, p=8, seed=41, i8_lo=-128, i8_hi=127)
+    assert rec.N * rec.S * rec.idx_row >= 256 << 20
+    run = _runner(rec)
+    run.load_round(0)
+    kr = rec.k_per_req()
+    run.select(kr)
+    ss = (rec.s_max + 31) // 32 * 32
+    sc = run.export("scores", torch.int32, (rec.N, run.Km, ss)).cpu().numpy()
+    topk = run.topk.cpu().numpy()
+    qi = rec.index_queries(0, 0, rec.N)
+    for r in (0, 37, 63):
+        keys = rec.index_keys(r, r + 1)[0]
+        for j in range(int(kr[r])):
+            want = index_scores(qi[r, j], keys, rec.S)
+            assert np.array_equal(sc[r, j, :rec.S].astype(np.int64), want), "r=%d j=%d" % (r, j)
+            assert np.array_equal(topk[r, j], topk_ordered(want, rec.topk)), "r=%d j=%d" % (r, j)
+    assert run.ctx.stats()["device_error"] == 0
+
+
 def test_index_scores_extreme_values():
     """The largest magnitudes a 512-byte row can produce: every product is
     (-128)(-128) or (-128)(127), so the scores are +2^23 and -2^23 + 65536
