@@ -79,7 +79,7 @@ __host__ __device__ inline size_t union_base_bytes(const DevCtx &c) {
   const size_t sw = (size_t)slice / 32;  // words of one slice
   const size_t pw = (size_t)((c.B + 31) / 32);
   const size_t KK = (size_t)c.Kmax * c.k;
-  return sw * 12 + pw * 8 + (size_t)c.B * 8 + KK * 4 + (KK + 3) / 4 * 4;
+  return sw * 8 + pw * 8 + (size_t)c.B * 8 + KK * 8 + (KK + 3) / 4 * 4;
 }
 __host__ __device__ inline bool union_map_prefetch(const DevCtx &c) {
   return union_base_bytes(c) + (size_t)union_slice(c.Sm) * 8 <= kMaxDynSmem;
@@ -115,13 +115,13 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   const int nw = row_hi > row_lo ? (int)((row_hi - row_lo + 31) >> 5) : 0;
   uint32_t *bm = reinterpret_cast<uint32_t *>(smem);
   uint32_t *wp = bm + sw;
-  int *mcw = reinterpret_cast<int *>(wp + sw);  // misses per word, then their prefix
-  uint32_t *prot = reinterpret_cast<uint32_t *>(mcw + sw);  // protected slots (the leader: of the request)
+  uint32_t *prot = wp + sw;  // protected slots (the leader: of the request)
   uint32_t *now = prot + pw;  // slots stamped by this tick (likewise)
   int32_t *candB = reinterpret_cast<int32_t *>(now + pw);
   int32_t *lru_s = candB + B;  // leader: LRU order at the start of the call
   int32_t *ul = lru_s + B;     // location of each union row of this slice
-  uint32_t *umw = reinterpret_cast<uint32_t *>(ul + KK);  // query masks, one byte per union row
+  int32_t *urow = ul + KK;     // the slice's union rows, by union index
+  uint32_t *umw = reinterpret_cast<uint32_t *>(urow + KK);  // query masks, one byte per union row
   const int umw_words = (KK + 3) / 4;
   const bool pf = union_map_prefetch(c);
   int32_t *hmap_s = reinterpret_cast<int32_t *>(umw + umw_words);  // slice's hot-map entries (when pf)
@@ -184,8 +184,9 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   }
   __syncthreads();  // the slice's bitmap is complete
 
-  // 2. ascending compaction of the slice: each thread owns a run of words and
-  //    records, for every word, the union index of its first row
+  // 2. ascending compaction of the slice: each thread owns a run of words,
+  //    records for every word the union index of its first row, and lists
+  //    the run's rows by union index
   const int per = (nw + bs - 1) / bs;
   const int w0 = min(nw, tid * per), w1 = min(nw, w0 + per);
   int cnt = 0;
@@ -195,87 +196,65 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
     int q = ublock_excl_scan(cnt, warp_sums, Uc);
     for (int w = w0; w < w1; ++w) {
       wp[w] = q;
-      q += __popc(bm[w]);
+      for (uint32_t bits = bm[w]; bits; bits &= bits - 1)
+        urow[q++] = (int32_t)(row_lo + ((w << 5) | (__ffs(bits) - 1)));
     }
   }
 
   cp_async_wait_all();
-  __syncthreads();  // word prefixes and prefetched map entries are in place
+  __syncthreads();  // the row list and prefetched map entries are in place
 
   // 3. probe each union row of the slice: live ring tail, optional map, hot
-  //    cache, else miss; the protected and stamped hot slots are marked.  A
-  //    warp takes one word at a time, a lane one bit, so the rows of a word
-  //    are probed side by side; each word's miss count is kept for the ranks.
-  const int lane = tid & 31, nwarps = bs >> 5;
-  const uint32_t lt = (1u << lane) - 1u;
-  int ring_h = 0, opt_h = 0, hot_h = 0;
-  constexpr int kWordsInFlight = 4;  // map loads of several words in flight (global maps)
-  for (int w0p = tid >> 5; w0p < nw; w0p += kWordsInFlight * nwarps) {
-    uint32_t wb[kWordsInFlight];
-    int32_t hsv[kWordsInFlight], omv[kWordsInFlight];
+  //    cache, else miss; the protected and stamped hot slots are marked.
+  //    Thread t takes the union indices [t * pr, (t + 1) * pr), in order, so
+  //    the misses are ranked by one scan.
+  const int pr = (Uc + bs - 1) / bs;
+  const int q0 = min(Uc, tid * pr), q1 = min(Uc, q0 + pr);
+  int ring_h = 0, opt_h = 0, hot_h = 0, misses_here = 0;
+  for (int qb = q0; qb < q1; qb += kBatch) {
+    int32_t hsv[kBatch], omv[kBatch];
 #pragma unroll
-    for (int k = 0; k < kWordsInFlight; ++k) {
-      const int w = w0p + k * nwarps;
-      wb[k] = w < nw ? bm[w] : 0u;
-      hsv[k] = omv[k] = -1;
-      if ((wb[k] >> lane) & 1u) {
-        const int rel = (w << 5) | lane;
-        const int32_t u = (int32_t)(row_lo + rel);
-        hsv[k] = pf ? hmap_s[rel] : hot_map[u];
-        if (any_opt) omv[k] = pf ? omap_s[rel] : opt_map[u];
+    for (int i = 0; i < kBatch; ++i) {  // map loads of the batch in flight together
+      hsv[i] = omv[i] = -1;
+      const int q = qb + i;
+      if (q < q1) {
+        const int32_t u = urow[q];
+        const int rel = (int)(u - row_lo);
+        hsv[i] = pf ? hmap_s[rel] : hot_map[u];
+        if (any_opt) omv[i] = pf ? omap_s[rel] : opt_map[u];
       }
     }
 #pragma unroll
-    for (int k = 0; k < kWordsInFlight; ++k) {
-      const int w = w0p + k * nwarps;
-      if (w >= nw) break;
-      const uint32_t bits = wb[k];
-      if (bits == 0) {
-        if (lane == 0) mcw[w] = 0;
-        continue;
+    for (int i = 0; i < kBatch; ++i) {
+      const int q = qb + i;
+      if (q >= q1) break;
+      const int32_t u = urow[q];
+      const int32_t hs = hsv[i], om = omv[i];
+      if (hs >= 0) atomicOr(&prot[hs >> 5], 1u << (hs & 31));
+      int32_t l;
+      if (u >= ring_lo && u < n) {
+        l = make_loc(DHS_LOC_RING, (int)(u % c.Rd));
+        ++ring_h;
+      } else if (om >= 0) {
+        l = make_loc(DHS_LOC_OPT, om);
+        ++opt_h;
+      } else if (hs >= 0) {
+        l = make_loc(DHS_LOC_HOT, hs);
+        hot_stamp[hs] = tick;
+        atomicOr(&now[hs >> 5], 1u << (hs & 31));
+        ++hot_h;
+      } else {
+        l = kMissMark;
+        ++misses_here;
       }
-      bool missing = false;
-      if ((bits >> lane) & 1u) {
-        const int32_t u = (int32_t)(row_lo + ((w << 5) | lane));
-        const int32_t hs = hsv[k], om = omv[k];
-        if (hs >= 0) atomicOr(&prot[hs >> 5], 1u << (hs & 31));
-        int32_t l;
-        if (u >= ring_lo && u < n) {
-          l = make_loc(DHS_LOC_RING, (int)(u % c.Rd));
-          ++ring_h;
-        } else if (om >= 0) {
-          l = make_loc(DHS_LOC_OPT, om);
-          ++opt_h;
-        } else if (hs >= 0) {
-          l = make_loc(DHS_LOC_HOT, hs);
-          hot_stamp[hs] = tick;
-          atomicOr(&now[hs >> 5], 1u << (hs & 31));
-          ++hot_h;
-        } else {
-          l = kMissMark;
-          missing = true;
-        }
-        ul[wp[w] + __popc(bits & lt)] = l;
-      }
-      const uint32_t mm = __ballot_sync(0xffffffffu, missing);
-      if (lane == 0) mcw[w] = __popc(mm);
+      ul[q] = l;
     }
   }
   warp_add(&sh_cnt[0], ring_h);
   warp_add(&sh_cnt[1], opt_h);
   warp_add(&sh_cnt[2], hot_h);
-  __syncthreads();  // every word's miss count is known
   int Mc;
-  {
-    int mc = 0;
-    for (int w = w0; w < w1; ++w) mc += mcw[w];
-    int m = ublock_excl_scan(mc, warp_sums, Mc);
-    for (int w = w0; w < w1; ++w) {  // miss count -> index of the word's first miss
-      const int x = mcw[w];
-      mcw[w] = m;
-      m += x;
-    }
-  }
+  const int m_local = ublock_excl_scan(misses_here, warp_sums, Mc);
   if (tid == 0) {
     sh_u = Uc;
     sh_m = Mc;
@@ -306,23 +285,16 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       prot[i] = pv;
       now[i] = nv;
     }
-  // union rows and misses of the slice get their request-wide ranks, a word
-  // per warp as in the probe
-  for (int w = tid >> 5; w < nw; w += nwarps) {
-    const uint32_t bits = bm[w];
-    if (bits == 0) continue;
-    const bool mine = (bits >> lane) & 1u;
-    const int q = wp[w] + __popc(bits & lt);
-    const bool missing = mine && ul[q] == kMissMark;
-    const uint32_t mm = __ballot_sync(0xffffffffu, missing);
-    if (!mine) continue;
-    const int32_t u = (int32_t)(row_lo + ((w << 5) | lane));
+  // union rows and misses of the slice get their request-wide ranks, each
+  // thread over the union indices it probed
+  for (int q = q0, m = m_base + m_local; q < q1; ++q) {
+    const int32_t u = urow[q];
     uni[u_base + q] = u;
-    if (missing) {
-      const int m = m_base + mcw[w] + __popc(mm & lt);
+    if (ul[q] == kMissMark) {
       miss[m] = u;
       c.first_occ[(size_t)r * KK + m] = INT_MAX;
       ul[q] = make_loc(DHS_LOC_STAGE, m);
+      ++m;
     }
     *reinterpret_cast<int2 *>(&uent[u_base + q]) = make_int2(u, ul[q]);
   }
