@@ -304,6 +304,7 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   d.k = g.topk;
   d.Sm = g.s_max;
   d.Ss = (g.s_max + 31) / 32 * 32;
+  d.kinv = 0xFFFFFFFFu / (uint32_t)g.topk + 1u;
   d.idx_row = g.idx_heads * g.idx_dim;
   d.Hq = g.q_heads;
   d.Hkv = g.kv_heads;

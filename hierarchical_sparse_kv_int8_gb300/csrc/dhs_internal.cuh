@@ -50,6 +50,7 @@ struct DevCtx {
   int N, Kmax, k;
   int64_t Sm;
   int64_t Ss;  // row stride of the score buffer: Sm rounded up to 32
+  uint32_t kinv;  // ceil(2^32 / k): e / k = umulhi(e, kinv) for e < 8k
   int idx_row;           // H_idx * d_idx bytes per index-key row
   int Hq, Hkv, dqk, dv, row;  // row = bf16 elements per stored row
   int layout;

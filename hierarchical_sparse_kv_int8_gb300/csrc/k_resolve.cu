@@ -95,7 +95,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
-  __shared__ int sh_cnt[5];  // ring, opt, hot hits, selections, miss selections
+  __shared__ int sh_cnt[6];  // ring, opt, hot hits, selections, miss selections, mask bits
   __shared__ int sh_u, sh_m, sh_p;  // this CTA's union rows and misses; the leader's P
   const int crank = (int)cl.block_rank();
   const int r = blockIdx.x / kUnionCluster;
@@ -162,7 +162,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   for (int i = tid; i < sw; i += bs) bm[i] = 0;
   for (int i = tid; i < umw_words; i += bs) umw[i] = 0;
   for (int i = tid; i < 2 * pw; i += bs) prot[i] = 0;  // prot and now
-  if (tid < 5) sh_cnt[tid] = 0;
+  if (tid < 6) sh_cnt[tid] = 0;
   __syncthreads();
   for (int e0 = tid; e0 < nsel; e0 += kBatch * bs) {
     int32_t sv[kBatch];
@@ -325,8 +325,10 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       const uint32_t word = bm[rel >> 5];
       const int q = wp[rel >> 5] + __popc(word & ((1u << (rel & 31)) - 1u));
       int32_t l = ul[q];
-      const uint32_t qbit = 1u << ((q & 3) * 8 + e / k);
-      if (atomicOr(&umw[q >> 2], qbit) & qbit) record_error(c.err, DC_DUPLICATE, K_UNION_PROBE);
+      // query e / k, by a multiply with the rounded-up reciprocal of k (exact
+      // for e < 8k and k < 2^14)
+      const uint32_t qbit = 1u << ((q & 3) * 8 + (int)__umulhi((unsigned)e, c.kinv));
+      atomicOr(&umw[q >> 2], qbit);
       ++sel_here;
       if (loc_tier(l) == DHS_LOC_STAGE) {
         ++missel;
@@ -342,10 +344,19 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   warp_add(&sh_cnt[3], sel_here);
   warp_add(&sh_cnt[4], missel);
   __syncthreads();  // the query masks of the slice are complete
-  // 5. second half of each union entry: the queries that selected the row
-  for (int q = tid; q < Uc; q += bs)
-    *reinterpret_cast<int2 *>(&uent[u_base + q].z) =
-        make_int2((int)((umw[q >> 2] >> ((q & 3) * 8)) & 0xFFu), 0);
+  // 5. second half of each union entry: the queries that selected the row.
+  //    A row listed twice by one query sets one bit for two selections, so
+  //    the slice's bits fall short of its selections exactly when a query
+  //    repeats a row (checked at the end).
+  {
+    int bits_here = 0;
+    for (int q = tid; q < Uc; q += bs) {
+      const uint32_t qm = (umw[q >> 2] >> ((q & 3) * 8)) & 0xFFu;
+      bits_here += __popc(qm);
+      *reinterpret_cast<int2 *>(&uent[u_base + q].z) = make_int2((int)qm, 0);
+    }
+    warp_add(&sh_cnt[5], bits_here);
+  }
   // 6. victims (leader): unprotected slots in LRU order (stamp, slot), empty first
   const int perB = (B + bs - 1) / bs;
   const int b0 = min(B, tid * perB), b1 = min(B, b0 + perB);
@@ -392,6 +403,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       c.inst[(size_t)r * KK + c.first_occ[(size_t)r * KK + p]] = candB[p];
   __syncthreads();
   if (tid == 0) {
+    if (sh_cnt[5] != sh_cnt[3]) record_error(c.err, DC_DUPLICATE, K_UNION_PROBE);
     atomicAdd(&c.stats[ST_SEL], (unsigned long long)sh_cnt[3]);
     atomicAdd(&c.stats[ST_RING], (unsigned long long)sh_cnt[0]);
     atomicAdd(&c.stats[ST_OPT], (unsigned long long)sh_cnt[1]);
