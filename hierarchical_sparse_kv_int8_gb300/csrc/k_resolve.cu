@@ -56,19 +56,23 @@ __device__ __forceinline__ void warp_add(int *dst, int v) {
 }
 
 // The union/probe of one request runs on a cluster of kUnionCluster CTAs.
-// CTA c owns the c-th slice of the history rows: its shared memory holds the
-// union bitmap of that slice, the prefix count of every word and the
-// location of every union row in the slice, and the protected-slot and
+// CTA c >= 1 owns the (c-1)-th slice of the history rows: its shared memory
+// holds the union bitmap of that slice, the prefix count of every word, the
+// slice's union rows and their locations, and the protected-slot and
 // stamped-now bitmaps of the hot cache marked by its own probes (shared-memory
-// atomics).  After the first cluster barrier the leader CTA (rank 0) merges
-// the slices' bitmaps through distributed shared memory and chooses the
-// victims.
+// atomics).  After the first cluster barrier the leader CTA (rank 0), which
+// owns no slice, merges the slices' bitmaps through distributed shared memory
+// and chooses the victims while the other CTAs form their locations.
 constexpr int kUnionCluster = 8;
 constexpr int32_t kMissMark = -2;
 constexpr int kBatch = 8;  // independent global loads in flight per thread
 
+// The history is cut into kUnionSlices slices, one per CTA of ranks
+// 1..kUnionCluster-1; the leader (rank 0) owns no slice, so its victim choice
+// runs while the other CTAs form their locations.
+constexpr int kUnionSlices = kUnionCluster - 1;
 __host__ __device__ static inline int union_slice(int64_t s_max) {
-  return (int)((((s_max + kUnionCluster - 1) / kUnionCluster) + 31) & ~31);
+  return (int)((((s_max + kUnionSlices - 1) / kUnionSlices) + 31) & ~31);
 }
 
 // Shared memory of one CTA without, and with, the slice's hot and optional
@@ -110,8 +114,8 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   const int slice = union_slice(c.Sm);
   const int sw = slice / 32;
   const int pw = (B + 31) >> 5;
-  const int64_t row_lo = (int64_t)crank * slice;
-  const int64_t row_hi = min(n, row_lo + slice);
+  const int64_t row_lo = crank == 0 ? 0 : (int64_t)(crank - 1) * slice;
+  const int64_t row_hi = crank == 0 ? 0 : min(n, row_lo + slice);
   const int nw = row_hi > row_lo ? (int)((row_hi - row_lo + 31) >> 5) : 0;
   uint32_t *bm = reinterpret_cast<uint32_t *>(smem);
   uint32_t *wp = bm + sw;
@@ -164,7 +168,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   for (int i = tid; i < 2 * pw; i += bs) prot[i] = 0;  // prot and now
   if (tid < 6) sh_cnt[tid] = 0;
   __syncthreads();
-  for (int e0 = tid; e0 < nsel; e0 += kBatch * bs) {
+  for (int e0 = crank == 0 ? nsel : tid; e0 < nsel; e0 += kBatch * bs) {
     int32_t sv[kBatch];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
@@ -177,7 +181,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       if (s >= row_lo && s < row_hi) {
         const int rel = (int)(s - row_lo);
         atomicOr(&bm[rel >> 5], 1u << (rel & 31));
-      } else if (crank == 0 && s != -1 && (s < 0 || s >= n)) {
+      } else if (crank == 1 && s != -1 && (s < 0 || s >= n)) {
         record_error(c.err, DC_ROW_RANGE, K_UNION_PROBE);
       }
     }
@@ -304,7 +308,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   //    depend on the ranks only, so every CTA forms them before the leader's
   //    victim choice)
   int sel_here = 0, missel = 0;
-  for (int e0 = tid; e0 < nsel; e0 += kBatch * bs) {
+  for (int e0 = crank == 0 ? nsel : tid; e0 < nsel; e0 += kBatch * bs) {
     int32_t sv[kBatch];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
@@ -318,7 +322,7 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
       const int32_t s = sv[i];
       const bool mine = s >= row_lo && s < row_hi;
       if (!mine) {
-        if (crank == 0 && (s < 0 || s >= n)) loc_out[(size_t)r * KK + e] = -1;
+        if (crank == 1 && (s < 0 || s >= n)) loc_out[(size_t)r * KK + e] = -1;
         continue;
       }
       const int rel = (int)(s - row_lo);
