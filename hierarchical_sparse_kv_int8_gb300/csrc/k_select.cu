@@ -566,14 +566,37 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
     // counts of this CTA's warps, then of the cluster's CTAs
     const int run = ((((p1 - p0) + 31) / 32) + 31) & ~31;
     const int r0 = min(p1, p0 + wid * run), r1 = min(p1, r0 + run);
-    int ngt = 0, neq = 0;
+    const unsigned lt = (1u << lane) - 1u;
+    // With staged scores and exact bins, the counting pass also compacts the
+    // warp's winners, in row order, into the front of its own run of the
+    // stage (a write never lands beyond the row being read), packed as
+    // (above T, value, row - p0); the collection then reads only these lists.
+    const bool inplace = staged && passes <= 1;
+    uint32_t *wl = reinterpret_cast<uint32_t *>(stg) + (r0 - p0);
+    int ngt = 0, neq = 0, wcount = 0;
+    if (inplace) {
+#pragma unroll 4
+      for (int base = r0; base < r1; base += 32) {
+        const int s = base + lane;
+        const bool ok = s < r1;
+        const uint32_t v = ok ? (uint32_t)(val(s) - lo) : 0u;
+        const bool gt = ok && v > T, eq = ok && v == T;
+        const unsigned bw = __ballot_sync(0xffffffffu, gt || eq);
+        if (gt || eq)
+          wl[wcount + __popc(bw & lt)] = (gt ? 0x80000000u : 0u) | (v << 17) | (uint32_t)(s - p0);
+        wcount += __popc(bw);
+        ngt += __popc(__ballot_sync(0xffffffffu, gt));
+      }
+      neq = wcount - ngt;
+    } else {
 #pragma unroll 8
-    for (int base = r0; base < r1; base += 32) {
-      const int s = base + lane;
-      const bool ok = s < r1;
-      const uint32_t v = ok ? (uint32_t)(val(s) - lo) : 0u;
-      ngt += __popc(__ballot_sync(0xffffffffu, ok && v > T));
-      neq += __popc(__ballot_sync(0xffffffffu, ok && v == T));
+      for (int base = r0; base < r1; base += 32) {
+        const int s = base + lane;
+        const bool ok = s < r1;
+        const uint32_t v = ok ? (uint32_t)(val(s) - lo) : 0u;
+        ngt += __popc(__ballot_sync(0xffffffffu, ok && v > T));
+        neq += __popc(__ballot_sync(0xffffffffu, ok && v == T));
+      }
     }
     if (lane == 0) {
       wgt[wid] = ngt;
@@ -609,10 +632,28 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
     // the cluster barrier above, so the histogram area is free for reuse.
     const bool exact = passes <= 1;
     const int *base = reinterpret_cast<const int *>(hist + (1 << kRadixBits));
-    const unsigned lt = (1u << lane) - 1u;
     const int gt_end = gt_off + ngt, eq_end = eq_off + neq;
+    if (inplace) {
+      for (int i0 = 0; i0 < wcount; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t e = i < wcount ? wl[i] : 0u;
+        const bool gt = i < wcount && (e >> 31), eq = i < wcount && !(e >> 31);
+        const unsigned bgt = __ballot_sync(0xffffffffu, gt);
+        const unsigned beq = __ballot_sync(0xffffffffu, eq);
+        const uint32_t v = (e >> 17) & 0x3FFFu;
+        const int s = p0 + (int)(e & 0x1FFFFu);
+        if (gt) cand[gt_off + __popc(bgt & lt)] = topk_key(v, s);
+        if (eq) {
+          const int rr = eq_off + __popc(beq & lt);  // rank among this CTA's ties
+          if (rr < kept_eq) out[c_gt + eq_base + rr] = s;
+        }
+        gt_off += __popc(bgt);
+        eq_off += __popc(beq);
+      }
+    }
 #pragma unroll 4
-    for (int bs = r0; bs < r1 && (gt_off < gt_end || (eq_off < eq_end && eq_off < kept_eq));
+    for (int bs = r0; !inplace && bs < r1 &&
+                      (gt_off < gt_end || (eq_off < eq_end && eq_off < kept_eq));
          bs += 32) {
       const int s = bs + lane;
       const bool ok = s < r1;
@@ -1068,7 +1109,8 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, const int8_t *q_
   // a CTA's part of the widest domain, staged in shared memory when it fits
   const int part = ((max(max_dom, 1) + kTopkCluster - 1) / kTopkCluster + 31) & ~31;
   int stage_cap = 0;
-  if (smem_topk + 8 + (size_t)part * 4 <= kMaxDynSmem) {
+  // (the in-place winner lists pack a row's place in the part into 17 bits)
+  if (smem_topk + 8 + (size_t)part * 4 <= kMaxDynSmem && part <= (1 << 17)) {
     stage_cap = part;
     smem_topk = (((size_t)kp * 8 + 15) & ~(size_t)15) + ((size_t)2 << kRadixBits) * 4 +
                 (size_t)part * 4;
