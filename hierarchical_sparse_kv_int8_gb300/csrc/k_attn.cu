@@ -27,6 +27,7 @@
 #include "dhs_internal.cuh"
 #include "ptx_util.cuh"
 
+#include <cooperative_groups.h>
 #include <math_constants.h>
 
 namespace dhs {
@@ -35,6 +36,9 @@ constexpr int kAttnStages = 3;
 constexpr int kTileRows = 16;
 constexpr int kAttnThreads = 128;
 constexpr int kAttnSpinLimit = 1 << 20;  // bounded wait for a stage's copies
+// An item split exactly kAttnCluster ways (128-dim heads) runs its splits as
+// one thread-block cluster and merges them through distributed shared memory.
+constexpr int kAttnCluster = 8;
 
 bool attn_shape_supported(int dqk, int dv, int layout) {
   if (layout == DHS_KV_SPLIT) return dqk == 128 && dv == 128;
@@ -66,6 +70,8 @@ int attn_splits(const DevCtx &c, int active_queries) {
   const int max_ns = (rows + gran - 1) / gran;
   if (ns > max_ns) ns = max_ns;
   if (ns < 1) ns = 1;
+  // near kAttnCluster splits, take exactly that many: the cluster merge
+  if (c.dqk == 128 && ns >= 6 && ns <= 12 && kAttnCluster <= max_ns) return kAttnCluster;
   int chunk = (rows + ns - 1) / ns;
   chunk = (chunk + gran - 1) / gran * gran;
   return (rows + chunk - 1) / chunk;
@@ -422,6 +428,12 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   __syncthreads();
   const size_t qbase = ((size_t)r * c.Kmax + j) * c.Hq + (size_t)kvh * G;
   const float ln2 = 0.69314718055994531f;
+  // this split's partial (O, max, sum) for the cluster merge, after the
+  // in-CTA buffers
+  const bool cmerge = DQK == 128 && n_split == kAttnCluster;
+  float *Pm = Wt, *Pl = Pm + 16;
+  float *Po = reinterpret_cast<float *>(
+      (reinterpret_cast<uintptr_t>(Pl + 16) + 15) & ~static_cast<uintptr_t>(15));
   for (int idx = tid; idx < G * DV / 2; idx += kAttnThreads) {
     const int h = (2 * idx) / DV, d = (2 * idx) % DV;
     float M = -CUDART_INF_F;
@@ -440,6 +452,12 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
       const float inv = L > 0.f ? 1.f / L : 0.f;
       *reinterpret_cast<uint32_t *>(out + (qbase + h) * DV + d) = pack_bf16(a * inv, b * inv);
       if (lse && d == 0) lse[qbase + h] = L > 0.f ? (M + log2f(L)) * ln2 : -CUDART_INF_F;
+    } else if (cmerge) {
+      *reinterpret_cast<float2 *>(Po + (size_t)h * DV + d) = make_float2(a, b);
+      if (d == 0) {
+        Pm[h] = M;
+        Pl[h] = L;
+      }
     } else {
       float *po = c.part_o + ((qbase + h) * n_split + split) * DV + d;
       po[0] = a;
@@ -451,6 +469,41 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
     }
   }
   if (n_split == 1) return;
+
+  if (cmerge) {
+    // ---- the item's splits form a cluster: split q merges heads h = q
+    //      (mod kAttnCluster) from every split's shared memory
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();  // every split's partial is in its shared memory
+    for (int h0 = split; h0 < G; h0 += kAttnCluster) {
+      float wgt[kAttnCluster];
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int qs = 0; qs < kAttnCluster; ++qs) M = fmaxf(M, cl.map_shared_rank(Pm, qs)[h0]);
+      const float ref = M == -CUDART_INF_F ? 0.f : M;
+      float L = 0.f;
+#pragma unroll
+      for (int qs = 0; qs < kAttnCluster; ++qs) {
+        wgt[qs] = exp2f(cl.map_shared_rank(Pm, qs)[h0] - ref);
+        L += wgt[qs] * cl.map_shared_rank(Pl, qs)[h0];
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int d = 2 * tid; d < DV; d += 2 * kAttnThreads) {
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int qs = 0; qs < kAttnCluster; ++qs) {
+          const float2 v = *reinterpret_cast<const float2 *>(cl.map_shared_rank(Po, qs) + (size_t)h0 * DV + d);
+          a += wgt[qs] * v.x;
+          b += wgt[qs] * v.y;
+        }
+        *reinterpret_cast<uint32_t *>(out + (qbase + h0) * DV + d) = pack_bf16(a * inv, b * inv);
+      }
+      if (lse && tid == 0) lse[qbase + h0] = L > 0.f ? (M + log2f(L)) * ln2 : -CUDART_INF_F;
+    }
+    cl.sync();  // no split leaves while another reads its shared memory
+    return;
+  }
 
   // ---- the CTA that finishes an item last merges its splits
   const int item = ((r * c.Kmax + j) * c.Hkv) + kvh;
@@ -555,8 +608,27 @@ static cudaError_t launch_attn_t(const DevCtx &c, const uint16_t *q, const uint1
   if (e != cudaSuccess) return e;
   dim3 grid(n_split, c.Kmax, c.N * c.Hkv);
   if (tm) tm->begin(K_ATTN, s);
-  e = launch_pdl(k_attn<DQK, DV>, grid, dim3(kAttnThreads), smem, s, c, q, block, loc, out, lse,
-                 n_split, chunk, body, loc_off);
+  if (DQK == 128 && n_split == kAttnCluster) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = kAttnCluster;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, k_attn<DQK, DV>, c, q, block, loc, out, lse, n_split, chunk, body,
+                           loc_off);
+  } else {
+    e = launch_pdl(k_attn<DQK, DV>, grid, dim3(kAttnThreads), smem, s, c, q, block, loc, out,
+                   lse, n_split, chunk, body, loc_off);
+  }
   if (tm) tm->end(K_ATTN, s);
   return e;
 }
