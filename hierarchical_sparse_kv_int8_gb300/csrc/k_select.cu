@@ -44,14 +44,19 @@ constexpr int kScoreThreads = 256;
 constexpr int kDirectChunks = 8;  // rows up to 128 bytes use direct loads
 
 template <int NC>
-__device__ __forceinline__ void score_direct(const int8_t *__restrict__ krow, const uint4 *qs,
-                                             int Kr, int nc_rt, int (&acc)[kMaxKmax]) {
+__device__ __forceinline__ void load_direct(const int8_t *__restrict__ krow, int nc_rt,
+                                            uint4 (&kv)[kDirectChunks]) {
   const int nc = NC > 0 ? NC : nc_rt;
   const uint4 *p = reinterpret_cast<const uint4 *>(krow);
-  uint4 kv[kDirectChunks];
 #pragma unroll
   for (int ch = 0; ch < kDirectChunks; ++ch)
     if (ch < nc) kv[ch] = __ldg(p + ch);
+}
+
+template <int NC>
+__device__ __forceinline__ void score_direct(const uint4 (&kv)[kDirectChunks], const uint4 *qs,
+                                             int Kr, int nc_rt, int (&acc)[kMaxKmax]) {
+  const int nc = NC > 0 ? NC : nc_rt;
 #pragma unroll
   for (int ch = 0; ch < kDirectChunks; ++ch) {
     if (ch >= nc) break;
@@ -93,6 +98,10 @@ k_index_score(const DevCtx c, const int8_t *__restrict__ q_idx,
   const int RB = c.idx_row, nc = RB >> 4;
   const int rows = (int)(dom_r - row0 < kScoreThreads ? dom_r - row0 : kScoreThreads);
   const int8_t *keys = c.keys[r] + row0 * RB;
+  // the row's key chunks are requested first, so their latency overlaps the
+  // query copy below
+  uint4 kv[kDirectChunks];
+  if (threadIdx.x < rows) load_direct<NC>(keys + (size_t)threadIdx.x * RB, nc, kv);
   uint4 *qs = reinterpret_cast<uint4 *>(smem);
   const int8_t *qb = q_idx ? q_idx : reinterpret_cast<const int8_t *>(ctl.w + ctl_qidx_word(c.N, c.Kmax));
   const uint4 *qsrc = reinterpret_cast<const uint4 *>(qb + (size_t)r * c.Kmax * RB);
@@ -104,7 +113,7 @@ k_index_score(const DevCtx c, const int8_t *__restrict__ q_idx,
 #pragma unroll
   for (int j = 0; j < kMaxKmax; ++j) acc[j] = 0;
   if (t < rows) {
-    score_direct<NC>(keys + (size_t)t * RB, qs, Kr, nc, acc);
+    score_direct<NC>(kv, qs, Kr, nc, acc);
     const int64_t s = row0 + t;
 #pragma unroll
     for (int j = 0; j < kMaxKmax; ++j)
