@@ -7,7 +7,9 @@
 // Split-KV flash decoding.  One CTA of four warps handles one split (a range
 // of the row list) of one (request, query, kv head) item.  Rows are gathered
 // by location into shared memory with 16-byte cp.async, three stages in
-// flight, each tracked by an mbarrier.  The split's rows of the hot cache,
+// flight, each tracked by an mbarrier (rows of the context's pools arrive by
+// bulk asynchronous copies of the TMA engine, the caller's block rows by
+// cp.async).  The split's rows of the hot cache,
 // optional pool and draft ring, and its block rows, are attended first, while
 // the preceding gather may still be running; its staging rows follow once the
 // gather has finished.  The query heads that share the kv head (padded to 16) form the M
@@ -216,8 +218,10 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
   const int n_pre = nE > grp ? (nE - grp + SUB - 1) / SUB : 0;
   const int gtid = wi * 32 + lane;  // thread index within the group
   __shared__ __align__(8) uint64_t mbar[SUB][kAttnStages];
-  if (gtid == 0)
+  if (gtid == 0) {
     for (int s = 0; s < kAttnStages; ++s) mbar_init(&mbar[grp][s], NW * 32);
+    fence_proxy_async_smem();  // the bulk copies see the initialised barriers
+  }
   __syncthreads();
   // Copy one tile into its stage: lanes 0..15 of every warp decode one row's
   // source address (location tag, bounds check), the group's threads copy the
@@ -231,13 +235,16 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
     const int n_in = late_tile ? n_late : n_early;
     unsigned char *st = stage_base + (size_t)(it % kAttnStages) * kTileRows * stride;
     int *vf = vflag + (it % kAttnStages) * kTileRows;
+    uint64_t *bar = &mbar[grp][it % kAttnStages];
     const uint16_t *mysrc = nullptr;
+    bool pooled = false;  // a row of the context's pools (device memory)
     if (lane < kTileRows) {
       const int i = i0 + lane;
       if (i < n_in) {
         const int pos = lst[i], e = split + pos * n_split;
         if (e < k) {
           mysrc = loc_row(c, r, lsm[pos]);
+          pooled = mysrc != nullptr;
           if (mysrc == nullptr && wi == 0) record_error(c.err, DC_LOC_RANGE, K_ATTN);
         } else {
           mysrc = brow + (size_t)(e - k) * c.row;
@@ -245,8 +252,19 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
       }
       if (wi == 0) vf[lane] = mysrc != nullptr;
     }
+    // pool rows: one bulk asynchronous copy (TMA engine) per row, issued by
+    // the group's first warp and counted in bytes on the stage's barrier
+    const unsigned bulk_rows = __ballot_sync(0xffffffffu, pooled);
+    if (wi == 0 && bulk_rows) {
+      if (lane == 0) mbar_expect_tx(bar, (uint32_t)__popc(bulk_rows) * (uint32_t)rowb);
+      __syncwarp();
+      if (pooled) bulk_g2s(st + (size_t)lane * stride, mysrc, (uint32_t)rowb, bar);
+    }
+    // the caller's block rows (which may be page-locked host memory) and
+    // empty rows (zero-filled) by 16-byte cp.async
 #pragma unroll 4
     for (int rr = 0; rr < kTileRows; ++rr) {
+      if ((bulk_rows >> rr) & 1u) continue;
       const uint16_t *src = reinterpret_cast<const uint16_t *>(
           __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mysrc), rr));
       unsigned char *dst = st + (size_t)rr * stride;
@@ -254,7 +272,7 @@ k_attn(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restric
         cp_async_16_zfill(dst + v * 16, src ? (const void *)(src + v * 8) : (const void *)c.ring,
                           src ? 16 : 0);
     }
-    cp_async_arrive_noinc(&mbar[grp][it % kAttnStages]);
+    cp_async_arrive_noinc(bar);
   };
   auto wait_stage = [&](int it) {
     const uint32_t parity = (uint32_t)((it / kAttnStages) & 1);

@@ -115,6 +115,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(void *bar, uint32_t bytes)
                "r"(bytes)
                : "memory");
 }
+// Adds `bytes` to the transaction count the barrier's current phase waits for
+// (no arrival).
+__device__ __forceinline__ void mbar_expect_tx(void *bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
 // Makes initialised mbarriers visible to the asynchronous (bulk copy) proxy.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
