@@ -488,7 +488,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
       const int nbins = 1 << width;
       ++passes;
       nb_last = nbins;
-      cl.sync();  // every CTA has finished reading the previous histograms
+      if (passes > 1) cl.sync();  // every CTA has finished reading the previous histograms
       for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
       __syncthreads();
 #pragma unroll 4
