@@ -129,6 +129,22 @@ def _dptr(x) -> Optional[int]:
     return x.data_ptr()
 
 
+_ptr_memo: dict = {}
+
+
+def _host_ptr(a: np.ndarray) -> int:
+    """Address of a host array; remembered per array object, since asking
+    numpy for it costs about a microsecond per call."""
+    hit = _ptr_memo.get(id(a))
+    if hit is not None and hit[0] is a:
+        return hit[1]
+    ptr = a.ctypes.data
+    if len(_ptr_memo) > 64:
+        _ptr_memo.clear()
+    _ptr_memo[id(a)] = (a, ptr)
+    return ptr
+
+
 def _host_i32(x, n) -> np.ndarray:
     if isinstance(x, np.ndarray) and x.dtype == np.int32 and x.flags.c_contiguous:
         a = x
@@ -212,7 +228,7 @@ class Context:
         p = None
         if pos is not None:
             p = np.ascontiguousarray(np.asarray(pos, dtype=np.int64))
-        self._check(self._lib.dhs_select(self.h, _dptr(q_idx), kr.ctypes.data,
+        self._check(self._lib.dhs_select(self.h, _dptr(q_idx), _host_ptr(kr),
                                          None if p is None else p.ctypes.data, _dptr(topk_out),
                                          _stream(stream)), "dhs_select")
 
@@ -226,7 +242,7 @@ class Context:
 
     def commit(self, accepted_len, stream=None):
         a = _host_i32(accepted_len, self.cfg.n_slots)
-        self._check(self._lib.dhs_commit(self.h, a.ctypes.data, _stream(stream)), "dhs_commit")
+        self._check(self._lib.dhs_commit(self.h, _host_ptr(a), _stream(stream)), "dhs_commit")
 
     def set_residency(self, slot, rows, stream=None):
         rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
@@ -279,6 +295,6 @@ class Context:
     def round_host(self, q_idx, k_per_req, q, block_kv, accepted_len, out, lse=None, stream=None):
         kr = _host_i32(k_per_req, self.cfg.n_slots)
         a = _host_i32(accepted_len, self.cfg.n_slots)
-        self._check(self._lib.dhs_round_host(self.h, _dptr(q_idx), kr.ctypes.data, _dptr(q),
-                                             _dptr(block_kv), a.ctypes.data, _dptr(out),
+        self._check(self._lib.dhs_round_host(self.h, _dptr(q_idx), _host_ptr(kr), _dptr(q),
+                                             _dptr(block_kv), _host_ptr(a), _dptr(out),
                                              _dptr(lse), _stream(stream)), "dhs_round_host")

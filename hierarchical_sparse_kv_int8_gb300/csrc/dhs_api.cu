@@ -777,6 +777,18 @@ int dhs_round_host(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, co
   const DevCtx &d = c->d;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t nq = (size_t)d.N * d.Kmax;
+  // The indexer is launched first, so the GPU starts while the host prepares
+  // the rest.  Small index rows travel in its launch parameters, else
+  // through a device buffer.
+  const bool inline_q =
+      (size_t)ctl_qidx_word(d.N, d.Kmax) * 4 + nq * d.idx_row <= (size_t)kUploadWords * 4;
+  if (!inline_q &&
+      cudaMemcpyAsync(c->rh_qidx, q_idx, nq * d.idx_row, cudaMemcpyHostToDevice, s))
+    return DHS_ERR_CUDA;
+  int rc = inline_q ? select_impl(c, nullptr, q_idx, k_per_req, nullptr, c->rh_topk, stream)
+                    : dhs_select(c, c->rh_qidx, k_per_req, nullptr, c->rh_topk, stream);
+  if (!rc) rc = dhs_resolve(c, c->rh_topk, c->rh_loc, 1, stream);
+  if (rc) return rc;
   // Queries, block rows and outputs in page-locked host memory are used in
   // place: the attention kernel reads them and writes its results across the
   // host link (zero copy).  Other host memory goes through device buffers.
@@ -793,19 +805,8 @@ int dhs_round_host(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, co
       return DHS_ERR_CUDA;
     b_dev = c->rh_block;
   }
-  // small index rows travel in the indexer's launch parameters, else through
-  // a device buffer
-  const bool inline_q =
-      (size_t)ctl_qidx_word(d.N, d.Kmax) * 4 + nq * d.idx_row <= (size_t)kUploadWords * 4;
-  if (!inline_q &&
-      cudaMemcpyAsync(c->rh_qidx, q_idx, nq * d.idx_row, cudaMemcpyHostToDevice, s))
-    return DHS_ERR_CUDA;
-  int rc = inline_q ? select_impl(c, nullptr, q_idx, k_per_req, nullptr, c->rh_topk, stream)
-                    : dhs_select(c, c->rh_qidx, k_per_req, nullptr, c->rh_topk, stream);
-  if (!rc) rc = dhs_resolve(c, c->rh_topk, c->rh_loc, 1, stream);
-  if (!rc)
-    rc = dhs_attend(c, q_dev, b_dev, c->rh_loc, o_dev ? o_dev : c->rh_out,
-                    lse ? (l_dev ? l_dev : c->rh_lse) : nullptr, stream);
+  rc = dhs_attend(c, q_dev, b_dev, c->rh_loc, o_dev ? o_dev : c->rh_out,
+                  lse ? (l_dev ? l_dev : c->rh_lse) : nullptr, stream);
   if (!rc) rc = dhs_commit(c, accepted_len, stream);
   if (rc) return rc;
   if ((!o_dev &&
