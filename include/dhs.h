@@ -115,9 +115,9 @@ typedef struct {
  *   UNION    : each (request, kv head) streams the union U_r once and masks
  *              every score by the queries that selected the row; up to K_r
  *              times fewer row reads, best when the round is bound by HBM.
- *   AUTO     : UNION when the per-query pass would stream more than 128 MiB
- *              of rows per round (n_slots * k_max * (topk + k_max) rows), else
- *              PER_QUERY. */
+ *   AUTO     : UNION for 128-dim heads when the per-query pass would stream
+ *              more than 128 MiB of rows per round (n_slots * k_max *
+ *              (topk + k_max) rows), else PER_QUERY (always for latent rows). */
 enum { DHS_ATTN_AUTO = 0, DHS_ATTN_PER_QUERY = 1, DHS_ATTN_UNION = 2 };
 
 /* Cumulative counters since dhs_create (or dhs_reset_stats). */
