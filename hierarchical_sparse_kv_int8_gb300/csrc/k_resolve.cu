@@ -305,8 +305,8 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   __syncthreads();  // the slice's locations and first-selection slots are set
 
   // 4. one location per selected entry whose row lies in this slice (they
-  //    depend on the ranks only, so every CTA forms them before the leader's
-  //    victim choice)
+  //    depend on the ranks only; the slice-free leader skips this phase and
+  //    picks the victims meanwhile)
   int sel_here = 0, missel = 0;
   for (int e0 = crank == 0 ? nsel : tid; e0 < nsel; e0 += kBatch * bs) {
     int32_t sv[kBatch];
