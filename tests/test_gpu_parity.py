@@ -265,6 +265,18 @@ def test_cfg2_full(attn_pass):
     assert o.stats.hot_hits > 0 and o.stats.misses > 0
 
 
+# Sixteen query heads per kv head with the per-query pass split eight ways:
+# the splits of an item merge as one cluster, each CTA finishing two heads.
+CLUSTER16 = wl.Recipe("cluster_merge_16_heads", N=4, K=8, S=4096, H_idx=1, d_idx=64, topk=2048,
+                      Hq=16, Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=512,
+                      rho_within=0.8, rho_cross=0.8, W=64, p=8, seed=51)
+
+
+@pytest.mark.parametrize("shared", [True, False], ids=["shared", "per_query_retrieval"])
+def test_cluster_merged_splits_16_heads(shared):
+    _rounds(CLUSTER16, 2, shared=shared, attn_pass=PER_QUERY, label="cluster16")
+
+
 def _sampled(rec, slots, rounds=2, shared=True, k_max=None, opt_rows_max=None, kr=None,
              residency=None):
     run = _runner(rec, k_max=k_max, opt_rows_max=opt_rows_max)
