@@ -177,18 +177,18 @@ def test_index_scores_exact(rec):
     assert run.ctx.stats()["device_error"] == 0
 
 
-@pytest.mark.parametrize("d_idx", [64, 128], ids=["64B", "128B"])
-def test_index_scores_exact_large_launch(d_idx):
+@pytest.mark.parametrize("d_idx,N,S", [(64, 64, 65536), (128, 64, 32768)], ids=["64B", "128B"])
+def test_index_scores_exact_large_launch(d_idx, N, S):
     """64- and 128-byte index rows go to the tensor-core scorer once a launch
     streams 256 MB of keys or more: sampled requests' scores and top-k lists
     equal the oracle's."""
     from oracle.dhs_oracle import index_scores, topk_ordered
     import torch
-    S = 65536 if d_idx == 64 else 32768
-    rec = wl.Recipe("large_launch_%dB" % d_idx, N=64, K=4, S=S, H_idx=1, d_idx=d_idx, topk=256,
-                    Hq=8, Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=64, rho_within=0.5,
-                    rho_cross=0.6, W=16, p=8, seed=41, i8_lo=-128, i8_hi=127)
-    assert rec.N * rec.S * rec.idx_row >= 256 << 20
+    rec = wl.Recipe("large_launch_%dB_%d" % (d_idx, N), N=N, K=4, S=S, H_idx=1, d_idx=d_idx,
+                    topk=256, Hq=8, Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=64,
+                    rho_within=0.5, rho_cross=0.6, W=16, p=8, seed=41, i8_lo=-128, i8_hi=127)
+    key_bytes = rec.N * rec.S * rec.idx_row
+    assert key_bytes >= 256 << 20
     run = _runner(rec)
     run.load_round(0)
     kr = rec.k_per_req()
@@ -197,7 +197,7 @@ def test_index_scores_exact_large_launch(d_idx):
     sc = run.export("scores", torch.int32, (rec.N, run.Km, ss)).cpu().numpy()
     topk = run.topk.cpu().numpy()
     qi = rec.index_queries(0, 0, rec.N)
-    for r in (0, 37, 63):
+    for r in (0, N // 2 + 5, N - 1):
         keys = rec.index_keys(r, r + 1)[0]
         for j in range(int(kr[r])):
             want = index_scores(qi[r, j], keys, rec.S)
@@ -206,12 +206,13 @@ def test_index_scores_exact_large_launch(d_idx):
     assert run.ctx.stats()["device_error"] == 0
 
 
-def test_index_scores_extreme_values():
-    """The largest magnitudes a 512-byte row can produce: every product is
-    (-128)(-128) or (-128)(127), so the scores are +2^23 and -2^23 + 65536
-    exactly, every row ties, and each top-k is the lowest rows in order."""
+@pytest.mark.parametrize("rec", [TINY_TC512_FULL, TINY_GQA], ids=["512B", "64B"])
+def test_index_scores_extreme_values(rec):
+    """The largest magnitudes a row can produce: every product is
+    (-128)(-128) or (-128)(127), so the scores are 16384 and -16256 times the
+    row's bytes exactly (+2^23 and -2^23 + 65536 for 512 bytes), every row
+    ties, and each top-k is the lowest rows in order."""
     import torch
-    rec = TINY_TC512_FULL
     run = _runner(rec)
     run.load_round(0)
     run.keys.fill_(-128)
@@ -224,7 +225,7 @@ def test_index_scores_extreme_values():
     topk = run.topk.cpu().numpy()
     for r in range(rec.N):
         for j in range(int(kr[r])):
-            want = (1 << 23) if j % 2 == 0 else -(128 * 127 * 512)
+            want = 16384 * rec.idx_row if j % 2 == 0 else -(128 * 127 * rec.idx_row)
             assert (sc[r, j, :rec.S] == want).all(), "r=%d j=%d" % (r, j)
             assert np.array_equal(topk[r, j], np.arange(rec.topk)), "r=%d j=%d" % (r, j)
     assert run.ctx.stats()["device_error"] == 0
