@@ -413,8 +413,13 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
   const int crank = (int)cl.block_rank();
   const int prob = blockIdx.x / kTopkCluster;
   const int r = prob / c.Kmax, j = prob % c.Kmax;
-  if (j >= c.Kr[r]) return;  // the whole cluster leaves together
+  // the round's control values, requested together (all are in range
+  // whatever K_r is)
+  const int Kr = c.Kr[r];
   const int dom = c.dom[r * c.Kmax + j];
+  const int lo = c.minmax[(r * c.Kmax + j) * 2 + 0];
+  const int hi = c.minmax[(r * c.Kmax + j) * 2 + 1];
+  if (j >= Kr) return;  // the whole cluster leaves together
   const int k = c.k;
   const int32_t *__restrict__ sc = c.scores + ((size_t)r * c.Kmax + j) * c.Ss;
   int32_t *out = topk_out + ((size_t)r * c.Kmax + j) * k;
@@ -430,8 +435,6 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
   const int ksel = min(k, dom);
   const int part = (((dom + kTopkCluster - 1) / kTopkCluster) + 31) & ~31;
   const int p0 = min(dom, crank * part), p1 = min(dom, p0 + part);
-  const int lo = c.minmax[(r * c.Kmax + j) * 2 + 0];
-  const int hi = c.minmax[(r * c.Kmax + j) * 2 + 1];
   // This CTA's part of the scores, read by every pass below: when it fits
   // (stage_cap scores), one bulk asynchronous copy brings it into shared
   // memory first; otherwise the passes read global memory.
@@ -491,11 +494,28 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
       if (passes > 1) cl.sync();  // every CTA has finished reading the previous histograms
       for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
       __syncthreads();
+      if (passes == 1 && staged) {
+        // the first pass counts every row (v <= range < 2^(shift + width)),
+        // four staged scores per load
+        const int n = p1 - p0, n4 = n >> 2;
+        const int4 *s4 = reinterpret_cast<const int4 *>(stg);
+#pragma unroll 2
+        for (int i = tid; i < n4; i += kTopkThreads) {
+          const int4 x = s4[i];
+          atomicAdd(&hist[((uint32_t)(x.x - lo) >> shift) & (nbins - 1)], 1u);
+          atomicAdd(&hist[((uint32_t)(x.y - lo) >> shift) & (nbins - 1)], 1u);
+          atomicAdd(&hist[((uint32_t)(x.z - lo) >> shift) & (nbins - 1)], 1u);
+          atomicAdd(&hist[((uint32_t)(x.w - lo) >> shift) & (nbins - 1)], 1u);
+        }
+        for (int i = 4 * n4 + tid; i < n; i += kTopkThreads)
+          atomicAdd(&hist[((uint32_t)(stg[i] - lo) >> shift) & (nbins - 1)], 1u);
+      } else {
 #pragma unroll 4
-      for (int s = p0 + tid; s < p1; s += kTopkThreads) {
-        const uint32_t v = (uint32_t)(val(s) - lo);
-        if ((uint32_t)((unsigned long long)v >> (shift + width)) == prefix)
-          atomicAdd(&hist[(v >> shift) & (nbins - 1)], 1u);
+        for (int s = p0 + tid; s < p1; s += kTopkThreads) {
+          const uint32_t v = (uint32_t)(val(s) - lo);
+          if ((uint32_t)((unsigned long long)v >> (shift + width)) == prefix)
+            atomicAdd(&hist[(v >> shift) & (nbins - 1)], 1u);
+        }
       }
       // thread t owns a run of bins counted from the top; the runs' counts
       // in this CTA first, so that only runs at or above the threshold need
@@ -517,7 +537,66 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
       int total;
       const int above = block_excl_scan(local, warp_sums, total);
       const bool exact_pass = passes == 1 && shift == 0;
-      if (local > 0 && above < k_rem && (exact_pass || k_rem <= above + local)) {
+      // The thread whose run holds the threshold finds its bin; in the exact
+      // pass every run at or above the threshold in which this CTA has rows
+      // also needs base[b] = rows of the domain above offset value b plus
+      // rows equal to b in earlier CTAs, which decides the place of each of
+      // its winners.  Both need the cluster's count of each bin of the run.
+      const bool thr = local > 0 && above < k_rem && k_rem <= above + local;
+      const bool need_base = exact_pass && ccnt[tid] > 0 && above < k_rem;
+      int *base = reinterpret_cast<int *>(hist + (1 << kRadixBits));
+      // The runs at or above the threshold are the first nq threads' (above
+      // grows in thread order), so their bins form one window at the top.
+      // When it fits in the candidate area (free until the collection) it is
+      // gathered once, consecutive threads reading consecutive bins, as the
+      // cluster count G and the count in earlier CTAs P of every bin; else
+      // each run reads its own bins.
+      int *G = reinterpret_cast<int *>(cand), *P = G + kp;
+      int b_min = nbins;
+      bool win = false;
+      if (exact_pass) {
+        const int nq = __syncthreads_count(above < k_rem);
+        b_min = max(0, nbins - nq * per);
+        win = nbins - b_min <= kp;
+        if (win) {
+          for (int b = b_min + tid; b < nbins; b += kTopkThreads) {
+            int hv[kTopkCluster];
+#pragma unroll
+            for (int q = 0; q < kTopkCluster; ++q) hv[q] = (int)hr[q][b];
+            int g = 0, pc = 0;
+#pragma unroll
+            for (int q = 0; q < kTopkCluster; ++q) {
+              g += hv[q];
+              if (q < crank) pc += hv[q];
+            }
+            G[b - b_min] = g;
+            P[b - b_min] = pc;
+          }
+          __syncthreads();
+        }
+      }
+      if (win && (thr || need_base)) {
+        // (this thread's run lies in the window: it is one of the first nq)
+        if (thr) {
+          int acc = above;
+          for (int b = b_hi - 1; b >= b_lo; --b) {
+            const int g = G[b - b_min];
+            if (acc + g >= k_rem) {
+              sh_bin = b;
+              sh_above = acc;
+              break;
+            }
+            acc += g;
+          }
+        }
+        if (need_base) {
+          int acc = above;
+          for (int b = b_hi - 1; b >= b_lo; --b) {
+            base[b] = acc + P[b - b_min];
+            acc += G[b - b_min];
+          }
+        }
+      } else if (thr || need_base) {
         int gsum[kBinsPerThread], psum[kBinsPerThread];  // cluster count; count in earlier CTAs
 #pragma unroll
         for (int t = 0; t < kBinsPerThread; ++t) {
@@ -534,7 +613,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
           gsum[t] = g;
           psum[t] = pc;
         }
-        if (k_rem <= above + local) {
+        if (thr) {
           int acc = above;
 #pragma unroll
           for (int t = kBinsPerThread - 1; t >= 0; --t) {
@@ -548,11 +627,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
             acc += gsum[t];
           }
         }
-        if (exact_pass) {
-          // a single pass decides: base[b] = rows of the domain above offset
-          // value b plus rows equal to b in earlier CTAs, for the exact
-          // placement (needed for the bins above the threshold only)
-          int *base = reinterpret_cast<int *>(hist + (1 << kRadixBits));
+        if (need_base) {
           int acc = above;
 #pragma unroll
           for (int t = kBinsPerThread - 1; t >= 0; --t) {
@@ -573,29 +648,53 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
     const int c_gt = k - need;  // rows strictly above T
 
     // counts of this CTA's warps, then of the cluster's CTAs
-    const int run = ((((p1 - p0) + 31) / 32) + 31) & ~31;
+    // (runs of a multiple of 128 rows, so that the vector reads below stay
+    // inside the warp's own run)
+    const int run = ((((p1 - p0) + 31) / 32) + 127) & ~127;
     const int r0 = min(p1, p0 + wid * run), r1 = min(p1, r0 + run);
     const unsigned lt = (1u << lane) - 1u;
     // With staged scores and exact bins, the counting pass also compacts the
     // warp's winners, in row order, into the front of its own run of the
-    // stage (a write never lands beyond the row being read), packed as
+    // stage (a write never lands beyond the rows already read), packed as
     // (above T, value, row - p0); the collection then reads only these lists.
+    // Each lane reads four consecutive rows at a time; a group of 128 rows
+    // with no row at or above T costs one vote.
     const bool inplace = staged && passes <= 1;
     uint32_t *wl = reinterpret_cast<uint32_t *>(stg) + (r0 - p0);
     int ngt = 0, neq = 0, wcount = 0;
     if (inplace) {
-#pragma unroll 4
-      for (int base = r0; base < r1; base += 32) {
-        const int s = base + lane;
-        const bool ok = s < r1;
-        const uint32_t v = ok ? (uint32_t)(val(s) - lo) : 0u;
-        const bool gt = ok && v > T, eq = ok && v == T;
-        const unsigned bw = __ballot_sync(0xffffffffu, gt || eq);
-        if (gt || eq)
-          wl[wcount + __popc(bw & lt)] = (gt ? 0x80000000u : 0u) | (v << 17) | (uint32_t)(s - p0);
-        wcount += __popc(bw);
-        ngt += __popc(__ballot_sync(0xffffffffu, gt));
+      int gt_lane = 0;
+      for (int base = r0; base < r1; base += 128) {
+        const int s0 = base + 4 * lane;  // s0 - p0 is a multiple of 4
+        int4 x = make_int4(0, 0, 0, 0);
+        if (s0 < r1) x = *reinterpret_cast<const int4 *>(stg + (s0 - p0));
+        const uint32_t v[4] = {(uint32_t)(x.x - lo), (uint32_t)(x.y - lo), (uint32_t)(x.z - lo),
+                               (uint32_t)(x.w - lo)};
+        bool cnd[4];
+        int nc = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          cnd[i] = s0 + i < r1 && v[i] >= T;
+          nc += cnd[i];
+        }
+        if (!__any_sync(0xffffffffu, nc > 0)) continue;
+        int inc = nc;  // inclusive scan of the lanes' counts: row order
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += y;
+        }
+        int pos = wcount + inc - nc;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (!cnd[i]) continue;
+          const bool gt = v[i] > T;
+          gt_lane += gt;
+          wl[pos++] = (gt ? 0x80000000u : 0u) | (v[i] << 17) | (uint32_t)(s0 + i - p0);
+        }
+        wcount += __shfl_sync(0xffffffffu, inc, 31);
       }
+      ngt = (int)__reduce_add_sync(0xffffffffu, (unsigned)gt_lane);
       neq = wcount - ngt;
     } else {
 #pragma unroll 8
@@ -629,8 +728,12 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
     int eq_off = __shfl_sync(0xffffffffu, ex - weq[lane], wid);
     cl.sync();  // every CTA's totals are published
     empty_range();
-    int eq_base = 0;                       // rows equal to T in earlier CTAs
-    for (int q = 0; q < crank; ++q) eq_base += *cl.map_shared_rank(&sh_cta_eq, q);
+    int eq_base = 0;  // rows equal to T in earlier CTAs
+#pragma unroll
+    for (int q = 0; q < kTopkCluster; ++q) {
+      const int e = *cl.map_shared_rank(&sh_cta_eq, q);
+      if (q < crank) eq_base += e;
+    }
     cluster_arrive();  // this CTA's distributed reads are done; waited for before it leaves
     const int my_gt = sh_cta_gt, my_eq = sh_cta_eq;
     const int kept_eq = max(0, min(my_eq, need - eq_base));
