@@ -441,6 +441,11 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
   const bool staged = p1 - p0 <= stage_cap && dom > k;
   int32_t *stg = reinterpret_cast<int32_t *>(smem + (((size_t)kp * 8 + 15) & ~(size_t)15) +
                                              ((size_t)2 << kRadixBits) * 4);
+  // The first radix pass's histogram size (also computed by the pass loop).
+  const uint32_t range = (uint32_t)(hi - lo);
+  const int shift0 = range ? 32 - __clz((int)range) : 0;
+  const int nbins0 = shift0 > 0 ? 1 << min(kRadixBits, shift0) : 0;
+  const bool prezeroed = staged && p1 > p0 && dom > k;
   if (staged && p1 > p0) {
     __shared__ __align__(8) uint64_t sbar;
     if (tid == 0) {
@@ -450,16 +455,23 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
       mbar_arrive_expect_tx(&sbar, bytes);
       bulk_g2s(stg, sc + p0, bytes, &sbar);
     }
-    __syncthreads();
-    int spins = 0;
-    while (!mbar_try_wait(&sbar, 0u))
-      if (++spins > kTopkSpinLimit) {
-        record_error(c.err, DC_TIMEOUT, K_TOPK);
-        spins = 0;
-        while (!mbar_try_wait(&sbar, 0u) && ++spins <= kTopkSpinLimit) {
+    // the first pass's histogram is cleared while the copy is in flight
+    if (prezeroed)
+      for (int i = tid; i < nbins0; i += kTopkThreads) hist[i] = 0;
+    // one warp waits for the copy; the block barrier then releases the rest
+    if (wid == 0) {
+      __syncwarp();
+      int spins = 0;
+      while (!mbar_try_wait(&sbar, 0u))
+        if (++spins > kTopkSpinLimit) {
+          record_error(c.err, DC_TIMEOUT, K_TOPK);
+          spins = 0;
+          while (!mbar_try_wait(&sbar, 0u) && ++spins <= kTopkSpinLimit) {
+          }
+          break;
         }
-        break;
-      }
+    }
+    __syncthreads();
   }
   auto val = [&](int s) -> int32_t { return staged ? stg[s - p0] : sc[s]; };
   // Once every CTA of the cluster has read the range (after its first
@@ -477,8 +489,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
       cand[s - p0] = topk_key((uint32_t)(val(s) - lo), s);
     nloc = p1 - p0;
   } else {
-    const uint32_t range = (uint32_t)(hi - lo);
-    int shift = range ? 32 - __clz((int)range) : 0;
+    int shift = shift0;
     uint32_t prefix = 0;
     int k_rem = k;
     const uint32_t *hr[kTopkCluster];
@@ -492,7 +503,8 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
       ++passes;
       nb_last = nbins;
       if (passes > 1) cl.sync();  // every CTA has finished reading the previous histograms
-      for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
+      if (!(passes == 1 && prezeroed))
+        for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
       __syncthreads();
       if (passes == 1 && staged) {
         // the first pass counts every row (v <= range < 2^(shift + width)),
@@ -525,8 +537,22 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
       const int b_lo = max(0, b_hi - per);
       __syncthreads();  // this CTA's histogram is complete
       {
+        // (vector reads: a run of 2, 4 or 8 bins starts at a multiple of its
+        // length, and the histogram area is 16-byte aligned)
         int lc = 0;
-        for (int b = b_lo; b < b_hi; ++b) lc += (int)hist[b];
+        if (b_hi - b_lo == 8) {
+          const uint4 x = *reinterpret_cast<const uint4 *>(hist + b_lo);
+          const uint4 y = *reinterpret_cast<const uint4 *>(hist + b_lo + 4);
+          lc = (int)(x.x + x.y + x.z + x.w + y.x + y.y + y.z + y.w);
+        } else if (b_hi - b_lo == 4) {
+          const uint4 x = *reinterpret_cast<const uint4 *>(hist + b_lo);
+          lc = (int)(x.x + x.y + x.z + x.w);
+        } else if (b_hi - b_lo == 2) {
+          const uint2 x = *reinterpret_cast<const uint2 *>(hist + b_lo);
+          lc = (int)(x.x + x.y);
+        } else {
+          for (int b = b_lo; b < b_hi; ++b) lc += (int)hist[b];
+        }
         ccnt[tid] = lc;
       }
       cl.sync();  // all histograms of the cluster are complete
@@ -599,19 +625,34 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
       } else if (thr || need_base) {
         int gsum[kBinsPerThread], psum[kBinsPerThread];  // cluster count; count in earlier CTAs
 #pragma unroll
-        for (int t = 0; t < kBinsPerThread; ++t) {
-          const int b = b_lo + t;
-          int g = 0, pc = 0;
-          if (b < b_hi) {
+        for (int t = 0; t < kBinsPerThread; ++t) gsum[t] = psum[t] = 0;
+        auto add = [&](int t, uint32_t v, int q) {
+          gsum[t] += (int)v;
+          if (q < crank) psum[t] += (int)v;
+        };
+        if (b_hi - b_lo == 8) {  // vector reads, as for the run counts
 #pragma unroll
-            for (int q = 0; q < kTopkCluster; ++q) {
-              const int hv = (int)hr[q][b];
-              g += hv;
-              if (q < crank) pc += hv;
+          for (int q = 0; q < kTopkCluster; ++q) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(hr[q] + b_lo);
+            const uint4 y = *reinterpret_cast<const uint4 *>(hr[q] + b_lo + 4);
+            add(0, x.x, q); add(1, x.y, q); add(2, x.z, q); add(3, x.w, q);
+            add(4, y.x, q); add(5, y.y, q); add(6, y.z, q); add(7, y.w, q);
+          }
+        } else if (b_hi - b_lo == 4) {
+#pragma unroll
+          for (int q = 0; q < kTopkCluster; ++q) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(hr[q] + b_lo);
+            add(0, x.x, q); add(1, x.y, q); add(2, x.z, q); add(3, x.w, q);
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < kBinsPerThread; ++t) {
+            const int b = b_lo + t;
+            if (b < b_hi) {
+#pragma unroll
+              for (int q = 0; q < kTopkCluster; ++q) add(t, hr[q][b], q);
             }
           }
-          gsum[t] = g;
-          psum[t] = pc;
         }
         if (thr) {
           int acc = above;
@@ -678,13 +719,13 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
           nc += cnd[i];
         }
         if (!__any_sync(0xffffffffu, nc > 0)) continue;
-        int inc = nc;  // inclusive scan of the lanes' counts: row order
+        // row order: every candidate of the lanes below, then the lane's own
+        unsigned bal[4];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, inc, o);
-          if (lane >= o) inc += y;
-        }
-        int pos = wcount + inc - nc;
+        for (int i = 0; i < 4; ++i) bal[i] = __ballot_sync(0xffffffffu, cnd[i]);
+        int pos = wcount;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pos += __popc(bal[i] & lt);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           if (!cnd[i]) continue;
@@ -692,7 +733,8 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
           gt_lane += gt;
           wl[pos++] = (gt ? 0x80000000u : 0u) | (v[i] << 17) | (uint32_t)(s0 + i - p0);
         }
-        wcount += __shfl_sync(0xffffffffu, inc, 31);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) wcount += __popc(bal[i]);
       }
       ngt = (int)__reduce_add_sync(0xffffffffu, (unsigned)gt_lane);
       neq = wcount - ngt;
