@@ -100,7 +100,10 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int warp_sums[32];
   __shared__ int sh_cnt[6];  // ring, opt, hot hits, selections, miss selections, mask bits
-  __shared__ int sh_u, sh_m, sh_p;  // this CTA's union rows and misses; the leader's P
+  __shared__ int sh_p;  // the leader's P
+  // every CTA's union rows, misses and hot hits, written by that CTA into
+  // each CTA of the cluster before the first cluster barrier
+  __shared__ int cl_cnt[kUnionCluster][3];
   const int crank = (int)cl.block_rank();
   const int r = blockIdx.x / kUnionCluster;
   const int Kr = c.Kr[r];  // written two launches back (scoring)
@@ -108,6 +111,9 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
     pdl_wait();
     return;  // the whole cluster leaves together
   }
+  // (split cluster barrier: every CTA has started before any CTA writes
+  // into another's shared memory; the wait comes just before those writes)
+  cluster_arrive_relaxed();
   const int tid = threadIdx.x, bs = blockDim.x;
   const int64_t n = c.n[r];
   const int k = c.k, KK = c.Kmax * k, B = c.B;
@@ -259,23 +265,26 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   warp_add(&sh_cnt[2], hot_h);
   int Mc;
   const int m_local = ublock_excl_scan(misses_here, warp_sums, Mc);
-  if (tid == 0) {
-    sh_u = Uc;
-    sh_m = Mc;
+  cluster_wait();
+  if (tid < kUnionCluster) {  // (remote stores: no round trip; S1 orders them)
+    int *dst = cl.map_shared_rank(&cl_cnt[crank][0], tid);
+    dst[0] = Uc;
+    dst[1] = Mc;
+    dst[2] = sh_cnt[2];
   }
   cl.sync();  // S1: counts published, protected and stamped slots complete
 
   int u_base = 0, m_base = 0, U = 0, M = 0, hits = 0;
 #pragma unroll
   for (int qr = 0; qr < kUnionCluster; ++qr) {
-    const int uq = *cl.map_shared_rank(&sh_u, qr), mq = *cl.map_shared_rank(&sh_m, qr);
+    const int uq = cl_cnt[qr][0], mq = cl_cnt[qr][1];
     if (qr < crank) {
       u_base += uq;
       m_base += mq;
     }
     U += uq;
     M += mq;
-    if (crank == 0) hits += *cl.map_shared_rank(&sh_cnt[2], qr);
+    hits += cl_cnt[qr][2];
   }
   // the leader merges the protected and stamped slots of every slice
   if (crank == 0)

@@ -420,6 +420,9 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
   const int lo = c.minmax[(r * c.Kmax + j) * 2 + 0];
   const int hi = c.minmax[(r * c.Kmax + j) * 2 + 1];
   if (j >= Kr) return;  // the whole cluster leaves together
+  // (split cluster barrier: every CTA has started before any CTA writes into
+  // another's shared memory; the wait follows the staging copy)
+  cluster_arrive_relaxed();
   const int k = c.k;
   const int32_t *__restrict__ sc = c.scores + ((size_t)r * c.Kmax + j) * c.Ss;
   int32_t *out = topk_out + ((size_t)r * c.Kmax + j) * k;
@@ -430,6 +433,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
   __shared__ int warp_sums[32];
   __shared__ int wgt[32], weq[32];
   __shared__ int sh_bin, sh_above, sh_cta_gt, sh_cta_eq;
+  __shared__ int tot_eq[kTopkCluster];  // every CTA's rows equal to T, pushed by that CTA
   __shared__ int ccnt[kTopkThreads];  // per-thread run counts of a radix pass
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int ksel = min(k, dom);
@@ -473,6 +477,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
     }
     __syncthreads();
   }
+  cluster_wait();
   auto val = [&](int s) -> int32_t { return staged ? stg[s - p0] : sc[s]; };
   // Once every CTA of the cluster has read the range (after its first
   // cluster barrier), the leader empties it for the next round's scores.
@@ -492,6 +497,7 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
     int shift = shift0;
     uint32_t prefix = 0;
     int k_rem = k;
+    int *rcnt = reinterpret_cast<int *>(hist) + (2 << kRadixBits) - kTopkCluster * kTopkThreads;
     const uint32_t *hr[kTopkCluster];
 #pragma unroll
     for (int q = 0; q < kTopkCluster; ++q) hr[q] = cl.map_shared_rank(hist, q);
@@ -554,11 +560,17 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
           for (int b = b_lo; b < b_hi; ++b) lc += (int)hist[b];
         }
         ccnt[tid] = lc;
+        // and into every CTA's copy of the cluster's run counts (remote
+        // stores, ordered by the barrier below; the copies sit at the top of
+        // the base area, which is written only after they are read)
+#pragma unroll
+        for (int q = 0; q < kTopkCluster; ++q)
+          *cl.map_shared_rank(rcnt + crank * kTopkThreads + tid, q) = lc;
       }
-      cl.sync();  // all histograms of the cluster are complete
+      cl.sync();  // all histograms and run counts of the cluster are complete
       int local = 0;  // the run's count in the cluster
 #pragma unroll
-      for (int q = 0; q < kTopkCluster; ++q) local += *cl.map_shared_rank(&ccnt[tid], q);
+      for (int q = 0; q < kTopkCluster; ++q) local += rcnt[q * kTopkThreads + tid];
       // an exclusive scan in thread order counts the rows above each run
       int total;
       const int above = block_excl_scan(local, warp_sums, total);
@@ -765,6 +777,8 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
     if (tid == 31) {
       sh_cta_gt = gx;
       sh_cta_eq = ex;
+#pragma unroll
+      for (int q = 0; q < kTopkCluster; ++q) *cl.map_shared_rank(&tot_eq[crank], q) = ex;
     }
     int gt_off = __shfl_sync(0xffffffffu, gx - wgt[lane], wid);   // within this CTA
     int eq_off = __shfl_sync(0xffffffffu, ex - weq[lane], wid);
@@ -772,10 +786,8 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
     empty_range();
     int eq_base = 0;  // rows equal to T in earlier CTAs
 #pragma unroll
-    for (int q = 0; q < kTopkCluster; ++q) {
-      const int e = *cl.map_shared_rank(&sh_cta_eq, q);
-      if (q < crank) eq_base += e;
-    }
+    for (int q = 0; q < kTopkCluster; ++q)
+      if (q < crank) eq_base += tot_eq[q];
     cluster_arrive();  // this CTA's distributed reads are done; waited for before it leaves
     const int my_gt = sh_cta_gt, my_eq = sh_cta_eq;
     const int kept_eq = max(0, min(my_eq, need - eq_base));
@@ -1264,7 +1276,19 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, const int8_t *q_
   const int part = ((max(max_dom, 1) + kTopkCluster - 1) / kTopkCluster + 31) & ~31;
   int stage_cap = 0;
   // (the in-place winner lists pack a row's place in the part into 17 bits)
-  if (smem_topk + 8 + (size_t)part * 4 <= kMaxDynSmem && part <= (1 << 17)) {
+  // the dynamic shared memory a top-k CTA may take beside its static arrays
+  static size_t topk_dyn_max = 0;
+  if (!topk_dyn_max) {
+    int dev = 0, optin = 0;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k_topk);
+    if (e != cudaSuccess) return e;
+    topk_dyn_max = std::min(kMaxDynSmem, (size_t)optin - fa.sharedSizeBytes);
+  }
+  if (smem_topk + 8 + (size_t)part * 4 <= topk_dyn_max && part <= (1 << 17)) {
     stage_cap = part;
     smem_topk = (((size_t)kp * 8 + 15) & ~(size_t)15) + ((size_t)2 << kRadixBits) * 4 +
                 (size_t)part * 4;

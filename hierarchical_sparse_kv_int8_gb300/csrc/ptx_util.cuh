@@ -145,6 +145,12 @@ __device__ __forceinline__ void cluster_arrive() {
   __syncwarp();
   asm volatile("barrier.cluster.arrive.release;\n" ::: "memory");
 }
+// Arrive without ordering any memory operation: only that the CTA has
+// started (before another CTA writes into its shared memory).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.relaxed;\n" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() {
   __syncwarp();
   asm volatile("barrier.cluster.wait.acquire;\n" ::: "memory");
