@@ -479,6 +479,12 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
   }
   cluster_wait();
   auto val = [&](int s) -> int32_t { return staged ? stg[s - p0] : sc[s]; };
+  // the scores of rows s0..s0+3, s0 - p0 a multiple of 4 (16-byte aligned in
+  // the stage and in the padded score row; the caller masks rows past its end)
+  auto val4 = [&](int s0) -> int4 {
+    return staged ? *reinterpret_cast<const int4 *>(stg + (s0 - p0))
+                  : __ldg(reinterpret_cast<const int4 *>(sc + s0));
+  };
   // Once every CTA of the cluster has read the range (after its first
   // cluster barrier), the leader empties it for the next round's scores.
   auto empty_range = [&]() {
@@ -527,6 +533,28 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
         }
         for (int i = 4 * n4 + tid; i < n; i += kTopkThreads)
           atomicAdd(&hist[((uint32_t)(stg[i] - lo) >> shift) & (nbins - 1)], 1u);
+      } else if (passes == 1) {
+        // likewise from global memory, four batches of four scores per
+        // thread in flight
+        const int n = p1 - p0, n4 = n >> 2;
+        for (int i0 = tid; i0 < n4; i0 += 4 * kTopkThreads) {
+          int4 x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kTopkThreads;
+            if (i < n4) x[u] = val4(p0 + 4 * i);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (i0 + u * kTopkThreads >= n4) continue;
+            atomicAdd(&hist[((uint32_t)(x[u].x - lo) >> shift) & (nbins - 1)], 1u);
+            atomicAdd(&hist[((uint32_t)(x[u].y - lo) >> shift) & (nbins - 1)], 1u);
+            atomicAdd(&hist[((uint32_t)(x[u].z - lo) >> shift) & (nbins - 1)], 1u);
+            atomicAdd(&hist[((uint32_t)(x[u].w - lo) >> shift) & (nbins - 1)], 1u);
+          }
+        }
+        for (int s = p0 + 4 * n4 + tid; s < p1; s += kTopkThreads)
+          atomicAdd(&hist[((uint32_t)(val(s) - lo) >> shift) & (nbins - 1)], 1u);
       } else {
 #pragma unroll 4
         for (int s = p0 + tid; s < p1; s += kTopkThreads) {
@@ -751,14 +779,24 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
       ngt = (int)__reduce_add_sync(0xffffffffu, (unsigned)gt_lane);
       neq = wcount - ngt;
     } else {
-#pragma unroll 8
-      for (int base = r0; base < r1; base += 32) {
-        const int s = base + lane;
-        const bool ok = s < r1;
-        const uint32_t v = ok ? (uint32_t)(val(s) - lo) : 0u;
-        ngt += __popc(__ballot_sync(0xffffffffu, ok && v > T));
-        neq += __popc(__ballot_sync(0xffffffffu, ok && v == T));
+      // four rows per lane and load; per-lane counts, summed once
+      int gt_lane = 0, eq_lane = 0;
+#pragma unroll 2
+      for (int base = r0; base < r1; base += 128) {
+        const int s0 = base + 4 * lane;
+        if (s0 >= r1) continue;
+        const int4 x = val4(s0);
+        const uint32_t v[4] = {(uint32_t)(x.x - lo), (uint32_t)(x.y - lo), (uint32_t)(x.z - lo),
+                               (uint32_t)(x.w - lo)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const bool ok = s0 + i < r1;
+          gt_lane += ok && v[i] > T;
+          eq_lane += ok && v[i] == T;
+        }
       }
+      ngt = (int)__reduce_add_sync(0xffffffffu, (unsigned)gt_lane);
+      neq = (int)__reduce_add_sync(0xffffffffu, (unsigned)eq_lane);
     }
     if (lane == 0) {
       wgt[wid] = ngt;
@@ -817,25 +855,48 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
         eq_off += __popc(beq);
       }
     }
-#pragma unroll 4
+    // (four rows per lane and load, in row order: lanes first, then the
+    // lane's own rows)
     for (int bs = r0; !inplace && bs < r1 &&
                       (gt_off < gt_end || (eq_off < eq_end && eq_off < kept_eq));
-         bs += 32) {
-      const int s = bs + lane;
-      const bool ok = s < r1;
-      const uint32_t v = ok ? (uint32_t)(val(s) - lo) : 0u;
-      const unsigned bgt = __ballot_sync(0xffffffffu, ok && v > T);
-      const unsigned beq = __ballot_sync(0xffffffffu, ok && v == T);
-      if (ok && v > T) cand[gt_off + __popc(bgt & lt)] = topk_key(v, s);
-      if (ok && v == T) {
-        const int rr = eq_off + __popc(beq & lt);  // rank among this CTA's ties
-        if (rr < kept_eq) {
-          if (exact) out[c_gt + eq_base + rr] = s;
-          else cand[my_gt + rr] = topk_key(v, s);
+         bs += 128) {
+      const int s0 = bs + 4 * lane;
+      int4 x = make_int4(0, 0, 0, 0);
+      if (s0 < r1) x = val4(s0);
+      const uint32_t v[4] = {(uint32_t)(x.x - lo), (uint32_t)(x.y - lo), (uint32_t)(x.z - lo),
+                             (uint32_t)(x.w - lo)};
+      bool gt[4], eq[4];
+      unsigned bg[4], be[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool ok = s0 + i < r1;
+        gt[i] = ok && v[i] > T;
+        eq[i] = ok && v[i] == T;
+        bg[i] = __ballot_sync(0xffffffffu, gt[i]);
+        be[i] = __ballot_sync(0xffffffffu, eq[i]);
+      }
+      int pg = gt_off, pe = eq_off;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        pg += __popc(bg[i] & lt);
+        pe += __popc(be[i] & lt);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (gt[i]) cand[pg++] = topk_key(v[i], s0 + i);
+        if (eq[i]) {
+          const int rr = pe++;  // rank among this CTA's ties
+          if (rr < kept_eq) {
+            if (exact) out[c_gt + eq_base + rr] = s0 + i;
+            else cand[my_gt + rr] = topk_key(v[i], s0 + i);
+          }
         }
       }
-      gt_off += __popc(bgt);
-      eq_off += __popc(beq);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        gt_off += __popc(bg[i]);
+        eq_off += __popc(be[i]);
+      }
     }
     if (exact) {
       // This CTA's winners above T, one thread each: a winner of value v takes

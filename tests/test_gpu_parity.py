@@ -206,6 +206,31 @@ def test_index_scores_exact_large_launch(d_idx, N, S):
     assert run.ctx.stats()["device_error"] == 0
 
 
+@pytest.mark.parametrize("full_range", [False, True], ids=["one_pass", "multi_pass"])
+def test_topk_parts_read_from_global_memory(full_range):
+    """Domains whose quarter no longer fits in a top-k CTA's shared memory
+    (here 40 000 scores per CTA) are read from global memory by every pass;
+    with full-range int8 the scores span more than 2^13 values and the radix
+    select takes several passes.  Every top-k list equals the oracle's."""
+    from oracle.dhs_oracle import index_scores, topk_ordered
+    kw = dict(i8_lo=-128, i8_hi=127) if full_range else {}
+    rec = wl.Recipe("unstaged_%s" % ("multi" if full_range else "one"), N=2, K=2, S=160000,
+                    H_idx=1, d_idx=128, topk=256, Hq=8, Hkv=1, qk_dim=128, v_dim=128,
+                    kv_layout=0, B=64, rho_within=0.5, rho_cross=0.6, W=16, p=8, seed=43, **kw)
+    run = _runner(rec)
+    run.load_round(0)
+    kr = rec.k_per_req()
+    run.select(kr)
+    topk = run.topk.cpu().numpy()
+    qi = rec.index_queries(0, 0, rec.N)
+    keys = rec.index_keys(0, rec.N)
+    for r in range(rec.N):
+        for j in range(int(kr[r])):
+            want = index_scores(qi[r, j], keys[r], rec.S)
+            assert np.array_equal(topk[r, j], topk_ordered(want, rec.topk)), "r=%d j=%d" % (r, j)
+    assert run.ctx.stats()["device_error"] == 0
+
+
 @pytest.mark.parametrize("rec", [TINY_TC512_FULL, TINY_GQA], ids=["512B", "64B"])
 def test_index_scores_extreme_values(rec):
     """The largest magnitudes a row can produce: every product is
