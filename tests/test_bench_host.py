@@ -1,0 +1,76 @@
+"""Host-side logic of bench.py, on the CPU: the algorithmic bytes behind the
+roofline figures, the rule that ncu traffic is reported only for the kernel
+sources it was captured from, and the reference arm's JSON line."""
+import json
+import types
+
+import numpy as np
+
+import bench
+import workload as wl
+
+
+def test_algorithmic_bytes_of_the_benchmark_workload():
+    """Byte counts written out from the workload's shapes (8 requests, K = 4,
+    S = 32768, 64-byte index rows, top-k 2048, 512-byte K+V rows, 8 query
+    heads of 128 dims) with per-request union / miss counts of 3745 / 1271."""
+    rec = wl.CONFIGS["cfg2"]
+    counts = np.array([[3745, 1271, 1271, 2474]] * 8, np.int64)
+    ab = bench.algorithmic_bytes(rec, counts, rec.k_per_req())
+    keys = 8 * 32768 * 64
+    queries = 8 * 4 * 64
+    lists = 4 * 8 * 4 * 2048
+    U, M = 8 * 3745, 8 * 1271
+    assert ab["select"] == keys + queries + lists == 17_041_408
+    kb = ab["kernel_bytes"]
+    assert kb["index_score"] == keys + queries
+    assert kb["topk"] == 4 * 8 * 4 * 32768 + lists
+    assert kb["gather"] == ab["gather"] == M * 512 == 5_206_016
+    assert kb["union_probe"] == 2 * lists + 8 * U + 4 * (U + M)
+    qo = 2 * 8 * 4 * 8 * (128 + 128)
+    assert kb["attn"] == U * 512 + 2 * 32 * 512 + qo + lists
+    assert ab["union"] == U and ab["misses"] == M
+
+
+def test_idle_requests_do_not_count():
+    rec = wl.CONFIGS["cfg2"]
+    kr = rec.k_per_req().copy()
+    kr[3] = 0
+    counts = np.zeros((8, 4), np.int64)
+    ab = bench.algorithmic_bytes(rec, counts, kr)
+    assert ab["select"] == 7 * 32768 * 64 + 7 * 4 * 64 + 4 * 7 * 4 * 2048
+
+
+def test_ncu_traffic_only_for_matching_sources(tmp_path, monkeypatch):
+    summary = tmp_path / "summary.md"
+    body = ("# capture\n\n`csrc-sha256: %s`\n\n## k_topk\n- duration: 14.9 us\n"
+            "- DRAM read: 4.261888 Mbyte\n- DRAM write: 0.5 Kbyte\n\n"
+            "## k_gather<1>\n- DRAM read: 0.531712 Mbyte\n- DRAM write: 5.888 Kbyte\n")
+    monkeypatch.setattr(bench, "NCU_SUMMARY", str(summary))
+    assert bench.ncu_traffic("topk") is None  # no summary at all
+    summary.write_text(body % bench.csrc_hash())
+    assert bench.ncu_traffic("topk") == 4_261_888 + 500
+    assert bench.ncu_traffic("gather") == 531_712 + 5_888
+    assert bench.ncu_traffic("commit") is None  # no section for it
+    summary.write_text(body % "0123456789abcdef")
+    assert bench.ncu_traffic("topk") is None  # sources changed since the capture
+
+
+def test_csrc_hash_is_stable():
+    h = bench.csrc_hash()
+    assert h == bench.csrc_hash() and len(h) == 16
+    int(h, 16)
+
+
+def test_reference_arm_line(capsys):
+    """The reference arm times the oracle on one request's round per step and
+    prints the contract's line with impl = reference."""
+    args = types.SimpleNamespace(workload="cfg1", steps=1, warmup=0, batch=0)
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["unit"] == "query-tokens/s" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["steps"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["config"]["workload"] == wl.CONFIGS["cfg1"].name
