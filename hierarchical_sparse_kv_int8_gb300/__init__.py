@@ -70,6 +70,18 @@ _SIGS = {
     "dhs_commit": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "dhs_set_residency": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                            ctypes.c_void_p], ctypes.c_int),
+    "dhs_policy_create": ([ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(ctypes.c_void_p)],
+                          ctypes.c_int),
+    "dhs_policy_destroy": ([ctypes.c_void_p], None),
+    "dhs_policy_admit": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                          ctypes.c_void_p], ctypes.c_int),
+    "dhs_policy_complete": ([ctypes.c_void_p, ctypes.c_int32], ctypes.c_int),
+    "dhs_policy_repopulate": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                              ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
+    "dhs_policy_query": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                         ctypes.c_void_p], ctypes.c_int),
+    "dhs_policy_free_pages": ([ctypes.c_void_p], ctypes.c_int64),
     "dhs_get_stats": ([ctypes.c_void_p, ctypes.POINTER(Stats), ctypes.c_void_p], ctypes.c_int),
     "dhs_reset_stats": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "dhs_buffer_bytes": ([ctypes.c_void_p, ctypes.c_int32], ctypes.c_int64),
@@ -182,6 +194,68 @@ def make_config(**kw) -> Config:
     for name, _ in Config._fields_:
         setattr(c, name, kw.get(name, 0))
     return c
+
+
+class Policy:
+    """Residency policy of optional history (dhs_policy_*): page accounting
+    on the host, no device.  admit() returns (admitted, optional_pages,
+    reclaimed request ids); repopulate() returns [(request, pages added)]."""
+
+    def __init__(self, total_pages: int, reserve_pages: int = 0):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        rc = self._lib.dhs_policy_create(int(total_pages), int(reserve_pages), ctypes.byref(h))
+        if rc:
+            raise DhsError(rc, "dhs_policy_create")
+        self.h = h.value
+        self.requests = []  # admitted ids, admission order (sizes the output arrays)
+
+    def close(self):
+        if getattr(self, "h", None):
+            self._lib.dhs_policy_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        self.close()
+
+    def _check(self, rc, what):
+        if rc:
+            raise DhsError(rc, what)
+
+    def admit(self, request: int, required_pages: int, history_pages: int):
+        cap = max(1, len(self.requests))
+        rec = np.zeros(cap, np.int32)
+        ok, opt, n = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int32()
+        self._check(self._lib.dhs_policy_admit(self.h, int(request), int(required_pages),
+                                               int(history_pages), ctypes.byref(ok),
+                                               ctypes.byref(opt), rec.ctypes.data, cap,
+                                               ctypes.byref(n)), "dhs_policy_admit")
+        if ok.value:
+            self.requests.append(int(request))
+        return bool(ok.value), int(opt.value), [int(x) for x in rec[:n.value]]
+
+    def complete(self, request: int):
+        self._check(self._lib.dhs_policy_complete(self.h, int(request)), "dhs_policy_complete")
+        self.requests.remove(int(request))
+
+    def repopulate(self, max_pages: int):
+        cap = max(1, len(self.requests))
+        req, pg = np.zeros(cap, np.int32), np.zeros(cap, np.int64)
+        n = ctypes.c_int32()
+        self._check(self._lib.dhs_policy_repopulate(self.h, int(max_pages), req.ctypes.data,
+                                                    pg.ctypes.data, cap, ctypes.byref(n)),
+                    "dhs_policy_repopulate")
+        return [(int(req[i]), int(pg[i])) for i in range(n.value)]
+
+    def query(self, request: int):
+        r, o, h = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        self._check(self._lib.dhs_policy_query(self.h, int(request), ctypes.byref(r),
+                                               ctypes.byref(o), ctypes.byref(h)),
+                    "dhs_policy_query")
+        return int(r.value), int(o.value), int(h.value)
+
+    def free_pages(self) -> int:
+        return int(self._lib.dhs_policy_free_pages(self.h))
 
 
 class Context:

@@ -335,6 +335,62 @@ int dhs_select_noalloc(const int8_t *q_idx, const int8_t *keys, int32_t n_querie
 /* Text of the CUDA runtime error behind the context's last DHS_ERR_CUDA ("" if none). */
 const char *dhs_last_error(const dhs_ctx *ctx);
 
+/* ------------------------------------------------------------------------
+ * Residency policy, [ADHS] 3.1, eq. (3) and (4): the host-side page accounting
+ * that decides how much optional history each admitted request holds.  Pure
+ * host logic (no CUDA call, no device); the caller carries its decisions out
+ * with dhs_set_residency.  Units are pages (the workloads use 64-row pages).
+ *
+ * Budget, eq. (3): required pages (hot cache and tail, never lent) + optional
+ * pages + reserve <= total, after every call.  The reclaim order is the
+ * admission order, oldest first.  Not thread-safe: one caller per policy. */
+typedef struct dhs_policy dhs_policy;
+
+/* total_pages >= reserve_pages >= 0.  DHS_ERR_INVALID otherwise; DHS_ERR_OOM. */
+int dhs_policy_create(int64_t total_pages, int64_t reserve_pages, dhs_policy **out);
+void dhs_policy_destroy(dhs_policy *p); /* NULL is a no-op */
+
+/* Admit `request` (an id not admitted now) with `required_pages` and
+ * `history_pages` of imported history it could hold as optional pages.
+ * When the free pages cover the required ones it is admitted and keeps
+ * min(history, free - required) optional pages (resident-first admission).
+ * Otherwise, with deficit D = required - free, the shortest prefix of the
+ * reclaim order whose optional pages sum to at least D loses all of them,
+ * eq. (4); those of its requests that held pages are written to reclaimed[]
+ * (host int32, n_reclaimed of them), and the new request keeps
+ * min(history, freed + free - required) optional pages.  If all optional
+ * pages together cannot cover D, the admission waits: *admitted = 0 and
+ * nothing changes.  The caller backs up a reclaimed request's history rows
+ * and retires its optional rows (dhs_set_residency with no rows) before the
+ * new request's pages are written.  DHS_ERR_INVALID for a bad argument or an
+ * id already admitted; DHS_ERR_CAPACITY if more than reclaimed_cap requests
+ * would lose pages (nothing changes). */
+int dhs_policy_admit(dhs_policy *p, int32_t request, int64_t required_pages,
+                     int64_t history_pages, int32_t *admitted, int64_t *optional_pages,
+                     int32_t *reclaimed, int32_t reclaimed_cap, int32_t *n_reclaimed);
+
+/* Completion releases the request's required and optional pages.
+ * DHS_ERR_INVALID if it is not admitted. */
+int dhs_policy_complete(dhs_policy *p, int32_t request);
+
+/* One bounded round-robin repopulation attempt: starting after the request
+ * the previous attempt served last, admitted requests (admission order,
+ * cyclically, each visited once) get optional pages up to their history, in
+ * total at most min(max_pages, free pages).  Writes (requests[i], pages[i]),
+ * i < *n_out, the pages added per request; the caller copies those rows and
+ * publishes them ready after the copy (dhs_set_residency).  cap must be at
+ * least the number of admitted requests (DHS_ERR_CAPACITY, nothing changes). */
+int dhs_policy_repopulate(dhs_policy *p, int64_t max_pages, int32_t *requests, int64_t *pages,
+                          int32_t cap, int32_t *n_out);
+
+/* The request's required, optional and history pages; DHS_ERR_INVALID if it
+ * is not admitted. */
+int dhs_policy_query(const dhs_policy *p, int32_t request, int64_t *required_pages,
+                     int64_t *optional_pages, int64_t *history_pages);
+
+/* total - reserve - required - optional pages; -1 for NULL. */
+int64_t dhs_policy_free_pages(const dhs_policy *p);
+
 #ifdef __cplusplus
 }
 #endif

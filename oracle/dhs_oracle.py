@@ -25,6 +25,10 @@ other than this file):
                                            (a library routine), closed forms
   commit / rollback                        Fig. 3 example, stage-K-then-commit-a
                                            equals stage-a-then-commit-a
+  residency policy                         eq. (4) against numpy searchsorted over
+                                           the cumulative pages, a hand-worked
+                                           trace (tests/golden), eq. (3) and the
+                                           reclaim invariants on random sequences
   LRU replacement                          invariants of [ADHS] 3.2 and one
                                            hand-worked trace.  Beyond those the
                                            replacement order (one clock tick per
@@ -482,3 +486,84 @@ class Oracle:
         c, q = self.cfg, self.req[r]
         lo = max(q.ring_first, q.n - c.ring_window)
         return {t: q.ring[t % c.R_d].copy() for t in range(lo, q.n)}
+
+
+# ---------------------------------------------------------------------------
+# Residency policy of optional history, [ADHS] 3.1, eq. (3) and (4)
+# ---------------------------------------------------------------------------
+def reclaim_prefix(a: List[int], delta: int) -> Optional[int]:
+    """Eq. (4): the least q with a_1 + ... + a_q >= delta, walking the reclaim
+    order; None when even all of them fall short (the admission waits)."""
+    if delta <= 0:
+        return 0
+    s = 0
+    for q, pages in enumerate(a, start=1):
+        s += pages
+        if s >= delta:
+            return q
+    return None
+
+
+class ResidencyPolicy:
+    """Page accounting of [ADHS] 3.1 under the budget of eq. (3):
+    required + optional + reserve <= total.  Readings where the section
+    leaves a choice: the reclaim order is the admission order; an admitted
+    request keeps min(history, free pages) optional pages (resident-first
+    admission; after a reclaim the new request takes the freed pages); a
+    repopulation attempt walks the admitted requests cyclically from just
+    after the last one the previous attempt served, giving each up to its
+    unmet history until the attempt's bound or the free pages run out."""
+
+    def __init__(self, total: int, reserve: int):
+        self.total, self.reserve = total, reserve
+        self.reqs: List[dict] = []  # admission order
+        self.cursor = 0
+
+    def free(self) -> int:
+        return self.total - self.reserve - sum(r["required"] + r["optional"] for r in self.reqs)
+
+    def admit(self, rid: int, required: int, history: int):
+        free = self.free()
+        freed, reclaimed = 0, []
+        if required > free:
+            q = reclaim_prefix([r["optional"] for r in self.reqs], required - free)
+            if q is None:
+                return False, 0, []
+            for r in self.reqs[:q]:
+                if r["optional"] > 0:
+                    reclaimed.append(r["id"])
+                    freed += r["optional"]
+                    r["optional"] = 0
+        opt = min(history, free + freed - required)
+        self.reqs.append(dict(id=rid, required=required, history=history, optional=opt))
+        return True, opt, reclaimed
+
+    def complete(self, rid: int):
+        i = [r["id"] for r in self.reqs].index(rid)
+        del self.reqs[i]
+        if i < self.cursor:
+            self.cursor -= 1
+        if self.cursor >= len(self.reqs):
+            self.cursor = 0
+
+    def repopulate(self, max_pages: int):
+        budget = min(max_pages, self.free())
+        n, out, nxt = len(self.reqs), [], self.cursor
+        for k in range(n):
+            if budget <= 0:
+                break
+            i = (self.cursor + k) % n
+            r = self.reqs[i]
+            give = min(r["history"] - r["optional"], budget)
+            if give <= 0:
+                continue
+            r["optional"] += give
+            budget -= give
+            out.append((r["id"], give))
+            nxt = (i + 1) % n
+        self.cursor = nxt
+        return out
+
+    def query(self, rid: int):
+        r = next(x for x in self.reqs if x["id"] == rid)
+        return r["required"], r["optional"], r["history"]
