@@ -7,7 +7,8 @@ import os
 import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-CSRC = os.path.join(HERE, "csrc")
+CSRC = os.path.join(HERE, "csrc")  # CUDA kernels and the C ABI
+HOST = os.path.join(HERE, "host")  # host-only runtime parts (plain C++, no CUDA call)
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdhs.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -23,7 +24,7 @@ def _nvcc() -> str:
 
 
 def sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu"))) + sorted(glob.glob(os.path.join(HOST, "*.cpp")))
 
 
 def _stale() -> bool:
@@ -44,7 +45,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode != 0:
