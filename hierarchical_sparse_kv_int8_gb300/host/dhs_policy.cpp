@@ -69,6 +69,9 @@ int dhs_policy_admit(dhs_policy *p, int32_t request, int64_t required_pages,
       history_pages < 0 || reclaimed_cap < 0 || (reclaimed_cap > 0 && !reclaimed) ||
       p->find(request) >= 0)
     return DHS_ERR_INVALID;
+  // Eq. (3) with every other request gone still cannot hold it: no reclaim
+  // or completion can ever admit it, so it is refused rather than left waiting.
+  if (required_pages > p->total - p->reserve) return DHS_ERR_CAPACITY;
   const int64_t free0 = p->free_pages();
   int64_t freed = 0;
   size_t q = 0;  // the reclaimed prefix of the admission order

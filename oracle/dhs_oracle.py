@@ -523,6 +523,11 @@ class ResidencyPolicy:
         return self.total - self.reserve - sum(r["required"] + r["optional"] for r in self.reqs)
 
     def admit(self, rid: int, required: int, history: int):
+        # eq. (3) cannot hold a request whose required pages exceed the whole
+        # budget less the reserve, even with no other request admitted: it
+        # could only wait forever, so it is refused
+        if required > self.total - self.reserve:
+            raise ValueError("capacity")
         free = self.free()
         freed, reclaimed = 0, []
         if required > free:

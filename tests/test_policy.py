@@ -161,3 +161,26 @@ def test_library_argument_checks():
     with pytest.raises(dhs.DhsError):
         p.query(9)
     assert p.free_pages() == 10 - 2 - 3
+
+
+def test_request_larger_than_the_budget_is_refused():
+    """A request whose required pages exceed total - reserve can never satisfy
+    eq. (3), even alone, so it is refused (capacity) instead of waiting; the
+    oracle and the library agree and nothing changes."""
+    import hierarchical_sparse_kv_int8_gb300 as dhs
+    o, lib = ResidencyPolicy(100, 10), _lib_policy(100, 10)
+    for p in (o, lib):
+        assert p.admit(1, 30, 50)[0]
+    with pytest.raises(ValueError, match="capacity"):
+        o.admit(2, 91, 0)
+    with pytest.raises(dhs.DhsError) as e:
+        lib.admit(2, 91, 0)
+    assert e.value.code == 3
+    assert o.free() == lib.free_pages() == 100 - 10 - 30 - 50
+    # within the budget it waits while the optional pages cannot cover it ...
+    assert o.admit(3, 90, 0) == lib.admit(3, 90, 0) == (False, 0, [])
+    # ... and exactly the budget less the reserve is admitted once it fits
+    for p in (o, lib):
+        p.complete(1)
+    assert o.admit(3, 90, 0) == lib.admit(3, 90, 0) == (True, 0, [])
+    assert o.free() == lib.free_pages() == 0
