@@ -242,24 +242,37 @@ k_na_topk(const int32_t *__restrict__ scores, const int32_t *__restrict__ minmax
     o[i] = i < ksel ? (int32_t)(uint32_t)(cand[i] & 0xFFFFFFFFull) : -1;
 }
 
-// Device address of g_noalloc_scratch, looked up once per device with that
-// device current.
+// Per-device state, kept under g_noalloc_mu: the device address of
+// g_noalloc_scratch (looked up once per device, with that device current) and
+// the dynamic shared memory each kernel has been granted on that device
+// (cudaFuncSetAttribute applies to the current device only).
+constexpr int kNoallocMaxDevices = 64;
+struct NoallocDevice {
+  int32_t *scratch = nullptr;
+  size_t granted_score = 0, granted_topk = 0;
+};
 std::mutex g_noalloc_mu;
-int32_t *g_noalloc_ptr[64] = {};
+NoallocDevice g_noalloc_dev[kNoallocMaxDevices];
 
-cudaError_t noalloc_scratch(int32_t **out) {
+// Scratch address for the current device, after granting the two kernels
+// `smem_score` and `smem_topk` bytes of dynamic shared memory on it.
+cudaError_t noalloc_setup(size_t smem_score, size_t smem_topk, int32_t **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  NoallocDevice &d = g_noalloc_dev[dev];
+  if (!d.scratch) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = static_cast<int32_t *>(p);
+    d.scratch = static_cast<int32_t *>(p);
   }
-  *out = g_noalloc_ptr[dev];
+  e = ensure_smem(k_na_score, smem_score, d.granted_score);
+  if (e == cudaSuccess) e = ensure_smem(k_na_topk, smem_topk, d.granted_topk);
+  if (e != cudaSuccess) return e;
+  *out = d.scratch;
   return cudaSuccess;
 }
 
@@ -275,27 +288,18 @@ extern "C" int dhs_select_noalloc(const int8_t *q_idx, const int8_t *keys, int32
       topk > 4096 || topk % 32 || ((uintptr_t)q_idx & 15u) || ((uintptr_t)keys & 15u))
     return DHS_ERR_INVALID;
   if ((int64_t)n_queries * n_rows > kNoallocScoreWords) return DHS_ERR_CAPACITY;
+  const size_t smem_score = (size_t)(kNaTile + kMaxKmax) * idx_row_bytes;
+  int kp = 1;
+  while (kp < topk) kp <<= 1;
+  const size_t smem_topk = (size_t)kp * 8 + ((size_t)1 << 13) * 4;
   int32_t *scratch = nullptr;
-  if (noalloc_scratch(&scratch) != cudaSuccess) {
+  if (noalloc_setup(smem_score, smem_topk, &scratch) != cudaSuccess) {
     cudaGetLastError();
     return DHS_ERR_CUDA;
   }
   int32_t *scores = scratch;
   int32_t *minmax = scratch + kNoallocScoreWords;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t smem_score = (size_t)(kNaTile + kMaxKmax) * idx_row_bytes;
-  int kp = 1;
-  while (kp < topk) kp <<= 1;
-  const size_t smem_topk = (size_t)kp * 8 + ((size_t)1 << 13) * 4;
-  static size_t granted_score = 0, granted_topk = 0;
-  {
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (ensure_smem(k_na_score, smem_score, granted_score) != cudaSuccess ||
-        ensure_smem(k_na_topk, smem_topk, granted_topk) != cudaSuccess) {
-      cudaGetLastError();
-      return DHS_ERR_CUDA;
-    }
-  }
   k_na_clear<<<1, 32, 0, s>>>(minmax, n_queries);
   k_na_score<<<(unsigned)((n_rows + kNaTile - 1) / kNaTile), kNaTile, smem_score, s>>>(
       q_idx, keys, n_queries, n_rows, idx_row_bytes, scores, minmax);

@@ -236,7 +236,11 @@ int dhs_commit(dhs_ctx *ctx, const int32_t *accepted_len, dhs_stream stream);
  * i.  Bytes are copied from the host backing first and the map entries
  * published after the copy, in stream order.  The previous optional set of the
  * slot stops being ready.  n_rows = 0 clears it.  DHS_ERR_CAPACITY if n_rows >
- * opt_rows_max. */
+ * opt_rows_max.  `rows` is uploaded with an asynchronous copy on `stream`: a
+ * pageable array is staged before the call returns and may be reused at once,
+ * but a page-locked one (cudaHostAlloc / cudaHostRegister) is read when the
+ * stream reaches the copy, so it must stay unchanged until then (for example
+ * until an event recorded after this call has completed). */
 int dhs_set_residency(dhs_ctx *ctx, int32_t slot, const int32_t *rows, int64_t n_rows,
                       dhs_stream stream);
 
@@ -363,8 +367,10 @@ void dhs_policy_destroy(dhs_policy *p); /* NULL is a no-op */
  * nothing changes.  The caller backs up a reclaimed request's history rows
  * and retires its optional rows (dhs_set_residency with no rows) before the
  * new request's pages are written.  DHS_ERR_INVALID for a bad argument or an
- * id already admitted; DHS_ERR_CAPACITY if more than reclaimed_cap requests
- * would lose pages (nothing changes). */
+ * id already admitted; DHS_ERR_CAPACITY if required_pages exceeds total -
+ * reserve (no reclaim or completion could ever admit it, so it is refused
+ * instead of waiting) or if more than reclaimed_cap requests would lose
+ * pages; nothing changes on an error. */
 int dhs_policy_admit(dhs_policy *p, int32_t request, int64_t required_pages,
                      int64_t history_pages, int32_t *admitted, int64_t *optional_pages,
                      int32_t *reclaimed, int32_t reclaimed_cap, int32_t *n_reclaimed);
