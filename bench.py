@@ -1,14 +1,17 @@
 """Benchmark of one verification round per layer on GB300.
 
-Workload: the DSpark-style verification configuration (K = 4 draft queries
-per request at positions S..S+3, batch 8, S = 32768, int8 indexer d_idx = 64,
-top-k 2048, GQA 8/1 with d = 128 in bf16, hot cache 4096 rows per request
-with ~70% overlap to the previous selection, draft ring window 2048,
-accepted_len uniform in 0..4), synthetic and seeded.  A step is one whole
-round: select (indexer + top-k), resolve (union, probe, compaction, shared
-host gather), attend (ring write, split-KV attention, merge, hot-cache
-install) and commit.  Metric: verified query-tokens per second per layer =
-N * K / step time.
+Workload: the DFlash2-style block verification configuration (K = 8 verify
+queries per request at positions S..S+7, batch 128, S = 102400, int8
+indexer with 4 heads of 128 summed, top-k 2048, GQA 16/1 with d = 128 in
+bf16, hot cache 4096 rows per request, optional residency 0, queries of a
+request sharing ~60% of their top rows), synthetic and seeded.  A step is
+one whole round: select (indexer + top-k), resolve (union, probe,
+compaction, shared host gather), attend (ring write, attention over the
+union, merge, hot-cache install) and commit.  Metric: verified query-tokens
+per second per layer = N * K / step time.  ``--workload`` times the other
+configurations (diagnostics); ``--sweep`` runs the load-adaptive sweep
+(optional residency 0/5/25/100% of history x K = 1/2/4/8, shared against
+per-query retrieval) on the same shapes.
 
 Each timed step starts from the same state (the snapshot taken after the
 previous-step round), restored outside the timed region, and the L2 cache is
@@ -20,7 +23,7 @@ step time is the maximum over ranks.
 
 --impl reference times the oracle (the plain CPU restatement in ``oracle/``)
 on the host cores: each step is one request's round, a bounded sample of the
-same workload.
+same workload, and the steps run on a pool of processes, one per core.
 """
 from __future__ import annotations
 
@@ -36,7 +39,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "cfg2"
+WORKLOAD = "cfg3"
 
 
 def wl_configs():
@@ -55,6 +58,10 @@ def parse():
                     help="configuration to time (the headline is %s)" % WORKLOAD)
     ap.add_argument("--attn-pass", type=int, default=0, choices=[0, 1, 2],
                     help="attention pass after a shared resolve: 0 auto, 1 per query, 2 union")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the load-adaptive sweep on the DFlash2-style shapes: optional residency "
+                         "0/5/25/100%% x K = 1/2/4/8, shared against per-query retrieval; one JSON "
+                         "line per point, then a summary line")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per GPU (default: the configuration's); a smaller batch is a "
                          "cut of the workload for profiling, not a bench line")
@@ -95,10 +102,10 @@ class ClockSampler:
     def __init__(self, gpu: int):
         self.gpu = gpu
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu)
+        import tempfile
+        self.path = os.path.join(tempfile.mkdtemp(prefix="dhs_clocks_"), "clocks_gpu%d.csv" % gpu)
 
     def start(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
@@ -177,31 +184,70 @@ def oracle_step(o, rec, rnd, slots):
     o.commit(acc_s)
 
 
-def cpu_baseline(rec, budget_s=10.0):
-    """Time the oracle on the host: round 1 (select, resolve, attend, commit)
-    of the workload's requests, repeated from the state round 0 leaves, until
-    about ``budget_s`` seconds of oracle work have been timed.  Set-up (input
-    generation, round 0, copying the state) is not timed."""
-    import copy
-    prepared = []
-    for r in range(rec.N):
-        o = oracle_requests(rec, [r])
-        oracle_step(o, rec, 0, [r])          # previous step: warms the hot cache
-        prepared.append(o)
-    done, t_total = 0, 0.0
-    while t_total < budget_s:
-        for r in range(rec.N):
-            o = copy.deepcopy(prepared[r])
-            t0 = time.perf_counter()
-            oracle_step(o, rec, 1, [r])
-            t_total += time.perf_counter() - t0
-            done += 1
-    value = done * rec.K / t_total
-    return {"value": value, "unit": "query-tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "%d request-rounds (K=%d, S=%d; the %d requests of the workload, "
-                      "repeated), single-threaded numpy (int64 scores, float64 attention)"
-                      % (done, rec.K, rec.S, rec.N),
-            "seconds": round(t_total, 2)}
+def _oracle_request_round(job):
+    """One bounded sample of the workload on the oracle: request ``r``'s
+    previous-step round (untimed; it leaves the hot cache as the workload
+    describes), then its timed verification round.  Runs in a worker
+    process; returns (request, seconds of the timed round)."""
+    rec, r = job
+    o = oracle_requests(rec, [r])
+    oracle_step(o, rec, 0, [r])
+    t0 = time.perf_counter()
+    oracle_step(o, rec, 1, [r])
+    return r, time.perf_counter() - t0
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_pool(rec, n_jobs, workers):
+    """Run ``n_jobs`` request-rounds of the oracle (requests taken in order,
+    cyclically) on ``workers`` processes started with ``spawn`` (each one
+    single-threaded: numpy's thread pools are limited to one thread), all
+    running at once.  Returns the per-job timed seconds and the wall time of
+    the whole pool."""
+    import multiprocessing as mp
+    keep = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                           "MKL_NUM_THREADS")}
+    for k in keep:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        t0 = time.perf_counter()
+        with ctx.Pool(workers) as pool:
+            res = list(pool.imap_unordered(_oracle_request_round,
+                                           [(rec, i % rec.N) for i in range(n_jobs)]))
+        wall = time.perf_counter() - t0
+    finally:
+        for k, v in keep.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return [dt for _, dt in res], wall
+
+
+def cpu_baseline(rec, rounds_per_core=2):
+    """Time the oracle on the host cores: request-rounds of the workload
+    (round 1, from the state round 0 leaves) on one single-threaded process
+    per core, all running together, ``rounds_per_core`` each.  The value is
+    the cores' summed rate: query-tokens of the timed rounds / mean timed
+    round time x cores.  Set-up (input generation, round 0) is not timed."""
+    cores = host_cores()
+    times, wall = oracle_pool(rec, rounds_per_core * cores, cores)
+    per = float(np.mean(times))
+    return {"value": round(cores * rec.K / per, 2), "unit": "query-tokens/s", "cores": cores,
+            "kind": "oracle",
+            "single_thread_value": round(rec.K / per, 3),
+            "sample": "%d request-rounds of the workload (K=%d, S=%d; requests 0..%d), one "
+                      "single-threaded numpy process per host core (int64 scores, float64 "
+                      "attention), all cores busy together; value = cores x K / mean timed "
+                      "round" % (len(times), rec.K, rec.S, min(rec.N, len(times)) - 1),
+            "seconds_timed": round(float(np.sum(times)), 2), "wall_s": round(wall, 2)}
 
 
 # ---------------------------------------------------------------- algorithmic bytes
@@ -242,7 +288,15 @@ def algorithmic_bytes(rec, counts, k_per_req):
             "kernel_bytes": kernel}
 
 
-NCU_SUMMARY = os.path.join(ROOT, "profiles", "kernels_cfg2_ncu_full.md")
+# ncu --set full summaries per workload: DRAM traffic per launch of each
+# kernel, captured on the whole workload or on a cut of its requests (the
+# summary states "captured requests: n"; traffic grows with the requests, so
+# it is scaled to the full batch).
+NCU_SUMMARIES = {
+    "cfg2": os.path.join(ROOT, "profiles", "kernels_cfg2_ncu_full.md"),
+    "cfg3": os.path.join(ROOT, "profiles", "kernels_cfg3_batch16_ncu_full.md"),
+}
+NCU_SUMMARY = NCU_SUMMARIES["cfg3"]
 NCU_NAMES = {"index_score": "k_index_score", "topk": "k_topk", "union_probe": "k_union_probe",
              "gather": "k_gather", "attn": "k_attn<", "attn_union": "k_uattn",
              "commit": "k_commit"}
@@ -259,17 +313,23 @@ def csrc_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(name):
-    """DRAM bytes (read + write) per launch of kernel ``name`` from the committed
-    ncu --set full summary of the benchmark workload, or None when the summary
+def ncu_traffic(name, path=None, full_requests=None):
+    """DRAM bytes (read + write) per launch of kernel ``name`` from a committed
+    ncu --set full summary (default NCU_SUMMARY), scaled from the captured
+    requests to ``full_requests`` when both are known; None when the summary
     is missing or the kernel sources have changed since it was captured."""
     import re
-    if name not in NCU_NAMES or not os.path.exists(NCU_SUMMARY):
+    path = path or NCU_SUMMARY
+    if name not in NCU_NAMES or not os.path.exists(path):
         return None
-    text = open(NCU_SUMMARY).read()
+    text = open(path).read()
     m = re.search(r"csrc-sha256: ([0-9a-f]+)", text)
     if not m or m.group(1) != csrc_hash():
         return None
+    scale_req = 1.0
+    mc = re.search(r"captured requests: (\d+)", text)
+    if mc and full_requests:
+        scale_req = full_requests / float(mc.group(1))
     scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
     for sec in text.split("\n## ")[1:]:
         if not sec.startswith(NCU_NAMES[name]):
@@ -277,7 +337,8 @@ def ncu_traffic(name):
         rd = re.search(r"DRAM read: ([0-9.]+) (\w+)", sec)
         wr = re.search(r"DRAM write: ([0-9.]+) (\w+)", sec)
         if rd and wr and rd.group(2) in scale and wr.group(2) in scale:
-            return int(float(rd.group(1)) * scale[rd.group(2)] + float(wr.group(1)) * scale[wr.group(2)])
+            return int(scale_req * (float(rd.group(1)) * scale[rd.group(2)] +
+                                    float(wr.group(1)) * scale[wr.group(2)]))
     return None
 
 
@@ -451,7 +512,9 @@ def run_native(args):
         peak = h2d_peak if link else hbm_peak
         roofs[name] = {"kernel": name, "bound": "h2d" if link else "hbm",
                        "achieved": round(ach, 1), "peak": round(peak, 1), "unit": "GB/s",
-                       "frac": round(ach / peak, 4), "traffic": ncu_traffic(name),
+                       "frac": round(ach / peak, 4),
+                       "traffic": (ncu_traffic(name, NCU_SUMMARIES[args.workload], rec.N)
+                                   if args.workload in NCU_SUMMARIES else None),
                        "algorithmic_bytes": byts,
                        "avg_launch_ms": round(avg_ms, 5),
                        "peak_source": ("host link: pinned host-to-device copy measured in this run"
@@ -462,10 +525,22 @@ def run_native(args):
             "not DRAM, and its staging and hot-slot writes stay in L2 during the launch")
     roof = roofs.get(dom)
     sel_t = sum(per[k][1] / per[k][0] for k in ("index_score", "topk") if k in per)
+    att_t = sum(per[k][1] / per[k][0] for k in ("attn", "attn_union") if k in per)
+    sa_bytes = ab["select"] + ab["attn"]
     families = {
         "select": {"achieved": round(ab["select"] / (sel_t * 1e-3) / 1e9, 1), "unit": "GB/s",
                    "frac_of_hbm": round(ab["select"] / (sel_t * 1e-3) / 1e9 / hbm_peak, 4),
                    "algorithmic_bytes": ab["select"], "ms": round(sel_t, 5)},
+        "attend": {"achieved": round(ab["attn"] / (att_t * 1e-3) / 1e9, 1), "unit": "GB/s",
+                   "frac_of_hbm": round(ab["attn"] / (att_t * 1e-3) / 1e9 / hbm_peak, 4),
+                   "algorithmic_bytes": ab["attn"], "ms": round(att_t, 5)},
+        # steps 1 and 5 together: indexer + top-k + attention bytes over the
+        # sum of their average launch times
+        "select+attend": {
+            "achieved": round(sa_bytes / ((sel_t + att_t) * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "frac_of_hbm": round(sa_bytes / ((sel_t + att_t) * 1e-3) / 1e9 / hbm_peak, 4),
+            "algorithmic_bytes": sa_bytes, "ms": round(sel_t + att_t, 5),
+            "peak": round(hbm_peak, 1), "peak_source": hbm_src},
     }
     if "gather" in roofs:
         families["shared gather"] = {
@@ -482,13 +557,11 @@ def run_native(args):
         "value": round(value, 1), "unit": "query-tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+int8",
-        "data": "synthetic (seeded; shapes of the DSpark-style verification configuration)",
-        "config": {"workload": rec.name, "batch": rec.N, "K": rec.K, "S": rec.S,
-                   "topk": rec.topk, "d_idx": rec.d_idx, "q_heads": rec.Hq,
-                   "kv_heads": rec.Hkv, "head_dim": rec.qk_dim, "hot_cache_rows": rec.B,
-                   "ring_window": rec.W, "l2": "flushed (512 MiB write) before every step",
-                   "state": "restored from snapshot before every step (untimed)",
-                   "attention_pass": "union" if "attn_union" in per else "per_query"},
+        "data": "synthetic (seeded; shapes of the %s configuration)" % rec.name,
+        "config": dict(workload_config(rec),
+                       l2="flushed (512 MiB write) before every step",
+                       state="restored from snapshot before every step (untimed)",
+                       attention_pass="union" if "attn_union" in per else "per_query"),
         "e2e": {"value": round(e2e_value, 1), "unit": "query-tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_ms, 5),
@@ -516,7 +589,126 @@ def run_native(args):
 
 
 # ---------------------------------------------------------------- reference arm
+def run_sweep(args):
+    """The load-adaptive sweep on the DFlash2-style shapes.
+
+    One context with an optional pool for the whole history serves every
+    point.  For each optional-residency fraction (whole pages, seeded) every
+    slot is bound again and its optional rows set; for each K the
+    previous-step round runs with K queries per request (it leaves the hot
+    cache), its state is snapshotted, and round 1 is timed from that state
+    with shared retrieval and with per-query retrieval (each missing
+    selection fetched on its own).  Per point: the host-fetched fraction of
+    the selected rows (rows fetched / valid selections, one round), the
+    selections per fetched row, and verify-query throughput N * K / step time
+    (CUDA events around each eager round, state restored and L2 flushed
+    before every step, outside the timed region)."""
+    import torch
+    import workload as wl
+    import hierarchical_sparse_kv_int8_gb300 as dhs
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+
+    torch.cuda.set_device(0)
+    dhs.build()
+    base_rec = wl.sweep_recipe(1.0)
+    if args.batch:
+        base_rec = base_rec.scaled(N=args.batch)
+    stream = torch.cuda.Stream()
+    points = []
+    steps = max(1, args.steps)
+    with torch.cuda.stream(stream):
+        run = Runner(base_rec, stream=stream)
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        for opt in wl.SWEEP_OPT:
+            rec = wl.sweep_recipe(opt).scaled(N=base_rec.N)
+            run.rebind()
+            run.set_residency(rec.residency_rows)
+            base = run.ctx.snapshot(stream)
+            for K in wl.SWEEP_K:
+                kr = np.full(rec.N, K, np.int32)
+                run.ctx.restore(base, stream)
+                run.load_round(0)
+                run.round(kr, rec.accepted(0, kr))
+                run.load_round(1)
+                snap = run.ctx.snapshot(stream)
+                acc = rec.accepted(1, kr)
+                for shared in (True, False):
+                    # one round for the counters
+                    run.ctx.restore(snap, stream)
+                    run.ctx.reset_stats(stream)
+                    run.round(kr, acc, shared)
+                    st = run.ctx.stats(stream)
+                    for i in range(args.warmup):
+                        run.ctx.restore(snap, stream)
+                        run.round(kr, acc, shared)
+                    ev = []
+                    for i in range(steps):
+                        run.ctx.restore(snap, stream)
+                        flush.fill_(i & 0xFF)
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record(stream)
+                        run.round(kr, acc, shared)
+                        b.record(stream)
+                        ev.append((a, b))
+                    stream.synchronize()
+                    ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+                    sel = max(1, st["selections"])
+                    pt = {"sweep_point": True, "workload": rec.name, "optional_residency": opt,
+                          "K": K, "retrieval": "shared" if shared else "per_query",
+                          "selections": st["selections"], "union_rows": st["union_rows"],
+                          "misses": st["misses"], "miss_selections": st["miss_selections"],
+                          "host_rows_fetched": st["host_rows_fetched"],
+                          "host_fetched_frac": round(st["host_rows_fetched"] / sel, 5),
+                          "selections_per_fetched_row": (
+                              round(st["miss_selections"] / st["host_rows_fetched"], 4)
+                              if st["host_rows_fetched"] else None),
+                          "opt_hits": st["opt_hits"], "hot_hits": st["hot_hits"],
+                          "ring_hits": st["ring_hits"], "direct_only": st["direct_only"],
+                          "ms_per_step": round(ms, 5),
+                          "query_tokens_per_s": round(rec.N * K / (ms * 1e-3), 1)}
+                    points.append(pt)
+                    print(json.dumps(pt), flush=True)
+                run.ctx.snapshot_free(snap)
+            run.ctx.snapshot_free(base)
+    # shared against per-query retrieval, per (residency, K)
+    pairs = {}
+    for p in points:
+        pairs.setdefault((p["optional_residency"], p["K"]), {})[p["retrieval"]] = p
+    summary = []
+    for (opt, K), d in sorted(pairs.items()):
+        sh, pq = d["shared"], d["per_query"]
+        summary.append({
+            "optional_residency": opt, "K": K,
+            "host_fetched_frac_shared": sh["host_fetched_frac"],
+            "host_fetched_frac_per_query": pq["host_fetched_frac"],
+            "fetch_reduction": (round(1 - sh["host_rows_fetched"] / pq["host_rows_fetched"], 4)
+                                if pq["host_rows_fetched"] else None),
+            "query_tokens_per_s_shared": sh["query_tokens_per_s"],
+            "query_tokens_per_s_per_query": pq["query_tokens_per_s"]})
+    print(json.dumps({"sweep": "load-adaptive (optional residency x K x retrieval)",
+                      "workload": base_rec.name, "batch": base_rec.N, "S": base_rec.S,
+                      "steps": steps, "warmup": args.warmup,
+                      "timing": "median of CUDA-event times around eager rounds; state restored "
+                                "and L2 flushed before every step (untimed)",
+                      "points": summary}), flush=True)
+
+
+def workload_config(rec):
+    """The ``config`` object of both arms' lines: the workload and its shapes."""
+    return {"workload": rec.name, "batch": rec.N, "K": rec.K, "S": rec.S, "topk": rec.topk,
+            "idx_heads": rec.H_idx, "d_idx": rec.d_idx, "q_heads": rec.Hq,
+            "kv_heads": rec.Hkv, "head_dim": rec.qk_dim, "hot_cache_rows": rec.B,
+            "ring_window": rec.W, "optional_residency": rec.opt_frac}
+
+
 def run_reference(args):
+    """The oracle on the host cores.  Each step is one request's verification
+    round (its previous-step round runs first, untimed), a bounded sample of
+    the workload; the steps run on a spawn pool of one single-threaded
+    process per core, all cores busy together, and the first ``warmup``
+    rounds to finish are dropped.  The host's cores serve the whole node, so
+    under torchrun rank 0 alone runs and the value covers every core of the
+    node, whatever the number of ranks."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -524,31 +716,29 @@ def run_reference(args):
     rec = wl.CONFIGS[args.workload]
     if args.batch:
         rec = rec.scaled(N=args.batch)
-    times = []
-    for i in range(args.warmup + args.steps):
-        r = i % rec.N
-        o = oracle_requests(rec, [r])
-        oracle_step(o, rec, 0, [r])
-        t0 = time.perf_counter()
-        oracle_step(o, rec, 1, [r])
-        dt = time.perf_counter() - t0
-        if i >= args.warmup:
-            times.append(dt)
-    ms = 1e3 * float(np.mean(times))
+    cores = host_cores()
+    times, wall = oracle_pool(rec, args.warmup + args.steps, cores)
+    times = times[args.warmup:] if len(times) > args.warmup else times
+    mean = float(np.mean(times))
+    ms = 1e3 * mean / cores          # pool time per request-round, all cores busy
     value = rec.K / (ms * 1e-3)
     line = {
         "impl": "reference",
         "metric": "verified query-tokens/s per layer (select+resolve+attend)",
         "value": round(value, 2), "unit": "query-tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64",
-        "data": "synthetic (seeded; shapes of the DSpark-style verification configuration)",
-        "config": {"workload": rec.name, "batch": rec.N, "K": rec.K, "S": rec.S,
-                   "topk": rec.topk, "sample": "one request's round per step"},
-        "cpu_baseline": {"value": round(value, 2), "unit": "query-tokens/s", "cores": 1,
-                         "kind": "oracle",
-                         "sample": "one request's verification round per step, "
-                                   "single-threaded numpy"},
+        "higher_is_better": True, "scaling": "none", "vs_baseline": None, "dtype": "int64+f64",
+        "per_rank": False,
+        "reference_scope": "every host core of the node, run by rank 0 alone; the host's "
+                           "cores are shared by all ranks, so the value does not grow with "
+                           "n_gpus",
+        "data": "synthetic (seeded; shapes of the %s configuration)" % rec.name,
+        "config": workload_config(rec),
+        "cpu_baseline": {"value": round(value, 2), "unit": "query-tokens/s", "cores": cores,
+                         "kind": "oracle", "single_thread_value": round(rec.K / mean, 3),
+                         "sample": "one request's verification round per step (%d timed), "
+                                   "one single-threaded numpy process per host core" % len(times),
+                         "wall_s": round(wall, 2)},
         "e2e": {"value": round(value, 2), "unit": "query-tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -559,5 +749,7 @@ if __name__ == "__main__":
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.sweep:
+        run_sweep(a)
     else:
         run_native(a)

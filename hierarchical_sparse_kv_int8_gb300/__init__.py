@@ -96,6 +96,7 @@ _SIGS = {
     "dhs_snapshot": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p],
                      ctypes.c_int),
     "dhs_restore": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
+    "dhs_snapshot_free": ([ctypes.c_void_p, ctypes.c_int32], ctypes.c_int),
     "dhs_round_host": ([ctypes.c_void_p] * 9, ctypes.c_int),
     "dhs_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "dhs_last_error": ([ctypes.c_void_p], ctypes.c_char_p),
@@ -365,6 +366,9 @@ class Context:
 
     def restore(self, sid: int, stream=None):
         self._check(self._lib.dhs_restore(self.h, sid, _stream(stream)), "dhs_restore")
+
+    def snapshot_free(self, sid: int):
+        self._check(self._lib.dhs_snapshot_free(self.h, sid), "dhs_snapshot_free")
 
     def round_host(self, q_idx, k_per_req, q, block_kv, accepted_len, out, lse=None, stream=None):
         kr = _host_i32(k_per_req, self.cfg.n_slots)

@@ -738,8 +738,19 @@ int dhs_snapshot(dhs_ctx *c, int32_t *snapshot_id, dhs_stream stream) {
   return DHS_OK;
 }
 
+int dhs_snapshot_free(dhs_ctx *c, int32_t id) {
+  if (!c || id < 0 || id >= (int32_t)c->snaps.size() || c->snaps[id].bufs.empty())
+    return DHS_ERR_INVALID;
+  // the buffers may still be read by copies in flight on any stream
+  if (cudaDeviceSynchronize() != cudaSuccess) return DHS_ERR_CUDA;
+  for (void *p : c->snaps[id].bufs) cudaFree(p);
+  c->snaps[id].bufs.clear();
+  return DHS_OK;
+}
+
 int dhs_restore(dhs_ctx *c, int32_t id, dhs_stream stream) {
-  if (!c || id < 0 || id >= (int32_t)c->snaps.size()) return DHS_ERR_INVALID;
+  if (!c || id < 0 || id >= (int32_t)c->snaps.size() || c->snaps[id].bufs.empty())
+    return DHS_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   Snapshot &sn = c->snaps[id];
   int i = 0;

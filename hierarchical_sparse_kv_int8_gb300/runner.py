@@ -54,6 +54,13 @@ class Runner:
         for r in range(N):
             self.ctx.bind(r, self.host[r], self.keys[r], rec.S, stream)
 
+    def rebind(self):
+        """Bind every slot again at the recipe's history length: empty hot
+        cache, no optional rows, no live ring rows (rows the previous rounds
+        committed past the history stay in the host tier, unused)."""
+        for r in range(self.rec.N):
+            self.ctx.bind(r, self.host[r], self.keys[r], self.rec.S, self.stream)
+
     def set_residency(self, frac_rows=None):
         for r in range(self.rec.N):
             rows = self.rec.residency_rows(r) if frac_rows is None else frac_rows(r)

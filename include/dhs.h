@@ -294,6 +294,9 @@ int32_t dhs_kernel_count(void);
  * device copies on `stream`. */
 int dhs_snapshot(dhs_ctx *ctx, int32_t *snapshot_id, dhs_stream stream);
 int dhs_restore(dhs_ctx *ctx, int32_t snapshot_id, dhs_stream stream);
+/* Free a snapshot's device copies (synchronises the device first); its id is
+ * not reused and restoring it afterwards is DHS_ERR_INVALID. */
+int dhs_snapshot_free(dhs_ctx *ctx, int32_t snapshot_id);
 
 /* One whole round through host buffers: runs select, resolve (shared),
  * attend and commit on q_idx, q and block_kv in host memory and returns out

@@ -63,8 +63,9 @@ def test_csrc_hash_is_stable():
 
 
 def test_reference_arm_line(capsys):
-    """The reference arm times the oracle on one request's round per step and
-    prints the contract's line with impl = reference."""
+    """The reference arm times the oracle on one request's round per step, on
+    a pool of one process per host core, and prints the contract's line with
+    impl = reference and the native arm's config object."""
     args = types.SimpleNamespace(workload="cfg1", steps=1, warmup=0, batch=0)
     bench.run_reference(args)
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
@@ -72,8 +73,9 @@ def test_reference_arm_line(capsys):
     assert line["unit"] == "query-tokens/s" and line["higher_is_better"] is True
     assert line["value"] > 0 and line["steps"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
-    assert line["config"]["workload"] == wl.CONFIGS["cfg1"].name
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["cores"] == bench.host_cores() >= 1
+    assert line["config"] == bench.workload_config(wl.CONFIGS["cfg1"])
 
 
 def test_reference_arm_under_two_ranks():
@@ -98,3 +100,6 @@ def test_reference_arm_under_two_ranks():
     assert len(lines) == 1, p.stdout
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
+    # one pool over the node's cores, not one per rank: labelled as such
+    assert line["per_rank"] is False and line["scaling"] == "none"
+    assert "does not grow with n_gpus" in line["reference_scope"]

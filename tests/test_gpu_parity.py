@@ -125,6 +125,9 @@ def test_tiny_gqa_rounds(shared, attn_pass):
     assert st["ring_hits"] == o.stats.ring_hits and st["opt_hits"] == o.stats.opt_hits
     assert st["host_rows_fetched"] == o.stats.host_rows_fetched
     assert st["installs"] == o.stats.installs and st["evictions"] == o.stats.evictions
+    assert st["direct_only"] == o.stats.direct_only
+    assert st["selections"] == o.stats.selections
+    assert st["miss_selections"] == o.stats.miss_selections
     assert o.stats.ring_hits > 0 and o.stats.opt_hits > 0 and o.stats.evictions > 0
 
 

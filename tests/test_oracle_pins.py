@@ -184,6 +184,58 @@ def test_fig3_shared_retrieval_one_copy_per_row():
     assert o2.stats.host_rows_fetched == 12         # one fetch per selection
     # the per-query baseline leaves the same cache state
     assert list(o.req[0].hot_row) == list(o2.req[0].hot_row)
+    # per-query placement: selection (j, i) of a missing row is fetched into
+    # staging row j*k + i, and that row holds the original c_s (eq. 11)
+    for j in range(4):
+        for i in range(3):
+            assert decode_loc(int(o2.loc[0, j, i])) == (STAGE, j * 3 + i)
+            assert np.array_equal(o2.staging[0][j * 3 + i], o2.req[0].host[int(sel[0, j, i])])
+    o2.check_placement()
+    o.check_placement()
+
+
+def test_direct_only_means_every_row_resolved_in_step_one():
+    """Fig. 2: steps 2 and 3 (hot-cache scan, host fetch) are skipped only
+    when every selected row of the request resolves in step 1 (the live ring
+    tail or the ready optional map).  Random rounds on a tiny source; the
+    count is checked against set membership computed here, by brute force."""
+    rng = np.random.default_rng(7)
+    K, k, n0 = 2, 3, 24
+    c = _tiny_cfg(n_slots=3, k_max=K, topk=k, budget=4, ring_window=6, s_max=64,
+                  opt_rows_max=12)
+    o = Oracle(c)
+    for r in range(3):
+        o.bind(r, _host(c, r), np.zeros((c.s_max, 8), np.int8), n0)
+    want, seen_direct, seen_other = 0, 0, 0
+    for rnd in range(40):
+        sel = np.full((3, K, k), -1, np.int64)
+        step1 = {}
+        for r in range(3):
+            q = o.req[r]
+            q.K = K
+            ring = set(range(max(q.ring_first, q.n - c.ring_window), q.n))
+            step1[r] = ring | set(q.opt_slot)
+            pool = sorted(step1[r]) if rng.random() < 0.5 and step1[r] else list(range(q.n))
+            for j in range(K):
+                m = min(int(rng.integers(1, k + 1)), len(pool))
+                sel[r, j, :m] = rng.choice(pool, m, replace=False)
+        before = o.stats.direct_only
+        o.resolve(sel, shared=True)
+        for r in range(3):
+            U = set(int(x) for x in sel[r].reshape(-1) if x >= 0)
+            d = U <= step1[r]
+            want += d
+            seen_direct += d
+            seen_other += not d
+        assert o.stats.direct_only == want
+        o.attend(np.zeros((3, K, c.q_heads, c.qk_dim), np.uint16),
+                 np.zeros((3, K, c.row_elems), np.uint16))
+        o.commit(np.full(3, int(rng.integers(0, K + 1))))
+        if rnd % 5 == 0:
+            for r in range(3):
+                rows = rng.choice(o.req[r].n, 8, replace=False).astype(np.int32)
+                o.set_residency(r, rows)
+    assert seen_direct > 10 and seen_other > 10
 
 
 @pytest.mark.parametrize("seed", range(12))

@@ -49,3 +49,61 @@ def test_noalloc_select_matches_context_select_twice():
         torch.cuda.synchronize()
         assert torch.equal(got, want[0]), "call %d differs from dhs_select" % call
     assert ctx.stats()["device_error"] == 0
+
+
+def _noalloc_vs_oracle(n_q, n_rows, row_bytes, topk, seed, lo=-8, hi=8):
+    """dhs_select_noalloc on seeded keys and queries against the oracle's
+    exact scores and ordered top-k, query by query."""
+    import torch
+    import hierarchical_sparse_kv_int8_gb300 as dhs
+    from oracle.dhs_oracle import index_scores, topk_ordered
+
+    dhs.build()
+    keys = wl.i8(n_rows * row_bytes, seed, 1, 0, lo, hi).reshape(n_rows, row_bytes)
+    q = wl.i8(n_q * row_bytes, seed, 2, 0, lo, hi).reshape(n_q, row_bytes)
+    got = torch.full((n_q, topk), -7, dtype=torch.int32, device="cuda")
+    dhs.select_noalloc(torch.from_numpy(q).cuda(), torch.from_numpy(keys).cuda(), n_q, n_rows,
+                       row_bytes, topk, got)
+    got = got.cpu().numpy()
+    for j in range(n_q):
+        sc = index_scores(q[j], keys, n_rows)
+        want = topk_ordered(sc, topk)
+        assert np.array_equal(got[j], want), "query %d differs from the oracle" % j
+    return keys, q
+
+
+@pytest.mark.parametrize("row_bytes", [16, 128, 1024])
+def test_noalloc_full_range_multi_pass(row_bytes):
+    """Full-range int8 keys and queries: every query's scores span more than
+    2^13 values, so the radix select takes several passes; rows of 16, 128 and
+    1024 bytes cover the shared-memory rotation for 1, 8 and 64 chunks."""
+    n_rows = {16: 60000, 128: 40000, 1024: 6000}[row_bytes]
+    keys, q = _noalloc_vs_oracle(8, n_rows, row_bytes, 2048, seed=61 + row_bytes,
+                                 lo=-128, hi=127)
+    sc = keys.astype(np.int64) @ q[0].astype(np.int64)
+    assert sc.max() - sc.min() >= 1 << 13
+
+
+def test_noalloc_domain_shorter_than_k():
+    """n_rows < topk: every row is kept, ordered, and the list is padded with -1."""
+    _noalloc_vs_oracle(3, 3000, 64, 4096, seed=71)
+
+
+def test_noalloc_topk_4096():
+    """The largest list (4096 entries, beyond the context's 2048), over a
+    domain larger than it, with many ties (narrow int8 range)."""
+    _noalloc_vs_oracle(5, 200000, 64, 4096, seed=72)
+
+
+def test_noalloc_capacity_edge():
+    """n_queries * n_rows = 2^21 fills the fixed scratch exactly and is
+    served; one row more is refused with DHS_ERR_CAPACITY before any launch."""
+    import torch
+    import hierarchical_sparse_kv_int8_gb300 as dhs
+    _noalloc_vs_oracle(8, 1 << 18, 16, 256, seed=73)
+    keys = torch.zeros(((1 << 21) + 1, 16), dtype=torch.int8, device="cuda")
+    q = torch.zeros((1, 16), dtype=torch.int8, device="cuda")
+    out = torch.zeros((1, 256), dtype=torch.int32, device="cuda")
+    with pytest.raises(dhs.DhsError) as e:
+        dhs.select_noalloc(q, keys, 1, (1 << 21) + 1, 16, 256, out)
+    assert e.value.code == 3
