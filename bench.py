@@ -56,12 +56,19 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(wl_configs()),
                     help="configuration to time (the headline is %s)" % WORKLOAD)
-    ap.add_argument("--attn-pass", type=int, default=0, choices=[0, 1, 2],
-                    help="attention pass after a shared resolve: 0 auto, 1 per query, 2 union")
+    ap.add_argument("--attn-pass", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="attention pass after a shared resolve: 0 auto, 1 per query, 2 union "
+                         "(mma.sync), 3 union on the fifth-generation tensor cores")
     ap.add_argument("--sweep", action="store_true",
                     help="the load-adaptive sweep on the DFlash2-style shapes: optional residency "
                          "0/5/25/100%% x K = 1/2/4/8, shared against per-query retrieval; one JSON "
                          "line per point, then a summary line")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layer-group diagnostic: one index producer and LAYERS-1 follower payload "
+                         "layers on --chi shared staging arenas, timed on one stream and pipelined "
+                         "(resolves with their host gathers on a copy stream while the previous "
+                         "layer attends on a compute stream); prints one JSON line")
+    ap.add_argument("--chi", type=int, default=2, help="staging arenas of the layer group")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per GPU (default: the configuration's); a smaller batch is a "
                          "cut of the workload for profiling, not a bench line")
@@ -693,6 +700,129 @@ def run_sweep(args):
                       "points": summary}), flush=True)
 
 
+def run_layers(args):
+    """Layer-group pipelining on the workload's shapes (a diagnostic).
+
+    Layer 0 produces the positions (indexer + top-k); layers 1..L-1 are
+    follower payload layers with their own host rows, hot caches and rings
+    that take those positions.  All stage in ``chi`` shared arenas (layer l
+    in arena l mod chi).  A step is every layer's resolve and attention plus
+    the commits.  Sequential: all on one stream, layer after layer.
+    Pipelined: resolves on a copy stream, each layer's attention on a
+    compute stream one layer behind, so a layer's host gather overlaps the
+    previous layer's attention; a resolve into an arena waits on the GPU for
+    its previous user's attention.  Both start every step from the same
+    snapshot, with the L2 flushed (untimed)."""
+    import torch
+    import workload as wl
+    import hierarchical_sparse_kv_int8_gb300 as dhs
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+
+    torch.cuda.set_device(0)
+    dhs.build()
+    base = wl.CONFIGS[args.workload].scaled(N=args.batch or 32)
+    L, chi = max(2, args.layers), max(1, args.chi)
+    recs = [base.scaled(seed=base.seed + l) for l in range(L)]
+    comp, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    arenas = dhs.Arenas(chi, base.N, base.kmax, base.topk, base.row_elems)
+    runs = [Runner(recs[0], arenas=arenas, arena=0, stream=comp)]
+    for l in range(1, L):
+        runs.append(Runner(recs[l], arenas=arenas, arena=l % chi, role=dhs.ROLE_FOLLOWER,
+                           keys=runs[0].keys, stream=comp))
+    kr = base.k_per_req()
+    for rnd in range(2):  # the previous step, then the timed step's inputs
+        for run in runs:
+            run.load_round(rnd)
+        torch.cuda.synchronize()
+        if rnd == 0:
+            p = runs[0]
+            p.ctx.select(p.q_idx, kr, p.topk, None, comp)
+            for l, run in enumerate(runs):
+                if l:
+                    run.topk = p.topk
+                    run.ctx.adopt(kr, None, comp)
+                run.ctx.resolve(run.topk, run.loc, True, comp)
+                run.ctx.attend(run.q, run.block, run.loc, run.out, run.lse, comp)
+            for run in runs:
+                run.ctx.commit(base.accepted(0, kr), comp)
+    torch.cuda.synchronize()
+    snaps = [run.ctx.snapshot(comp) for run in runs]
+    acc = base.accepted(1, kr)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+
+    def step(pipelined):
+        p = runs[0]
+        p.ctx.select(p.q_idx, kr, p.topk, None, comp)
+        cs = copy if pipelined else comp
+        if pipelined:
+            ev = torch.cuda.Event()
+            ev.record(comp)
+            copy.wait_event(ev)
+        for l, run in enumerate(runs):
+            if l:
+                run.topk = p.topk
+                run.ctx.adopt(kr, None, cs)
+            run.ctx.resolve(run.topk, run.loc, True, cs)
+            if not pipelined:
+                run.ctx.attend(run.q, run.block, run.loc, run.out, run.lse, comp)
+            elif l:
+                prev = runs[l - 1]
+                prev.ctx.attend(prev.q, prev.block, prev.loc, prev.out, prev.lse, comp)
+        if pipelined:
+            last = runs[-1]
+            last.ctx.attend(last.q, last.block, last.loc, last.out, last.lse, comp)
+        for run in runs:
+            run.ctx.commit(acc, comp)
+
+    res = {}
+    for mode in ("sequential", "pipelined"):
+        times = []
+        for i in range(args.warmup + args.steps):
+            for run, sn in zip(runs, snaps):
+                run.ctx.restore(sn, comp)
+            flush.fill_(i & 0xFF)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(comp)
+            step(mode == "pipelined")
+            b.record(comp)   # every layer's work ends in its commit, on this stream
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                times.append(a.elapsed_time(b))
+        res[mode] = float(np.median(times))
+    # the gathers alone: per-kernel times of one sequential step
+    for run in runs:
+        run.ctx.set_timing(True)
+    for run, sn in zip(runs, snaps):
+        run.ctx.restore(sn, comp)
+    torch.cuda.synchronize()
+    step(False)
+    torch.cuda.synchronize()
+    per = {}
+    for run in runs:
+        for name, (n, ms) in run.ctx.kernel_times().items():
+            if n:
+                per[name] = per.get(name, 0.0) + ms
+        run.ctx.set_timing(False)
+    dedicated = L * base.N * base.kmax * base.topk * base.row_bytes
+    line = {"diagnostic": "layer-group pipelining (producer + follower payload layers)",
+            "workload": base.name, "batch": base.N, "K": base.K, "layers": L, "chi": chi,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step_sequential": round(res["sequential"], 4),
+            "ms_per_step_pipelined": round(res["pipelined"], 4),
+            "speedup": round(res["sequential"] / res["pipelined"], 3),
+            "kernel_ms_one_sequential_step": {k: round(v, 4) for k, v in per.items()},
+            "gather_ms_hidden": round(res["sequential"] - res["pipelined"], 4),
+            "gather_ms_total": round(per.get("gather", 0.0), 4),
+            "staging_bytes_shared_arenas": arenas.nbytes(),
+            "staging_bytes_one_arena_per_layer": dedicated,
+            "staging_ratio": round(dedicated / arenas.nbytes(), 2)}
+    print(json.dumps(line), flush=True)
+    for run in runs:
+        run.ctx.close()
+    arenas.close()
+
+
 def workload_config(rec):
     """The ``config`` object of both arms' lines: the workload and its shapes."""
     return {"workload": rec.name, "batch": rec.N, "K": rec.K, "S": rec.S, "topk": rec.topk,
@@ -751,5 +881,7 @@ if __name__ == "__main__":
         run_reference(a)
     elif a.sweep:
         run_sweep(a)
+    elif a.layers:
+        run_layers(a)
     else:
         run_native(a)

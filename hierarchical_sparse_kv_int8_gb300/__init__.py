@@ -18,8 +18,8 @@ import numpy as np
 
 from . import _build
 
-__all__ = ["Config", "Context", "DhsError", "build", "load", "LOC_RING", "LOC_OPT", "LOC_HOT",
-           "LOC_STAGE", "BUF"]
+__all__ = ["Arenas", "Config", "Context", "DhsError", "build", "load", "LOC_RING", "LOC_OPT",
+           "LOC_HOT", "LOC_STAGE", "BUF", "ROLE_FULL", "ROLE_FOLLOWER"]
 
 LOC_RING, LOC_OPT, LOC_HOT, LOC_STAGE = 0, 1, 2, 3
 LOC_TIER_SHIFT = 28
@@ -36,9 +36,11 @@ class Config(ctypes.Structure):
                 ("v_dim", ctypes.c_int32), ("kv_layout", ctypes.c_int32),
                 ("budget", ctypes.c_int32), ("ring_window", ctypes.c_int32),
                 ("page_rows", ctypes.c_int32), ("opt_rows_max", ctypes.c_int64),
-                ("softmax_scale", ctypes.c_float), ("attn_pass", ctypes.c_int32)]
+                ("softmax_scale", ctypes.c_float), ("attn_pass", ctypes.c_int32),
+                ("topk_pass", ctypes.c_int32)]
 
-ATTN_AUTO, ATTN_PER_QUERY, ATTN_UNION = 0, 1, 2
+ATTN_AUTO, ATTN_PER_QUERY, ATTN_UNION, ATTN_UNION_TC = 0, 1, 2, 3
+TOPK_AUTO, TOPK_CLUSTER, TOPK_ROW = 0, 1, 2
 
 
 class Stats(ctypes.Structure):
@@ -97,6 +99,13 @@ _SIGS = {
                      ctypes.c_int),
     "dhs_restore": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p], ctypes.c_int),
     "dhs_snapshot_free": ([ctypes.c_void_p, ctypes.c_int32], ctypes.c_int),
+    "dhs_arenas_create": ([ctypes.c_int32] * 5 + [ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
+    "dhs_arenas_bytes": ([ctypes.c_void_p], ctypes.c_int64),
+    "dhs_arenas_destroy": ([ctypes.c_void_p], ctypes.c_int),
+    "dhs_create_on_arena": ([ctypes.POINTER(Config), ctypes.c_void_p, ctypes.c_int32,
+                             ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
+    "dhs_adopt": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+                  ctypes.c_int),
     "dhs_round_host": ([ctypes.c_void_p] * 9, ctypes.c_int),
     "dhs_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "dhs_last_error": ([ctypes.c_void_p], ctypes.c_char_p),
@@ -259,17 +268,57 @@ class Policy:
         return int(self._lib.dhs_policy_free_pages(self.h))
 
 
-class Context:
-    """One KV source (layer) with ``n_slots`` request slots; see include/dhs.h."""
+ROLE_FULL, ROLE_FOLLOWER = 0, 1
 
-    def __init__(self, cfg: Config):
+
+class Arenas:
+    """chi staging arenas shared by the sources of a layer group (dhs_arenas_*)."""
+
+    def __init__(self, chi: int, n_slots: int, k_max: int, topk: int, row_elems: int):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        rc = self._lib.dhs_arenas_create(chi, n_slots, k_max, topk, row_elems, ctypes.byref(h))
+        if rc:
+            raise DhsError(rc, "dhs_arenas_create")
+        self.h = h.value
+        self.chi = chi
+
+    def nbytes(self) -> int:
+        return int(self._lib.dhs_arenas_bytes(self.h))
+
+    def close(self):
+        if getattr(self, "h", None):
+            rc = self._lib.dhs_arenas_destroy(self.h)
+            if rc:
+                raise DhsError(rc, "dhs_arenas_destroy")
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Context:
+    """One KV source (layer) with ``n_slots`` request slots; see include/dhs.h.
+    With ``arenas`` the context stages in arena ``arena`` of that set
+    (dhs_create_on_arena) and may be a follower (``role``)."""
+
+    def __init__(self, cfg: Config, arenas: Optional[Arenas] = None, arena: int = 0,
+                 role: int = ROLE_FULL):
         self.cfg = cfg
         self._lib = load()
         h = ctypes.c_void_p()
-        rc = self._lib.dhs_create(ctypes.byref(cfg), ctypes.byref(h))
+        if arenas is None:
+            rc = self._lib.dhs_create(ctypes.byref(cfg), ctypes.byref(h))
+        else:
+            rc = self._lib.dhs_create_on_arena(ctypes.byref(cfg), arenas.h, arena, role,
+                                               ctypes.byref(h))
         if rc:
             raise DhsError(rc, "dhs_create")
         self.h = h
+        self.arenas = arenas  # kept alive while the context uses them
 
     def close(self):
         if getattr(self, "h", None):
@@ -306,6 +355,14 @@ class Context:
         self._check(self._lib.dhs_select(self.h, _dptr(q_idx), _host_ptr(kr),
                                          None if p is None else p.ctypes.data, _dptr(topk_out),
                                          _stream(stream)), "dhs_select")
+
+    def adopt(self, k_per_req, pos=None, stream=None):
+        kr = _host_i32(k_per_req, self.cfg.n_slots)
+        p = None
+        if pos is not None:
+            p = np.ascontiguousarray(np.asarray(pos, dtype=np.int64))
+        self._check(self._lib.dhs_adopt(self.h, _host_ptr(kr), None if p is None else p.ctypes.data,
+                                        _stream(stream)), "dhs_adopt")
 
     def resolve(self, topk, loc_out, shared=True, stream=None):
         self._check(self._lib.dhs_resolve(self.h, _dptr(topk), _dptr(loc_out), 1 if shared else 0,

@@ -123,6 +123,19 @@ using namespace dhs;
 
 enum Phase { PH_IDLE = 0, PH_SELECTED, PH_RESOLVED, PH_ATTENDED };
 
+// Verification staging shared by the sources of a layer group.  Arena i is
+// taken by one context at a time: its dhs_resolve claims it (after the
+// previous user's attention readers, through `released`), its dhs_attend
+// calls read it and record `released` after their kernels.
+struct dhs_arenas {
+  int chi = 0, N = 0, Kmax = 0, k = 0, row = 0;
+  uint16_t *base = nullptr;
+  std::vector<cudaEvent_t> released;
+  std::vector<dhs_ctx *> owner;   // context whose resolve last filled the arena
+  std::vector<char> unread;       // that resolve's attention not yet issued
+  int users = 0;                  // contexts created on these arenas
+};
+
 struct Snapshot {
   std::vector<void *> bufs;
   std::vector<int64_t> n, ring_first, opt_count;
@@ -158,6 +171,12 @@ struct dhs_ctx {
   const int8_t **d_keys = nullptr;
   const uint16_t **d_host = nullptr;
   const char *last_error = "";
+  // layer groups: staging from shared arenas, calls ordered across streams
+  dhs_arenas *arenas = nullptr;
+  int arena = -1;
+  int role = DHS_ROLE_FULL;
+  cudaEvent_t last_ev = nullptr;  // recorded after every call's work
+  bool last_valid = false;
 };
 
 namespace {
@@ -180,6 +199,8 @@ cudaError_t dalloc(dhs_ctx *c, T **p, size_t count) {
 void free_all(dhs_ctx *c) {
   for (void *p : c->allocs) cudaFree(p);
   c->allocs.clear();
+  if (c->last_ev) cudaEventDestroy(c->last_ev);
+  c->last_ev = nullptr;
   for (auto &s : c->snaps)
     for (void *p : s.bufs) cudaFree(p);
   c->snaps.clear();
@@ -246,6 +267,22 @@ int upload_words(dhs_ctx *c, int32_t *dst, const std::vector<int32_t> &w, cudaSt
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// A context on shared arenas may be driven from several streams (its
+// gathers on a copy stream, its attention on a compute stream): every call
+// first waits for the work of the context's previous call, wherever it ran,
+// and records the point its own work ends.
+int order_enter(dhs_ctx *c, cudaStream_t s) {
+  if (c->arenas && c->last_valid && cudaStreamWaitEvent(s, c->last_ev, 0) != cudaSuccess)
+    return cuda_fail(c, cudaGetLastError());
+  return DHS_OK;
+}
+int order_leave(dhs_ctx *c, cudaStream_t s) {
+  if (!c->arenas) return DHS_OK;
+  if (cudaEventRecord(c->last_ev, s) != cudaSuccess) return cuda_fail(c, cudaGetLastError());
+  c->last_valid = true;
+  return DHS_OK;
+}
+
 
 }  // namespace
 
@@ -271,9 +308,13 @@ const char *dhs_kernel_name(int32_t id) {
   return (id >= 0 && id < K_COUNT) ? kKernelNames[id] : "?";
 }
 
-int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
+}  // extern "C"
+
+namespace {
+int create_impl(const dhs_config *cfg, dhs_arenas *arenas, int arena, int role, dhs_ctx **out) {
   if (!cfg || !out) return DHS_ERR_INVALID;
   *out = nullptr;
+  if (role != DHS_ROLE_FULL && role != DHS_ROLE_FOLLOWER) return DHS_ERR_INVALID;
   const dhs_config &g = *cfg;
   if (g.n_slots < 1 || g.n_slots > kMaxSlots || g.k_max < 1 || g.k_max > kMaxKmax ||
       g.topk < 32 || g.topk > kMaxTopk || g.topk % 32 || g.s_max < 1 || g.s_max > (1 << 27) ||
@@ -281,7 +322,8 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
       g.idx_heads * g.idx_dim > 1024 || g.q_heads < 1 || g.kv_heads < 1 ||
       g.q_heads % g.kv_heads || g.q_heads / g.kv_heads > 16 || g.q_heads > 128 || g.budget < 1 ||
       g.budget > 65535 || g.ring_window < 1 || g.page_rows < 1 || g.opt_rows_max < 0 ||
-      g.opt_rows_max > g.s_max || g.attn_pass < DHS_ATTN_AUTO || g.attn_pass > DHS_ATTN_UNION)
+      g.opt_rows_max > g.s_max || g.attn_pass < DHS_ATTN_AUTO || g.attn_pass > DHS_ATTN_UNION_TC ||
+      g.topk_pass < DHS_TOPK_AUTO || g.topk_pass > DHS_TOPK_ROW)
     return DHS_ERR_INVALID;
   if (g.kv_layout != DHS_KV_SPLIT && g.kv_layout != DHS_KV_LATENT) return DHS_ERR_INVALID;
   if (g.kv_layout == DHS_KV_LATENT && (g.kv_heads != 1 || g.v_dim > g.qk_dim))
@@ -292,10 +334,16 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   const int64_t Rd = (int64_t)g.page_rows *
                      ((g.ring_window + g.page_rows - 1 + g.k_max + g.page_rows - 1) / g.page_rows);
   if (Rd > DHS_LOC_INDEX_MASK) return DHS_ERR_INVALID;
+  if (arenas && (arena < 0 || arena >= arenas->chi || arenas->N != g.n_slots ||
+                 arenas->Kmax != g.k_max || arenas->k != g.topk || arenas->row != row))
+    return DHS_ERR_INVALID;
 
   dhs_ctx *c = new (std::nothrow) dhs_ctx();
   if (!c) return DHS_ERR_OOM;
   c->cfg = g;
+  c->arenas = arenas;
+  c->arena = arenas ? arena : -1;
+  c->role = role;
   cudaGetDevice(&c->device);
   DevCtx &d = c->d;
   memset(&d, 0, sizeof(d));
@@ -332,14 +380,14 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   {
     const bool can = uattn_supported(d);
     const double pq_bytes = (double)d.N * d.Kmax * (d.k + d.Kmax) * row * 2;
-    if (g.attn_pass == DHS_ATTN_UNION && !can) {
+    if ((g.attn_pass == DHS_ATTN_UNION || g.attn_pass == DHS_ATTN_UNION_TC) && !can) {
       delete c;
       return DHS_ERR_INVALID;
     }
     // AUTO: the union pass for 128-dim heads once the per-query pass would
     // stream more than 128 MiB; latent (MLA) rows keep the per-query pass,
     // which measured 3.6x faster on them (0.46 against 1.69 ms at S = 512K)
-    c->fused = g.attn_pass == DHS_ATTN_UNION ||
+    c->fused = g.attn_pass == DHS_ATTN_UNION || g.attn_pass == DHS_ATTN_UNION_TC ||
                (g.attn_pass == DHS_ATTN_AUTO && can && d.dqk == 128 &&
                 pq_bytes > 128.0 * 1024 * 1024);
   }
@@ -349,12 +397,14 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
 #define ALLOC(ptr, count) \
   if (e == cudaSuccess) e = dalloc(c, &(ptr), (count))
   uint16_t *pool = nullptr;
-  const size_t pool_rows = N * (B + KK + (size_t)d.Rd + (size_t)d.opt_max);
+  // (a context on shared arenas stages its misses in its arena instead)
+  const size_t own_stage = arenas ? 0 : KK;
+  const size_t pool_rows = N * (B + own_stage + (size_t)d.Rd + (size_t)d.opt_max);
   ALLOC(pool, pool_rows * R);
   if (e == cudaSuccess) {
     d.hot_data = pool;
-    d.stage = d.hot_data + N * B * R;
-    d.ring = d.stage + N * KK * R;
+    d.stage = arenas ? arenas->base + (size_t)arena * N * KK * R : d.hot_data + N * B * R;
+    d.ring = d.hot_data + N * (B + own_stage) * R;
     d.opt = d.ring + N * d.Rd * R;
   }
   ALLOC(c->d_keys, N);
@@ -370,7 +420,8 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   ALLOC(d.opt_map, N * (size_t)d.Sm);
   ALLOC(d.opt_list, N * (size_t)std::max<int64_t>(1, d.opt_max));
   ALLOC(d.opt_count, N);
-  ALLOC(d.scores, N * d.Kmax * (size_t)d.Ss);
+  // a follower never scores (its positions come from a producer)
+  ALLOC(d.scores, role == DHS_ROLE_FOLLOWER ? 4 : N * d.Kmax * (size_t)d.Ss);
   ALLOC(d.minmax, N * d.Kmax * 2);
   ALLOC(d.uni, N * KK);
   ALLOC(d.uent, N * KK);
@@ -424,12 +475,14 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   }
   if (e == cudaSuccess) e = cudaMemset(d.opt_count, 0, N * 8);
   if (e == cudaSuccess) e = cudaMemset(pool, 0, pool_rows * R * 2);
+  if (e == cudaSuccess && arenas) e = cudaEventCreateWithFlags(&c->last_ev, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     free_all(c);
     delete c;
     return DHS_ERR_CUDA;
   }
+  if (arenas) arenas->users += 1;
   c->n.assign(N, 0);
   c->ring_first.assign(N, 0);
   c->opt_count.assign(N, 0);
@@ -440,10 +493,88 @@ int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
   *out = c;
   return DHS_OK;
 }
+}  // namespace
+
+extern "C" {
+
+int dhs_create(const dhs_config *cfg, dhs_ctx **out) {
+  return create_impl(cfg, nullptr, -1, DHS_ROLE_FULL, out);
+}
+
+int dhs_create_on_arena(const dhs_config *cfg, dhs_arenas *arenas, int32_t arena, int32_t role,
+                        dhs_ctx **out) {
+  if (!arenas) return DHS_ERR_INVALID;
+  return create_impl(cfg, arenas, arena, role, out);
+}
+
+int dhs_arenas_create(int32_t chi, int32_t n_slots, int32_t k_max, int32_t topk,
+                      int32_t row_elems, dhs_arenas **out) {
+  if (!out || chi < 1 || chi > 256 || n_slots < 1 || n_slots > kMaxSlots || k_max < 1 ||
+      k_max > kMaxKmax || topk < 32 || topk > kMaxTopk || topk % 32 || row_elems < 8 ||
+      row_elems * 2 > 2048 || row_elems % 8)
+    return DHS_ERR_INVALID;
+  *out = nullptr;
+  dhs_arenas *a = new (std::nothrow) dhs_arenas();
+  if (!a) return DHS_ERR_OOM;
+  a->chi = chi;
+  a->N = n_slots;
+  a->Kmax = k_max;
+  a->k = topk;
+  a->row = row_elems;
+  const size_t bytes = (size_t)chi * n_slots * k_max * topk * row_elems * 2;
+  if (cudaMalloc(&a->base, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete a;
+    return DHS_ERR_OOM;
+  }
+  a->released.assign(chi, nullptr);
+  a->owner.assign(chi, nullptr);
+  a->unread.assign(chi, 0);
+  for (int i = 0; i < chi; ++i) {
+    if (cudaEventCreateWithFlags(&a->released[i], cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      for (int j = 0; j < i; ++j) cudaEventDestroy(a->released[j]);
+      cudaFree(a->base);
+      delete a;
+      return DHS_ERR_CUDA;
+    }
+  }
+  if (cudaMemset(a->base, 0, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    for (auto ev : a->released) cudaEventDestroy(ev);
+    cudaFree(a->base);
+    delete a;
+    return DHS_ERR_CUDA;
+  }
+  *out = a;
+  return DHS_OK;
+}
+
+int64_t dhs_arenas_bytes(const dhs_arenas *a) {
+  return a ? (int64_t)a->chi * a->N * a->Kmax * a->k * a->row * 2 : 0;
+}
+
+int dhs_arenas_destroy(dhs_arenas *a) {
+  if (!a) return DHS_OK;
+  if (a->users > 0) return DHS_ERR_INVALID;  // a context still stages there
+  cudaDeviceSynchronize();
+  for (auto ev : a->released) cudaEventDestroy(ev);
+  cudaFree(a->base);
+  delete a;
+  return DHS_OK;
+}
 
 void dhs_destroy(dhs_ctx *c) {
   if (!c) return;
   cudaDeviceSynchronize();
+  if (c->arenas) {
+    dhs_arenas *a = c->arenas;
+    if (a->owner[c->arena] == c) {
+      a->owner[c->arena] = nullptr;
+      a->unread[c->arena] = 0;
+    }
+    a->users -= 1;
+  }
   free_all(c);
   delete c;
 }
@@ -469,6 +600,7 @@ int dhs_bind_request(dhs_ctx *c, int32_t slot, const void *host_kv, const int8_t
     cudaGetLastError();
     return DHS_ERR_INVALID;  // not page-locked host memory
   }
+  if (int rc = order_enter(c, s)) return rc;
   c->host_ptr[slot] = dev_host;
   c->key_ptr[slot] = idx_keys;
   if (cudaMemcpyAsync(c->d_host, c->host_ptr.data(), c->d.N * sizeof(void *),
@@ -486,7 +618,7 @@ int dhs_bind_request(dhs_ctx *c, int32_t slot, const void *host_kv, const int8_t
   c->opt_count[slot] = 0;
   c->K[slot] = 0;
   c->bound[slot] = 1;
-  return DHS_OK;
+  return order_leave(c, s);
 }
 
 }  // extern "C"
@@ -494,16 +626,23 @@ int dhs_bind_request(dhs_ctx *c, int32_t slot, const void *host_kv, const int8_t
 namespace {
 // dhs_select, with the index rows either in device memory (q_idx) or, when
 // q_idx is null, on the host (q_inline), carried in the launch parameters.
-int select_impl(dhs_ctx *c, const int8_t *q_idx, const int8_t *q_inline,
-                const int32_t *k_per_req, const int64_t *pos, int32_t *topk_out,
-                dhs_stream stream) {
-  if (c->phase != PH_IDLE) return DHS_ERR_INVALID;
+// The round's K_r and causal domains as control words (K_r of every
+// request, then the domain of every (request, query)), after the checks
+// shared by dhs_select and dhs_adopt: a new round starts idle; after a
+// round's attention (before its commit) another layer of the same source
+// may select again (a Reindex consumer) with the same K_r.
+int round_words(dhs_ctx *c, const int32_t *k_per_req, const int64_t *pos,
+                std::vector<int32_t> &w, int &max_dom, int &active) {
   const DevCtx &d = c->d;
-  std::vector<int32_t> w(d.N + d.N * d.Kmax, 0);
-  int max_dom = 0;
+  if (c->phase != PH_IDLE && c->phase != PH_ATTENDED) return DHS_ERR_INVALID;
+  w.assign(d.N + d.N * d.Kmax, 0);
+  max_dom = 0;
+  active = 0;
   for (int r = 0; r < d.N; ++r) {
     const int kr = k_per_req[r];
     if (kr < 0 || kr > d.Kmax || (kr > 0 && !c->bound[r])) return DHS_ERR_INVALID;
+    if (c->phase == PH_ATTENDED && kr != c->K[r]) return DHS_ERR_INVALID;
+    active += kr;
   }
   for (int r = 0; r < d.N; ++r) {
     const int kr = k_per_req[r];
@@ -515,14 +654,27 @@ int select_impl(dhs_ctx *c, const int8_t *q_idx, const int8_t *q_inline,
       max_dom = std::max<int>(max_dom, (int)dom);
     }
   }
+  return DHS_OK;
+}
+
+int select_impl(dhs_ctx *c, const int8_t *q_idx, const int8_t *q_inline,
+                const int32_t *k_per_req, const int64_t *pos, int32_t *topk_out,
+                dhs_stream stream) {
+  if (c->role == DHS_ROLE_FOLLOWER) return DHS_ERR_INVALID;
+  const DevCtx &d = c->d;
+  std::vector<int32_t> w;
+  int max_dom = 0, active = 0;
+  if (int rc = round_words(c, k_per_req, pos, w, max_dom, active)) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (int rc = order_enter(c, s)) return rc;
   {
-    cudaError_t e_ = launch_select(d, q_idx, q_inline, topk_out, max_dom, w.data(), s, &c->timer);
+    cudaError_t e_ = launch_select(d, q_idx, q_inline, topk_out, max_dom, w.data(), active,
+                                   c->cfg.topk_pass, s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
   }
   for (int r = 0; r < d.N; ++r) c->K[r] = k_per_req[r];
   c->phase = PH_SELECTED;
-  return DHS_OK;
+  return order_leave(c, s);
 }
 }  // namespace
 
@@ -534,20 +686,58 @@ int dhs_select(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const 
   return select_impl(c, q_idx, nullptr, k_per_req, pos, topk_out, stream);
 }
 
+int dhs_adopt(dhs_ctx *c, const int32_t *k_per_req, const int64_t *pos, dhs_stream stream) {
+  if (!c || !k_per_req) return DHS_ERR_INVALID;
+  const DevCtx &d = c->d;
+  std::vector<int32_t> w;
+  int max_dom = 0, active = 0;
+  if (int rc = round_words(c, k_per_req, pos, w, max_dom, active)) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (int rc = order_enter(c, s)) return rc;
+  // K_r, then the domains, published by two ordinary launches: both have
+  // completed before the resolve's first kernel starts
+  {
+    cudaError_t e_ = launch_upload(d.Kr, w.data(), d.N, s);
+    if (e_ == cudaSuccess) {
+      std::vector<int32_t> dw(w.begin() + d.N, w.end());
+      if (upload_words(c, d.dom, dw, s)) return DHS_ERR_CUDA;
+    } else {
+      return cuda_fail(c, e_);
+    }
+  }
+  for (int r = 0; r < d.N; ++r) c->K[r] = k_per_req[r];
+  c->phase = PH_SELECTED;
+  (void)max_dom;
+  (void)active;
+  return order_leave(c, s);
+}
+
 int dhs_resolve(dhs_ctx *c, const int32_t *topk, int32_t *loc_out, int32_t shared,
                 dhs_stream stream) {
   if (!c || !topk || !loc_out || (shared != 0 && shared != 1)) return DHS_ERR_INVALID;
   if (c->phase != PH_SELECTED) return DHS_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  dhs_arenas *ar = c->arenas;
+  // the arena's previous user must have issued its attention before its
+  // staging rows can be replaced
+  if (ar && ar->owner[c->arena] && ar->owner[c->arena] != c && ar->unread[c->arena])
+    return DHS_ERR_INVALID;
+  if (c->tick + 1 > 0x7FFFFFF0) return DHS_ERR_CAPACITY;
+  if (int rc = order_enter(c, s)) return rc;
+  if (ar && cudaStreamWaitEvent(s, ar->released[c->arena], 0) != cudaSuccess)
+    return cuda_fail(c, cudaGetLastError());
   c->tick += 1;
-  if (c->tick > 0x7FFFFFF0) return DHS_ERR_CAPACITY;
   {
     cudaError_t e_ = launch_resolve(c->d, topk, loc_out, shared, 1, (int)c->tick, s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
   }
+  if (ar) {
+    ar->owner[c->arena] = c;
+    ar->unread[c->arena] = 1;
+  }
   c->last_shared = shared;
   c->phase = PH_RESOLVED;
-  return DHS_OK;
+  return order_leave(c, s);
 }
 
 int dhs_attend(dhs_ctx *c, const void *q, const void *block_kv, const int32_t *loc, void *out,
@@ -555,19 +745,30 @@ int dhs_attend(dhs_ctx *c, const void *q, const void *block_kv, const int32_t *l
   if (!c || !q || !block_kv || !loc || !out) return DHS_ERR_INVALID;
   if (!aligned16(block_kv) || ((uintptr_t)q & 3u) || ((uintptr_t)out & 3u))
     return DHS_ERR_INVALID;
-  if (c->phase != PH_RESOLVED) return DHS_ERR_INVALID;
+  // after a resolve, or again after an attend of the same resolve: a Reuse
+  // consumer of the same source and location vector
+  if (c->phase != PH_RESOLVED && c->phase != PH_ATTENDED) return DHS_ERR_INVALID;
+  if (c->arenas && c->arenas->owner[c->arena] != c) return DHS_ERR_INVALID;  // arena taken
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (int rc = order_enter(c, s)) return rc;
   {
     const uint16_t *q16 = static_cast<const uint16_t *>(q);
     const uint16_t *b16 = static_cast<const uint16_t *>(block_kv);
     uint16_t *o16 = static_cast<uint16_t *>(out);
-    cudaError_t e_ = (c->last_shared && c->fused)
-                         ? launch_uattn(c->d, q16, b16, o16, lse, s, &c->timer)
-                         : launch_attend(c->d, q16, b16, loc, o16, lse, c->n_split, s, &c->timer);
+    const bool tc = c->cfg.attn_pass == DHS_ATTN_UNION_TC && uattn_tc_supported(c->d);
+    cudaError_t e_ = !(c->last_shared && c->fused)
+                         ? launch_attend(c->d, q16, b16, loc, o16, lse, c->n_split, s, &c->timer)
+                     : tc ? launch_uattn_tc(c->d, q16, b16, o16, lse, s, &c->timer)
+                          : launch_uattn(c->d, q16, b16, o16, lse, s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
   }
+  if (c->arenas) {
+    if (cudaEventRecord(c->arenas->released[c->arena], s) != cudaSuccess)
+      return cuda_fail(c, cudaGetLastError());
+    c->arenas->unread[c->arena] = 0;
+  }
   c->phase = PH_ATTENDED;
-  return DHS_OK;
+  return order_leave(c, s);
 }
 
 int dhs_commit(dhs_ctx *c, const int32_t *accepted_len, dhs_stream stream) {
@@ -589,6 +790,7 @@ int dhs_commit(dhs_ctx *c, const int32_t *accepted_len, dhs_stream stream) {
     w[r * 4 + 3] = c->K[r] ? 1 : 0;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (int rc = order_enter(c, s)) return rc;
   {
     cudaError_t e_ = launch_commit(d, w.data(), s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
@@ -599,7 +801,7 @@ int dhs_commit(dhs_ctx *c, const int32_t *accepted_len, dhs_stream stream) {
     c->K[r] = 0;
   }
   c->phase = PH_IDLE;
-  return DHS_OK;
+  return order_leave(c, s);
 }
 
 int dhs_set_residency(dhs_ctx *c, int32_t slot, const int32_t *rows, int64_t n_rows,
@@ -618,6 +820,7 @@ int dhs_set_residency(dhs_ctx *c, int32_t slot, const int32_t *rows, int64_t n_r
     }
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (int rc = order_enter(c, s)) return rc;
   {
     cudaError_t e_ = launch_residency(c->d, slot, c->opt_count[slot], -1, s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
@@ -631,7 +834,7 @@ int dhs_set_residency(dhs_ctx *c, int32_t slot, const int32_t *rows, int64_t n_r
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
   }
   c->opt_count[slot] = n_rows;
-  return DHS_OK;
+  return order_leave(c, s);
 }
 
 int dhs_get_stats(dhs_ctx *c, dhs_stats *out, dhs_stream stream) {

@@ -194,14 +194,20 @@ __host__ __device__ inline int ctl_qidx_word(int N, int Kmax) { return (N + N * 
 cudaError_t launch_upload(int32_t *dst, const int32_t *words, int n, cudaStream_t s);
 // q_idx: device index rows, or nullptr with q_inline holding them on the host
 // (carried in the launch parameters; ctl_qidx_word + bytes/4 <= kUploadWords).
+// active_queries: sum of K_r this round; topk_pass: DHS_TOPK_* of the config.
 cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, const int8_t *q_inline,
                           int32_t *topk_out, int max_dom, const int32_t *ctl_words,
-                          cudaStream_t s, class Timer *tm);
+                          int active_queries, int topk_pass, cudaStream_t s, class Timer *tm);
 cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_out,
                            int shared, int gather, int tick, cudaStream_t s, class Timer *tm);
 cudaError_t launch_uattn(const DevCtx &c, const uint16_t *q, const uint16_t *block,
                          uint16_t *out, float *lse, cudaStream_t s, class Timer *tm);
 bool uattn_supported(const DevCtx &c);
+// The union pass on the fifth-generation tensor cores (128-dim heads, at most
+// 128 (query, head) pairs per kv head): one CTA per (request, kv head).
+bool uattn_tc_supported(const DevCtx &c);
+cudaError_t launch_uattn_tc(const DevCtx &c, const uint16_t *q, const uint16_t *block,
+                            uint16_t *out, float *lse, cudaStream_t s, class Timer *tm);
 size_t uattn_partial_floats(const DevCtx &c);
 cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *block,
                           const int32_t *loc, uint16_t *out, float *lse, int n_split,

@@ -1012,6 +1012,312 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
     for (int i = ksel + tid; i < k; i += kTopkThreads) out[i] = -1;
 }
 
+// ---------------------------------------------------------------- top-k, one CTA per query
+// For rounds with at least as many active queries as SMs: each (request,
+// query) is one CTA of kRowThreads threads with a 32 KB histogram and a
+// 32 KB candidate area, so several CTAs share an SM and one's passes over
+// global memory overlap another's placement.
+//  (1) exact radix select on the offset scores (13 bits a pass) over global
+//      memory, several 16-byte loads in flight per thread; the pass that
+//      resolves the last bits also counts the rows equal to the threshold T;
+//  (2) when the rows at or above T fit the candidate area, one more pass
+//      collects them.  If one pass resolved every bit (the scores span fewer
+//      than 2^13 values), each histogram bin is one score value: the bins at
+//      or above T become the first place of their value's group (rows above
+//      it), a collected row claims a place in its group, and its final place
+//      is the group's start plus the number of the group's rows below its own
+//      row -- the ordered list with no sort.  Otherwise the collected rows
+//      are sorted by (score descending, row ascending) with a bitonic network;
+//  (3) otherwise (many rows equal to T) the rows above T are collected and
+//      sorted the same way, and the lowest rows equal to T follow them, placed
+//      by an ordered pass in which each warp owns a contiguous run of rows.
+constexpr int kRowThreads = 512;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kRowCap = 4096;      // candidates: 4096 keys of 8 bytes
+constexpr int kRowUnroll = 4;      // 16-byte loads in flight per thread in a pass
+constexpr size_t kRowSmem = (size_t)kRowCap * 8 + ((size_t)1 << kRadixBits) * 4;
+static_assert(kMaxTopk <= kRowCap, "the rows above the threshold always fit the candidates");
+
+// Ascending bitonic sort of kp keys (a power of two) in shared memory.
+__device__ __forceinline__ void row_bitonic(unsigned long long *key, int kp) {
+  for (int size = 2; size <= kp; size <<= 1) {
+    for (int ls = __ffs(size) - 2; ls >= 0; --ls) {  // stride = 2^ls
+      const int stride = 1 << ls;
+      for (int i = threadIdx.x; i < (kp >> 1); i += kRowThreads) {
+        const int a = ((i >> ls) << (ls + 1)) | (i & (stride - 1)), b = a + stride;
+        const bool asc = (a & size) == 0;
+        const unsigned long long x = key[a], y = key[b];
+        if ((x > y) == asc) {
+          key[a] = y;
+          key[b] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kRowThreads, 3)
+k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned long long *cand = reinterpret_cast<unsigned long long *>(smem);
+  uint32_t *hist = reinterpret_cast<uint32_t *>(smem + (size_t)kRowCap * 8);
+  __shared__ int warp_sums[32];
+  __shared__ int wcnt[kRowWarps];
+  __shared__ int sh_bin, sh_above, sh_eq, sh_cnt;
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x / c.Kmax, j = blockIdx.x % c.Kmax;
+  if (j >= c.Kr[r]) return;
+  const int dom = c.dom[r * c.Kmax + j];
+  int32_t *mm = c.minmax + (r * c.Kmax + j) * 2;
+  const int lo = mm[0], hi = mm[1];
+  const int k = c.k;
+  const int32_t *__restrict__ sc = c.scores + ((size_t)r * c.Kmax + j) * c.Ss;
+  int32_t *out = topk_out + ((size_t)r * c.Kmax + j) * k;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int ksel = min(k, dom);
+  if (tid == 0) sh_cnt = 0;
+  __syncthreads();  // every thread has read the range: empty it for the next round
+  if (tid == 0) {
+    mm[0] = INT_MAX;
+    mm[1] = INT_MIN;
+  }
+  for (int i = ksel + tid; i < k; i += kRowThreads) out[i] = -1;
+  if (dom <= 0) return;
+  // (a score row is padded to a multiple of 32 entries, so a 16-byte load at
+  // any multiple of 4 below dom stays inside it; entries past dom are masked)
+  auto load4 = [&](int s) -> int4 { return __ldg(reinterpret_cast<const int4 *>(sc + s)); };
+  // Every row whose offset value passes keep(v), claimed in any order into
+  // cand[] as (~v << 32 | row); returns nothing, sh_cnt counts them.
+  auto collect = [&](auto keep) {
+    for (int s0 = wid * 128; s0 < dom; s0 += kRowWarps * 128) {
+      const int s = s0 + 4 * lane;
+      int4 x = make_int4(0, 0, 0, 0);
+      if (s < dom) x = load4(s);
+      const int xv[4] = {x.x, x.y, x.z, x.w};
+      bool kp4[4];
+      int n = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kp4[e] = s + e < dom && keep((uint32_t)(xv[e] - lo));
+        n += kp4[e];
+      }
+      const unsigned any = __ballot_sync(0xffffffffu, n > 0);
+      if (!any) continue;
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int base = 0;
+      if (lane == 31) base = atomicAdd(&sh_cnt, incl);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      int pos = base + incl - n;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (!kp4[e]) continue;
+        if (pos < kRowCap)
+          cand[pos] = ((unsigned long long)(0xFFFFFFFFu - (uint32_t)(xv[e] - lo)) << 32) |
+                      (uint32_t)(s + e);
+        else
+          record_error(c.err, DC_CAPACITY, K_TOPK);
+        ++pos;
+      }
+    }
+  };
+  // sort the n collected keys and write the first `m` rows to out[o0..)
+  auto sort_out = [&](int n, int o0, int m) {
+    int kp = 1;
+    while (kp < n) kp <<= 1;
+    for (int i = n + tid; i < kp; i += kRowThreads) cand[i] = ~0ull;
+    __syncthreads();
+    row_bitonic(cand, kp);
+    for (int i = tid; i < m; i += kRowThreads)
+      out[o0 + i] = (int32_t)(uint32_t)(cand[i] & 0xFFFFFFFFull);
+  };
+
+  if (dom <= k) {  // every row of the domain is kept, in order
+    collect([](uint32_t) { return true; });
+    __syncthreads();
+    sort_out(dom, 0, dom);
+    return;
+  }
+  const uint32_t range = (uint32_t)(hi - lo);
+  int shift = range ? 32 - __clz((int)range) : 0;
+  uint32_t prefix = 0;
+  int k_rem = k;
+  int n_eq = dom;  // rows equal to T (all of them when every score is equal)
+  bool first = true;
+  int passes = 0;
+  while (shift > 0) {
+    ++passes;
+    const int width = min(kRadixBits, shift);
+    shift -= width;
+    const int nbins = 1 << width;
+    for (int i = tid; i < nbins; i += kRowThreads) hist[i] = 0;
+    __syncthreads();
+    const int hs = shift + width;
+    for (int s0 = wid * 128; s0 < dom; s0 += kRowWarps * 128 * kRowUnroll) {
+      int4 x[kRowUnroll];
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int s = s0 + u * kRowWarps * 128 + 4 * lane;
+        if (s < dom) x[u] = load4(s);
+      }
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int s = s0 + u * kRowWarps * 128 + 4 * lane;
+        const int xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (s + e >= dom) continue;
+          const uint32_t v = (uint32_t)(xv[e] - lo);
+          if (first || (uint32_t)((unsigned long long)v >> hs) == prefix)
+            atomicAdd(&hist[(v >> shift) & (nbins - 1)], 1u);
+        }
+      }
+    }
+    __syncthreads();
+    // thread t owns a run of bins counted from the top; an exclusive scan in
+    // thread order counts the rows above each run
+    const int per = (nbins + kRowThreads - 1) / kRowThreads;
+    const int b_hi = nbins - tid * per;
+    const int b_lo = max(0, b_hi - per);
+    int local = 0;
+    for (int b = b_lo; b < b_hi; ++b) local += (int)hist[b];
+    int total;
+    const int above = block_excl_scan(local, warp_sums, total);
+    if (local > 0 && above < k_rem && k_rem <= above + local) {
+      int acc = above;
+      for (int b = b_hi - 1; b >= b_lo; --b) {
+        const int g = (int)hist[b];
+        if (acc + g >= k_rem) {
+          sh_bin = b;
+          sh_above = acc;
+          sh_eq = g;
+          break;
+        }
+        acc += g;
+      }
+    }
+    __syncthreads();
+    const int thr_bin = sh_bin;
+    k_rem -= sh_above;
+    prefix = (prefix << width) | (uint32_t)thr_bin;
+    n_eq = sh_eq;
+    first = false;
+    if (passes == 1 && shift == 0 && (uint32_t)b_hi > (uint32_t)thr_bin) {
+      // exact bins: bin b >= T becomes the first place of value b's group,
+      // the rows of the domain above b (this thread's run, from its top)
+      int acc = above;
+      for (int b = b_hi - 1; b >= max(b_lo, thr_bin); --b) {
+        const int g = (int)hist[b];
+        hist[b] = (uint32_t)acc;
+        acc += g;
+      }
+    }
+    __syncthreads();  // the histogram may be reused (or holds the group starts)
+  }
+  const uint32_t T = prefix;  // the k-th largest offset score
+  const int need = k_rem;     // rows equal to T that are kept
+  const int c_gt = k - need;  // rows strictly above T
+  if (c_gt + n_eq <= kRowCap && passes == 1 && shift == 0) {
+    // claim a place in the value's group, in any order ...
+    for (int s0 = wid * 128; s0 < dom; s0 += kRowWarps * 128) {
+      const int s = s0 + 4 * lane;
+      if (s >= dom) continue;
+      const int4 x = load4(s);
+      const int xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t v = (uint32_t)(xv[e] - lo);
+        if (s + e < dom && v >= T) {
+          const uint32_t p = atomicAdd(&hist[v], 1u);
+          if (p < (uint32_t)kRowCap)
+            cand[p] = ((unsigned long long)v << 32) | (uint32_t)(s + e);
+          else
+            record_error(c.err, DC_CAPACITY, K_TOPK);
+        }
+      }
+    }
+    __syncthreads();
+    // ... then its place: the group's start plus the group's rows below it
+    const int n = c_gt + n_eq;
+    for (int p = tid; p < n; p += kRowThreads) {
+      const unsigned long long me = cand[p];
+      const uint32_t v = (uint32_t)(me >> 32), row = (uint32_t)me;
+      int left = 0, below = 0;
+      for (int q = p - 1; q >= 0 && (uint32_t)(cand[q] >> 32) == v; --q) {
+        ++left;
+        below += (uint32_t)cand[q] < row;
+      }
+      for (int q = p + 1; q < n && (uint32_t)(cand[q] >> 32) == v; ++q)
+        below += (uint32_t)cand[q] < row;
+      const int fin = p - left + below;
+      if (fin < k) out[fin] = (int32_t)row;
+    }
+    return;
+  }
+  if (c_gt + n_eq <= kRowCap) {
+    collect([T](uint32_t v) { return v >= T; });
+    __syncthreads();
+    if (sh_cnt != c_gt + n_eq) record_error(c.err, DC_CAPACITY, K_TOPK);
+    sort_out(min(sh_cnt, kRowCap), 0, k);
+    return;
+  }
+  // many rows equal to T: the rows above it first ...
+  collect([T](uint32_t v) { return v > T; });
+  __syncthreads();
+  if (sh_cnt != c_gt) record_error(c.err, DC_CAPACITY, K_TOPK);
+  if (c_gt > 0) sort_out(min(sh_cnt, kRowCap), 0, c_gt);
+  // ... then the lowest `need` rows equal to T, in row order: warp w owns
+  // rows [w * run, (w + 1) * run); count, scan the warps' counts, place
+  const int run = ((dom + kRowWarps - 1) / kRowWarps + 127) & ~127;
+  const int r0 = min(dom, wid * run), r1 = min(dom, r0 + run);
+  int eq_lane = 0;
+  for (int s = r0 + 4 * lane; s < r1; s += 128) {
+    const int4 x = load4(s);
+    const int xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) eq_lane += s + e < r1 && (uint32_t)(xv[e] - lo) == T;
+  }
+  const int weq = (int)__reduce_add_sync(0xffffffffu, (unsigned)eq_lane);
+  if (lane == 0) wcnt[wid] = weq;
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < wid; ++w) wbase += wcnt[w];
+  if (wbase < need) {
+    const unsigned lt = (1u << lane) - 1u;
+    for (int s0 = r0; s0 < r1 && wbase < need; s0 += 128) {
+      const int s = s0 + 4 * lane;
+      int4 x = make_int4(0, 0, 0, 0);
+      if (s < r1) x = load4(s);
+      const int xv[4] = {x.x, x.y, x.z, x.w};
+      bool eq[4];
+      unsigned bal[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        eq[e] = s + e < r1 && (uint32_t)(xv[e] - lo) == T;
+        bal[e] = __ballot_sync(0xffffffffu, eq[e]);
+      }
+      // row order: every equal row of the lanes below, then the lane's own
+      int pos = wbase;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pos += __popc(bal[e] & lt);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (!eq[e]) continue;
+        if (pos < need) out[c_gt + pos] = s + e;
+        ++pos;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) wbase += __popc(bal[e]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- scores on tensor cores
 // Rows of 64 * NG bytes (NG = 1..8).  The score of eq. (1) is an exact
 // integer dot product, and so is this kernel's: every int8 value becomes the
@@ -1261,7 +1567,7 @@ k_index_score_tc(const DevCtx c, const int8_t *__restrict__ q_idx,
 
 cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, const int8_t *q_inline,
                           int32_t *topk_out, int max_dom, const int32_t *ctl_words,
-                          cudaStream_t s, Timer *tm) {
+                          int active_queries, int topk_pass, cudaStream_t s, Timer *tm) {
   UploadWords ctl;
   const int nw = c.N + c.N * c.Kmax;
   for (int i = 0; i < nw; ++i) ctl.w[i] = ctl_words[i];
@@ -1334,6 +1640,16 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, const int8_t *q_
     e = launch_pdl(kern, grid, dim3(kScoreThreads), smem, s, c, q_idx, ctl);
     if (tm) tm->end(K_SCORE, s);
     if (e != cudaSuccess) return e;
+  }
+  if (topk_pass == DHS_TOPK_ROW || (topk_pass == DHS_TOPK_AUTO && active_queries >= c.sms)) {
+    static size_t granted_row = 0;
+    const size_t smem_row = kRowSmem;
+    cudaError_t e3 = ensure_smem(k_topk_row, smem_row, granted_row);
+    if (e3 != cudaSuccess) return e3;
+    if (tm) tm->begin(K_TOPK, s);
+    e3 = launch_pdl(k_topk_row, dim3(c.N * c.Kmax), dim3(kRowThreads), smem_row, s, c, topk_out);
+    if (tm) tm->end(K_TOPK, s);
+    return e3;
   }
   int kp = 1;
   while (kp < c.k) kp <<= 1;

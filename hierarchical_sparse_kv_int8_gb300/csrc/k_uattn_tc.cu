@@ -1,0 +1,381 @@
+// Step 5 for shared retrieval, 128-dim heads, on the fifth-generation tensor
+// cores: the attention of all K_r queries of a request in one pass over the
+// union of their selections.
+//
+// "Adaptive DHiSparse", eq. (6) and Fig. 3 callout 2: each distinct row of the
+// union U_r is read once per round, whichever queries selected it; eq. (1),
+// (5): query j attends over its own selection S_{r,j} and the block rows
+// n_r .. n_r + j.  Visiting U_r once and keeping a row's score only for the
+// queries that selected it gives each query exactly its own rows.
+//
+// One CTA per (request, kv head).  Its M = K_max x G (query, head) pairs are
+// the 128 lanes of tensor memory (padded), one lane per pair; the walk (U_r in
+// ascending row order, then the K_r block rows) is cut into tiles of kTcN
+// rows.  Per tile: S = Q K^T (M = 128, N = kTcN, K = 128) into one of two
+// tensor-memory buffers; each softmax thread reads its lane's kTcN scores,
+// masks them by the queries that selected each row, keeps a running maximum
+// in log2 units (the output is rescaled only when the maximum grows by more
+// than kTcRescale, so the exponentials stay below 2^kTcRescale) and writes
+// its row of P (bf16) to shared memory; then O += P V (M = 128, N = 128, K =
+// kTcN) accumulates in tensor memory.  Warp roles: warps 0-3 are the softmax
+// threads (warp w owns lanes 32w..32w+31), one thread of warp 4 issues every
+// MMA, warps 5-7 copy rows into a ring of kTcStages stages with 16-byte
+// cp.async from wherever the union/probe located them (hot cache, optional
+// pool, draft ring, staging) or from the caller's block rows, which they also
+// write to the draft ring.  The stages, S buffers and P buffers are handed
+// between the roles with mbarriers (MMA completion arrives through
+// tcgen05.commit); every wait is bounded and, when it runs out, records a
+// device error and lets the CTA finish, so tensor memory is always freed.
+#include "dhs_internal.cuh"
+#include "ptx_util.cuh"
+#include "tc_util.cuh"
+
+#include <math_constants.h>
+
+namespace dhs {
+namespace {
+
+constexpr int kTcM = 128;              // (query, head) pairs: tensor-memory lanes
+constexpr int kTcD = 128;              // key and value dims
+constexpr int kTcN = 64;               // walk rows per tile
+constexpr int kTcStages = 4;
+constexpr int kTcThreads = 256;
+constexpr int kTcSoftmax = 128;        // warps 0-3
+constexpr int kTcMmaWarp = 4;
+constexpr int kTcLoadWarp0 = 5;        // warps 5-7 copy
+constexpr int kTcLoaders = 96;
+constexpr uint32_t kTcCols = 256;      // S: two buffers of kTcN columns; O: 128 columns
+constexpr uint32_t kTcColO = 128;
+constexpr int kTcSpin = 1 << 20;
+constexpr float kTcRescale = 8.f;
+
+// Shared memory.  Operands use the core-matrix layouts of tc_util.cuh.
+//   Q: K-major, cores along K 128 B apart, 8-row groups 2048 B apart
+//   stage: keys (K-major, as Q) then values (MN-major: cores along the value
+//          dims 128 B apart, groups of 8 walk rows 2048 B apart)
+//   P: K-major over the tile's rows, cores 128 B apart, 8-row groups 1024 B
+constexpr int kOffQ = 0;
+constexpr int kQBytes = kTcM * kTcD * 2;
+constexpr int kOffStage = kOffQ + kQBytes;
+constexpr int kKBytes = kTcN * kTcD * 2;
+constexpr int kStageBytes = 2 * kKBytes;
+constexpr int kOffP = kOffStage + kTcStages * kStageBytes;
+constexpr int kPBytes = kTcM * kTcN * 2;
+constexpr int kOffMask = kOffP + 2 * kPBytes;
+constexpr int kOffBar = kOffMask + kTcStages * kTcN * 4;
+constexpr int kNumBars = kTcStages * 2 + 2 * 4 + 1;
+constexpr int kOffTmem = kOffBar + kNumBars * 8;
+constexpr int kTcSmem = kOffTmem + 16;
+static_assert(kTcSmem <= (int)kMaxDynSmem, "shared memory of the tensor-core union pass");
+
+constexpr uint32_t kIdescQK = tc_idesc_bf16(kTcM, kTcN, 0, 0);
+constexpr uint32_t kIdescPV = tc_idesc_bf16(kTcM, kTcD, 0, 1);
+
+__device__ __forceinline__ int kmaj(int row, int chunk, int sbo) {
+  return (row >> 3) * sbo + chunk * 128 + (row & 7) * 16;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restrict__ block,
+           uint16_t *__restrict__ out, float *__restrict__ lse) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  __shared__ int abort_flag;
+  const int item = blockIdx.x;
+  const int r = item / c.Hkv, kvh = item - r * c.Hkv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  uint64_t *full = bars, *empty = bars + kTcStages;
+  uint64_t *s_full = bars + 2 * kTcStages, *s_free = s_full + 2, *p_full = s_full + 4,
+           *pv_done = s_full + 6, *o_done = s_full + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmem);
+  volatile int *abort_v = &abort_flag;
+
+  // everything earlier launches wrote (control words, union entries,
+  // staging rows) and the caller's queries and block rows
+  pdl_wait();
+  pdl_trigger();
+  const int Kr = c.Kr[r];
+  if (Kr == 0) return;
+
+  if (tid == 0) {
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&full[i], kTcLoaders + kTcN);  // every copy thread's copies, every row's mask
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], kTcSoftmax);
+      mbar_init(&p_full[i], kTcSoftmax);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(o_done, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == kTcMmaWarp) tmem_alloc(tmem_slot, kTcCols);
+
+  const int G = c.Hq / c.Hkv, Mq = c.Kmax * G;
+  const int KK = c.Kmax * c.k;
+  const int U = c.counts[r * 4 + 0];
+  const int L = U + Kr;  // union rows, then block rows
+  const int T = (L + kTcN - 1) / kTcN;
+  const int64_t n = c.n[r];
+  const uint16_t *brow = block + (size_t)r * c.Kmax * c.row;
+
+  // query tile: lane m is query m / G, head m % G of this kv head
+  for (int idx = tid; idx < kTcM * (kTcD / 8); idx += kTcThreads) {
+    const int m = idx >> 4, ch = idx & 15;
+    const int j = m / G;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (m < Mq && j < Kr)
+      v = *reinterpret_cast<const uint4 *>(
+          q + (((size_t)r * c.Kmax + j) * c.Hq + (size_t)kvh * G + (m - j * G)) * kTcD + ch * 8);
+    *reinterpret_cast<uint4 *>(smem + kOffQ + kmaj(m, ch, 2048)) = v;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // (force: keep waiting after another thread gave up -- used for the
+  // completion of the MMAs before tensor memory is freed)
+  auto wait = [&](uint64_t *bar, uint32_t parity, bool force = false) {
+    int spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+      if (!force && *abort_v) return;
+      if (++spins > kTcSpin) {
+        record_error(c.err, DC_TIMEOUT, K_ATTN_UNION);
+        *abort_v = 1;
+        return;
+      }
+    }
+  };
+
+  if (warp >= kTcLoadWarp0) {
+    // ---------------------------------------------------------------- copies
+    const int lw = warp - kTcLoadWarp0;
+    // the block rows go into their draft-ring slots (this kv head's parts)
+    for (int i = lw; i < Kr; i += 3) {
+      const int off = lane < 16 ? kvh * kTcD + lane * 8 : c.Hkv * kTcD + kvh * kTcD + (lane - 16) * 8;
+      const uint4 v = *reinterpret_cast<const uint4 *>(brow + (size_t)i * c.row + off);
+      *reinterpret_cast<uint4 *>(c.ring + ((size_t)r * c.Rd + (n + i) % c.Rd) * c.row + off) = v;
+    }
+    const int4 *uent = c.uent + (size_t)r * KK;
+    const uint32_t all_q = (1u << Kr) - 1u;
+    // lane l of copy warp lw holds the union entry of row lw + 3 l of a
+    // tile: loaded one tile ahead, turned into a source address when its
+    // tile is issued.  A stage is complete when every copy thread's copies
+    // have landed (asynchronous arrivals) and every row's query mask is
+    // written (an ordinary arrival by the lane that wrote it).
+    const int li = lw + 3 * lane;
+    int4 nent = make_int4(0, 0, 0, 0);
+    auto fetch = [&](int t) {
+      const int e = t * kTcN + li;
+      if (li < kTcN && e < U) nent = uent[e];
+    };
+    fetch(0);
+    const int off = lane < 16 ? kvh * kTcD + lane * 8 : c.Hkv * kTcD + kvh * kTcD + (lane - 16) * 8;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % kTcStages;
+      const int4 ent = nent;
+      if (t + 1 < T) fetch(t + 1);
+      const uint16_t *tsrc = nullptr;
+      uint32_t tmask = 0u;
+      {
+        const int e = t * kTcN + li;
+        if (li < kTcN && e < U) {
+          tsrc = loc_row(c, r, ent.y);
+          if (tsrc == nullptr) record_error(c.err, DC_LOC_RANGE, K_ATTN_UNION);
+          tmask = (uint32_t)ent.z;
+        } else if (li < kTcN && e < L) {
+          tsrc = brow + (size_t)(e - U) * c.row;
+          tmask = all_q & ~((1u << (e - U)) - 1u);
+        }
+      }
+      if (t >= kTcStages) wait(&empty[s], (uint32_t)(((t / kTcStages) - 1) & 1));
+      unsigned char *kst = smem + kOffStage + s * kStageBytes, *vst = kst + kKBytes;
+      uint32_t *msk = reinterpret_cast<uint32_t *>(smem + kOffMask) + s * kTcN;
+      for (int it = 0; it * 3 + lw < kTcN; ++it) {
+        const int i = lw + 3 * it;
+        const uint16_t *src = reinterpret_cast<const uint16_t *>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(tsrc), it));
+        unsigned char *dst = lane < 16 ? kst + kmaj(i, lane, 2048) : vst + kmaj(i, lane - 16, 2048);
+        cp_async_16_zfill(dst, src ? (const void *)(src + off) : (const void *)c.ring, src ? 16 : 0);
+      }
+      cp_async_arrive_noinc(&full[s]);
+      if (li < kTcN) {
+        msk[li] = tsrc ? tmask : 0u;
+        mbar_arrive(&full[s]);
+      }
+    }
+  } else if (warp == kTcMmaWarp) {
+    // ---------------------------------------------------------------- MMAs
+    if (lane == 0) {
+      const uint32_t sQ = smem_u32(smem + kOffQ);
+      auto pv = [&](int u) {
+        const int b = u & 1, s = u % kTcStages;
+        wait(&p_full[b], (uint32_t)((u >> 1) & 1));
+        tc_fence_after();
+        const uint32_t sP = smem_u32(smem + kOffP + b * kPBytes);
+        const uint32_t sV = smem_u32(smem + kOffStage + s * kStageBytes + kKBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTcN / 16; ++kk)
+          tc_mma(tmem + kTcColO, tc_desc(sP + kk * 256, 128, 1024),
+                 tc_desc(sV + kk * 4096, 2048, 128), kIdescPV, (u > 0 || kk > 0) ? 1 : 0);
+        tc_commit(&pv_done[b]);
+        tc_commit(&empty[s]);
+      };
+      for (int t = 0; t < T; ++t) {
+        const int s = t % kTcStages, b = t & 1;
+        wait(&full[s], (uint32_t)((t / kTcStages) & 1));
+        fence_proxy_async_smem();  // the stage's copies, seen by the tensor cores
+        if (t >= 2) wait(&s_free[b], (uint32_t)(((t - 2) >> 1) & 1));
+        tc_fence_after();
+        const uint32_t sK = smem_u32(smem + kOffStage + s * kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTcD / 16; ++kk)
+          tc_mma(tmem + (uint32_t)(b * kTcN), tc_desc(sQ + kk * 256, 128, 2048),
+                 tc_desc(sK + kk * 256, 128, 2048), kIdescQK, kk > 0 ? 1 : 0);
+        tc_commit(&s_full[b]);
+        if (t >= 1) pv(t - 1);
+      }
+      pv(T - 1);
+      tc_commit(o_done);
+      wait(o_done, 0u, true);  // every MMA has completed before tensor memory is freed
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- softmax
+    const int m = tid;
+    const int j = m / G;
+    const bool valid = m < Mq && j < Kr;
+    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    const float sl2 = c.scale_log2;
+    float m_run = -CUDART_INF_F, l = 0.f;
+    for (int t = 0; t < T; ++t) {
+      const int b = t & 1, s = t % kTcStages;
+      wait(&s_full[b], (uint32_t)((t >> 1) & 1));
+      wait(&full[s], (uint32_t)((t / kTcStages) & 1));  // the tile's masks
+      tc_fence_after();
+      uint32_t sv[kTcN];
+      {
+        uint32_t a[32], bb[32];
+        tmem_ld32(tmem + lrow + (uint32_t)(b * kTcN), a);
+        tmem_ld32(tmem + lrow + (uint32_t)(b * kTcN + 32), bb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          sv[i] = a[i];
+          sv[32 + i] = bb[i];
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[b]);
+      const uint32_t *msk = reinterpret_cast<const uint32_t *>(smem + kOffMask) + s * kTcN;
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int i = 0; i < kTcN; ++i) {
+        const bool keep = valid && ((msk[i] >> j) & 1u);
+        const float x = keep ? __uint_as_float(sv[i]) * sl2 : -CUDART_INF_F;
+        sv[i] = __float_as_uint(x);
+        mx = fmaxf(mx, x);
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const bool need = m_new > m_run + kTcRescale;  // false while nothing is kept
+      if (__any_sync(0xffffffffu, need) && t >= 1) {
+        // rescale this lane's output after the previous tile's P V completed
+        wait(&pv_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1));
+        tc_fence_after();
+        const float f = need ? exp2f(m_run - m_new) : 1.f;
+#pragma unroll
+        for (int cc = 0; cc < kTcD; cc += 32) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lrow + kTcColO + (uint32_t)cc, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+          tmem_st32(tmem + lrow + kTcColO + (uint32_t)cc, ov);
+        }
+        tmem_wait_st();
+      }
+      if (need) {
+        l *= exp2f(m_run - m_new);
+        m_run = m_new;
+      }
+      // P_t replaces P_{t-2}: its P V must have completed
+      if (t >= 2) wait(&pv_done[b], (uint32_t)(((t - 2) >> 1) & 1));
+      unsigned char *prow = smem + kOffP + b * kPBytes + (m >> 3) * 1024 + (m & 7) * 16;
+      const bool live = m_run != -CUDART_INF_F;
+#pragma unroll
+      for (int ch = 0; ch < kTcN / 8; ++ch) {
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          p[i] = live ? exp2f(__uint_as_float(sv[ch * 8 + i]) - m_run) : 0.f;
+          l += p[i];
+        }
+        uint4 w;
+        w.x = pack_bf16(p[0], p[1]);
+        w.y = pack_bf16(p[2], p[3]);
+        w.z = pack_bf16(p[4], p[5]);
+        w.w = pack_bf16(p[6], p[7]);
+        *reinterpret_cast<uint4 *>(prow + ch * 128) = w;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[b]);
+    }
+    // output: O / l, and the natural-log sum-exp
+    wait(o_done, 0u);
+    tc_fence_after();
+    const int h = kvh * G + (m - j * G);
+    uint16_t *orow = valid ? out + (((size_t)r * c.Kmax + j) * c.Hq + h) * kTcD : nullptr;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int cc = 0; cc < kTcD; cc += 32) {
+      uint32_t ov[32];
+      tmem_ld32(tmem + lrow + kTcColO + (uint32_t)cc, ov);
+      tmem_wait_ld();
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(ov[i + 0]) * inv, __uint_as_float(ov[i + 1]) * inv);
+          w.y = pack_bf16(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+          w.z = pack_bf16(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
+          w.w = pack_bf16(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
+          *reinterpret_cast<uint4 *>(orow + cc + i) = w;
+        }
+      }
+    }
+    if (valid && lse)
+      lse[((size_t)r * c.Kmax + j) * c.Hq + h] =
+          l > 0.f ? (m_run + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kTcMmaWarp) tmem_dealloc(tmem, kTcCols);
+}
+
+}  // namespace
+
+bool uattn_tc_supported(const DevCtx &c) {
+  return c.dqk == kTcD && c.dv == kTcD && c.layout == DHS_KV_SPLIT &&
+         c.Kmax * (c.Hq / c.Hkv) <= kTcM;
+}
+
+cudaError_t launch_uattn_tc(const DevCtx &c, const uint16_t *q, const uint16_t *block,
+                            uint16_t *out, float *lse, cudaStream_t s, Timer *tm) {
+  static size_t granted = 0;
+  cudaError_t e = ensure_smem(k_uattn_tc, (size_t)kTcSmem, granted);
+  if (e != cudaSuccess) return e;
+  if (tm) tm->begin(K_ATTN_UNION, s);
+  e = launch_pdl(k_uattn_tc, dim3(c.N * c.Hkv), dim3(kTcThreads), (size_t)kTcSmem, s, c, q,
+                 block, out, lse);
+  if (tm) tm->end(K_ATTN_UNION, s);
+  return e;
+}
+
+}  // namespace dhs

@@ -14,35 +14,43 @@ from . import Context, make_config
 
 
 def config_for(rec, k_max: Optional[int] = None, opt_rows_max: Optional[int] = None,
-               attn_pass: int = 0):
+               attn_pass: int = 0, topk_pass: int = 0):
     return make_config(
         n_slots=rec.N, k_max=k_max or rec.kmax, topk=rec.topk, s_max=rec.s_max,
         idx_heads=rec.H_idx, idx_dim=rec.d_idx, q_heads=rec.Hq, kv_heads=rec.Hkv,
         qk_dim=rec.qk_dim, v_dim=rec.v_dim, kv_layout=rec.kv_layout, budget=rec.B,
         ring_window=rec.W, page_rows=rec.p,
         opt_rows_max=rec.opt_rows_max if opt_rows_max is None else opt_rows_max,
-        softmax_scale=0.0, attn_pass=attn_pass)
+        softmax_scale=0.0, attn_pass=attn_pass, topk_pass=topk_pass)
 
 
 class Runner:
     def __init__(self, rec, k_max: Optional[int] = None, opt_rows_max: Optional[int] = None,
-                 stream=None, attn_pass: int = 0):
+                 stream=None, attn_pass: int = 0, topk_pass: int = 0, arenas=None, arena: int = 0,
+                 role: int = 0, keys=None):
+        """``arenas``/``arena``/``role``: a source of a layer group staging in a
+        shared arena (a follower takes positions from a producer).  ``keys``:
+        device index keys to bind instead of generating them (a follower
+        never reads them)."""
         import torch
         self.torch = torch
         self.rec = rec
-        self.cfg = config_for(rec, k_max, opt_rows_max, attn_pass)
+        self.cfg = config_for(rec, k_max, opt_rows_max, attn_pass, topk_pass)
         self.Km = self.cfg.k_max
-        self.ctx = Context(self.cfg)
+        self.ctx = Context(self.cfg, arenas, arena, role)
         self.stream = stream
         N, Sm, row = rec.N, rec.s_max, rec.row_elems
         self.host = torch.empty((N, Sm, row), dtype=torch.int16, pin_memory=True)
         rec.host_rows_into(self.host, 0, N)
         dev = torch.device("cuda")
-        self.keys = torch.empty((N, Sm, rec.idx_row), dtype=torch.int8, device=dev)
-        chunk = max(1, (1 << 30) // max(1, Sm * rec.idx_row))
-        for r0 in range(0, N, chunk):
-            r1 = min(N, r0 + chunk)
-            self.keys[r0:r1].copy_(torch.from_numpy(rec.index_keys(r0, r1)))
+        if keys is not None:
+            self.keys = keys
+        else:
+            self.keys = torch.empty((N, Sm, rec.idx_row), dtype=torch.int8, device=dev)
+            chunk = max(1, (1 << 30) // max(1, Sm * rec.idx_row))
+            for r0 in range(0, N, chunk):
+                r1 = min(N, r0 + chunk)
+                self.keys[r0:r1].copy_(torch.from_numpy(rec.index_keys(r0, r1)))
         Km = self.Km
         self.q_idx = torch.zeros((N, Km, rec.idx_row), dtype=torch.int8, device=dev)
         self.q = torch.zeros((N, Km, rec.Hq, rec.qk_dim), dtype=torch.int16, device=dev)
@@ -78,6 +86,11 @@ class Runner:
 
     def select(self, k_per_req, pos=None):
         self.ctx.select(self.q_idx, k_per_req, self.topk, pos, self.stream)
+
+    def adopt(self, k_per_req, topk, pos=None):
+        """Take a producer's selection (its top-k tensor) for this round."""
+        self.topk = topk
+        self.ctx.adopt(k_per_req, pos, self.stream)
 
     def resolve(self, shared=True):
         self.ctx.resolve(self.topk, self.loc, shared, self.stream)

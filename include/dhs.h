@@ -105,7 +105,17 @@ typedef struct {
   int64_t opt_rows_max; /* optional-pool rows per request (0 = no optional map) */
   float softmax_scale;  /* 0 = 1/sqrt(qk_dim)                                   */
   int32_t attn_pass;    /* attention kernel for shared retrieval, DHS_ATTN_*    */
+  int32_t topk_pass;    /* top-k kernel of dhs_select, DHS_TOPK_*               */
 } dhs_config;
+
+/* Top-k kernel of dhs_select.  Both return the same ordered lists:
+ *   CLUSTER: a cluster of four CTAs per query, the query's scores staged in
+ *            their shared memory; spreads few queries over many SMs.
+ *   ROW    : one CTA per query with a small footprint, several per SM, the
+ *            scores read from global memory; for rounds with many queries.
+ *   AUTO   : ROW when the round's active queries (sum of K_r) are at least
+ *            the device's SM count, else CLUSTER. */
+enum { DHS_TOPK_AUTO = 0, DHS_TOPK_CLUSTER = 1, DHS_TOPK_ROW = 2 };
 
 /* Attention kernel used after a shared dhs_resolve (per-query resolution
  * always uses the per-query pass).  Both compute eq. (5) for every query; they
@@ -115,10 +125,15 @@ typedef struct {
  *   UNION    : each (request, kv head) streams the union U_r once and masks
  *              every score by the queries that selected the row; up to K_r
  *              times fewer row reads, best when the round is bound by HBM.
+ *              The product tiles run on mma.sync.
+ *   UNION_TC : the union pass on the fifth-generation tensor cores (tcgen05
+ *              MMAs, scores and output accumulated in tensor memory, one CTA
+ *              per (request, kv head)); 128-dim heads with at most 128
+ *              (query, head) pairs per kv head, else as UNION.
  *   AUTO     : UNION for 128-dim heads when the per-query pass would stream
  *              more than 128 MiB of rows per round (n_slots * k_max *
  *              (topk + k_max) rows), else PER_QUERY (always for latent rows). */
-enum { DHS_ATTN_AUTO = 0, DHS_ATTN_PER_QUERY = 1, DHS_ATTN_UNION = 2 };
+enum { DHS_ATTN_AUTO = 0, DHS_ATTN_PER_QUERY = 1, DHS_ATTN_UNION = 2, DHS_ATTN_UNION_TC = 3 };
 
 /* Cumulative counters since dhs_create (or dhs_reset_stats). */
 typedef struct {
@@ -176,7 +191,9 @@ int dhs_bind_request(dhs_ctx *ctx, int32_t slot, const void *host_kv, const int8
  *   topk_out   device int32 [n_slots][k_max][topk]: rows ordered by score
  *              descending, ties to the lower row, padded with -1.  Entries of
  *              idle queries are left untouched.
- * Score I[s] = sum_h sum_d q[h][d] * K[s][h][d] in exact int32 arithmetic. */
+ * Score I[s] = sum_h sum_d q[h][d] * K[s][h][d] in exact int32 arithmetic.
+ * Called on an idle context (a new round), or after the round's dhs_attend
+ * by a Reindex layer of the same source (see "Physical-source sharing"). */
 int dhs_select(dhs_ctx *ctx, const int8_t *q_idx, const int32_t *k_per_req,
                const int64_t *pos, int32_t *topk_out, dhs_stream stream);
 
@@ -338,6 +355,75 @@ const char *dhs_strerror(int code);
 int dhs_select_noalloc(const int8_t *q_idx, const int8_t *keys, int32_t n_queries,
                        int64_t n_rows, int32_t idx_row_bytes, int32_t topk, int32_t *topk_out,
                        dhs_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Physical-source sharing and layer groups, [ADHS] 2.2 ("physical-source
+ * sharing": Full, Reindex and Reuse layers), 3.2 (a Reuse consumer inherits
+ * the preceding selected-location vector; a Reindex consumer re-selects over
+ * the shared source, reusing the rows present; GLM-style index producers
+ * announce positions for several follower payload layers) and 3.4 (staging
+ * arenas reused across layer groups, M_stage = chi N K_max k d_KV).
+ *
+ * On one context (one physical source):
+ *   - Reindex: after a round's dhs_attend and before its dhs_commit, another
+ *     layer may call dhs_select (same K_r per request), dhs_resolve and
+ *     dhs_attend again: the source's one cache state serves both selections,
+ *     rows fetched for the earlier one stay available, and a fresh selection
+ *     fetches only the rows absent from that state.
+ *   - Reuse: dhs_attend may be called again after an attend of the same
+ *     resolve, with another layer's queries and the same location vector:
+ *     no resolution and no copy.  block_kv must be the same rows (the shared
+ *     source's new rows; they are written to the draft ring again).
+ *   - One dhs_commit ends the step for every layer of the source.
+ * Across sources (layers with their own payload):
+ *   - A follower layer (DHS_ROLE_FOLLOWER: no indexer scratch) takes the
+ *     positions a producer's dhs_select returned: dhs_adopt(k_per_req, pos)
+ *     sets the round's K_r and causal domains as dhs_select would, then
+ *     dhs_resolve is given the producer's top-k list and fetches this
+ *     source's own rows into this source's staging.
+ *   - Layer groups: contexts created on shared arenas (dhs_create_on_arena)
+ *     stage their misses in arena `arena` of the set instead of a staging
+ *     buffer of their own; contexts of a layer group take distinct arenas,
+ *     and the next group's contexts reuse them.  A resolve waits (on the GPU)
+ *     for the attention readers of the arena's previous user; a resolve
+ *     whose arena still holds another context's rows that no dhs_attend has
+ *     read yet is refused (DHS_ERR_INVALID), as is an attend after another
+ *     context took the arena.  Each call of such a context also waits for
+ *     the work of that context's previous call, whatever stream it ran on,
+ *     so a caller can issue the next group's resolves (with their host
+ *     gathers) on a copy stream while this group attends on a compute
+ *     stream.  These orderings use CUDA events recorded and waited on by the
+ *     calls; issue them outside stream capture.  Not thread-safe: one host
+ *     thread drives the contexts of a set of arenas.
+ */
+typedef struct dhs_arenas dhs_arenas;
+enum { DHS_ROLE_FULL = 0, DHS_ROLE_FOLLOWER = 1 };
+
+/* chi staging arenas, each n_slots * k_max * topk rows of row_elems bf16
+ * (cudaMalloc on the current device).  DHS_ERR_INVALID for bad sizes,
+ * DHS_ERR_OOM if the allocation fails. */
+int dhs_arenas_create(int32_t chi, int32_t n_slots, int32_t k_max, int32_t topk,
+                      int32_t row_elems, dhs_arenas **out);
+/* Device bytes the arenas hold: M_stage = chi * n_slots * k_max * topk * row bytes. */
+int64_t dhs_arenas_bytes(const dhs_arenas *arenas);
+/* Frees the arenas (synchronises the device); DHS_ERR_INVALID while a
+ * context created on them still exists.  NULL is a no-op. */
+int dhs_arenas_destroy(dhs_arenas *arenas);
+
+/* dhs_create for a source of a layer group: staging is arena `arena` (0 <=
+ * arena < chi) of `arenas`, whose n_slots, k_max, topk and row width must
+ * match the config.  role DHS_ROLE_FOLLOWER allocates no indexer scratch and
+ * refuses dhs_select (it takes positions through dhs_adopt). */
+int dhs_create_on_arena(const dhs_config *cfg, dhs_arenas *arenas, int32_t arena, int32_t role,
+                        dhs_ctx **out);
+
+/* A round whose positions another source's indexer chose ([ADHS] 3.2,
+ * follower-layer copies): sets K_r (host int32 [n_slots]) and the causal
+ * domains (pos as in dhs_select, NULL = n_r + j) exactly as dhs_select would,
+ * without scoring; the caller then passes the producer's top-k list to
+ * dhs_resolve (entries must be rows below this source's n_r).  Allowed where
+ * dhs_select is. */
+int dhs_adopt(dhs_ctx *ctx, const int32_t *k_per_req, const int64_t *pos, dhs_stream stream);
 
 /* Text of the CUDA runtime error behind the context's last DHS_ERR_CUDA ("" if none). */
 const char *dhs_last_error(const dhs_ctx *ctx);

@@ -25,6 +25,13 @@ other than this file):
                                            (a library routine), closed forms
   commit / rollback                        Fig. 3 example, stage-K-then-commit-a
                                            equals stage-a-then-commit-a
+  source sharing (adopt, Reindex, Reuse)   a follower's attention equals attention
+                                           over its own rows at the producer's
+                                           positions; a Reindex selection misses
+                                           exactly the rows absent after the first
+                                           selection's update; a Reuse consumer's
+                                           output is attention over the inherited
+                                           rows (fp64 closed computation)
   residency policy                         eq. (4) against numpy searchsorted over
                                            the cumulative pages, a hand-worked
                                            trace (tests/golden), eq. (3) and the
@@ -284,6 +291,18 @@ class Oracle:
                 out[r, j] = topk_ordered(sc, c.topk)
         self.topk = out
         return out
+
+    # -- a follower source takes another source's positions, [ADHS] 3.2 ----
+    def adopt(self, topk: np.ndarray, k_per_req: np.ndarray):
+        """A layer with its own payload takes the ordered selections another
+        source's indexer announced (GLM-style index sharing: producers
+        announce positions for several follower payload layers).  Nothing is
+        scored; ``resolve`` then maps the same positions to this source's
+        own cache and host rows, and ``attend`` reads this source's rows."""
+        for r, q in self.req.items():
+            q.K = int(k_per_req[r])
+        self.topk = np.asarray(topk, np.int64).copy()
+        return self.topk
 
     # -- steps 2-4: union, probe, compact, shared gather, [ADHS] 3.2-3.3 ---
     def resolve(self, topk: np.ndarray, shared: bool = True):

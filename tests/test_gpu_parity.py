@@ -115,10 +115,13 @@ def _rounds(rec, n_rounds, shared=True, k_sched=None, residency=True, attn_pass=
     return run, o, st
 
 
-PER_QUERY, UNION = 1, 2
+PER_QUERY, UNION, UNION_TC = 1, 2, 3
 
 
-@pytest.mark.parametrize("shared,attn_pass", [(True, PER_QUERY), (True, UNION), (False, 0)])
+@pytest.mark.parametrize("shared,attn_pass", [(True, PER_QUERY), (True, UNION), (True, UNION_TC),
+                                              (False, 0)],
+                         ids=["per_query_pass", "union_mma_sync", "union_tensor_cores",
+                              "per_query_retrieval"])
 def test_tiny_gqa_rounds(shared, attn_pass):
     _, o, st = _rounds(TINY_GQA, 4, shared=shared, attn_pass=attn_pass, label="tiny_gqa")
     assert st["misses"] == o.stats.misses and st["hot_hits"] == o.stats.hot_hits
@@ -131,7 +134,7 @@ def test_tiny_gqa_rounds(shared, attn_pass):
     assert o.stats.ring_hits > 0 and o.stats.opt_hits > 0 and o.stats.evictions > 0
 
 
-@pytest.mark.parametrize("attn_pass", [PER_QUERY, UNION])
+@pytest.mark.parametrize("attn_pass", [PER_QUERY, UNION, UNION_TC])
 def test_tiny_two_kv_heads(attn_pass):
     _rounds(TINY_GQA2, 3, attn_pass=attn_pass, label="tiny_hkv2")
 
@@ -286,7 +289,7 @@ def test_cfg1_full():
     _rounds(rec, 2, label="cfg1")
 
 
-@pytest.mark.parametrize("attn_pass", [0, UNION])
+@pytest.mark.parametrize("attn_pass", [0, UNION, UNION_TC])
 def test_cfg2_full(attn_pass):
     """The benchmark workload: round 0 is the previous step, round 1 is timed."""
     rec = wl.CONFIGS["cfg2"]
@@ -334,6 +337,30 @@ def _sampled(rec, slots, rounds=2, shared=True, k_max=None, opt_rows_max=None, k
 def test_cfg3_full_sampled():
     rec = wl.CONFIGS["cfg3"]
     _sampled(rec, [0, 77, 127])
+
+
+def test_cfg3_union_tensor_cores_sampled():
+    """The DFlash2-style configuration (a 24-request cut) with the union pass
+    on the fifth-generation tensor cores: 128 (query, head) pairs per kv head,
+    every tensor-memory lane in use."""
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+    rec = wl.CONFIGS["cfg3"].scaled(N=24)
+    slots = [0, 23]
+    run = Runner(rec, attn_pass=UNION_TC)
+    o = build_oracle(rec, slots)
+    kr = rec.k_per_req()
+    for rnd in range(2):
+        acc = rec.accepted(rnd, kr)
+        run.load_round(rnd)
+        run.select(kr)
+        run.resolve(True)
+        run.attend()
+        ores = oracle_round(o, rec, rnd, slots, kr, None, True)
+        compare_round(run, o, ores, slots, kr, "cfg3 tensor-core union round %d" % rnd)
+        run.commit(acc)
+        o.commit(acc)
+        compare_state(run, o, slots, "cfg3 tensor-core union round %d" % rnd, full_host=False)
+    assert run.ctx.stats()["device_error"] == 0
 
 
 def test_cfg4_full_sampled():
@@ -398,4 +425,75 @@ def test_round_through_host_buffers(attn_pass, pinned, big):
     got_state = [run.export(w, torch.int32, (N, B)).cpu() for w in ("hot_row", "hot_stamp", "lru")]
     for g, w in zip(got_state, want_state):
         assert torch.equal(g, w)
+    assert run.ctx.stats()["device_error"] == 0
+
+
+# ---------------------------------------------------------------- one-CTA-per-query top-k
+TOPK_ROW = 2
+
+
+@pytest.mark.parametrize("rec", [TINY_GQA, TINY_SHORT, TINY_WIDE_FULL, TINY_TC512_FULL],
+                         ids=["64B", "short_history", "768B_full_range", "512B_full_range"])
+def test_topk_row_kernel_rounds(rec):
+    """The one-CTA-per-query top-k, forced on small recipes: whole rounds
+    (lists, locations, outputs, cache state) equal the oracle's, including
+    domains shorter than k and scores spanning more than 2^13 values."""
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+    run = Runner(rec, topk_pass=TOPK_ROW)
+    slots = list(range(rec.N))
+    o = build_oracle(rec, slots)
+    if rec.opt_frac > 0:
+        run.set_residency()
+        for r in slots:
+            o.set_residency(r, rec.residency_rows(r))
+    sched = (lambda rnd: np.array([2, 0] if rnd % 2 == 0 else [1, 2], np.int32)) \
+        if rec is TINY_SHORT else (lambda rnd: rec.k_per_req())
+    for rnd in range(3):
+        kr = sched(rnd)
+        acc = rec.accepted(rnd, kr)
+        run.load_round(rnd)
+        run.select(kr)
+        run.resolve(True)
+        run.attend()
+        ores = oracle_round(o, rec, rnd, slots, kr, None, True)
+        compare_round(run, o, ores, slots, kr, "%s row top-k round %d" % (rec.name, rnd))
+        run.commit(acc)
+        o.commit(acc)
+        compare_state(run, o, slots, "%s row top-k round %d" % (rec.name, rnd))
+    assert run.ctx.stats()["device_error"] == 0
+
+
+@pytest.mark.parametrize("S,fill", [(3000, "ties"), (9000, "ties"), (160000, "one_pass"),
+                                    (160000, "multi_pass")],
+                         ids=["all_equal_collected", "all_equal_ordered_fallback",
+                              "long_one_pass", "long_multi_pass"])
+def test_topk_row_kernel_lists(S, fill):
+    """Lists of the one-CTA-per-query top-k against the oracle's ordered
+    top-k: every score equal (3000 rows: all rows are candidates and sorted;
+    9000 rows: too many ties for the candidate area, so the lowest rows equal
+    to the threshold are placed by the ordered pass), and long domains read
+    from global memory in one radix pass (uniform -8..8) or several
+    (full-range int8)."""
+    from oracle.dhs_oracle import index_scores, topk_ordered
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+    kw = dict(i8_lo=-128, i8_hi=127) if fill == "multi_pass" else {}
+    rec = wl.Recipe("row_topk_%s_%d" % (fill, S), N=3, K=3, S=S, H_idx=1, d_idx=128, topk=256,
+                    Hq=8, Hkv=1, qk_dim=128, v_dim=128, kv_layout=0, B=64, rho_within=0.5,
+                    rho_cross=0.6, W=16, p=8, seed=44, **kw)
+    run = Runner(rec, topk_pass=TOPK_ROW)
+    run.load_round(0)
+    if fill == "ties":
+        run.keys.fill_(3)
+        run.q_idx.fill_(-2)
+    kr = rec.k_per_req()
+    pos = np.array([[S - 1, S // 2, 100], [S + 5, 700, 257], [0, 255, S - 2]], np.int64)
+    run.select(kr, pos)
+    topk = run.topk.cpu().numpy()
+    qi = run.q_idx.cpu().numpy()
+    keys = run.keys.cpu().numpy()
+    for r in range(rec.N):
+        for j in range(int(kr[r])):
+            dom = max(0, min(S, int(pos[r, j]) + 1))
+            want = topk_ordered(index_scores(qi[r, j], keys[r], dom), rec.topk)
+            assert np.array_equal(topk[r, j], want), "r=%d j=%d dom=%d" % (r, j, dom)
     assert run.ctx.stats()["device_error"] == 0

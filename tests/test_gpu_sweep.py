@@ -43,6 +43,9 @@ def _sweep_rounds(run, rec, rows_of, kr, shared, rounds=2):
     run.rebind()
     run.ctx.reset_stats()
     o = build_oracle(rec, SLOTS, k_max=run.Km, opt_rows_max=run.cfg.opt_rows_max)
+    # the LRU clock belongs to the source and keeps running across binds:
+    # start the oracle's where the context's stands
+    o.t = run.ctx.stats()["resolve_calls"]
     if rows_of is not None:
         run.set_residency(rows_of)
         for r in SLOTS:

@@ -482,3 +482,100 @@ def test_location_encoding_roundtrip():
         for idx in (0, 1, 12345, (1 << 28) - 1):
             l = encode_loc(tier, idx)
             assert l >= 0 and decode_loc(l) == (tier, idx)
+
+
+# ---------------------------------------------------------------- source sharing (2.2, 3.2)
+def _direct_attention(c, rows, block, q, j):
+    """softmax(scale K q) V over the given original rows then block rows 0..j,
+    written out in float64 here (per query head)."""
+    R = oracle.bf16_to_f64(np.concatenate([rows, block[:j + 1]]))
+    outs = []
+    for h in range(c.q_heads):
+        Kh, Vh = oracle.split_row(R, h // (c.q_heads // c.Hkv), c)
+        lg = c.scale * (Kh @ oracle.bf16_to_f64(q[h]))
+        w = np.exp(lg - lg.max())
+        outs.append(w @ Vh / w.sum())
+    return np.stack(outs)
+
+
+def test_follower_attends_its_own_rows_at_the_producers_positions():
+    """GLM-style index sharing (3.2): a follower payload layer takes the
+    positions a producer selected, fetches its own rows for them and attends
+    over its own bytes."""
+    rng = np.random.default_rng(3)
+    K, k = 3, 5
+    c = _tiny_cfg(n_slots=1, k_max=K, topk=k, budget=4, s_max=48)
+    prod, foll = Oracle(c), Oracle(c)
+    prod.bind(0, _host(c, 1), rng.integers(-8, 9, (c.s_max, 8)).astype(np.int8), 30)
+    foll.bind(0, _host(c, 2), np.zeros((c.s_max, 8), np.int8), 30)
+    qi = rng.integers(-8, 9, (1, K, 8)).astype(np.int8)
+    sel = prod.select(qi, np.array([K]))
+    foll.adopt(sel, np.array([K]))
+    foll.resolve(sel)
+    foll.check_placement()                     # eq. (11) against the follower's own rows
+    q = _bf16(rng.standard_normal((1, K, c.q_heads, c.qk_dim)))
+    blk = _bf16(rng.standard_normal((1, K, c.row_elems)))
+    out, _ = foll.attend(q, blk)
+    host = foll.req[0].host
+    for j in range(K):
+        rows = host[[int(s) for s in sel[0, j] if s >= 0]]
+        assert np.allclose(out[0, j], _direct_attention(c, rows, blk[0], q[0, j], j), atol=1e-12)
+    assert not np.array_equal(_host(c, 1), host)   # the producer's bytes were not used
+
+
+def test_reindex_fetches_only_rows_absent_after_the_first_selection():
+    """A Reindex layer (2.2, 3.2) selects again over the shared source before
+    the step commits: its misses are exactly its union less the rows ready
+    after the first layer's update (ring, optional, hot rows including the
+    first layer's promotions), and rows the first layer fetched and promoted
+    are hits for it."""
+    rng = np.random.default_rng(11)
+    K, k, B = 2, 6, 10
+    c = _tiny_cfg(n_slots=1, k_max=K, topk=k, budget=B, s_max=64, ring_window=6)
+    o = Oracle(c)
+    o.bind(0, _host(c, 4), np.zeros((c.s_max, 8), np.int8), 40)
+    for step in range(6):
+        q = o.req[0]
+        q.K = K
+        sel1 = np.full((1, K, k), -1, np.int64)
+        for j in range(K):
+            sel1[0, j] = rng.choice(q.n, k, replace=False)
+        o.resolve(sel1)
+        o.attend(np.zeros((1, K, c.q_heads, c.qk_dim), np.uint16), np.zeros((1, K, c.row_elems), np.uint16))
+        ready = set(int(x) for x in q.hot_row if x >= 0) | set(q.opt_slot) | \
+            set(range(max(q.ring_first, q.n - c.ring_window), q.n))
+        sel2 = np.full((1, K, k), -1, np.int64)
+        for j in range(K):
+            # half the rows of the first selection, half fresh
+            keep = rng.choice(sel1[0, j], k // 2, replace=False)
+            rest = rng.choice(np.setdiff1d(np.arange(q.n), keep), k - k // 2, replace=False)
+            sel2[0, j] = np.concatenate([keep, rest])
+        q.K = K
+        o.resolve(sel2)
+        U2 = set(int(s) for s in sel2[0].reshape(-1))
+        assert list(o.misses[0]) == sorted(U2 - ready)
+        o.check_placement()
+        o.attend(np.zeros((1, K, c.q_heads, c.qk_dim), np.uint16), np.zeros((1, K, c.row_elems), np.uint16))
+        o.commit(np.array([int(rng.integers(0, K + 1))]))
+
+
+def test_reuse_consumer_attends_the_inherited_rows():
+    """A Reuse layer (2.2, 3.2) consumes the preceding selected-location
+    vector with its own queries: its output is attention over the original
+    rows of that selection (eq. 11), with no further resolution."""
+    rng = np.random.default_rng(5)
+    K, k = 3, 4
+    c = _tiny_cfg(n_slots=1, k_max=K, topk=k, budget=3, s_max=40)
+    o = Oracle(c)
+    o.bind(0, _host(c, 6), rng.integers(-8, 9, (c.s_max, 8)).astype(np.int8), 25)
+    sel = o.select(rng.integers(-8, 9, (1, K, 8)).astype(np.int8), np.array([K]))
+    o.resolve(sel)
+    blk = _bf16(rng.standard_normal((1, K, c.row_elems)))
+    calls = o.stats.misses
+    for layer in range(2):
+        q = _bf16(rng.standard_normal((1, K, c.q_heads, c.qk_dim)))
+        out, _ = o.attend(q, blk)
+        for j in range(K):
+            rows = o.req[0].host[[int(s) for s in sel[0, j] if s >= 0]]
+            assert np.allclose(out[0, j], _direct_attention(c, rows, blk[0], q[0, j], j), atol=1e-12)
+    assert o.stats.misses == calls and o.t == 1   # no second resolution
