@@ -58,7 +58,7 @@ def parse():
                     help="configuration to time (the headline is %s)" % WORKLOAD)
     ap.add_argument("--attn-pass", type=int, default=0, choices=[0, 1, 2, 3],
                     help="attention pass after a shared resolve: 0 auto, 1 per query, 2 union "
-                         "(mma.sync), 3 union on the fifth-generation tensor cores")
+                         "(tensor cores where the shape allows), 3 union on mma.sync")
     ap.add_argument("--sweep", action="store_true",
                     help="the load-adaptive sweep on the DFlash2-style shapes: optional residency "
                          "0/5/25/100%% x K = 1/2/4/8, shared against per-query retrieval; one JSON "

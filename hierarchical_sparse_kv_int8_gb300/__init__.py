@@ -39,7 +39,7 @@ class Config(ctypes.Structure):
                 ("softmax_scale", ctypes.c_float), ("attn_pass", ctypes.c_int32),
                 ("topk_pass", ctypes.c_int32)]
 
-ATTN_AUTO, ATTN_PER_QUERY, ATTN_UNION, ATTN_UNION_TC = 0, 1, 2, 3
+ATTN_AUTO, ATTN_PER_QUERY, ATTN_UNION, ATTN_UNION_MMA = 0, 1, 2, 3
 TOPK_AUTO, TOPK_CLUSTER, TOPK_ROW = 0, 1, 2
 
 

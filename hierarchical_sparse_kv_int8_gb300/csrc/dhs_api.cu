@@ -322,7 +322,7 @@ int create_impl(const dhs_config *cfg, dhs_arenas *arenas, int arena, int role, 
       g.idx_heads * g.idx_dim > 1024 || g.q_heads < 1 || g.kv_heads < 1 ||
       g.q_heads % g.kv_heads || g.q_heads / g.kv_heads > 16 || g.q_heads > 128 || g.budget < 1 ||
       g.budget > 65535 || g.ring_window < 1 || g.page_rows < 1 || g.opt_rows_max < 0 ||
-      g.opt_rows_max > g.s_max || g.attn_pass < DHS_ATTN_AUTO || g.attn_pass > DHS_ATTN_UNION_TC ||
+      g.opt_rows_max > g.s_max || g.attn_pass < DHS_ATTN_AUTO || g.attn_pass > DHS_ATTN_UNION_MMA ||
       g.topk_pass < DHS_TOPK_AUTO || g.topk_pass > DHS_TOPK_ROW)
     return DHS_ERR_INVALID;
   if (g.kv_layout != DHS_KV_SPLIT && g.kv_layout != DHS_KV_LATENT) return DHS_ERR_INVALID;
@@ -380,14 +380,14 @@ int create_impl(const dhs_config *cfg, dhs_arenas *arenas, int arena, int role, 
   {
     const bool can = uattn_supported(d);
     const double pq_bytes = (double)d.N * d.Kmax * (d.k + d.Kmax) * row * 2;
-    if ((g.attn_pass == DHS_ATTN_UNION || g.attn_pass == DHS_ATTN_UNION_TC) && !can) {
+    if ((g.attn_pass == DHS_ATTN_UNION || g.attn_pass == DHS_ATTN_UNION_MMA) && !can) {
       delete c;
       return DHS_ERR_INVALID;
     }
     // AUTO: the union pass for 128-dim heads once the per-query pass would
     // stream more than 128 MiB; latent (MLA) rows keep the per-query pass,
     // which measured 3.6x faster on them (0.46 against 1.69 ms at S = 512K)
-    c->fused = g.attn_pass == DHS_ATTN_UNION || g.attn_pass == DHS_ATTN_UNION_TC ||
+    c->fused = g.attn_pass == DHS_ATTN_UNION || g.attn_pass == DHS_ATTN_UNION_MMA ||
                (g.attn_pass == DHS_ATTN_AUTO && can && d.dqk == 128 &&
                 pq_bytes > 128.0 * 1024 * 1024);
   }
@@ -755,7 +755,7 @@ int dhs_attend(dhs_ctx *c, const void *q, const void *block_kv, const int32_t *l
     const uint16_t *q16 = static_cast<const uint16_t *>(q);
     const uint16_t *b16 = static_cast<const uint16_t *>(block_kv);
     uint16_t *o16 = static_cast<uint16_t *>(out);
-    const bool tc = c->cfg.attn_pass == DHS_ATTN_UNION_TC && uattn_tc_supported(c->d);
+    const bool tc = c->cfg.attn_pass != DHS_ATTN_UNION_MMA && uattn_tc_supported(c->d);
     cudaError_t e_ = !(c->last_shared && c->fused)
                          ? launch_attend(c->d, q16, b16, loc, o16, lse, c->n_split, s, &c->timer)
                      : tc ? launch_uattn_tc(c->d, q16, b16, o16, lse, s, &c->timer)

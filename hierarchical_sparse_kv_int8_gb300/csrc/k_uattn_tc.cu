@@ -272,11 +272,26 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
       }
       tc_fence_before();
       mbar_arrive(&s_free[b]);
+      // the tile's query masks: lane l of each softmax warp reads rows l and
+      // 32 + l; one ballot per query and half-tile turns them into the
+      // 64-bit word of rows this thread's query selected
       const uint32_t *msk = reinterpret_cast<const uint32_t *>(smem + kOffMask) + s * kTcN;
+      const uint32_t ma = msk[lane], mb = msk[32 + lane];
+      uint32_t klo = 0u, khi = 0u;
+#pragma unroll
+      for (int jj = 0; jj < kMaxKmax; ++jj) {
+        const uint32_t ba = __ballot_sync(0xffffffffu, (ma >> jj) & 1u);
+        const uint32_t bb = __ballot_sync(0xffffffffu, (mb >> jj) & 1u);
+        if (jj == j) {
+          klo = ba;
+          khi = bb;
+        }
+      }
+      if (!valid) klo = khi = 0u;
       float mx = -CUDART_INF_F;
 #pragma unroll
       for (int i = 0; i < kTcN; ++i) {
-        const bool keep = valid && ((msk[i] >> j) & 1u);
+        const bool keep = ((i < 32 ? klo >> i : khi >> (i - 32)) & 1u) != 0u;
         const float x = keep ? __uint_as_float(sv[i]) * sl2 : -CUDART_INF_F;
         sv[i] = __float_as_uint(x);
         mx = fmaxf(mx, x);
@@ -287,7 +302,7 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
         // rescale this lane's output after the previous tile's P V completed
         wait(&pv_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1));
         tc_fence_after();
-        const float f = need ? exp2f(m_run - m_new) : 1.f;
+        const float f = need ? ex2_approx(m_run - m_new) : 1.f;
 #pragma unroll
         for (int cc = 0; cc < kTcD; cc += 32) {
           uint32_t ov[32];
@@ -300,7 +315,7 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
         tmem_wait_st();
       }
       if (need) {
-        l *= exp2f(m_run - m_new);
+        l *= ex2_approx(m_run - m_new);
         m_run = m_new;
       }
       // P_t replaces P_{t-2}: its P V must have completed
@@ -312,7 +327,7 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
         float p[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          p[i] = live ? exp2f(__uint_as_float(sv[ch * 8 + i]) - m_run) : 0.f;
+          p[i] = live ? ex2_approx(__uint_as_float(sv[ch * 8 + i]) - m_run) : 0.f;
           l += p[i];
         }
         uint4 w;

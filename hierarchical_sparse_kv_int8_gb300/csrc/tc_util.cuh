@@ -104,6 +104,15 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
+// 2^x by the PTX ISA's approximate base-2 exponential instruction
+// (ex2.approx.ftz; -inf gives +0), for softmax weights that are rounded to
+// bf16 anyway.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Plain arrival on an mbarrier (release at CTA scope).
 __device__ __forceinline__ void mbar_arrive(void *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");

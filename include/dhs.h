@@ -125,15 +125,17 @@ enum { DHS_TOPK_AUTO = 0, DHS_TOPK_CLUSTER = 1, DHS_TOPK_ROW = 2 };
  *   UNION    : each (request, kv head) streams the union U_r once and masks
  *              every score by the queries that selected the row; up to K_r
  *              times fewer row reads, best when the round is bound by HBM.
- *              The product tiles run on mma.sync.
- *   UNION_TC : the union pass on the fifth-generation tensor cores (tcgen05
- *              MMAs, scores and output accumulated in tensor memory, one CTA
- *              per (request, kv head)); 128-dim heads with at most 128
- *              (query, head) pairs per kv head, else as UNION.
+ *              For 128-dim heads with at most 128 (query, head) pairs per kv
+ *              head it runs on the fifth-generation tensor cores (tcgen05
+ *              MMAs with the scores and the output accumulated in tensor
+ *              memory, one CTA per (request, kv head)); otherwise on mma.sync
+ *              tiles.
+ *   UNION_MMA: the union pass on mma.sync tiles whatever the shape (for
+ *              comparison).
  *   AUTO     : UNION for 128-dim heads when the per-query pass would stream
  *              more than 128 MiB of rows per round (n_slots * k_max *
  *              (topk + k_max) rows), else PER_QUERY (always for latent rows). */
-enum { DHS_ATTN_AUTO = 0, DHS_ATTN_PER_QUERY = 1, DHS_ATTN_UNION = 2, DHS_ATTN_UNION_TC = 3 };
+enum { DHS_ATTN_AUTO = 0, DHS_ATTN_PER_QUERY = 1, DHS_ATTN_UNION = 2, DHS_ATTN_UNION_MMA = 3 };
 
 /* Cumulative counters since dhs_create (or dhs_reset_stats). */
 typedef struct {

@@ -115,12 +115,12 @@ def _rounds(rec, n_rounds, shared=True, k_sched=None, residency=True, attn_pass=
     return run, o, st
 
 
-PER_QUERY, UNION, UNION_TC = 1, 2, 3
+PER_QUERY, UNION, UNION_MMA = 1, 2, 3
 
 
-@pytest.mark.parametrize("shared,attn_pass", [(True, PER_QUERY), (True, UNION), (True, UNION_TC),
+@pytest.mark.parametrize("shared,attn_pass", [(True, PER_QUERY), (True, UNION), (True, UNION_MMA),
                                               (False, 0)],
-                         ids=["per_query_pass", "union_mma_sync", "union_tensor_cores",
+                         ids=["per_query_pass", "union_tensor_cores", "union_mma_sync",
                               "per_query_retrieval"])
 def test_tiny_gqa_rounds(shared, attn_pass):
     _, o, st = _rounds(TINY_GQA, 4, shared=shared, attn_pass=attn_pass, label="tiny_gqa")
@@ -134,7 +134,7 @@ def test_tiny_gqa_rounds(shared, attn_pass):
     assert o.stats.ring_hits > 0 and o.stats.opt_hits > 0 and o.stats.evictions > 0
 
 
-@pytest.mark.parametrize("attn_pass", [PER_QUERY, UNION, UNION_TC])
+@pytest.mark.parametrize("attn_pass", [PER_QUERY, UNION, UNION_MMA])
 def test_tiny_two_kv_heads(attn_pass):
     _rounds(TINY_GQA2, 3, attn_pass=attn_pass, label="tiny_hkv2")
 
@@ -289,7 +289,7 @@ def test_cfg1_full():
     _rounds(rec, 2, label="cfg1")
 
 
-@pytest.mark.parametrize("attn_pass", [0, UNION, UNION_TC])
+@pytest.mark.parametrize("attn_pass", [0, UNION, UNION_MMA])
 def test_cfg2_full(attn_pass):
     """The benchmark workload: round 0 is the previous step, round 1 is timed."""
     rec = wl.CONFIGS["cfg2"]
@@ -339,14 +339,14 @@ def test_cfg3_full_sampled():
     _sampled(rec, [0, 77, 127])
 
 
-def test_cfg3_union_tensor_cores_sampled():
+def test_cfg3_union_mma_sync_sampled():
     """The DFlash2-style configuration (a 24-request cut) with the union pass
-    on the fifth-generation tensor cores: 128 (query, head) pairs per kv head,
-    every tensor-memory lane in use."""
+    forced onto mma.sync tiles (the automatic choice takes the tensor-core
+    pass, which the full-size sampled test covers)."""
     from hierarchical_sparse_kv_int8_gb300.runner import Runner
     rec = wl.CONFIGS["cfg3"].scaled(N=24)
     slots = [0, 23]
-    run = Runner(rec, attn_pass=UNION_TC)
+    run = Runner(rec, attn_pass=UNION_MMA)
     o = build_oracle(rec, slots)
     kr = rec.k_per_req()
     for rnd in range(2):
@@ -356,10 +356,10 @@ def test_cfg3_union_tensor_cores_sampled():
         run.resolve(True)
         run.attend()
         ores = oracle_round(o, rec, rnd, slots, kr, None, True)
-        compare_round(run, o, ores, slots, kr, "cfg3 tensor-core union round %d" % rnd)
+        compare_round(run, o, ores, slots, kr, "cfg3 mma.sync union round %d" % rnd)
         run.commit(acc)
         o.commit(acc)
-        compare_state(run, o, slots, "cfg3 tensor-core union round %d" % rnd, full_host=False)
+        compare_state(run, o, slots, "cfg3 mma.sync union round %d" % rnd, full_host=False)
     assert run.ctx.stats()["device_error"] == 0
 
 

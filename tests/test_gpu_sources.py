@@ -41,7 +41,7 @@ def _layer_oracle_round(o, rec, rnd, slots, kr, sel, acc=None):
                 staging={r: o.staging[r].copy() for r in slots if r in o.staging})
 
 
-@pytest.mark.parametrize("attn_pass", [1, 2, 3], ids=["per_query", "union", "union_tensor_cores"])
+@pytest.mark.parametrize("attn_pass", [1, 2, 3], ids=["per_query", "union_tensor_cores", "union_mma_sync"])
 def test_layer_group_followers_on_shared_arenas(attn_pass):
     import torch
     import hierarchical_sparse_kv_int8_gb300 as dhs
@@ -109,7 +109,7 @@ def test_layer_group_followers_on_shared_arenas(attn_pass):
     arenas.close()
 
 
-@pytest.mark.parametrize("attn_pass", [1, 2, 3], ids=["per_query", "union", "union_tensor_cores"])
+@pytest.mark.parametrize("attn_pass", [1, 2, 3], ids=["per_query", "union_tensor_cores", "union_mma_sync"])
 def test_reindex_and_reuse_on_one_source(attn_pass):
     import torch
     import hierarchical_sparse_kv_int8_gb300 as dhs
