@@ -69,6 +69,10 @@ def parse():
                          "(resolves with their host gathers on a copy stream while the previous "
                          "layer attends on a compute stream); prints one JSON line")
     ap.add_argument("--chi", type=int, default=2, help="staging arenas of the layer group")
+    ap.add_argument("--groups", type=int, default=0,
+                    help="request-group diagnostic: the workload's requests split into GROUPS "
+                         "contexts on as many streams, each running its own round, so that one "
+                         "group's host gather can overlap another's indexer; prints one JSON line")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per GPU (default: the configuration's); a smaller batch is a "
                          "cut of the workload for profiling, not a bench line")
@@ -823,6 +827,87 @@ def run_layers(args):
     arenas.close()
 
 
+def run_groups(args):
+    """The round of the workload's requests as G independent request groups
+    (a diagnostic).  Requests are independent, so the round of N requests is
+    G rounds of N/G requests, each on its own context and stream: one group's
+    host gather (host link) may then run while another group's indexer
+    (HBM) runs.  One stream, G streams and the one-context round are timed
+    from the same snapshots, with the L2 flushed before every step."""
+    import torch
+    import workload as wl
+    import hierarchical_sparse_kv_int8_gb300 as dhs
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+
+    torch.cuda.set_device(0)
+    dhs.build()
+    rec = wl.CONFIGS[args.workload]
+    if args.batch:
+        rec = rec.scaled(N=args.batch)
+    G = max(1, args.groups)
+    assert rec.N % G == 0
+    n = rec.N // G
+    streams = [torch.cuda.Stream() for _ in range(G)]
+    main = torch.cuda.Stream()
+    runs = []
+    for g in range(G):
+        sub = rec.scaled(N=n, req0=g * n)
+        runs.append(Runner(sub, stream=streams[g]))
+    kr = runs[0].rec.k_per_req()
+    for rnd in range(2):
+        for run in runs:
+            run.load_round(rnd)
+        torch.cuda.synchronize()
+        if rnd == 0:
+            for run in runs:
+                run.round(kr, run.rec.accepted(0, kr))
+    torch.cuda.synchronize()
+    snaps = [run.ctx.snapshot(run.stream) for run in runs]
+    accs = [run.rec.accepted(1, kr) for run in runs]
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+
+    def step(parallel):
+        ev0 = torch.cuda.Event()
+        ev0.record(main)
+        for g, run in enumerate(runs):
+            s = run.stream if parallel else main
+            s.wait_event(ev0)
+            run.ctx.select(run.q_idx, kr, run.topk, None, s)
+            run.ctx.resolve(run.topk, run.loc, True, s)
+            run.ctx.attend(run.q, run.block, run.loc, run.out, run.lse, s)
+            run.ctx.commit(accs[g], s)
+            if parallel:
+                e = torch.cuda.Event()
+                e.record(s)
+                main.wait_event(e)
+
+    res = {}
+    for mode in ("one_stream", "parallel"):
+        times = []
+        for i in range(args.warmup + args.steps):
+            for run, sn in zip(runs, snaps):
+                run.ctx.restore(sn, run.stream)
+            flush.fill_(i & 0xFF)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            step(mode == "parallel")
+            b.record(main)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                times.append(a.elapsed_time(b))
+        res[mode] = float(np.median(times))
+    tokens = rec.N * rec.K
+    line = {"diagnostic": "request groups on parallel streams", "workload": rec.name,
+            "batch": rec.N, "groups": G, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step_one_stream": round(res["one_stream"], 4),
+            "ms_per_step_parallel": round(res["parallel"], 4),
+            "query_tokens_per_s_one_stream": round(tokens / (res["one_stream"] * 1e-3), 1),
+            "query_tokens_per_s_parallel": round(tokens / (res["parallel"] * 1e-3), 1)}
+    print(json.dumps(line), flush=True)
+
+
 def workload_config(rec):
     """The ``config`` object of both arms' lines: the workload and its shapes."""
     return {"workload": rec.name, "batch": rec.N, "K": rec.K, "S": rec.S, "topk": rec.topk,
@@ -883,5 +968,7 @@ if __name__ == "__main__":
         run_sweep(a)
     elif a.layers:
         run_layers(a)
+    elif a.groups:
+        run_groups(a)
     else:
         run_native(a)

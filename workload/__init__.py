@@ -154,6 +154,7 @@ class Recipe:
     s_slack: int = 64
     i8_lo: int = -8      # indexer keys and queries are uniform over i8_lo..i8_hi
     i8_hi: int = 8
+    req0: int = 0        # request r of this recipe is request req0 + r of the workload
 
     @property
     def kmax(self) -> int:
@@ -193,13 +194,13 @@ class Recipe:
         """int8 [r1-r0][s_max][H_idx*d_idx], uniform over i8_lo..i8_hi."""
         per = self.s_max * self.idx_row
         out = np.empty((r1 - r0, self.s_max, self.idx_row), np.int8)
-        fill_i8(out, self.seed, S_KEYS, r0 * per, self.i8_lo, self.i8_hi)
+        fill_i8(out, self.seed, S_KEYS, (self.req0 + r0) * per, self.i8_lo, self.i8_hi)
         return out
 
     def host_rows_into(self, dst, r0: int, r1: int):
         """Fill bf16 bits [r1-r0][s_max][row_elems] (numpy or pinned torch CPU)."""
         per = self.s_max * self.row_elems
-        return fill_bf16_normal(dst, self.seed, S_HOST, r0 * per)
+        return fill_bf16_normal(dst, self.seed, S_HOST, (self.req0 + r0) * per)
 
     def host_rows(self, r0: int, r1: int) -> np.ndarray:
         out = np.empty((r1 - r0, self.s_max, self.row_elems), np.uint16)
@@ -227,6 +228,7 @@ class Recipe:
         elements from the previous step.
         """
         E, Km, n = self.idx_row, self.kmax, r1 - r0
+        r0 += self.req0
         lo, hi = self.i8_lo, self.i8_hi
         base = i8(n * E, self.seed, S_QI_BASE, r0 * E, lo, hi).reshape(n, 1, E)
         base = self._drift(base, rnd, S_QI_XSEL, S_QI_XFRESH, r0 * E)
@@ -242,13 +244,13 @@ class Recipe:
         """bf16 bits [r1-r0][K_max][Hq][qk_dim]."""
         per = self.kmax * self.Hq * self.qk_dim
         out = np.empty((r1 - r0, self.kmax, self.Hq, self.qk_dim), np.uint16)
-        return fill_bf16_normal(out, self.seed, S_QA + ROUND_STRIDE * rnd, r0 * per)
+        return fill_bf16_normal(out, self.seed, S_QA + ROUND_STRIDE * rnd, (self.req0 + r0) * per)
 
     def block_rows(self, rnd: int, r0: int, r1: int) -> np.ndarray:
         """bf16 bits [r1-r0][K_max][row_elems]: K/V rows the target computes for the block."""
         per = self.kmax * self.row_elems
         out = np.empty((r1 - r0, self.kmax, self.row_elems), np.uint16)
-        return fill_bf16_normal(out, self.seed, S_BLOCK + ROUND_STRIDE * rnd, r0 * per)
+        return fill_bf16_normal(out, self.seed, S_BLOCK + ROUND_STRIDE * rnd, (self.req0 + r0) * per)
 
     def k_per_req(self) -> np.ndarray:
         return np.full(self.N, self.K, np.int32)
@@ -256,7 +258,7 @@ class Recipe:
     def accepted(self, rnd: int, k_per_req: Optional[np.ndarray] = None) -> np.ndarray:
         """int32 [N]: rows kept at commit, uniform over 0..K_r."""
         kr = self.k_per_req() if k_per_req is None else k_per_req
-        w = u32(self.N, self.seed, S_ACCEPT + ROUND_STRIDE * rnd).astype(np.uint64)
+        w = u32(self.N, self.seed, S_ACCEPT + ROUND_STRIDE * rnd, self.req0).astype(np.uint64)
         return ((w * (kr.astype(np.uint64) + 1)) >> np.uint64(32)).astype(np.int32)
 
     def residency_rows(self, r: int) -> np.ndarray:
@@ -265,7 +267,7 @@ class Recipe:
         if m == 0:
             return np.zeros(0, np.int32)
         n_pages = self.S // self.p
-        keys = u32(n_pages, self.seed, S_RESID, r * n_pages)
+        keys = u32(n_pages, self.seed, S_RESID, (self.req0 + r) * n_pages)
         order = np.lexsort((np.arange(n_pages), keys))
         pages = np.sort(order[:m]).astype(np.int64)
         rows = (pages[:, None] * self.p + np.arange(self.p)[None, :]).reshape(-1)
