@@ -69,6 +69,9 @@ def parse():
                          "(resolves with their host gathers on a copy stream while the previous "
                          "layer attends on a compute stream); prints one JSON line")
     ap.add_argument("--chi", type=int, default=2, help="staging arenas of the layer group")
+    ap.add_argument("--round-groups", type=int, default=4,
+                    help="issue each round as one dhs_round call with the requests split into "
+                         "this many groups on internal streams (0: the four separate calls)")
     ap.add_argument("--groups", type=int, default=0,
                     help="request-group diagnostic: the workload's requests split into GROUPS "
                          "contexts on as many streams, each running its own round, so that one "
@@ -391,7 +394,8 @@ def run_native(args):
         rec = rec.scaled(seed=rec.seed + rank)   # each rank serves its own requests
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
-        run = Runner(rec, stream=stream, attn_pass=args.attn_pass)
+        run = Runner(rec, stream=stream, attn_pass=args.attn_pass,
+                     round_groups=max(0, args.round_groups))
         kr = rec.k_per_req()
         # previous decode step: leaves the hot cache holding its selection
         run.load_round(0)
@@ -404,6 +408,9 @@ def run_native(args):
         h2d_peak = measure_h2d(torch, stream)
 
         def step():
+            if args.round_groups:
+                run.round_fused(kr, acc1)
+                return
             run.select(kr)
             run.resolve(True)
             run.attend()
@@ -513,21 +520,29 @@ def run_native(args):
     hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
     hbm_src = "MEASURED_PEAKS.json hbm_gbs (copy, burst)" if peaks else "fallback 6.8 TB/s"
     roofs = {}
+    # a kernel may run several times per step (once per request group): its
+    # achieved rate is the round's algorithmic bytes over its event time per
+    # step, which equals the bytes of one launch over that launch's time;
+    # algorithmic bytes and ncu traffic are reported per launch
     for name, (n_l, t_l) in per.items():
         byts = ab["kernel_bytes"].get(name)
         if byts is None:
             continue
         avg_ms = t_l / n_l
-        ach = byts / (avg_ms * 1e-3) / 1e9
+        step_ms = t_l / args.steps
+        ach = byts / (step_ms * 1e-3) / 1e9
         link = name == "gather"
         peak = h2d_peak if link else hbm_peak
         roofs[name] = {"kernel": name, "bound": "h2d" if link else "hbm",
                        "achieved": round(ach, 1), "peak": round(peak, 1), "unit": "GB/s",
                        "frac": round(ach / peak, 4),
-                       "traffic": (ncu_traffic(name, NCU_SUMMARIES[args.workload], rec.N)
+                       "traffic": (ncu_traffic(name, NCU_SUMMARIES[args.workload],
+                                               rec.N * args.steps / n_l)
                                    if args.workload in NCU_SUMMARIES else None),
-                       "algorithmic_bytes": byts,
+                       "algorithmic_bytes": int(byts * args.steps / n_l),
                        "avg_launch_ms": round(avg_ms, 5),
+                       "launches_per_step": round(n_l / args.steps, 3),
+                       "ms_per_step": round(step_ms, 5),
                        "peak_source": ("host link: pinned host-to-device copy measured in this run"
                                        if link else hbm_src)}
     if "gather" in roofs:
@@ -535,8 +550,8 @@ def run_native(args):
             "DRAM bytes from ncu; the gather's algorithmic bytes cross the host link, "
             "not DRAM, and its staging and hot-slot writes stay in L2 during the launch")
     roof = roofs.get(dom)
-    sel_t = sum(per[k][1] / per[k][0] for k in ("index_score", "topk") if k in per)
-    att_t = sum(per[k][1] / per[k][0] for k in ("attn", "attn_union") if k in per)
+    sel_t = sum(per[k][1] / args.steps for k in ("index_score", "topk") if k in per)
+    att_t = sum(per[k][1] / args.steps for k in ("attn", "attn_union") if k in per)
     sa_bytes = ab["select"] + ab["attn"]
     families = {
         "select": {"achieved": round(ab["select"] / (sel_t * 1e-3) / 1e9, 1), "unit": "GB/s",
@@ -563,6 +578,9 @@ def run_native(args):
     # every kernel of the round is timed (the control words travel as kernel
     # parameters, so no upload launch is needed)
     launches_per_step = sum(n for n, _ in per.values()) / args.steps
+    if args.round_groups > 1:
+        # the timed graph issues every kernel once per request group
+        launches_per_step *= args.round_groups
     line = {
         "metric": "verified query-tokens/s per layer (select+resolve+attend)",
         "value": round(value, 1), "unit": "query-tokens/s", "n_gpus": world,
@@ -572,14 +590,23 @@ def run_native(args):
         "config": dict(workload_config(rec),
                        l2="flushed (512 MiB write) before every step",
                        state="restored from snapshot before every step (untimed)",
-                       attention_pass="union" if "attn_union" in per else "per_query"),
+                       attention_pass="union" if "attn_union" in per else "per_query",
+                       round=("one dhs_round call, requests in %d groups on internal streams"
+                              % max(1, args.round_groups) if args.round_groups
+                              else "dhs_select, dhs_resolve, dhs_attend, dhs_commit")),
         "e2e": {"value": round(e2e_value, 1), "unit": "query-tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_ms, 5),
                 "api": "dhs_round_host (pinned host inputs and outputs)"},
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "eager_ms_per_step": round(eager_ms, 5),
-        "launch": "CUDA graph of one round (select, resolve, attend, commit), replayed per step; "
+        "launch": ("CUDA graph of one round (one dhs_round call: select, resolve, attend, commit "
+                   "per request group, the %d groups overlapping on internal streams), replayed "
+                   "per step; kernel times (roofline, families, kernels) from a second replay of "
+                   "the same steps issued as one request group (each kernel over the whole batch, "
+                   "none overlapping) with an event pair around every kernel" % max(1, args.round_groups))
+                  if args.round_groups else
+                  "CUDA graph of one round (select, resolve, attend, commit), replayed per step; "
                   "kernel times from a second replay of the same steps with per-kernel events",
         "roofline": roof,
         "roofline_all": roofs,

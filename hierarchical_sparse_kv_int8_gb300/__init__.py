@@ -37,7 +37,7 @@ class Config(ctypes.Structure):
                 ("budget", ctypes.c_int32), ("ring_window", ctypes.c_int32),
                 ("page_rows", ctypes.c_int32), ("opt_rows_max", ctypes.c_int64),
                 ("softmax_scale", ctypes.c_float), ("attn_pass", ctypes.c_int32),
-                ("topk_pass", ctypes.c_int32)]
+                ("topk_pass", ctypes.c_int32), ("round_groups", ctypes.c_int32)]
 
 ATTN_AUTO, ATTN_PER_QUERY, ATTN_UNION, ATTN_UNION_MMA = 0, 1, 2, 3
 TOPK_AUTO, TOPK_CLUSTER, TOPK_ROW = 0, 1, 2
@@ -107,6 +107,7 @@ _SIGS = {
     "dhs_adopt": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
                   ctypes.c_int),
     "dhs_round_host": ([ctypes.c_void_p] * 9, ctypes.c_int),
+    "dhs_round": ([ctypes.c_void_p] * 11, ctypes.c_int),
     "dhs_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "dhs_last_error": ([ctypes.c_void_p], ctypes.c_char_p),
     "dhs_select_noalloc": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
@@ -426,6 +427,15 @@ class Context:
 
     def snapshot_free(self, sid: int):
         self._check(self._lib.dhs_snapshot_free(self.h, sid), "dhs_snapshot_free")
+
+    def round(self, q_idx, k_per_req, q, block_kv, accepted_len, topk_out, loc_out, out, lse=None,
+              stream=None):
+        kr = _host_i32(k_per_req, self.cfg.n_slots)
+        a = _host_i32(accepted_len, self.cfg.n_slots)
+        self._check(self._lib.dhs_round(self.h, _dptr(q_idx), _host_ptr(kr), _dptr(q),
+                                        _dptr(block_kv), _host_ptr(a), _dptr(topk_out),
+                                        _dptr(loc_out), _dptr(out), _dptr(lse), _stream(stream)),
+                    "dhs_round")
 
     def round_host(self, q_idx, k_per_req, q, block_kv, accepted_len, out, lse=None, stream=None):
         kr = _host_i32(k_per_req, self.cfg.n_slots)

@@ -177,6 +177,10 @@ struct dhs_ctx {
   int role = DHS_ROLE_FULL;
   cudaEvent_t last_ev = nullptr;  // recorded after every call's work
   bool last_valid = false;
+  // dhs_round: request groups on internal streams
+  int groups = 1;
+  std::vector<cudaStream_t> gstream;
+  std::vector<cudaEvent_t> gevent;  // [0]: fork; [1 + g]: group g done
 };
 
 namespace {
@@ -199,6 +203,10 @@ cudaError_t dalloc(dhs_ctx *c, T **p, size_t count) {
 void free_all(dhs_ctx *c) {
   for (void *p : c->allocs) cudaFree(p);
   c->allocs.clear();
+  for (auto st : c->gstream) cudaStreamDestroy(st);
+  c->gstream.clear();
+  for (auto ev : c->gevent) cudaEventDestroy(ev);
+  c->gevent.clear();
   if (c->last_ev) cudaEventDestroy(c->last_ev);
   c->last_ev = nullptr;
   for (auto &s : c->snaps)
@@ -323,7 +331,8 @@ int create_impl(const dhs_config *cfg, dhs_arenas *arenas, int arena, int role, 
       g.q_heads % g.kv_heads || g.q_heads / g.kv_heads > 16 || g.q_heads > 128 || g.budget < 1 ||
       g.budget > 65535 || g.ring_window < 1 || g.page_rows < 1 || g.opt_rows_max < 0 ||
       g.opt_rows_max > g.s_max || g.attn_pass < DHS_ATTN_AUTO || g.attn_pass > DHS_ATTN_UNION_MMA ||
-      g.topk_pass < DHS_TOPK_AUTO || g.topk_pass > DHS_TOPK_ROW)
+      g.topk_pass < DHS_TOPK_AUTO || g.topk_pass > DHS_TOPK_ROW || g.round_groups < 0 ||
+      g.round_groups > g.n_slots || g.round_groups > 16)
     return DHS_ERR_INVALID;
   if (g.kv_layout != DHS_KV_SPLIT && g.kv_layout != DHS_KV_LATENT) return DHS_ERR_INVALID;
   if (g.kv_layout == DHS_KV_LATENT && (g.kv_heads != 1 || g.v_dim > g.qk_dim))
@@ -476,6 +485,17 @@ int create_impl(const dhs_config *cfg, dhs_arenas *arenas, int arena, int role, 
   if (e == cudaSuccess) e = cudaMemset(d.opt_count, 0, N * 8);
   if (e == cudaSuccess) e = cudaMemset(pool, 0, pool_rows * R * 2);
   if (e == cudaSuccess && arenas) e = cudaEventCreateWithFlags(&c->last_ev, cudaEventDisableTiming);
+  c->groups = g.round_groups > 1 ? g.round_groups : 1;
+  for (int i = 0; e == cudaSuccess && c->groups > 1 && i < c->groups; ++i) {
+    cudaStream_t st = nullptr;
+    e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    if (e == cudaSuccess) c->gstream.push_back(st);
+  }
+  for (int i = 0; e == cudaSuccess && c->groups > 1 && i <= c->groups; ++i) {
+    cudaEvent_t ev = nullptr;
+    e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) c->gevent.push_back(ev);
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     free_all(c);
@@ -676,9 +696,141 @@ int select_impl(dhs_ctx *c, const int8_t *q_idx, const int8_t *q_inline,
   c->phase = PH_SELECTED;
   return order_leave(c, s);
 }
+
+// The context's slots [a, b) as a context of their own: the same buffers,
+// every per-slot pointer advanced to slot a, N = b - a.  The launches of a
+// request group take it; stats and the error word stay shared.
+DevCtx slot_view(const DevCtx &d, int a, int b, int n_split) {
+  DevCtx v = d;
+  const size_t A = (size_t)a, KK = (size_t)d.Kmax * d.k, B = d.B, R = d.row;
+  v.N = b - a;
+  v.keys = d.keys + A;
+  v.host = d.host + A;
+  v.n = d.n + A;
+  v.ring_first = d.ring_first + A;
+  v.Kr = d.Kr + A;
+  v.dom = d.dom + A * d.Kmax;
+  v.hot_data = d.hot_data + A * B * R;
+  v.stage = d.stage + A * KK * R;
+  v.ring = d.ring + A * d.Rd * R;
+  v.opt = d.opt + A * (size_t)d.opt_max * R;
+  v.hot_row = d.hot_row + A * B;
+  v.hot_stamp = d.hot_stamp + A * B;
+  v.lru = d.lru + A * B;
+  v.hot_map = d.hot_map + A * d.Sm;
+  v.opt_map = d.opt_map + A * d.Sm;
+  v.opt_list = d.opt_list + A * (size_t)d.opt_max;
+  v.opt_count = d.opt_count + A;
+  v.scores = d.scores + (d.Ss ? A * d.Kmax * d.Ss : 0);
+  v.minmax = d.minmax + A * d.Kmax * 2;
+  v.uni = d.uni + A * KK;
+  v.uent = d.uent + A * KK;
+  v.miss = d.miss + A * KK;
+  v.first_occ = d.first_occ + A * KK;
+  v.counts = d.counts + A * 4;
+  v.promo_dst = d.promo_dst + A * B;
+  v.now_bits = d.now_bits + A * ((B + 31) / 32);
+  v.lru_next = d.lru_next + A * B;
+  v.inst = d.inst + A * KK;
+  if (d.topk_last) v.topk_last = d.topk_last + A * d.Kmax * d.k;
+  if (n_split > 1) {
+    v.part_o = d.part_o + A * d.Kmax * d.Hq * n_split * d.dv;
+    v.part_ml = d.part_ml + A * d.Kmax * d.Hq * n_split * 2;
+  }
+  v.ticket = d.ticket + A * d.Kmax * d.Hkv;
+  v.u_ticket = d.u_ticket + A * d.Hkv;
+  return v;
+}
 }  // namespace
 
 extern "C" {
+
+int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const void *q,
+              const void *block_kv, const int32_t *accepted_len, int32_t *topk_out,
+              int32_t *loc_out, void *out, float *lse, dhs_stream stream) {
+  if (!c || !q_idx || !k_per_req || !q || !block_kv || !accepted_len || !topk_out || !loc_out ||
+      !out || !aligned16(q_idx) || !aligned16(block_kv) || ((uintptr_t)q & 3u) ||
+      ((uintptr_t)out & 3u))
+    return DHS_ERR_INVALID;
+  if (c->phase != PH_IDLE || c->role == DHS_ROLE_FOLLOWER || c->arenas) return DHS_ERR_INVALID;
+  const DevCtx &d = c->d;
+  std::vector<int32_t> w;
+  int max_dom = 0, active = 0;
+  if (int rc = round_words(c, k_per_req, nullptr, w, max_dom, active)) return rc;
+  for (int r = 0; r < d.N; ++r) {
+    const int kr = k_per_req[r];
+    if (!kr) continue;
+    if (accepted_len[r] < 0 || accepted_len[r] > kr) return DHS_ERR_INVALID;
+    if (c->n[r] + accepted_len[r] > d.Sm) return DHS_ERR_CAPACITY;
+  }
+  if (c->tick + 1 > 0x7FFFFFF0) return DHS_ERR_CAPACITY;
+  const bool tc = c->cfg.attn_pass != DHS_ATTN_UNION_MMA && uattn_tc_supported(d);
+  // (the mma.sync union pass sizes its partials for the whole context; with
+  // per-kernel timing on, the round is issued as one group on the caller's
+  // stream, so each kernel's events bracket that kernel alone over the whole
+  // batch)
+  const int G = ((c->fused && !tc) || c->timer.enabled) ? 1 : c->groups;
+  const bool fork = G > 1;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int tick = (int)(c->tick + 1);
+  if (fork && cudaEventRecord(c->gevent[0], s) != cudaSuccess) return cuda_fail(c, cudaGetLastError());
+  const size_t KK = (size_t)d.Kmax * d.k;
+  const uint16_t *q16 = static_cast<const uint16_t *>(q);
+  const uint16_t *b16 = static_cast<const uint16_t *>(block_kv);
+  uint16_t *o16 = static_cast<uint16_t *>(out);
+  for (int g = 0; g < G; ++g) {
+    const int a = (int)((int64_t)d.N * g / G), b = (int)((int64_t)d.N * (g + 1) / G);
+    if (a == b) continue;
+    cudaStream_t sg = fork ? c->gstream[g] : s;
+    if (fork && cudaStreamWaitEvent(sg, c->gevent[0], 0) != cudaSuccess)
+      return cuda_fail(c, cudaGetLastError());
+    const DevCtx v = slot_view(d, a, b, c->n_split);
+    const int n = b - a;
+    std::vector<int32_t> wg(n + (size_t)n * d.Kmax), cw((size_t)n * 4);
+    int dom_g = 0, act_g = 0;
+    for (int r = 0; r < n; ++r) {
+      wg[r] = w[a + r];
+      act_g += w[a + r];
+      for (int j = 0; j < d.Kmax; ++j) {
+        wg[n + r * d.Kmax + j] = w[d.N + (a + r) * d.Kmax + j];
+        dom_g = std::max(dom_g, w[d.N + (a + r) * d.Kmax + j]);
+      }
+      const int kr = k_per_req[a + r];
+      cw[r * 4 + 0] = kr ? accepted_len[a + r] : 0;
+      cw[r * 4 + 1] = (int32_t)(uint32_t)(c->n[a + r] & 0xFFFFFFFF);
+      cw[r * 4 + 2] = (int32_t)(c->n[a + r] >> 32);
+      cw[r * 4 + 3] = kr ? 1 : 0;
+    }
+    cudaError_t e = launch_select(v, q_idx + (size_t)a * d.Kmax * d.idx_row, nullptr,
+                                  topk_out + (size_t)a * KK, dom_g, wg.data(), act_g,
+                                  c->cfg.topk_pass, sg, &c->timer);
+    if (e == cudaSuccess)
+      e = launch_resolve(v, topk_out + (size_t)a * KK, loc_out + (size_t)a * KK, 1, 1, tick, sg,
+                         &c->timer);
+    const size_t qoff = (size_t)a * d.Kmax * d.Hq;
+    if (e == cudaSuccess)
+      e = !c->fused ? launch_attend(v, q16 + qoff * d.dqk, b16 + (size_t)a * d.Kmax * d.row,
+                                    loc_out + (size_t)a * KK, o16 + qoff * d.dv,
+                                    lse ? lse + qoff : nullptr, c->n_split, sg, &c->timer)
+          : tc ? launch_uattn_tc(v, q16 + qoff * d.dqk, b16 + (size_t)a * d.Kmax * d.row,
+                                 o16 + qoff * d.dv, lse ? lse + qoff : nullptr, sg, &c->timer)
+               : launch_uattn(v, q16 + qoff * d.dqk, b16 + (size_t)a * d.Kmax * d.row,
+                              o16 + qoff * d.dv, lse ? lse + qoff : nullptr, sg, &c->timer);
+    if (e == cudaSuccess) e = launch_commit(v, cw.data(), sg, &c->timer);
+    if (e != cudaSuccess) return cuda_fail(c, e);
+    if (fork && (cudaEventRecord(c->gevent[1 + g], sg) != cudaSuccess ||
+                 cudaStreamWaitEvent(s, c->gevent[1 + g], 0) != cudaSuccess))
+      return cuda_fail(c, cudaGetLastError());
+  }
+  c->tick = tick;
+  c->last_shared = 1;
+  for (int r = 0; r < d.N; ++r) {
+    if (k_per_req[r]) c->n[r] += accepted_len[r];
+    c->K[r] = 0;
+  }
+  c->phase = PH_IDLE;
+  return DHS_OK;
+}
 
 int dhs_select(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const int64_t *pos,
                int32_t *topk_out, dhs_stream stream) {
@@ -995,6 +1147,36 @@ int dhs_round_host(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, co
   const DevCtx &d = c->d;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t nq = (size_t)d.N * d.Kmax;
+  if (c->groups > 1 && !c->arenas && c->role == DHS_ROLE_FULL) {
+    // request groups: the whole round through dhs_round on device copies of
+    // the index rows (queries, block rows and outputs used in place when
+    // page-locked, else through device buffers)
+    if (cudaMemcpyAsync(c->rh_qidx, q_idx, nq * d.idx_row, cudaMemcpyHostToDevice, s))
+      return DHS_ERR_CUDA;
+    const void *q_dev = mapped_ptr(q), *b_dev = mapped_ptr(block_kv);
+    void *o_dev = mapped_ptr(out);
+    float *l_dev = lse ? static_cast<float *>(mapped_ptr(lse)) : nullptr;
+    if (!q_dev) {
+      if (cudaMemcpyAsync(c->rh_q, q, nq * d.Hq * d.dqk * 2, cudaMemcpyHostToDevice, s))
+        return DHS_ERR_CUDA;
+      q_dev = c->rh_q;
+    }
+    if (!b_dev) {
+      if (cudaMemcpyAsync(c->rh_block, block_kv, nq * d.row * 2, cudaMemcpyHostToDevice, s))
+        return DHS_ERR_CUDA;
+      b_dev = c->rh_block;
+    }
+    int rc = dhs_round(c, c->rh_qidx, k_per_req, q_dev, b_dev, accepted_len, c->rh_topk,
+                       c->rh_loc, o_dev ? o_dev : c->rh_out,
+                       lse ? (l_dev ? l_dev : c->rh_lse) : nullptr, stream);
+    if (rc) return rc;
+    if ((!o_dev &&
+         cudaMemcpyAsync(out, c->rh_out, nq * d.Hq * d.dv * 2, cudaMemcpyDeviceToHost, s)) ||
+        (lse && !l_dev &&
+         cudaMemcpyAsync(lse, c->rh_lse, nq * d.Hq * 4, cudaMemcpyDeviceToHost, s)))
+      return DHS_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? DHS_OK : DHS_ERR_CUDA;
+  }
   // The indexer is launched first, so the GPU starts while the host prepares
   // the rest.  Small index rows travel in its launch parameters, else
   // through a device buffer.

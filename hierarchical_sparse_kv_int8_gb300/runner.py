@@ -14,20 +14,20 @@ from . import Context, make_config
 
 
 def config_for(rec, k_max: Optional[int] = None, opt_rows_max: Optional[int] = None,
-               attn_pass: int = 0, topk_pass: int = 0):
+               attn_pass: int = 0, topk_pass: int = 0, round_groups: int = 0):
     return make_config(
         n_slots=rec.N, k_max=k_max or rec.kmax, topk=rec.topk, s_max=rec.s_max,
         idx_heads=rec.H_idx, idx_dim=rec.d_idx, q_heads=rec.Hq, kv_heads=rec.Hkv,
         qk_dim=rec.qk_dim, v_dim=rec.v_dim, kv_layout=rec.kv_layout, budget=rec.B,
         ring_window=rec.W, page_rows=rec.p,
         opt_rows_max=rec.opt_rows_max if opt_rows_max is None else opt_rows_max,
-        softmax_scale=0.0, attn_pass=attn_pass, topk_pass=topk_pass)
+        softmax_scale=0.0, attn_pass=attn_pass, topk_pass=topk_pass, round_groups=round_groups)
 
 
 class Runner:
     def __init__(self, rec, k_max: Optional[int] = None, opt_rows_max: Optional[int] = None,
                  stream=None, attn_pass: int = 0, topk_pass: int = 0, arenas=None, arena: int = 0,
-                 role: int = 0, keys=None):
+                 role: int = 0, keys=None, round_groups: int = 0):
         """``arenas``/``arena``/``role``: a source of a layer group staging in a
         shared arena (a follower takes positions from a producer).  ``keys``:
         device index keys to bind instead of generating them (a follower
@@ -35,7 +35,7 @@ class Runner:
         import torch
         self.torch = torch
         self.rec = rec
-        self.cfg = config_for(rec, k_max, opt_rows_max, attn_pass, topk_pass)
+        self.cfg = config_for(rec, k_max, opt_rows_max, attn_pass, topk_pass, round_groups)
         self.Km = self.cfg.k_max
         self.ctx = Context(self.cfg, arenas, arena, role)
         self.stream = stream
@@ -100,6 +100,12 @@ class Runner:
 
     def commit(self, accepted):
         self.ctx.commit(accepted, self.stream)
+
+    def round_fused(self, k_per_req, accepted):
+        """The whole round in one dhs_round call (request groups on internal
+        streams when the config asks for them)."""
+        self.ctx.round(self.q_idx, k_per_req, self.q, self.block, accepted, self.topk, self.loc,
+                       self.out, self.lse, self.stream)
 
     def round(self, k_per_req, accepted, shared=True):
         self.select(k_per_req)

@@ -106,6 +106,7 @@ typedef struct {
   float softmax_scale;  /* 0 = 1/sqrt(qk_dim)                                   */
   int32_t attn_pass;    /* attention kernel for shared retrieval, DHS_ATTN_*    */
   int32_t topk_pass;    /* top-k kernel of dhs_select, DHS_TOPK_*               */
+  int32_t round_groups; /* dhs_round: request groups on internal streams (0/1 = one) */
 } dhs_config;
 
 /* Top-k kernel of dhs_select.  Both return the same ordered lists:
@@ -296,7 +297,10 @@ int dhs_export(dhs_ctx *ctx, int32_t which, void *dst, int64_t bytes, dhs_stream
 /* Per-kernel timing: when enabled, every kernel launch of the context is
  * bracketed by CUDA events on its stream; dhs_kernel_times synchronises and
  * returns, per kernel id, the number of launches and total milliseconds since
- * the last reset.  Kernel ids and names: dhs_kernel_name(id). */
+ * the last reset.  While it is enabled, dhs_round issues the round as one
+ * request group on the caller's stream (no overlapping launches), so each
+ * duration is that kernel's alone over the whole batch.  Kernel ids and
+ * names: dhs_kernel_name(id). */
 int dhs_set_timing(dhs_ctx *ctx, int32_t enable);
 int dhs_kernel_times(dhs_ctx *ctx, int32_t max_ids, int64_t *launches, double *total_ms);
 
@@ -317,6 +321,24 @@ int dhs_restore(dhs_ctx *ctx, int32_t snapshot_id, dhs_stream stream);
  * not reused and restoring it afterwards is DHS_ERR_INVALID. */
 int dhs_snapshot_free(dhs_ctx *ctx, int32_t snapshot_id);
 
+/* One whole round on device buffers: select (causal domains at n_r + j),
+ * resolve (shared retrieval), attend and commit, with the shapes of the
+ * separate calls (topk_out and loc_out receive the selections and locations).
+ * With cfg.round_groups = G > 1 the request slots are split into G contiguous
+ * groups whose rounds are issued on G internal streams forked from `stream`
+ * and joined back into it before the call's work ends: requests are
+ * independent ([ADHS] eq. (6): the union, misses and cache state are per
+ * request), so one group's host gather (bound by the host link) can run while
+ * another group's indexer (bound by HBM) runs -- the overlap of the copy path
+ * with compute of [ADHS] 3.2 / 4.3.2.  Results equal those of the separate
+ * calls; the LRU clock advances once per call.  Forking and joining use CUDA
+ * events, which stream capture turns into graph dependencies.  Not for
+ * contexts on shared arenas or followers (DHS_ERR_INVALID); with the union
+ * pass on mma.sync tiles the groups run one after the other on `stream`. */
+int dhs_round(dhs_ctx *ctx, const int8_t *q_idx, const int32_t *k_per_req, const void *q,
+              const void *block_kv, const int32_t *accepted_len, int32_t *topk_out,
+              int32_t *loc_out, void *out, float *lse, dhs_stream stream);
+
 /* One whole round through host buffers: runs select, resolve (shared),
  * attend and commit on q_idx, q and block_kv in host memory and returns out
  * and lse (lse may be NULL) in host memory.  q_idx is copied to a device
@@ -324,7 +346,8 @@ int dhs_snapshot_free(dhs_ctx *ctx, int32_t snapshot_id);
  * page-locked (cudaHostAlloc / cudaHostRegister): the attention kernel reads
  * and writes them across the host link.  Pageable buffers are copied through
  * device buffers instead.  Synchronises `stream` before returning.  Shapes as
- * in the calls above. */
+ * in the calls above.  With cfg.round_groups > 1 the round runs through
+ * dhs_round (request groups on internal streams). */
 int dhs_round_host(dhs_ctx *ctx, const int8_t *q_idx, const int32_t *k_per_req, const void *q,
                    const void *block_kv, const int32_t *accepted_len, void *out, float *lse,
                    dhs_stream stream);

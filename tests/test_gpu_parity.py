@@ -497,3 +497,81 @@ def test_topk_row_kernel_lists(S, fill):
             want = topk_ordered(index_scores(qi[r, j], keys[r], dom), rec.topk)
             assert np.array_equal(topk[r, j], want), "r=%d j=%d dom=%d" % (r, j, dom)
     assert run.ctx.stats()["device_error"] == 0
+
+
+# ---------------------------------------------------------------- one call per round, request groups
+@pytest.mark.parametrize("rec,groups,attn_pass",
+                         [(TINY_GQA, 2, PER_QUERY), (TINY_GQA, 3, UNION), (TINY_GQA2, 2, UNION),
+                          (TINY_GQA, 2, UNION_MMA), (TINY_MLA, 2, 0)],
+                         ids=["per_query_2", "union_tc_3", "hkv2_union_tc_2", "union_mma_2",
+                              "latent_auto_2"])
+def test_round_in_request_groups(rec, groups, attn_pass):
+    """dhs_round issues select, resolve, attend and commit in one call, the
+    request slots split into groups on internal streams (uneven groups when
+    the slots do not divide): every round equals the oracle's, state included."""
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+    run = Runner(rec, attn_pass=attn_pass, round_groups=groups)
+    slots = list(range(rec.N))
+    o = build_oracle(rec, slots)
+    if rec.opt_frac > 0:
+        run.set_residency()
+        for r in slots:
+            o.set_residency(r, rec.residency_rows(r))
+    for rnd in range(3):
+        kr = rec.k_per_req()
+        if rnd == 1:
+            kr = kr.copy()
+            kr[0] = 0  # an idle slot in one group
+        acc = rec.accepted(rnd, kr)
+        run.load_round(rnd)
+        run.round_fused(kr, acc)
+        ores = oracle_round(o, rec, rnd, slots, kr, acc, True)
+        compare_round(run, o, ores, slots, kr, "%s groups round %d" % (rec.name, rnd))
+        compare_state(run, o, slots, "%s groups round %d" % (rec.name, rnd))
+    st = run.ctx.stats()
+    assert st["device_error"] == 0 and st["resolve_calls"] == 3
+
+
+def test_cfg3_round_in_four_groups_sampled():
+    """The DFlash2-style configuration in one dhs_round call with four request
+    groups on internal streams: sampled requests of every group equal the oracle."""
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+    rec = wl.CONFIGS["cfg3"]
+    slots = [0, 40, 95, 127]
+    run = Runner(rec, round_groups=4)
+    o = build_oracle(rec, slots)
+    kr = rec.k_per_req()
+    for rnd in range(2):
+        acc = rec.accepted(rnd, kr)
+        run.load_round(rnd)
+        run.round_fused(kr, acc)
+        ores = oracle_round(o, rec, rnd, slots, kr, acc, True)
+        compare_round(run, o, ores, slots, kr, "cfg3 groups round %d" % rnd)
+        compare_state(run, o, slots, "cfg3 groups round %d" % rnd, full_host=False)
+    assert run.ctx.stats()["device_error"] == 0
+
+
+def test_round_host_in_request_groups():
+    """dhs_round_host with request groups gives the outputs of the grouped
+    device round (pinned host buffers used in place)."""
+    import torch
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+    rec = TINY_GQA
+    run = Runner(rec, attn_pass=UNION, round_groups=2)
+    kr = rec.k_per_req()
+    run.load_round(0)
+    run.round_fused(kr, rec.accepted(0, kr))
+    run.load_round(1)
+    sid = run.ctx.snapshot()
+    acc1 = rec.accepted(1, kr)
+    run.round_fused(kr, acc1)
+    want_out, want_lse = run.out.cpu(), run.lse.cpu()
+    run.ctx.restore(sid)
+    qi, q, bl = run.q_idx.cpu().pin_memory(), run.q.cpu().pin_memory(), run.block.cpu().pin_memory()
+    out = torch.zeros(run.out.shape, dtype=run.out.dtype, pin_memory=True)
+    lse = torch.zeros(run.lse.shape, dtype=run.lse.dtype, pin_memory=True)
+    run.ctx.round_host(qi, kr, q, bl, acc1, out, lse)
+    for r in range(rec.N):
+        for j in range(int(kr[r])):
+            assert torch.equal(out[r, j], want_out[r, j]) and torch.equal(lse[r, j], want_lse[r, j])
+    assert run.ctx.stats()["device_error"] == 0
