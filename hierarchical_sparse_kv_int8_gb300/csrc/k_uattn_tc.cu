@@ -17,9 +17,12 @@
 // in log2 units (the output is rescaled only when the maximum grows by more
 // than kTcRescale, so the exponentials stay below 2^kTcRescale) and writes
 // its row of P (bf16) to shared memory; then O += P V (M = 128, N = 128, K =
-// kTcN) accumulates in tensor memory.  Warp roles: warps 0-3 are the softmax
-// threads (warp w owns lanes 32w..32w+31), one thread of warp 4 issues every
-// MMA, warps 5-7 copy rows into a ring of kTcStages stages with 16-byte
+// kTcN) accumulates in tensor memory.  Warp roles: warps 0-7 are the softmax
+// threads in two warpgroups (warps w and w + 4 own lanes 32(w mod 4) ..
+// +31, the first group the first half of a tile's columns and of the output,
+// the second the second half; they agree on each row's running maximum
+// through shared memory), one thread of warp 8 issues every MMA, warps 9-11
+// copy rows into a ring of kTcStages stages with 16-byte
 // cp.async from wherever the union/probe located them (hot cache, optional
 // pool, draft ring, staging) or from the caller's block rows, which they also
 // write to the draft ring.  The stages, S buffers and P buffers are handed
@@ -39,11 +42,12 @@ constexpr int kTcM = 128;              // (query, head) pairs: tensor-memory lan
 constexpr int kTcD = 128;              // key and value dims
 constexpr int kTcN = 64;               // walk rows per tile
 constexpr int kTcStages = 4;
-constexpr int kTcThreads = 256;
-constexpr int kTcSoftmax = 128;        // warps 0-3
-constexpr int kTcMmaWarp = 4;
-constexpr int kTcLoadWarp0 = 5;        // warps 5-7 copy
+constexpr int kTcThreads = 384;
+constexpr int kTcSoftmax = 256;        // warps 0-7: two warpgroups, one per half tile
+constexpr int kTcMmaWarp = 8;
+constexpr int kTcLoadWarp0 = 9;        // warps 9-11 copy
 constexpr int kTcLoaders = 96;
+constexpr int kTcHalf = kTcN / 2;      // columns of a tile per softmax warpgroup
 constexpr uint32_t kTcCols = 256;      // S: two buffers of kTcN columns; O: 128 columns
 constexpr uint32_t kTcColO = 128;
 constexpr int kTcSpin = 1 << 20;
@@ -62,7 +66,8 @@ constexpr int kStageBytes = 2 * kKBytes;
 constexpr int kOffP = kOffStage + kTcStages * kStageBytes;
 constexpr int kPBytes = kTcM * kTcN * 2;
 constexpr int kOffMask = kOffP + 2 * kPBytes;
-constexpr int kOffBar = kOffMask + kTcStages * kTcN * 4;
+constexpr int kOffRed = kOffMask + kTcStages * kTcN * 4;  // [2][2][128] partial maxima, [2][128] sums
+constexpr int kOffBar = kOffRed + (2 * 2 * kTcM + 2 * kTcM) * 4;
 constexpr int kNumBars = kTcStages * 2 + 2 * 4 + 1;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kTcSmem = kOffTmem + 16;
@@ -164,22 +169,24 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
     const int4 *uent = c.uent + (size_t)r * KK;
     const uint32_t all_q = (1u << Kr) - 1u;
     // lane l of copy warp lw holds the union entry of row lw + 3 l of a
-    // tile: loaded one tile ahead, turned into a source address when its
+    // tile: loaded three tiles ahead, turned into a source address when its
     // tile is issued.  A stage is complete when every copy thread's copies
     // have landed (asynchronous arrivals) and every row's query mask is
     // written (an ordinary arrival by the lane that wrote it).
     const int li = lw + 3 * lane;
-    int4 nent = make_int4(0, 0, 0, 0);
-    auto fetch = [&](int t) {
+    auto fetch = [&](int t) -> int4 {
       const int e = t * kTcN + li;
-      if (li < kTcN && e < U) nent = uent[e];
+      return (li < kTcN && e < U && t < T) ? uent[e] : make_int4(0, 0, 0, 0);
     };
-    fetch(0);
+    // entries of tiles t, t + 1, t + 2 (loaded three tiles ahead of their use)
+    int4 e0 = fetch(0), e1 = fetch(1), e2 = fetch(2);
     const int off = lane < 16 ? kvh * kTcD + lane * 8 : c.Hkv * kTcD + kvh * kTcD + (lane - 16) * 8;
     for (int t = 0; t < T; ++t) {
       const int s = t % kTcStages;
-      const int4 ent = nent;
-      if (t + 1 < T) fetch(t + 1);
+      const int4 ent = e0;
+      e0 = e1;
+      e1 = e2;
+      e2 = fetch(t + 3);
       const uint16_t *tsrc = nullptr;
       uint32_t tmask = 0u;
       {
@@ -247,70 +254,65 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax
-    const int m = tid;
+    const int hg = warp >> 2;              // warpgroup: half of the tile's columns
+    const int m = tid & (kTcM - 1);        // tensor-memory lane: the (query, head) pair
     const int j = m / G;
     const bool valid = m < Mq && j < Kr;
-    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = c.scale_log2;
+    float *red = reinterpret_cast<float *>(smem + kOffRed);  // [tile parity][group][lane]
+    float *lsum = red + 2 * 2 * kTcM;                        // [group][lane]
     float m_run = -CUDART_INF_F, l = 0.f;
     for (int t = 0; t < T; ++t) {
       const int b = t & 1, s = t % kTcStages;
       wait(&s_full[b], (uint32_t)((t >> 1) & 1));
       wait(&full[s], (uint32_t)((t / kTcStages) & 1));  // the tile's masks
       tc_fence_after();
-      uint32_t sv[kTcN];
-      {
-        uint32_t a[32], bb[32];
-        tmem_ld32(tmem + lrow + (uint32_t)(b * kTcN), a);
-        tmem_ld32(tmem + lrow + (uint32_t)(b * kTcN + 32), bb);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sv[i] = a[i];
-          sv[32 + i] = bb[i];
-        }
-      }
+      uint32_t sv[kTcHalf];
+      tmem_ld32(tmem + lrow + (uint32_t)(b * kTcN + hg * kTcHalf), sv);
+      tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&s_free[b]);
-      // the tile's query masks: lane l of each softmax warp reads rows l and
-      // 32 + l; one ballot per query and half-tile turns them into the
-      // 64-bit word of rows this thread's query selected
+      // this half's query masks: lane l reads row hg * 32 + l; one ballot
+      // per query gives the 32-bit word of rows this thread's query selected
       const uint32_t *msk = reinterpret_cast<const uint32_t *>(smem + kOffMask) + s * kTcN;
-      const uint32_t ma = msk[lane], mb = msk[32 + lane];
-      uint32_t klo = 0u, khi = 0u;
+      const uint32_t ma = msk[hg * kTcHalf + lane];
+      uint32_t kw = 0u;
 #pragma unroll
       for (int jj = 0; jj < kMaxKmax; ++jj) {
         const uint32_t ba = __ballot_sync(0xffffffffu, (ma >> jj) & 1u);
-        const uint32_t bb = __ballot_sync(0xffffffffu, (mb >> jj) & 1u);
-        if (jj == j) {
-          klo = ba;
-          khi = bb;
-        }
+        if (jj == j) kw = ba;
       }
-      if (!valid) klo = khi = 0u;
+      if (!valid) kw = 0u;
       float mx = -CUDART_INF_F;
 #pragma unroll
-      for (int i = 0; i < kTcN; ++i) {
-        const bool keep = ((i < 32 ? klo >> i : khi >> (i - 32)) & 1u) != 0u;
+      for (int i = 0; i < kTcHalf; ++i) {
+        const bool keep = ((kw >> i) & 1u) != 0u;
         const float x = keep ? __uint_as_float(sv[i]) * sl2 : -CUDART_INF_F;
         sv[i] = __float_as_uint(x);
         mx = fmaxf(mx, x);
       }
+      // both halves of a row agree on its maximum
+      red[(b * 2 + hg) * kTcM + m] = mx;
+      named_sync(1, kTcSoftmax);
+      mx = fmaxf(mx, red[(b * 2 + (hg ^ 1)) * kTcM + m]);
       const float m_new = fmaxf(m_run, mx);
       const bool need = m_new > m_run + kTcRescale;  // false while nothing is kept
       if (__any_sync(0xffffffffu, need) && t >= 1) {
-        // rescale this lane's output after the previous tile's P V completed
+        // rescale this lane's half of the output after the previous tile's
+        // P V completed
         wait(&pv_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1));
         tc_fence_after();
         const float f = need ? ex2_approx(m_run - m_new) : 1.f;
 #pragma unroll
-        for (int cc = 0; cc < kTcD; cc += 32) {
+        for (int cc = 0; cc < kTcD / 2; cc += 32) {
+          const uint32_t ta = tmem + lrow + kTcColO + (uint32_t)(hg * (kTcD / 2) + cc);
           uint32_t ov[32];
-          tmem_ld32(tmem + lrow + kTcColO + (uint32_t)cc, ov);
+          tmem_ld32(ta, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
-          tmem_st32(tmem + lrow + kTcColO + (uint32_t)cc, ov);
+          tmem_st32(ta, ov);
         }
         tmem_wait_st();
       }
@@ -323,7 +325,7 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
       unsigned char *prow = smem + kOffP + b * kPBytes + (m >> 3) * 1024 + (m & 7) * 16;
       const bool live = m_run != -CUDART_INF_F;
 #pragma unroll
-      for (int ch = 0; ch < kTcN / 8; ++ch) {
+      for (int ch = 0; ch < kTcHalf / 8; ++ch) {
         float p[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -335,22 +337,26 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
         w.y = pack_bf16(p[2], p[3]);
         w.z = pack_bf16(p[4], p[5]);
         w.w = pack_bf16(p[6], p[7]);
-        *reinterpret_cast<uint4 *>(prow + ch * 128) = w;
+        *reinterpret_cast<uint4 *>(prow + (hg * (kTcHalf / 8) + ch) * 128) = w;
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[b]);
     }
-    // output: O / l, and the natural-log sum-exp
+    // output: O / l over both halves' sums, and the natural-log sum-exp
+    lsum[hg * kTcM + m] = l;
     wait(o_done, 0u);
+    named_sync(1, kTcSoftmax);
+    l += lsum[(hg ^ 1) * kTcM + m];
     tc_fence_after();
     const int h = kvh * G + (m - j * G);
     uint16_t *orow = valid ? out + (((size_t)r * c.Kmax + j) * c.Hq + h) * kTcD : nullptr;
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-    for (int cc = 0; cc < kTcD; cc += 32) {
+    for (int cc = 0; cc < kTcD / 2; cc += 32) {
+      const int col = hg * (kTcD / 2) + cc;
       uint32_t ov[32];
-      tmem_ld32(tmem + lrow + kTcColO + (uint32_t)cc, ov);
+      tmem_ld32(tmem + lrow + kTcColO + (uint32_t)col, ov);
       tmem_wait_ld();
       if (valid) {
 #pragma unroll
@@ -360,11 +366,11 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
           w.y = pack_bf16(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
           w.z = pack_bf16(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
           w.w = pack_bf16(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
-          *reinterpret_cast<uint4 *>(orow + cc + i) = w;
+          *reinterpret_cast<uint4 *>(orow + col + i) = w;
         }
       }
     }
-    if (valid && lse)
+    if (valid && lse && hg == 0)
       lse[((size_t)r * c.Kmax + j) * c.Hq + h] =
           l > 0.f ? (m_run + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
   }
