@@ -47,7 +47,8 @@ class Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "resolve_calls", "selections", "union_rows", "ring_hits", "opt_hits", "hot_hits",
         "misses", "miss_selections", "host_rows_fetched", "host_bytes", "installs", "evictions",
-        "direct_only")] + [("device_error", ctypes.c_int32), ("device_error_site", ctypes.c_int32)]
+        "direct_only")] + [("device_error", ctypes.c_int32), ("device_error_site", ctypes.c_int32),
+                        ("topk_rescans", ctypes.c_int64)]
 
 
 class DhsError(RuntimeError):

@@ -1012,6 +1012,7 @@ int dhs_get_stats(dhs_ctx *c, dhs_stats *out, dhs_stream stream) {
   out->installs = st[ST_INSTALL];
   out->evictions = st[ST_EVICT];
   out->direct_only = st[ST_DIRECT];
+  out->topk_rescans = st[ST_TOPK_RESCAN];
   out->device_error = err[0];
   out->device_error_site = err[1];
   return err[0] ? DHS_ERR_DEVICE_CHECK : DHS_OK;

@@ -107,7 +107,7 @@ struct DevCtx {
 
 enum StatIdx {
   ST_RESOLVE = 0, ST_SEL, ST_UNION, ST_RING, ST_OPT, ST_HOT, ST_MISS, ST_MISS_SEL,
-  ST_FETCHED, ST_INSTALL, ST_EVICT, ST_DIRECT, ST_COUNT
+  ST_FETCHED, ST_INSTALL, ST_EVICT, ST_DIRECT, ST_TOPK_RESCAN, ST_COUNT
 };
 
 __device__ __forceinline__ void record_error(int32_t *err, int code, int site) {

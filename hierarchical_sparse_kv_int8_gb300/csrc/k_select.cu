@@ -1031,10 +1031,20 @@ k_topk(const DevCtx c, int32_t *__restrict__ topk_out, int stage_cap) {
 //  (3) otherwise (many rows equal to T) the rows above T are collected and
 //      sorted the same way, and the lowest rows equal to T follow them, placed
 //      by an ordered pass in which each warp owns a contiguous run of rows.
+// Domains of at least kRowSampleMin rows first try a single read: a
+// histogram of a 1/16 systematic sample gives a value t with about
+// (k + kRowCap) / 2 rows expected at or above it, one pass stashes those
+// rows, and when between k and kRowCap of them were found the stash holds
+// every row at or above T, so T, the group starts and the places (or, for
+// scores spanning more than 2^13 values, a sort) come from the stash alone.
+// A stash outside those bounds (a sample unlike the domain) is counted in
+// the statistics and (1)-(3) run.
 constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kRowCap = 4096;      // candidates: 4096 keys of 8 bytes
 constexpr int kRowUnroll = 4;      // 16-byte loads in flight per thread in a pass
+constexpr int kRowSampleMin = 32768;  // domains from which the threshold is estimated
+constexpr int kRowSampleStride = 16;  // one 128-row chunk in 16 is sampled
 constexpr size_t kRowSmem = (size_t)kRowCap * 8 + ((size_t)1 << kRadixBits) * 4;
 static_assert(kMaxTopk <= kRowCap, "the rows above the threshold always fit the candidates");
 
@@ -1062,8 +1072,7 @@ k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned long long *cand = reinterpret_cast<unsigned long long *>(smem);
   uint32_t *hist = reinterpret_cast<uint32_t *>(smem + (size_t)kRowCap * 8);
-  __shared__ int warp_sums[32];
-  __shared__ int wcnt[kRowWarps];
+  __shared__ int wcnt[kRowWarps], wsum[kRowWarps];
   __shared__ int sh_bin, sh_above, sh_eq, sh_cnt;
   pdl_wait();
   pdl_trigger();
@@ -1137,6 +1146,129 @@ k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
     for (int i = tid; i < m; i += kRowThreads)
       out[o0 + i] = (int32_t)(uint32_t)(cand[i] & 0xFFFFFFFFull);
   };
+  // Every row whose offset value is at least t, claimed in any order into
+  // cand[] as (~v << 32 | row) by one pass over the domain with several
+  // 16-byte loads in flight per thread; sh_cnt counts them all, and only the
+  // first kRowCap are stored.  A load's four scores are tested at once
+  // against lo + t (at most hi: no overflow); only the lanes holding a row
+  // at or above it look at single rows (the last load of the domain may
+  // hold rows past its end, which they skip).
+  auto stash = [&](uint32_t t) {
+    const int thr = lo + (int)t;
+    for (int s0 = wid * 128; s0 < dom; s0 += kRowWarps * 128 * kRowUnroll) {
+      int4 x[kRowUnroll];
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int s = s0 + u * kRowWarps * 128 + 4 * lane;
+        x[u] = s < dom ? load4(s) : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
+      }
+      unsigned um = 0;
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u)
+        um |= (unsigned)(max(max(x[u].x, x[u].y), max(x[u].z, x[u].w)) >= thr) << u;
+      if (!__any_sync(0xffffffffu, um != 0)) continue;
+      if (um == 0) continue;
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        if (!((um >> u) & 1u)) continue;
+        const int s = s0 + u * kRowWarps * 128 + 4 * lane;
+        const int xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (xv[e] < thr || s + e >= dom) continue;
+          const int pos = atomicAdd(&sh_cnt, 1);
+          if (pos < kRowCap)
+            cand[pos] = ((unsigned long long)(0xFFFFFFFFu - (uint32_t)(xv[e] - lo)) << 32) |
+                        (uint32_t)(s + e);
+        }
+      }
+    }
+  };
+  // hist[0..nbins) = 0 (16-byte stores; the area holds 2^13 bins)
+  auto zero_hist = [&](int nbins) {
+    uint4 *h4 = reinterpret_cast<uint4 *>(hist);
+    for (int i = tid; i < (nbins + 3) >> 2; i += kRowThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
+  };
+  // Warp w owns the w-th run of bins of hist[0..nbins) counted from the top,
+  // its lanes reading consecutive bins (lane 0 the highest of each group of
+  // 32); the warps' totals give the rows above each run, and the warp whose
+  // run holds the kr-th row from the top publishes that bin (sh_bin), the
+  // rows above it (sh_above) and its count (sh_eq).  With `starts`, every
+  // bin at or above it then holds the rows above it: the first place of its
+  // value's group.  Ends with a barrier.
+  auto find_bin = [&](int nbins, int kr, bool starts) {
+    const int per = (nbins + kRowWarps - 1) / kRowWarps;
+    const int b_hi = nbins - wid * per;
+    const int b_lo = max(0, b_hi - per);
+    int sum = 0;
+    for (int b = b_hi - 1 - lane; b >= b_lo; b -= 32) sum += (int)hist[b];
+    sum = (int)__reduce_add_sync(0xffffffffu, (unsigned)sum);
+    if (lane == 0) wsum[wid] = sum;
+    __syncthreads();
+    int above = 0;
+    for (int w = 0; w < wid; ++w) above += wsum[w];
+    // counts of the 32 bins b0 - lane, b0 >= b1, and their inclusive sums in
+    // lane order (from the top)
+    auto group = [&](int b0, int b1, int &g) {
+      const int b = b0 - lane;
+      g = b >= b1 ? (int)hist[b] : 0;
+      int incl = g;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      return incl;
+    };
+    if (sum > 0 && above < kr && kr <= above + sum) {
+      int acc = above;
+      for (int b0 = b_hi - 1; b0 >= b_lo; b0 -= 32) {
+        int g;
+        const int incl = group(b0, b_lo, g);
+        const int tot = __shfl_sync(0xffffffffu, incl, 31);
+        if (acc + tot >= kr) {
+          const unsigned m = __ballot_sync(0xffffffffu, acc + incl >= kr);
+          if (lane == __ffs(m) - 1) {
+            sh_bin = b0 - lane;
+            sh_above = acc + incl - g;
+            sh_eq = g;
+          }
+          break;
+        }
+        acc += tot;
+      }
+    }
+    __syncthreads();
+    if (starts) {
+      const int b1 = max(b_lo, sh_bin);
+      int acc = above;
+      for (int b0 = b_hi - 1; b0 >= b1; b0 -= 32) {
+        int g;
+        const int incl = group(b0, b1, g);
+        if (b0 - lane >= b1) hist[b0 - lane] = (uint32_t)(acc + incl - g);
+        acc += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      __syncthreads();
+    }
+  };
+  // cand[0..n) holds the rows at or above the threshold, each at a place
+  // claimed in its value's group (v << 32 | row); its final place is the
+  // group's start plus the number of the group's rows below its own row.
+  auto place = [&](int n) {
+    for (int p = tid; p < n; p += kRowThreads) {
+      const unsigned long long me = cand[p];
+      const uint32_t v = (uint32_t)(me >> 32), row = (uint32_t)me;
+      int left = 0, below = 0;
+      for (int q = p - 1; q >= 0 && (uint32_t)(cand[q] >> 32) == v; --q) {
+        ++left;
+        below += (uint32_t)cand[q] < row;
+      }
+      for (int q = p + 1; q < n && (uint32_t)(cand[q] >> 32) == v; ++q)
+        below += (uint32_t)cand[q] < row;
+      const int fin = p - left + below;
+      if (fin < k) out[fin] = (int32_t)row;
+    }
+  };
 
   if (dom <= k) {  // every row of the domain is kept, in order
     collect([](uint32_t) { return true; });
@@ -1146,6 +1278,93 @@ k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
   }
   const uint32_t range = (uint32_t)(hi - lo);
   int shift = range ? 32 - __clz((int)range) : 0;
+  if (dom >= kRowSampleMin && 2 * k <= kRowCap && shift > 0) {
+    // Long domains: the threshold is first estimated from a systematic
+    // sample (the 128-row chunks whose index is a multiple of
+    // kRowSampleStride) as the value with about (k + kRowCap) / 2 rows of
+    // the domain at or above it, and one pass stashes those rows.  When the
+    // stash holds at least k rows and fits, it holds every row at or above
+    // the true threshold, so the list follows from the stash alone and the
+    // scores are read once; otherwise the exact passes below run.
+    const int sh = max(0, shift - kRadixBits), nb = 1 << min(kRadixBits, shift);
+    zero_hist(nb);
+    __syncthreads();
+    constexpr int kSampleStep = 128 * kRowSampleStride;
+    const int nsamp = ((dom + 127) / 128 + kRowSampleStride - 1) / kRowSampleStride;
+    for (int i0 = wid; i0 < nsamp; i0 += kRowWarps * kRowUnroll) {
+      int4 x[kRowUnroll];
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int i = i0 + u * kRowWarps, s = i * kSampleStep + 4 * lane;
+        x[u] = i < nsamp && s < dom ? load4(s) : make_int4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int i = i0 + u * kRowWarps, s = i * kSampleStep + 4 * lane;
+        if (i >= nsamp) continue;
+        const int xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (s + e < dom) atomicAdd(&hist[((uint32_t)(xv[e] - lo) >> sh) & (nb - 1)], 1u);
+      }
+    }
+    __syncthreads();
+    // sampled rows: every sampled chunk but the last is whole
+    const int m = (nsamp - 1) * 128 + min(128, dom - (nsamp - 1) * kSampleStep);
+    const int target = (k + kRowCap) / 2;
+    const int qs = (int)(((long long)target * m + dom - 1) / dom);
+    find_bin(nb, qs, false);
+    const uint32_t t_est = (uint32_t)sh_bin << sh;
+    stash(t_est);
+    __syncthreads();
+    const int n = sh_cnt;
+    if (n >= k && n <= kRowCap) {
+      if (sh == 0) {
+        // bins are values: count the stash, find T and the group starts,
+        // then each stashed row at or above T claims a place in its group
+        // (the stash is read into registers first, as the places overwrite it)
+        zero_hist(nb);
+        __syncthreads();
+        for (int p = tid; p < n; p += kRowThreads)
+          atomicAdd(&hist[(0xFFFFFFFFu - (uint32_t)(cand[p] >> 32)) & (nb - 1)], 1u);
+        __syncthreads();
+        find_bin(nb, k, true);
+        const uint32_t T = (uint32_t)sh_bin;
+        const int ng = sh_above + sh_eq;
+        constexpr int kPer = kRowCap / kRowThreads;
+        unsigned long long mine[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int p = tid + i * kRowThreads;
+          mine[i] = p < n ? cand[p] : 0ull;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          if (tid + i * kRowThreads >= n) continue;
+          const uint32_t v = 0xFFFFFFFFu - (uint32_t)(mine[i] >> 32);
+          if (v < T) continue;
+          const uint32_t p = atomicAdd(&hist[v], 1u);
+          if (p < (uint32_t)kRowCap)
+            cand[p] = ((unsigned long long)v << 32) | (uint32_t)mine[i];
+          else
+            record_error(c.err, DC_CAPACITY, K_TOPK);
+        }
+        __syncthreads();
+        place(ng);
+      } else {
+        // coarse bins: the stash sorted by (score desc, row asc)
+        sort_out(n, 0, k);
+      }
+      return;
+    }
+    // the estimate missed (too few rows at or above it, or too many to keep)
+    __syncthreads();  // every thread has read the count
+    if (tid == 0) {
+      sh_cnt = 0;
+      atomicAdd(&c.stats[ST_TOPK_RESCAN], 1ull);
+    }
+  }
   uint32_t prefix = 0;
   int k_rem = k;
   int n_eq = dom;  // rows equal to T (all of them when every score is equal)
@@ -1156,7 +1375,7 @@ k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
     const int width = min(kRadixBits, shift);
     shift -= width;
     const int nbins = 1 << width;
-    for (int i = tid; i < nbins; i += kRowThreads) hist[i] = 0;
+    zero_hist(nbins);
     __syncthreads();
     const int hs = shift + width;
     for (int s0 = wid * 128; s0 < dom; s0 += kRowWarps * 128 * kRowUnroll) {
@@ -1180,45 +1399,12 @@ k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
       }
     }
     __syncthreads();
-    // thread t owns a run of bins counted from the top; an exclusive scan in
-    // thread order counts the rows above each run
-    const int per = (nbins + kRowThreads - 1) / kRowThreads;
-    const int b_hi = nbins - tid * per;
-    const int b_lo = max(0, b_hi - per);
-    int local = 0;
-    for (int b = b_lo; b < b_hi; ++b) local += (int)hist[b];
-    int total;
-    const int above = block_excl_scan(local, warp_sums, total);
-    if (local > 0 && above < k_rem && k_rem <= above + local) {
-      int acc = above;
-      for (int b = b_hi - 1; b >= b_lo; --b) {
-        const int g = (int)hist[b];
-        if (acc + g >= k_rem) {
-          sh_bin = b;
-          sh_above = acc;
-          sh_eq = g;
-          break;
-        }
-        acc += g;
-      }
-    }
-    __syncthreads();
-    const int thr_bin = sh_bin;
+    // (with exact bins, bin b >= T becomes the first place of value b's group)
+    find_bin(nbins, k_rem, passes == 1 && shift == 0);
     k_rem -= sh_above;
-    prefix = (prefix << width) | (uint32_t)thr_bin;
+    prefix = (prefix << width) | (uint32_t)sh_bin;
     n_eq = sh_eq;
     first = false;
-    if (passes == 1 && shift == 0 && (uint32_t)b_hi > (uint32_t)thr_bin) {
-      // exact bins: bin b >= T becomes the first place of value b's group,
-      // the rows of the domain above b (this thread's run, from its top)
-      int acc = above;
-      for (int b = b_hi - 1; b >= max(b_lo, thr_bin); --b) {
-        const int g = (int)hist[b];
-        hist[b] = (uint32_t)acc;
-        acc += g;
-      }
-    }
-    __syncthreads();  // the histogram may be reused (or holds the group starts)
   }
   const uint32_t T = prefix;  // the k-th largest offset score
   const int need = k_rem;     // rows equal to T that are kept
@@ -1244,20 +1430,7 @@ k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
     }
     __syncthreads();
     // ... then its place: the group's start plus the group's rows below it
-    const int n = c_gt + n_eq;
-    for (int p = tid; p < n; p += kRowThreads) {
-      const unsigned long long me = cand[p];
-      const uint32_t v = (uint32_t)(me >> 32), row = (uint32_t)me;
-      int left = 0, below = 0;
-      for (int q = p - 1; q >= 0 && (uint32_t)(cand[q] >> 32) == v; --q) {
-        ++left;
-        below += (uint32_t)cand[q] < row;
-      }
-      for (int q = p + 1; q < n && (uint32_t)(cand[q] >> 32) == v; ++q)
-        below += (uint32_t)cand[q] < row;
-      const int fin = p - left + below;
-      if (fin < k) out[fin] = (int32_t)row;
-    }
+    place(c_gt + n_eq);
     return;
   }
   if (c_gt + n_eq <= kRowCap) {

@@ -155,6 +155,10 @@ typedef struct {
   int64_t direct_only;       /* requests whose union resolved in step 1 only  */
   int32_t device_error;      /* first device check code (0 = none)           */
   int32_t device_error_site; /* kernel id that recorded it                    */
+  int64_t topk_rescans;      /* long-domain queries whose sampled threshold
+                                estimate missed, so top-k read the scores
+                                again (an implementation counter; the result
+                                is the same either way)                       */
 } dhs_stats;
 
 /* Create a context.  Allocates (cudaMalloc, on the current device) the hot

@@ -463,17 +463,33 @@ def test_topk_row_kernel_rounds(rec):
     assert run.ctx.stats()["device_error"] == 0
 
 
-@pytest.mark.parametrize("S,fill", [(3000, "ties"), (9000, "ties"), (160000, "one_pass"),
-                                    (160000, "multi_pass")],
+# (rows of the 128-row chunks whose index is a multiple of 16 form the
+# kernel's threshold sample on long domains)
+ROW_SAMPLE_STRIDE = 16
+
+
+def _sampled_rows(S):
+    return (np.arange(S) // 128) % ROW_SAMPLE_STRIDE == 0
+
+
+@pytest.mark.parametrize("S,fill,rescans",
+                         [(3000, "ties", 0), (9000, "ties", 0), (160000, "one_pass", 0),
+                          (160000, "multi_pass", 0), (160000, "sample_high", 4),
+                          (160000, "sample_low", 4), (160000, "long_ties", 4)],
                          ids=["all_equal_collected", "all_equal_ordered_fallback",
-                              "long_one_pass", "long_multi_pass"])
-def test_topk_row_kernel_lists(S, fill):
+                              "long_one_pass", "long_multi_pass", "estimate_too_high",
+                              "estimate_too_low", "long_ties"])
+def test_topk_row_kernel_lists(S, fill, rescans):
     """Lists of the one-CTA-per-query top-k against the oracle's ordered
     top-k: every score equal (3000 rows: all rows are candidates and sorted;
     9000 rows: too many ties for the candidate area, so the lowest rows equal
     to the threshold are placed by the ordered pass), and long domains read
     from global memory in one radix pass (uniform -8..8) or several
-    (full-range int8)."""
+    (full-range int8).  Long domains first try the sampled single read; the
+    last three cases defeat the sample (sampled rows scoring above the rest,
+    below the rest, or a domain of ties) so that the exact passes run after
+    it, which the rescan counter confirms for the four long domains."""
+    import torch
     from oracle.dhs_oracle import index_scores, topk_ordered
     from hierarchical_sparse_kv_int8_gb300.runner import Runner
     kw = dict(i8_lo=-128, i8_hi=127) if fill == "multi_pass" else {}
@@ -485,8 +501,23 @@ def test_topk_row_kernel_lists(S, fill):
     if fill == "ties":
         run.keys.fill_(3)
         run.q_idx.fill_(-2)
+    elif fill in ("sample_high", "sample_low", "long_ties"):
+        # one positive query word: a row's score is the sum of its key bytes
+        run.q_idx.fill_(1)
+        g = torch.Generator().manual_seed(7)
+        samp = torch.from_numpy(_sampled_rows(S))
+        if fill == "long_ties":
+            keys = torch.full((rec.N, S, rec.idx_row), 3, dtype=torch.int8)
+            keys[:, ::997] = 4  # 161 rows above a domain of ties
+        else:
+            high = torch.randint(0, 9, (rec.N, S, rec.idx_row), generator=g, dtype=torch.int8)
+            low = torch.randint(-8, 1, (rec.N, S, rec.idx_row), generator=g, dtype=torch.int8)
+            hi_rows = samp if fill == "sample_high" else ~samp
+            keys = torch.where(hi_rows[None, :, None], high, low)
+        run.keys[:, :S].copy_(keys.to(run.keys.device))
     kr = rec.k_per_req()
     pos = np.array([[S - 1, S // 2, 100], [S + 5, 700, 257], [0, 255, S - 2]], np.int64)
+    run.ctx.reset_stats(run.stream)
     run.select(kr, pos)
     topk = run.topk.cpu().numpy()
     qi = run.q_idx.cpu().numpy()
@@ -496,7 +527,9 @@ def test_topk_row_kernel_lists(S, fill):
             dom = max(0, min(S, int(pos[r, j]) + 1))
             want = topk_ordered(index_scores(qi[r, j], keys[r], dom), rec.topk)
             assert np.array_equal(topk[r, j], want), "r=%d j=%d dom=%d" % (r, j, dom)
-    assert run.ctx.stats()["device_error"] == 0
+    st = run.ctx.stats()
+    assert st["device_error"] == 0
+    assert st["topk_rescans"] == rescans
 
 
 # ---------------------------------------------------------------- one call per round, request groups
