@@ -181,6 +181,7 @@ struct dhs_ctx {
   int groups = 1;
   std::vector<cudaStream_t> gstream;
   std::vector<cudaEvent_t> gevent;  // [0]: fork; [1 + g]: group g done
+  std::vector<cudaEvent_t> gsel;    // [g]: group g's selection issued
 };
 
 namespace {
@@ -207,6 +208,8 @@ void free_all(dhs_ctx *c) {
   c->gstream.clear();
   for (auto ev : c->gevent) cudaEventDestroy(ev);
   c->gevent.clear();
+  for (auto ev : c->gsel) cudaEventDestroy(ev);
+  c->gsel.clear();
   if (c->last_ev) cudaEventDestroy(c->last_ev);
   c->last_ev = nullptr;
   for (auto &s : c->snaps)
@@ -441,6 +444,7 @@ int create_impl(const dhs_config *cfg, dhs_arenas *arenas, int arena, int role, 
   ALLOC(d.now_bits, N * (size_t)((B + 31) / 32));
   ALLOC(d.lru_next, N * B);
   ALLOC(d.inst, N * KK);
+  if (union_spill_ints_per_request(d) > 0) ALLOC(d.uspill, N * union_spill_ints_per_request(d));
   const size_t pf = attn_partial_floats(d, c->n_split);
   ALLOC(d.part_o, c->n_split > 1 ? pf : 1);
   ALLOC(d.part_ml, c->n_split > 1 ? N * d.Kmax * d.Hq * c->n_split * 2 : 1);
@@ -486,15 +490,27 @@ int create_impl(const dhs_config *cfg, dhs_arenas *arenas, int arena, int role, 
   if (e == cudaSuccess) e = cudaMemset(pool, 0, pool_rows * R * 2);
   if (e == cudaSuccess && arenas) e = cudaEventCreateWithFlags(&c->last_ev, cudaEventDisableTiming);
   c->groups = g.round_groups > 1 ? g.round_groups : 1;
+  // group g's stream has the g-th highest priority: when SMs free up, the
+  // pending kernels of earlier groups (retrieval, attention) are placed
+  // before later groups' indexer CTAs
+  int prio_least = 0, prio_greatest = 0;
+  if (e == cudaSuccess && c->groups > 1)
+    e = cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest);
   for (int i = 0; e == cudaSuccess && c->groups > 1 && i < c->groups; ++i) {
     cudaStream_t st = nullptr;
-    e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    e = cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking,
+                                     std::min(prio_least, prio_greatest + i));
     if (e == cudaSuccess) c->gstream.push_back(st);
   }
   for (int i = 0; e == cudaSuccess && c->groups > 1 && i <= c->groups; ++i) {
     cudaEvent_t ev = nullptr;
     e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
     if (e == cudaSuccess) c->gevent.push_back(ev);
+  }
+  for (int i = 0; e == cudaSuccess && c->groups > 1 && i < c->groups; ++i) {
+    cudaEvent_t ev = nullptr;
+    e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) c->gsel.push_back(ev);
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -732,6 +748,7 @@ DevCtx slot_view(const DevCtx &d, int a, int b, int n_split) {
   v.now_bits = d.now_bits + A * ((B + 31) / 32);
   v.lru_next = d.lru_next + A * B;
   v.inst = d.inst + A * KK;
+  if (d.uspill) v.uspill = d.uspill + A * union_spill_ints_per_request(d);
   if (d.topk_last) v.topk_last = d.topk_last + A * d.Kmax * d.k;
   if (n_split > 1) {
     v.part_o = d.part_o + A * d.Kmax * d.Hq * n_split * d.dv;
@@ -778,6 +795,7 @@ int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const v
   const uint16_t *q16 = static_cast<const uint16_t *>(q);
   const uint16_t *b16 = static_cast<const uint16_t *>(block_kv);
   uint16_t *o16 = static_cast<uint16_t *>(out);
+  int prev_sel = -1;  // the last group whose selection was issued
   for (int g = 0; g < G; ++g) {
     const int a = (int)((int64_t)d.N * g / G), b = (int)((int64_t)d.N * (g + 1) / G);
     if (a == b) continue;
@@ -801,12 +819,25 @@ int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const v
       cw[r * 4 + 2] = (int32_t)(c->n[a + r] >> 32);
       cw[r * 4 + 3] = kr ? 1 : 0;
     }
-    cudaError_t e = launch_select(v, q_idx + (size_t)a * d.Kmax * d.idx_row, nullptr,
-                                  topk_out + (size_t)a * KK, dom_g, wg.data(), act_g,
-                                  c->cfg.topk_pass, sg, &c->timer);
+    // The groups' selections run one after another: a group's indexer starts
+    // once the previous group's top-k has finished (each indexer alone
+    // streams HBM at full rate), and the previous group's union/probe,
+    // gather and attention, sized to fit beside two indexer CTAs on an SM
+    // (the attention on few SMs), overlap this group's indexer.
+    cudaError_t e = cudaSuccess;
+    if (fork && prev_sel >= 0) e = cudaStreamWaitEvent(sg, c->gsel[prev_sel], 0);
     if (e == cudaSuccess)
-      e = launch_resolve(v, topk_out + (size_t)a * KK, loc_out + (size_t)a * KK, 1, 1, tick, sg,
+      e = launch_select(v, q_idx + (size_t)a * d.Kmax * d.idx_row, nullptr,
+                        topk_out + (size_t)a * KK, dom_g, wg.data(), act_g, c->cfg.topk_pass, sg,
+                        &c->timer);
+    if (e == cudaSuccess && fork) e = cudaEventRecord(c->gsel[g], sg);
+    prev_sel = g;
+    if (e == cudaSuccess)
+      e = launch_resolve(v, topk_out + (size_t)a * KK, loc_out + (size_t)a * KK, 1, 0, tick, sg,
                          &c->timer);
+    if (e == cudaSuccess)
+      e = launch_gather(v, topk_out + (size_t)a * KK, loc_out + (size_t)a * KK, 1, tick, sg,
+                        &c->timer);
     const size_t qoff = (size_t)a * d.Kmax * d.Hq;
     if (e == cudaSuccess)
       e = !c->fused ? launch_attend(v, q16 + qoff * d.dqk, b16 + (size_t)a * d.Kmax * d.row,

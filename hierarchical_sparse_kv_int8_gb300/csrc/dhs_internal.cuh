@@ -92,6 +92,8 @@ struct DevCtx {
   int32_t *promo_dst;   // [N][B]: hot slot taken by miss p (p < P)
   uint32_t *now_bits;   // [N][ceil(B/32)]: hot slots stamped by this tick
   int32_t *lru_next;    // [N][B]: the LRU order being rebuilt
+  int32_t *uspill;      // [N][slices][...] union/probe scratch of slices whose
+                        // union outgrows shared memory (or nullptr: never)
   int32_t *inst;        // [N][Kmax*k] per-query mode: hot slot a staged entry
                         // also fills, else -1 (written for staged entries only)
   int32_t *topk_last;   // [N][Kmax][k] selection seen by the last resolve
@@ -174,9 +176,32 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
+  // the stream's priority travels with the launch (also into captured graphs)
+  int prio = 0;
+  if (cudaStreamGetPriority(s, &prio) != cudaSuccess) prio = 0;
+  at[1].id = cudaLaunchAttributePriority;
+  at[1].val.priority = prio;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
+}
+// An ordinary launch (no early start) with the stream's priority.
+template <typename... P, typename... A>
+cudaError_t launch_prio(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                        A &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  int prio = 0;
+  if (cudaStreamGetPriority(s, &prio) != cudaSuccess) prio = 0;
+  at[0].id = cudaLaunchAttributePriority;
+  at[0].val.priority = prio;
   cfg.attrs = at;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
@@ -200,6 +225,12 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, const int8_t *q_
                           int active_queries, int topk_pass, cudaStream_t s, class Timer *tm);
 cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_out,
                            int shared, int gather, int tick, cudaStream_t s, class Timer *tm);
+// The shared host gather alone (launch_resolve with gather = 1 issues the
+// union/probe and then this).
+cudaError_t launch_gather(const DevCtx &c, const int32_t *topk, int32_t *loc_out, int shared,
+                          int tick, cudaStream_t s, class Timer *tm);
+// int32 words of union/probe scratch per request slot (0: none needed).
+size_t union_spill_ints_per_request(const DevCtx &c);
 cudaError_t launch_uattn(const DevCtx &c, const uint16_t *q, const uint16_t *block,
                          uint16_t *out, float *lse, cudaStream_t s, class Timer *tm);
 bool uattn_supported(const DevCtx &c);

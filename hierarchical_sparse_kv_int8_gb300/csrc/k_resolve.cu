@@ -20,7 +20,15 @@
 
 namespace dhs {
 
-constexpr int kUnionThreads = 1024;
+// 512 threads with at most 64 registers each (half an SM's registers) and a
+// shared-memory footprint kept under kUnionSmemBudget, so that a probe CTA
+// fits on an SM beside two indexer CTAs of another request group.
+constexpr int kUnionThreads = 512;
+constexpr int kUnionSmemBudget = 96 * 1024;
+// Union rows of one slice held in shared memory; a slice with more (a union
+// concentrated in one part of the history) keeps its rows, locations and
+// query masks in a global scratch area of its own instead.
+constexpr int kUnionCap = 4096;
 
 __device__ __forceinline__ int ublock_excl_scan(int v, int *warp_sums, int &total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -75,24 +83,36 @@ __host__ __device__ static inline int union_slice(int64_t s_max) {
   return (int)((((s_max + kUnionSlices - 1) / kUnionSlices) + 31) & ~31);
 }
 
+// Union rows a slice keeps in shared memory.
+__host__ __device__ inline int union_cap(const DevCtx &c) { return min(c.Kmax * c.k, kUnionCap); }
 // Shared memory of one CTA without, and with, the slice's hot and optional
 // map entries; the entries are kept (fetched while the bitmap is built) when
-// they fit.
+// they fit the budget.
 __host__ __device__ inline size_t union_base_bytes(const DevCtx &c) {
   const int slice = union_slice(c.Sm);
   const size_t sw = (size_t)slice / 32;  // words of one slice
   const size_t pw = (size_t)((c.B + 31) / 32);
-  const size_t KK = (size_t)c.Kmax * c.k;
-  return sw * 8 + pw * 8 + (size_t)c.B * 8 + KK * 8 + (KK + 3) / 4 * 4;
+  const size_t uc = (size_t)union_cap(c);
+  return sw * 8 + pw * 8 + (size_t)c.B * 8 + uc * 8 + (uc + 3) / 4 * 4;
 }
 __host__ __device__ inline bool union_map_prefetch(const DevCtx &c) {
-  return union_base_bytes(c) + (size_t)union_slice(c.Sm) * 8 <= kMaxDynSmem;
+  return union_base_bytes(c) + (size_t)union_slice(c.Sm) * 8 <= (size_t)kUnionSmemBudget;
+}
+// Global scratch of a slice whose union outgrows union_cap: rows and
+// locations (Kmax * k each) and the query-mask bytes; none when the cap
+// covers every selection of a request.
+__host__ __device__ inline size_t union_spill_ints(const DevCtx &c) {
+  const size_t KK = (size_t)c.Kmax * c.k;
+  return KK > (size_t)kUnionCap ? 2 * KK + (KK + 3) / 4 : 0;
+}
+size_t union_spill_ints_per_request(const DevCtx &c) {
+  return union_spill_ints(c) * kUnionSlices;
 }
 size_t union_smem_bytes(const DevCtx &c) {
   return union_base_bytes(c) + (union_map_prefetch(c) ? (size_t)union_slice(c.Sm) * 8 : 0);
 }
 
-__global__ void __cluster_dims__(kUnionCluster, 1, 1) __launch_bounds__(kUnionThreads)
+__global__ void __cluster_dims__(kUnionCluster, 1, 1) __launch_bounds__(kUnionThreads, 2)
 k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restrict__ loc_out,
               int shared, int tick) {
   namespace cg = cooperative_groups;
@@ -129,12 +149,13 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   uint32_t *now = prot + pw;  // slots stamped by this tick (likewise)
   int32_t *candB = reinterpret_cast<int32_t *>(now + pw);
   int32_t *lru_s = candB + B;  // leader: LRU order at the start of the call
+  const int ucap = union_cap(c);
+  // (these three move to the slice's global scratch when its union outgrows ucap)
   int32_t *ul = lru_s + B;     // location of each union row of this slice
-  int32_t *urow = ul + KK;     // the slice's union rows, by union index
-  uint32_t *umw = reinterpret_cast<uint32_t *>(urow + KK);  // query masks, one byte per union row
-  const int umw_words = (KK + 3) / 4;
+  int32_t *urow = ul + ucap;   // the slice's union rows, by union index
+  uint32_t *umw = reinterpret_cast<uint32_t *>(urow + ucap);  // query masks, one byte per union row
   const bool pf = union_map_prefetch(c);
-  int32_t *hmap_s = reinterpret_cast<int32_t *>(umw + umw_words);  // slice's hot-map entries (when pf)
+  int32_t *hmap_s = reinterpret_cast<int32_t *>(umw + (ucap + 3) / 4);  // slice's hot-map entries (when pf)
   int32_t *omap_s = hmap_s + slice;
 
   const int32_t *tk = topk + (size_t)r * KK;
@@ -170,7 +191,6 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
 
   // 1. union bitmap of this CTA's slice
   for (int i = tid; i < sw; i += bs) bm[i] = 0;
-  for (int i = tid; i < umw_words; i += bs) umw[i] = 0;
   for (int i = tid; i < 2 * pw; i += bs) prot[i] = 0;  // prot and now
   if (tid < 6) sh_cnt[tid] = 0;
   __syncthreads();
@@ -204,6 +224,13 @@ k_union_probe(const DevCtx c, const int32_t *__restrict__ topk, int32_t *__restr
   int Uc;
   {
     int q = ublock_excl_scan(cnt, warp_sums, Uc);
+    if (Uc > ucap) {  // (the same in every thread; only slice CTAs have rows)
+      int32_t *sp = c.uspill + ((size_t)r * kUnionSlices + (crank - 1)) * union_spill_ints(c);
+      ul = sp;
+      urow = sp + KK;
+      umw = reinterpret_cast<uint32_t *>(sp + 2 * (size_t)KK);
+    }
+    for (int i = tid; i < (Uc + 3) / 4; i += bs) umw[i] = 0;
     for (int w = w0; w < w1; ++w) {
       wp[w] = q;
       for (uint32_t bits = bm[w]; bits; bits &= bits - 1)
@@ -517,8 +544,10 @@ k_gather(const DevCtx c, const int32_t *__restrict__ topk, const int32_t *__rest
   constexpr int kGatherVec = GatherShape<VEC>::kGatherVec;
   constexpr int kGatherBatch = GatherShape<VEC>::kGatherBatch;
   __shared__ int warp_sums[32];
+  // (no early trigger: the attention that follows waits for every gathered
+  // row, so launched early its CTAs would only hold SMs, and their shared
+  // memory, that another request group's kernels can use meanwhile)
   pdl_wait();
-  pdl_trigger();
   const int r = blockIdx.y;
   const int Kr = c.Kr[r];
   if (Kr == 0) return;
@@ -606,6 +635,12 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
                  union_smem_bytes(c), s, c, topk, loc_out, shared, tick);
   if (tm) tm->end(K_UNION_PROBE, s);
   if (e != cudaSuccess || !gather) return e;
+  return launch_gather(c, topk, loc_out, shared, tick, s, tm);
+}
+
+cudaError_t launch_gather(const DevCtx &c, const int32_t *topk, int32_t *loc_out, int shared,
+                          int tick, cudaStream_t s, Timer *tm) {
+  cudaError_t e = cudaSuccess;
   const int vec = (c.row * 2 + 511) / 512;
   if (vec > kGatherMaxVec) return cudaErrorInvalidValue;
   void (*kern)(const DevCtx, const int32_t *, const int32_t *, int, int) =
@@ -617,9 +652,9 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
   }
   // One CTA per SM, one resident wave over the whole device: 8 warps with
   // 4-8 rows in flight each saturate the host link (far more than its
-  // bandwidth-delay product), and the registers of two attention CTAs stay
-  // free on every SM, so the attention launch that follows works on its
-  // resident rows while the gather runs.
+  // bandwidth-delay product), and with no shared memory and a quarter of the
+  // registers a CTA leaves room for other kernels (another request group's
+  // indexer) on its SM.
   int blocks_per_req = (c.sms + c.N - 1) / c.N;
   if (blocks_per_req < 1) blocks_per_req = 1;
   dim3 grid(blocks_per_req, c.N);
@@ -627,8 +662,7 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
   // An ordinary launch: its CTAs are placed once the union/probe has left the
   // SMs, one per SM; placed early they would crowd onto the SMs the
   // union/probe leaves free and keep attention CTAs off them.
-  kern<<<grid, kGatherWarps * 32, 0, s>>>(c, topk, loc_out, shared, tick);
-  e = cudaGetLastError();
+  e = launch_prio(kern, grid, dim3(kGatherWarps * 32), 0, s, c, topk, loc_out, shared, tick);
   if (tm) tm->end(K_GATHER, s);
   return e;
 }

@@ -1045,6 +1045,9 @@ constexpr int kRowCap = 4096;      // candidates: 4096 keys of 8 bytes
 constexpr int kRowUnroll = 4;      // 16-byte loads in flight per thread in a pass
 constexpr int kRowSampleMin = 32768;  // domains from which the threshold is estimated
 constexpr int kRowSampleStride = 16;  // one 128-row chunk in 16 is sampled
+constexpr int kRowQueue = 64;         // loads a warp queues in the stash pass
+constexpr int kRowAhead = 2;          // pass steps prefetched into L2 ahead of the loads
+static_assert(kRowWarps * kRowQueue * 20 <= (4 << kRadixBits), "the queues fit the histogram area");
 constexpr size_t kRowSmem = (size_t)kRowCap * 8 + ((size_t)1 << kRadixBits) * 4;
 static_assert(kMaxTopk <= kRowCap, "the rows above the threshold always fit the candidates");
 
@@ -1150,39 +1153,100 @@ k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
   // cand[] as (~v << 32 | row) by one pass over the domain with several
   // 16-byte loads in flight per thread; sh_cnt counts them all, and only the
   // first kRowCap are stored.  A load's four scores are tested at once
-  // against lo + t (at most hi: no overflow); only the lanes holding a row
-  // at or above it look at single rows (the last load of the domain may
-  // hold rows past its end, which they skip).
+  // against lo + t (at most hi: no overflow); the loads holding a row at or
+  // above it go to the warp's queue (kRowQueue loads and their first rows, in
+  // the histogram area, which the pass does not use), and every 32 queued
+  // loads are taken one per lane, so that single rows are looked at by
+  // converged lanes (the last load of the domain may hold rows past its end,
+  // which are skipped there).
+  // One pass step of the CTA covers kRowStep rows; step `it`'s scores are
+  // prefetched into L2 kRowAhead steps before the warps load them (the row
+  // is padded to a multiple of 32 entries, so the rounded end stays inside).
+  constexpr int kRowStep = kRowWarps * 128 * kRowUnroll;
+  auto prefetch_step = [&](int it) {
+    const int r0 = it * kRowStep;
+    if (r0 >= dom) return;
+    const int r1 = min((dom + 3) & ~3, r0 + kRowStep);
+    bulk_prefetch_l2(sc + r0, (uint32_t)(r1 - r0) * 4u);
+  };
   auto stash = [&](uint32_t t) {
     const int thr = lo + (int)t;
-    for (int s0 = wid * 128; s0 < dom; s0 += kRowWarps * 128 * kRowUnroll) {
+    int4 *qx = reinterpret_cast<int4 *>(hist) + wid * kRowQueue;
+    int *qs = reinterpret_cast<int *>(hist) + kRowWarps * kRowQueue * 4 + wid * kRowQueue;
+    const unsigned lt = (1u << lane) - 1u;
+    int qn = 0;  // queued loads (the same in every lane)
+    auto drain = [&](int m) {
+      __syncwarp();
+      int4 y = make_int4(0, 0, 0, 0);
+      int sy = dom;
+      if (lane < m) {
+        y = qx[lane];
+        sy = qs[lane];
+      }
+      const int yv[4] = {y.x, y.y, y.z, y.w};
+      bool kp4[4];
+      int n = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kp4[e] = sy + e < dom && yv[e] >= thr;
+        n += kp4[e];
+      }
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y2 = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y2;
+      }
+      int base = 0;
+      if (lane == 31 && incl > 0) base = atomicAdd(&sh_cnt, incl);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      int pos = base + incl - n;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (!kp4[e]) continue;
+        if (pos < kRowCap)
+          cand[pos] = ((unsigned long long)(0xFFFFFFFFu - (uint32_t)(yv[e] - lo)) << 32) |
+                      (uint32_t)(sy + e);
+        ++pos;
+      }
+      // the loads queued after the first m move to the front
+      const int rest = qn - m;
+      int4 z = make_int4(0, 0, 0, 0);
+      int sz = 0;
+      if (lane < rest) {
+        z = qx[m + lane];
+        sz = qs[m + lane];
+      }
+      __syncwarp();
+      if (lane < rest) {
+        qx[lane] = z;
+        qs[lane] = sz;
+      }
+      qn = rest;
+    };
+    for (int s0 = wid * 128, it = 0; s0 < dom; s0 += kRowStep, ++it) {
+      if (tid == 0) prefetch_step(it + kRowAhead);
       int4 x[kRowUnroll];
 #pragma unroll
       for (int u = 0; u < kRowUnroll; ++u) {
         const int s = s0 + u * kRowWarps * 128 + 4 * lane;
         x[u] = s < dom ? load4(s) : make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
       }
-      unsigned um = 0;
-#pragma unroll
-      for (int u = 0; u < kRowUnroll; ++u)
-        um |= (unsigned)(max(max(x[u].x, x[u].y), max(x[u].z, x[u].w)) >= thr) << u;
-      if (!__any_sync(0xffffffffu, um != 0)) continue;
-      if (um == 0) continue;
 #pragma unroll
       for (int u = 0; u < kRowUnroll; ++u) {
-        if (!((um >> u) & 1u)) continue;
-        const int s = s0 + u * kRowWarps * 128 + 4 * lane;
-        const int xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (xv[e] < thr || s + e >= dom) continue;
-          const int pos = atomicAdd(&sh_cnt, 1);
-          if (pos < kRowCap)
-            cand[pos] = ((unsigned long long)(0xFFFFFFFFu - (uint32_t)(xv[e] - lo)) << 32) |
-                        (uint32_t)(s + e);
+        const bool h = max(max(x[u].x, x[u].y), max(x[u].z, x[u].w)) >= thr;
+        const unsigned bal = __ballot_sync(0xffffffffu, h);
+        if (!bal) continue;
+        if (h) {
+          const int p = qn + __popc(bal & lt);
+          qx[p] = x[u];
+          qs[p] = s0 + u * kRowWarps * 128 + 4 * lane;
         }
+        qn += __popc(bal);
+        if (qn >= 32) drain(32);
       }
     }
+    while (qn > 0) drain(min(qn, 32));
   };
   // hist[0..nbins) = 0 (16-byte stores; the area holds 2^13 bins)
   auto zero_hist = [&](int nbins) {
@@ -1287,6 +1351,8 @@ k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
     // the true threshold, so the list follows from the stash alone and the
     // scores are read once; otherwise the exact passes below run.
     const int sh = max(0, shift - kRadixBits), nb = 1 << min(kRadixBits, shift);
+    if (tid == 0)
+      for (int it = 0; it < kRowAhead; ++it) prefetch_step(it);
     zero_hist(nb);
     __syncthreads();
     constexpr int kSampleStep = 128 * kRowSampleStride;
@@ -1517,6 +1583,7 @@ k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
 // operands see the same permutation and the dot products are unchanged.
 constexpr int kTcWarps = 4;
 constexpr int kTcMaxStages = 8;
+constexpr int kTcTilesPerWarp = 48;  // tiles of a warp in launches larger than one wave
 constexpr int kTcSpinLimit = 1 << 22;
 constexpr int kTcMinGroups = 3;                     // always for rows of 192 B and more
 constexpr size_t kTcNarrowBytes = (size_t)256 << 20;  // 64/128-B rows: from 256 MB of keys
@@ -1766,8 +1833,12 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, const int8_t *q_
     // rows of up to 128 bytes: a smaller ring per warp, so that twice as many
     // CTAs (warps to issue the conversions and MMAs) fit on an SM with about
     // the same bytes in flight (measured on 64 histories of 524 288 rows of
-    // 128 bytes: 1.08 -> 0.85 ms)
-    const size_t ring_budget = ng <= 2 ? (36u << 10) : (110u << 10);
+    // 128 bytes: 1.08 -> 0.85 ms).  Wider rows: two stages per warp (64 KB
+    // a CTA for 512-byte rows, still about twice the bytes in flight HBM
+    // needs per SM), which leaves an SM with two indexer CTAs room for a
+    // top-k or union/probe CTA of another request group (measured on 128
+    // histories of 102 400 rows of 512 bytes: 1.054 -> 1.030 ms alone)
+    const size_t ring_budget = ng <= 2 ? (36u << 10) : (70u << 10);
     const int stages = (int)std::min<size_t>(kTcMaxStages, std::max<size_t>(2, ring_budget / stage_set));
     const size_t smem = stage_set * stages + (size_t)(c.N + 1) * 4;
     TcKern kern = kerns[ng - 1];
@@ -1780,8 +1851,20 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, const int8_t *q_
       grid_of[ng - 1] = c.sms * std::max(1, per_sm);
       grid_smem[ng - 1] = smem;
     }
+    // at least one resident wave; larger launches are cut into CTAs of
+    // kTcTilesPerWarp tiles per warp, so that SMs free up while the launch
+    // runs and kernels of other streams (request groups) get onto them
+    int64_t tiles = 0;
+    for (int r = 0; r < c.N; ++r) {
+      int dm = 0;
+      for (int j = 0; j < ctl_words[r]; ++j) dm = std::max(dm, ctl_words[c.N + r * c.Kmax + j]);
+      tiles += (dm + 15) / 16;
+    }
+    const int64_t per_cta = (int64_t)kTcWarps * kTcTilesPerWarp;
+    const int grid = (int)std::max<int64_t>(grid_of[ng - 1],
+                                            std::min<int64_t>((tiles + per_cta - 1) / per_cta, 1 << 30));
     if (tm) tm->begin(K_SCORE, s);
-    e = launch_pdl(kern, dim3(grid_of[ng - 1]), dim3(kTcWarps * 32), smem, s, c, q_idx, ctl, stages);
+    e = launch_pdl(kern, dim3(grid), dim3(kTcWarps * 32), smem, s, c, q_idx, ctl, stages);
     if (tm) tm->end(K_SCORE, s);
     if (e != cudaSuccess) return e;
   } else {

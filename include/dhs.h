@@ -334,7 +334,11 @@ int dhs_snapshot_free(dhs_ctx *ctx, int32_t snapshot_id);
  * independent ([ADHS] eq. (6): the union, misses and cache state are per
  * request), so one group's host gather (bound by the host link) can run while
  * another group's indexer (bound by HBM) runs -- the overlap of the copy path
- * with compute of [ADHS] 3.2 / 4.3.2.  Results equal those of the separate
+ * with compute of [ADHS] 3.2 / 4.3.2.  The groups' selections run one
+ * after another (group g's indexer starts when group g - 1's top-k has
+ * finished), the internal streams have decreasing priorities in group order,
+ * and the rest of each group's round overlaps the next group's indexer.
+ * Results equal those of the separate
  * calls; the LRU clock advances once per call.  Forking and joining use CUDA
  * events, which stream capture turns into graph dependencies.  Not for
  * contexts on shared arenas or followers (DHS_ERR_INVALID); with the union
