@@ -71,6 +71,8 @@ _SIGS = {
                      ctypes.c_void_p], ctypes.c_int),
     "dhs_attend": ([ctypes.c_void_p] * 6 + [ctypes.c_void_p], ctypes.c_int),
     "dhs_commit": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "dhs_append_keys": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+                        ctypes.c_int),
     "dhs_set_residency": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                            ctypes.c_void_p], ctypes.c_int),
     "dhs_policy_create": ([ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(ctypes.c_void_p)],
@@ -377,6 +379,13 @@ class Context:
     def commit(self, accepted_len, stream=None):
         a = _host_i32(accepted_len, self.cfg.n_slots)
         self._check(self._lib.dhs_commit(self.h, _host_ptr(a), _stream(stream)), "dhs_commit")
+
+    def append_keys(self, accepted_len, block_idx_keys, stream=None):
+        """Index keys of the rows the coming commit keeps (device int8
+        [n_slots][k_max][idx_row]) into the bound key buffers."""
+        a = _host_i32(accepted_len, self.cfg.n_slots)
+        self._check(self._lib.dhs_append_keys(self.h, _host_ptr(a), _dptr(block_idx_keys),
+                                              _stream(stream)), "dhs_append_keys")
 
     def set_residency(self, slot, rows, stream=None):
         rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))

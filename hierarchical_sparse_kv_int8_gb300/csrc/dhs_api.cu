@@ -987,6 +987,34 @@ int dhs_commit(dhs_ctx *c, const int32_t *accepted_len, dhs_stream stream) {
   return order_leave(c, s);
 }
 
+int dhs_append_keys(dhs_ctx *c, const int32_t *accepted_len, const int8_t *block_idx_keys,
+                    dhs_stream stream) {
+  if (!c || !accepted_len || !block_idx_keys || !aligned16(block_idx_keys)) return DHS_ERR_INVALID;
+  if (c->role == DHS_ROLE_FOLLOWER) return DHS_ERR_INVALID;
+  const DevCtx &d = c->d;
+  bool any = false;
+  for (int r = 0; r < d.N; ++r) {
+    const int a = accepted_len[r];
+    if (a < 0 || a > d.Kmax || (a > 0 && !c->bound[r])) return DHS_ERR_INVALID;
+    if (c->n[r] + a > d.Sm) return DHS_ERR_CAPACITY;
+    any = any || a > 0;
+  }
+  if (!any) return DHS_OK;
+  std::vector<int32_t> w(d.N * 4, 0);
+  for (int r = 0; r < d.N; ++r) {
+    w[r * 4 + 0] = accepted_len[r];
+    w[r * 4 + 1] = (int32_t)(uint32_t)(c->n[r] & 0xFFFFFFFF);
+    w[r * 4 + 2] = (int32_t)(c->n[r] >> 32);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (int rc = order_enter(c, s)) return rc;
+  {
+    cudaError_t e_ = launch_append_keys(d, block_idx_keys, w.data(), s);
+    if (e_ != cudaSuccess) return cuda_fail(c, e_);
+  }
+  return order_leave(c, s);
+}
+
 int dhs_set_residency(dhs_ctx *c, int32_t slot, const int32_t *rows, int64_t n_rows,
                       dhs_stream stream) {
   if (!c || slot < 0 || slot >= c->d.N || n_rows < 0 || (n_rows > 0 && !rows))

@@ -245,6 +245,9 @@ cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *bl
                           cudaStream_t s, class Timer *tm);
 cudaError_t launch_commit(const DevCtx &c, const int32_t *aux_words, cudaStream_t s,
                           class Timer *tm);
+// aux: a_r and n_r per slot, as launch_commit's first three words.
+cudaError_t launch_append_keys(const DevCtx &c, const int8_t *block, const int32_t *aux_words,
+                               cudaStream_t s);
 cudaError_t launch_residency(const DevCtx &c, int slot, int64_t old_count, int64_t new_count,
                              cudaStream_t s, class Timer *tm);
 cudaError_t launch_bind_reset(const DevCtx &c, int slot, int64_t n_committed, cudaStream_t s,

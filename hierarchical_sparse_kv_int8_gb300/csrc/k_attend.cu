@@ -47,6 +47,41 @@ cudaError_t launch_commit(const DevCtx &c, const int32_t *aux_words, cudaStream_
   return e;
 }
 
+// ---------------------------------------------------------------- index keys of kept rows
+// aux[r*4 + 0] = a_r, aux[r*4 + 1..2] = n_r (lo, hi words): key rows 0..a_r-1
+// of slot r's block go to rows n_r .. n_r + a_r - 1 of its bound key buffer
+// (16-byte vectors when a key row is a multiple of 16 bytes; both buffers are
+// 16-byte aligned).
+__global__ void __launch_bounds__(256) k_append_keys(const DevCtx c, const int8_t *__restrict__ block,
+                                                     const __grid_constant__ UploadWords aux) {
+  const int r = blockIdx.y;
+  const int a = aux.w[r * 4 + 0];
+  if (a == 0) return;
+  const int64_t n = (int64_t)(uint32_t)aux.w[r * 4 + 1] | ((int64_t)aux.w[r * 4 + 2] << 32);
+  const size_t bytes = (size_t)a * c.idx_row;
+  const int8_t *src = block + (size_t)r * c.Kmax * c.idx_row;
+  int8_t *dst = const_cast<int8_t *>(c.keys[r]) + (size_t)n * c.idx_row;
+  if ((c.idx_row & 15) == 0) {
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    for (size_t i = threadIdx.x; i < bytes / 16; i += blockDim.x) d4[i] = s4[i];
+  } else {
+    for (size_t i = threadIdx.x; i < bytes; i += blockDim.x) dst[i] = src[i];
+  }
+}
+
+cudaError_t launch_append_keys(const DevCtx &c, const int8_t *block, const int32_t *aux_words,
+                               cudaStream_t s) {
+  UploadWords aux;
+  for (int i = 0; i < c.N * 4; ++i) aux.w[i] = aux_words[i];
+  static bool carved = false;
+  if (!carved) {
+    same_carveout(k_append_keys);
+    carved = true;
+  }
+  return launch_prio(k_append_keys, dim3(1, c.N), dim3(256), 0, s, c, block, aux);
+}
+
 // ---------------------------------------------------------------- residency
 __global__ void k_res_clear(const DevCtx c, int slot, int64_t old_count) {
   int32_t *map = c.opt_map + (size_t)slot * c.Sm;

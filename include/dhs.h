@@ -255,6 +255,25 @@ int dhs_attend(dhs_ctx *ctx, const void *q, const void *block_kv, const int32_t 
  * DHS_ERR_CAPACITY if n_r + a_r > s_max; nothing changes on error. */
 int dhs_commit(dhs_ctx *ctx, const int32_t *accepted_len, dhs_stream stream);
 
+/* Index keys of committed rows, [ADHS] 3.3 (kept rows join the immutable
+ * history) with 2.2 (the compact indexer state of the history stays on the
+ * GPU): the rows a commit keeps take their index keys with them.
+ *   accepted_len    host int32 [n_slots]: a_r, the rows this round's commit
+ *                   keeps (0 for idle or unbound slots)
+ *   block_idx_keys  device int8 [n_slots][k_max][idx_heads * idx_dim], 16-byte
+ *                   aligned: the index keys the target computed for positions
+ *                   n_r .. n_r + K_r - 1
+ * Copies block_idx_keys[r][u] to row n_r + u of the index-key buffer bound to
+ * slot r (dhs_bind_request; it must be writable device memory), u < a_r, with
+ * n_r the slot's committed history when the call is issued: issue it before
+ * the round's dhs_commit, or before dhs_round.  The indexer reads rows below
+ * n_r only, so later rounds see the keys and this round is unaffected.
+ * DHS_ERR_INVALID if a_r < 0 or a_r > k_max, a_r > 0 on an unbound slot, or
+ * the context is a follower (it holds no keys); DHS_ERR_CAPACITY if
+ * n_r + a_r > s_max; nothing is copied on error. */
+int dhs_append_keys(dhs_ctx *ctx, const int32_t *accepted_len, const int8_t *block_idx_keys,
+                    dhs_stream stream);
+
 /* Optional residency, [ADHS] 3.1: make `rows` (host int32 [n_rows], distinct,
  * each < n_r) the ready optional history of `slot`; rows[i] occupies pool slot
  * i.  Bytes are copied from the host backing first and the map entries

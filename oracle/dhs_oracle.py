@@ -25,6 +25,10 @@ other than this file):
                                            (a library routine), closed forms
   commit / rollback                        Fig. 3 example, stage-K-then-commit-a
                                            equals stage-a-then-commit-a
+  append_keys                              kept rows' key rows equal the block's,
+                                           the rest untouched; the next round's
+                                           hand-computed maximum score puts exactly
+                                           the kept rows first
   source sharing (adopt, Reindex, Reuse)   a follower's attention equals attention
                                            over its own rows at the producer's
                                            positions; a Reindex selection misses
@@ -499,6 +503,27 @@ class Oracle:
                 q.host[q.n + u] = q.ring[(q.n + u) % c.R_d]
             q.n += a
             q.K = 0
+
+    # -- index keys of kept rows, [ADHS] 3.3 with 2.2 ----------------------
+    def append_keys(self, accepted: np.ndarray, block_keys: np.ndarray):
+        """Rows a commit keeps join the history with their index keys.
+
+        Called before that commit: key row n_r + u of request r becomes
+        block_keys[r][u] for u < a_r (n_r the committed history at the
+        call).  Later rounds score those rows like every other history row;
+        the current round's domains end below n_r.
+        """
+        c = self.cfg
+        for r in range(len(accepted)):
+            a = int(accepted[r])
+            if a < 0 or a > c.k_max or (a > 0 and r not in self.req):
+                raise ValueError("invalid")
+            if a and self.req[r].n + a > c.s_max:
+                raise ValueError("capacity")
+        for r, q in self.req.items():
+            a = int(accepted[r])
+            if a:
+                q.keys[q.n:q.n + a] = block_keys[r, :a]
 
     def ring_live(self, r: int) -> Dict[int, np.ndarray]:
         """Live ring positions [max(first, n - W), n) and their rows."""

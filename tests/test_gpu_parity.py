@@ -608,3 +608,42 @@ def test_round_host_in_request_groups():
         for j in range(int(kr[r])):
             assert torch.equal(out[r, j], want_out[r, j]) and torch.equal(lse[r, j], want_lse[r, j])
     assert run.ctx.stats()["device_error"] == 0
+
+
+# ---------------------------------------------------------------- index keys of kept rows
+@pytest.mark.parametrize("fused", [False, True], ids=["separate_calls", "dhs_round"])
+def test_kept_rows_take_their_index_keys(fused):
+    """dhs_append_keys before each round's commit: the bound key buffers hold
+    the block keys of the kept rows, and later rounds (which score those rows)
+    equal the oracle's, through the separate calls and through dhs_round."""
+    import torch
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+    rec = TINY_GQA
+    run = Runner(rec, attn_pass=UNION, round_groups=2 if fused else 0)
+    slots = list(range(rec.N))
+    o = build_oracle(rec, slots)
+    bkeys = torch.zeros((rec.N, run.Km, rec.idx_row), dtype=torch.int8, device="cuda")
+    for rnd in range(4):
+        kr = rec.k_per_req()
+        acc = rec.accepted(rnd, kr)
+        bk = rec.block_index_keys(rnd, 0, rec.N)
+        bkeys[:, :bk.shape[1]].copy_(torch.from_numpy(bk))
+        run.load_round(rnd)
+        if fused:
+            run.ctx.append_keys(acc, bkeys, run.stream)
+            run.round_fused(kr, acc)
+        else:
+            run.select(kr)
+            run.resolve(True)
+            run.attend()
+            run.ctx.append_keys(acc, bkeys, run.stream)
+            run.commit(acc)
+        ores = oracle_round(o, rec, rnd, slots, kr, None, True)
+        o.append_keys(acc, bk)
+        o.commit(acc)
+        compare_round(run, o, ores, slots, kr, "key append round %d" % rnd)
+        compare_state(run, o, slots, "key append round %d" % rnd)
+        keys = run.keys.cpu().numpy()
+        for r in slots:
+            assert np.array_equal(keys[r], o.req[r].keys), "key rows r=%d round %d" % (r, rnd)
+    assert run.ctx.stats()["device_error"] == 0

@@ -579,3 +579,51 @@ def test_reuse_consumer_attends_the_inherited_rows():
             rows = o.req[0].host[[int(s) for s in sel[0, j] if s >= 0]]
             assert np.allclose(out[0, j], _direct_attention(c, rows, blk[0], q[0, j], j), atol=1e-12)
     assert o.stats.misses == calls and o.t == 1   # no second resolution
+
+
+# ---------------------------------------------------------------- index keys of kept rows (3.3 with 2.2)
+def test_kept_rows_join_the_history_with_their_index_keys():
+    """Kept rows join the history with the index keys the target computed
+    for them: key row n_r + u becomes block key u (u < a_r), earlier rows and
+    rows past the kept prefix are untouched, and the next round ranks those
+    rows by their keys.  The block keys here point along the sign of the next
+    round's first query with the largest int8 magnitude, so each kept row
+    reaches the maximum possible score 8 * sum|q| (computed here by hand), and
+    the query's list starts with exactly the kept rows in row order."""
+    rng = np.random.default_rng(11)
+    c = _tiny_cfg(n_slots=2, k_max=3, topk=6, s_max=48, budget=8)
+    row = c.idx_heads * c.idx_dim
+    o = Oracle(c)
+    keys = [rng.integers(-8, 9, (c.s_max, row)).astype(np.int8) for _ in range(2)]
+    for r in range(2):
+        o.bind(r, _host(c, r), keys[r], 30)
+    q0 = rng.integers(-8, 9, (2, c.k_max, row)).astype(np.int8)
+    q1 = rng.integers(-8, 9, (2, c.k_max, row)).astype(np.int8)
+    q1[:, 0, 0] = 5  # (no all-zero query)
+    kr = np.array([3, 2], np.int32)
+    sel = o.select(q0, kr)
+    o.resolve(sel, shared=True)
+    o.attend(np.zeros((2, c.k_max, c.q_heads, c.qk_dim), np.uint16),
+             np.zeros((2, c.k_max, c.row_elems), np.uint16))
+    acc = np.array([2, 1], np.int32)
+    block = np.zeros((2, c.k_max, row), np.int8)
+    for r in range(2):
+        block[r, :] = (8 * np.sign(q1[r, 0].astype(np.int64))).astype(np.int8)
+    before = [k.copy() for k in keys]
+    o.append_keys(acc, block)
+    o.commit(acc)
+    for r in range(2):
+        a = int(acc[r])
+        assert np.array_equal(keys[r][:30], before[r][:30])
+        assert np.array_equal(keys[r][30:30 + a], block[r, :a])
+        assert np.array_equal(keys[r][30 + a:], before[r][30 + a:])
+        assert o.req[r].n == 30 + a
+    sel1 = o.select(q1, np.array([1, 1], np.int32))
+    for r in range(2):
+        a = int(acc[r])
+        top = 8 * sum(abs(int(x)) for x in q1[r, 0])
+        for u in range(a):  # the kept rows' scores, element by element
+            assert sum(int(q1[r, 0, e]) * int(keys[r][30 + u, e]) for e in range(row)) == top
+        assert list(sel1[r, 0, :a]) == [30 + u for u in range(a)]
+    with pytest.raises(ValueError):
+        o.append_keys(np.array([4, 0]), block)  # more rows than the block holds

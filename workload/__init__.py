@@ -109,6 +109,7 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 S_KEYS, S_HOST, S_QI_BASE, S_QI_FRESH, S_QI_SEL = 1, 2, 3, 4, 5
 S_QI_XSEL, S_QI_XFRESH, S_QA, S_BLOCK, S_ACCEPT, S_RESID = 6, 7, 8, 9, 10, 11
 S_QI_FSEL, S_QI_FFRESH = 12, 13
+S_BLOCK_KEYS = 14
 ROUND_STRIDE = 1000
 
 
@@ -251,6 +252,15 @@ class Recipe:
         per = self.kmax * self.row_elems
         out = np.empty((r1 - r0, self.kmax, self.row_elems), np.uint16)
         return fill_bf16_normal(out, self.seed, S_BLOCK + ROUND_STRIDE * rnd, (self.req0 + r0) * per)
+
+    def block_index_keys(self, rnd: int, r0: int, r1: int) -> np.ndarray:
+        """int8 [r1-r0][K_max][H_idx*d_idx]: index keys the target computes for
+        the block rows, uniform over i8_lo..i8_hi."""
+        per = self.kmax * self.idx_row
+        out = np.empty((r1 - r0, self.kmax, self.idx_row), np.int8)
+        fill_i8(out, self.seed, S_BLOCK_KEYS + ROUND_STRIDE * rnd, (self.req0 + r0) * per,
+                self.i8_lo, self.i8_hi)
+        return out
 
     def k_per_req(self) -> np.ndarray:
         return np.full(self.N, self.K, np.int32)
