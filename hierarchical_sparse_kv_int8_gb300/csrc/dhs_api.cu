@@ -762,6 +762,9 @@ DevCtx slot_view(const DevCtx &d, int a, int b, int n_split) {
 
 extern "C" {
 
+// Relative sizes of dhs_round's request groups (all but the last, the last).
+constexpr int kGroupWeight = 100, kLastGroupWeight = 60;
+
 int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const void *q,
               const void *block_kv, const int32_t *accepted_len, int32_t *topk_out,
               int32_t *loc_out, void *out, float *lse, dhs_stream stream) {
@@ -796,8 +799,16 @@ int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const v
   const uint16_t *b16 = static_cast<const uint16_t *>(block_kv);
   uint16_t *o16 = static_cast<uint16_t *>(out);
   int prev_sel = -1;  // the last group whose selection was issued
+  // Group g covers slots [edge(g), edge(g + 1)): equal weights, except a
+  // lighter last group, whose gather and attention nothing overlaps (they
+  // end the round); measured on 128 histories of 102 400 rows in four
+  // groups: last weight 1 -> 0.6, 1.876 -> 1.825 ms; 0.4 was slower.
+  const int64_t tot_w = (int64_t)kGroupWeight * (G - 1) + kLastGroupWeight;
+  auto edge = [&](int x) {
+    return x >= G ? d.N : (int)((int64_t)d.N * ((int64_t)kGroupWeight * x) / tot_w);
+  };
   for (int g = 0; g < G; ++g) {
-    const int a = (int)((int64_t)d.N * g / G), b = (int)((int64_t)d.N * (g + 1) / G);
+    const int a = edge(g), b = edge(g + 1);
     if (a == b) continue;
     cudaStream_t sg = fork ? c->gstream[g] : s;
     if (fork && cudaStreamWaitEvent(sg, c->gevent[0], 0) != cudaSuccess)

@@ -348,7 +348,9 @@ int dhs_snapshot_free(dhs_ctx *ctx, int32_t snapshot_id);
  * resolve (shared retrieval), attend and commit, with the shapes of the
  * separate calls (topk_out and loc_out receive the selections and locations).
  * With cfg.round_groups = G > 1 the request slots are split into G contiguous
- * groups whose rounds are issued on G internal streams forked from `stream`
+ * groups (the last one about 0.6 the size of the others, as nothing overlaps
+ * its retrieval and attention) whose rounds are issued on G internal streams
+ * forked from `stream`
  * and joined back into it before the call's work ends: requests are
  * independent ([ADHS] eq. (6): the union, misses and cache state are per
  * request), so one group's host gather (bound by the host link) can run while
