@@ -37,7 +37,8 @@ class Config(ctypes.Structure):
                 ("budget", ctypes.c_int32), ("ring_window", ctypes.c_int32),
                 ("page_rows", ctypes.c_int32), ("opt_rows_max", ctypes.c_int64),
                 ("softmax_scale", ctypes.c_float), ("attn_pass", ctypes.c_int32),
-                ("topk_pass", ctypes.c_int32), ("round_groups", ctypes.c_int32)]
+                ("topk_pass", ctypes.c_int32), ("round_groups", ctypes.c_int32),
+                ("tokens_per_row", ctypes.c_int32)]
 
 ATTN_AUTO, ATTN_PER_QUERY, ATTN_UNION, ATTN_UNION_MMA = 0, 1, 2, 3
 TOPK_AUTO, TOPK_CLUSTER, TOPK_ROW = 0, 1, 2
@@ -73,6 +74,8 @@ _SIGS = {
     "dhs_commit": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "dhs_append_keys": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
                         ctypes.c_int),
+    "dhs_commit_compressed": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                               ctypes.c_void_p], ctypes.c_int),
     "dhs_set_residency": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                            ctypes.c_void_p], ctypes.c_int),
     "dhs_policy_create": ([ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(ctypes.c_void_p)],
@@ -379,6 +382,16 @@ class Context:
     def commit(self, accepted_len, stream=None):
         a = _host_i32(accepted_len, self.cfg.n_slots)
         self._check(self._lib.dhs_commit(self.h, _host_ptr(a), _stream(stream)), "dhs_commit")
+
+    def commit_compressed(self, accepted_len, rows_kv, rows_idx_keys=None, stream=None):
+        """Commit for a source packing tokens_per_row positions into a row:
+        the stored rows the kept positions complete, from the compressor's
+        rows (device bf16 [n_slots][ceil(k_max/m)][row_elems]) and keys
+        (device int8 [n_slots][ceil(k_max/m)][idx_row], or None)."""
+        a = _host_i32(accepted_len, self.cfg.n_slots)
+        self._check(self._lib.dhs_commit_compressed(self.h, _host_ptr(a), _dptr(rows_kv),
+                                                    _dptr(rows_idx_keys), _stream(stream)),
+                    "dhs_commit_compressed")
 
     def append_keys(self, accepted_len, block_idx_keys, stream=None):
         """Index keys of the rows the coming commit keeps (device int8

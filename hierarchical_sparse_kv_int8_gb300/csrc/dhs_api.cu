@@ -138,7 +138,7 @@ struct dhs_arenas {
 
 struct Snapshot {
   std::vector<void *> bufs;
-  std::vector<int64_t> n, ring_first, opt_count;
+  std::vector<int64_t> n, tok, ring_first, opt_count;
   std::vector<int32_t> K;
   int64_t tick;
   int phase;
@@ -152,8 +152,9 @@ struct dhs_ctx {
   bool fused = false;      // shared retrieval attends with the union pass
   int last_shared = 0;     // mode of the last dhs_resolve
   std::vector<void *> allocs;
-  // host mirrors
-  std::vector<int64_t> n, ring_first, opt_count;
+  // host mirrors (n: history rows; tok: committed token positions, = n when m = 1)
+  int m = 1;
+  std::vector<int64_t> n, tok, ring_first, opt_count;
   std::vector<int32_t> K;
   std::vector<char> bound;
   std::vector<const void *> host_ptr;
@@ -335,7 +336,8 @@ int create_impl(const dhs_config *cfg, dhs_arenas *arenas, int arena, int role, 
       g.budget > 65535 || g.ring_window < 1 || g.page_rows < 1 || g.opt_rows_max < 0 ||
       g.opt_rows_max > g.s_max || g.attn_pass < DHS_ATTN_AUTO || g.attn_pass > DHS_ATTN_UNION_MMA ||
       g.topk_pass < DHS_TOPK_AUTO || g.topk_pass > DHS_TOPK_ROW || g.round_groups < 0 ||
-      g.round_groups > g.n_slots || g.round_groups > 16)
+      g.round_groups > g.n_slots || g.round_groups > 16 || g.tokens_per_row < 0 ||
+      g.tokens_per_row > 64)
     return DHS_ERR_INVALID;
   if (g.kv_layout != DHS_KV_SPLIT && g.kv_layout != DHS_KV_LATENT) return DHS_ERR_INVALID;
   if (g.kv_layout == DHS_KV_LATENT && (g.kv_heads != 1 || g.v_dim > g.qk_dim))
@@ -519,7 +521,9 @@ int create_impl(const dhs_config *cfg, dhs_arenas *arenas, int arena, int role, 
     return DHS_ERR_CUDA;
   }
   if (arenas) arenas->users += 1;
+  c->m = g.tokens_per_row > 1 ? g.tokens_per_row : 1;
   c->n.assign(N, 0);
+  c->tok.assign(N, 0);
   c->ring_first.assign(N, 0);
   c->opt_count.assign(N, 0);
   c->K.assign(N, 0);
@@ -627,8 +631,9 @@ int64_t dhs_device_bytes(const dhs_ctx *c) {
 int dhs_bind_request(dhs_ctx *c, int32_t slot, const void *host_kv, const int8_t *idx_keys,
                      int64_t n_committed, dhs_stream stream) {
   if (!c || slot < 0 || slot >= c->d.N || !host_kv || !idx_keys || n_committed < 0 ||
-      n_committed > c->d.Sm || !aligned16(host_kv) || !aligned16(idx_keys))
+      n_committed / c->m > c->d.Sm || !aligned16(host_kv) || !aligned16(idx_keys))
     return DHS_ERR_INVALID;
+  const int64_t rows = n_committed / c->m;  // complete stored rows
   if (c->phase != PH_IDLE) return DHS_ERR_INVALID;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   void *dev_host = nullptr;
@@ -646,11 +651,12 @@ int dhs_bind_request(dhs_ctx *c, int32_t slot, const void *host_kv, const int8_t
     return DHS_ERR_CUDA;
   // the host arrays above are pageable: the copies are staged before returning
   {
-    cudaError_t e_ = launch_bind_reset(c->d, slot, n_committed, s, &c->timer);
+    cudaError_t e_ = launch_bind_reset(c->d, slot, rows, s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
   }
-  c->n[slot] = n_committed;
-  c->ring_first[slot] = n_committed;
+  c->n[slot] = rows;
+  c->tok[slot] = n_committed;
+  c->ring_first[slot] = rows;
   c->opt_count[slot] = 0;
   c->K[slot] = 0;
   c->bound[slot] = 1;
@@ -684,8 +690,9 @@ int round_words(dhs_ctx *c, const int32_t *k_per_req, const int64_t *pos,
     const int kr = k_per_req[r];
     w[r] = kr;
     for (int j = 0; j < kr; ++j) {
-      int64_t p = pos ? pos[(size_t)r * d.Kmax + j] : c->n[r] + j;
-      int64_t dom = std::max<int64_t>(0, std::min<int64_t>(c->n[r], p + 1));
+      // (stored rows complete up to position p: floor((p + 1) / m), eq. (8))
+      const int64_t p = pos ? pos[(size_t)r * d.Kmax + j] : c->tok[r] + j;
+      const int64_t dom = std::max<int64_t>(0, std::min<int64_t>(c->n[r], (p + 1) / c->m));
       w[d.N + r * d.Kmax + j] = (int32_t)dom;
       max_dom = std::max<int>(max_dom, (int)dom);
     }
@@ -772,7 +779,8 @@ int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const v
       !out || !aligned16(q_idx) || !aligned16(block_kv) || ((uintptr_t)q & 3u) ||
       ((uintptr_t)out & 3u))
     return DHS_ERR_INVALID;
-  if (c->phase != PH_IDLE || c->role == DHS_ROLE_FOLLOWER || c->arenas) return DHS_ERR_INVALID;
+  if (c->phase != PH_IDLE || c->role == DHS_ROLE_FOLLOWER || c->arenas || c->m > 1)
+    return DHS_ERR_INVALID;
   const DevCtx &d = c->d;
   std::vector<int32_t> w;
   int max_dom = 0, active = 0;
@@ -867,7 +875,10 @@ int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const v
   c->tick = tick;
   c->last_shared = 1;
   for (int r = 0; r < d.N; ++r) {
-    if (k_per_req[r]) c->n[r] += accepted_len[r];
+    if (k_per_req[r]) {
+      c->n[r] += accepted_len[r];
+      c->tok[r] += accepted_len[r];
+    }
     c->K[r] = 0;
   }
   c->phase = PH_IDLE;
@@ -967,7 +978,7 @@ int dhs_attend(dhs_ctx *c, const void *q, const void *block_kv, const int32_t *l
 
 int dhs_commit(dhs_ctx *c, const int32_t *accepted_len, dhs_stream stream) {
   if (!c || !accepted_len) return DHS_ERR_INVALID;
-  if (c->phase != PH_ATTENDED) return DHS_ERR_INVALID;
+  if (c->phase != PH_ATTENDED || c->m > 1) return DHS_ERR_INVALID;
   const DevCtx &d = c->d;
   for (int r = 0; r < d.N; ++r) {
     if (c->K[r] == 0) continue;
@@ -992,6 +1003,49 @@ int dhs_commit(dhs_ctx *c, const int32_t *accepted_len, dhs_stream stream) {
   for (int r = 0; r < d.N; ++r) {
     if (c->K[r] == 0) continue;
     c->n[r] += accepted_len[r];
+    c->tok[r] += accepted_len[r];
+    c->K[r] = 0;
+  }
+  c->phase = PH_IDLE;
+  return order_leave(c, s);
+}
+
+int dhs_commit_compressed(dhs_ctx *c, const int32_t *accepted_len, const void *rows_kv,
+                          const int8_t *rows_idx_keys, dhs_stream stream) {
+  if (!c || !accepted_len || !rows_kv || !aligned16(rows_kv) ||
+      (rows_idx_keys && !aligned16(rows_idx_keys)))
+    return DHS_ERR_INVALID;
+  if (c->phase != PH_ATTENDED) return DHS_ERR_INVALID;
+  const DevCtx &d = c->d;
+  const int m = c->m;
+  for (int r = 0; r < d.N; ++r) {
+    if (c->K[r] == 0) continue;
+    const int a = accepted_len[r];
+    if (a < 0 || a > c->K[r]) return DHS_ERR_INVALID;
+    if ((c->tok[r] + a) / m > d.Sm) return DHS_ERR_CAPACITY;
+  }
+  // per slot: completed rows, the first of them (lo, hi words), active
+  std::vector<int32_t> w(d.N * 4, 0);
+  for (int r = 0; r < d.N; ++r) {
+    if (c->K[r] == 0) continue;
+    const int64_t lo = c->tok[r] / m, hi = (c->tok[r] + accepted_len[r]) / m;
+    w[r * 4 + 0] = (int32_t)(hi - lo);
+    w[r * 4 + 1] = (int32_t)(uint32_t)(lo & 0xFFFFFFFF);
+    w[r * 4 + 2] = (int32_t)(lo >> 32);
+    w[r * 4 + 3] = 1;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (int rc = order_enter(c, s)) return rc;
+  {
+    cudaError_t e_ = launch_commit_rows(d, static_cast<const uint16_t *>(rows_kv), rows_idx_keys,
+                                        (d.Kmax + m - 1) / m, w.data(), s, &c->timer);
+    if (e_ != cudaSuccess) return cuda_fail(c, e_);
+  }
+  for (int r = 0; r < d.N; ++r) {
+    if (c->K[r] == 0) continue;
+    c->tok[r] += accepted_len[r];
+    c->n[r] = c->tok[r] / m;
+    c->ring_first[r] = c->n[r];
     c->K[r] = 0;
   }
   c->phase = PH_IDLE;
@@ -1001,7 +1055,7 @@ int dhs_commit(dhs_ctx *c, const int32_t *accepted_len, dhs_stream stream) {
 int dhs_append_keys(dhs_ctx *c, const int32_t *accepted_len, const int8_t *block_idx_keys,
                     dhs_stream stream) {
   if (!c || !accepted_len || !block_idx_keys || !aligned16(block_idx_keys)) return DHS_ERR_INVALID;
-  if (c->role == DHS_ROLE_FOLLOWER) return DHS_ERR_INVALID;
+  if (c->role == DHS_ROLE_FOLLOWER || c->m > 1) return DHS_ERR_INVALID;
   const DevCtx &d = c->d;
   bool any = false;
   for (int r = 0; r < d.N; ++r) {
@@ -1154,6 +1208,7 @@ int dhs_snapshot(dhs_ctx *c, int32_t *snapshot_id, dhs_stream stream) {
       return DHS_ERR_CUDA;
   }
   sn.n = c->n;
+  sn.tok = c->tok;
   sn.ring_first = c->ring_first;
   sn.opt_count = c->opt_count;
   sn.K = c->K;
@@ -1202,6 +1257,7 @@ int dhs_restore(dhs_ctx *c, int32_t id, dhs_stream stream) {
   std::vector<int32_t> wk(sn.K.begin(), sn.K.end());
   if (upload_words(c, c->d.Kr, wk, s)) return DHS_ERR_CUDA;
   c->n = sn.n;
+  c->tok = sn.tok;
   c->ring_first = sn.ring_first;
   c->opt_count = sn.opt_count;
   c->K = sn.K;

@@ -246,6 +246,10 @@ cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *bl
 cudaError_t launch_commit(const DevCtx &c, const int32_t *aux_words, cudaStream_t s,
                           class Timer *tm);
 // aux: a_r and n_r per slot, as launch_commit's first three words.
+// rows/keys: [N][cmax][row] bf16 and [N][cmax][idx_row] int8 (keys may be
+// nullptr); aux: completed rows, first row (lo, hi), active, per slot.
+cudaError_t launch_commit_rows(const DevCtx &c, const uint16_t *rows, const int8_t *keys, int cmax,
+                               const int32_t *aux_words, cudaStream_t s, class Timer *tm);
 cudaError_t launch_append_keys(const DevCtx &c, const int8_t *block, const int32_t *aux_words,
                                cudaStream_t s);
 cudaError_t launch_residency(const DevCtx &c, int slot, int64_t old_count, int64_t new_count,

@@ -47,6 +47,56 @@ cudaError_t launch_commit(const DevCtx &c, const int32_t *aux_words, cudaStream_
   return e;
 }
 
+// ---------------------------------------------------------------- commit of completed stored rows
+// aux[r*4 + 0] = rows completed, aux[r*4 + 1..2] = the first of them (lo, hi
+// words), aux[r*4 + 3] = slot active.  Row i of slot r's `rows` (and key row
+// i of `keys`, when given) becomes stored row first + i of the host backing
+// (and of the bound key buffer); the history then ends after the last of
+// them, and the ring holds no history row of the slot.
+__global__ void __launch_bounds__(256) k_commit_rows(const DevCtx c, const uint16_t *__restrict__ rows,
+                                                     const int8_t *__restrict__ keys, int cmax,
+                                                     const __grid_constant__ UploadWords aux) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.y;
+  const int cnt = aux.w[r * 4 + 0];
+  const int64_t first = (int64_t)(uint32_t)aux.w[r * 4 + 1] | ((int64_t)aux.w[r * 4 + 2] << 32);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nv = (c.row * 2) >> 4, nk = c.idx_row >> 4;
+  uint16_t *host = const_cast<uint16_t *>(c.host[r]);
+  int8_t *kdst = const_cast<int8_t *>(c.keys[r]);
+  for (int i = wid; i < cnt; i += 8) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(rows + ((size_t)r * cmax + i) * c.row);
+    uint4 *dst = reinterpret_cast<uint4 *>(host + (size_t)(first + i) * c.row);
+    for (int v = lane; v < nv; v += 32) dst[v] = src[v];
+    if (keys) {
+      const uint4 *ks = reinterpret_cast<const uint4 *>(keys + ((size_t)r * cmax + i) * c.idx_row);
+      uint4 *kd = reinterpret_cast<uint4 *>(kdst + (size_t)(first + i) * c.idx_row);
+      for (int v = lane; v < nk; v += 32) kd[v] = ks[v];
+    }
+  }
+  if (threadIdx.x == 0 && aux.w[r * 4 + 3]) {
+    c.n[r] = first + cnt;
+    c.ring_first[r] = first + cnt;
+    c.Kr[r] = 0;
+  }
+}
+
+cudaError_t launch_commit_rows(const DevCtx &c, const uint16_t *rows, const int8_t *keys, int cmax,
+                               const int32_t *aux_words, cudaStream_t s, Timer *tm) {
+  UploadWords aux;
+  for (int i = 0; i < c.N * 4; ++i) aux.w[i] = aux_words[i];
+  static bool carved = false;
+  if (!carved) {
+    same_carveout(k_commit_rows);
+    carved = true;
+  }
+  if (tm) tm->begin(K_COMMIT, s);
+  cudaError_t e = launch_pdl(k_commit_rows, dim3(1, c.N), dim3(256), 0, s, c, rows, keys, cmax, aux);
+  if (tm) tm->end(K_COMMIT, s);
+  return e;
+}
+
 // ---------------------------------------------------------------- index keys of kept rows
 // aux[r*4 + 0] = a_r, aux[r*4 + 1..2] = n_r (lo, hi words): key rows 0..a_r-1
 // of slot r's block go to rows n_r .. n_r + a_r - 1 of its bound key buffer

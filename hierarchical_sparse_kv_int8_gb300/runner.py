@@ -21,7 +21,8 @@ def config_for(rec, k_max: Optional[int] = None, opt_rows_max: Optional[int] = N
         qk_dim=rec.qk_dim, v_dim=rec.v_dim, kv_layout=rec.kv_layout, budget=rec.B,
         ring_window=rec.W, page_rows=rec.p,
         opt_rows_max=rec.opt_rows_max if opt_rows_max is None else opt_rows_max,
-        softmax_scale=0.0, attn_pass=attn_pass, topk_pass=topk_pass, round_groups=round_groups)
+        softmax_scale=0.0, attn_pass=attn_pass, topk_pass=topk_pass, round_groups=round_groups,
+        tokens_per_row=rec.m)
 
 
 class Runner:
@@ -60,14 +61,14 @@ class Runner:
         self.out = torch.zeros((N, Km, rec.Hq, rec.v_dim), dtype=torch.bfloat16, device=dev)
         self.lse = torch.zeros((N, Km, rec.Hq), dtype=torch.float32, device=dev)
         for r in range(N):
-            self.ctx.bind(r, self.host[r], self.keys[r], rec.S, stream)
+            self.ctx.bind(r, self.host[r], self.keys[r], rec.S * rec.m, stream)
 
     def rebind(self):
         """Bind every slot again at the recipe's history length: empty hot
         cache, no optional rows, no live ring rows (rows the previous rounds
         committed past the history stay in the host tier, unused)."""
         for r in range(self.rec.N):
-            self.ctx.bind(r, self.host[r], self.keys[r], self.rec.S, self.stream)
+            self.ctx.bind(r, self.host[r], self.keys[r], self.rec.S * self.rec.m, self.stream)
 
     def set_residency(self, frac_rows=None):
         for r in range(self.rec.N):
@@ -100,6 +101,18 @@ class Runner:
 
     def commit(self, accepted):
         self.ctx.commit(accepted, self.stream)
+
+    def commit_compressed(self, rnd: int, accepted):
+        """Commit of a compressed source (rec.m > 1) with round ``rnd``'s
+        compressor rows and keys from the recipe."""
+        torch, rec = self.torch, self.rec
+        if not hasattr(self, "crows"):
+            cm = rec.cmax
+            self.crows = torch.zeros((rec.N, cm, rec.row_elems), dtype=torch.int16, device="cuda")
+            self.ckeys = torch.zeros((rec.N, cm, rec.idx_row), dtype=torch.int8, device="cuda")
+        self.crows.copy_(torch.from_numpy(rec.compressed_rows(rnd, 0, rec.N).view(np.int16)))
+        self.ckeys.copy_(torch.from_numpy(rec.compressed_keys(rnd, 0, rec.N)))
+        self.ctx.commit_compressed(accepted, self.crows, self.ckeys, self.stream)
 
     def round_fused(self, k_per_req, accepted):
         """The whole round in one dhs_round call (request groups on internal

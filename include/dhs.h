@@ -107,6 +107,13 @@ typedef struct {
   int32_t attn_pass;    /* attention kernel for shared retrieval, DHS_ATTN_*    */
   int32_t topk_pass;    /* top-k kernel of dhs_select, DHS_TOPK_*               */
   int32_t round_groups; /* dhs_round: request groups on internal streams (0/1 = one) */
+  int32_t tokens_per_row; /* m of [ADHS] eq. (8): token positions packed into one
+                             stored row of this source (0 or 1: uncompressed;
+                             at most 64).  With m > 1 the history, the caches,
+                             s_max and every selected index count stored rows,
+                             n_committed and positions count tokens, and the
+                             rows a round completes are committed with
+                             dhs_commit_compressed. */
 } dhs_config;
 
 /* Top-k kernel of dhs_select.  Both return the same ordered lists:
@@ -273,6 +280,30 @@ int dhs_commit(dhs_ctx *ctx, const int32_t *accepted_len, dhs_stream stream);
  * n_r + a_r > s_max; nothing is copied on error. */
 int dhs_append_keys(dhs_ctx *ctx, const int32_t *accepted_len, const int8_t *block_idx_keys,
                     dhs_stream stream);
+
+/* Commit for a source that packs m = cfg.tokens_per_row token positions into
+ * each stored row, [ADHS] eq. (8) and 3.3.  Keeping a_r of the block's
+ * positions (0 <= a_r <= K_r, as dhs_commit) moves the slot's token count
+ * from n_r to n_r + a_r, and the stored rows
+ *     floor(n_r / m) <= s < floor((n_r + a_r) / m)
+ * become complete (the page garbles the upper bound's bracket; the floor
+ * keeps a partial group in the tail).  Their payload and index keys come
+ * from the model's compressor:
+ *   rows_kv        device bf16 [n_slots][ceil(k_max / m)][row_elems], 16-byte
+ *                  aligned: row i of slot r is stored row floor(n_r / m) + i
+ *   rows_idx_keys  device int8 [n_slots][ceil(k_max / m)][idx_heads*idx_dim],
+ *                  16-byte aligned, or NULL when the caller writes the keys
+ * They join the history: written to the host backing (its backup) and the
+ * bound key buffer, and the history grows to floor((n_r + a_r) / m) rows.
+ * The positions of a partial group stay counted in n_r with no row
+ * published; the draft ring (the block's token rows) serves no history row
+ * of such a source.  Follows dhs_attend like dhs_commit, which (with
+ * dhs_append_keys and dhs_round) refuses contexts with m > 1; with m = 1 this
+ * call commits the caller's rows in place of the ring's.  DHS_ERR_INVALID
+ * as dhs_commit, DHS_ERR_CAPACITY if a history would pass s_max rows;
+ * nothing changes on error. */
+int dhs_commit_compressed(dhs_ctx *ctx, const int32_t *accepted_len, const void *rows_kv,
+                          const int8_t *rows_idx_keys, dhs_stream stream);
 
 /* Optional residency, [ADHS] 3.1: make `rows` (host int32 [n_rows], distinct,
  * each < n_r) the ready optional history of `slot`; rows[i] occupies pool slot

@@ -95,17 +95,29 @@ def staging_bytes(chi: int, N: int, K_max: int, k: int, d_kv: int) -> int:
 # ---------------------------------------------------------------------------
 # Selection, [ADHS] 2.1 eq. (1) and 3.3 eq. (5)
 # ---------------------------------------------------------------------------
-def domain_length(n: int, pos: Optional[int]) -> int:
+def domain_length(n: int, pos: Optional[int], m: int = 1) -> int:
     """Selectable history rows of a query at position ``pos``.
 
     [ADHS] eq. (5) splits the visible set of query j into the committed
     history v < n (served through the hierarchy, hence selectable) and the
     current block, which is read from the tail and not selected.  A query
-    placed inside the history (pos < n) sees rows v <= pos only.
+    placed inside the history (pos < n) sees rows v <= pos only.  For a
+    source packing m token positions into a row (eq. 8), n counts complete
+    rows and row s holds positions s m .. s m + m - 1, so a query at ``pos``
+    sees the complete rows whose last position is at most pos: s < (pos+1)//m.
     """
     if pos is None:
         return n
-    return max(0, min(n, pos + 1))
+    return max(0, min(n, (pos + 1) // m))
+
+
+def completed_rows(n_tok: int, a: int, m: int) -> range:
+    """Source rows a round completes, [ADHS] eq. (8): committing a of the
+    block's positions moves the token frontier from n_tok to n_tok + a, and
+    the rows floor(n_tok / m) <= s < floor((n_tok + a) / m) become complete
+    (the bracket of the equation's upper bound is garbled on the page; the
+    floor is the reading under which a partial group stays in the tail)."""
+    return range(n_tok // m, (n_tok + a) // m)
 
 
 def index_scores(q: np.ndarray, keys: np.ndarray, dom: int) -> np.ndarray:
@@ -187,6 +199,11 @@ class Config:
     page_rows: int = 64
     opt_rows_max: int = 0
     softmax_scale: float = 0.0
+    tokens_per_row: int = 1    # m of [ADHS] eq. (8); 1 = uncompressed
+
+    @property
+    def m(self) -> int:
+        return max(1, self.tokens_per_row)
 
     @property
     def row_elems(self) -> int:
@@ -205,7 +222,7 @@ class Config:
 class Request:
     host: np.ndarray           # bf16 bits [s_max][row_elems]: host backing H_r
     keys: np.ndarray           # int8 [s_max][H_idx*d_idx]: GPU index state
-    n: int                     # committed frontier n_r
+    n: int                     # committed history rows (n_r when m = 1)
     ring_first: int            # first position ever committed through the ring
     hot_row: np.ndarray        # int64 [B], -1 = empty
     hot_stamp: np.ndarray      # int64 [B], -1 = never used
@@ -214,6 +231,7 @@ class Request:
     opt_slot: Dict[int, int] = field(default_factory=dict)
     opt_pool: Optional[np.ndarray] = None
     K: int = 0
+    tok: int = 0               # committed token positions n_r (= n when m = 1)
 
 
 @dataclass
@@ -249,9 +267,10 @@ class Oracle:
 
     # -- binding ---------------------------------------------------------
     def bind(self, slot: int, host: np.ndarray, keys: np.ndarray, n: int):
+        """``n``: committed token positions; the history holds n // m rows."""
         c = self.cfg
         self.req[slot] = Request(
-            host=host, keys=keys, n=n, ring_first=n,
+            host=host, keys=keys, n=n // c.m, ring_first=n // c.m, tok=n,
             hot_row=np.full(c.budget, -1, np.int64),
             hot_stamp=np.full(c.budget, -1, np.int64),
             hot_payload=np.zeros((c.budget, c.row_elems), np.uint16),
@@ -290,7 +309,7 @@ class Oracle:
             q.K = int(k_per_req[r])
             for j in range(q.K):
                 p = None if pos is None else int(pos[r][j])
-                dom = domain_length(q.n, p)
+                dom = domain_length(q.n, p, c.m)
                 sc = index_scores(q_idx[r][j].reshape(-1), q.keys, dom)
                 out[r, j] = topk_ordered(sc, c.topk)
         self.topk = out
@@ -489,6 +508,8 @@ class Oracle:
         are never published: the frontier simply does not pass them.
         """
         c = self.cfg
+        if c.m > 1:
+            raise ValueError("invalid")  # compressed rows come from commit_compressed
         for r, q in self.req.items():
             a = int(accepted[r])
             if q.K and not (0 <= a <= q.K):
@@ -502,6 +523,41 @@ class Oracle:
             for u in range(a):
                 q.host[q.n + u] = q.ring[(q.n + u) % c.R_d]
             q.n += a
+            q.tok += a
+            q.K = 0
+
+    def commit_compressed(self, accepted: np.ndarray, rows: np.ndarray,
+                          row_keys: Optional[np.ndarray] = None):
+        """Commit for a source packing m positions into a row, [ADHS] eq. (8).
+
+        Keeping a_r positions moves the token frontier by a_r; the rows the
+        round completes (``completed_rows``) join the immutable history with
+        the payload and index keys the model's compressor gave them (rows[r][i]
+        and row_keys[r][i] for the i-th completed row), written to the host
+        backing as every committed row is.  A partial group stays in the
+        tail: its positions count, no row of it is published.  Such rows
+        never come from the draft ring (it holds the block's token rows), so
+        the ring serves no history row of a compressed source.
+        """
+        c = self.cfg
+        for r, q in self.req.items():
+            a = int(accepted[r])
+            if q.K and not (0 <= a <= q.K):
+                raise ValueError("invalid")
+            if q.K and (q.tok + a) // c.m > c.s_max:
+                raise ValueError("capacity")
+        for r, q in self.req.items():
+            if q.K == 0:
+                continue
+            a = int(accepted[r])
+            done = completed_rows(q.tok, a, c.m)
+            for i, s in enumerate(done):
+                q.host[s] = rows[r, i]
+                if row_keys is not None:
+                    q.keys[s] = row_keys[r, i]
+            q.tok += a
+            q.n = q.tok // c.m
+            q.ring_first = q.n
             q.K = 0
 
     # -- index keys of kept rows, [ADHS] 3.3 with 2.2 ----------------------
@@ -514,6 +570,8 @@ class Oracle:
         the current round's domains end below n_r.
         """
         c = self.cfg
+        if c.m > 1:
+            raise ValueError("invalid")  # compressed rows bring their keys at commit
         for r in range(len(accepted)):
             a = int(accepted[r])
             if a < 0 or a > c.k_max or (a > 0 and r not in self.req):

@@ -24,13 +24,14 @@ def oracle_config(rec, k_max=None, opt_rows_max=None):
                          idx_heads=rec.H_idx, idx_dim=rec.d_idx, q_heads=rec.Hq, Hkv=rec.Hkv,
                          qk_dim=rec.qk_dim, v_dim=rec.v_dim, kv_layout=rec.kv_layout,
                          budget=rec.B, ring_window=rec.W, page_rows=rec.p,
-                         opt_rows_max=rec.opt_rows_max if opt_rows_max is None else opt_rows_max)
+                         opt_rows_max=rec.opt_rows_max if opt_rows_max is None else opt_rows_max,
+                         tokens_per_row=rec.m)
 
 
 def build_oracle(rec, slots, k_max=None, opt_rows_max=None):
     o = oracle.Oracle(oracle_config(rec, k_max, opt_rows_max))
     for r in slots:
-        o.bind(r, rec.host_rows(r, r + 1)[0], rec.index_keys(r, r + 1)[0], rec.S)
+        o.bind(r, rec.host_rows(r, r + 1)[0], rec.index_keys(r, r + 1)[0], rec.S * rec.m)
     return o
 
 

@@ -627,3 +627,89 @@ def test_kept_rows_join_the_history_with_their_index_keys():
         assert list(sel1[r, 0, :a]) == [30 + u for u in range(a)]
     with pytest.raises(ValueError):
         o.append_keys(np.array([4, 0]), block)  # more rows than the block holds
+
+
+# ---------------------------------------------------------------- compressed sources, eq. (8)
+def test_rows_completed_by_a_round_eq8():
+    """[ADHS] eq. (8): with m positions per stored row, committing a of the
+    block's positions from token frontier n completes the rows
+    floor(n/m) <= s < floor((n+a)/m).  Worked by hand: 5 -> 12 with m = 4
+    completes rows 1 and 2 (positions 4..11); 8 -> 11 completes none (row 2
+    still lacks position 11); 7 -> 8 completes row 1; m = 1 completes exactly
+    the kept positions."""
+    from oracle.dhs_oracle import completed_rows, domain_length
+    assert list(completed_rows(5, 7, 4)) == [1, 2]
+    assert list(completed_rows(8, 3, 4)) == []
+    assert list(completed_rows(7, 1, 4)) == [1]
+    assert list(completed_rows(10, 0, 4)) == []
+    assert list(completed_rows(9, 4, 1)) == [9, 10, 11, 12]
+    # a query at position p sees the complete rows whose positions are all <= p
+    assert domain_length(10, 17, 4) == 4     # rows 0..3 hold positions 0..15; row 4 ends at 19
+    assert domain_length(10, 19, 4) == 5
+    assert domain_length(3, 40, 4) == 3      # capped by the complete history
+    assert domain_length(10, 2, 4) == 0
+
+
+def test_compressed_source_rounds():
+    """A source with m = 3: each round's commit publishes exactly the rows
+    eq. (8) completes, with the compressor's payload and keys; the partial
+    group stays out of every domain; the ring serves no history row (every
+    union row resolves through the hot cache or the host); with m = 1 the
+    compressed commit given the block rows leaves the host backing of the
+    ordinary commit."""
+    rng = np.random.default_rng(3)
+    for m in (3, 1):
+        c = _tiny_cfg(n_slots=2, k_max=4, topk=6, s_max=48, budget=6, tokens_per_row=m)
+        row = c.idx_heads * c.idx_dim
+        o = Oracle(c)
+        ref = Oracle(_tiny_cfg(n_slots=2, k_max=4, topk=6, s_max=48, budget=6)) if m == 1 else None
+        n_tok = [30, 31] if m == 3 else [10, 11]
+        for r in range(2):
+            keys = rng.integers(-8, 9, (c.s_max, row)).astype(np.int8)
+            host = _host(c, r)
+            o.bind(r, host.copy(), keys.copy(), n_tok[r])
+            if ref:
+                ref.bind(r, host.copy(), keys.copy(), n_tok[r])
+            assert o.req[r].n == n_tok[r] // m
+        for rnd in range(5):
+            qi = rng.integers(-8, 9, (2, c.k_max, row)).astype(np.int8)
+            kr = np.array([4, 3], np.int32)
+            sel = o.select(qi, kr)
+            for r in range(2):
+                assert sel[r].max() < o.req[r].n  # only complete rows are selectable
+            o.resolve(sel, shared=True)
+            assert o.stats.ring_hits == 0 or m == 1
+            qa = rng.standard_normal((2, c.k_max, c.q_heads, c.qk_dim)).astype(np.float32)
+            bl = rng.standard_normal((2, c.k_max, c.row_elems)).astype(np.float32)
+            o.attend(_bf16(qa), _bf16(bl))
+            acc = rng.integers(0, kr + 1).astype(np.int32)
+            cm = (c.k_max + m - 1) // m
+            rows = _bf16(rng.standard_normal((2, cm, c.row_elems)))
+            rkeys = rng.integers(-8, 9, (2, cm, row)).astype(np.int8)
+            before = [(q.tok, q.n, q.host.copy(), q.keys.copy()) for q in (o.req[0], o.req[1])]
+            if m == 1:
+                ref.select(qi, kr)
+                ref.resolve(sel, shared=True)
+                ref.attend(_bf16(qa), _bf16(bl))
+                ref.commit(acc)
+                rows = np.stack([np.stack([ref.req[r].host[before[r][0] + u] if u < acc[r]
+                                           else np.zeros(c.row_elems, np.uint16)
+                                           for u in range(cm)]) for r in range(2)])
+            o.commit_compressed(acc, rows, rkeys)
+            for r in range(2):
+                tok0, n0, host0, keys0 = before[r]
+                q = o.req[r]
+                done = list(range(tok0 // m, (tok0 + int(acc[r])) // m))
+                assert q.tok == tok0 + int(acc[r]) and q.n == q.tok // m
+                assert q.n == (done[-1] + 1 if done else n0)
+                for i, s in enumerate(done):
+                    assert np.array_equal(q.host[s], rows[r, i])
+                    assert np.array_equal(q.keys[s], rkeys[r, i])
+                keep = np.ones(c.s_max, bool)
+                keep[done] = False
+                assert np.array_equal(q.host[keep], host0[keep])
+                assert np.array_equal(q.keys[keep], keys0[keep])
+                if ref:
+                    assert np.array_equal(q.host, ref.req[r].host)
+    with pytest.raises(ValueError):
+        Oracle(_tiny_cfg(tokens_per_row=2)).commit(np.zeros(2, np.int32))

@@ -110,6 +110,7 @@ S_KEYS, S_HOST, S_QI_BASE, S_QI_FRESH, S_QI_SEL = 1, 2, 3, 4, 5
 S_QI_XSEL, S_QI_XFRESH, S_QA, S_BLOCK, S_ACCEPT, S_RESID = 6, 7, 8, 9, 10, 11
 S_QI_FSEL, S_QI_FFRESH = 12, 13
 S_BLOCK_KEYS = 14
+S_CROWS, S_CKEYS = 15, 16
 ROUND_STRIDE = 1000
 
 
@@ -155,6 +156,7 @@ class Recipe:
     s_slack: int = 64
     i8_lo: int = -8      # indexer keys and queries are uniform over i8_lo..i8_hi
     i8_hi: int = 8
+    m: int = 1           # token positions per stored row (eq. 8); S counts stored rows
     req0: int = 0        # request r of this recipe is request req0 + r of the workload
 
     @property
@@ -252,6 +254,26 @@ class Recipe:
         per = self.kmax * self.row_elems
         out = np.empty((r1 - r0, self.kmax, self.row_elems), np.uint16)
         return fill_bf16_normal(out, self.seed, S_BLOCK + ROUND_STRIDE * rnd, (self.req0 + r0) * per)
+
+    @property
+    def cmax(self) -> int:
+        """Stored rows one round can complete: ceil(K_max / m)."""
+        return (self.kmax + self.m - 1) // self.m
+
+    def compressed_rows(self, rnd: int, r0: int, r1: int) -> np.ndarray:
+        """bf16 bits [r1-r0][cmax][row_elems]: stored rows a compressor gives
+        the rows round ``rnd`` completes, N(0, 1)."""
+        per = self.cmax * self.row_elems
+        out = np.empty((r1 - r0, self.cmax, self.row_elems), np.uint16)
+        return fill_bf16_normal(out, self.seed, S_CROWS + ROUND_STRIDE * rnd, (self.req0 + r0) * per)
+
+    def compressed_keys(self, rnd: int, r0: int, r1: int) -> np.ndarray:
+        """int8 [r1-r0][cmax][H_idx*d_idx]: index keys of those rows."""
+        per = self.cmax * self.idx_row
+        out = np.empty((r1 - r0, self.cmax, self.idx_row), np.int8)
+        fill_i8(out, self.seed, S_CKEYS + ROUND_STRIDE * rnd, (self.req0 + r0) * per,
+                self.i8_lo, self.i8_hi)
+        return out
 
     def block_index_keys(self, rnd: int, r0: int, r1: int) -> np.ndarray:
         """int8 [r1-r0][K_max][H_idx*d_idx]: index keys the target computes for
