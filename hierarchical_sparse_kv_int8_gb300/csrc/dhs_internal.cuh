@@ -102,7 +102,9 @@ struct DevCtx {
   int32_t *ticket;      // [N][Kmax][Hkv]: finished splits of each attention item
   float *u_part;        // union attention, per (request, kv head) and cluster:
                         // O [C][M][dv], then (m, l) [C][M][2]
-  int32_t *u_ticket;    // [N][Hkv]: clusters of an item that have finished
+  int32_t *u_ticket;    // [N][Hkv]: clusters (or split CTAs) of an item that have finished
+  float *tc_part;       // tensor-core union pass, split-KV parts: per item and
+                        // split, O [M][dv] then (m, l) [M] (or nullptr: no split)
   unsigned long long *stats;  // counters, see StatIdx
   int32_t *err;               // [2]: code, site
 };
@@ -237,8 +239,13 @@ bool uattn_supported(const DevCtx &c);
 // The union pass on the fifth-generation tensor cores (128-dim heads, at most
 // 128 (query, head) pairs per kv head): one CTA per (request, kv head).
 bool uattn_tc_supported(const DevCtx &c);
+// split: CTAs per (request, kv head) item (split-KV), 0 = automatic (up to
+// the SM count, at most four).
 cudaError_t launch_uattn_tc(const DevCtx &c, const uint16_t *q, const uint16_t *block,
-                            uint16_t *out, float *lse, cudaStream_t s, class Timer *tm);
+                            uint16_t *out, float *lse, cudaStream_t s, class Timer *tm,
+                            int split = 0);
+// floats of the split-KV scratch of a context (tc_part)
+size_t uattn_tc_part_floats(const DevCtx &c);
 size_t uattn_partial_floats(const DevCtx &c);
 cudaError_t launch_attend(const DevCtx &c, const uint16_t *q, const uint16_t *block,
                           const int32_t *loc, uint16_t *out, float *lse, int n_split,

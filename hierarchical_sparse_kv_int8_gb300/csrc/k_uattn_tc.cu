@@ -29,6 +29,12 @@
 // between the roles with mbarriers (MMA completion arrives through
 // tcgen05.commit); every wait is bounded and, when it runs out, records a
 // device error and lets the CTA finish, so tensor memory is always freed.
+//
+// Launches with few (request, kv head) items split each item's walk into
+// nsplit contiguous ranges of tiles, one CTA each (split-KV): a CTA writes its
+// unnormalised O, running maximum and sum to a scratch area, and the last of
+// the item's CTAs to finish (a device-scope ticket) merges them with the
+// usual log-sum-exp weights and writes the output.
 #include "dhs_internal.cuh"
 #include "ptx_util.cuh"
 #include "tc_util.cuh"
@@ -73,6 +79,8 @@ constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kTcSmem = kOffTmem + 16;
 static_assert(kTcSmem <= (int)kMaxDynSmem, "shared memory of the tensor-core union pass");
 
+constexpr int kTcMaxSplit = 4;
+constexpr int kTcPartFloats = kTcM * kTcD + kTcM * 2;  // O [M][D], then (m, l) [M]
 constexpr uint32_t kIdescQK = tc_idesc_bf16(kTcM, kTcN, 0, 0);
 constexpr uint32_t kIdescPV = tc_idesc_bf16(kTcM, kTcD, 0, 1);
 
@@ -82,10 +90,10 @@ __device__ __forceinline__ int kmaj(int row, int chunk, int sbo) {
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restrict__ block,
-           uint16_t *__restrict__ out, float *__restrict__ lse) {
+           uint16_t *__restrict__ out, float *__restrict__ lse, int nsplit) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  __shared__ int abort_flag;
-  const int item = blockIdx.x;
+  __shared__ int abort_flag, sh_last;
+  const int item = blockIdx.x / nsplit, sp = blockIdx.x - item * nsplit;
   const int r = item / c.Hkv, kvh = item - r * c.Hkv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
@@ -124,6 +132,9 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
   const int U = c.counts[r * 4 + 0];
   const int L = U + Kr;  // union rows, then block rows
   const int T = (L + kTcN - 1) / kTcN;
+  // this CTA's tiles: [t0, t1), TL of them (barrier phases count from t0)
+  const int t0 = (int)((int64_t)T * sp / nsplit), t1 = (int)((int64_t)T * (sp + 1) / nsplit);
+  const int TL = t1 - t0;
   const int64_t n = c.n[r];
   const uint16_t *brow = block + (size_t)r * c.Kmax * c.row;
 
@@ -160,8 +171,9 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
   if (warp >= kTcLoadWarp0) {
     // ---------------------------------------------------------------- copies
     const int lw = warp - kTcLoadWarp0;
-    // the block rows go into their draft-ring slots (this kv head's parts)
-    for (int i = lw; i < Kr; i += 3) {
+    // the block rows go into their draft-ring slots (this kv head's parts;
+    // the item's first CTA writes them)
+    for (int i = lw; i < (sp == 0 ? Kr : 0); i += 3) {
       const int off = lane < 16 ? kvh * kTcD + lane * 8 : c.Hkv * kTcD + kvh * kTcD + (lane - 16) * 8;
       const uint4 v = *reinterpret_cast<const uint4 *>(brow + (size_t)i * c.row + off);
       *reinterpret_cast<uint4 *>(c.ring + ((size_t)r * c.Rd + (n + i) % c.Rd) * c.row + off) = v;
@@ -176,13 +188,13 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
     const int li = lw + 3 * lane;
     auto fetch = [&](int t) -> int4 {
       const int e = t * kTcN + li;
-      return (li < kTcN && e < U && t < T) ? uent[e] : make_int4(0, 0, 0, 0);
+      return (li < kTcN && e < U && t < t1) ? uent[e] : make_int4(0, 0, 0, 0);
     };
     // entries of tiles t, t + 1, t + 2 (loaded three tiles ahead of their use)
-    int4 e0 = fetch(0), e1 = fetch(1), e2 = fetch(2);
+    int4 e0 = fetch(t0), e1 = fetch(t0 + 1), e2 = fetch(t0 + 2);
     const int off = lane < 16 ? kvh * kTcD + lane * 8 : c.Hkv * kTcD + kvh * kTcD + (lane - 16) * 8;
-    for (int t = 0; t < T; ++t) {
-      const int s = t % kTcStages;
+    for (int tl = 0; tl < TL; ++tl) {
+      const int t = t0 + tl, s = tl % kTcStages;
       const int4 ent = e0;
       e0 = e1;
       e1 = e2;
@@ -200,7 +212,7 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
           tmask = all_q & ~((1u << (e - U)) - 1u);
         }
       }
-      if (t >= kTcStages) wait(&empty[s], (uint32_t)(((t / kTcStages) - 1) & 1));
+      if (tl >= kTcStages) wait(&empty[s], (uint32_t)(((tl / kTcStages) - 1) & 1));
       unsigned char *kst = smem + kOffStage + s * kStageBytes, *vst = kst + kKBytes;
       uint32_t *msk = reinterpret_cast<uint32_t *>(smem + kOffMask) + s * kTcN;
       for (int it = 0; it * 3 + lw < kTcN; ++it) {
@@ -233,11 +245,11 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
         tc_commit(&pv_done[b]);
         tc_commit(&empty[s]);
       };
-      for (int t = 0; t < T; ++t) {
-        const int s = t % kTcStages, b = t & 1;
-        wait(&full[s], (uint32_t)((t / kTcStages) & 1));
+      for (int tl = 0; tl < TL; ++tl) {
+        const int s = tl % kTcStages, b = tl & 1;
+        wait(&full[s], (uint32_t)((tl / kTcStages) & 1));
         fence_proxy_async_smem();  // the stage's copies, seen by the tensor cores
-        if (t >= 2) wait(&s_free[b], (uint32_t)(((t - 2) >> 1) & 1));
+        if (tl >= 2) wait(&s_free[b], (uint32_t)(((tl - 2) >> 1) & 1));
         tc_fence_after();
         const uint32_t sK = smem_u32(smem + kOffStage + s * kStageBytes);
 #pragma unroll
@@ -245,9 +257,9 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
           tc_mma(tmem + (uint32_t)(b * kTcN), tc_desc(sQ + kk * 256, 128, 2048),
                  tc_desc(sK + kk * 256, 128, 2048), kIdescQK, kk > 0 ? 1 : 0);
         tc_commit(&s_full[b]);
-        if (t >= 1) pv(t - 1);
+        if (tl >= 1) pv(tl - 1);
       }
-      pv(T - 1);
+      if (TL > 0) pv(TL - 1);
       tc_commit(o_done);
       wait(o_done, 0u, true);  // every MMA has completed before tensor memory is freed
     }
@@ -263,10 +275,10 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
     float *red = reinterpret_cast<float *>(smem + kOffRed);  // [tile parity][group][lane]
     float *lsum = red + 2 * 2 * kTcM;                        // [group][lane]
     float m_run = -CUDART_INF_F, l = 0.f;
-    for (int t = 0; t < T; ++t) {
-      const int b = t & 1, s = t % kTcStages;
-      wait(&s_full[b], (uint32_t)((t >> 1) & 1));
-      wait(&full[s], (uint32_t)((t / kTcStages) & 1));  // the tile's masks
+    for (int tl = 0; tl < TL; ++tl) {
+      const int b = tl & 1, s = tl % kTcStages;
+      wait(&s_full[b], (uint32_t)((tl >> 1) & 1));
+      wait(&full[s], (uint32_t)((tl / kTcStages) & 1));  // the tile's masks
       tc_fence_after();
       uint32_t sv[kTcHalf];
       tmem_ld32(tmem + lrow + (uint32_t)(b * kTcN + hg * kTcHalf), sv);
@@ -298,10 +310,10 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
       mx = fmaxf(mx, red[(b * 2 + (hg ^ 1)) * kTcM + m]);
       const float m_new = fmaxf(m_run, mx);
       const bool need = m_new > m_run + kTcRescale;  // false while nothing is kept
-      if (__any_sync(0xffffffffu, need) && t >= 1) {
+      if (__any_sync(0xffffffffu, need) && tl >= 1) {
         // rescale this lane's half of the output after the previous tile's
         // P V completed
-        wait(&pv_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1));
+        wait(&pv_done[(tl - 1) & 1], (uint32_t)(((tl - 1) >> 1) & 1));
         tc_fence_after();
         const float f = need ? ex2_approx(m_run - m_new) : 1.f;
 #pragma unroll
@@ -321,7 +333,7 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
         m_run = m_new;
       }
       // P_t replaces P_{t-2}: its P V must have completed
-      if (t >= 2) wait(&pv_done[b], (uint32_t)(((t - 2) >> 1) & 1));
+      if (tl >= 2) wait(&pv_done[b], (uint32_t)(((tl - 2) >> 1) & 1));
       unsigned char *prow = smem + kOffP + b * kPBytes + (m >> 3) * 1024 + (m & 7) * 16;
       const bool live = m_run != -CUDART_INF_F;
 #pragma unroll
@@ -351,6 +363,80 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
     tc_fence_after();
     const int h = kvh * G + (m - j * G);
     uint16_t *orow = valid ? out + (((size_t)r * c.Kmax + j) * c.Hq + h) * kTcD : nullptr;
+    if (nsplit > 1) {
+      // this CTA's part: O (zero for an empty range), then (m, l) per lane
+      float *po = c.tc_part + ((size_t)item * nsplit + sp) * kTcPartFloats;
+#pragma unroll
+      for (int cc = 0; cc < kTcD / 2; cc += 32) {
+        const int col = hg * (kTcD / 2) + cc;
+        uint32_t ov[32];
+        if (TL > 0) {
+          tmem_ld32(tmem + lrow + kTcColO + (uint32_t)col, ov);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4 *>(po + (size_t)m * kTcD + col + i) =
+              make_float4(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1]),
+                          __uint_as_float(ov[i + 2]), __uint_as_float(ov[i + 3]));
+      }
+      if (hg == 0) *reinterpret_cast<float2 *>(po + kTcM * kTcD + 2 * m) = make_float2(m_run, l);
+      __threadfence();
+      named_sync(1, kTcSoftmax);
+      if (tid == 0) sh_last = atomicAdd(&c.u_ticket[item], 1) == nsplit - 1;
+      named_sync(1, kTcSoftmax);
+      if (sh_last) {
+        // the item's last CTA: out = sum_s w_s O_s / sum_s w_s l_s with
+        // w_s = 2^(m_s - max_s m_s), for this lane's half of the columns
+        __threadfence();
+        const float *pi = c.tc_part + (size_t)item * nsplit * kTcPartFloats;
+        float mm = -CUDART_INF_F;
+        for (int s2 = 0; s2 < nsplit; ++s2)
+          mm = fmaxf(mm, pi[(size_t)s2 * kTcPartFloats + kTcM * kTcD + 2 * m]);
+        float den = 0.f;
+        float wsp[kTcMaxSplit];
+#pragma unroll
+        for (int s2 = 0; s2 < kTcMaxSplit; ++s2) {
+          wsp[s2] = 0.f;
+          if (s2 < nsplit) {
+            const float2 ml = *reinterpret_cast<const float2 *>(
+                pi + (size_t)s2 * kTcPartFloats + kTcM * kTcD + 2 * m);
+            wsp[s2] = ml.x == -CUDART_INF_F ? 0.f : ex2_approx(ml.x - mm);
+            den += wsp[s2] * ml.y;
+          }
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        if (valid) {
+          for (int col = hg * (kTcD / 2); col < (hg + 1) * (kTcD / 2); col += 8) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s2 = 0; s2 < kTcMaxSplit; ++s2) {
+              if (s2 >= nsplit || wsp[s2] == 0.f) continue;
+              const float *o = pi + (size_t)s2 * kTcPartFloats + (size_t)m * kTcD + col;
+              const float4 a0 = *reinterpret_cast<const float4 *>(o);
+              const float4 a1 = *reinterpret_cast<const float4 *>(o + 4);
+              acc[0] += wsp[s2] * a0.x; acc[1] += wsp[s2] * a0.y;
+              acc[2] += wsp[s2] * a0.z; acc[3] += wsp[s2] * a0.w;
+              acc[4] += wsp[s2] * a1.x; acc[5] += wsp[s2] * a1.y;
+              acc[6] += wsp[s2] * a1.z; acc[7] += wsp[s2] * a1.w;
+            }
+            uint4 w;
+            w.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+            w.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+            w.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+            w.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+            *reinterpret_cast<uint4 *>(orow + col) = w;
+          }
+          if (lse && hg == 0)
+            lse[((size_t)r * c.Kmax + j) * c.Hq + h] =
+                den > 0.f ? (mm + log2f(den)) * 0.69314718055994531f : -CUDART_INF_F;
+        }
+        if (tid == 0) c.u_ticket[item] = 0;  // ready for the next launch
+      }
+    } else {
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int cc = 0; cc < kTcD / 2; cc += 32) {
@@ -373,6 +459,7 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
     if (valid && lse && hg == 0)
       lse[((size_t)r * c.Kmax + j) * c.Hq + h] =
           l > 0.f ? (m_run + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -387,14 +474,24 @@ bool uattn_tc_supported(const DevCtx &c) {
          c.Kmax * (c.Hq / c.Hkv) <= kTcM;
 }
 
+size_t uattn_tc_part_floats(const DevCtx &c) {
+  return (size_t)c.N * c.Hkv * kTcMaxSplit * kTcPartFloats;
+}
+
 cudaError_t launch_uattn_tc(const DevCtx &c, const uint16_t *q, const uint16_t *block,
-                            uint16_t *out, float *lse, cudaStream_t s, Timer *tm) {
+                            uint16_t *out, float *lse, cudaStream_t s, Timer *tm, int split) {
   static size_t granted = 0;
   cudaError_t e = ensure_smem(k_uattn_tc, (size_t)kTcSmem, granted);
   if (e != cudaSuccess) return e;
+  // one CTA per SM (its shared memory): split the items' walks while the
+  // launch leaves SMs idle
+  const int items = c.N * c.Hkv;
+  int nsplit = split > 0 ? split : c.sms / std::max(1, items);
+  nsplit = std::max(1, std::min(kTcMaxSplit, nsplit));
+  if (!c.tc_part) nsplit = 1;
   if (tm) tm->begin(K_ATTN_UNION, s);
-  e = launch_pdl(k_uattn_tc, dim3(c.N * c.Hkv), dim3(kTcThreads), (size_t)kTcSmem, s, c, q,
-                 block, out, lse);
+  e = launch_pdl(k_uattn_tc, dim3(items * nsplit), dim3(kTcThreads), (size_t)kTcSmem, s, c, q,
+                 block, out, lse, nsplit);
   if (tm) tm->end(K_ATTN_UNION, s);
   return e;
 }
