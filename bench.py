@@ -348,6 +348,9 @@ def ncu_traffic(name, path=None, full_requests=None):
     for sec in text.split("\n## ")[1:]:
         if not sec.startswith(NCU_NAMES[name]):
             continue
+        ms = re.search(r"captured requests: (\d+)", sec)  # a section captured on its own cut
+        if ms and full_requests:
+            scale_req = full_requests / float(ms.group(1))
         rd = re.search(r"DRAM read: ([0-9.]+) (\w+)", sec)
         wr = re.search(r"DRAM write: ([0-9.]+) (\w+)", sec)
         if rd and wr and rd.group(2) in scale and wr.group(2) in scale:
