@@ -581,9 +581,12 @@ def run_native(args):
     # every kernel of the round is timed (the control words travel as kernel
     # parameters, so no upload launch is needed)
     launches_per_step = sum(n for n, _ in per.values()) / args.steps
-    if args.round_groups > 1:
+    # dhs_round forms request groups for the tensor-core union pass only
+    groups = (args.round_groups if args.round_groups > 1 and "attn_union" in per
+              and args.attn_pass != 3 else 1)
+    if groups > 1:
         # the timed graph issues every kernel once per request group
-        launches_per_step *= args.round_groups
+        launches_per_step *= groups
     line = {
         "metric": "verified query-tokens/s per layer (select+resolve+attend)",
         "value": round(value, 1), "unit": "query-tokens/s", "n_gpus": world,
@@ -595,7 +598,7 @@ def run_native(args):
                        state="restored from snapshot before every step (untimed)",
                        attention_pass="union" if "attn_union" in per else "per_query",
                        round=("one dhs_round call, requests in %d groups on internal streams"
-                              % max(1, args.round_groups) if args.round_groups
+                              % groups if args.round_groups
                               else "dhs_select, dhs_resolve, dhs_attend, dhs_commit")),
         "e2e": {"value": round(e2e_value, 1), "unit": "query-tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -607,7 +610,7 @@ def run_native(args):
                    "per request group, the %d groups overlapping on internal streams), replayed "
                    "per step; kernel times (roofline, families, kernels) from a second replay of "
                    "the same steps issued as one request group (each kernel over the whole batch, "
-                   "none overlapping) with an event pair around every kernel" % max(1, args.round_groups))
+                   "none overlapping) with an event pair around every kernel" % groups)
                   if args.round_groups else
                   "CUDA graph of one round (select, resolve, attend, commit), replayed per step; "
                   "kernel times from a second replay of the same steps with per-kernel events",

@@ -795,11 +795,14 @@ int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const v
   }
   if (c->tick + 1 > 0x7FFFFFF0) return DHS_ERR_CAPACITY;
   const bool tc = c->cfg.attn_pass != DHS_ATTN_UNION_MMA && uattn_tc_supported(d);
-  // (the mma.sync union pass sizes its partials for the whole context; with
-  // per-kernel timing on, the round is issued as one group on the caller's
-  // stream, so each kernel's events bracket that kernel alone over the whole
-  // batch)
-  const int G = ((c->fused && !tc) || c->timer.enabled) ? 1 : c->groups;
+  // Request groups for the tensor-core union pass only: the mma.sync union
+  // pass sizes its partials for the whole context, and the per-query pass
+  // measured slower in groups (64 histories of 524 288 latent rows: 3.97 ms
+  // in one group, 6.1-6.3 ms in two or four; 8 of 32 768 rows: 0.085 against
+  // 0.091-0.122 ms).  With per-kernel timing on, the round is issued as one
+  // group on the caller's stream, so each kernel's events bracket that kernel
+  // alone over the whole batch.
+  const int G = (!c->fused || !tc || c->timer.enabled) ? 1 : c->groups;
   const bool fork = G > 1;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int tick = (int)(c->tick + 1);
@@ -858,7 +861,7 @@ int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const v
                          &c->timer);
     if (e == cudaSuccess)
       e = launch_gather(v, topk_out + (size_t)a * KK, loc_out + (size_t)a * KK, 1, tick, sg,
-                        &c->timer);
+                        &c->timer, !c->fused);
     const size_t qoff = (size_t)a * d.Kmax * d.Hq;
     if (e == cudaSuccess)
       e = !c->fused ? launch_attend(v, q16 + qoff * d.dqk, b16 + (size_t)a * d.Kmax * d.row,
@@ -940,7 +943,9 @@ int dhs_resolve(dhs_ctx *c, const int32_t *topk, int32_t *loc_out, int32_t share
     return cuda_fail(c, cudaGetLastError());
   c->tick += 1;
   {
-    cudaError_t e_ = launch_resolve(c->d, topk, loc_out, shared, 1, (int)c->tick, s, &c->timer);
+    // (2: the per-query attention pass follows, which the gather releases early)
+    cudaError_t e_ = launch_resolve(c->d, topk, loc_out, shared, (c->fused && shared) ? 1 : 2,
+                                    (int)c->tick, s, &c->timer);
     if (e_ != cudaSuccess) return cuda_fail(c, e_);
   }
   if (ar) {

@@ -227,10 +227,11 @@ cudaError_t launch_select(const DevCtx &c, const int8_t *q_idx, const int8_t *q_
                           int active_queries, int topk_pass, cudaStream_t s, class Timer *tm);
 cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_out,
                            int shared, int gather, int tick, cudaStream_t s, class Timer *tm);
-// The shared host gather alone (launch_resolve with gather = 1 issues the
-// union/probe and then this).
+// The shared host gather alone (launch_resolve with gather = 1 or 2 issues
+// the union/probe and then this; 2 when the per-query attention pass follows,
+// which the gather then releases early: `early`).
 cudaError_t launch_gather(const DevCtx &c, const int32_t *topk, int32_t *loc_out, int shared,
-                          int tick, cudaStream_t s, class Timer *tm);
+                          int tick, cudaStream_t s, class Timer *tm, bool early);
 // int32 words of union/probe scratch per request slot (0: none needed).
 size_t union_spill_ints_per_request(const DevCtx &c);
 cudaError_t launch_uattn(const DevCtx &c, const uint16_t *q, const uint16_t *block,

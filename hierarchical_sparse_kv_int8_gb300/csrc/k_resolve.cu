@@ -540,14 +540,17 @@ __device__ void hot_update(const DevCtx &c, int r, int tick, int *warp_sums) {
 template <int VEC>
 __global__ void __launch_bounds__(kGatherWarps * 32)
 k_gather(const DevCtx c, const int32_t *__restrict__ topk, const int32_t *__restrict__ loc,
-         int shared, int tick) {
+         int shared, int tick, int early) {
   constexpr int kGatherVec = GatherShape<VEC>::kGatherVec;
   constexpr int kGatherBatch = GatherShape<VEC>::kGatherBatch;
   __shared__ int warp_sums[32];
-  // (no early trigger: the attention that follows waits for every gathered
-  // row, so launched early its CTAs would only hold SMs, and their shared
-  // memory, that another request group's kernels can use meanwhile)
+  // The per-query attention pass attends the rows already on the GPU
+  // before it waits for this gather, so it is released early (`early`); the
+  // union passes wait for every gathered row first, and launched early their
+  // CTAs would only hold SMs, and their shared memory, that another request
+  // group's kernels can use meanwhile.
   pdl_wait();
+  if (early) pdl_trigger();
   const int r = blockIdx.y;
   const int Kr = c.Kr[r];
   if (Kr == 0) return;
@@ -635,15 +638,15 @@ cudaError_t launch_resolve(const DevCtx &c, const int32_t *topk, int32_t *loc_ou
                  union_smem_bytes(c), s, c, topk, loc_out, shared, tick);
   if (tm) tm->end(K_UNION_PROBE, s);
   if (e != cudaSuccess || !gather) return e;
-  return launch_gather(c, topk, loc_out, shared, tick, s, tm);
+  return launch_gather(c, topk, loc_out, shared, tick, s, tm, gather == 2);
 }
 
 cudaError_t launch_gather(const DevCtx &c, const int32_t *topk, int32_t *loc_out, int shared,
-                          int tick, cudaStream_t s, Timer *tm) {
+                          int tick, cudaStream_t s, Timer *tm, bool early) {
   cudaError_t e = cudaSuccess;
   const int vec = (c.row * 2 + 511) / 512;
   if (vec > kGatherMaxVec) return cudaErrorInvalidValue;
-  void (*kern)(const DevCtx, const int32_t *, const int32_t *, int, int) =
+  void (*kern)(const DevCtx, const int32_t *, const int32_t *, int, int, int) =
       vec == 1 ? k_gather<1> : vec == 2 ? k_gather<2> : vec == 3 ? k_gather<3> : k_gather<4>;
   static bool carved[kGatherMaxVec + 1] = {};
   if (!carved[vec]) {
@@ -662,7 +665,8 @@ cudaError_t launch_gather(const DevCtx &c, const int32_t *topk, int32_t *loc_out
   // An ordinary launch: its CTAs are placed once the union/probe has left the
   // SMs, one per SM; placed early they would crowd onto the SMs the
   // union/probe leaves free and keep attention CTAs off them.
-  e = launch_prio(kern, grid, dim3(kGatherWarps * 32), 0, s, c, topk, loc_out, shared, tick);
+  e = launch_prio(kern, grid, dim3(kGatherWarps * 32), 0, s, c, topk, loc_out, shared, tick,
+                  early ? 1 : 0);
   if (tm) tm->end(K_GATHER, s);
   return e;
 }

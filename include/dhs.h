@@ -244,12 +244,13 @@ int dhs_resolve(dhs_ctx *ctx, const int32_t *topk, int32_t *loc_out, int32_t sha
  *   loc       device int32 [n_slots][k_max][topk] from dhs_resolve
  *   out       device bf16 [n_slots][k_max][q_heads][v_dim]
  *   lse       device fp32 [n_slots][k_max][q_heads] natural-log sum-exp, or NULL
- * Follows the dhs_resolve of the same round on the stream.  The kernel
- * attends the rows held on the GPU (hot cache, optional pool, draft ring) and
- * the block rows while the resolve's host gather is still running, and the
- * staging rows after it; q, block_kv and loc must therefore be complete when
- * the call's first kernel starts (in stream order, with no caller kernel in
- * between that releases its dependents before writing them). */
+ * Follows the dhs_resolve of the same round on the stream.  The per-query
+ * pass attends the rows held on the GPU (hot cache, optional pool, draft
+ * ring) and the block rows while the resolve's host gather is still running,
+ * and the staging rows after it; the union passes start once the gather has
+ * finished.  q, block_kv and loc must therefore be complete when the call's
+ * first kernel starts (in stream order, with no caller kernel in between that
+ * releases its dependents before writing them). */
 int dhs_attend(dhs_ctx *ctx, const void *q, const void *block_kv, const int32_t *loc,
                void *out, float *lse, dhs_stream stream);
 
@@ -393,8 +394,9 @@ int dhs_snapshot_free(dhs_ctx *ctx, int32_t snapshot_id);
  * Results equal those of the separate
  * calls; the LRU clock advances once per call.  Forking and joining use CUDA
  * events, which stream capture turns into graph dependencies.  Not for
- * contexts on shared arenas or followers (DHS_ERR_INVALID); with the union
- * pass on mma.sync tiles the groups run one after the other on `stream`. */
+ * contexts on shared arenas or followers (DHS_ERR_INVALID).  Groups apply to
+ * contexts whose attention is the tensor-core union pass; others (per-query
+ * pass, union pass on mma.sync tiles) run the round as one group on `stream`. */
 int dhs_round(dhs_ctx *ctx, const int8_t *q_idx, const int32_t *k_per_req, const void *q,
               const void *block_kv, const int32_t *accepted_len, int32_t *topk_out,
               int32_t *loc_out, void *out, float *lse, dhs_stream stream);

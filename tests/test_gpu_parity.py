@@ -541,7 +541,8 @@ def test_topk_row_kernel_lists(S, fill, rescans):
 def test_round_in_request_groups(rec, groups, attn_pass):
     """dhs_round issues select, resolve, attend and commit in one call, the
     request slots split into groups on internal streams (uneven groups when
-    the slots do not divide): every round equals the oracle's, state included."""
+    the slots do not divide) for the tensor-core union pass, as one group for
+    the other passes: every round equals the oracle's, state included."""
     from hierarchical_sparse_kv_int8_gb300.runner import Runner
     run = Runner(rec, attn_pass=attn_pass, round_groups=groups)
     slots = list(range(rec.N))
