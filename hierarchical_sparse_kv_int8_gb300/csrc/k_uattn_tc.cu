@@ -21,9 +21,9 @@
 // threads in two warpgroups (warps w and w + 4 own lanes 32(w mod 4) ..
 // +31, the first group the first half of a tile's columns and of the output,
 // the second the second half; they agree on each row's running maximum
-// through shared memory), one thread of warp 8 issues every MMA, warps 9-11
-// copy rows into a ring of kTcStages stages with 16-byte
-// cp.async from wherever the union/probe located them (hot cache, optional
+// through shared memory), one thread of warp 8 issues every MMA, the
+// kTcCopyWarps warps after it copy rows into a ring of kTcStages stages with
+// 16-byte cp.async from wherever the union/probe located them (hot cache, optional
 // pool, draft ring, staging) or from the caller's block rows, which they also
 // write to the draft ring.  The stages, S buffers and P buffers are handed
 // between the roles with mbarriers (MMA completion arrives through
@@ -48,11 +48,12 @@ constexpr int kTcM = 128;              // (query, head) pairs: tensor-memory lan
 constexpr int kTcD = 128;              // key and value dims
 constexpr int kTcN = 64;               // walk rows per tile
 constexpr int kTcStages = 4;
-constexpr int kTcThreads = 384;
+constexpr int kTcCopyWarps = 6;        // warps that copy rows (each issues ~64/6 rows a tile)
+constexpr int kTcThreads = (9 + kTcCopyWarps) * 32;
 constexpr int kTcSoftmax = 256;        // warps 0-7: two warpgroups, one per half tile
 constexpr int kTcMmaWarp = 8;
-constexpr int kTcLoadWarp0 = 9;        // warps 9-11 copy
-constexpr int kTcLoaders = 96;
+constexpr int kTcLoadWarp0 = 9;        // warps 9 .. 8 + kTcCopyWarps copy
+constexpr int kTcLoaders = kTcCopyWarps * 32;
 constexpr int kTcHalf = kTcN / 2;      // columns of a tile per softmax warpgroup
 constexpr uint32_t kTcCols = 256;      // S: two buffers of kTcN columns; O: 128 columns
 constexpr uint32_t kTcColO = 128;
@@ -173,19 +174,19 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
     const int lw = warp - kTcLoadWarp0;
     // the block rows go into their draft-ring slots (this kv head's parts;
     // the item's first CTA writes them)
-    for (int i = lw; i < (sp == 0 ? Kr : 0); i += 3) {
+    for (int i = lw; i < (sp == 0 ? Kr : 0); i += kTcCopyWarps) {
       const int off = lane < 16 ? kvh * kTcD + lane * 8 : c.Hkv * kTcD + kvh * kTcD + (lane - 16) * 8;
       const uint4 v = *reinterpret_cast<const uint4 *>(brow + (size_t)i * c.row + off);
       *reinterpret_cast<uint4 *>(c.ring + ((size_t)r * c.Rd + (n + i) % c.Rd) * c.row + off) = v;
     }
     const int4 *uent = c.uent + (size_t)r * KK;
     const uint32_t all_q = (1u << Kr) - 1u;
-    // lane l of copy warp lw holds the union entry of row lw + 3 l of a
+    // lane l of copy warp lw holds the union entry of row lw + kTcCopyWarps l of a
     // tile: loaded three tiles ahead, turned into a source address when its
     // tile is issued.  A stage is complete when every copy thread's copies
     // have landed (asynchronous arrivals) and every row's query mask is
     // written (an ordinary arrival by the lane that wrote it).
-    const int li = lw + 3 * lane;
+    const int li = lw + kTcCopyWarps * lane;
     auto fetch = [&](int t) -> int4 {
       const int e = t * kTcN + li;
       return (li < kTcN && e < U && t < t1) ? uent[e] : make_int4(0, 0, 0, 0);
@@ -215,8 +216,8 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
       if (tl >= kTcStages) wait(&empty[s], (uint32_t)(((tl / kTcStages) - 1) & 1));
       unsigned char *kst = smem + kOffStage + s * kStageBytes, *vst = kst + kKBytes;
       uint32_t *msk = reinterpret_cast<uint32_t *>(smem + kOffMask) + s * kTcN;
-      for (int it = 0; it * 3 + lw < kTcN; ++it) {
-        const int i = lw + 3 * it;
+      for (int it = 0; it * kTcCopyWarps + lw < kTcN; ++it) {
+        const int i = lw + kTcCopyWarps * it;
         const uint16_t *src = reinterpret_cast<const uint16_t *>(
             __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(tsrc), it));
         unsigned char *dst = lane < 16 ? kst + kmaj(i, lane, 2048) : vst + kmaj(i, lane - 16, 2048);
