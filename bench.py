@@ -69,7 +69,7 @@ def parse():
                          "(resolves with their host gathers on a copy stream while the previous "
                          "layer attends on a compute stream); prints one JSON line")
     ap.add_argument("--chi", type=int, default=2, help="staging arenas of the layer group")
-    ap.add_argument("--round-groups", type=int, default=4,
+    ap.add_argument("--round-groups", type=int, default=3,
                     help="issue each round as one dhs_round call with the requests split into "
                          "this many groups on internal streams (0: the four separate calls)")
     ap.add_argument("--groups", type=int, default=0,
@@ -439,12 +439,14 @@ def run_native(args):
         eager_ms = float(np.mean([a.elapsed_time(b) for a, b in ev0]))
 
         # The timed step is the same round captured once as a CUDA graph (the
-        # state is restored before every launch, so the round is identical).
+        # state is restored before every launch, so the round is identical),
+        # through the library's capture, which keeps the launches' priorities
+        # that order the request groups (a plain graph ignores them).
         def capture(timing):
             run.ctx.set_timing(timing)
             run.ctx.restore(snap, stream)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            stream.synchronize()
+            with dhs.Graph.capture(stream) as g:
                 step()
             stream.synchronize()
             return g
@@ -607,8 +609,9 @@ def run_native(args):
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "eager_ms_per_step": round(eager_ms, 5),
         "launch": ("CUDA graph of one round (one dhs_round call: select, resolve, attend, commit "
-                   "per request group, the %d groups overlapping on internal streams), replayed "
-                   "per step; kernel times (roofline, families, kernels) from a second replay of "
+                   "per request group, the %d groups overlapping on internal streams of "
+                   "decreasing priority; captured with dhs_graph_*, which instantiates it with "
+                   "the launches' priorities honoured), replayed per step; kernel times (roofline, families, kernels) from a second replay of "
                    "the same steps issued as one request group (each kernel over the whole batch, "
                    "none overlapping) with an event pair around every kernel" % groups)
                   if args.round_groups else

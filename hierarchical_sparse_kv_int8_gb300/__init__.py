@@ -96,6 +96,10 @@ _SIGS = {
     "dhs_export": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                     ctypes.c_void_p], ctypes.c_int),
     "dhs_set_timing": ([ctypes.c_void_p, ctypes.c_int32], ctypes.c_int),
+    "dhs_graph_begin": ([ctypes.c_void_p], ctypes.c_int),
+    "dhs_graph_end": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
+    "dhs_graph_launch": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "dhs_graph_destroy": ([ctypes.c_void_p], None),
     "dhs_kernel_times": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p],
                          ctypes.c_int),
     "dhs_kernel_name": ([ctypes.c_int32], ctypes.c_char_p),
@@ -211,6 +215,54 @@ def make_config(**kw) -> Config:
     for name, _ in Config._fields_:
         setattr(c, name, kw.get(name, 0))
     return c
+
+
+class Graph:
+    """A CUDA graph of library calls captured on one stream, instantiated with
+    the launches' priorities honoured (dhs_graph_*).  Use as
+    ``with Graph.capture(stream) as g: ...calls on stream...`` then
+    ``g.replay()``."""
+
+    def __init__(self):
+        self._lib = load()
+        self.h = None
+        self._stream = None
+
+    @classmethod
+    def capture(cls, stream):
+        g = cls()
+        g._stream = stream
+        return g
+
+    def __enter__(self):
+        rc = self._lib.dhs_graph_begin(_stream(self._stream))
+        if rc:
+            raise DhsError(rc, "dhs_graph_begin")
+        return self
+
+    def __exit__(self, exc_type, exc, tb):
+        h = ctypes.c_void_p()
+        rc = self._lib.dhs_graph_end(_stream(self._stream), ctypes.byref(h))
+        if rc and exc_type is None:
+            raise DhsError(rc, "dhs_graph_end")
+        self.h = h.value
+        return False
+
+    def replay(self, stream=None):
+        rc = self._lib.dhs_graph_launch(self.h, _stream(stream if stream is not None else self._stream))
+        if rc:
+            raise DhsError(rc, "dhs_graph_launch")
+
+    def close(self):
+        if self.h:
+            self._lib.dhs_graph_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class Policy:

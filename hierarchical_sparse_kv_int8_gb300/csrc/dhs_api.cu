@@ -1231,6 +1231,49 @@ int dhs_snapshot(dhs_ctx *c, int32_t *snapshot_id, dhs_stream stream) {
   return DHS_OK;
 }
 
+struct dhs_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+int dhs_graph_begin(dhs_stream stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed) == cudaSuccess ? DHS_OK
+                                                                                : DHS_ERR_CUDA;
+}
+
+int dhs_graph_end(dhs_stream stream, dhs_graph **out) {
+  if (!out) return DHS_ERR_INVALID;
+  *out = nullptr;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  dhs_graph *g = new (std::nothrow) dhs_graph();
+  if (!g) return DHS_ERR_OOM;
+  if (cudaStreamEndCapture(s, &g->graph) != cudaSuccess || !g->graph ||
+      cudaGraphInstantiateWithFlags(&g->exec, g->graph, cudaGraphInstantiateFlagUseNodePriority) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    if (g->graph) cudaGraphDestroy(g->graph);
+    delete g;
+    return DHS_ERR_CUDA;
+  }
+  *out = g;
+  return DHS_OK;
+}
+
+int dhs_graph_launch(dhs_graph *g, dhs_stream stream) {
+  if (!g || !g->exec) return DHS_ERR_INVALID;
+  return cudaGraphLaunch(g->exec, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DHS_OK
+             : DHS_ERR_CUDA;
+}
+
+void dhs_graph_destroy(dhs_graph *g) {
+  if (!g) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+}
+
 int dhs_snapshot_free(dhs_ctx *c, int32_t id) {
   if (!c || id < 0 || id >= (int32_t)c->snaps.size() || c->snaps[id].bufs.empty())
     return DHS_ERR_INVALID;

@@ -376,6 +376,21 @@ int dhs_restore(dhs_ctx *ctx, int32_t snapshot_id, dhs_stream stream);
  * not reused and restoring it afterwards is DHS_ERR_INVALID. */
 int dhs_snapshot_free(dhs_ctx *ctx, int32_t snapshot_id);
 
+/* Graph capture that keeps launch priorities (no counterpart in the paper).
+ * dhs_round's request groups rely on the priorities of its internal streams,
+ * which every kernel launch carries as an attribute; a CUDA graph ignores such
+ * per-node priorities unless it is instantiated to use them.  dhs_graph_begin
+ * starts capturing `stream` (relaxed mode); the caller then issues library
+ * calls on it; dhs_graph_end stops the capture and instantiates the graph
+ * with node priorities honoured.  dhs_graph_launch replays it on a stream;
+ * dhs_graph_destroy frees it (NULL is a no-op).  DHS_ERR_CUDA if a CUDA call
+ * fails (the capture is then ended and discarded). */
+typedef struct dhs_graph dhs_graph;
+int dhs_graph_begin(dhs_stream stream);
+int dhs_graph_end(dhs_stream stream, dhs_graph **out);
+int dhs_graph_launch(dhs_graph *graph, dhs_stream stream);
+void dhs_graph_destroy(dhs_graph *graph);
+
 /* One whole round on device buffers: select (causal domains at n_r + j),
  * resolve (shared retrieval), attend and commit, with the shapes of the
  * separate calls (topk_out and loc_out receive the selections and locations).

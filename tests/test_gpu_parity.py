@@ -648,3 +648,42 @@ def test_kept_rows_take_their_index_keys(fused):
         for r in slots:
             assert np.array_equal(keys[r], o.req[r].keys), "key rows r=%d round %d" % (r, rnd)
     assert run.ctx.stats()["device_error"] == 0
+
+
+# ---------------------------------------------------------------- graphs that keep launch priorities
+def test_round_replayed_from_a_priority_graph():
+    """dhs_graph_* capture a dhs_round (three request groups on prioritised
+    streams) into a graph instantiated with the launches' priorities; replays
+    from the same snapshot give the eager call's outputs and cache state."""
+    import torch
+    import hierarchical_sparse_kv_int8_gb300 as dhs
+    from hierarchical_sparse_kv_int8_gb300.runner import Runner
+    rec = TINY_GQA
+    stream = torch.cuda.Stream()
+    run = Runner(rec, attn_pass=UNION, round_groups=3, stream=stream)
+    kr = rec.k_per_req()
+    acc = rec.accepted(0, kr)
+    run.load_round(0)
+    sid = run.ctx.snapshot(stream)
+    run.round_fused(kr, acc)
+    stream.synchronize()
+    names = ("hot_row", "hot_stamp", "lru")
+    state = [run.export(w, torch.int32, (rec.N, rec.B)) for w in names]  # (on the runner's stream)
+    stream.synchronize()
+    want = [run.out.clone(), run.lse.clone()] + [t.clone() for t in state]
+    run.ctx.restore(sid, stream)
+    stream.synchronize()
+    with dhs.Graph.capture(stream) as g:
+        run.round_fused(kr, acc)
+    for _ in range(2):
+        run.ctx.restore(sid, stream)
+        with torch.cuda.stream(stream):
+            run.out.zero_()
+            run.lse.zero_()
+        g.replay()
+        got = [run.out, run.lse] + [run.export(w, torch.int32, (rec.N, rec.B)) for w in names]
+        stream.synchronize()
+        for a, b in zip(got, want):
+            assert torch.equal(a, b)
+    g.close()
+    assert run.ctx.stats()["device_error"] == 0
