@@ -56,6 +56,22 @@ def test_ncu_traffic_only_for_matching_sources(tmp_path, monkeypatch):
     assert bench.ncu_traffic("topk") is None  # sources changed since the capture
 
 
+def test_ncu_traffic_scales_by_captured_requests(tmp_path, monkeypatch):
+    """A summary captured on a cut of the workload scales each kernel's DRAM
+    bytes to the full batch by the file's captured requests, or by a
+    section's own count when that kernel was captured on another cut."""
+    summary = tmp_path / "summary.md"
+    summary.write_text(
+        "# capture\n\ncaptured requests: 16\n\n`csrc-sha256: %s`\n\n"
+        "## k_index_score_tc<8>\n- DRAM read: 800 Mbyte\n- DRAM write: 40 Mbyte\n\n"
+        "## k_topk_row\n- (second capture; captured requests: 48)\n"
+        "- DRAM read: 150 Mbyte\n- DRAM write: 3 Mbyte\n" % bench.csrc_hash())
+    monkeypatch.setattr(bench, "NCU_SUMMARY", str(summary))
+    assert bench.ncu_traffic("index_score", full_requests=128) == 8 * 840_000_000
+    assert bench.ncu_traffic("topk", full_requests=96) == 2 * 153_000_000
+    assert bench.ncu_traffic("topk") == 153_000_000  # no scaling without a batch
+
+
 def test_csrc_hash_is_stable():
     h = bench.csrc_hash()
     assert h == bench.csrc_hash() and len(h) == 16
