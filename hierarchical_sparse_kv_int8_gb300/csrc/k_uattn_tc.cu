@@ -60,15 +60,21 @@ constexpr uint32_t kTcColO = 128;
 constexpr int kTcSpin = 1 << 20;
 constexpr float kTcRescale = 8.f;
 
-// Shared memory.  Operands use the core-matrix layouts of tc_util.cuh.
-//   Q: K-major, cores along K 128 B apart, 8-row groups 2048 B apart
-//   stage: keys (K-major, as Q) then values (MN-major: cores along the value
-//          dims 128 B apart, groups of 8 walk rows 2048 B apart)
-//   P: K-major over the tile's rows, cores 128 B apart, 8-row groups 1024 B
+// Shared memory (from a 1024-byte boundary).
+//   Q: K-major core-matrix layout of tc_util.cuh, cores along K 128 B apart,
+//      8-row groups 2048 B apart
+//   stage: keys, then values, each in the 128-byte-swizzled layout: two
+//          8 KB halves (dims 0-63, 64-127), a walk row's half in 128
+//          contiguous bytes at row * 128, its 16-byte chunk c at chunk
+//          position c ^ (row mod 8) (keys K-major, values MN-major), so that
+//          a warp's copy of a row's 512 bytes fills each 128-byte line once
+//   P: K-major core-matrix layout over the tile's rows, cores 128 B apart,
+//      8-row groups 1024 B
 constexpr int kOffQ = 0;
 constexpr int kQBytes = kTcM * kTcD * 2;
 constexpr int kOffStage = kOffQ + kQBytes;
 constexpr int kKBytes = kTcN * kTcD * 2;
+constexpr int kHalfBytes = kKBytes / 2;  // 64 dims of the tile's rows
 constexpr int kStageBytes = 2 * kKBytes;
 constexpr int kOffP = kOffStage + kTcStages * kStageBytes;
 constexpr int kPBytes = kTcM * kTcN * 2;
@@ -77,7 +83,7 @@ constexpr int kOffRed = kOffMask + kTcStages * kTcN * 4;  // [2][2][128] partial
 constexpr int kOffBar = kOffRed + (2 * 2 * kTcM + 2 * kTcM) * 4;
 constexpr int kNumBars = kTcStages * 2 + 2 * 4 + 1;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
-constexpr int kTcSmem = kOffTmem + 16;
+constexpr int kTcSmem = kOffTmem + 16 + 1024;  // (+ alignment of the swizzled stages)
 static_assert(kTcSmem <= (int)kMaxDynSmem, "shared memory of the tensor-core union pass");
 
 constexpr int kTcMaxSplit = 4;
@@ -88,11 +94,19 @@ constexpr uint32_t kIdescPV = tc_idesc_bf16(kTcM, kTcD, 0, 1);
 __device__ __forceinline__ int kmaj(int row, int chunk, int sbo) {
   return (row >> 3) * sbo + chunk * 128 + (row & 7) * 16;
 }
+// byte offset of 16-byte chunk `chunk` (0-15) of walk row `row` in a
+// 128-byte-swizzled 64 x 128 operand
+__device__ __forceinline__ int sw128(int row, int chunk) {
+  return (chunk >> 3) * kHalfBytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__restrict__ block,
            uint16_t *__restrict__ out, float *__restrict__ lse, int nsplit) {
-  extern __shared__ __align__(1024) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the swizzle pattern follows shared-memory address bits: start the
+  // operands on a 1024-byte boundary
+  unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ int abort_flag, sh_last;
   const int item = blockIdx.x / nsplit, sp = blockIdx.x - item * nsplit;
   const int r = item / c.Hkv, kvh = item - r * c.Hkv;
@@ -220,7 +234,7 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
         const int i = lw + kTcCopyWarps * it;
         const uint16_t *src = reinterpret_cast<const uint16_t *>(
             __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(tsrc), it));
-        unsigned char *dst = lane < 16 ? kst + kmaj(i, lane, 2048) : vst + kmaj(i, lane - 16, 2048);
+        unsigned char *dst = (lane < 16 ? kst : vst) + sw128(i, lane & 15);
         cp_async_16_zfill(dst, src ? (const void *)(src + off) : (const void *)c.ring, src ? 16 : 0);
       }
       cp_async_arrive_noinc(&full[s]);
@@ -242,7 +256,8 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
 #pragma unroll
         for (int kk = 0; kk < kTcN / 16; ++kk)
           tc_mma(tmem + kTcColO, tc_desc(sP + kk * 256, 128, 1024),
-                 tc_desc(sV + kk * 4096, 2048, 128), kIdescPV, (u > 0 || kk > 0) ? 1 : 0);
+                 tc_desc_sw128(sV + kk * 2048, kHalfBytes, 1024), kIdescPV,
+                 (u > 0 || kk > 0) ? 1 : 0);
         tc_commit(&pv_done[b]);
         tc_commit(&empty[s]);
       };
@@ -256,7 +271,8 @@ k_uattn_tc(const DevCtx c, const uint16_t *__restrict__ q, const uint16_t *__res
 #pragma unroll
         for (int kk = 0; kk < kTcD / 16; ++kk)
           tc_mma(tmem + (uint32_t)(b * kTcN), tc_desc(sQ + kk * 256, 128, 2048),
-                 tc_desc(sK + kk * 256, 128, 2048), kIdescQK, kk > 0 ? 1 : 0);
+                 tc_desc_sw128(sK + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
+                 kIdescQK, kk > 0 ? 1 : 0);
         tc_commit(&s_full[b]);
         if (tl >= 1) pv(tl - 1);
       }

@@ -26,6 +26,18 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr, uint32_t lbo, uint32
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
 }
 
+// The same for an operand in the 128-byte-swizzled layout (layout type 2):
+// rows of 128 bytes, 16-byte chunk c of row r stored at chunk position
+// c ^ (r mod 8) within its 1024-byte group of 8 rows (the pattern follows
+// address bits 4-6 and 7-9, so the groups start on 1024-byte boundaries).
+// K-major: `sbo` = bytes between groups of 8 rows, `lbo` unused (16); the K
+// steps of one MMA advance the start address within the 128-byte row.
+// MN-major: `lbo` = bytes between 64-element blocks along N, `sbo` = bytes
+// between groups of 8 K indices.
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return tc_desc(saddr, lbo, sbo) | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor of a dense kind::f16 MMA with bf16 A and B, fp32 D:
 // D format (bits 4-5) = f32, A and B formats (bits 7-9, 10-12) = bf16, A and B
 // major-ness (bits 15, 16; 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (24-28).
