@@ -86,7 +86,7 @@ constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kTcSmem = kOffTmem + 16 + 1024;  // (+ alignment of the swizzled stages)
 static_assert(kTcSmem <= (int)kMaxDynSmem, "shared memory of the tensor-core union pass");
 
-constexpr int kTcMaxSplit = 4;
+constexpr int kTcMaxSplit = 5;  // CTAs per item at most (30 items x 5 fill 150 of 152 SMs)
 constexpr int kTcPartFloats = kTcM * kTcD + kTcM * 2;  // O [M][D], then (m, l) [M]
 constexpr uint32_t kIdescQK = tc_idesc_bf16(kTcM, kTcN, 0, 0);
 constexpr uint32_t kIdescPV = tc_idesc_bf16(kTcM, kTcD, 0, 1);
