@@ -1388,14 +1388,17 @@ k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
       if (sh == 0) {
         // bins are values: count the stash, find T and the group starts,
         // then each stashed row at or above T claims a place in its group
-        // (the stash is read into registers first, as the places overwrite it)
-        zero_hist(nb);
+        // (the stash is read into registers first, as the places overwrite it).
+        // Every stashed value lies in t_est .. range, so the bins cover only
+        // that window (the scans walk a fraction of the 2^13 bins).
+        const int nw = (int)(range - t_est) + 1;
+        zero_hist(nw);
         __syncthreads();
         for (int p = tid; p < n; p += kRowThreads)
-          atomicAdd(&hist[(0xFFFFFFFFu - (uint32_t)(cand[p] >> 32)) & (nb - 1)], 1u);
+          atomicAdd(&hist[(0xFFFFFFFFu - (uint32_t)(cand[p] >> 32)) - t_est], 1u);
         __syncthreads();
-        find_bin(nb, k, true);
-        const uint32_t T = (uint32_t)sh_bin;
+        find_bin(nw, k, true);
+        const uint32_t T = t_est + (uint32_t)sh_bin;
         const int ng = sh_above + sh_eq;
         constexpr int kPer = kRowCap / kRowThreads;
         unsigned long long mine[kPer];
@@ -1410,7 +1413,7 @@ k_topk_row(const DevCtx c, int32_t *__restrict__ topk_out) {
           if (tid + i * kRowThreads >= n) continue;
           const uint32_t v = 0xFFFFFFFFu - (uint32_t)(mine[i] >> 32);
           if (v < T) continue;
-          const uint32_t p = atomicAdd(&hist[v], 1u);
+          const uint32_t p = atomicAdd(&hist[v - t_est], 1u);
           if (p < (uint32_t)kRowCap)
             cand[p] = ((unsigned long long)v << 32) | (uint32_t)mine[i];
           else
