@@ -812,6 +812,42 @@ int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const v
   const uint16_t *b16 = static_cast<const uint16_t *>(block_kv);
   uint16_t *o16 = static_cast<uint16_t *>(out);
   int prev_sel = -1;  // the last group whose selection was issued
+  // a group's attention and commit, issued once the next group's selection is
+  struct Tail {
+    int a;
+    DevCtx v;
+    std::vector<int32_t> cw;
+    cudaStream_t sg;
+    bool pending;
+  };
+  std::vector<Tail> tails(G);
+  auto issue_tail = [&](int g) -> int {
+    Tail &T = tails[g];
+    T.pending = false;
+    const int a = T.a;
+    const DevCtx &v = T.v;
+    cudaStream_t sg = T.sg;
+    const size_t qoff = (size_t)a * d.Kmax * d.Hq;
+    cudaError_t e =
+        !c->fused ? launch_attend(v, q16 + qoff * d.dqk, b16 + (size_t)a * d.Kmax * d.row,
+                                  loc_out + (size_t)a * KK, o16 + qoff * d.dv,
+                                  lse ? lse + qoff : nullptr, c->n_split, sg, &c->timer)
+        // (split-KV over idle SMs for the last group only: the earlier
+        // groups' attention overlaps the next indexer, whose SMs it would
+        // take; measured 1.91 -> 1.87 ms against no split on 128
+        // histories of 102 400 rows in four groups, 1.94 splitting all)
+        : tc ? launch_uattn_tc(v, q16 + qoff * d.dqk, b16 + (size_t)a * d.Kmax * d.row,
+                               o16 + qoff * d.dv, lse ? lse + qoff : nullptr, sg, &c->timer,
+                               g == G - 1 ? 0 : 1)
+             : launch_uattn(v, q16 + qoff * d.dqk, b16 + (size_t)a * d.Kmax * d.row,
+                            o16 + qoff * d.dv, lse ? lse + qoff : nullptr, sg, &c->timer);
+    if (e == cudaSuccess) e = launch_commit(v, T.cw.data(), sg, &c->timer);
+    if (e != cudaSuccess) return cuda_fail(c, e);
+    if (fork && (cudaEventRecord(c->gevent[1 + g], sg) != cudaSuccess ||
+                 cudaStreamWaitEvent(s, c->gevent[1 + g], 0) != cudaSuccess))
+      return cuda_fail(c, cudaGetLastError());
+    return DHS_OK;
+  };
   // Group g covers slots [edge(g), edge(g + 1)): equal weights, except a
   // lighter last group, whose gather and attention nothing overlaps (they
   // end the round); measured on 128 histories of 102 400 rows in four
@@ -855,6 +891,15 @@ int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const v
                         topk_out + (size_t)a * KK, dom_g, wg.data(), act_g, c->cfg.topk_pass, sg,
                         &c->timer);
     if (e == cudaSuccess && fork) e = cudaEventRecord(c->gsel[g], sg);
+    if (e != cudaSuccess) return cuda_fail(c, e);
+    // the previous group's attention starts after this group's top-k: its
+    // CTAs (a whole SM each) would otherwise slow the top-k that the next
+    // indexer waits for
+    if (prev_sel >= 0 && tails[prev_sel].pending) {
+      if (cudaStreamWaitEvent(tails[prev_sel].sg, c->gsel[g], 0) != cudaSuccess)
+        return cuda_fail(c, cudaGetLastError());
+      if (int rc = issue_tail(prev_sel)) return rc;
+    }
     prev_sel = g;
     if (e == cudaSuccess)
       e = launch_resolve(v, topk_out + (size_t)a * KK, loc_out + (size_t)a * KK, 1, 0, tick, sg,
@@ -862,26 +907,15 @@ int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const v
     if (e == cudaSuccess)
       e = launch_gather(v, topk_out + (size_t)a * KK, loc_out + (size_t)a * KK, 1, tick, sg,
                         &c->timer, !c->fused);
-    const size_t qoff = (size_t)a * d.Kmax * d.Hq;
-    if (e == cudaSuccess)
-      e = !c->fused ? launch_attend(v, q16 + qoff * d.dqk, b16 + (size_t)a * d.Kmax * d.row,
-                                    loc_out + (size_t)a * KK, o16 + qoff * d.dv,
-                                    lse ? lse + qoff : nullptr, c->n_split, sg, &c->timer)
-          // (split-KV over idle SMs for the last group only: the earlier
-          // groups' attention overlaps the next indexer, whose SMs it would
-          // take; measured 1.91 -> 1.87 ms against no split on 128
-          // histories of 102 400 rows in four groups, 1.94 splitting all)
-          : tc ? launch_uattn_tc(v, q16 + qoff * d.dqk, b16 + (size_t)a * d.Kmax * d.row,
-                                 o16 + qoff * d.dv, lse ? lse + qoff : nullptr, sg, &c->timer,
-                                 g == G - 1 ? 0 : 1)
-               : launch_uattn(v, q16 + qoff * d.dqk, b16 + (size_t)a * d.Kmax * d.row,
-                              o16 + qoff * d.dv, lse ? lse + qoff : nullptr, sg, &c->timer);
-    if (e == cudaSuccess) e = launch_commit(v, cw.data(), sg, &c->timer);
     if (e != cudaSuccess) return cuda_fail(c, e);
-    if (fork && (cudaEventRecord(c->gevent[1 + g], sg) != cudaSuccess ||
-                 cudaStreamWaitEvent(s, c->gevent[1 + g], 0) != cudaSuccess))
-      return cuda_fail(c, cudaGetLastError());
+    tails[g] = Tail{a, v, std::move(cw), sg, true};
+    if (!fork || g == G - 1)
+      if (int rc = issue_tail(g)) return rc;
   }
+  // (a last group left empty by the weights leaves the previous one pending)
+  for (int g = 0; g < G; ++g)
+    if (tails[g].pending)
+      if (int rc = issue_tail(g)) return rc;
   c->tick = tick;
   c->last_shared = 1;
   for (int r = 0; r < d.N; ++r) {
