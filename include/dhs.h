@@ -405,7 +405,8 @@ void dhs_graph_destroy(dhs_graph *graph);
  * with compute of [ADHS] 3.2 / 4.3.2.  The groups' selections run one
  * after another (group g's indexer starts when group g - 1's top-k has
  * finished), the internal streams have decreasing priorities in group order,
- * and the rest of each group's round overlaps the next group's indexer.
+ * the rest of each group's round overlaps the next group's indexer, and a
+ * group's attention starts once the next group's top-k has finished.
  * Results equal those of the separate
  * calls; the LRU clock advances once per call.  Forking and joining use CUDA
  * events, which stream capture turns into graph dependencies.  Not for
