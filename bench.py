@@ -610,7 +610,9 @@ def run_native(args):
         "eager_ms_per_step": round(eager_ms, 5),
         "launch": ("CUDA graph of one round (one dhs_round call: select, resolve, attend, commit "
                    "per request group, the %d groups overlapping on internal streams of "
-                   "decreasing priority; captured with dhs_graph_*, which instantiates it with "
+                   "decreasing priority, a group's indexer after the previous group's top-k and "
+                   "its attention after the next group's top-k; captured with dhs_graph_*, which "
+                   "instantiates it with "
                    "the launches' priorities honoured), replayed per step; kernel times (roofline, families, kernels) from a second replay of "
                    "the same steps issued as one request group (each kernel over the whole batch, "
                    "none overlapping) with an event pair around every kernel" % groups)
