@@ -881,9 +881,9 @@ int dhs_round(dhs_ctx *c, const int8_t *q_idx, const int32_t *k_per_req, const v
     }
     // The groups' selections run one after another: a group's indexer starts
     // once the previous group's top-k has finished (each indexer alone
-    // streams HBM at full rate), and the previous group's union/probe,
-    // gather and attention, sized to fit beside two indexer CTAs on an SM
-    // (the attention on few SMs), overlap this group's indexer.
+    // streams HBM at full rate), and the previous group's union/probe and
+    // gather, sized to fit beside two indexer CTAs on an SM, overlap this
+    // group's indexer (its attention, below, waits for this group's top-k).
     cudaError_t e = cudaSuccess;
     if (fork && prev_sel >= 0) e = cudaStreamWaitEvent(sg, c->gsel[prev_sel], 0);
     if (e == cudaSuccess)

@@ -241,7 +241,7 @@ bool uattn_supported(const DevCtx &c);
 // 128 (query, head) pairs per kv head): one CTA per (request, kv head).
 bool uattn_tc_supported(const DevCtx &c);
 // split: CTAs per (request, kv head) item (split-KV), 0 = automatic (up to
-// the SM count, at most four).
+// the SM count, at most five).
 cudaError_t launch_uattn_tc(const DevCtx &c, const uint16_t *q, const uint16_t *block,
                             uint16_t *out, float *lse, cudaStream_t s, class Timer *tm,
                             int split = 0);
